@@ -1,0 +1,12 @@
+"""Float64 CPU oracle of the differential-attention forward.
+
+Test infrastructure: only the tests, the smoke check and the benchmark's CPU
+baseline use it.  It shares no code with the CUDA library.
+"""
+from .diffattn_oracle import (  # noqa: F401
+    differential_attention,
+    differential_lambda,
+    lambda_init_schedule,
+    signed_map,
+    softmax_maps,
+)

@@ -1,0 +1,189 @@
+"""Float64 CPU oracle for the Differential Transformer attention forward.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this module.  The product path (the C-ABI library
+and its Python binding) never imports, calls or links it, and shares no code
+with it.
+
+What it computes (plain definition, written out; no blocking beyond a loop over
+query rows, no fusion, no reordering):
+
+  S_b   = Q_b K_b^T / sqrt(D) + M                       b = 1, 2
+  A_b   = softmax over keys of S_b (max-subtracted, two passes)
+  O     = (A_1 - lambda A_2) V
+  lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init
+
+Sources:
+  * paperleet "Differential Transformer Attention" -- Formula and conventions:
+    the two masked maps, the signed combination, the [B,H,T,D] / [B,H,T,2D]
+    shapes, the scale 1/sqrt(D) with D the Q/K width, the causal mask (0 on
+    allowed positions, -inf on future ones, applied to both branches), and the
+    lambda parameterisation.  Per-head normalisation and its fixed multiplier
+    are outside this operation and are not applied.
+  * aifetchly "Differential Transformer: Canceling LLM Attention Noise" --
+    section 1 (the DiffAttn formula), section 3 (the lambda re-parameterisation
+    and the lambda_init depth schedule), and the numerically stable softmax
+    (subtract the row maximum before exponentiating).
+  * ultralytics glossary "Differential Transformer" -- "So funktioniert
+    differentielle Aufmerksamkeit": each map sums to 1 per row, so the signed
+    map's rows sum to 1 - lambda and can hold negative entries.
+
+Readings where the pages leave a step open:
+  * A masked position contributes exactly zero weight (exp(-inf) = 0); with
+    the causal mask, key j is visible to query i iff j <= i, so no row is
+    ever fully masked.
+  * lambda is any finite real (not clamped to [0, 1]).
+
+Parity is pinned by tests/test_oracle.py (brute-force scalar softmax on tiny
+inputs, a library attention routine at lambda = 0, row sums, the identical-map
+and value-offset identities, closed forms, and the printed worked example).
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "lambda_init_schedule",
+    "differential_lambda",
+    "softmax_maps",
+    "signed_map",
+    "differential_attention",
+]
+
+
+def lambda_init_schedule(layer: int) -> float:
+    """lambda_init = 0.8 - 0.6 exp(-0.3 (l - 1)) for layer l >= 1
+    (aifetchly, section 3; paperleet, Formula and conventions)."""
+    if layer < 1:
+        raise ValueError("layers are counted from 1")
+    return 0.8 - 0.6 * math.exp(-0.3 * (layer - 1))
+
+
+def differential_lambda(lq1, lk1, lq2, lk2, lambda_init: float = 0.2) -> float:
+    """lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init, in float64
+    (aifetchly, section 3; paperleet, Formula and conventions: equal-length,
+    non-empty vectors, the result is not restricted to [0, 1])."""
+    vecs = [np.asarray(x, dtype=np.float64).reshape(-1) for x in (lq1, lk1, lq2, lk2)]
+    n = vecs[0].size
+    if n == 0 or any(x.size != n for x in vecs):
+        raise ValueError("lambda vectors must be non-empty and of equal length")
+    dot1 = float(np.dot(vecs[0], vecs[1]))
+    dot2 = float(np.dot(vecs[2], vecs[3]))
+    return math.exp(dot1) - math.exp(dot2) + float(lambda_init)
+
+
+# ---------------------------------------------------------------------------
+# The steps of one head, on float64 arrays.  Kept separate so that each can be
+# read against the formula on its own.
+# ---------------------------------------------------------------------------
+
+def _scores(q: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """S = Q K^T / sqrt(D) for query rows q [R, D] and all keys k [T, D]."""
+    D = q.shape[-1]
+    return (q @ k.T) / math.sqrt(D)
+
+
+def _mask(s: np.ndarray, rows: np.ndarray, causal: bool) -> np.ndarray:
+    """Add M: -inf where key j > query i (causal), nothing otherwise."""
+    if not causal:
+        return s
+    keys = np.arange(s.shape[-1])
+    future = keys[None, :] > rows[:, None]
+    out = s.copy()
+    out[future] = -np.inf
+    return out
+
+
+def _softmax(s: np.ndarray) -> np.ndarray:
+    """Row softmax over keys: subtract the row max, exponentiate, divide by the
+    row sum (two passes).  exp(-inf) is exactly 0."""
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def _combine(a1: np.ndarray, a2: np.ndarray, lam: float) -> np.ndarray:
+    """The signed map A_1 - lambda A_2."""
+    return a1 - lam * a2
+
+
+def _head_rows(q1, k1, q2, k2, rows, lam, causal):
+    """Signed-map rows of one head for the given query rows."""
+    a1 = _softmax(_mask(_scores(q1[rows], k1), rows, causal))
+    a2 = _softmax(_mask(_scores(q2[rows], k2), rows, causal))
+    return _combine(a1, a2, lam)
+
+
+def _as64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+def _check_shapes(q1, k1, q2, k2, v=None):
+    if not (q1.shape == k1.shape == q2.shape == k2.shape):
+        raise ValueError("Q1, K1, Q2, K2 must share one shape [B, H, T, D]")
+    if q1.ndim != 4 or min(q1.shape) < 1:
+        raise ValueError("expected non-empty [B, H, T, D] tensors")
+    if v is not None:
+        B, H, T, D = q1.shape
+        if v.shape != (B, H, T, 2 * D):
+            raise ValueError("V must be [B, H, T, 2D]")
+
+
+def softmax_maps(q1, k1, q2, k2, causal: bool = True):
+    """The two attention maps A_1, A_2 as [B, H, T, T] float64 (small inputs)."""
+    q1, k1, q2, k2 = (_as64(x) for x in (q1, k1, q2, k2))
+    _check_shapes(q1, k1, q2, k2)
+    B, H, T, _ = q1.shape
+    rows = np.arange(T)
+    a1 = np.empty((B, H, T, T))
+    a2 = np.empty((B, H, T, T))
+    for b in range(B):
+        for h in range(H):
+            a1[b, h] = _softmax(_mask(_scores(q1[b, h], k1[b, h]), rows, causal))
+            a2[b, h] = _softmax(_mask(_scores(q2[b, h], k2[b, h]), rows, causal))
+    return a1, a2
+
+
+def signed_map(q1, k1, q2, k2, lam: float, causal: bool = True) -> np.ndarray:
+    """The signed map A_1 - lambda A_2 as [B, H, T, T] float64 (small inputs)."""
+    a1, a2 = softmax_maps(q1, k1, q2, k2, causal)
+    return _combine(a1, a2, float(lam))
+
+
+def differential_attention(q1, k1, q2, k2, v, lam: float, causal: bool = True,
+                           rows: Optional[Sequence[int]] = None,
+                           heads: Optional[Sequence[tuple]] = None,
+                           block: int = 256) -> np.ndarray:
+    """O = (A_1 - lambda A_2) V in float64.
+
+    q1, k1, q2, k2: [B, H, T, D]; v: [B, H, T, 2D] (any real dtype, upcast to
+    float64).  lam: the scalar lambda.  causal: apply the causal mask to both
+    branches.
+
+    rows: optional query rows to evaluate (every row when None).  Every output
+    row depends only on its own query row and all keys/values of its head, so
+    a row subset is exact, not an approximation.
+    heads: optional list of (b, h) to evaluate (every head when None).
+
+    Returns [B, H, R, 2D] for all heads, or [len(heads), R, 2D] when heads is
+    given.  Query rows are processed `block` at a time only to bound memory.
+    """
+    _check_shapes(q1, k1, q2, k2, v)
+    B, H, T, D = q1.shape
+    lam = float(lam)
+    row_idx = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    if row_idx.size and (row_idx.min() < 0 or row_idx.max() >= T):
+        raise ValueError("row index out of range")
+    head_list = [(b, h) for b in range(B) for h in range(H)] if heads is None else list(heads)
+    out = np.empty((len(head_list), row_idx.size, 2 * D))
+    for n, (b, h) in enumerate(head_list):
+        hq1, hk1, hq2, hk2, hv = (_as64(x[b, h]) for x in (q1, k1, q2, k2, v))
+        for r0 in range(0, row_idx.size, block):
+            r = row_idx[r0:r0 + block]
+            out[n, r0:r0 + block] = _head_rows(hq1, hk1, hq2, hk2, r, lam, causal) @ hv
+    if heads is None:
+        out = out.reshape(B, H, row_idx.size, 2 * D)
+    return out

@@ -1,0 +1,323 @@
+"""Pins for the float64 oracle, independent of the oracle's own code.
+
+Each pin checks the oracle against something the pages or the mathematics fix:
+  * a brute-force scalar softmax written with plain Python loops (the
+    "independent scalar softmax" the paperleet exercise names for verification);
+  * torch's scaled_dot_product_attention at lambda = 0 (paperleet, Formula and
+    conventions: "At lambda=0 it becomes ordinary attention");
+  * row sums 1 - lambda (paperleet; ultralytics "So funktioniert ...");
+  * identical maps cancel exactly at lambda = 1 (paperleet);
+  * a value offset shared by every token responds by exactly (1 - lambda)
+    (paperleet, Toy experiment);
+  * closed forms on two-token inputs and for the causal first row;
+  * the worked example printed on the ultralytics page (row sum 0.20, 13 of 36
+    negative weights);
+  * lambda: zero vectors give lambda_init (aifetchly, section 3), the depth
+    schedule gives 0.2 at layer 1.
+The mutation tests at the end plant a plausible mistake in one oracle step and
+check that some pin fails.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import diffattn_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_inputs(B, H, T, D, seed):
+    rng = np.random.default_rng(seed)
+    q1, k1, q2, k2 = (rng.standard_normal((B, H, T, D)) for _ in range(4))
+    v = rng.standard_normal((B, H, T, 2 * D))
+    return q1, k1, q2, k2, v
+
+
+def brute_force(q1, k1, q2, k2, v, lam, causal):
+    """Per-element scalar evaluation with Python floats and math.exp."""
+    B, H, T, D = q1.shape
+    Dv = v.shape[-1]
+    out = np.zeros((B, H, T, Dv))
+    for b in range(B):
+        for h in range(H):
+            for i in range(T):
+                weights = [0.0] * T
+                for q, k, sign in ((q1, k1, 1.0), (q2, k2, -lam)):
+                    visible = [j for j in range(T) if (not causal) or j <= i]
+                    logits = {}
+                    for j in visible:
+                        dot = 0.0
+                        for c in range(D):
+                            dot += float(q[b, h, i, c]) * float(k[b, h, j, c])
+                        logits[j] = dot / math.sqrt(D)
+                    top = max(logits.values())
+                    ex = {j: math.exp(x - top) for j, x in logits.items()}
+                    z = sum(ex.values())
+                    for j in visible:
+                        weights[j] += sign * ex[j] / z
+                for c in range(Dv):
+                    acc = 0.0
+                    for j in range(T):
+                        acc += weights[j] * float(v[b, h, j, c])
+                    out[b, h, i, c] = acc
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Pins (plain functions so the mutation tests can rerun them)
+# ---------------------------------------------------------------------------
+
+def pin_brute_force():
+    for (B, H, T, D, seed) in [(1, 2, 5, 3, 0), (2, 1, 8, 4, 1), (1, 1, 1, 2, 2), (1, 1, 7, 6, 3)]:
+        q1, k1, q2, k2, v = rand_inputs(B, H, T, D, seed)
+        for lam in (0.0, 0.2, 0.8, 1.0, -0.35, 1.7):
+            for causal in (True, False):
+                got = oracle.differential_attention(q1, k1, q2, k2, v, lam, causal)
+                ref = brute_force(q1, k1, q2, k2, v, lam, causal)
+                assert np.max(np.abs(got - ref)) <= 1e-12, (B, H, T, D, lam, causal)
+
+
+def pin_sdpa_lambda0():
+    for causal in (True, False):
+        q1, k1, q2, k2, v = rand_inputs(2, 3, 37, 16, 7)
+        got = oracle.differential_attention(q1, k1, q2, k2, v, 0.0, causal)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q1), torch.from_numpy(k1), torch.from_numpy(v),
+            is_causal=causal).numpy()
+        assert np.max(np.abs(got - ref)) <= 1e-12
+
+
+def pin_row_sums():
+    q1, k1, q2, k2, _ = rand_inputs(1, 2, 33, 8, 11)
+    for lam in (0.0, 0.5, 0.8, 1.3, -2.0):
+        for causal in (True, False):
+            m = oracle.signed_map(q1, k1, q2, k2, lam, causal)
+            assert np.max(np.abs(m.sum(-1) - (1.0 - lam))) <= 1e-12
+            ones = np.ones((1, 2, 33, 16))
+            o = oracle.differential_attention(q1, k1, q2, k2, ones, lam, causal)
+            assert np.max(np.abs(o - (1.0 - lam))) <= 1e-12
+
+
+def pin_identical_maps():
+    q1, k1, _, _, v = rand_inputs(1, 2, 29, 8, 12)
+    for causal in (True, False):
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q1), torch.from_numpy(k1), torch.from_numpy(v),
+            is_causal=causal).numpy()
+        for lam in (0.0, 0.3, 0.8):
+            got = oracle.differential_attention(q1, k1, q1, k1, v, lam, causal)
+            assert np.max(np.abs(got - (1.0 - lam) * ref)) <= 1e-12
+        got1 = oracle.differential_attention(q1, k1, q1, k1, v, 1.0, causal)
+        assert np.all(got1 == 0.0)
+
+
+def pin_value_offset():
+    q1, k1, q2, k2, v = rand_inputs(2, 2, 24, 8, 13)
+    c = np.random.default_rng(5).normal(0.0, 2.0, size=(2, 2, 1, 16))
+    for lam in (0.0, 0.25, 0.5, 1.0, 1.5):
+        for causal in (True, False):
+            base = oracle.differential_attention(q1, k1, q2, k2, v, lam, causal)
+            shifted = oracle.differential_attention(q1, k1, q2, k2, v + c, lam, causal)
+            assert np.max(np.abs((shifted - base) - (1.0 - lam) * c)) <= 1e-12
+
+
+def pin_closed_forms():
+    # Two tokens, D = 4 (scale 1/2).  Branch 1: q = (a,0,0,0), k0 = (b,0,0,0),
+    # k1 = 0, so w0 = sigmoid(a b / 2).  Branch 2: q = 0, uniform weights 1/2.
+    a, b, lam = 1.3, -0.7, 0.6
+    q1 = np.zeros((1, 1, 2, 4)); q1[0, 0, :, 0] = a
+    k1 = np.zeros((1, 1, 2, 4)); k1[0, 0, 0, 0] = b
+    q2 = np.zeros((1, 1, 2, 4)); k2 = np.random.default_rng(0).standard_normal((1, 1, 2, 4))
+    v = np.random.default_rng(1).standard_normal((1, 1, 2, 8))
+    w0 = 1.0 / (1.0 + math.exp(-a * b / 2.0))
+    expect_last = (w0 - lam / 2) * v[0, 0, 0] + ((1 - w0) - lam / 2) * v[0, 0, 1]
+    got = oracle.differential_attention(q1, k1, q2, k2, v, lam, causal=False)
+    assert np.max(np.abs(got[0, 0, 1] - expect_last)) <= 1e-14
+    assert np.max(np.abs(got[0, 0, 0] - expect_last)) <= 1e-14  # same query, same keys
+    got_c = oracle.differential_attention(q1, k1, q2, k2, v, lam, causal=True)
+    # Causal first row sees only key 0 in both branches: (1 - lambda) v0.
+    assert np.max(np.abs(got_c[0, 0, 0] - (1 - lam) * v[0, 0, 0])) <= 1e-15
+    assert np.max(np.abs(got_c[0, 0, 1] - expect_last)) <= 1e-14
+    # Causal row 0 on random data: (1 - lambda) v0 for every head.
+    q1, k1, q2, k2, v = rand_inputs(2, 3, 17, 5, 21)
+    o = oracle.differential_attention(q1, k1, q2, k2, v, 0.37, True)
+    assert np.max(np.abs(o[:, :, 0] - 0.63 * v[:, :, 0])) <= 1e-15
+    # The last causal row sees every key: equal to the non-causal last row.
+    onc = oracle.differential_attention(q1, k1, q2, k2, v, 0.37, False)
+    assert np.max(np.abs(o[:, :, -1] - onc[:, :, -1])) <= 1e-13
+
+
+def pin_worked_example():
+    with open(os.path.join(GOLDEN, "p4_worked_example.json")) as f:
+        g = json.load(f)
+    torch.manual_seed(0)
+    n, d, lam = g["n"], g["d"], g["lambda"]
+    q1, k1, q2, k2 = torch.randn(4, n, d).double()
+    m = oracle.signed_map(*(x.numpy()[None, None] for x in (q1, k1, q2, k2)), lam, causal=False)
+    assert f"{m[0, 0, 0].sum():.2f}" == g["printed_row_sum"]
+    assert int((m < 0).sum()) == g["printed_negative_weights"]
+    assert m[0, 0].size == g["printed_total_weights"]
+
+
+def pin_lambda():
+    z = np.zeros(16)
+    assert oracle.differential_lambda(z, z, z, z, 0.37) == 0.37
+    assert oracle.lambda_init_schedule(1) == pytest.approx(0.2, abs=1e-15)
+    assert oracle.lambda_init_schedule(12) == pytest.approx(0.8 - 0.6 * math.exp(-3.3), abs=1e-15)
+    e = np.zeros(4); e[0] = 1.0
+    two = np.zeros(4); two[0] = 2.0
+    # exp(1*2) - exp(0) + 0.2
+    assert oracle.differential_lambda(e, two, z[:4], z[:4], 0.2) == pytest.approx(math.exp(2) - 1 + 0.2, abs=1e-13)
+    # exp(0) - exp(1*2) + 0.2  (second term subtracts; negative result allowed)
+    assert oracle.differential_lambda(z[:4], z[:4], e, two, 0.2) == pytest.approx(1 - math.exp(2) + 0.2, abs=1e-13)
+    # Dot product, not elementwise mismatch: (1,2).(3,4) = 11 -> exp(11)
+    assert oracle.differential_lambda([1, 2], [3, 4], [0, 0], [0, 0], 0.0) == pytest.approx(math.exp(11) - 1, rel=1e-14)
+    with pytest.raises(ValueError):
+        oracle.differential_lambda([], [], [], [])
+    with pytest.raises(ValueError):
+        oracle.differential_lambda([1, 2], [1], [1, 2], [1, 2])
+
+
+ALL_PINS = [pin_brute_force, pin_sdpa_lambda0, pin_row_sums, pin_identical_maps,
+            pin_value_offset, pin_closed_forms, pin_worked_example]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS + [pin_lambda], ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+def test_row_subset_is_exact():
+    q1, k1, q2, k2, v = rand_inputs(2, 2, 300, 8, 31)
+    full = oracle.differential_attention(q1, k1, q2, k2, v, 0.7, True)
+    rows = [0, 5, 127, 128, 255, 256, 299]
+    sub = oracle.differential_attention(q1, k1, q2, k2, v, 0.7, True, rows=rows)
+    assert np.array_equal(sub, full[:, :, rows])
+    one = oracle.differential_attention(q1, k1, q2, k2, v, 0.7, True, rows=rows, heads=[(1, 0)])
+    assert np.array_equal(one[0], full[1, 0, rows])
+
+
+def test_block_size_does_not_matter():
+    q1, k1, q2, k2, v = rand_inputs(1, 1, 70, 8, 32)
+    a = oracle.differential_attention(q1, k1, q2, k2, v, 0.7, True, block=256)
+    b = oracle.differential_attention(q1, k1, q2, k2, v, 0.7, True, block=7)
+    assert np.array_equal(a, b)
+
+
+def test_noncausal_key_permutation_invariance():
+    q1, k1, q2, k2, v = rand_inputs(1, 2, 19, 8, 33)
+    perm = np.random.default_rng(3).permutation(19)
+    a = oracle.differential_attention(q1, k1, q2, k2, v, 0.8, False)
+    b = oracle.differential_attention(q1, k1[:, :, perm], q2, k2[:, :, perm], v[:, :, perm], 0.8, False)
+    assert np.max(np.abs(a - b)) <= 1e-12
+
+
+def test_shape_validation():
+    q1, k1, q2, k2, v = rand_inputs(1, 1, 4, 4, 0)
+    with pytest.raises(ValueError):
+        oracle.differential_attention(q1, k1, q2, k2, v[..., :4], 0.5)
+    with pytest.raises(ValueError):
+        oracle.differential_attention(q1, k1[:, :, :3], q2, k2, v, 0.5)
+
+
+# ---------------------------------------------------------------------------
+# Mutation tests: a mistake planted in one step of the oracle must fail a pin.
+# ---------------------------------------------------------------------------
+
+def _wrong_sign(a1, a2, lam):
+    return a1 + lam * a2
+
+
+def _lambda_on_first(a1, a2, lam):
+    return lam * a1 - a2
+
+
+def _scale_by_D(q, k):
+    return (q @ k.T) / q.shape[-1]
+
+
+def _no_scale(q, k):
+    return q @ k.T
+
+
+def _transposed_scores(q, k):
+    # S^T in place of S (only expressible when every query row is evaluated).
+    if q.shape[0] != k.shape[0]:
+        return (q @ k.T) / math.sqrt(q.shape[-1])
+    return (k @ q.T) / math.sqrt(q.shape[-1])
+
+
+def _mask_diag_off(s, rows, causal):
+    if not causal:
+        return s
+    keys = np.arange(s.shape[-1])
+    out = s.copy()
+    out[keys[None, :] >= rows[:, None]] = -np.inf
+    out[np.all(np.isinf(out), axis=-1)] = 0.0
+    return out
+
+
+def _mask_upper_kept(s, rows, causal):
+    if not causal:
+        return s
+    keys = np.arange(s.shape[-1])
+    out = s.copy()
+    out[keys[None, :] < rows[:, None]] = -np.inf
+    return out
+
+
+def _mask_branch1_only(q1, k1, q2, k2, rows, lam, causal):
+    a1 = O._softmax(O._mask(O._scores(q1[rows], k1), rows, causal))
+    a2 = O._softmax(O._scores(q2[rows], k2))
+    return O._combine(a1, a2, lam)
+
+
+def _softmax_wrong_axis(s):
+    m = np.max(s, axis=0, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=0, keepdims=True)
+
+
+def _softmax_unnormalised(s):
+    m = np.max(s, axis=-1, keepdims=True)
+    return np.exp(s - m)
+
+
+MUTANTS = [
+    ("_combine", _wrong_sign),
+    ("_combine", _lambda_on_first),
+    ("_scores", _scale_by_D),
+    ("_scores", _no_scale),
+    ("_scores", _transposed_scores),
+    ("_mask", _mask_diag_off),
+    ("_mask", _mask_upper_kept),
+    ("_softmax", _softmax_wrong_axis),
+    ("_softmax", _softmax_unnormalised),
+    ("_head_rows", _mask_branch1_only),
+]
+
+
+@pytest.mark.parametrize("name,mutant", MUTANTS, ids=[m[1].__name__ for m in MUTANTS])
+def test_planted_mistake_is_caught(monkeypatch, name, mutant):
+    monkeypatch.setattr(O, name, mutant)
+    failures = 0
+    for pin in ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin()
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            failures += 1
+    assert failures > 0, f"no pin caught the planted mistake in {name}"
+
+
+def test_planted_lambda_sign_is_caught(monkeypatch):
+    def bad(lq1, lk1, lq2, lk2, lambda_init=0.2):
+        return math.exp(np.dot(lq1, lk1)) + math.exp(np.dot(lq2, lk2)) + lambda_init
+    monkeypatch.setattr(oracle, "differential_lambda", bad)
+    with pytest.raises(AssertionError):
+        pin_lambda()

@@ -1,0 +1,180 @@
+"""Seeded synthetic inputs for the differential-attention forward.
+
+This module only draws random numbers and lays them out; it holds none of the
+method's arithmetic (no scores, no softmax, no lambda). Both the float64 oracle
+(through the tests and the benchmark) and the CUDA path are fed from here, so
+the two sides see bit-identical inputs.
+
+Shapes follow the exercise specification of the Differential Transformer
+attention (paperleet "Differential Transformer Attention", Formula and
+conventions): Q1, K1, Q2, K2 are [B, H, T, D]; V is [B, H, T, 2D].
+
+Recipe (all draws from numpy's PCG64 generator, float32, in this order):
+  q1, k1, q2, k2 ~ N(0, 1)      each [B, H, T, D]
+  v               ~ N(0, 1)      [B, H, T, 2D]
+  lq1, lk1, lq2, lk2 ~ N(0, 0.1^2)  each [D]   (the lambda parameter vectors)
+  then, per workload:
+    planted keys: for each (b, h), 8 distinct key rows j_s ~ U[0, T) and a
+      partner query row i_s ~ U[j_s, T); K1[b, h, j_s] = 4 * Q1[b, h, i_s]
+      (a causally visible, strongly aligned key in branch 1 only)
+    value offset: one vector c ~ N(0, 2^2) of width 2D per (b, h), added to
+      every token's value row
+The float32 draws are then rounded to the compute dtype (bf16 round to nearest
+even, or kept as float32).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic input recipe."""
+    name: str
+    B: int
+    H: int
+    T: int
+    D: int
+    dtype: str               # "bf16" or "f32"
+    causal: bool
+    seed: int
+    layer: Optional[int] = None          # lambda_init from the depth schedule
+    lambda_init: Optional[float] = None  # explicit lambda_init
+    lambdas: Optional[Sequence[float]] = None  # lambda given directly (swept)
+    planted: int = 0                     # planted aligned keys per head
+    value_offset_sigma: float = 0.0      # std of the shared per-channel value offset
+
+    @property
+    def Dv(self) -> int:
+        return 2 * self.D
+
+    @property
+    def pairs_per_head(self) -> int:
+        """Unmasked (query, key) pairs of one head."""
+        T = self.T
+        return T * (T + 1) // 2 if self.causal else T * T
+
+    @property
+    def flops(self) -> int:
+        """Algorithmic FLOPs: 2 QK^T (2D each) + 2 PV (2*2D each) per unmasked pair."""
+        return self.B * self.H * self.pairs_per_head * 12 * self.D
+
+
+# The five input recipes.  Sizes, distributions and lambda recipes are the
+# ones the workload table fixes; seeds 0..4 in table order.
+WORKLOADS = {
+    "tiny_f32": Workload("tiny_f32", B=1, H=2, T=128, D=32, dtype="f32",
+                         causal=True, seed=0, layer=1),
+    "b4h16t2048": Workload("b4h16t2048", B=4, H=16, T=2048, D=64, dtype="bf16",
+                           causal=True, seed=1, layer=12),
+    "b2h16t8192": Workload("b2h16t8192", B=2, H=16, T=8192, D=64, dtype="bf16",
+                           causal=True, seed=2, layer=24),
+    "b1h16t32768_planted": Workload("b1h16t32768_planted", B=1, H=16, T=32768, D=64,
+                                    dtype="bf16", causal=True, seed=3,
+                                    lambda_init=0.8, planted=8),
+    "b8h32t4096_offset": Workload("b8h32t4096_offset", B=8, H=32, T=4096, D=64,
+                                  dtype="bf16", causal=False, seed=4,
+                                  lambdas=(0.0, 0.5, 1.0), value_offset_sigma=2.0),
+}
+
+HEADLINE = "b2h16t8192"
+
+
+@dataclasses.dataclass
+class Inputs:
+    """Drawn inputs.  Arrays are float32 holding exactly the values the device
+    sees (already rounded to the compute dtype)."""
+    q1: np.ndarray
+    k1: np.ndarray
+    q2: np.ndarray
+    k2: np.ndarray
+    v: np.ndarray
+    lq1: np.ndarray
+    lk1: np.ndarray
+    lq2: np.ndarray
+    lk2: np.ndarray
+    planted_keys: Optional[np.ndarray] = None     # [B, H, planted] key rows
+    planted_queries: Optional[np.ndarray] = None  # [B, H, planted] query rows
+    value_offset: Optional[np.ndarray] = None     # [B, H, 2D]
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 to the nearest bfloat16 (ties to even), returned as float32.
+
+    Pure bit manipulation on the float32 encoding; inputs are finite."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = (u + np.uint32(0x7FFF) + lsb) & np.uint32(0xFFFF0000)
+    return r.view(np.float32)
+
+
+def draw(w: Workload, B: Optional[int] = None, H: Optional[int] = None,
+         T: Optional[int] = None, D: Optional[int] = None, seed: Optional[int] = None,
+         dtype: Optional[str] = None) -> Inputs:
+    """Draw the inputs of workload `w` (optionally overriding its sizes)."""
+    B = w.B if B is None else B
+    H = w.H if H is None else H
+    T = w.T if T is None else T
+    D = w.D if D is None else D
+    dtype = w.dtype if dtype is None else dtype
+    rng = np.random.Generator(np.random.PCG64(w.seed if seed is None else seed))
+    shp = (B, H, T, D)
+    q1 = rng.standard_normal(shp, dtype=np.float32)
+    k1 = rng.standard_normal(shp, dtype=np.float32)
+    q2 = rng.standard_normal(shp, dtype=np.float32)
+    k2 = rng.standard_normal(shp, dtype=np.float32)
+    v = rng.standard_normal((B, H, T, 2 * D), dtype=np.float32)
+    lam_vecs = [(0.1 * rng.standard_normal(D)).astype(np.float32) for _ in range(4)]
+    planted_keys = planted_queries = offset = None
+    if w.planted:
+        n = min(w.planted, T)
+        planted_keys = np.zeros((B, H, n), dtype=np.int64)
+        planted_queries = np.zeros((B, H, n), dtype=np.int64)
+        for b in range(B):
+            for h in range(H):
+                js = rng.choice(T, size=n, replace=False)
+                for s, j in enumerate(js):
+                    i = int(rng.integers(j, T))
+                    planted_keys[b, h, s] = j
+                    planted_queries[b, h, s] = i
+                    k1[b, h, j] = 4.0 * q1[b, h, i]
+    if w.value_offset_sigma:
+        offset = (w.value_offset_sigma *
+                  rng.standard_normal((B, H, 2 * D), dtype=np.float32)).astype(np.float32)
+        v += offset[:, :, None, :]
+    if dtype == "bf16":
+        q1, k1, q2, k2, v = (round_to_bf16(a) for a in (q1, k1, q2, k2, v))
+    elif dtype != "f32":
+        raise ValueError(f"unknown dtype {dtype}")
+    return Inputs(q1, k1, q2, k2, v, *lam_vecs, planted_keys=planted_keys,
+                  planted_queries=planted_queries, value_offset=offset)
+
+
+def lambda_init_for(w: Workload) -> float:
+    """lambda_init of a workload: explicit, or the depth schedule at its layer
+    (0.8 - 0.6 exp(-0.3 (l - 1)), layers counted from 1)."""
+    if w.lambda_init is not None:
+        return float(w.lambda_init)
+    if w.layer is None:
+        raise ValueError(f"{w.name}: no lambda_init and no layer")
+    return 0.8 - 0.6 * math.exp(-0.3 * (w.layer - 1))
+
+
+def check_rows(T: int, extra: Sequence[int] = (), n_random: int = 0,
+               seed: int = 1234, tile: int = 128) -> np.ndarray:
+    """Query rows for sampled parity checks: 0, T-1, both sides of every
+    128-row tile boundary, any extra rows, and n_random uniform rows."""
+    rows = {0, T - 1}
+    for t in range(tile, T, tile):
+        rows.add(t - 1)
+        rows.add(t)
+    rows.update(int(r) for r in extra)
+    if n_random:
+        rng = np.random.Generator(np.random.PCG64(seed))
+        rows.update(int(r) for r in rng.integers(0, T, size=n_random))
+    return np.array(sorted(r for r in rows if 0 <= r < T), dtype=np.int64)
