@@ -1,0 +1,186 @@
+"""Differential-attention forward for NVIDIA GB300 (sm_103a).
+
+Python binding over the C ABI in include/diffattn.h.  The two functions
+mirror the interface of the paperleet "Differential Transformer Attention"
+exercise (Functions to implement):
+
+    differential_lambda(q1, k1, q2, k2, lambda_init=0.2) -> 0-d tensor
+    differential_attention(q1, k1, q2, k2, value, coefficient, causal=True) -> tensor
+
+This module only marshals arguments (shapes, strides, device pointers, the
+current CUDA stream); every step of the computation runs in the library's
+CUDA kernels.  There is no CPU path: without the built library, or for
+tensors that are not on a CUDA device, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import numbers
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import (DIFFATTN_BF16, DIFFATTN_F32, DIFFATTN_KERNEL_SIMT,  # noqa: F401
+                   DIFFATTN_KERNEL_TCGEN05, DiffattnDesc, DiffattnError)
+
+__all__ = ["differential_lambda", "differential_attention", "make_desc", "select_kernel",
+           "get_device_error", "version", "DiffattnError"]
+
+_DTYPES = {torch.bfloat16: DIFFATTN_BF16, torch.float32: DIFFATTN_F32}
+
+
+def _stream_handle(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _require_cuda(t: torch.Tensor, name: str) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device}); there is no CPU path")
+
+
+def version() -> int:
+    return _lib.load().diffattn_version()
+
+
+def differential_lambda(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor, k2: torch.Tensor,
+                        lambda_init: float = 0.2) -> torch.Tensor:
+    """lambda = exp(q1 . k1) - exp(q2 . k2) + lambda_init as a 0-d tensor.
+
+    q1, k1, q2, k2 are the four lambda parameter vectors [D_lambda] (equal
+    length, non-empty) on one CUDA device.  The result is float32 on that
+    device, computed in float64 by the library's kernel.  (Forward only.)
+    """
+    vecs = []
+    for name, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2)):
+        _require_cuda(t, name)
+        if t.dim() != 1:
+            raise ValueError(f"{name} must be a 1-D parameter vector")
+        vecs.append(t.detach().to(torch.float32).contiguous())
+    n = vecs[0].numel()
+    if n == 0 or any(v.numel() != n for v in vecs):
+        raise ValueError("lambda vectors must be non-empty and of equal length")
+    dev = vecs[0].device
+    if any(v.device != dev for v in vecs):
+        raise ValueError("lambda vectors must be on one device")
+    out = torch.empty((), dtype=torch.float32, device=dev)
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        rc = lib.diffattn_lambda(*(ctypes.c_void_p(v.data_ptr()) for v in vecs), n,
+                                 float(lambda_init), ctypes.c_void_p(out.data_ptr()),
+                                 _stream_handle(dev))
+    _lib.check(rc, "diffattn_lambda")
+    return out
+
+
+def make_desc(q1, k1, q2, k2, v, out) -> DiffattnDesc:
+    """Fill a diffattn_desc from tensors (sizes, dtype, B/H/T element strides)."""
+    B, H, T, D = q1.shape
+    d = DiffattnDesc()
+    d.B, d.H, d.T, d.D = B, H, T, D
+    d.dtype = _DTYPES[q1.dtype]
+    d.reserved = 0
+    for field, t in (("q1_stride", q1), ("k1_stride", k1), ("q2_stride", q2), ("k2_stride", k2),
+                     ("v_stride", v), ("o_stride", out)):
+        s = t.stride()
+        getattr(d, field)[:] = (s[0], s[1], s[2])
+    return d
+
+
+def _prepare(q1, k1, q2, k2, value):
+    ts = [q1, k1, q2, k2, value]
+    names = ["q1", "k1", "q2", "k2", "value"]
+    for n, t in zip(names, ts):
+        _require_cuda(t, n)
+        if t.dim() != 4:
+            raise ValueError(f"{n} must be 4-D [B, H, T, *]")
+    if not (q1.shape == k1.shape == q2.shape == k2.shape):
+        raise ValueError("q1, k1, q2, k2 must share one shape [B, H, T, D]")
+    B, H, T, D = q1.shape
+    if tuple(value.shape) != (B, H, T, 2 * D):
+        raise ValueError(f"value must be [B, H, T, 2D] = {(B, H, T, 2 * D)}, got {tuple(value.shape)}")
+    dt = q1.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}; expected bfloat16 or float32")
+    if any(t.dtype != dt for t in ts):
+        raise ValueError("all inputs must share one dtype")
+    dev = q1.device
+    if any(t.device != dev for t in ts):
+        raise ValueError("all inputs must be on one device")
+    # The ABI wants a contiguous innermost dimension; other strides pass through.
+    ts = [t if t.stride(-1) == 1 or t.shape[-1] == 1 else t.contiguous() for t in ts]
+    return ts, dev
+
+
+def select_kernel(q1, k1, q2, k2, value, out=None) -> int:
+    """Which kernel differential_attention would launch (DIFFATTN_KERNEL_*)."""
+    (q1, k1, q2, k2, value), dev = _prepare(q1, k1, q2, k2, value)
+    if out is None:
+        out = torch.empty_like(value, memory_format=torch.contiguous_format)
+    d = make_desc(q1, k1, q2, k2, value, out)
+    rc = _lib.load().diffattn_select_kernel(ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in
+                                                               (q1, k1, q2, k2, value, out)))
+    if rc < 0:
+        _lib.check(rc, "diffattn_select_kernel")
+    return rc
+
+
+def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor, k2: torch.Tensor,
+                           value: torch.Tensor, coefficient, causal: bool = True,
+                           out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """O = (softmax(Q1 K1^T/sqrt(D) + M) - lambda softmax(Q2 K2^T/sqrt(D) + M)) V.
+
+    q1, k1, q2, k2: [B, H, T, D]; value: [B, H, T, 2D]; all bfloat16 or all
+    float32 on one CUDA device, innermost dimension contiguous (other strides
+    are passed through).  coefficient: lambda, a Python number or a scalar
+    tensor (a CUDA float32 scalar is read by the kernel without a host sync).
+    causal: mask key j > query i in both branches.  out: optional preallocated
+    [B, H, T, 2D] output of the same dtype.  Returns the [B, H, T, 2D] output;
+    the launch is asynchronous on the current CUDA stream.  (Forward only.)
+    """
+    (q1, k1, q2, k2, value), dev = _prepare(q1, k1, q2, k2, value)
+    B, H, T, D = q1.shape
+    if out is None:
+        out = torch.empty((B, H, T, 2 * D), dtype=q1.dtype, device=dev)
+    else:
+        _require_cuda(out, "out")
+        if tuple(out.shape) != (B, H, T, 2 * D) or out.dtype != q1.dtype or out.device != dev:
+            raise ValueError("out must be [B, H, T, 2D] with the inputs' dtype and device")
+        if out.stride(-1) != 1:
+            raise ValueError("out must have a contiguous innermost dimension")
+    lam_host = 0.0
+    lam_dev = None
+    if isinstance(coefficient, torch.Tensor):
+        if coefficient.numel() != 1:
+            raise ValueError("coefficient must be a scalar")
+        if coefficient.device.type == "cuda":
+            if coefficient.device != dev:
+                raise ValueError("coefficient tensor must be on the inputs' device")
+            lam_dev = coefficient.detach().reshape(()).to(torch.float32)
+        else:
+            lam_host = float(coefficient.item())
+    elif isinstance(coefficient, numbers.Real):
+        lam_host = float(coefficient)
+    else:
+        raise TypeError("coefficient must be a real number or a scalar tensor")
+    d = make_desc(q1, k1, q2, k2, value, out)
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        rc = lib.diffattn_fwd(ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in
+                                                  (q1, k1, q2, k2, value)),
+                              ctypes.c_float(lam_host),
+                              ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0),
+                              1 if causal else 0, ctypes.c_void_p(out.data_ptr()),
+                              _stream_handle(dev))
+    _lib.check(rc, "diffattn_fwd")
+    return out
+
+
+def get_device_error(device=None) -> int:
+    """Synchronise the current stream and return the library's device status
+    (0, or DIFFATTN_ERR_TIMEOUT if a kernel's bounded wait ran out)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return _lib.load().diffattn_get_device_error(_stream_handle(dev))

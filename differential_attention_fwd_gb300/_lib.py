@@ -1,0 +1,90 @@
+"""ctypes loader and signatures of libdiffattn.so (include/diffattn.h)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdiffattn.so")
+
+DIFFATTN_OK = 0
+DIFFATTN_ERR_INVALID = -1
+DIFFATTN_ERR_UNSUPPORTED = -2
+DIFFATTN_ERR_CUDA = -3
+DIFFATTN_ERR_TIMEOUT = -4
+
+DIFFATTN_BF16 = 0
+DIFFATTN_F32 = 1
+
+DIFFATTN_KERNEL_TCGEN05 = 1
+DIFFATTN_KERNEL_SIMT = 2
+
+# Every symbol include/diffattn.h declares.
+EXPORTED = (
+    "diffattn_lambda",
+    "diffattn_fwd",
+    "diffattn_select_kernel",
+    "diffattn_get_device_error",
+    "diffattn_strerror",
+    "diffattn_version",
+)
+
+
+class DiffattnDesc(ctypes.Structure):
+    """Mirror of diffattn_desc."""
+    _fields_ = [
+        ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64), ("D", ctypes.c_int64),
+        ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("q1_stride", ctypes.c_int64 * 3), ("k1_stride", ctypes.c_int64 * 3),
+        ("q2_stride", ctypes.c_int64 * 3), ("k2_stride", ctypes.c_int64 * 3),
+        ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+    ]
+
+
+class DiffattnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.diffattn_lambda.argtypes = [vp, vp, vp, vp, i64, ctypes.c_double, vp, vp]
+    lib.diffattn_lambda.restype = ctypes.c_int
+    lib.diffattn_fwd.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, ctypes.c_float,
+                                 vp, ctypes.c_int, vp, vp]
+    lib.diffattn_fwd.restype = ctypes.c_int
+    lib.diffattn_select_kernel.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, vp]
+    lib.diffattn_select_kernel.restype = ctypes.c_int
+    lib.diffattn_get_device_error.argtypes = [vp]
+    lib.diffattn_get_device_error.restype = ctypes.c_int
+    lib.diffattn_strerror.argtypes = [ctypes.c_int]
+    lib.diffattn_strerror.restype = ctypes.c_char_p
+    lib.diffattn_version.argtypes = []
+    lib.diffattn_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load().diffattn_strerror(code).decode()
+    except RuntimeError:
+        return f"error {code}"
+
+
+def check(code: int, what: str) -> None:
+    if code != DIFFATTN_OK:
+        raise DiffattnError(code, what)

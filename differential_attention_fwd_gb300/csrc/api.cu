@@ -1,0 +1,247 @@
+// api.cu -- the C ABI declared in include/diffattn.h: argument checks, kernel
+// selection, TMA tensor-map encoding and launches on the caller's stream.
+#include "diffattn.h"
+#include "kernels.h"
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+namespace diffattn {
+
+// The library's device status word (one per device, module scope).  Kernels
+// OR status bits into it; diffattn_get_device_error reads and clears it.
+__device__ uint32_t g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    uint32_t* status = nullptr;   // device address of g_status_word
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DIFFATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& st = g_devices[dev];
+    if (!st.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return DIFFATTN_ERR_CUDA;
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+        st.num_sms = sms;
+        st.status = static_cast<uint32_t*>(addr);
+        st.ready = true;
+    }
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return DIFFATTN_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *out = &st;
+    return DIFFATTN_OK;
+}
+
+bool strides_nonneg(const int64_t s[3]) { return s[0] >= 0 && s[1] >= 0 && s[2] >= 0; }
+
+int validate(const diffattn_desc* d, const void* q1, const void* k1, const void* q2,
+             const void* k2, const void* v, const void* out) {
+    if (!d || !q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID;
+    if (d->B < 1 || d->H < 1 || d->T < 1 || d->D < 1 || d->D > 128) return DIFFATTN_ERR_INVALID;
+    if (d->dtype != DIFFATTN_BF16 && d->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID;
+    if (d->reserved != 0) return DIFFATTN_ERR_INVALID;
+    if (!strides_nonneg(d->q1_stride) || !strides_nonneg(d->k1_stride) ||
+        !strides_nonneg(d->q2_stride) || !strides_nonneg(d->k2_stride) ||
+        !strides_nonneg(d->v_stride) || !strides_nonneg(d->o_stride))
+        return DIFFATTN_ERR_INVALID;
+    // Index arithmetic limits of the kernels (int32 rows, tiles and items).
+    if (d->T > INT32_MAX - 128 || d->B > INT32_MAX || d->H > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
+    const int64_t nq = (d->T + 127) / 128;
+    if (d->B * d->H > INT32_MAX / nq) return DIFFATTN_ERR_UNSUPPORTED;
+    return DIFFATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A stride qualifies for the tensor-core path if its dimension has size 1
+// (never stepped) or it is a positive multiple of 8 elements (16 bytes).
+bool tc_stride_ok(int64_t stride, int64_t size) {
+    return size == 1 || (stride > 0 && stride % 8 == 0 && stride < (int64_t(1) << 38));
+}
+bool tc_strides_ok(const int64_t s[3], const diffattn_desc* d) {
+    return tc_stride_ok(s[0], d->B) && tc_stride_ok(s[1], d->H) && tc_stride_ok(s[2], d->T);
+}
+
+int select(const diffattn_desc* d, const void* q1, const void* k1, const void* q2,
+           const void* k2, const void* v, const void* out) {
+    if (d->dtype == DIFFATTN_BF16 && d->D == 64 && aligned16(q1) && aligned16(k1) &&
+        aligned16(q2) && aligned16(k2) && aligned16(v) && aligned16(out) &&
+        tc_strides_ok(d->q1_stride, d) && tc_strides_ok(d->k1_stride, d) &&
+        tc_strides_ok(d->q2_stride, d) && tc_strides_ok(d->k2_stride, d) &&
+        tc_strides_ok(d->v_stride, d) && tc_strides_ok(d->o_stride, d))
+        return DIFFATTN_KERNEL_TCGEN05;
+    return DIFFATTN_KERNEL_SIMT;
+}
+
+// 4-D bf16 tensor map {inner, T, H, B} with a {box_inner, 128, 1, 1} box and
+// 128-byte swizzling; rows past T read as zeros.
+int encode_map(CUtensorMap* m, const void* base, int64_t inner, const diffattn_desc* d,
+               const int64_t s[3], uint32_t box_inner) {
+    int64_t sT = s[2], sH = s[1], sB = s[0];
+    // A size-1 dimension is never stepped; give it a stride the encoder accepts.
+    if (d->T == 1) sT = inner;
+    if (d->H == 1) sH = sT * d->T;
+    if (d->B == 1) sB = sH * d->H;
+    const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)d->T, (cuuint64_t)d->H,
+                                (cuuint64_t)d->B};
+    const cuuint64_t strides[3] = {(cuuint64_t)sT * 2, (cuuint64_t)sH * 2, (cuuint64_t)sB * 2};
+    const cuuint32_t box[4] = {box_inner, 128, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+void copy3(int64_t dst[3], const int64_t src[3]) {
+    dst[0] = src[0];
+    dst[1] = src[1];
+    dst[2] = src[2];
+}
+
+}  // namespace
+}  // namespace diffattn
+
+using namespace diffattn;
+
+extern "C" {
+
+int diffattn_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                    int64_t n, double lambda_init, float* lambda_out, diffattn_stream_t stream) {
+    if (!lq1 || !lk1 || !lq2 || !lk2 || !lambda_out || n < 1 || !std::isfinite(lambda_init))
+        return DIFFATTN_ERR_INVALID;
+    return launch_lambda(lq1, lk1, lq2, lk2, n, lambda_init, lambda_out,
+                         reinterpret_cast<cudaStream_t>(stream)) == 0
+               ? DIFFATTN_OK
+               : DIFFATTN_ERR_CUDA;
+}
+
+int diffattn_select_kernel(const diffattn_desc* desc, const void* q1, const void* k1,
+                           const void* q2, const void* k2, const void* v, const void* out) {
+    const int rc = validate(desc, q1, k1, q2, k2, v, out);
+    if (rc != DIFFATTN_OK) return rc;
+    return select(desc, q1, k1, q2, k2, v, out);
+}
+
+int diffattn_fwd(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
+                 const void* k2, const void* v, float lambda, const float* lambda_dev,
+                 int causal, void* out, diffattn_stream_t stream) {
+    int rc = validate(desc, q1, k1, q2, k2, v, out);
+    if (rc != DIFFATTN_OK) return rc;
+    if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
+    const diffattn_desc& d = *desc;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    DeviceState* dev = nullptr;
+    rc = device_state(&dev);
+    if (rc != DIFFATTN_OK) return rc;
+
+    if (select(desc, q1, k1, q2, k2, v, out) == DIFFATTN_KERNEL_TCGEN05) {
+        CUtensorMap maps[5];
+        if (encode_map(&maps[0], q1, 64, &d, d.q1_stride, 64) != DIFFATTN_OK ||
+            encode_map(&maps[1], k1, 64, &d, d.k1_stride, 64) != DIFFATTN_OK ||
+            encode_map(&maps[2], q2, 64, &d, d.q2_stride, 64) != DIFFATTN_OK ||
+            encode_map(&maps[3], k2, 64, &d, d.k2_stride, 64) != DIFFATTN_OK ||
+            encode_map(&maps[4], v, 128, &d, d.v_stride, 64) != DIFFATTN_OK)
+            return DIFFATTN_ERR_CUDA;
+        TcParams p;
+        p.B = (int)d.B;
+        p.H = (int)d.H;
+        p.T = (int)d.T;
+        p.nq = (int)((d.T + 127) / 128);
+        p.total_items = (int)(d.B * d.H * p.nq);
+        p.causal = causal ? 1 : 0;
+        p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.D));
+        p.lambda = lambda;
+        p.lambda_dev = lambda_dev;
+        p.out = static_cast<__nv_bfloat16*>(out);
+        p.o_sB = d.o_stride[0];
+        p.o_sH = d.o_stride[1];
+        p.o_sT = d.o_stride[2];
+        p.status = dev->status;
+        const int grid = p.total_items < dev->num_sms ? p.total_items : dev->num_sms;
+        return launch_fwd_tc(maps, p, grid, st) == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+    }
+
+    SimtParams p;
+    p.B = (int)d.B;
+    p.H = (int)d.H;
+    p.T = (int)d.T;
+    p.D = (int)d.D;
+    p.causal = causal ? 1 : 0;
+    p.scale = (float)(1.0 / std::sqrt((double)d.D));
+    p.lambda = lambda;
+    p.lambda_dev = lambda_dev;
+    p.q1 = q1;
+    p.k1 = k1;
+    p.q2 = q2;
+    p.k2 = k2;
+    p.v = v;
+    p.out = out;
+    copy3(p.s_q1, d.q1_stride);
+    copy3(p.s_k1, d.k1_stride);
+    copy3(p.s_q2, d.q2_stride);
+    copy3(p.s_k2, d.k2_stride);
+    copy3(p.s_v, d.v_stride);
+    copy3(p.s_o, d.o_stride);
+    rc = (d.dtype == DIFFATTN_F32) ? launch_fwd_simt_f32(p, st) : launch_fwd_simt_bf16(p, st);
+    return rc == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+int diffattn_get_device_error(diffattn_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DIFFATTN_ERR_CUDA;
+    DeviceState* dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != DIFFATTN_OK) return rc;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DIFFATTN_ERR_CUDA;
+    if (word == 0) return DIFFATTN_OK;
+    if (cudaMemset(dev->status, 0, sizeof(word)) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return DIFFATTN_ERR_CUDA;
+    return DIFFATTN_ERR_TIMEOUT;
+}
+
+const char* diffattn_strerror(int code) {
+    switch (code) {
+        case DIFFATTN_OK: return "success";
+        case DIFFATTN_ERR_INVALID: return "invalid argument";
+        case DIFFATTN_ERR_UNSUPPORTED: return "unsupported request";
+        case DIFFATTN_ERR_CUDA: return "CUDA error";
+        case DIFFATTN_ERR_TIMEOUT: return "a kernel wait ran out of time";
+        default: return "unknown error code";
+    }
+}
+
+int diffattn_version(void) { return 100; }
+
+}  // extern "C"

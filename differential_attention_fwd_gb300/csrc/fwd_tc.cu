@@ -1,0 +1,469 @@
+// fwd_tc.cu -- differential-attention forward on the sm_103a tensor cores.
+//
+// Computes O = (softmax(Q1 K1^T / sqrt(D) + M) - lambda softmax(Q2 K2^T / sqrt(D) + M)) V
+// (paperleet "Differential Transformer Attention", Formula and conventions;
+// aifetchly "Differential Transformer...", section 1) for bf16 inputs with
+// D = 64 and V width 128, fp32 accumulation, bf16 output.
+//
+// One CTA per SM (persistent).  A work item is (batch b, head h, 128-query
+// tile).  Per item the CTA loads Q1/Q2 once and streams (K1, K2) and V tiles
+// of 128 keys through TMA rings in shared memory.  Both score products
+// S_b = Q_b K_b^T run as tcgen05 MMAs into tensor memory (TMEM); each branch
+// keeps its own streaming-softmax row state (max and sum) in the registers of
+// its own warpgroup, one query row per thread; the probabilities P_b are
+// written back over S_b in TMEM as bf16 and feed the O_b += P_b V MMAs, both
+// reading the same V tile from shared memory.  The epilogue writes
+// O_1 / l_1 - lambda O_2 / l_2.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax + epilogue, branch 1 (TMEM lanes 0-127)
+//   warps 4-7  softmax + epilogue, branch 2
+//   warp  8    TMA producer
+//   warp  9    TMEM allocation and MMA issue
+// TMEM columns: S1 [0,128)  S2 [128,256)  O1 [256,384)  O2 [384,512).
+//
+// Causal masking (both branches): KV tiles above the diagonal are never
+// loaded; the diagonal tile masks key > query with -inf before the row max.
+//
+// Streaming softmax: the running max m is kept in log2 units of the scaled
+// scores.  O and l are rescaled only when a tile's row max exceeds m by more
+// than 8 (a factor 256), so P stays <= 256 and the rescale (a TMEM
+// read-modify-write of the O row) is rare.  This lazy rescaling is the
+// conditional-rescale idea of FlashAttention-4; the final O / l is exact
+// whichever m was used.
+#include "ptx.cuh"
+#include "kernels.h"
+
+namespace diffattn {
+namespace tc {
+
+constexpr int BM = 128;            // query rows per tile (= TMEM lanes)
+constexpr int BN = 128;            // keys per KV tile
+constexpr int HD = 64;             // Q/K width D
+constexpr int VD = 128;            // V/O width 2D
+constexpr int KSTAGES = 3;         // (K1, K2) ring depth
+constexpr int VSTAGES = 2;         // V ring depth
+constexpr int NUM_THREADS = 320;
+
+constexpr uint32_t Q_BYTES = BM * HD * 2;        // 16 KB per branch
+constexpr uint32_t K_BYTES = BN * HD * 2;        // 16 KB per branch
+constexpr uint32_t V_HALF_BYTES = BN * 64 * 2;   // 16 KB per 64-column half
+constexpr uint32_t V_BYTES = 2 * V_HALF_BYTES;   // 32 KB
+
+// Shared-memory layout (offsets from a 1024-byte aligned base).
+constexpr uint32_t OFF_Q1 = 0;
+constexpr uint32_t OFF_Q2 = OFF_Q1 + Q_BYTES;
+constexpr uint32_t OFF_K = OFF_Q2 + Q_BYTES;                    // stage s: K1 at +0, K2 at +K_BYTES
+constexpr uint32_t OFF_V = OFF_K + KSTAGES * 2 * K_BYTES;       // stage s: cols 0-63 at +0, 64-127 at +V_HALF
+constexpr uint32_t OFF_BAR = OFF_V + VSTAGES * V_BYTES;
+// barriers
+constexpr int BAR_Q_FULL = 0;
+constexpr int BAR_Q_EMPTY = 1;
+constexpr int BAR_K_FULL = 2;
+constexpr int BAR_K_EMPTY = BAR_K_FULL + KSTAGES;
+constexpr int BAR_V_FULL = BAR_K_EMPTY + KSTAGES;
+constexpr int BAR_V_EMPTY = BAR_V_FULL + VSTAGES;
+constexpr int BAR_S_FULL = BAR_V_EMPTY + VSTAGES;      // [2]
+constexpr int BAR_P_FULL = BAR_S_FULL + 2;             // [2]
+constexpr int BAR_O_FULL = BAR_P_FULL + 2;
+constexpr int BAR_O_EMPTY = BAR_O_FULL + 1;
+constexpr int BAR_L_READY = BAR_O_EMPTY + 1;           // 1/l of both branches in smem
+constexpr int BAR_FINAL = BAR_L_READY + 1;
+constexpr int NUM_BARS = BAR_FINAL + 1;
+constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
+constexpr uint32_t OFF_INVL = (OFF_ABORT + 4 + 15) & ~15u;    // float [2][128]
+constexpr uint32_t SMEM_USED = OFF_INVL + 2 * BM * 4;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;               // + alignment slack
+
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);   // Q (K-major) x K^T (K-major)
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, VD, 0, 1);  // P (TMEM) x V (MN-major)
+
+struct Item {
+    int qt, b, h, n_kv;
+};
+
+// The CTA's k-th work item in a boustrophedon order over the item list, so
+// that with causal items sorted longest-first every CTA gets a similar total.
+__device__ __forceinline__ int item_index(int k, int cta, int grid) {
+    const int base = k * grid;
+    return base + ((k & 1) ? (grid - 1 - cta) : cta);
+}
+
+__device__ __forceinline__ Item decode_item(int idx, const TcParams& p) {
+    const int BH = p.B * p.H;
+    const int r = idx / BH;
+    const int bh = idx - r * BH;
+    Item it;
+    it.qt = p.causal ? (p.nq - 1 - r) : r;
+    it.b = bh / p.H;
+    it.h = bh - it.b * p.H;
+    it.n_kv = p.causal ? (it.qt + 1) : p.nq;
+    return it;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
+                       const __grid_constant__ CUtensorMap tm_k1,
+                       const __grid_constant__ CUtensorMap tm_q2,
+                       const __grid_constant__ CUtensorMap tm_k2,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + OFF_TMEM_PTR);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_ABORT);
+    float* inv_l = reinterpret_cast<float*>(smem + OFF_INVL);
+
+    const uint32_t warp = warp_id();
+    const uint32_t lane = threadIdx.x & 31;
+    const AbortState ab{abort_flag, p.status};
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[BAR_Q_FULL], 1);
+        mbar_init(&bars[BAR_Q_EMPTY], 1);
+        for (int s = 0; s < KSTAGES; ++s) {
+            mbar_init(&bars[BAR_K_FULL + s], 1);
+            mbar_init(&bars[BAR_K_EMPTY + s], 1);
+        }
+        for (int s = 0; s < VSTAGES; ++s) {
+            mbar_init(&bars[BAR_V_FULL + s], 1);
+            mbar_init(&bars[BAR_V_EMPTY + s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars[BAR_S_FULL + b], 1);
+            mbar_init(&bars[BAR_P_FULL + b], 4);
+        }
+        mbar_init(&bars[BAR_O_FULL], 1);
+        mbar_init(&bars[BAR_O_EMPTY], 8);
+        mbar_init(&bars[BAR_L_READY], 8);
+        mbar_init(&bars[BAR_FINAL], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(tmem_ptr, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_ptr;
+
+    const int grid = gridDim.x;
+    const int cta = blockIdx.x;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (elect_one()) {
+            tma_prefetch_desc(&tm_q1);
+            tma_prefetch_desc(&tm_k1);
+            tma_prefetch_desc(&tm_q2);
+            tma_prefetch_desc(&tm_k2);
+            tma_prefetch_desc(&tm_v);
+            uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0;
+            uint32_t armed_q = 0, armed_k[KSTAGES] = {}, armed_v[VSTAGES] = {};
+            bool ok = true;
+            bool first = true;
+            for (int k = 0; ok; ++k) {
+                if (k * grid >= p.total_items) break;
+                const int idx = item_index(k, cta, grid);
+                if (idx >= p.total_items) continue;
+                const Item it = decode_item(idx, p);
+                if (!first) {
+                    if (!(ok = mbar_wait(&bars[BAR_Q_EMPTY], qph, ab))) break;
+                    qph ^= 1;
+                }
+                first = false;
+                mbar_arrive_expect_tx(&bars[BAR_Q_FULL], 2 * Q_BYTES);
+                tma_load_4d(smem + OFF_Q1, &tm_q1, &bars[BAR_Q_FULL], 0, it.qt * BM, it.h, it.b);
+                tma_load_4d(smem + OFF_Q2, &tm_q2, &bars[BAR_Q_FULL], 0, it.qt * BM, it.h, it.b);
+                ++armed_q;
+                for (int j = 0; j < it.n_kv; ++j) {
+                    if (!(ok = mbar_wait(&bars[BAR_K_EMPTY + kst], kph ^ 1, ab))) break;
+                    uint8_t* kdst = smem + OFF_K + kst * 2 * K_BYTES;
+                    mbar_arrive_expect_tx(&bars[BAR_K_FULL + kst], 2 * K_BYTES);
+                    tma_load_4d(kdst, &tm_k1, &bars[BAR_K_FULL + kst], 0, j * BN, it.h, it.b);
+                    tma_load_4d(kdst + K_BYTES, &tm_k2, &bars[BAR_K_FULL + kst], 0, j * BN, it.h, it.b);
+                    ++armed_k[kst];
+                    if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
+
+                    if (!(ok = mbar_wait(&bars[BAR_V_EMPTY + vst], vph ^ 1, ab))) break;
+                    uint8_t* vdst = smem + OFF_V + vst * V_BYTES;
+                    mbar_arrive_expect_tx(&bars[BAR_V_FULL + vst], V_BYTES);
+                    tma_load_4d(vdst, &tm_v, &bars[BAR_V_FULL + vst], 0, j * BN, it.h, it.b);
+                    tma_load_4d(vdst + V_HALF_BYTES, &tm_v, &bars[BAR_V_FULL + vst], 64, j * BN, it.h, it.b);
+                    ++armed_v[vst];
+                    if (++vst == VSTAGES) { vst = 0; vph ^= 1; }
+                }
+            }
+            // Never leave a copy in flight into shared memory we are about to
+            // give back: wait (bounded) for the last armed phase of every ring.
+            const uint64_t lim = 200ull * 1000ull * 1000ull;
+            if (armed_q) mbar_wait_teardown(&bars[BAR_Q_FULL], (armed_q - 1) & 1, lim);
+            for (int s = 0; s < KSTAGES; ++s)
+                if (armed_k[s]) mbar_wait_teardown(&bars[BAR_K_FULL + s], (armed_k[s] - 1) & 1, lim);
+            for (int s = 0; s < VSTAGES; ++s)
+                if (armed_v[s]) mbar_wait_teardown(&bars[BAR_V_FULL + s], (armed_v[s] - 1) & 1, lim);
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issue
+        if (elect_one()) {
+            const uint32_t sq[2] = {smem_u32(smem + OFF_Q1), smem_u32(smem + OFF_Q2)};
+            const uint32_t sk0 = smem_u32(smem + OFF_K);
+            const uint32_t sv0 = smem_u32(smem + OFF_V);
+            uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0, oeph = 0;
+            uint32_t pph[2] = {0, 0};
+            bool ok = true;
+
+            auto issue_s = [&](int br, uint32_t stage) {
+                const uint32_t d = tmem_base + br * 128;
+                const uint32_t qa = sq[br];
+                const uint32_t ka = sk0 + stage * 2 * K_BYTES + br * K_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    mma_ss(d, sdesc_sw128(qa + kk * 32, 16, 1024), sdesc_sw128(ka + kk * 32, 16, 1024),
+                           IDESC_S, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int br, uint32_t stage, bool acc) {
+                const uint32_t d = tmem_base + 256 + br * 128;
+                const uint32_t pa = tmem_base + br * 128;
+                const uint32_t va = sv0 + stage * V_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    mma_ts(d, pa + kk * 8, sdesc_sw128(va + kk * 2048, V_HALF_BYTES, 1024), IDESC_PV,
+                           (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+
+            bool first = true;
+            for (int k = 0; ok; ++k) {
+                if (k * grid >= p.total_items) break;
+                const int idx = item_index(k, cta, grid);
+                if (idx >= p.total_items) continue;
+                const Item it = decode_item(idx, p);
+                if (!(ok = mbar_wait(&bars[BAR_Q_FULL], qph, ab))) break;
+                qph ^= 1;
+                if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
+                tc_fence_after();
+                issue_s(0, kst);
+                mma_commit(&bars[BAR_S_FULL + 0]);
+                issue_s(1, kst);
+                mma_commit(&bars[BAR_S_FULL + 1]);
+                mma_commit(&bars[BAR_K_EMPTY + kst]);
+                if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
+                if (it.n_kv == 1) mma_commit(&bars[BAR_Q_EMPTY]);
+
+                for (int j = 0; j < it.n_kv; ++j) {
+                    // branch 1: O1 += P1 V(j), then S1(j+1)
+                    if (!(ok = mbar_wait(&bars[BAR_P_FULL + 0], pph[0], ab))) break;
+                    pph[0] ^= 1;
+                    if (j == 0 && !first) {
+                        if (!(ok = mbar_wait(&bars[BAR_O_EMPTY], oeph, ab))) break;
+                        oeph ^= 1;
+                    }
+                    if (!(ok = mbar_wait(&bars[BAR_V_FULL + vst], vph, ab))) break;
+                    tc_fence_after();
+                    issue_pv(0, vst, j > 0);
+                    const bool more = (j + 1 < it.n_kv);
+                    if (more) {
+                        if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
+                        tc_fence_after();
+                        issue_s(0, kst);
+                        mma_commit(&bars[BAR_S_FULL + 0]);
+                    }
+                    // branch 2: O2 += P2 V(j), then S2(j+1)
+                    if (!(ok = mbar_wait(&bars[BAR_P_FULL + 1], pph[1], ab))) break;
+                    pph[1] ^= 1;
+                    tc_fence_after();
+                    issue_pv(1, vst, j > 0);
+                    mma_commit(&bars[BAR_V_EMPTY + vst]);
+                    if (++vst == VSTAGES) { vst = 0; vph ^= 1; }
+                    if (more) {
+                        issue_s(1, kst);
+                        mma_commit(&bars[BAR_S_FULL + 1]);
+                        mma_commit(&bars[BAR_K_EMPTY + kst]);
+                        if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
+                        if (j + 2 == it.n_kv) mma_commit(&bars[BAR_Q_EMPTY]);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&bars[BAR_O_FULL]);
+                first = false;
+            }
+            // Every MMA issued so far must have finished before TMEM is freed.
+            mma_commit(&bars[BAR_FINAL]);
+            mbar_wait_teardown(&bars[BAR_FINAL], 0, 200ull * 1000ull * 1000ull);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- softmax + epilogue
+        const int br = warp >> 2;            // branch
+        const uint32_t quad = warp & 3;      // TMEM lane quadrant
+        const int row = quad * 32 + lane;    // query row within the tile
+        const uint32_t lane_base = tmem_base + ((quad * 32u) << 16);
+        const uint32_t tS = lane_base + br * 128;
+        const uint32_t tO = lane_base + 256 + br * 128;
+        const float sl2 = p.scale_log2;
+        const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
+        uint32_t sph = 0, ofph = 0, lph = 0;
+        bool ok = true;
+
+        for (int k = 0; ok; ++k) {
+            if (k * grid >= p.total_items) break;
+            const int idx = item_index(k, cta, grid);
+            if (idx >= p.total_items) continue;
+            const Item it = decode_item(idx, p);
+            const int q = it.qt * BM + row;
+            float m_run = -INFINITY;
+            float l = 0.f;
+
+            for (int j = 0; j < it.n_kv; ++j) {
+                if (!(ok = mbar_wait_warp(&bars[BAR_S_FULL + br], sph, ab))) break;
+                sph ^= 1;
+                tc_fence_after();
+                uint32_t u[128];
+                tmem_ld32(tS + 0, &u[0]);
+                tmem_ld32(tS + 32, &u[32]);
+                tmem_ld32(tS + 64, &u[64]);
+                tmem_ld32(tS + 96, &u[96]);
+                tmem_wait_ld();
+                float s[128];
+#pragma unroll
+                for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
+
+                const int kv0 = j * BN;
+                if (p.causal && j == it.n_kv - 1) {
+                    const int lim = q - kv0;           // keys kv0 + c with c > lim are in the future
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) s[c] = (c > lim) ? -INFINITY : s[c];
+                } else if (!p.causal && kv0 + BN > p.T) {
+                    const int lim = p.T - kv0;         // keys at or beyond T do not exist
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) s[c] = (c >= lim) ? -INFINITY : s[c];
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int c = 4; c < 128; c += 4) {
+                    mx0 = fmaxf(mx0, s[c]);
+                    mx1 = fmaxf(mx1, s[c + 1]);
+                    mx2 = fmaxf(mx2, s[c + 2]);
+                    mx3 = fmaxf(mx3, s[c + 3]);
+                }
+                const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+
+                if (j == 0) {
+                    m_run = mxs;
+                } else {
+                    const bool need = mxs > m_run + 8.0f;
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float m_new = fmaxf(m_run, mxs);
+                        const float alpha = ex2_approx(m_run - m_new);
+                        l *= alpha;
+                        m_run = m_new;
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c4 * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st32(tO + c4 * 32, o);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                const float neg = -m_run;
+                float rs0 = 0.f, rs1 = 0.f;
+                uint32_t pk[64];
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float p0 = ex2_approx(fmaf(s[2 * c], sl2, neg));
+                    const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, neg));
+                    rs0 += p0;
+                    rs1 += p1;
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + 0, &pk[0]);
+                tmem_st32(tS + 32, &pk[32]);
+                tmem_wait_st();
+                l += rs0 + rs1;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[BAR_P_FULL + br]);
+            }
+            if (!ok) break;
+
+            // ---------------------------------------------------- epilogue
+            if (!(ok = mbar_wait_warp(&bars[BAR_O_FULL], ofph, ab))) break;
+            ofph ^= 1;
+            tc_fence_after();
+            inv_l[br * BM + row] = 1.0f / l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[BAR_L_READY]);
+            if (!(ok = mbar_wait_warp(&bars[BAR_L_READY], lph, ab))) break;
+            lph ^= 1;
+            const float inv1 = inv_l[row];
+            const float inv2 = inv_l[BM + row];
+            const int c0 = br * 64;          // this warpgroup writes output columns [c0, c0+64)
+            const bool valid = q < p.T;
+            __nv_bfloat16* orow = p.out + (int64_t)it.b * p.o_sB + (int64_t)it.h * p.o_sH +
+                                  (int64_t)q * p.o_sT + c0;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t o1[32], o2[32];
+                tmem_ld32(lane_base + 256 + c0 + half * 32, o1);
+                tmem_ld32(lane_base + 384 + c0 + half * 32, o2);
+                tmem_wait_ld();
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float r[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float a = __fmul_rn(__uint_as_float(o1[2 * i + e]), inv1);
+                        const float bb = __fmul_rn(__uint_as_float(o2[2 * i + e]), inv2);
+                        r[e] = __fsub_rn(a, __fmul_rn(lam, bb));
+                    }
+                    packed[i] = pack_bf16x2(r[0], r[1]);
+                }
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + half * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                            packed[4 * i + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[BAR_O_EMPTY]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace tc
+
+int launch_fwd_tc(const CUtensorMap* maps, const TcParams& p, int grid, cudaStream_t stream) {
+    static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
+    cudaError_t e = cudaFuncSetAttribute(tc::diffattn_fwd_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tc::SMEM_BYTES);
+    if (e != cudaSuccess) return -1;
+    tc::diffattn_fwd_tc_kernel<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace diffattn

@@ -1,0 +1,46 @@
+// kernels.h -- internal interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace diffattn {
+
+// Parameters of the tensor-core kernel (bf16, D = 64).
+struct TcParams {
+    int B, H, T;
+    int nq;                 // number of 128-row tiles along T
+    int total_items;        // B * H * nq
+    int causal;
+    float scale_log2;       // log2(e) / sqrt(D)
+    float lambda;           // used when lambda_dev == nullptr
+    const float* lambda_dev;
+    __nv_bfloat16* out;
+    int64_t o_sB, o_sH, o_sT;
+    uint32_t* status;       // device status word
+};
+
+// Parameters of the CUDA-core kernel (any D <= 128, fp32 or bf16).
+struct SimtParams {
+    int B, H, T, D;
+    int causal;
+    float scale;            // 1 / sqrt(D)
+    float lambda;
+    const float* lambda_dev;
+    const void* q1; const void* k1; const void* q2; const void* k2; const void* v;
+    void* out;
+    int64_t s_q1[3], s_k1[3], s_q2[3], s_k2[3], s_v[3], s_o[3];
+};
+
+// Each returns 0 on success, -1 if the launch failed.
+int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v*/, const TcParams& p, int grid,
+                  cudaStream_t stream);
+int launch_fwd_simt_f32(const SimtParams& p, cudaStream_t stream);
+int launch_fwd_simt_bf16(const SimtParams& p, cudaStream_t stream);
+int launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                  int64_t n, double lambda_init, float* out, cudaStream_t stream);
+
+}  // namespace diffattn

@@ -1,0 +1,160 @@
+/*
+ * diffattn.h -- C ABI of the differential-attention forward for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operation (paperleet "Differential Transformer Attention", Formula and
+ * conventions; aifetchly "Differential Transformer: Canceling LLM Attention
+ * Noise", section 1):
+ *
+ *     A_b = softmax(Q_b K_b^T / sqrt(D) + M)      b = 1, 2, softmax over keys
+ *     O   = (A_1 - lambda * A_2) V
+ *
+ * with Q1, K1, Q2, K2 of shape [B, H, T, D], V and O of shape [B, H, T, 2D],
+ * and M the optional causal mask: 0 where key j <= query i, -inf where
+ * j > i, applied to both branches.  The scalar lambda comes from four
+ * parameter vectors (aifetchly, section 3; paperleet, Formula and conventions):
+ *
+ *     lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init
+ *
+ * It is not restricted to [0, 1].  Per-head normalisation, its fixed
+ * (1 - lambda_init) multiplier and the projections are not part of this
+ * operation.
+ *
+ * Conventions shared by every entry point:
+ *   - Return value: DIFFATTN_OK (0) on success, a negative DIFFATTN_ERR_* code
+ *     otherwise.  No exception, signal or abort crosses the ABI.
+ *   - Ownership: the caller owns every buffer.  The library never allocates
+ *     device memory per call and never frees caller memory.  Inputs are const
+ *     and are never written.
+ *   - Asynchrony: device work is enqueued on the caller's stream (a
+ *     cudaStream_t; NULL means the legacy default stream).  No entry point
+ *     synchronises the stream except diffattn_get_device_error.
+ *   - Argument checks happen on the host before any CUDA call; a call that
+ *     fails them touches neither the GPU nor any buffer.
+ *   - Thread safety: entry points may be called from several host threads.
+ */
+#ifndef DIFFATTN_H
+#define DIFFATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque stream handle, binary-compatible with cudaStream_t. */
+typedef struct CUstream_st *diffattn_stream_t;
+
+/* Return codes. */
+#define DIFFATTN_OK               0
+#define DIFFATTN_ERR_INVALID     -1  /* bad shape, stride, pointer, dtype or non-finite scalar */
+#define DIFFATTN_ERR_UNSUPPORTED -2  /* a valid request this build has no kernel for */
+#define DIFFATTN_ERR_CUDA        -3  /* a CUDA runtime or driver call failed (incl. launch) */
+#define DIFFATTN_ERR_TIMEOUT     -4  /* a kernel's bounded wait ran out (see get_device_error) */
+
+/* Element types of Q1, K1, Q2, K2, V and O (all six share one type). */
+#define DIFFATTN_BF16 0   /* bfloat16 storage, fp32 accumulation, bf16 output */
+#define DIFFATTN_F32  1   /* float32 storage and arithmetic */
+
+/* Kernel identifiers returned by diffattn_select_kernel. */
+#define DIFFATTN_KERNEL_TCGEN05 1  /* tensor-core kernel: bf16, D == 64 */
+#define DIFFATTN_KERNEL_SIMT    2  /* CUDA-core kernel: any supported shape */
+
+/*
+ * Shape and layout of one call.
+ *
+ * B, H, T, D: batch, heads, sequence length and Q/K width; all >= 1.  V and
+ * O have width 2*D.  D <= 128.
+ * dtype: DIFFATTN_BF16 or DIFFATTN_F32.
+ * *_stride: element strides of the B, H and T dimensions of each tensor
+ * ([0] = B, [1] = H, [2] = T).  The innermost (D or 2D) dimension is always
+ * contiguous (stride 1).  Strides must be >= 0; a stride of 0 is allowed on B
+ * and H (broadcast).  Distinct tensors may alias each other, except that O
+ * must not overlap any input.
+ */
+typedef struct {
+    int64_t B, H, T, D;
+    int32_t dtype;
+    int32_t reserved;          /* must be 0 */
+    int64_t q1_stride[3];
+    int64_t k1_stride[3];
+    int64_t q2_stride[3];
+    int64_t k2_stride[3];
+    int64_t v_stride[3];
+    int64_t o_stride[3];
+} diffattn_desc;
+
+/*
+ * diffattn_lambda -- lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init.
+ *
+ * lq1, lk1, lq2, lk2: device pointers to n contiguous float32 values each
+ * (the lambda parameter vectors, paperleet: "equal nonempty parameter vectors
+ * [D_lambda]").  n >= 1.
+ * lambda_init: the layer's initial value, e.g. 0.8 - 0.6 exp(-0.3 (l - 1)).
+ * lambda_out: device pointer to one float32; receives lambda, computed with
+ * float64 dot products and exponentials and rounded once to float32.
+ * Launches one small kernel on `stream`.  Errors: DIFFATTN_ERR_INVALID for a
+ * NULL pointer, n < 1 or a non-finite lambda_init; DIFFATTN_ERR_CUDA if the
+ * launch fails.
+ */
+int diffattn_lambda(const float *lq1, const float *lk1, const float *lq2,
+                    const float *lk2, int64_t n, double lambda_init,
+                    float *lambda_out, diffattn_stream_t stream);
+
+/*
+ * diffattn_fwd -- O = (A_1 - lambda A_2) V.
+ *
+ * desc: shape, dtype and strides (host pointer, read during the call only).
+ * q1, k1, q2, k2, v: device pointers to the inputs, laid out as desc says.
+ * lambda: the coefficient, used when lambda_dev is NULL; must be finite.
+ * lambda_dev: optional device pointer to one float32 holding lambda (for
+ * example the output of diffattn_lambda); when non-NULL it overrides `lambda`
+ * and is read by the kernel, so no host synchronisation is needed.
+ * causal: non-zero applies the causal mask to both branches.
+ * out: device pointer to O, [B, H, T, 2D] with desc->o_stride, same dtype as
+ * the inputs (bf16 results are rounded to nearest even from fp32).
+ * stream: the CUDA stream to launch on.
+ *
+ * The tensor-core kernel runs when dtype is bf16, D == 64, every base pointer
+ * is 16-byte aligned and every stride is a multiple of 8 elements; any other
+ * valid request runs on the CUDA-core kernel.  One kernel launch per call.
+ * Errors: DIFFATTN_ERR_INVALID (NULL pointers, sizes < 1, D > 128, unknown
+ * dtype, negative strides, non-zero reserved field, non-finite lambda);
+ * DIFFATTN_ERR_CUDA (tensor-map encoding or launch failure).
+ */
+int diffattn_fwd(const diffattn_desc *desc, const void *q1, const void *k1,
+                 const void *q2, const void *k2, const void *v, float lambda,
+                 const float *lambda_dev, int causal, void *out,
+                 diffattn_stream_t stream);
+
+/*
+ * diffattn_select_kernel -- which kernel diffattn_fwd would launch for this
+ * descriptor and these pointers (DIFFATTN_KERNEL_*), or a negative error code
+ * if the arguments are invalid.  Host only; touches no GPU state.
+ */
+int diffattn_select_kernel(const diffattn_desc *desc, const void *q1,
+                           const void *k1, const void *q2, const void *k2,
+                           const void *v, const void *out);
+
+/*
+ * diffattn_get_device_error -- synchronise `stream`, then report whether any
+ * kernel of this library on the current device ran out of a bounded wait
+ * since the previous call (DIFFATTN_ERR_TIMEOUT), and clear that record.
+ * Every wait inside the kernels has an iteration and time limit; on expiry
+ * the kernel records the failure, stops issuing work, releases what it holds
+ * and returns, leaving the CUDA context usable.  Returns DIFFATTN_OK when no
+ * wait ran out, DIFFATTN_ERR_CUDA if the synchronisation itself fails.
+ */
+int diffattn_get_device_error(diffattn_stream_t stream);
+
+/* Human-readable text for a return code (static storage, never NULL). */
+const char *diffattn_strerror(int code);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int diffattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIFFATTN_H */

@@ -1,0 +1,69 @@
+"""Shared test utilities: device placement and the parity tolerances.
+
+Tolerances (stated for this operation): bf16 inputs with fp32 accumulation,
+max-abs error <= 2e-2 and mean-abs error <= 2e-3 against the float64 oracle;
+float32 path, max-abs error <= 1e-4.
+
+bf16 output rounding: an output of magnitude >= 8 cannot be represented in
+bf16 to within 2e-2 (half an ulp there is 2^-5 = 0.031).  For those elements
+the bound applies to the error in excess of half an ulp of the oracle value,
+i.e. to what the kernel adds beyond rounding its fp32 result to bf16.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+BF16_MAX_ABS = 2e-2
+BF16_MEAN_ABS = 2e-3
+F32_MAX_ABS = 1e-4
+
+
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half a unit in the last place of bf16 (8 significant bits) at |x|."""
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return 2.0 ** (e - 8)
+
+
+def compare(got: np.ndarray, ref: np.ndarray, dtype: str) -> dict:
+    """Error statistics of `got` against the float64 oracle `ref`."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "non-finite output"
+    err = np.abs(got - ref)
+    stats = {"max_abs": float(err.max()) if err.size else 0.0,
+             "mean_abs": float(err.mean()) if err.size else 0.0, "n": int(err.size)}
+    if dtype == "bf16":
+        big = np.abs(ref) >= 8.0
+        small_err = err[~big]
+        stats["max_abs_below_8"] = float(small_err.max()) if small_err.size else 0.0
+        excess = err[big] - bf16_half_ulp(ref[big])
+        stats["n_ge_8"] = int(big.sum())
+        stats["max_excess_ge_8"] = float(excess.max()) if excess.size else 0.0
+    return stats
+
+
+def assert_close(got, ref, dtype: str, what: str = "") -> dict:
+    s = compare(got, ref, dtype)
+    if dtype == "f32":
+        assert s["max_abs"] <= F32_MAX_ABS, f"{what} fp32 max-abs {s}"
+    else:
+        assert s["max_abs_below_8"] <= BF16_MAX_ABS, f"{what} bf16 max-abs {s}"
+        assert s["max_excess_ge_8"] <= BF16_MAX_ABS, f"{what} bf16 excess over rounding {s}"
+        assert s["mean_abs"] <= BF16_MEAN_ABS, f"{what} bf16 mean-abs {s}"
+    return s
+
+
+def torch_dtype(dtype: str):
+    return {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+
+
+def to_device(x: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    """float32 array holding dtype-representable values -> device tensor."""
+    return torch.from_numpy(np.ascontiguousarray(x)).to(device=device, dtype=torch_dtype(dtype))
+
+
+def to_numpy(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(device="cpu", dtype=torch.float64).numpy()

@@ -1,0 +1,151 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+symbol include/diffattn.h declares; argument checks reject bad calls before
+any CUDA call (so these run without a GPU); kernel selection is host logic."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from differential_attention_fwd_gb300 import _lib
+from differential_attention_fwd_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "diffattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(diffattn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(_lib.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), f"missing export {n}"
+
+
+def test_desc_layout_matches_header():
+    # 4 x int64, 2 x int32, 6 x int64[3]
+    assert ctypes.sizeof(_lib.DiffattnDesc) == 4 * 8 + 2 * 4 + 6 * 3 * 8
+
+
+def test_version_and_strerror(lib):
+    assert lib.diffattn_version() == 100
+    for code in (0, -1, -2, -3, -4, 7):
+        assert isinstance(lib.diffattn_strerror(code), bytes)
+    assert lib.diffattn_strerror(-4) != lib.diffattn_strerror(0)
+
+
+FAKE = 0x10000  # 64 KiB-aligned stand-in addresses; never dereferenced on the host path
+
+
+def desc(B=1, H=2, T=128, D=64, dtype=_lib.DIFFATTN_BF16, contiguous=True):
+    d = _lib.DiffattnDesc()
+    d.B, d.H, d.T, d.D, d.dtype, d.reserved = B, H, T, D, dtype, 0
+    for f, w in (("q1_stride", D), ("k1_stride", D), ("q2_stride", D), ("k2_stride", D),
+                 ("v_stride", 2 * D), ("o_stride", 2 * D)):
+        getattr(d, f)[:] = (H * T * w, T * w, w)
+    return d
+
+
+def ptrs(n=6, base=FAKE):
+    return [ctypes.c_void_p(base * (i + 1)) for i in range(n)]
+
+
+def select(lib, d, p=None):
+    p = p or ptrs()
+    return lib.diffattn_select_kernel(ctypes.byref(d), *p)
+
+
+def test_select_tcgen05_for_aligned_bf16_d64(lib):
+    assert select(lib, desc()) == _lib.DIFFATTN_KERNEL_TCGEN05
+
+
+@pytest.mark.parametrize("kw", [dict(D=32), dict(D=128), dict(D=48), dict(dtype=_lib.DIFFATTN_F32)])
+def test_select_simt_otherwise(lib, kw):
+    assert select(lib, desc(**kw)) == _lib.DIFFATTN_KERNEL_SIMT
+
+
+def test_select_simt_for_unaligned(lib):
+    p = ptrs()
+    p[2] = ctypes.c_void_p(FAKE * 3 + 2)   # q2 not 16-byte aligned
+    assert select(lib, desc(), p) == _lib.DIFFATTN_KERNEL_SIMT
+    d = desc()
+    d.v_stride[2] = 132                     # row stride not a multiple of 8 elements
+    assert select(lib, d) == _lib.DIFFATTN_KERNEL_SIMT
+
+
+def test_size_one_dims_ignore_strides(lib):
+    d = desc(B=1, H=1, T=1)
+    for f in ("q1_stride", "k1_stride", "q2_stride", "k2_stride", "v_stride", "o_stride"):
+        getattr(d, f)[:] = (0, 0, 3)
+    assert select(lib, d) == _lib.DIFFATTN_KERNEL_TCGEN05
+
+
+@pytest.mark.parametrize("mutate", [
+    lambda d: setattr(d, "B", 0),
+    lambda d: setattr(d, "H", 0),
+    lambda d: setattr(d, "T", 0),
+    lambda d: setattr(d, "D", 0),
+    lambda d: setattr(d, "D", 129),
+    lambda d: setattr(d, "dtype", 2),
+    lambda d: setattr(d, "reserved", 1),
+    lambda d: d.k2_stride.__setitem__(1, -1),
+])
+def test_invalid_desc_rejected_without_gpu(lib, mutate):
+    d = desc()
+    mutate(d)
+    assert select(lib, d) == _lib.DIFFATTN_ERR_INVALID
+    rc = lib.diffattn_fwd(ctypes.byref(d), *ptrs(5), ctypes.c_float(0.5), None, 1,
+                          ctypes.c_void_p(FAKE * 9), None)
+    assert rc == _lib.DIFFATTN_ERR_INVALID
+
+
+def test_null_pointers_rejected(lib):
+    d = desc()
+    for i in range(6):
+        p = ptrs()
+        p[i] = None
+        assert lib.diffattn_select_kernel(ctypes.byref(d), *p) == _lib.DIFFATTN_ERR_INVALID
+    assert lib.diffattn_fwd(None, *ptrs(5), ctypes.c_float(0.5), None, 1, ctypes.c_void_p(FAKE), None) \
+        == _lib.DIFFATTN_ERR_INVALID
+
+
+@pytest.mark.parametrize("lam", [float("nan"), float("inf"), -float("inf")])
+def test_non_finite_lambda_rejected(lib, lam):
+    rc = lib.diffattn_fwd(ctypes.byref(desc()), *ptrs(5), ctypes.c_float(lam), None, 1,
+                          ctypes.c_void_p(FAKE * 9), None)
+    assert rc == _lib.DIFFATTN_ERR_INVALID
+
+
+def test_oversized_rejected(lib):
+    d = desc(B=1 << 20, H=1 << 20, T=1 << 20)
+    assert select(lib, d) == _lib.DIFFATTN_ERR_UNSUPPORTED
+
+
+def test_lambda_args_rejected(lib):
+    p = ptrs(5)
+    assert lib.diffattn_lambda(p[0], p[1], p[2], p[3], 0, 0.2, p[4], None) == _lib.DIFFATTN_ERR_INVALID
+    assert lib.diffattn_lambda(None, p[1], p[2], p[3], 4, 0.2, p[4], None) == _lib.DIFFATTN_ERR_INVALID
+    assert lib.diffattn_lambda(p[0], p[1], p[2], p[3], 4, float("nan"), p[4], None) == _lib.DIFFATTN_ERR_INVALID
+    assert lib.diffattn_lambda(p[0], p[1], p[2], p[3], 4, 0.2, None, None) == _lib.DIFFATTN_ERR_INVALID
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    import differential_attention_fwd_gb300 as da
+    x = torch.zeros(1, 1, 4, 8)
+    v = torch.zeros(1, 1, 4, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        da.differential_attention(x, x, x, x, v, 0.5)
+    with pytest.raises(ValueError, match="CUDA"):
+        da.differential_lambda(torch.zeros(4), torch.zeros(4), torch.zeros(4), torch.zeros(4))
