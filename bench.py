@@ -1,0 +1,477 @@
+#!/usr/bin/env python3
+"""Benchmark of the differential-attention forward on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+lambda from its four parameter vectors (diffattn_lambda) followed by the
+forward O = (A1 - lambda A2) V (diffattn_fwd, reading lambda on the device).
+Default workload: B=2, H=16, T=8192, D=64, V width 128, bf16, causal.
+
+Prints one JSON line (rank 0).  Timing: W untimed warm-up steps, then K
+timed steps; each step is bracketed by CUDA events on the launch stream, and
+the L2 cache is flushed (a 256 MiB write) between steps outside the events.
+`value` is the algorithmic TFLOP/s of the whole job (unmasked pairs x 12 D,
+all ranks).  `e2e` repeats the measurement with inputs copied from pinned
+host memory and the output copied back inside the timed region.
+
+--impl reference times the float64 CPU oracle (the only reference
+implementation of this operation) on a bounded sample of the same workload.
+
+Multi-GPU: replicas only (each rank runs its own copy of the workload; the
+forward has no exchange step), so scaling is weak and value sums the ranks'
+work over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "diffattn_fwd TFLOP/s and % of GB300 bf16 tensor peak (B=2,H=16,T=8192,D=64 causal)"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1000 * 1000
+FLUSH_BYTES = 256 * 1024 * 1024
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "diffattn_fwd_tc_b2h16t8192.md")
+KERNEL_SOURCES = ["fwd_tc.cu", "ptx.cuh", "kernels.h"]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------
+# host logic shared by every rank count (tested on CPU with gloo)
+# --------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def job_value(flops_per_step: float, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank's work over the slowest rank's time."""
+    return flops_per_step * steps * world / max_seconds / 1e12
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "differential_attention_fwd_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source for this workload; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    m_traffic = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_work = re.search(r"workload:\s*(\S+)", text)
+    if not (m_hash and m_traffic and m_work):
+        return None
+    if m_hash.group(1) != kernel_source_hash() or m_work.group(1) != workload:
+        return None
+    return float(m_traffic.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        return self.parse(out)
+
+    @classmethod
+    def parse(cls, text: str):
+        """Median SM clock, max clock and the throttle reasons seen."""
+        rows = []
+        for line in text.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(cls.FIELDS):
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, x in enumerate(r) if x.lower() == "active"})
+        return {"sm_mhz": statistics.median(s for s, _, _ in rows),
+                "sm_max_mhz": max(m for _, m, _ in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+# --------------------------------------------------------------------------
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def oracle_rows_flops(rows, T, D, causal):
+    pairs = sum((int(r) + 1) if causal else T for r in rows)
+    return pairs * 12 * D
+
+
+def time_oracle(inp, w, lam, rows):
+    """Run the oracle on head (0, 0) for `rows`; returns (seconds, flops)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.differential_attention(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, lam, w.causal,
+                                  rows=rows, heads=[(0, 0)])
+    return time.perf_counter() - t0, oracle_rows_flops(rows, w.T, w.D, w.causal)
+
+
+def sample_rows(T, n, seed):
+    """n query rows spread evenly over [0, T) (so causal row costs average
+    out), shifted by a seed-dependent phase so that steps differ."""
+    n = max(1, min(n, T))
+    stride = T // n
+    start = (seed * 7919) % stride if stride > 1 else 0
+    return (start + np.arange(n, dtype=np.int64) * stride).clip(0, T - 1)
+
+
+def cpu_baseline(inp, w, lam, budget_s=15.0):
+    """Time the oracle, as it stands, on a bounded sample of the workload."""
+    t1, _ = time_oracle(inp, w, lam, sample_rows(w.T, 8, 0))
+    per_row = max(t1 / 8, 1e-5)
+    n = int(min(w.T, max(8, budget_s / per_row)))
+    secs, flops = time_oracle(inp, w, lam, sample_rows(w.T, n, 1))
+    return {"value": flops / secs / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"float64 NumPy oracle, head (0,0), {n} query rows spread over T={w.T} "
+                      f"({'causal' if w.causal else 'full'} rows, {flops / 1e9:.2f} GFLOP "
+                      f"algorithmic) in {secs:.1f} s"}
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return None
+    inp = W.draw(w)
+    lam = lambda_for(w, inp)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    t1, _ = time_oracle(inp, w, lam, sample_rows(w.T, 4, 0))
+    rows_per_step = int(max(1, min(w.T, budget / max(t1 / 4, 1e-5))))
+    total_s = 0.0
+    total_flops = 0
+    for step in range(args.warmup + args.steps):
+        rows = sample_rows(w.T, rows_per_step, step)
+        s, f = time_oracle(inp, w, lam, rows)
+        if step >= args.warmup:
+            total_s += s
+            total_flops += f
+    value = total_flops / total_s / 1e12
+    cores = blas_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, lam),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {rows_per_step} query rows of head (0,0) spread over "
+                                   f"T={w.T}, float64 NumPy oracle on the host cores"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def lambda_for(w, inp) -> float:
+    import oracle
+    if w.lambdas:
+        return float(w.lambdas[0])
+    return float(np.float32(oracle.differential_lambda(inp.lq1, inp.lk1, inp.lq2, inp.lk2,
+                                                       W.lambda_init_for(w))))
+
+
+def config_of(w, lam):
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "D": w.D, "Dv": w.Dv,
+            "causal": w.causal, "lambda_init": W.lambda_init_for(w) if not w.lambdas else None,
+            "lambda": lam, "gflop_per_step": w.flops / 1e9,
+            "l2": "flushed between steps (256 MiB write outside the timed events); "
+                  f"inputs {input_bytes(w) / 2**20:.0f} MiB",
+            "parallelism": "replicas"}
+
+
+def input_bytes(w):
+    el = 2 if w.dtype == "bf16" else 4
+    return w.B * w.H * w.T * (4 * w.D + 2 * w.D) * el
+
+
+# --------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------
+def run_ours(args, w, world, rank, local):
+    import torch
+    import differential_attention_fwd_gb300 as da
+    from differential_attention_fwd_gb300 import _lib
+    from differential_attention_fwd_gb300 import build as build_mod
+
+    build_mod.build()
+    lib = _lib.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    inp = W.draw(w)
+    lam_vecs_host = [torch.from_numpy(x) for x in (inp.lq1, inp.lk1, inp.lq2, inp.lk2)]
+    lam_init = W.lambda_init_for(w) if not w.lambdas else 0.0
+    host = [torch.from_numpy(x).to(tdt) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    d_in = [h.to(dev) for h in host]
+    d_lv = [v.to(dev) for v in lam_vecs_host]
+    d_lam = torch.empty((), dtype=torch.float32, device=dev)
+    d_out = torch.empty((w.B, w.H, w.T, w.Dv), dtype=tdt, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    desc = da.make_desc(*d_in, d_out)
+    ptr_in = [ctypes.c_void_p(t.data_ptr()) for t in d_in]
+    ptr_lv = [ctypes.c_void_p(t.data_ptr()) for t in d_lv]
+    p_lam, p_out = ctypes.c_void_p(d_lam.data_ptr()), ctypes.c_void_p(d_out.data_ptr())
+    nlam = int(d_lv[0].numel())
+    kernel = da.select_kernel(*d_in, out=d_out)
+
+    def step():
+        rc = lib.diffattn_lambda(*ptr_lv, nlam, ctypes.c_double(lam_init), p_lam, sh)
+        if rc:
+            raise _lib.DiffattnError(rc, "diffattn_lambda")
+
+    def fwd():
+        rc = lib.diffattn_fwd(ctypes.byref(desc), *ptr_in, ctypes.c_float(0.0), p_lam,
+                              1 if w.causal else 0, p_out, sh)
+        if rc:
+            raise _lib.DiffattnError(rc, "diffattn_fwd")
+
+    if w.lambdas:   # lambda given directly: no lambda kernel in the step
+        d_lam.fill_(float(w.lambdas[0]))
+        launches_per_step = 1
+    else:
+        launches_per_step = 2
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        if launches_per_step == 2:
+            step()
+        fwd()
+    torch.cuda.synchronize()
+    if da.get_device_error() != 0:
+        raise RuntimeError("a kernel wait ran out during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if (args.clocks and rank == 0) else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        if launches_per_step == 2:
+            step()
+        ev[i][1].record(stream)
+        fwd()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    barrier(world)
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    fwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    total_s = sum(step_ms) / 1e3
+    max_s = reduce_max(total_s, world)
+    if da.get_device_error() != 0:
+        raise RuntimeError("a kernel wait ran out during the timed steps")
+
+    value = job_value(w.flops, args.steps, world, max_s)
+    peaks, peak_src = load_peaks()
+    fwd_avg_s = statistics.mean(fwd_ms) / 1e3
+    achieved = w.flops / fwd_avg_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = profiled_traffic(w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+                "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"]),
+                "fwd_ms_median": statistics.median(fwd_ms), "fwd_ms_min": min(fwd_ms),
+                "fwd_ms_max": max(fwd_ms)}
+
+    e2e = None
+    if args.e2e:
+        e2e = run_e2e(args, w, lib, da, _lib, host, lam_vecs_host, lam_init, d_in, d_lv, d_lam,
+                      d_out, desc, launches_per_step, flush, stream, world)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": config_of(w, float(d_lam.item())),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": roofline, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "kernel": {1: "tcgen05", 2: "simt"}.get(kernel, str(kernel)),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(inp, w, float(d_lam.item()), args.cpu_budget)
+    return result
+
+
+def run_e2e(args, w, lib, da, _lib, host, lam_vecs_host, lam_init, d_in, d_lv, d_lam, d_out,
+            desc, launches_per_step, flush, stream, world):
+    """Same metric, inputs from pinned host memory, output back to the host."""
+    import torch
+    pin = [h.pin_memory() for h in host]
+    pin_lv = [v.pin_memory() for v in lam_vecs_host]
+    out_host = torch.empty(d_out.shape, dtype=d_out.dtype).pin_memory()
+    steps = max(1, min(args.steps, args.e2e_steps))
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    if launches_per_step == 2:
+        h2d += sum(t.numel() * t.element_size() for t in pin_lv)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for d, h in zip(d_in, pin):
+            d.copy_(h, non_blocking=True)
+        if launches_per_step == 2:
+            for d, h in zip(d_lv, pin_lv):
+                d.copy_(h, non_blocking=True)
+            lib.diffattn_lambda(*[ctypes.c_void_p(t.data_ptr()) for t in d_lv], int(d_lv[0].numel()),
+                                ctypes.c_double(lam_init), ctypes.c_void_p(d_lam.data_ptr()),
+                                ctypes.c_void_p(stream.cuda_stream))
+        rc = lib.diffattn_fwd(ctypes.byref(desc), *[ctypes.c_void_p(t.data_ptr()) for t in d_in],
+                              ctypes.c_float(0.0), ctypes.c_void_p(d_lam.data_ptr()),
+                              1 if w.causal else 0, ctypes.c_void_p(d_out.data_ptr()),
+                              ctypes.c_void_p(stream.cuda_stream))
+        if rc:
+            raise _lib.DiffattnError(rc, "diffattn_fwd")
+        out_host.copy_(d_out, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    barrier(world)
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        one()
+        b.record(stream)
+    torch.cuda.synchronize()
+    secs = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    max_s = reduce_max(secs, world)
+    return {"value": job_value(w.flops, steps, world, max_s), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": 1e3 * max_s / steps}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("at least 3 warm-up steps")
+
+    world, rank, local = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        res = run_reference(args, w, world, rank)
+    else:
+        res = run_ours(args, w, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -15,11 +15,15 @@
 // reading the same V tile from shared memory.  The epilogue writes
 // O_1 / l_1 - lambda O_2 / l_2.
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads = 3 warpgroups):
 //   warps 0-3  softmax + epilogue, branch 1 (TMEM lanes 0-127)
 //   warps 4-7  softmax + epilogue, branch 2
 //   warp  8    TMA producer
 //   warp  9    TMEM allocation and MMA issue
+//   warps 10-11 idle (they complete the third warpgroup)
+// Registers: launched at 168 per thread (384 x 168 = 64512); the third
+// warpgroup gives registers back (104 per thread) and the two softmax
+// warpgroups take them (200 per thread): 256 x 200 + 128 x 104 = 64512.
 // TMEM columns: S1 [0,128)  S2 [128,256)  O1 [256,384)  O2 [384,512).
 //
 // Causal masking (both branches): KV tiles above the diagonal are never
@@ -43,7 +47,10 @@ constexpr int HD = 64;             // Q/K width D
 constexpr int VD = 128;            // V/O width 2D
 constexpr int KSTAGES = 3;         // (K1, K2) ring depth
 constexpr int VSTAGES = 2;         // V ring depth
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;
+constexpr uint32_t REGS_SOFTMAX = 200;
+constexpr uint32_t REGS_OTHER = 104;
+static_assert(256 * REGS_SOFTMAX + 128 * REGS_OTHER <= NUM_THREADS * 168, "register split");
 
 constexpr uint32_t Q_BYTES = BM * HD * 2;        // 16 KB per branch
 constexpr uint32_t K_BYTES = BN * HD * 2;        // 16 KB per branch
@@ -157,7 +164,9 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
     const int grid = gridDim.x;
     const int cta = blockIdx.x;
 
-    if (warp == 8) {
+    if (warp >= 8) {
+      regs_dec<REGS_OTHER>();
+      if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (elect_one()) {
             tma_prefetch_desc(&tm_q1);
@@ -302,7 +311,9 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             mbar_wait_teardown(&bars[BAR_FINAL], 0, 200ull * 1000ull * 1000ull);
         }
         __syncwarp();
+      }
     } else {
+        regs_inc<REGS_SOFTMAX>();
         // ------------------------------------------------- softmax + epilogue
         const int br = warp >> 2;            // branch
         const uint32_t quad = warp & 3;      // TMEM lane quadrant
@@ -350,48 +361,60 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 }
                 float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-                for (int c = 4; c < 128; c += 4) {
-                    mx0 = fmaxf(mx0, s[c]);
-                    mx1 = fmaxf(mx1, s[c + 1]);
-                    mx2 = fmaxf(mx2, s[c + 2]);
-                    mx3 = fmaxf(mx3, s[c + 3]);
+                for (int c = 4; c < 128; c += 8) {
+                    mx0 = fmax3(mx0, s[c], s[c + 1]);
+                    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+                    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+                    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
                 }
-                const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                mx0 = fmax3(mx0, mx1, fmaxf(mx2, mx3));
+                const float mxs = mx0 * sl2;
 
+                // Lazy rescale: move the running max only when this tile's
+                // row max exceeds it by more than 2^8 (warp-uniform decision,
+                // the O rescale below is a warp-collective TMEM access).
+                float alpha = 1.0f;
+                bool rescale = false;
                 if (j == 0) {
                     m_run = mxs;
-                } else {
-                    const bool need = mxs > m_run + 8.0f;
-                    if (__any_sync(0xffffffffu, need)) {
-                        const float m_new = fmaxf(m_run, mxs);
-                        const float alpha = ex2_approx(m_run - m_new);
-                        l *= alpha;
-                        m_run = m_new;
-#pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4) {
-                            uint32_t o[32];
-                            tmem_ld32(tO + c4 * 32, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tmem_st32(tO + c4 * 32, o);
-                        }
-                        tmem_wait_st();
-                    }
+                } else if (__any_sync(0xffffffffu, mxs > m_run + 8.0f)) {
+                    const float m_new = fmaxf(m_run, mxs);
+                    alpha = ex2_approx(m_run - m_new);
+                    l *= alpha;
+                    m_run = m_new;
+                    rescale = true;
                 }
-                const float neg = -m_run;
-                float rs0 = 0.f, rs1 = 0.f;
+                // P = 2^(s * scale * log2(e) - m), two columns per packed op.
+                const uint64_t scale2 = f2_pack(sl2, sl2);
+                const uint64_t negm2 = f2_pack(-m_run, -m_run);
+                uint64_t rsum0 = 0, rsum1 = 0;
                 uint32_t pk[64];
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
-                    const float p0 = ex2_approx(fmaf(s[2 * c], sl2, neg));
-                    const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, neg));
-                    rs0 += p0;
-                    rs1 += p1;
+                    const uint64_t x = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), scale2, negm2);
+                    const float p0 = ex2_approx(f2_lo(x));
+                    const float p1 = ex2_approx(f2_hi(x));
+                    const uint64_t pp = f2_pack(p0, p1);
+                    if (c & 1) rsum1 = f2_add(rsum1, pp); else rsum0 = f2_add(rsum0, pp);
                     pk[c] = pack_bf16x2(p0, p1);
                 }
+                const uint64_t rsum = f2_add(rsum0, rsum1);
+                const float rs0 = f2_lo(rsum), rs1 = f2_hi(rsum);
                 tmem_st32(tS + 0, &pk[0]);
                 tmem_st32(tS + 32, &pk[32]);
+                if (rescale) {
+                    // O_b row *= alpha (the previous PV into O_b has completed:
+                    // the commit that signalled this S tile covers it).
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c4 * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + c4 * 32, o);
+                    }
+                }
                 tmem_wait_st();
                 l += rs0 + rs1;
                 tc_fence_before();

@@ -1,0 +1,86 @@
+"""Host logic of bench.py, on the CPU: the whole-job value, the max over
+ranks with two gloo ranks (the N > 1 path), the clock-record parser, the
+oracle sample and the profile-summary lookup."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_job_value_sums_ranks_over_slowest():
+    assert bench.job_value(1e12, 10, 1, 10.0) == pytest.approx(1.0)
+    assert bench.job_value(1e12, 10, 4, 10.0) == pytest.approx(4.0)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    bench.barrier(world)
+    m = bench.reduce_max(1.5 + rank, world)
+    q.put((rank, m))
+    bench.barrier(world)
+    dist.destroy_process_group()
+
+
+def test_reduce_max_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, 2.5), (1, 2.5)]
+
+
+def test_reduce_max_single_rank_is_identity():
+    assert bench.reduce_max(3.25, 1) == 3.25
+
+
+def test_clock_parser():
+    text = ("1965, 2070, 1100.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
+            "1980, 2070, 1200.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n"
+            "garbage line\n"
+            "2010, 2070, 1300.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+    r = bench.ClockSampler.parse(text)
+    assert r["sm_mhz"] == 1980 and r["sm_max_mhz"] == 2070
+    assert r["reasons"] == ["sw_power_cap"] and r["samples"] == 3
+    assert bench.ClockSampler.parse("") is None
+
+
+def test_sample_rows_and_flops():
+    rows = bench.sample_rows(8192, 100, 3)
+    assert rows.size == 100 and rows.min() >= 0 and rows.max() < 8192
+    assert not np.array_equal(rows, bench.sample_rows(8192, 100, 4))
+    assert bench.oracle_rows_flops([0, 9], 16, 64, True) == (1 + 10) * 12 * 64
+    assert bench.oracle_rows_flops([0, 9], 16, 64, False) == 2 * 16 * 12 * 64
+
+
+def test_profiled_traffic_requires_matching_kernel(tmp_path, monkeypatch):
+    f = tmp_path / "p.md"
+    f.write_text(f"workload: b2h16t8192\nkernel_source_sha256: {bench.kernel_source_hash()}\n"
+                 "traffic_bytes_per_launch: 1.5e9\n")
+    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(f))
+    assert bench.profiled_traffic("b2h16t8192") == 1.5e9
+    assert bench.profiled_traffic("b4h16t2048") is None
+    f.write_text("workload: b2h16t8192\nkernel_source_sha256: 0000\ntraffic_bytes_per_launch: 1.5e9\n")
+    assert bench.profiled_traffic("b2h16t8192") is None
+
+
+def test_headline_flops_count():
+    w = bench.W.WORKLOADS["b2h16t8192"]
+    assert w.flops == 2 * 16 * (8192 * 8193 // 2) * 12 * 64
+    assert abs(w.flops / 1e9 - 824.734) < 1e-3
