@@ -101,10 +101,10 @@ int select(const diffattn_desc* d, const void* q1, const void* k1, const void* q
     return DIFFATTN_KERNEL_SIMT;
 }
 
-// 4-D bf16 tensor map {inner, T, H, B} with a {box_inner, 128, 1, 1} box and
-// 128-byte swizzling; rows past T read as zeros.
+// 4-D bf16 tensor map {inner, T, H, B} with a {box_inner, box_rows, 1, 1} box
+// and 128-byte swizzling; rows past T read as zeros.
 int encode_map(CUtensorMap* m, const void* base, int64_t inner, const diffattn_desc* d,
-               const int64_t s[3], uint32_t box_inner) {
+               const int64_t s[3], uint32_t box_inner, uint32_t box_rows) {
     int64_t sT = s[2], sH = s[1], sB = s[0];
     // A size-1 dimension is never stepped; give it a stride the encoder accepts.
     if (d->T == 1) sT = inner;
@@ -113,7 +113,7 @@ int encode_map(CUtensorMap* m, const void* base, int64_t inner, const diffattn_d
     const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)d->T, (cuuint64_t)d->H,
                                 (cuuint64_t)d->B};
     const cuuint64_t strides[3] = {(cuuint64_t)sT * 2, (cuuint64_t)sH * 2, (cuuint64_t)sB * 2};
-    const cuuint32_t box[4] = {box_inner, 128, 1, 1};
+    const cuuint32_t box[4] = {box_inner, box_rows, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -166,18 +166,33 @@ int diffattn_fwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
 
     if (select(desc, q1, k1, q2, k2, v, out) == DIFFATTN_KERNEL_TCGEN05) {
         CUtensorMap maps[5];
-        if (encode_map(&maps[0], q1, 64, &d, d.q1_stride, 64) != DIFFATTN_OK ||
-            encode_map(&maps[1], k1, 64, &d, d.k1_stride, 64) != DIFFATTN_OK ||
-            encode_map(&maps[2], q2, 64, &d, d.q2_stride, 64) != DIFFATTN_OK ||
-            encode_map(&maps[3], k2, 64, &d, d.k2_stride, 64) != DIFFATTN_OK ||
-            encode_map(&maps[4], v, 128, &d, d.v_stride, 64) != DIFFATTN_OK)
+        // Q tiles are 128 query rows; K and V tiles are 64 key rows; every box
+        // is 64 elements (128 bytes) wide, the 128-byte swizzle span.
+        if (encode_map(&maps[0], q1, 64, &d, d.q1_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&maps[1], k1, 64, &d, d.k1_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[2], q2, 64, &d, d.q2_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&maps[3], k2, 64, &d, d.k2_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[4], v, 128, &d, d.v_stride, 64, 64) != DIFFATTN_OK)
             return DIFFATTN_ERR_CUDA;
         TcParams p;
         p.B = (int)d.B;
         p.H = (int)d.H;
         p.T = (int)d.T;
         p.nq = (int)((d.T + 127) / 128);
+        p.nk = (int)((d.T + 63) / 64);
         p.total_items = (int)(d.B * d.H * p.nq);
+        // Heads per scheduling group: their K1, K2 and V (256 bytes per key)
+        // take at most ~24 MiB, a fraction of the 126 MiB L2, but at least one
+        // head and enough items to keep every SM busy.
+        {
+            const int64_t head_bytes = d.T * 256;
+            int64_t g = (24ll << 20) / (head_bytes > 0 ? head_bytes : 1);
+            const int64_t min_g = (dev->num_sms + p.nq - 1) / p.nq;
+            if (g < min_g) g = min_g;
+            if (g < 1) g = 1;
+            if (g > d.B * d.H) g = d.B * d.H;
+            p.group = (int)g;
+        }
         p.causal = causal ? 1 : 0;
         p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.D));
         p.lambda = lambda;

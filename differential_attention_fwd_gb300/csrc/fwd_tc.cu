@@ -7,27 +7,34 @@
 //
 // One CTA per SM (persistent).  A work item is (batch b, head h, 128-query
 // tile).  Per item the CTA loads Q1/Q2 once and streams (K1, K2) and V tiles
-// of 128 keys through TMA rings in shared memory.  Both score products
-// S_b = Q_b K_b^T run as tcgen05 MMAs into tensor memory (TMEM); each branch
-// keeps its own streaming-softmax row state (max and sum) in the registers of
-// its own warpgroup, one query row per thread; the probabilities P_b are
-// written back over S_b in TMEM as bf16 and feed the O_b += P_b V MMAs, both
-// reading the same V tile from shared memory.  The epilogue writes
-// O_1 / l_1 - lambda O_2 / l_2.
+// of 64 keys through TMA rings in shared memory.  Both score products
+// S_b = Q_b K_b^T run as tcgen05 MMAs into tensor memory (TMEM), each branch
+// with two S buffers so that the MMA of tile j+1 overlaps the softmax of tile
+// j.  Each branch keeps its own streaming-softmax row state (max and sum) in
+// the registers of its own warpgroup, one query row per thread; the
+// probabilities P_b are written back over S_b in TMEM as bf16 and feed the
+// O_b += P_b V MMAs, both reading the same V tile from shared memory.  The
+// epilogue writes O_1 / l_1 - lambda O_2 / l_2.
 //
 // Warp roles (384 threads = 3 warpgroups):
-//   warps 0-3  softmax + epilogue, branch 1 (TMEM lanes 0-127)
-//   warps 4-7  softmax + epilogue, branch 2
-//   warp  8    TMA producer
-//   warp  9    TMEM allocation and MMA issue
+//   warps 0-3   softmax + epilogue, branch 1 (TMEM lanes 0-127)
+//   warps 4-7   softmax + epilogue, branch 2
+//   warp  8     TMA producer
+//   warp  9     TMEM allocation and MMA issue
 //   warps 10-11 idle (they complete the third warpgroup)
 // Registers: launched at 168 per thread (384 x 168 = 64512); the third
 // warpgroup gives registers back (104 per thread) and the two softmax
 // warpgroups take them (200 per thread): 256 x 200 + 128 x 104 = 64512.
-// TMEM columns: S1 [0,128)  S2 [128,256)  O1 [256,384)  O2 [384,512).
+// TMEM columns: S1 buffers [0,64) [64,128), S2 buffers [128,192) [192,256),
+// O1 [256,384), O2 [384,512).
+//
+// Tensor-core order per branch b (one issuing thread, executed in order):
+//   S_b(0), S_b(1), then for each tile j: PV_b(j), S_b(j+2) into the buffer
+//   PV_b(j) has just read P_b(j) from.
 //
 // Causal masking (both branches): KV tiles above the diagonal are never
-// loaded; the diagonal tile masks key > query with -inf before the row max.
+// loaded; tiles that cross the diagonal mask key > query with -inf before the
+// row max.
 //
 // Streaming softmax: the running max m is kept in log2 units of the scaled
 // scores.  O and l are rescaled only when a tile's row max exceeds m by more
@@ -42,20 +49,20 @@ namespace diffattn {
 namespace tc {
 
 constexpr int BM = 128;            // query rows per tile (= TMEM lanes)
-constexpr int BN = 128;            // keys per KV tile
+constexpr int BN = 64;             // keys per KV tile
 constexpr int HD = 64;             // Q/K width D
 constexpr int VD = 128;            // V/O width 2D
-constexpr int KSTAGES = 3;         // (K1, K2) ring depth
-constexpr int VSTAGES = 2;         // V ring depth
+constexpr int KSTAGES = 5;         // (K1, K2) ring depth
+constexpr int VSTAGES = 5;         // V ring depth
 constexpr int NUM_THREADS = 384;
 constexpr uint32_t REGS_SOFTMAX = 200;
 constexpr uint32_t REGS_OTHER = 104;
 static_assert(256 * REGS_SOFTMAX + 128 * REGS_OTHER <= NUM_THREADS * 168, "register split");
 
 constexpr uint32_t Q_BYTES = BM * HD * 2;        // 16 KB per branch
-constexpr uint32_t K_BYTES = BN * HD * 2;        // 16 KB per branch
-constexpr uint32_t V_HALF_BYTES = BN * 64 * 2;   // 16 KB per 64-column half
-constexpr uint32_t V_BYTES = 2 * V_HALF_BYTES;   // 32 KB
+constexpr uint32_t K_BYTES = BN * HD * 2;        // 8 KB per branch
+constexpr uint32_t V_HALF_BYTES = BN * 64 * 2;   // 8 KB per 64-column half
+constexpr uint32_t V_BYTES = 2 * V_HALF_BYTES;   // 16 KB
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 constexpr uint32_t OFF_Q1 = 0;
@@ -70,9 +77,10 @@ constexpr int BAR_K_FULL = 2;
 constexpr int BAR_K_EMPTY = BAR_K_FULL + KSTAGES;
 constexpr int BAR_V_FULL = BAR_K_EMPTY + KSTAGES;
 constexpr int BAR_V_EMPTY = BAR_V_FULL + VSTAGES;
-constexpr int BAR_S_FULL = BAR_V_EMPTY + VSTAGES;      // [2]
-constexpr int BAR_P_FULL = BAR_S_FULL + 2;             // [2]
-constexpr int BAR_O_FULL = BAR_P_FULL + 2;
+constexpr int BAR_S_FULL = BAR_V_EMPTY + VSTAGES;      // [branch][buffer]
+constexpr int BAR_P_FULL = BAR_S_FULL + 4;             // [branch][buffer]
+constexpr int BAR_PV_DONE = BAR_P_FULL + 4;            // [branch]
+constexpr int BAR_O_FULL = BAR_PV_DONE + 2;
 constexpr int BAR_O_EMPTY = BAR_O_FULL + 1;
 constexpr int BAR_L_READY = BAR_O_EMPTY + 1;           // 1/l of both branches in smem
 constexpr int BAR_FINAL = BAR_L_READY + 1;
@@ -86,8 +94,11 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;               // + alignment s
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_O = 256;                                   // O1 at 256, O2 at 384
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);   // Q (K-major) x K^T (K-major)
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, VD, 0, 1);  // P (TMEM) x V (MN-major)
+
+__device__ __forceinline__ uint32_t tm_s(int br, int buf) { return br * 128 + buf * 64; }
 
 struct Item {
     int qt, b, h, n_kv;
@@ -100,15 +111,26 @@ __device__ __forceinline__ int item_index(int k, int cta, int grid) {
     return base + ((k & 1) ? (grid - 1 - cta) : cta);
 }
 
+// Item list: heads are taken in groups of p.group heads (a group's K1/K2/V
+// fits comfortably in L2, so the CTAs working at the same time share it);
+// within a group, items run longest first (causal: last query tile first),
+// then head by head.
 __device__ __forceinline__ Item decode_item(int idx, const TcParams& p) {
     const int BH = p.B * p.H;
-    const int r = idx / BH;
-    const int bh = idx - r * BH;
+    const int per_group = p.group * p.nq;
+    const int g = idx / per_group;
+    const int g0 = g * p.group;
+    const int gsize = min(p.group, BH - g0);
+    const int w = idx - g * per_group;
+    const int r = w / gsize;
+    const int bh = g0 + (w - r * gsize);
     Item it;
     it.qt = p.causal ? (p.nq - 1 - r) : r;
     it.b = bh / p.H;
     it.h = bh - it.b * p.H;
-    it.n_kv = p.causal ? (it.qt + 1) : p.nq;
+    // 64-key tiles: all of them, or (causal) those holding a key <= the
+    // tile's last query.
+    it.n_kv = p.causal ? min(2 * it.qt + 2, p.nk) : p.nk;
     return it;
 }
 
@@ -141,10 +163,12 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             mbar_init(&bars[BAR_V_FULL + s], 1);
             mbar_init(&bars[BAR_V_EMPTY + s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars[BAR_S_FULL + b], 1);
-            mbar_init(&bars[BAR_P_FULL + b], 4);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&bars[BAR_S_FULL + i], 1);
+            mbar_init(&bars[BAR_P_FULL + i], 4);
         }
+        mbar_init(&bars[BAR_PV_DONE + 0], 1);
+        mbar_init(&bars[BAR_PV_DONE + 1], 1);
         mbar_init(&bars[BAR_O_FULL], 1);
         mbar_init(&bars[BAR_O_EMPTY], 8);
         mbar_init(&bars[BAR_L_READY], 8);
@@ -220,18 +244,18 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 if (armed_v[s]) mbar_wait_teardown(&bars[BAR_V_FULL + s], (armed_v[s] - 1) & 1, lim);
         }
         __syncwarp();
-    } else if (warp == 9) {
+      } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issue
         if (elect_one()) {
             const uint32_t sq[2] = {smem_u32(smem + OFF_Q1), smem_u32(smem + OFF_Q2)};
             const uint32_t sk0 = smem_u32(smem + OFF_K);
             const uint32_t sv0 = smem_u32(smem + OFF_V);
             uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0, oeph = 0;
-            uint32_t pph[2] = {0, 0};
+            uint32_t pph = 0;     // bit (2*branch + buffer): phase of P_FULL[branch][buffer]
             bool ok = true;
 
-            auto issue_s = [&](int br, uint32_t stage) {
-                const uint32_t d = tmem_base + br * 128;
+            auto issue_s = [&](int br, uint32_t stage, int buf) {
+                const uint32_t d = tmem_base + tm_s(br, buf);
                 const uint32_t qa = sq[br];
                 const uint32_t ka = sk0 + stage * 2 * K_BYTES + br * K_BYTES;
 #pragma unroll
@@ -240,15 +264,21 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                            IDESC_S, kk > 0);
                 }
             };
-            auto issue_pv = [&](int br, uint32_t stage, bool acc) {
-                const uint32_t d = tmem_base + 256 + br * 128;
-                const uint32_t pa = tmem_base + br * 128;
+            auto issue_pv = [&](int br, uint32_t stage, int buf, bool acc) {
+                const uint32_t d = tmem_base + TM_O + br * 128;
+                const uint32_t pa = tmem_base + tm_s(br, buf);
                 const uint32_t va = sv0 + stage * V_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     mma_ts(d, pa + kk * 8, sdesc_sw128(va + kk * 2048, V_HALF_BYTES, 1024), IDESC_PV,
                            (acc || kk > 0) ? 1u : 0u);
                 }
+            };
+            auto wait_p = [&](int br, int buf) {
+                const uint32_t bit = 1u << (2 * br + buf);
+                const bool r = mbar_wait(&bars[BAR_P_FULL + 2 * br + buf], (pph & bit) ? 1u : 0u, ab);
+                pph ^= bit;
+                return r;
             };
 
             bool first = true;
@@ -257,49 +287,55 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 const int idx = item_index(k, cta, grid);
                 if (idx >= p.total_items) continue;
                 const Item it = decode_item(idx, p);
+                const int n = it.n_kv;
                 if (!(ok = mbar_wait(&bars[BAR_Q_FULL], qph, ab))) break;
                 qph ^= 1;
-                if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
-                tc_fence_after();
-                issue_s(0, kst);
-                mma_commit(&bars[BAR_S_FULL + 0]);
-                issue_s(1, kst);
-                mma_commit(&bars[BAR_S_FULL + 1]);
-                mma_commit(&bars[BAR_K_EMPTY + kst]);
-                if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
-                if (it.n_kv == 1) mma_commit(&bars[BAR_Q_EMPTY]);
+                // S(0) and S(1) of both branches into buffers 0 and 1
+                for (int t = 0; t < 2 && t < n; ++t) {
+                    if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
+                    tc_fence_after();
+                    issue_s(0, kst, t);
+                    mma_commit(&bars[BAR_S_FULL + 0 + t]);
+                    issue_s(1, kst, t);
+                    mma_commit(&bars[BAR_S_FULL + 2 + t]);
+                    mma_commit(&bars[BAR_K_EMPTY + kst]);
+                    if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
+                }
+                if (!ok) break;
+                if (n <= 2) mma_commit(&bars[BAR_Q_EMPTY]);
 
-                for (int j = 0; j < it.n_kv; ++j) {
-                    // branch 1: O1 += P1 V(j), then S1(j+1)
-                    if (!(ok = mbar_wait(&bars[BAR_P_FULL + 0], pph[0], ab))) break;
-                    pph[0] ^= 1;
+                for (int j = 0; j < n; ++j) {
+                    const int buf = j & 1;
+                    const bool more = (j + 2 < n);
+                    // branch 1: O1 += P1(j) V(j), then S1(j+2) into the freed buffer
+                    if (!(ok = wait_p(0, buf))) break;
                     if (j == 0 && !first) {
                         if (!(ok = mbar_wait(&bars[BAR_O_EMPTY], oeph, ab))) break;
                         oeph ^= 1;
                     }
                     if (!(ok = mbar_wait(&bars[BAR_V_FULL + vst], vph, ab))) break;
                     tc_fence_after();
-                    issue_pv(0, vst, j > 0);
-                    const bool more = (j + 1 < it.n_kv);
+                    issue_pv(0, vst, buf, j > 0);
+                    mma_commit(&bars[BAR_PV_DONE + 0]);
                     if (more) {
                         if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
                         tc_fence_after();
-                        issue_s(0, kst);
-                        mma_commit(&bars[BAR_S_FULL + 0]);
+                        issue_s(0, kst, buf);
+                        mma_commit(&bars[BAR_S_FULL + 0 + buf]);
                     }
-                    // branch 2: O2 += P2 V(j), then S2(j+1)
-                    if (!(ok = mbar_wait(&bars[BAR_P_FULL + 1], pph[1], ab))) break;
-                    pph[1] ^= 1;
+                    // branch 2: O2 += P2(j) V(j), then S2(j+2)
+                    if (!(ok = wait_p(1, buf))) break;
                     tc_fence_after();
-                    issue_pv(1, vst, j > 0);
+                    issue_pv(1, vst, buf, j > 0);
+                    mma_commit(&bars[BAR_PV_DONE + 1]);
                     mma_commit(&bars[BAR_V_EMPTY + vst]);
                     if (++vst == VSTAGES) { vst = 0; vph ^= 1; }
                     if (more) {
-                        issue_s(1, kst);
-                        mma_commit(&bars[BAR_S_FULL + 1]);
+                        issue_s(1, kst, buf);
+                        mma_commit(&bars[BAR_S_FULL + 2 + buf]);
                         mma_commit(&bars[BAR_K_EMPTY + kst]);
                         if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
-                        if (j + 2 == it.n_kv) mma_commit(&bars[BAR_Q_EMPTY]);
+                        if (j + 3 == n) mma_commit(&bars[BAR_Q_EMPTY]);
                     }
                 }
                 if (!ok) break;
@@ -319,11 +355,12 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
         const uint32_t quad = warp & 3;      // TMEM lane quadrant
         const int row = quad * 32 + lane;    // query row within the tile
         const uint32_t lane_base = tmem_base + ((quad * 32u) << 16);
-        const uint32_t tS = lane_base + br * 128;
-        const uint32_t tO = lane_base + 256 + br * 128;
+        const uint32_t tO = lane_base + TM_O + br * 128;
         const float sl2 = p.scale_log2;
         const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
-        uint32_t sph = 0, ofph = 0, lph = 0;
+        uint32_t sph = 0;          // bit buf: phase of S_FULL[br][buf]
+        uint32_t ofph = 0, lph = 0;
+        uint32_t pv_count = 0;     // PV_b products issued for earlier items
         bool ok = true;
 
         for (int k = 0; ok; ++k) {
@@ -336,32 +373,34 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             float l = 0.f;
 
             for (int j = 0; j < it.n_kv; ++j) {
-                if (!(ok = mbar_wait_warp(&bars[BAR_S_FULL + br], sph, ab))) break;
-                sph ^= 1;
+                const int buf = j & 1;
+                const uint32_t tS = lane_base + tm_s(br, buf);
+                if (!(ok = mbar_wait_warp(&bars[BAR_S_FULL + 2 * br + buf], (sph >> buf) & 1u, ab))) break;
+                sph ^= 1u << buf;
                 tc_fence_after();
-                uint32_t u[128];
+                uint32_t u[64];
                 tmem_ld32(tS + 0, &u[0]);
                 tmem_ld32(tS + 32, &u[32]);
-                tmem_ld32(tS + 64, &u[64]);
-                tmem_ld32(tS + 96, &u[96]);
                 tmem_wait_ld();
-                float s[128];
+                float s[64];
 #pragma unroll
-                for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
+                for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(u[c]);
 
                 const int kv0 = j * BN;
-                if (p.causal && j == it.n_kv - 1) {
-                    const int lim = q - kv0;           // keys kv0 + c with c > lim are in the future
+                if (p.causal) {
+                    if (kv0 + BN - 1 > it.qt * BM) {     // the tile crosses the diagonal
+                        const int lim = q - kv0;          // keys kv0 + c with c > lim are in the future
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) s[c] = (c > lim) ? -INFINITY : s[c];
-                } else if (!p.causal && kv0 + BN > p.T) {
-                    const int lim = p.T - kv0;         // keys at or beyond T do not exist
+                        for (int c = 0; c < 64; ++c) s[c] = (c > lim) ? -INFINITY : s[c];
+                    }
+                } else if (kv0 + BN > p.T) {
+                    const int lim = p.T - kv0;            // keys at or beyond T do not exist
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) s[c] = (c >= lim) ? -INFINITY : s[c];
+                    for (int c = 0; c < 64; ++c) s[c] = (c >= lim) ? -INFINITY : s[c];
                 }
                 float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-                for (int c = 4; c < 128; c += 8) {
+                for (int c = 4; c < 64; c += 8) {
                     mx0 = fmax3(mx0, s[c], s[c + 1]);
                     mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
                     mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
@@ -388,9 +427,9 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 const uint64_t scale2 = f2_pack(sl2, sl2);
                 const uint64_t negm2 = f2_pack(-m_run, -m_run);
                 uint64_t rsum0 = 0, rsum1 = 0;
-                uint32_t pk[64];
+                uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < 32; ++c) {
                     const uint64_t x = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), scale2, negm2);
                     const float p0 = ex2_approx(f2_lo(x));
                     const float p1 = ex2_approx(f2_hi(x));
@@ -399,12 +438,12 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     pk[c] = pack_bf16x2(p0, p1);
                 }
                 const uint64_t rsum = f2_add(rsum0, rsum1);
-                const float rs0 = f2_lo(rsum), rs1 = f2_hi(rsum);
-                tmem_st32(tS + 0, &pk[0]);
-                tmem_st32(tS + 32, &pk[32]);
+                tmem_st32(tS, &pk[0]);
                 if (rescale) {
-                    // O_b row *= alpha (the previous PV into O_b has completed:
-                    // the commit that signalled this S tile covers it).
+                    // O_b row *= alpha, once PV_b(j-1) has completed (S_b(j)
+                    // completing already implies PV_b(j-2) has).
+                    if (!(ok = mbar_wait_warp(&bars[BAR_PV_DONE + br], (pv_count + j - 1) & 1u, ab))) break;
+                    tc_fence_after();
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) {
                         uint32_t o[32];
@@ -416,57 +455,59 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     }
                 }
                 tmem_wait_st();
-                l += rs0 + rs1;
+                l += f2_lo(rsum) + f2_hi(rsum);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[BAR_P_FULL + br]);
+                if (lane == 0) mbar_arrive(&bars[BAR_P_FULL + 2 * br + buf]);
             }
             if (!ok) break;
+            pv_count += it.n_kv;
 
             // ---------------------------------------------------- epilogue
             if (!(ok = mbar_wait_warp(&bars[BAR_O_FULL], ofph, ab))) break;
             ofph ^= 1;
             tc_fence_after();
             inv_l[br * BM + row] = 1.0f / l;
+            const int c0 = br * 64;          // this warpgroup writes output columns [c0, c0+64)
+            uint32_t o1[64], o2[64];
+            tmem_ld32(lane_base + TM_O + c0, &o1[0]);
+            tmem_ld32(lane_base + TM_O + c0 + 32, &o1[32]);
+            tmem_ld32(lane_base + TM_O + 128 + c0, &o2[0]);
+            tmem_ld32(lane_base + TM_O + 128 + c0 + 32, &o2[32]);
+            tmem_wait_ld();
+            // O is in registers: the next item's PV may overwrite TMEM.
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[BAR_L_READY]);
+            if (lane == 0) {
+                mbar_arrive(&bars[BAR_O_EMPTY]);
+                mbar_arrive(&bars[BAR_L_READY]);
+            }
             if (!(ok = mbar_wait_warp(&bars[BAR_L_READY], lph, ab))) break;
             lph ^= 1;
             const float inv1 = inv_l[row];
             const float inv2 = inv_l[BM + row];
-            const int c0 = br * 64;          // this warpgroup writes output columns [c0, c0+64)
-            const bool valid = q < p.T;
-            __nv_bfloat16* orow = p.out + (int64_t)it.b * p.o_sB + (int64_t)it.h * p.o_sH +
-                                  (int64_t)q * p.o_sT + c0;
+            if (q < p.T) {
+                __nv_bfloat16* orow = p.out + (int64_t)it.b * p.o_sB + (int64_t)it.h * p.o_sH +
+                                      (int64_t)q * p.o_sT + c0;
+                uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t o1[32], o2[32];
-                tmem_ld32(lane_base + 256 + c0 + half * 32, o1);
-                tmem_ld32(lane_base + 384 + c0 + half * 32, o2);
-                tmem_wait_ld();
-                uint32_t packed[16];
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t w4[4];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float r[2];
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 8 * i + 2 * e;
+                        float r[2];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float a = __fmul_rn(__uint_as_float(o1[2 * i + e]), inv1);
-                        const float bb = __fmul_rn(__uint_as_float(o2[2 * i + e]), inv2);
-                        r[e] = __fsub_rn(a, __fmul_rn(lam, bb));
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const float a = __fmul_rn(__uint_as_float(o1[c + h2]), inv1);
+                            const float bb = __fmul_rn(__uint_as_float(o2[c + h2]), inv2);
+                            r[h2] = __fsub_rn(a, __fmul_rn(lam, bb));
+                        }
+                        w4[e] = pack_bf16x2(r[0], r[1]);
                     }
-                    packed[i] = pack_bf16x2(r[0], r[1]);
-                }
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + half * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                            packed[4 * i + 3]);
+                    dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[BAR_O_EMPTY]);
         }
     }
 

@@ -12,8 +12,10 @@ namespace diffattn {
 // Parameters of the tensor-core kernel (bf16, D = 64).
 struct TcParams {
     int B, H, T;
-    int nq;                 // number of 128-row tiles along T
+    int nq;                 // number of 128-row query tiles along T
+    int nk;                 // number of 64-row key tiles along T
     int total_items;        // B * H * nq
+    int group;              // heads per scheduling group (L2 locality)
     int causal;
     float scale_log2;       // log2(e) / sqrt(D)
     float lambda;           // used when lambda_dev == nullptr
