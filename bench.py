@@ -304,6 +304,8 @@ def run_ours(args, w, world, rank, local):
     p_lam, p_out = ctypes.c_void_p(d_lam.data_ptr()), ctypes.c_void_p(d_out.data_ptr())
     nlam = int(d_lv[0].numel())
     kernel = da.select_kernel(*d_in, out=d_out)
+    ws = da.workspace_for(dev, stream)
+    p_ws, ws_bytes = ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel() * 4)
 
     def step():
         rc = lib.diffattn_lambda(*ptr_lv, nlam, ctypes.c_double(lam_init), p_lam, sh)
@@ -312,7 +314,7 @@ def run_ours(args, w, world, rank, local):
 
     def fwd():
         rc = lib.diffattn_fwd(ctypes.byref(desc), *ptr_in, ctypes.c_float(0.0), p_lam,
-                              1 if w.causal else 0, p_out, sh)
+                              1 if w.causal else 0, p_out, p_ws, ws_bytes, sh)
         if rc:
             raise _lib.DiffattnError(rc, "diffattn_fwd")
 
@@ -372,7 +374,7 @@ def run_ours(args, w, world, rank, local):
     e2e = None
     if args.e2e:
         e2e = run_e2e(args, w, lib, da, _lib, host, lam_vecs_host, lam_init, d_in, d_lv, d_lam,
-                      d_out, desc, launches_per_step, flush, stream, world)
+                      d_out, desc, launches_per_step, flush, stream, world, ws)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -391,7 +393,7 @@ def run_ours(args, w, world, rank, local):
 
 
 def run_e2e(args, w, lib, da, _lib, host, lam_vecs_host, lam_init, d_in, d_lv, d_lam, d_out,
-            desc, launches_per_step, flush, stream, world):
+            desc, launches_per_step, flush, stream, world, ws):
     """Same metric, inputs from pinned host memory, output back to the host."""
     import torch
     pin = [h.pin_memory() for h in host]
@@ -415,6 +417,7 @@ def run_e2e(args, w, lib, da, _lib, host, lam_vecs_host, lam_init, d_in, d_lv, d
         rc = lib.diffattn_fwd(ctypes.byref(desc), *[ctypes.c_void_p(t.data_ptr()) for t in d_in],
                               ctypes.c_float(0.0), ctypes.c_void_p(d_lam.data_ptr()),
                               1 if w.causal else 0, ctypes.c_void_p(d_out.data_ptr()),
+                              ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel() * 4),
                               ctypes.c_void_p(stream.cuda_stream))
         if rc:
             raise _lib.DiffattnError(rc, "diffattn_fwd")

@@ -34,6 +34,21 @@ def _stream_handle(device: torch.device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+_WORKSPACES = {}
+
+
+def workspace_for(device: torch.device, stream) -> torch.Tensor:
+    """The scheduler workspace for (device, stream): zero-filled once, left
+    zeroed by every call, one per stream so concurrent streams never share."""
+    key = (device.index, int(stream.cuda_stream))
+    ws = _WORKSPACES.get(key)
+    if ws is None:
+        nbytes = int(_lib.load().diffattn_workspace_bytes())
+        ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=device)
+        _WORKSPACES[key] = ws
+    return ws
+
+
 def _require_cuda(t: torch.Tensor, name: str) -> None:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -129,7 +144,8 @@ def select_kernel(q1, k1, q2, k2, value, out=None) -> int:
 
 def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor, k2: torch.Tensor,
                            value: torch.Tensor, coefficient, causal: bool = True,
-                           out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                           out: Optional[torch.Tensor] = None,
+                           dynamic_schedule: bool = True) -> torch.Tensor:
     """O = (softmax(Q1 K1^T/sqrt(D) + M) - lambda softmax(Q2 K2^T/sqrt(D) + M)) V.
 
     q1, k1, q2, k2: [B, H, T, D]; value: [B, H, T, 2D]; all bfloat16 or all
@@ -137,8 +153,10 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
     are passed through).  coefficient: lambda, a Python number or a scalar
     tensor (a CUDA float32 scalar is read by the kernel without a host sync).
     causal: mask key j > query i in both branches.  out: optional preallocated
-    [B, H, T, 2D] output of the same dtype.  Returns the [B, H, T, 2D] output;
-    the launch is asynchronous on the current CUDA stream.  (Forward only.)
+    [B, H, T, 2D] output of the same dtype.  dynamic_schedule: hand out work
+    items at run time through a small per-stream workspace (the result is
+    the same either way).  Returns the [B, H, T, 2D] output; the launch is
+    asynchronous on the current CUDA stream.  (Forward only.)
     """
     (q1, k1, q2, k2, value), dev = _prepare(q1, k1, q2, k2, value)
     B, H, T, D = q1.shape
@@ -168,12 +186,16 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
     d = make_desc(q1, k1, q2, k2, value, out)
     lib = _lib.load()
     with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev)
+        ws = workspace_for(dev, stream) if dynamic_schedule else None
         rc = lib.diffattn_fwd(ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in
                                                   (q1, k1, q2, k2, value)),
                               ctypes.c_float(lam_host),
                               ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0),
                               1 if causal else 0, ctypes.c_void_p(out.data_ptr()),
-                              _stream_handle(dev))
+                              ctypes.c_void_p(ws.data_ptr() if ws is not None else 0),
+                              ctypes.c_size_t(ws.numel() * 4 if ws is not None else 0),
+                              ctypes.c_void_p(stream.cuda_stream))
     _lib.check(rc, "diffattn_fwd")
     return out
 

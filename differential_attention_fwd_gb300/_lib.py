@@ -23,6 +23,7 @@ DIFFATTN_KERNEL_SIMT = 2
 EXPORTED = (
     "diffattn_lambda",
     "diffattn_fwd",
+    "diffattn_workspace_bytes",
     "diffattn_select_kernel",
     "diffattn_get_device_error",
     "diffattn_strerror",
@@ -64,7 +65,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_lambda.argtypes = [vp, vp, vp, vp, i64, ctypes.c_double, vp, vp]
     lib.diffattn_lambda.restype = ctypes.c_int
     lib.diffattn_fwd.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, ctypes.c_float,
-                                 vp, ctypes.c_int, vp, vp]
+                                 vp, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]
+    lib.diffattn_workspace_bytes.argtypes = []
+    lib.diffattn_workspace_bytes.restype = ctypes.c_size_t
     lib.diffattn_fwd.restype = ctypes.c_int
     lib.diffattn_select_kernel.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, vp]
     lib.diffattn_select_kernel.restype = ctypes.c_int

@@ -16,6 +16,9 @@ __device__ uint32_t g_status_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
+// Scheduler workspace: an item counter and a finished-CTA counter (2 words),
+// rounded up to leave room.
+constexpr size_t kWorkspaceBytes = 64;
 
 struct DeviceState {
     bool ready = false;
@@ -152,12 +155,18 @@ int diffattn_select_kernel(const diffattn_desc* desc, const void* q1, const void
     return select(desc, q1, k1, q2, k2, v, out);
 }
 
+size_t diffattn_workspace_bytes(void) { return kWorkspaceBytes; }
+
 int diffattn_fwd(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
                  const void* k2, const void* v, float lambda, const float* lambda_dev,
-                 int causal, void* out, diffattn_stream_t stream) {
+                 int causal, void* out, void* workspace, size_t workspace_bytes,
+                 diffattn_stream_t stream) {
     int rc = validate(desc, q1, k1, q2, k2, v, out);
     if (rc != DIFFATTN_OK) return rc;
     if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
+    if (workspace && (workspace_bytes < kWorkspaceBytes ||
+                      (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0))
+        return DIFFATTN_ERR_INVALID;
     const diffattn_desc& d = *desc;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     DeviceState* dev = nullptr;
@@ -181,10 +190,15 @@ int diffattn_fwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
         p.nq = (int)((d.T + 127) / 128);
         p.nk = (int)((d.T + 63) / 64);
         p.total_items = (int)(d.B * d.H * p.nq);
-        // Heads per scheduling group: their K1, K2 and V (256 bytes per key)
-        // take at most ~24 MiB, a fraction of the 126 MiB L2, but at least one
-        // head and enough items to keep every SM busy.
-        {
+        // Heads per scheduling group.  Causal items have unequal lengths and
+        // are balanced across CTAs by running them longest first over all
+        // heads (one group).  Non-causal items are all equally long, so heads
+        // are grouped for L2 locality: a group's K1, K2 and V (256 bytes per
+        // key) take at most ~24 MiB of the 126 MiB L2, with enough items to
+        // keep every SM busy.
+        if (causal) {
+            p.group = (int)(d.B * d.H);
+        } else {
             const int64_t head_bytes = d.T * 256;
             int64_t g = (24ll << 20) / (head_bytes > 0 ? head_bytes : 1);
             const int64_t min_g = (dev->num_sms + p.nq - 1) / p.nq;
@@ -202,6 +216,7 @@ int diffattn_fwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
         p.o_sH = d.o_stride[1];
         p.o_sT = d.o_stride[2];
         p.status = dev->status;
+        p.sched = static_cast<uint32_t*>(workspace);
         const int grid = p.total_items < dev->num_sms ? p.total_items : dev->num_sms;
         return launch_fwd_tc(maps, p, grid, st) == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
     }

@@ -20,17 +20,21 @@
 //   warps 0-3   softmax + epilogue, branch 1 (TMEM lanes 0-127)
 //   warps 4-7   softmax + epilogue, branch 2
 //   warp  8     TMA producer
-//   warp  9     TMEM allocation and MMA issue
-//   warps 10-11 idle (they complete the third warpgroup)
+//   warp  9     TMEM allocation; MMA issue for branch 1
+//   warp  10    MMA issue for branch 2
+//   warp  11    idle (it completes the third warpgroup)
+// One MMA-issuing thread per branch, so each branch's PV and next score
+// product go to the tensor core as soon as that branch's P is ready.
 // Registers: launched at 168 per thread (384 x 168 = 64512); the third
 // warpgroup gives registers back (104 per thread) and the two softmax
 // warpgroups take them (200 per thread): 256 x 200 + 128 x 104 = 64512.
 // TMEM columns: S1 buffers [0,64) [64,128), S2 buffers [128,192) [192,256),
 // O1 [256,384), O2 [384,512).
 //
-// Tensor-core order per branch b (one issuing thread, executed in order):
+// Tensor-core order per branch b (its own issuing thread, executed in order):
 //   S_b(0), S_b(1), then for each tile j: PV_b(j), S_b(j+2) into the buffer
-//   PV_b(j) has just read P_b(j) from.
+//   PV_b(j) has just read P_b(j) from.  Shared resources (a K or V stage, the
+//   Q tile, O) are released when both branches' commits have arrived.
 //
 // Causal masking (both branches): KV tiles above the diagonal are never
 // loaded; tiles that cross the diagonal mask key > query with -inf before the
@@ -83,12 +87,17 @@ constexpr int BAR_PV_DONE = BAR_P_FULL + 4;            // [branch]
 constexpr int BAR_O_FULL = BAR_PV_DONE + 2;
 constexpr int BAR_O_EMPTY = BAR_O_FULL + 1;
 constexpr int BAR_L_READY = BAR_O_EMPTY + 1;           // 1/l of both branches in smem
-constexpr int BAR_FINAL = BAR_L_READY + 1;
-constexpr int NUM_BARS = BAR_FINAL + 1;
+constexpr int BAR_FINAL = BAR_L_READY + 1;              // [branch]
+constexpr int ITEM_RING = 8;                            // published work items in flight
+constexpr int BAR_ITEM_FULL = BAR_FINAL + 2;            // [ITEM_RING] producer -> consumers
+constexpr int BAR_ITEM_EMPTY = BAR_ITEM_FULL + ITEM_RING;  // [ITEM_RING] 10 consumer warps
+constexpr int NUM_ITEM_CONSUMERS = 10;                  // 2 MMA warps + 8 softmax warps
+constexpr int NUM_BARS = BAR_ITEM_EMPTY + ITEM_RING;
 constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
 constexpr uint32_t OFF_INVL = (OFF_ABORT + 4 + 15) & ~15u;    // float [2][128]
-constexpr uint32_t SMEM_USED = OFF_INVL + 2 * BM * 4;
+constexpr uint32_t OFF_RING = OFF_INVL + 2 * BM * 4;            // int [ITEM_RING]
+constexpr uint32_t SMEM_USED = OFF_RING + ITEM_RING * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;               // + alignment slack
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -134,6 +143,35 @@ __device__ __forceinline__ Item decode_item(int idx, const TcParams& p) {
     return it;
 }
 
+// Work items are published by the producer thread into a small ring in shared
+// memory; every consumer warp reads the same sequence.  With a scheduler
+// counter (p.sched != nullptr) each CTA claims its next item from a global
+// counter when it needs one, so SMs that run slower simply take fewer items;
+// without one, CTA c takes the static boustrophedon sequence.  -1 ends the
+// sequence.
+struct ItemRing {
+    uint64_t* bars;
+    volatile int* slots;
+    const AbortState* ab;
+    // consumer side, single thread (the MMA-issuing thread of its warp)
+    __device__ __forceinline__ bool get_one(int k, int& idx) const {
+        const int s = k % ITEM_RING;
+        if (!mbar_wait(&bars[BAR_ITEM_FULL + s], (uint32_t)(k / ITEM_RING) & 1u, *ab)) return false;
+        idx = slots[s];
+        mbar_arrive(&bars[BAR_ITEM_EMPTY + s]);
+        return true;
+    }
+    // consumer side, whole warp (all lanes call; lane 0 arrives for the warp)
+    __device__ __forceinline__ bool get(int k, int& idx) const {
+        const int s = k % ITEM_RING;
+        if (!mbar_wait_warp(&bars[BAR_ITEM_FULL + s], (uint32_t)(k / ITEM_RING) & 1u, *ab)) return false;
+        idx = slots[s];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&bars[BAR_ITEM_EMPTY + s]);
+        return true;
+    }
+};
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                        const __grid_constant__ CUtensorMap tm_k1,
@@ -154,14 +192,14 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[BAR_Q_FULL], 1);
-        mbar_init(&bars[BAR_Q_EMPTY], 1);
+        mbar_init(&bars[BAR_Q_EMPTY], 2);
         for (int s = 0; s < KSTAGES; ++s) {
             mbar_init(&bars[BAR_K_FULL + s], 1);
-            mbar_init(&bars[BAR_K_EMPTY + s], 1);
+            mbar_init(&bars[BAR_K_EMPTY + s], 2);
         }
         for (int s = 0; s < VSTAGES; ++s) {
             mbar_init(&bars[BAR_V_FULL + s], 1);
-            mbar_init(&bars[BAR_V_EMPTY + s], 1);
+            mbar_init(&bars[BAR_V_EMPTY + s], 2);
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&bars[BAR_S_FULL + i], 1);
@@ -169,10 +207,15 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
         }
         mbar_init(&bars[BAR_PV_DONE + 0], 1);
         mbar_init(&bars[BAR_PV_DONE + 1], 1);
-        mbar_init(&bars[BAR_O_FULL], 1);
+        mbar_init(&bars[BAR_O_FULL], 2);
         mbar_init(&bars[BAR_O_EMPTY], 8);
         mbar_init(&bars[BAR_L_READY], 8);
-        mbar_init(&bars[BAR_FINAL], 1);
+        mbar_init(&bars[BAR_FINAL + 0], 1);
+        mbar_init(&bars[BAR_FINAL + 1], 1);
+        for (int i = 0; i < ITEM_RING; ++i) {
+            mbar_init(&bars[BAR_ITEM_FULL + i], 1);
+            mbar_init(&bars[BAR_ITEM_EMPTY + i], NUM_ITEM_CONSUMERS);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -187,6 +230,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
 
     const int grid = gridDim.x;
     const int cta = blockIdx.x;
+    const ItemRing ring{bars, reinterpret_cast<volatile int*>(smem + OFF_RING), &ab};
 
     if (warp >= 8) {
       regs_dec<REGS_OTHER>();
@@ -202,11 +246,32 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             uint32_t armed_q = 0, armed_k[KSTAGES] = {}, armed_v[VSTAGES] = {};
             bool ok = true;
             bool first = true;
+            // Item claimed for the current position of the sequence; the next
+            // claim is issued one item ahead so its latency overlaps the loads.
+            int sk = 0;    // static sequence position
+            auto claim = [&]() -> int {
+                if (p.sched) {
+                    const int idx = (int)atomicAdd(p.sched, 1u);
+                    return idx < p.total_items ? idx : -1;
+                }
+                for (; sk * grid < p.total_items; ++sk) {
+                    const int idx = item_index(sk, cta, grid);
+                    if (idx < p.total_items) { ++sk; return idx; }
+                }
+                return -1;
+            };
+            int idx = claim();
             for (int k = 0; ok; ++k) {
-                if (k * grid >= p.total_items) break;
-                const int idx = item_index(k, cta, grid);
-                if (idx >= p.total_items) continue;
+                // publish item k (or the end of the sequence) to the consumers
+                const int slot = k % ITEM_RING;
+                if (k >= ITEM_RING) {
+                    if (!(ok = mbar_wait(&bars[BAR_ITEM_EMPTY + slot], (uint32_t)(k / ITEM_RING - 1) & 1u, ab))) break;
+                }
+                ring.slots[slot] = idx;
+                mbar_arrive(&bars[BAR_ITEM_FULL + slot]);
+                if (idx < 0) break;
                 const Item it = decode_item(idx, p);
+                idx = claim();
                 if (!first) {
                     if (!(ok = mbar_wait(&bars[BAR_Q_EMPTY], qph, ab))) break;
                     qph ^= 1;
@@ -244,60 +309,50 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 if (armed_v[s]) mbar_wait_teardown(&bars[BAR_V_FULL + s], (armed_v[s] - 1) & 1, lim);
         }
         __syncwarp();
-      } else if (warp == 9) {
-        // ------------------------------------------------------------ MMA issue
+      } else if (warp == 9 || warp == 10) {
+        // ----------------------------------------- MMA issue, one warp per branch
+        const int br = warp - 9;
         if (elect_one()) {
-            const uint32_t sq[2] = {smem_u32(smem + OFF_Q1), smem_u32(smem + OFF_Q2)};
-            const uint32_t sk0 = smem_u32(smem + OFF_K);
-            const uint32_t sv0 = smem_u32(smem + OFF_V);
+            // Descriptors for stage 0 and K-step 0; other stages and K-steps
+            // differ only in the start-address field (address >> 4, which
+            // stays below 2^14 for every shared-memory address).
+            const uint64_t qdesc = sdesc_sw128(smem_u32(smem + (br ? OFF_Q2 : OFF_Q1)), 16, 1024);
+            const uint64_t kdesc = sdesc_sw128(smem_u32(smem + OFF_K + br * K_BYTES), 16, 1024);
+            const uint64_t vdesc = sdesc_sw128(smem_u32(smem + OFF_V), V_HALF_BYTES, 1024);
+            const uint32_t d_o = tmem_base + TM_O + br * 128;
             uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0, oeph = 0;
-            uint32_t pph = 0;     // bit (2*branch + buffer): phase of P_FULL[branch][buffer]
+            uint32_t pph = 0;     // bit buffer: phase of P_FULL[br][buffer]
             bool ok = true;
 
-            auto issue_s = [&](int br, uint32_t stage, int buf) {
+            auto issue_s = [&](uint32_t stage, int buf) {
                 const uint32_t d = tmem_base + tm_s(br, buf);
-                const uint32_t qa = sq[br];
-                const uint32_t ka = sk0 + stage * 2 * K_BYTES + br * K_BYTES;
+                const uint64_t kd = kdesc + ((stage * 2 * K_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    mma_ss(d, sdesc_sw128(qa + kk * 32, 16, 1024), sdesc_sw128(ka + kk * 32, 16, 1024),
-                           IDESC_S, kk > 0);
-                }
+                for (int kk = 0; kk < HD / 16; ++kk)
+                    mma_ss(d, qdesc + 2 * kk, kd + 2 * kk, IDESC_S, kk > 0);
             };
-            auto issue_pv = [&](int br, uint32_t stage, int buf, bool acc) {
-                const uint32_t d = tmem_base + TM_O + br * 128;
+            auto issue_pv = [&](uint32_t stage, int buf, bool acc) {
                 const uint32_t pa = tmem_base + tm_s(br, buf);
-                const uint32_t va = sv0 + stage * V_BYTES;
+                const uint64_t vd = vdesc + ((stage * V_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    mma_ts(d, pa + kk * 8, sdesc_sw128(va + kk * 2048, V_HALF_BYTES, 1024), IDESC_PV,
-                           (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-            auto wait_p = [&](int br, int buf) {
-                const uint32_t bit = 1u << (2 * br + buf);
-                const bool r = mbar_wait(&bars[BAR_P_FULL + 2 * br + buf], (pph & bit) ? 1u : 0u, ab);
-                pph ^= bit;
-                return r;
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(d_o, pa + kk * 8, vd + 128 * kk, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
             };
 
             bool first = true;
             for (int k = 0; ok; ++k) {
-                if (k * grid >= p.total_items) break;
-                const int idx = item_index(k, cta, grid);
-                if (idx >= p.total_items) continue;
+                int idx = -1;
+                if (!(ok = ring.get_one(k, idx)) || idx < 0) break;
                 const Item it = decode_item(idx, p);
                 const int n = it.n_kv;
                 if (!(ok = mbar_wait(&bars[BAR_Q_FULL], qph, ab))) break;
                 qph ^= 1;
-                // S(0) and S(1) of both branches into buffers 0 and 1
+                // S_b(0), S_b(1) into buffers 0 and 1
                 for (int t = 0; t < 2 && t < n; ++t) {
                     if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
                     tc_fence_after();
-                    issue_s(0, kst, t);
-                    mma_commit(&bars[BAR_S_FULL + 0 + t]);
-                    issue_s(1, kst, t);
-                    mma_commit(&bars[BAR_S_FULL + 2 + t]);
+                    issue_s(kst, t);
+                    mma_commit(&bars[BAR_S_FULL + 2 * br + t]);
                     mma_commit(&bars[BAR_K_EMPTY + kst]);
                     if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
                 }
@@ -306,33 +361,25 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
 
                 for (int j = 0; j < n; ++j) {
                     const int buf = j & 1;
-                    const bool more = (j + 2 < n);
-                    // branch 1: O1 += P1(j) V(j), then S1(j+2) into the freed buffer
-                    if (!(ok = wait_p(0, buf))) break;
+                    // O_b += P_b(j) V(j)
+                    if (!(ok = mbar_wait(&bars[BAR_P_FULL + 2 * br + buf], (pph >> buf) & 1u, ab))) break;
+                    pph ^= 1u << buf;
                     if (j == 0 && !first) {
                         if (!(ok = mbar_wait(&bars[BAR_O_EMPTY], oeph, ab))) break;
                         oeph ^= 1;
                     }
                     if (!(ok = mbar_wait(&bars[BAR_V_FULL + vst], vph, ab))) break;
                     tc_fence_after();
-                    issue_pv(0, vst, buf, j > 0);
-                    mma_commit(&bars[BAR_PV_DONE + 0]);
-                    if (more) {
-                        if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
-                        tc_fence_after();
-                        issue_s(0, kst, buf);
-                        mma_commit(&bars[BAR_S_FULL + 0 + buf]);
-                    }
-                    // branch 2: O2 += P2(j) V(j), then S2(j+2)
-                    if (!(ok = wait_p(1, buf))) break;
-                    tc_fence_after();
-                    issue_pv(1, vst, buf, j > 0);
-                    mma_commit(&bars[BAR_PV_DONE + 1]);
+                    issue_pv(vst, buf, j > 0);
+                    mma_commit(&bars[BAR_PV_DONE + br]);
                     mma_commit(&bars[BAR_V_EMPTY + vst]);
                     if (++vst == VSTAGES) { vst = 0; vph ^= 1; }
-                    if (more) {
-                        issue_s(1, kst, buf);
-                        mma_commit(&bars[BAR_S_FULL + 2 + buf]);
+                    // S_b(j+2) into the buffer P_b(j) was just read from
+                    if (j + 2 < n) {
+                        if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
+                        tc_fence_after();
+                        issue_s(kst, buf);
+                        mma_commit(&bars[BAR_S_FULL + 2 * br + buf]);
                         mma_commit(&bars[BAR_K_EMPTY + kst]);
                         if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
                         if (j + 3 == n) mma_commit(&bars[BAR_Q_EMPTY]);
@@ -342,9 +389,9 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 mma_commit(&bars[BAR_O_FULL]);
                 first = false;
             }
-            // Every MMA issued so far must have finished before TMEM is freed.
-            mma_commit(&bars[BAR_FINAL]);
-            mbar_wait_teardown(&bars[BAR_FINAL], 0, 200ull * 1000ull * 1000ull);
+            // Every MMA this thread issued must have finished before TMEM is freed.
+            mma_commit(&bars[BAR_FINAL + br]);
+            mbar_wait_teardown(&bars[BAR_FINAL + br], 0, 200ull * 1000ull * 1000ull);
         }
         __syncwarp();
       }
@@ -364,9 +411,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
         bool ok = true;
 
         for (int k = 0; ok; ++k) {
-            if (k * grid >= p.total_items) break;
-            const int idx = item_index(k, cta, grid);
-            if (idx >= p.total_items) continue;
+            int idx = -1;
+            if (!(ok = ring.get(k, idx)) || idx < 0) break;
             const Item it = decode_item(idx, p);
             const int q = it.qt * BM + row;
             float m_run = -INFINITY;
@@ -515,6 +561,15 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
     __syncthreads();
     tc_fence_after();
     if (warp == 9) tmem_dealloc(tmem_base, TMEM_COLS);
+    // The last CTA to finish returns the scheduler counter to zero for the
+    // next launch that uses it.
+    if (p.sched && threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.sched, 0u);
+            atomicExch(p.sched + 1, 0u);
+        }
+    }
 }
 
 }  // namespace tc

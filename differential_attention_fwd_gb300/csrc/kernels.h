@@ -23,6 +23,7 @@ struct TcParams {
     __nv_bfloat16* out;
     int64_t o_sB, o_sH, o_sT;
     uint32_t* status;       // device status word
+    uint32_t* sched;        // 2 words: item counter, finished CTAs (nullptr: static schedule)
 };
 
 // Parameters of the CUDA-core kernel (any D <= 128, fp32 or bf16).

@@ -36,6 +36,7 @@
 #ifndef DIFFATTN_H
 #define DIFFATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -102,6 +103,13 @@ int diffattn_lambda(const float *lq1, const float *lk1, const float *lq2,
                     float *lambda_out, diffattn_stream_t stream);
 
 /*
+ * diffattn_workspace_bytes -- size of the optional scheduler workspace that
+ * diffattn_fwd accepts (a few bytes; the value is stable for a given library
+ * version).
+ */
+size_t diffattn_workspace_bytes(void);
+
+/*
  * diffattn_fwd -- O = (A_1 - lambda A_2) V.
  *
  * desc: shape, dtype and strides (host pointer, read during the call only).
@@ -113,19 +121,29 @@ int diffattn_lambda(const float *lq1, const float *lk1, const float *lq2,
  * causal: non-zero applies the causal mask to both branches.
  * out: device pointer to O, [B, H, T, 2D] with desc->o_stride, same dtype as
  * the inputs (bf16 results are rounded to nearest even from fp32).
+ * workspace, workspace_bytes: optional device scratch of at least
+ * diffattn_workspace_bytes() bytes, 4-byte aligned, owned by the caller.  With
+ * it the tensor-core kernel hands out work items dynamically (a CTA claims its
+ * next item when it needs one), which balances the load when SMs run at
+ * different speeds; without it (NULL) items are assigned statically.  The
+ * workspace must hold zeros before its first use; every call leaves it zeroed
+ * when its kernel finishes.  Calls that may run at the same time on the GPU
+ * (different streams) must use different workspaces.  The result does not
+ * depend on the schedule.
  * stream: the CUDA stream to launch on.
  *
  * The tensor-core kernel runs when dtype is bf16, D == 64, every base pointer
  * is 16-byte aligned and every stride is a multiple of 8 elements; any other
  * valid request runs on the CUDA-core kernel.  One kernel launch per call.
  * Errors: DIFFATTN_ERR_INVALID (NULL pointers, sizes < 1, D > 128, unknown
- * dtype, negative strides, non-zero reserved field, non-finite lambda);
+ * dtype, negative strides, non-zero reserved field, non-finite lambda, a
+ * workspace smaller than diffattn_workspace_bytes() or not 4-byte aligned);
  * DIFFATTN_ERR_CUDA (tensor-map encoding or launch failure).
  */
 int diffattn_fwd(const diffattn_desc *desc, const void *q1, const void *k1,
                  const void *q2, const void *k2, const void *v, float lambda,
-                 const float *lambda_dev, int causal, void *out,
-                 diffattn_stream_t stream);
+                 const float *lambda_dev, int causal, void *out, void *workspace,
+                 size_t workspace_bytes, diffattn_stream_t stream);
 
 /*
  * diffattn_select_kernel -- which kernel diffattn_fwd would launch for this

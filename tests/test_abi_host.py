@@ -106,7 +106,7 @@ def test_invalid_desc_rejected_without_gpu(lib, mutate):
     mutate(d)
     assert select(lib, d) == _lib.DIFFATTN_ERR_INVALID
     rc = lib.diffattn_fwd(ctypes.byref(d), *ptrs(5), ctypes.c_float(0.5), None, 1,
-                          ctypes.c_void_p(FAKE * 9), None)
+                          ctypes.c_void_p(FAKE * 9), None, 0, None)
     assert rc == _lib.DIFFATTN_ERR_INVALID
 
 
@@ -116,14 +116,26 @@ def test_null_pointers_rejected(lib):
         p = ptrs()
         p[i] = None
         assert lib.diffattn_select_kernel(ctypes.byref(d), *p) == _lib.DIFFATTN_ERR_INVALID
-    assert lib.diffattn_fwd(None, *ptrs(5), ctypes.c_float(0.5), None, 1, ctypes.c_void_p(FAKE), None) \
-        == _lib.DIFFATTN_ERR_INVALID
+    assert lib.diffattn_fwd(None, *ptrs(5), ctypes.c_float(0.5), None, 1, ctypes.c_void_p(FAKE),
+                            None, 0, None) == _lib.DIFFATTN_ERR_INVALID
 
 
 @pytest.mark.parametrize("lam", [float("nan"), float("inf"), -float("inf")])
 def test_non_finite_lambda_rejected(lib, lam):
     rc = lib.diffattn_fwd(ctypes.byref(desc()), *ptrs(5), ctypes.c_float(lam), None, 1,
-                          ctypes.c_void_p(FAKE * 9), None)
+                          ctypes.c_void_p(FAKE * 9), None, 0, None)
+    assert rc == _lib.DIFFATTN_ERR_INVALID
+
+
+def test_bad_workspace_rejected(lib):
+    need = lib.diffattn_workspace_bytes()
+    assert 8 <= need <= 4096
+    ws = ctypes.c_void_p(FAKE * 11)
+    rc = lib.diffattn_fwd(ctypes.byref(desc()), *ptrs(5), ctypes.c_float(0.5), None, 1,
+                          ctypes.c_void_p(FAKE * 9), ws, need - 4, None)
+    assert rc == _lib.DIFFATTN_ERR_INVALID
+    rc = lib.diffattn_fwd(ctypes.byref(desc()), *ptrs(5), ctypes.c_float(0.5), None, 1,
+                          ctypes.c_void_p(FAKE * 9), ctypes.c_void_p(FAKE * 11 + 2), need, None)
     assert rc == _lib.DIFFATTN_ERR_INVALID
 
 

@@ -174,3 +174,33 @@ def test_empty_and_mismatched_inputs_rejected():
     e = torch.zeros(1, 1, 0, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(da.DiffattnError):
         da.differential_attention(e, e, e, e, torch.zeros(1, 1, 0, 128, dtype=torch.bfloat16, device="cuda"), 0.5)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_static_and_dynamic_schedules_agree(causal):
+    inp = inputs(3, 20, 700, 64, seed=15)
+    dev = [to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    a = da.differential_attention(*dev, 0.8, causal=causal, dynamic_schedule=False)
+    b = da.differential_attention(*dev, 0.8, causal=causal, dynamic_schedule=True)
+    c = da.differential_attention(*dev, 0.8, causal=causal, dynamic_schedule=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(b, c)
+    ws = da.workspace_for(dev[0].device, torch.cuda.current_stream())
+    assert torch.count_nonzero(ws).item() == 0      # left zeroed for the next call
+    rows = [0, 127, 128, 699]
+    r = oracle.differential_attention(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.8, causal, rows=rows)
+    assert_close(to_numpy(b[:, :, rows]), r, "bf16", "dynamic schedule")
+
+
+def test_dynamic_schedule_on_a_side_stream():
+    inp = inputs(2, 8, 1000, 64, seed=16)
+    dev = [to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    ref = da.differential_attention(*dev, 0.5, causal=True, dynamic_schedule=False)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        outs = [da.differential_attention(*dev, 0.5, causal=True) for _ in range(3)]
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert all(torch.equal(o, ref) for o in outs)
+    assert da.get_device_error() == 0
