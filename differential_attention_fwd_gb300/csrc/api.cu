@@ -174,14 +174,16 @@ int diffattn_fwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
     if (rc != DIFFATTN_OK) return rc;
 
     if (select(desc, q1, k1, q2, k2, v, out) == DIFFATTN_KERNEL_TCGEN05) {
-        CUtensorMap maps[5];
+        CUtensorMap maps[6];
         // Q tiles are 128 query rows; K and V tiles are 64 key rows; every box
-        // is 64 elements (128 bytes) wide, the 128-byte swizzle span.
+        // is 64 elements (128 bytes) wide, the 128-byte swizzle span.  O is
+        // stored by each warp in 32-row x 64-column boxes.
         if (encode_map(&maps[0], q1, 64, &d, d.q1_stride, 64, 128) != DIFFATTN_OK ||
             encode_map(&maps[1], k1, 64, &d, d.k1_stride, 64, 64) != DIFFATTN_OK ||
             encode_map(&maps[2], q2, 64, &d, d.q2_stride, 64, 128) != DIFFATTN_OK ||
             encode_map(&maps[3], k2, 64, &d, d.k2_stride, 64, 64) != DIFFATTN_OK ||
-            encode_map(&maps[4], v, 128, &d, d.v_stride, 64, 64) != DIFFATTN_OK)
+            encode_map(&maps[4], v, 128, &d, d.v_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[5], out, 128, &d, d.o_stride, 64, 32) != DIFFATTN_OK)
             return DIFFATTN_ERR_CUDA;
         TcParams p;
         p.B = (int)d.B;

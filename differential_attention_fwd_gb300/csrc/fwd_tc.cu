@@ -73,7 +73,9 @@ constexpr uint32_t OFF_Q1 = 0;
 constexpr uint32_t OFF_Q2 = OFF_Q1 + Q_BYTES;
 constexpr uint32_t OFF_K = OFF_Q2 + Q_BYTES;                    // stage s: K1 at +0, K2 at +K_BYTES
 constexpr uint32_t OFF_V = OFF_K + KSTAGES * 2 * K_BYTES;       // stage s: cols 0-63 at +0, 64-127 at +V_HALF
-constexpr uint32_t OFF_BAR = OFF_V + VSTAGES * V_BYTES;
+constexpr uint32_t OFF_OUT = OFF_V + VSTAGES * V_BYTES;          // output staging: [branch][warp] 32 rows x 128 B
+constexpr uint32_t OUT_BYTES = BM * VD * 2;                      // 32 KB
+constexpr uint32_t OFF_BAR = OFF_OUT + OUT_BYTES;
 // barriers
 constexpr int BAR_Q_FULL = 0;
 constexpr int BAR_Q_EMPTY = 1;
@@ -178,6 +180,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                        const __grid_constant__ CUtensorMap tm_q2,
                        const __grid_constant__ CUtensorMap tm_k2,
                        const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_o,
                        const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -532,29 +535,40 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             lph ^= 1;
             const float inv1 = inv_l[row];
             const float inv2 = inv_l[BM + row];
-            if (q < p.T) {
-                __nv_bfloat16* orow = p.out + (int64_t)it.b * p.o_sB + (int64_t)it.h * p.o_sH +
-                                      (int64_t)q * p.o_sT + c0;
-                uint4* dst = reinterpret_cast<uint4*>(orow);
+            // Stage this warp's 32 rows x 64 columns in shared memory (128-byte
+            // swizzled rows, as the output tensor map expects) and write them
+            // with one TMA store; rows at or past T are clipped by the TMA unit.
+            uint8_t* stage = smem + OFF_OUT + br * (OUT_BYTES / 2) + quad * 4096;
+            if (lane == 0) bulk_wait_read_all();     // the previous store has read the buffer
+            __syncwarp();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    uint32_t w4[4];
+            for (int i = 0; i < 8; ++i) {
+                uint32_t w4[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 8 * i + 2 * e;
-                        float r[2];
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 8 * i + 2 * e;
+                    float r[2];
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const float a = __fmul_rn(__uint_as_float(o1[c + h2]), inv1);
-                            const float bb = __fmul_rn(__uint_as_float(o2[c + h2]), inv2);
-                            r[h2] = __fsub_rn(a, __fmul_rn(lam, bb));
-                        }
-                        w4[e] = pack_bf16x2(r[0], r[1]);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const float a = __fmul_rn(__uint_as_float(o1[c + h2]), inv1);
+                        const float bb = __fmul_rn(__uint_as_float(o2[c + h2]), inv2);
+                        r[h2] = __fsub_rn(a, __fmul_rn(lam, bb));
                     }
-                    dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    w4[e] = pack_bf16x2(r[0], r[1]);
                 }
+                *reinterpret_cast<uint4*>(stage + lane * 128 + ((i ^ (lane & 7)) * 16)) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_4d(&tm_o, stage, c0, it.qt * BM + (int)quad * 32, it.h, it.b);
+                bulk_commit();
             }
         }
+        // Every output store must be complete before the CTA exits.
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -581,7 +595,7 @@ int launch_fwd_tc(const CUtensorMap* maps, const TcParams& p, int grid, cudaStre
                                          (int)tc::SMEM_BYTES);
     if (e != cudaSuccess) return -1;
     tc::diffattn_fwd_tc_kernel<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, stream>>>(
-        maps[0], maps[1], maps[2], maps[3], maps[4], p);
+        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -39,7 +39,7 @@ struct SimtParams {
 };
 
 // Each returns 0 on success, -1 if the launch failed.
-int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v*/, const TcParams& p, int grid,
+int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v,out*/, const TcParams& p, int grid,
                   cudaStream_t stream);
 int launch_fwd_simt_f32(const SimtParams& p, cudaStream_t stream);
 int launch_fwd_simt_bf16(const SimtParams& p, cudaStream_t stream);
