@@ -34,6 +34,10 @@ Readings where the pages leave a step open:
     ever fully masked.
   * lambda is any finite real (not clamped to [0, 1]).
 
+The step that follows the operation in the model (per-head normalisation,
+GroupNorm or RMSNorm, then x (1 - lambda_init)) is `head_norm`, pinned
+against torch's group_norm and rms_norm.
+
 Parity is pinned by tests/test_oracle.py (brute-force scalar softmax on tiny
 inputs, a library attention routine at lambda = 0, row sums, the identical-map
 and value-offset identities, closed forms, and the printed worked example).
@@ -51,6 +55,7 @@ __all__ = [
     "softmax_maps",
     "signed_map",
     "differential_attention",
+    "head_norm",
 ]
 
 
@@ -187,3 +192,41 @@ def differential_attention(q1, k1, q2, k2, v, lam: float, causal: bool = True,
     if heads is None:
         out = out.reshape(B, H, row_idx.size, 2 * D)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Per-head output normalisation and the fixed multiplier (the step after the
+# operation: aifetchly section 4 and the ultralytics glossary describe a
+# per-head GroupNorm followed by x (1 - lambda_init); the aiengineeringfromscratch
+# lesson describes the per-head normalisation of DIFF V1 as an RMSNorm).
+# ---------------------------------------------------------------------------
+
+def head_norm(o, kind: str, eps: float = 1e-5, weight=None, bias=None,
+              out_scale: float = 1.0) -> np.ndarray:
+    """Y = out_scale * (norm(O) * weight + bias), per (b, h, t) over the head's
+    2D output channels, in float64.
+
+    kind "rms":   norm(x) = x / sqrt(mean(x^2) + eps)
+    kind "group": norm(x) = (x - mean(x)) / sqrt(var(x) + eps), var the mean
+                  squared deviation (one group per head, as GroupNorm with
+                  num_groups = H over the H * 2D channels of a token)
+    kind "none":  norm(x) = x
+    weight, bias: optional [H, 2D] per-channel affine parameters.
+    """
+    o = np.asarray(o, dtype=np.float64)
+    if kind == "rms":
+        y = o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    elif kind == "group":
+        mu = np.mean(o, axis=-1, keepdims=True)
+        var = np.mean((o - mu) ** 2, axis=-1, keepdims=True)
+        y = (o - mu) / np.sqrt(var + eps)
+    elif kind == "none":
+        y = o.copy()
+    else:
+        raise ValueError(f"unknown norm {kind!r}")
+    H = o.shape[1]
+    if weight is not None:
+        y = y * np.asarray(weight, dtype=np.float64).reshape(1, H, 1, -1)
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float64).reshape(1, H, 1, -1)
+    return out_scale * y

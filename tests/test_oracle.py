@@ -321,3 +321,46 @@ def test_planted_lambda_sign_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "differential_lambda", bad)
     with pytest.raises(AssertionError):
         pin_lambda()
+
+
+# ---------------------------------------------------------------------------
+# Per-head norm and multiplier (the step after the operation)
+# ---------------------------------------------------------------------------
+
+def test_head_norm_group_matches_torch_group_norm():
+    rng = np.random.default_rng(40)
+    B, H, T, C = 2, 3, 5, 16
+    o = rng.normal(1.5, 2.0, size=(B, H, T, C))
+    w = rng.normal(size=(H, C))
+    b = rng.normal(size=(H, C))
+    got = oracle.head_norm(o, "group", 1e-5, w, b, out_scale=0.37)
+    x = torch.from_numpy(o).permute(0, 2, 1, 3).reshape(B * T, H * C)   # a token's channels
+    ref = torch.nn.functional.group_norm(x, H, torch.from_numpy(w.reshape(-1)),
+                                         torch.from_numpy(b.reshape(-1)), eps=1e-5)
+    ref = (0.37 * ref).reshape(B, T, H, C).permute(0, 2, 1, 3).numpy()
+    assert np.max(np.abs(got - ref)) <= 1e-12
+
+
+def test_head_norm_rms_matches_torch_rms_norm():
+    rng = np.random.default_rng(41)
+    o = rng.normal(0.3, 1.7, size=(2, 4, 6, 32))
+    w = rng.normal(size=(4, 32))
+    got = oracle.head_norm(o, "rms", 1e-6, w, None, out_scale=0.8)
+    ref = np.stack([torch.nn.functional.rms_norm(torch.from_numpy(o[:, h]), (32,),
+                                                 torch.from_numpy(w[h]), eps=1e-6).numpy()
+                    for h in range(4)], axis=1)
+    assert np.max(np.abs(got - 0.8 * ref)) <= 1e-12
+
+
+def test_head_norm_invariants():
+    rng = np.random.default_rng(42)
+    o = rng.normal(size=(1, 2, 7, 8))
+    g = oracle.head_norm(o, "group", 0.0)
+    assert np.max(np.abs(g.mean(-1))) <= 1e-12 and np.max(np.abs(g.var(-1) - 1)) <= 1e-12
+    r = oracle.head_norm(o, "rms", 0.0)
+    assert np.max(np.abs(np.mean(r * r, -1) - 1)) <= 1e-12
+    # scale invariance (eps = 0) and the multiplier
+    assert np.max(np.abs(oracle.head_norm(3.5 * o, "rms", 0.0) - r)) <= 1e-12
+    assert np.max(np.abs(oracle.head_norm(o, "none", out_scale=0.25) - 0.25 * o)) <= 0
+    with pytest.raises(ValueError):
+        oracle.head_norm(o, "layer")
