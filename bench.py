@@ -306,6 +306,17 @@ def run_ours(args, w, world, rank, local):
     kernel = da.select_kernel(*d_in, out=d_out)
     ws = da.workspace_for(dev, stream)
     p_ws, ws_bytes = ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel() * 4)
+    epi = None
+    if args.norm != "none":
+        # fused per-head norm with affine parameters, then x (1 - lambda_init)
+        g = torch.Generator(device="cpu").manual_seed(11)
+        nw = (1 + 0.1 * torch.randn(w.H, w.Dv, generator=g)).to(dev)
+        nb = (0.1 * torch.randn(w.H, w.Dv, generator=g)).to(dev)
+        epi = _lib.DiffattnEpilogue()
+        epi.norm = {"rms": _lib.DIFFATTN_NORM_RMS, "group": _lib.DIFFATTN_NORM_GROUP}[args.norm]
+        epi.eps, epi.weight, epi.bias = 1e-5, nw.data_ptr(), nb.data_ptr()
+        epi.out_scale, epi.reserved = 1.0 - lam_init, 0
+    p_epi = ctypes.byref(epi) if epi is not None else None
 
     def step():
         rc = lib.diffattn_lambda(*ptr_lv, nlam, ctypes.c_double(lam_init), p_lam, sh)
@@ -313,8 +324,8 @@ def run_ours(args, w, world, rank, local):
             raise _lib.DiffattnError(rc, "diffattn_lambda")
 
     def fwd():
-        rc = lib.diffattn_fwd(ctypes.byref(desc), *ptr_in, ctypes.c_float(0.0), p_lam,
-                              1 if w.causal else 0, p_out, p_ws, ws_bytes, sh)
+        rc = lib.diffattn_fwd_ex(ctypes.byref(desc), *ptr_in, ctypes.c_float(0.0), p_lam,
+                                 1 if w.causal else 0, p_epi, p_out, p_ws, ws_bytes, sh)
         if rc:
             raise _lib.DiffattnError(rc, "diffattn_fwd")
 
@@ -380,7 +391,8 @@ def run_ours(args, w, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": config_of(w, float(d_lam.item())),
+        "config": {**config_of(w, float(d_lam.item())),
+                   **({"epilogue": f"{args.norm} norm + affine + x(1-lambda_init)"} if args.norm != "none" else {})},
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": roofline, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -454,6 +466,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    ap.add_argument("--norm", choices=["none", "rms", "group"], default="none",
+                    help="fuse a per-head norm and the (1 - lambda_init) multiplier")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("at least 3 warm-up steps")

@@ -22,7 +22,8 @@ import torch
 
 from . import _lib
 from ._lib import (DIFFATTN_BF16, DIFFATTN_F32, DIFFATTN_KERNEL_SIMT,  # noqa: F401
-                   DIFFATTN_KERNEL_TCGEN05, DiffattnDesc, DiffattnError)
+                   DIFFATTN_KERNEL_TCGEN05, DIFFATTN_NORM_GROUP, DIFFATTN_NORM_NONE,
+                   DIFFATTN_NORM_RMS, DiffattnDesc, DiffattnEpilogue, DiffattnError)
 
 __all__ = ["differential_lambda", "differential_attention", "make_desc", "select_kernel",
            "get_device_error", "version", "DiffattnError"]
@@ -145,7 +146,10 @@ def select_kernel(q1, k1, q2, k2, value, out=None) -> int:
 def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor, k2: torch.Tensor,
                            value: torch.Tensor, coefficient, causal: bool = True,
                            out: Optional[torch.Tensor] = None,
-                           dynamic_schedule: bool = True) -> torch.Tensor:
+                           dynamic_schedule: bool = True, norm: Optional[str] = None,
+                           norm_eps: float = 1e-5, norm_weight: Optional[torch.Tensor] = None,
+                           norm_bias: Optional[torch.Tensor] = None,
+                           out_scale: float = 1.0) -> torch.Tensor:
     """O = (softmax(Q1 K1^T/sqrt(D) + M) - lambda softmax(Q2 K2^T/sqrt(D) + M)) V.
 
     q1, k1, q2, k2: [B, H, T, D]; value: [B, H, T, 2D]; all bfloat16 or all
@@ -155,8 +159,16 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
     causal: mask key j > query i in both branches.  out: optional preallocated
     [B, H, T, 2D] output of the same dtype.  dynamic_schedule: hand out work
     items at run time through a small per-stream workspace (the result is
-    the same either way).  Returns the [B, H, T, 2D] output; the launch is
-    asynchronous on the current CUDA stream.  (Forward only.)
+    the same either way).
+
+    Optional fused epilogue (the step after the operation in the model):
+    norm "rms" or "group" normalises each (b, h, t) row over the head's 2D
+    channels (eps norm_eps), then multiplies by norm_weight and adds
+    norm_bias ([H, 2D] float32 tensors, optional), and finally scales by
+    out_scale (e.g. 1 - lambda_init).
+
+    Returns the [B, H, T, 2D] output; the launch is asynchronous on the
+    current CUDA stream.  (Forward only.)
     """
     (q1, k1, q2, k2, value), dev = _prepare(q1, k1, q2, k2, value)
     B, H, T, D = q1.shape
@@ -184,20 +196,52 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
     else:
         raise TypeError("coefficient must be a real number or a scalar tensor")
     d = make_desc(q1, k1, q2, k2, value, out)
+    epi = _epilogue(norm, norm_eps, norm_weight, norm_bias, out_scale, H, 2 * D, dev)
     lib = _lib.load()
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev)
         ws = workspace_for(dev, stream) if dynamic_schedule else None
-        rc = lib.diffattn_fwd(ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in
-                                                  (q1, k1, q2, k2, value)),
-                              ctypes.c_float(lam_host),
-                              ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0),
-                              1 if causal else 0, ctypes.c_void_p(out.data_ptr()),
-                              ctypes.c_void_p(ws.data_ptr() if ws is not None else 0),
-                              ctypes.c_size_t(ws.numel() * 4 if ws is not None else 0),
-                              ctypes.c_void_p(stream.cuda_stream))
+        rc = lib.diffattn_fwd_ex(ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in
+                                                     (q1, k1, q2, k2, value)),
+                                 ctypes.c_float(lam_host),
+                                 ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0),
+                                 1 if causal else 0, ctypes.byref(epi[0]) if epi else None,
+                                 ctypes.c_void_p(out.data_ptr()),
+                                 ctypes.c_void_p(ws.data_ptr() if ws is not None else 0),
+                                 ctypes.c_size_t(ws.numel() * 4 if ws is not None else 0),
+                                 ctypes.c_void_p(stream.cuda_stream))
     _lib.check(rc, "diffattn_fwd")
     return out
+
+
+_NORMS = {None: DIFFATTN_NORM_NONE, "none": DIFFATTN_NORM_NONE, "rms": DIFFATTN_NORM_RMS,
+          "group": DIFFATTN_NORM_GROUP}
+
+
+def _epilogue(norm, eps, weight, bias, out_scale, H, Dv, dev):
+    """diffattn_epilogue for the call (None when there is nothing to apply);
+    returns (struct, tensors kept alive for the launch)."""
+    if norm not in _NORMS:
+        raise ValueError(f"norm must be one of {sorted(k for k in _NORMS if k)}, got {norm!r}")
+    code = _NORMS[norm]
+    if code == DIFFATTN_NORM_NONE and weight is None and bias is None and out_scale == 1.0:
+        return None
+    keep = []
+    ptrs = []
+    for name, t in (("norm_weight", weight), ("norm_bias", bias)):
+        if t is None:
+            ptrs.append(0)
+            continue
+        _require_cuda(t, name)
+        if t.device != dev or tuple(t.shape) not in ((H, Dv), (H * Dv,)):
+            raise ValueError(f"{name} must be [H, 2D] = {(H, Dv)} on the inputs' device")
+        t = t.detach().to(torch.float32).contiguous()
+        keep.append(t)
+        ptrs.append(t.data_ptr())
+    e = DiffattnEpilogue()
+    e.norm, e.eps, e.out_scale, e.reserved = code, float(eps), float(out_scale), 0
+    e.weight, e.bias = ptrs
+    return e, keep
 
 
 def get_device_error(device=None) -> int:

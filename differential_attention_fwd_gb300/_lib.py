@@ -19,10 +19,15 @@ DIFFATTN_F32 = 1
 DIFFATTN_KERNEL_TCGEN05 = 1
 DIFFATTN_KERNEL_SIMT = 2
 
+DIFFATTN_NORM_NONE = 0
+DIFFATTN_NORM_RMS = 1
+DIFFATTN_NORM_GROUP = 2
+
 # Every symbol include/diffattn.h declares.
 EXPORTED = (
     "diffattn_lambda",
     "diffattn_fwd",
+    "diffattn_fwd_ex",
     "diffattn_workspace_bytes",
     "diffattn_select_kernel",
     "diffattn_get_device_error",
@@ -39,6 +44,14 @@ class DiffattnDesc(ctypes.Structure):
         ("q1_stride", ctypes.c_int64 * 3), ("k1_stride", ctypes.c_int64 * 3),
         ("q2_stride", ctypes.c_int64 * 3), ("k2_stride", ctypes.c_int64 * 3),
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+    ]
+
+
+class DiffattnEpilogue(ctypes.Structure):
+    """Mirror of diffattn_epilogue."""
+    _fields_ = [
+        ("norm", ctypes.c_int32), ("eps", ctypes.c_float), ("weight", ctypes.c_void_p),
+        ("bias", ctypes.c_void_p), ("out_scale", ctypes.c_float), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -66,6 +79,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_lambda.restype = ctypes.c_int
     lib.diffattn_fwd.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, ctypes.c_float,
                                  vp, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]
+    lib.diffattn_fwd_ex.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, ctypes.c_float,
+                                    vp, ctypes.c_int, ctypes.POINTER(DiffattnEpilogue), vp, vp,
+                                    ctypes.c_size_t, vp]
+    lib.diffattn_fwd_ex.restype = ctypes.c_int
     lib.diffattn_workspace_bytes.argtypes = []
     lib.diffattn_workspace_bytes.restype = ctypes.c_size_t
     lib.diffattn_fwd.restype = ctypes.c_int

@@ -16,6 +16,8 @@ __device__ uint32_t g_status_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
+static_assert(DIFFATTN_NORM_NONE == kNormNone && DIFFATTN_NORM_RMS == kNormRms &&
+                  DIFFATTN_NORM_GROUP == kNormGroup, "norm codes");
 // Scheduler workspace: an item counter and a finished-CTA counter (2 words),
 // rounded up to leave room.
 constexpr size_t kWorkspaceBytes = 64;
@@ -161,8 +163,24 @@ int diffattn_fwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
                  const void* k2, const void* v, float lambda, const float* lambda_dev,
                  int causal, void* out, void* workspace, size_t workspace_bytes,
                  diffattn_stream_t stream) {
+    return diffattn_fwd_ex(desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal, nullptr, out,
+                           workspace, workspace_bytes, stream);
+}
+
+int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
+                    const void* k2, const void* v, float lambda, const float* lambda_dev,
+                    int causal, const diffattn_epilogue* epi, void* out, void* workspace,
+                    size_t workspace_bytes, diffattn_stream_t stream) {
     int rc = validate(desc, q1, k1, q2, k2, v, out);
     if (rc != DIFFATTN_OK) return rc;
+    diffattn_epilogue e{DIFFATTN_NORM_NONE, 0.f, nullptr, nullptr, 1.0f, 0};
+    if (epi) {
+        e = *epi;
+        if (e.reserved != 0 || e.norm < DIFFATTN_NORM_NONE || e.norm > DIFFATTN_NORM_GROUP ||
+            !std::isfinite(e.out_scale) ||
+            (e.norm != DIFFATTN_NORM_NONE && !(std::isfinite(e.eps) && e.eps > 0.f)))
+            return DIFFATTN_ERR_INVALID;
+    }
     if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
     if (workspace && (workspace_bytes < kWorkspaceBytes ||
                       (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0))
@@ -219,6 +237,11 @@ int diffattn_fwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
         p.o_sT = d.o_stride[2];
         p.status = dev->status;
         p.sched = static_cast<uint32_t*>(workspace);
+        p.norm = e.norm;
+        p.norm_eps = e.eps;
+        p.norm_weight = e.weight;
+        p.norm_bias = e.bias;
+        p.out_scale = e.out_scale;
         const int grid = p.total_items < dev->num_sms ? p.total_items : dev->num_sms;
         return launch_fwd_tc(maps, p, grid, st) == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
     }
@@ -244,6 +267,11 @@ int diffattn_fwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
     copy3(p.s_k2, d.k2_stride);
     copy3(p.s_v, d.v_stride);
     copy3(p.s_o, d.o_stride);
+    p.norm = e.norm;
+    p.norm_eps = e.eps;
+    p.norm_weight = e.weight;
+    p.norm_bias = e.bias;
+    p.out_scale = e.out_scale;
     rc = (d.dtype == DIFFATTN_F32) ? launch_fwd_simt_f32(p, st) : launch_fwd_simt_bf16(p, st);
     return rc == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }

@@ -127,14 +127,50 @@ diffattn_fwd_simt_kernel(const SimtParams p) {
     const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
     const float inv1 = 1.0f / l1;
     const float inv2 = 1.0f / l2;
+    float r[OPL];
 #pragma unroll
-    for (int r = 0; r < OPL; ++r) {
-        const int c = lane + 32 * r;
-        if (c < Dv) {
-            const float a = __fmul_rn(o1[r], inv1);
-            const float bb = __fmul_rn(o2[r], inv2);
-            store(out, c, __fsub_rn(a, __fmul_rn(lam, bb)));
+    for (int k = 0; k < OPL; ++k) {
+        const float a = __fmul_rn(o1[k], inv1);
+        const float bb = __fmul_rn(o2[k], inv2);
+        r[k] = __fsub_rn(a, __fmul_rn(lam, bb));
+    }
+    if (p.norm != kNormNone) {
+        // per-head normalisation over the row's 2D channels (spread over lanes)
+        float part = 0.f;
+#pragma unroll
+        for (int k = 0; k < OPL; ++k) {
+            const int c = lane + 32 * k;
+            if (c < Dv) part += (p.norm == kNormRms) ? r[k] * r[k] : r[k];
         }
+        const float tot = warp_sum(part);
+        float mu = 0.f, rinv;
+        if (p.norm == kNormRms) {
+            rinv = rsqrtf(tot / Dv + p.norm_eps);
+        } else {
+            mu = tot / Dv;
+            float dev = 0.f;
+#pragma unroll
+            for (int k = 0; k < OPL; ++k) {
+                const int c = lane + 32 * k;
+                if (c < Dv) dev += (r[k] - mu) * (r[k] - mu);
+            }
+            rinv = rsqrtf(warp_sum(dev) / Dv + p.norm_eps);
+        }
+#pragma unroll
+        for (int k = 0; k < OPL; ++k) {
+            const int c = lane + 32 * k;
+            if (c < Dv) {
+                float y = (r[k] - mu) * rinv;
+                if (p.norm_weight) y *= __ldg(p.norm_weight + h * Dv + c);
+                if (p.norm_bias) y += __ldg(p.norm_bias + h * Dv + c);
+                r[k] = y;
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < OPL; ++k) {
+        const int c = lane + 32 * k;
+        if (c < Dv) store(out, c, p.out_scale == 1.0f ? r[k] : r[k] * p.out_scale);
     }
 }
 

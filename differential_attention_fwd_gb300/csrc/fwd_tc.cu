@@ -57,7 +57,7 @@ constexpr int BN = 64;             // keys per KV tile
 constexpr int HD = 64;             // Q/K width D
 constexpr int VD = 128;            // V/O width 2D
 constexpr int KSTAGES = 5;         // (K1, K2) ring depth
-constexpr int VSTAGES = 5;         // V ring depth
+constexpr int VSTAGES = 4;         // V ring depth
 constexpr int NUM_THREADS = 384;
 constexpr uint32_t REGS_SOFTMAX = 200;
 constexpr uint32_t REGS_OTHER = 104;
@@ -94,12 +94,15 @@ constexpr int ITEM_RING = 8;                            // published work items 
 constexpr int BAR_ITEM_FULL = BAR_FINAL + 2;            // [ITEM_RING] producer -> consumers
 constexpr int BAR_ITEM_EMPTY = BAR_ITEM_FULL + ITEM_RING;  // [ITEM_RING] 10 consumer warps
 constexpr int NUM_ITEM_CONSUMERS = 10;                  // 2 MMA warps + 8 softmax warps
-constexpr int NUM_BARS = BAR_ITEM_EMPTY + ITEM_RING;
+constexpr int BAR_NORM_A = BAR_ITEM_EMPTY + ITEM_RING;  // per-row partial sums of both halves
+constexpr int BAR_NORM_B = BAR_NORM_A + 1;              // per-row partial squared deviations
+constexpr int NUM_BARS = BAR_NORM_B + 1;
 constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
 constexpr uint32_t OFF_INVL = (OFF_ABORT + 4 + 15) & ~15u;    // float [2][128]
 constexpr uint32_t OFF_RING = OFF_INVL + 2 * BM * 4;            // int [ITEM_RING]
-constexpr uint32_t SMEM_USED = OFF_RING + ITEM_RING * 4;
+constexpr uint32_t OFF_STAT = OFF_RING + ITEM_RING * 4;         // float [2 stats][2 halves][128]
+constexpr uint32_t SMEM_USED = OFF_STAT + 2 * 2 * BM * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;               // + alignment slack
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -219,6 +222,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             mbar_init(&bars[BAR_ITEM_FULL + i], 1);
             mbar_init(&bars[BAR_ITEM_EMPTY + i], NUM_ITEM_CONSUMERS);
         }
+        mbar_init(&bars[BAR_NORM_A], 8);
+        mbar_init(&bars[BAR_NORM_B], 8);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -409,7 +414,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
         const float sl2 = p.scale_log2;
         const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
         uint32_t sph = 0;          // bit buf: phase of S_FULL[br][buf]
-        uint32_t ofph = 0, lph = 0;
+        uint32_t ofph = 0, lph = 0, naph = 0, nbph = 0;
+        float* stat = reinterpret_cast<float*>(smem + OFF_STAT);
         uint32_t pv_count = 0;     // PV_b products issued for earlier items
         bool ok = true;
 
@@ -535,6 +541,61 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             lph ^= 1;
             const float inv1 = inv_l[row];
             const float inv2 = inv_l[BM + row];
+            // O = O1 / l1 - lambda O2 / l2 for this thread's 64 columns
+            float r[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float a = __fmul_rn(__uint_as_float(o1[c]), inv1);
+                const float bb = __fmul_rn(__uint_as_float(o2[c]), inv2);
+                r[c] = __fsub_rn(a, __fmul_rn(lam, bb));
+            }
+            if (p.norm != kNormNone) {
+                // Per-head normalisation over the row's 2D = 128 channels; the
+                // two warpgroups hold 64 channels each and exchange partial
+                // sums through shared memory.
+                float part = 0.f;
+                if (p.norm == kNormRms) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) part = fmaf(r[c], r[c], part);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) part += r[c];
+                }
+                stat[br * BM + row] = part;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[BAR_NORM_A]);
+                if (!(ok = mbar_wait_warp(&bars[BAR_NORM_A], naph, ab))) break;
+                naph ^= 1;
+                const float tot = stat[row] + stat[BM + row];
+                float mu = 0.f, rinv;
+                if (p.norm == kNormRms) {
+                    rinv = rsqrtf(tot * (1.0f / VD) + p.norm_eps);
+                } else {
+                    mu = tot * (1.0f / VD);
+                    float dev = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) dev = fmaf(r[c] - mu, r[c] - mu, dev);
+                    stat[2 * BM + br * BM + row] = dev;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[BAR_NORM_B]);
+                    if (!(ok = mbar_wait_warp(&bars[BAR_NORM_B], nbph, ab))) break;
+                    nbph ^= 1;
+                    const float var = (stat[2 * BM + row] + stat[3 * BM + row]) * (1.0f / VD);
+                    rinv = rsqrtf(var + p.norm_eps);
+                }
+                const float* wrow = p.norm_weight ? p.norm_weight + it.h * VD + c0 : nullptr;
+                const float* brow = p.norm_bias ? p.norm_bias + it.h * VD + c0 : nullptr;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    float y = (r[c] - mu) * rinv;
+                    if (wrow) y *= __ldg(wrow + c);
+                    if (brow) y += __ldg(brow + c);
+                    r[c] = y * p.out_scale;
+                }
+            } else if (p.out_scale != 1.0f) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) r[c] *= p.out_scale;
+            }
             // Stage this warp's 32 rows x 64 columns in shared memory (128-byte
             // swizzled rows, as the output tensor map expects) and write them
             // with one TMA store; rows at or past T are clipped by the TMA unit.
@@ -543,21 +604,10 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             __syncwarp();
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = 8 * i + 2 * e;
-                    float r[2];
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const float a = __fmul_rn(__uint_as_float(o1[c + h2]), inv1);
-                        const float bb = __fmul_rn(__uint_as_float(o2[c + h2]), inv2);
-                        r[h2] = __fsub_rn(a, __fmul_rn(lam, bb));
-                    }
-                    w4[e] = pack_bf16x2(r[0], r[1]);
-                }
+                const int c = 8 * i;
                 *reinterpret_cast<uint4*>(stage + lane * 128 + ((i ^ (lane & 7)) * 16)) =
-                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    make_uint4(pack_bf16x2(r[c], r[c + 1]), pack_bf16x2(r[c + 2], r[c + 3]),
+                               pack_bf16x2(r[c + 4], r[c + 5]), pack_bf16x2(r[c + 6], r[c + 7]));
             }
             fence_proxy_async_smem();
             __syncwarp();

@@ -9,6 +9,10 @@
 
 namespace diffattn {
 
+// Output epilogue applied after O = O1/l1 - lambda O2/l2 (the same values as
+// DIFFATTN_NORM_* in the public header).
+enum : int { kNormNone = 0, kNormRms = 1, kNormGroup = 2 };
+
 // Parameters of the tensor-core kernel (bf16, D = 64).
 struct TcParams {
     int B, H, T;
@@ -24,6 +28,11 @@ struct TcParams {
     int64_t o_sB, o_sH, o_sT;
     uint32_t* status;       // device status word
     uint32_t* sched;        // 2 words: item counter, finished CTAs (nullptr: static schedule)
+    int norm;               // kNorm*
+    float norm_eps;
+    const float* norm_weight;   // [H, 2D] or nullptr
+    const float* norm_bias;     // [H, 2D] or nullptr
+    float out_scale;            // applied last
 };
 
 // Parameters of the CUDA-core kernel (any D <= 128, fp32 or bf16).
@@ -36,6 +45,11 @@ struct SimtParams {
     const void* q1; const void* k1; const void* q2; const void* k2; const void* v;
     void* out;
     int64_t s_q1[3], s_k1[3], s_q2[3], s_k2[3], s_v[3], s_o[3];
+    int norm;
+    float norm_eps;
+    const float* norm_weight;
+    const float* norm_bias;
+    float out_scale;
 };
 
 // Each returns 0 on success, -1 if the launch failed.

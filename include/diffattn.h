@@ -145,6 +145,49 @@ int diffattn_fwd(const diffattn_desc *desc, const void *q1, const void *k1,
                  const float *lambda_dev, int causal, void *out, void *workspace,
                  size_t workspace_bytes, diffattn_stream_t stream);
 
+/* Per-head normalisation applied by diffattn_fwd_ex. */
+#define DIFFATTN_NORM_NONE  0   /* no normalisation */
+#define DIFFATTN_NORM_RMS   1   /* x / sqrt(mean(x^2) + eps) */
+#define DIFFATTN_NORM_GROUP 2   /* (x - mean(x)) / sqrt(var(x) + eps), var the mean squared deviation */
+
+/*
+ * Output epilogue of diffattn_fwd_ex: for every (b, h, t) row x of O (the
+ * head's 2D output channels),
+ *
+ *     y = out_scale * (norm(x) * weight[h] + bias[h])
+ *
+ * which is the step that follows the operation in the Differential
+ * Transformer: a per-head normalisation (called GroupNorm by aifetchly, section
+ * 4, and by the ultralytics glossary, RMSNorm for DIFF V1 by the
+ * aiengineeringfromscratch lesson), then the fixed multiplier (1 - lambda_init).
+ *
+ * norm: DIFFATTN_NORM_*.  eps: > 0 when norm != NONE (e.g. 1e-5).
+ * weight, bias: optional device pointers to [H, 2D] float32 per-channel
+ * affine parameters (NULL = 1 and 0).  out_scale: finite multiplier applied
+ * last (e.g. 1 - lambda_init; 1 for none).
+ */
+typedef struct {
+    int32_t norm;
+    float eps;
+    const float *weight;
+    const float *bias;
+    float out_scale;
+    int32_t reserved;   /* must be 0 */
+} diffattn_epilogue;
+
+/*
+ * diffattn_fwd_ex -- diffattn_fwd followed by the output epilogue `epi`
+ * (host pointer, read during the call only; NULL = none), fused into the
+ * same kernel.  Arguments and errors as diffattn_fwd, plus
+ * DIFFATTN_ERR_INVALID for an unknown norm, a non-positive or non-finite eps
+ * with a norm, a non-finite out_scale or a non-zero reserved field.
+ */
+int diffattn_fwd_ex(const diffattn_desc *desc, const void *q1, const void *k1,
+                    const void *q2, const void *k2, const void *v, float lambda,
+                    const float *lambda_dev, int causal, const diffattn_epilogue *epi,
+                    void *out, void *workspace, size_t workspace_bytes,
+                    diffattn_stream_t stream);
+
 /*
  * diffattn_select_kernel -- which kernel diffattn_fwd would launch for this
  * descriptor and these pointers (DIFFATTN_KERNEL_*), or a negative error code

@@ -161,3 +161,14 @@ def test_binding_rejects_cpu_tensors():
         da.differential_attention(x, x, x, x, v, 0.5)
     with pytest.raises(ValueError, match="CUDA"):
         da.differential_lambda(torch.zeros(4), torch.zeros(4), torch.zeros(4), torch.zeros(4))
+
+
+@pytest.mark.parametrize("field,value", [("norm", 3), ("norm", -1), ("eps", 0.0), ("eps", float("nan")),
+                                         ("out_scale", float("inf")), ("reserved", 2)])
+def test_bad_epilogue_rejected(lib, field, value):
+    e = _lib.DiffattnEpilogue()
+    e.norm, e.eps, e.out_scale, e.reserved = _lib.DIFFATTN_NORM_RMS, 1e-5, 1.0, 0
+    setattr(e, field, value)
+    rc = lib.diffattn_fwd_ex(ctypes.byref(desc()), *ptrs(5), ctypes.c_float(0.5), None, 1,
+                             ctypes.byref(e), ctypes.c_void_p(FAKE * 9), None, 0, None)
+    assert rc == _lib.DIFFATTN_ERR_INVALID
