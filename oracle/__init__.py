@@ -5,6 +5,7 @@ baseline use it.  It shares no code with the CUDA library.
 """
 from .diffattn_oracle import (  # noqa: F401
     differential_attention,
+    differential_attention_kv,
     differential_lambda,
     head_norm,
     lambda_init_schedule,

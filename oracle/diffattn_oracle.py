@@ -56,6 +56,7 @@ __all__ = [
     "signed_map",
     "differential_attention",
     "head_norm",
+    "differential_attention_kv",
 ]
 
 
@@ -91,12 +92,14 @@ def _scores(q: np.ndarray, k: np.ndarray) -> np.ndarray:
     return (q @ k.T) / math.sqrt(D)
 
 
-def _mask(s: np.ndarray, rows: np.ndarray, causal: bool) -> np.ndarray:
-    """Add M: -inf where key j > query i (causal), nothing otherwise."""
+def _mask(s: np.ndarray, rows: np.ndarray, causal: bool, offset: int = 0) -> np.ndarray:
+    """Add M: -inf where key j > query i + offset (causal), nothing otherwise.
+    offset = Tk - Tq places the queries at the end of the key sequence (a KV
+    cache); it is 0 when queries and keys are the same sequence."""
     if not causal:
         return s
     keys = np.arange(s.shape[-1])
-    future = keys[None, :] > rows[:, None]
+    future = keys[None, :] > rows[:, None] + offset
     out = s.copy()
     out[future] = -np.inf
     return out
@@ -115,10 +118,10 @@ def _combine(a1: np.ndarray, a2: np.ndarray, lam: float) -> np.ndarray:
     return a1 - lam * a2
 
 
-def _head_rows(q1, k1, q2, k2, rows, lam, causal):
+def _head_rows(q1, k1, q2, k2, rows, lam, causal, offset=0):
     """Signed-map rows of one head for the given query rows."""
-    a1 = _softmax(_mask(_scores(q1[rows], k1), rows, causal))
-    a2 = _softmax(_mask(_scores(q2[rows], k2), rows, causal))
+    a1 = _softmax(_mask(_scores(q1[rows], k1), rows, causal, offset))
+    a2 = _softmax(_mask(_scores(q2[rows], k2), rows, causal, offset))
     return _combine(a1, a2, lam)
 
 
@@ -230,3 +233,30 @@ def head_norm(o, kind: str, eps: float = 1e-5, weight=None, bias=None,
     if bias is not None:
         y = y + np.asarray(bias, dtype=np.float64).reshape(1, H, 1, -1)
     return out_scale * y
+
+
+def differential_attention_kv(q1, k1, q2, k2, v, lam: float, causal: bool = True) -> np.ndarray:
+    """O = (A_1 - lambda A_2) V for Tq queries against Tk >= Tq keys (decode
+    over a KV cache), in float64.
+
+    q1, q2: [B, H, Tq, D]; k1, k2: [B, H, Tk, D]; v: [B, H, Tk, 2D].  With the
+    causal mask, query i sits at position Tk - Tq + i of the key sequence and
+    sees keys j <= Tk - Tq + i (the usual KV-cache alignment; for Tq = Tk it is
+    the causal mask of differential_attention).  Returns [B, H, Tq, 2D].
+    """
+    q1, k1, q2, k2, v = (_as64(x) for x in (q1, k1, q2, k2, v))
+    if q1.shape != q2.shape or k1.shape != k2.shape or q1.ndim != 4 or k1.ndim != 4:
+        raise ValueError("Q1/Q2 must be [B, H, Tq, D] and K1/K2 [B, H, Tk, D]")
+    B, H, Tq, D = q1.shape
+    Tk = k1.shape[2]
+    if k1.shape[:2] != (B, H) or k1.shape[3] != D or v.shape != (B, H, Tk, 2 * D):
+        raise ValueError("inconsistent shapes")
+    if min(B, H, Tq, D, Tk) < 1 or (causal and Tk < Tq):
+        raise ValueError("need non-empty tensors and Tk >= Tq for the causal mask")
+    rows = np.arange(Tq)
+    out = np.empty((B, H, Tq, 2 * D))
+    for b in range(B):
+        for h in range(H):
+            w = _head_rows(q1[b, h], k1[b, h], q2[b, h], k2[b, h], rows, float(lam), causal, Tk - Tq)
+            out[b, h] = w @ v[b, h]
+    return out

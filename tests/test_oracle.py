@@ -183,8 +183,12 @@ def pin_lambda():
         oracle.differential_lambda([1, 2], [1], [1, 2], [1, 2])
 
 
+def pin_kv_decode():
+    test_kv_decode_brute_force()
+
+
 ALL_PINS = [pin_brute_force, pin_sdpa_lambda0, pin_row_sums, pin_identical_maps,
-            pin_value_offset, pin_closed_forms, pin_worked_example]
+            pin_value_offset, pin_closed_forms, pin_worked_example, pin_kv_decode]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS + [pin_lambda], ids=lambda f: f.__name__)
@@ -252,27 +256,27 @@ def _transposed_scores(q, k):
     return (k @ q.T) / math.sqrt(q.shape[-1])
 
 
-def _mask_diag_off(s, rows, causal):
+def _mask_diag_off(s, rows, causal, offset=0):
     if not causal:
         return s
     keys = np.arange(s.shape[-1])
     out = s.copy()
-    out[keys[None, :] >= rows[:, None]] = -np.inf
+    out[keys[None, :] >= rows[:, None] + offset] = -np.inf
     out[np.all(np.isinf(out), axis=-1)] = 0.0
     return out
 
 
-def _mask_upper_kept(s, rows, causal):
+def _mask_upper_kept(s, rows, causal, offset=0):
     if not causal:
         return s
     keys = np.arange(s.shape[-1])
     out = s.copy()
-    out[keys[None, :] < rows[:, None]] = -np.inf
+    out[keys[None, :] < rows[:, None] + offset] = -np.inf
     return out
 
 
-def _mask_branch1_only(q1, k1, q2, k2, rows, lam, causal):
-    a1 = O._softmax(O._mask(O._scores(q1[rows], k1), rows, causal))
+def _mask_branch1_only(q1, k1, q2, k2, rows, lam, causal, offset=0):
+    a1 = O._softmax(O._mask(O._scores(q1[rows], k1), rows, causal, offset))
     a2 = O._softmax(O._scores(q2[rows], k2))
     return O._combine(a1, a2, lam)
 
@@ -364,3 +368,52 @@ def test_head_norm_invariants():
     assert np.max(np.abs(oracle.head_norm(o, "none", out_scale=0.25) - 0.25 * o)) <= 0
     with pytest.raises(ValueError):
         oracle.head_norm(o, "layer")
+
+
+# ---------------------------------------------------------------------------
+# Decode over a KV cache (Tq queries at the end of Tk keys)
+# ---------------------------------------------------------------------------
+
+def brute_force_kv(q1, k1, q2, k2, v, lam, causal):
+    B, H, Tq, D = q1.shape
+    Tk = k1.shape[2]
+    out = np.zeros((B, H, Tq, v.shape[-1]))
+    for b in range(B):
+        for h in range(H):
+            for i in range(Tq):
+                pos = Tk - Tq + i
+                visible = [j for j in range(Tk) if (not causal) or j <= pos]
+                weights = [0.0] * Tk
+                for q, k, sign in ((q1, k1, 1.0), (q2, k2, -lam)):
+                    logit = {j: sum(float(q[b, h, i, c]) * float(k[b, h, j, c]) for c in range(D)) / math.sqrt(D)
+                             for j in visible}
+                    top = max(logit.values())
+                    z = sum(math.exp(x - top) for x in logit.values())
+                    for j in visible:
+                        weights[j] += sign * math.exp(logit[j] - top) / z
+                for c in range(v.shape[-1]):
+                    out[b, h, i, c] = sum(weights[j] * float(v[b, h, j, c]) for j in range(Tk))
+    return out
+
+
+def test_kv_decode_brute_force():
+    rng = np.random.default_rng(50)
+    for (Tq, Tk) in [(1, 7), (2, 9), (3, 3), (1, 1)]:
+        q1, q2 = rng.standard_normal((2, 1, 2, Tq, 4))
+        k1, k2 = rng.standard_normal((2, 1, 2, Tk, 4))
+        v = rng.standard_normal((1, 2, Tk, 8))
+        for lam in (0.0, 0.8, -0.4):
+            for causal in (True, False):
+                got = oracle.differential_attention_kv(q1, k1, q2, k2, v, lam, causal)
+                ref = brute_force_kv(q1, k1, q2, k2, v, lam, causal)
+                assert np.max(np.abs(got - ref)) <= 1e-12, (Tq, Tk, lam, causal)
+
+
+def test_kv_decode_rows_match_full_sequence():
+    """Decode of the last Tq positions equals those rows of the full causal pass."""
+    q1, k1, q2, k2, v = rand_inputs(1, 2, 40, 8, 51)
+    full = oracle.differential_attention(q1, k1, q2, k2, v, 0.6, True)
+    dec = oracle.differential_attention_kv(q1[:, :, -3:], k1, q2[:, :, -3:], k2, v, 0.6, True)
+    assert np.max(np.abs(dec - full[:, :, -3:])) <= 1e-13
+    with pytest.raises(ValueError):
+        oracle.differential_attention_kv(q1, k1[:, :, :5], q2, k2[:, :, :5], v[:, :, :5], 0.6, True)
