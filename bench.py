@@ -454,6 +454,77 @@ def run_e2e(args, w, lib, da, _lib, host, lam_vecs_host, lam_init, d_in, d_lv, d
             "ms_per_step": 1e3 * max_s / steps}
 
 
+def run_decode(args, world, rank, local):
+    """Decode (Tq queries over a Tk-key cache): HBM-bound, so the metric is
+    algorithmic GB/s (K1, K2, V read once; Q read and O written once)."""
+    import torch
+    import differential_attention_fwd_gb300 as da
+    from differential_attention_fwd_gb300 import _lib
+    from differential_attention_fwd_gb300 import build as build_mod
+
+    build_mod.build()
+    lib = _lib.load()
+    w = W.DECODE_WORKLOADS[args.decode_workload]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    inp = W.draw_kv(w)
+    d_in = [torch.from_numpy(x).to(dev, tdt) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    d_out = torch.empty((w.B, w.H, w.Tq, w.Dv), dtype=tdt, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    desc = da.make_kv_desc(*d_in, d_out)
+    need = int(lib.diffattn_decode_workspace_bytes(ctypes.byref(desc)))
+    ws = torch.empty(need // 4 + 4, dtype=torch.float32, device=dev)
+    ptrs = [ctypes.c_void_p(t.data_ptr()) for t in d_in]
+
+    def step():
+        rc = lib.diffattn_decode(ctypes.byref(desc), *ptrs, ctypes.c_float(w.lambda_value), None,
+                                 1 if w.causal else 0, None, ctypes.c_void_p(d_out.data_ptr()),
+                                 ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(need),
+                                 ctypes.c_void_p(stream.cuda_stream))
+        if rc:
+            raise _lib.DiffattnError(rc, "diffattn_decode")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local) if (args.clocks and rank == 0) else None
+    barrier(world)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms = [a.elapsed_time(b) for a, b in ev]
+    max_s = reduce_max(sum(ms) / 1e3, world)
+    peaks, src = load_peaks()
+    gbs = w.bytes / statistics.mean(ms) * 1e3 / 1e9
+    return {
+        "metric": f"diffattn_decode HBM GB/s (B={w.B},H={w.H},Tq={w.Tq},Tk={w.Tk},D={w.D})",
+        "value": w.bytes * args.steps * world / max_s / 1e9, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Tq": w.Tq, "Tk": w.Tk, "D": w.D,
+                   "causal": w.causal, "lambda": w.lambda_value, "gbytes_per_step": w.bytes / 1e9,
+                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "parallelism": "replicas"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                     "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                     "peak_source": f"{src} hbm_gbs (copy bandwidth)"},
+        "gpu_launches": 2 * args.steps, "clocks": clocks,
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -466,6 +537,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    ap.add_argument("--mode", choices=["forward", "decode"], default="forward")
+    ap.add_argument("--decode-workload", default="decode_b16h16q1k8192", choices=sorted(W.DECODE_WORKLOADS))
     ap.add_argument("--norm", choices=["none", "rms", "group"], default="none",
                     help="fuse a per-head norm and the (1 - lambda_init) multiplier")
     args = ap.parse_args(argv)
@@ -479,6 +552,14 @@ def main(argv=None):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     w = W.WORKLOADS[args.workload]
+    if args.mode == "decode" and args.impl == "ours":
+        res = run_decode(args, world, rank, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     if args.impl == "reference":
         res = run_reference(args, w, world, rank)
     else:

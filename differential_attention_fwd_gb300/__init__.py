@@ -23,10 +23,12 @@ import torch
 from . import _lib
 from ._lib import (DIFFATTN_BF16, DIFFATTN_F32, DIFFATTN_KERNEL_SIMT,  # noqa: F401
                    DIFFATTN_KERNEL_TCGEN05, DIFFATTN_NORM_GROUP, DIFFATTN_NORM_NONE,
-                   DIFFATTN_NORM_RMS, DiffattnDesc, DiffattnEpilogue, DiffattnError)
+                   DIFFATTN_NORM_RMS, DiffattnDesc, DiffattnEpilogue, DiffattnError,
+                   DiffattnKvDesc)
 
-__all__ = ["differential_lambda", "differential_attention", "make_desc", "select_kernel",
-           "get_device_error", "version", "DiffattnError"]
+__all__ = ["differential_lambda", "differential_attention", "differential_attention_decode",
+           "make_desc", "make_kv_desc", "select_kernel", "get_device_error", "version",
+           "DiffattnError"]
 
 _DTYPES = {torch.bfloat16: DIFFATTN_BF16, torch.float32: DIFFATTN_F32}
 
@@ -211,6 +213,89 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
                                  ctypes.c_size_t(ws.numel() * 4 if ws is not None else 0),
                                  ctypes.c_void_p(stream.cuda_stream))
     _lib.check(rc, "diffattn_fwd")
+    return out
+
+
+def make_kv_desc(q1, k1, q2, k2, v, out) -> DiffattnKvDesc:
+    """Fill a diffattn_kv_desc from tensors."""
+    B, H, Tq, D = q1.shape
+    d = DiffattnKvDesc()
+    d.B, d.H, d.Tq, d.Tk, d.D = B, H, Tq, k1.shape[2], D
+    d.dtype = _DTYPES[q1.dtype]
+    d.reserved = 0
+    for field, t in (("q1_stride", q1), ("k1_stride", k1), ("q2_stride", q2), ("k2_stride", k2),
+                     ("v_stride", v), ("o_stride", out)):
+        s = t.stride()
+        getattr(d, field)[:] = (s[0], s[1], s[2])
+    return d
+
+
+_DECODE_WS = {}
+
+
+def decode_workspace_for(device: torch.device, stream, nbytes: int) -> torch.Tensor:
+    """A per-(device, stream) decode workspace of at least nbytes (grown on
+    demand; its contents need no initialisation)."""
+    key = (device.index, int(stream.cuda_stream))
+    ws = _DECODE_WS.get(key)
+    if ws is None or ws.numel() * 4 < nbytes:
+        ws = torch.empty((nbytes + 15) // 4 + 4, dtype=torch.float32, device=device)
+        _DECODE_WS[key] = ws
+    return ws
+
+
+def differential_attention_decode(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
+                                  k2: torch.Tensor, value: torch.Tensor, coefficient,
+                                  causal: bool = True, out: Optional[torch.Tensor] = None,
+                                  norm: Optional[str] = None, norm_eps: float = 1e-5,
+                                  norm_weight: Optional[torch.Tensor] = None,
+                                  norm_bias: Optional[torch.Tensor] = None,
+                                  out_scale: float = 1.0) -> torch.Tensor:
+    """Decode: Tq new queries q1, q2 [B, H, Tq, D] over cached keys k1, k2
+    [B, H, Tk, D] and values [B, H, Tk, 2D].  With causal=True query i sits at
+    position Tk - Tq + i.  Epilogue arguments as differential_attention.
+    Returns [B, H, Tq, 2D].  (Forward only.)"""
+    ts = [q1, k1, q2, k2, value]
+    for n, t in zip(("q1", "k1", "q2", "k2", "value"), ts):
+        _require_cuda(t, n)
+        if t.dim() != 4:
+            raise ValueError(f"{n} must be 4-D")
+    B, H, Tq, D = q1.shape
+    Tk = k1.shape[2]
+    if q2.shape != q1.shape or k1.shape != k2.shape or tuple(k1.shape) != (B, H, Tk, D) or \
+            tuple(value.shape) != (B, H, Tk, 2 * D):
+        raise ValueError("expected q1, q2 [B, H, Tq, D], k1, k2 [B, H, Tk, D], value [B, H, Tk, 2D]")
+    dt, dev = q1.dtype, q1.device
+    if dt not in _DTYPES or any(t.dtype != dt or t.device != dev for t in ts):
+        raise ValueError("inputs must share one dtype (bfloat16 or float32) and device")
+    ts = [t if t.stride(-1) == 1 else t.contiguous() for t in ts]
+    q1, k1, q2, k2, value = ts
+    if out is None:
+        out = torch.empty((B, H, Tq, 2 * D), dtype=dt, device=dev)
+    lam_host, lam_dev = 0.0, None
+    if isinstance(coefficient, torch.Tensor):
+        if coefficient.device.type == "cuda":
+            lam_dev = coefficient.detach().reshape(()).to(torch.float32)
+        else:
+            lam_host = float(coefficient.item())
+    else:
+        lam_host = float(coefficient)
+    d = make_kv_desc(q1, k1, q2, k2, value, out)
+    epi = _epilogue(norm, norm_eps, norm_weight, norm_bias, out_scale, H, 2 * D, dev)
+    lib = _lib.load()
+    need = int(lib.diffattn_decode_workspace_bytes(ctypes.byref(d)))
+    if need == 0:
+        raise DiffattnError(_lib.DIFFATTN_ERR_UNSUPPORTED, "diffattn_decode_workspace_bytes")
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev)
+        ws = decode_workspace_for(dev, stream, need)
+        rc = lib.diffattn_decode(ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in ts),
+                                 ctypes.c_float(lam_host),
+                                 ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0),
+                                 1 if causal else 0, ctypes.byref(epi[0]) if epi else None,
+                                 ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                                 ctypes.c_size_t(ws.numel() * 4), ctypes.c_void_p(stream.cuda_stream))
+    _lib.check(rc, "diffattn_decode")
     return out
 
 

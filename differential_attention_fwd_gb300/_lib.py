@@ -28,6 +28,8 @@ EXPORTED = (
     "diffattn_lambda",
     "diffattn_fwd",
     "diffattn_fwd_ex",
+    "diffattn_decode",
+    "diffattn_decode_workspace_bytes",
     "diffattn_workspace_bytes",
     "diffattn_select_kernel",
     "diffattn_get_device_error",
@@ -41,6 +43,17 @@ class DiffattnDesc(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64), ("D", ctypes.c_int64),
         ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("q1_stride", ctypes.c_int64 * 3), ("k1_stride", ctypes.c_int64 * 3),
+        ("q2_stride", ctypes.c_int64 * 3), ("k2_stride", ctypes.c_int64 * 3),
+        ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+    ]
+
+
+class DiffattnKvDesc(ctypes.Structure):
+    """Mirror of diffattn_kv_desc."""
+    _fields_ = [
+        ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("Tq", ctypes.c_int64), ("Tk", ctypes.c_int64),
+        ("D", ctypes.c_int64), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
         ("q1_stride", ctypes.c_int64 * 3), ("k1_stride", ctypes.c_int64 * 3),
         ("q2_stride", ctypes.c_int64 * 3), ("k2_stride", ctypes.c_int64 * 3),
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
@@ -83,6 +96,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                     vp, ctypes.c_int, ctypes.POINTER(DiffattnEpilogue), vp, vp,
                                     ctypes.c_size_t, vp]
     lib.diffattn_fwd_ex.restype = ctypes.c_int
+    lib.diffattn_decode.argtypes = [ctypes.POINTER(DiffattnKvDesc), vp, vp, vp, vp, vp, ctypes.c_float,
+                                    vp, ctypes.c_int, ctypes.POINTER(DiffattnEpilogue), vp, vp,
+                                    ctypes.c_size_t, vp]
+    lib.diffattn_decode.restype = ctypes.c_int
+    lib.diffattn_decode_workspace_bytes.argtypes = [ctypes.POINTER(DiffattnKvDesc)]
+    lib.diffattn_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.diffattn_workspace_bytes.argtypes = []
     lib.diffattn_workspace_bytes.restype = ctypes.c_size_t
     lib.diffattn_fwd.restype = ctypes.c_int

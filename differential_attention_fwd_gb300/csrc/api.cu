@@ -133,6 +133,50 @@ void copy3(int64_t dst[3], const int64_t src[3]) {
     dst[2] = src[2];
 }
 
+// Checks of a decode descriptor that need no pointers; fills the key-range
+// split plan.
+struct DecodePlan {
+    int tq_bucket = 0, splits = 0, split_len = 0;
+    size_t work_bytes = 0;
+};
+
+int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
+    if (!d) return DIFFATTN_ERR_INVALID;
+    if (d->B < 1 || d->H < 1 || d->Tq < 1 || d->Tk < 1 || d->D < 1) return DIFFATTN_ERR_INVALID;
+    if (d->dtype != DIFFATTN_BF16 && d->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID;
+    if (d->reserved != 0) return DIFFATTN_ERR_INVALID;
+    if (!strides_nonneg(d->q1_stride) || !strides_nonneg(d->k1_stride) ||
+        !strides_nonneg(d->q2_stride) || !strides_nonneg(d->k2_stride) ||
+        !strides_nonneg(d->v_stride) || !strides_nonneg(d->o_stride))
+        return DIFFATTN_ERR_INVALID;
+    if (causal && d->Tk < d->Tq) return DIFFATTN_ERR_INVALID;
+    if (d->D != 32 && d->D != 64 && d->D != 128) return DIFFATTN_ERR_UNSUPPORTED;
+    if (d->Tk > INT32_MAX / 2 || d->Tq > 8) return DIFFATTN_ERR_UNSUPPORTED;
+    const int tqb = decode_tq_bucket((int)d->Tq, (int)d->D);
+    if (tqb == 0) return DIFFATTN_ERR_UNSUPPORTED;
+    const int64_t BH = d->B * d->H;
+    if (BH > (1ll << 24)) return DIFFATTN_ERR_UNSUPPORTED;
+    // Split every head's keys so that the whole launch has ~1024 CTAs, with
+    // at least 256 keys (one chunk) per split.
+    const int64_t chunks = (d->Tk + 255) / 256;
+    int64_t splits = (1024 + BH - 1) / BH;
+    if (splits > chunks) splits = chunks;
+    if (splits < 1) splits = 1;
+    const int64_t split_len = ((chunks + splits - 1) / splits) * 256;
+    splits = (d->Tk + split_len - 1) / split_len;
+    if (BH * splits > INT32_MAX || BH * d->Tq > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
+    plan->tq_bucket = tqb;
+    plan->splits = (int)splits;
+    plan->split_len = (int)split_len;
+    plan->work_bytes = decode_work_floats(d->B, d->H, (int)splits, tqb, d->D) * sizeof(float);
+    return DIFFATTN_OK;
+}
+
+bool kv_aligned(const void* p, const int64_t s[3], size_t esize) {
+    return aligned16(p) && (s[0] * (int64_t)esize) % 16 == 0 && (s[1] * (int64_t)esize) % 16 == 0 &&
+           (s[2] * (int64_t)esize) % 16 == 0;
+}
+
 }  // namespace
 }  // namespace diffattn
 
@@ -274,6 +318,74 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
     p.out_scale = e.out_scale;
     rc = (d.dtype == DIFFATTN_F32) ? launch_fwd_simt_f32(p, st) : launch_fwd_simt_bf16(p, st);
     return rc == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+size_t diffattn_decode_workspace_bytes(const diffattn_kv_desc* desc) {
+    DecodePlan plan;
+    // The plan does not depend on the mask; check the shape with it off.
+    if (plan_decode(desc, 0, &plan) != DIFFATTN_OK) return 0;
+    return plan.work_bytes;
+}
+
+int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1, const void* q2,
+                    const void* k2, const void* v, float lambda, const float* lambda_dev,
+                    int causal, const diffattn_epilogue* epi, void* out, void* workspace,
+                    size_t workspace_bytes, diffattn_stream_t stream) {
+    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID;
+    DecodePlan plan;
+    int rc = plan_decode(desc, causal, &plan);
+    if (rc != DIFFATTN_OK) return rc;
+    if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
+    if (!workspace || workspace_bytes < plan.work_bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
+        return DIFFATTN_ERR_INVALID;
+    diffattn_epilogue e{DIFFATTN_NORM_NONE, 0.f, nullptr, nullptr, 1.0f, 0};
+    if (epi) {
+        e = *epi;
+        if (e.reserved != 0 || e.norm < DIFFATTN_NORM_NONE || e.norm > DIFFATTN_NORM_GROUP ||
+            !std::isfinite(e.out_scale) ||
+            (e.norm != DIFFATTN_NORM_NONE && !(std::isfinite(e.eps) && e.eps > 0.f)))
+            return DIFFATTN_ERR_INVALID;
+    }
+    const diffattn_kv_desc& d = *desc;
+    const size_t esize = d.dtype == DIFFATTN_BF16 ? 2 : 4;
+    if (!kv_aligned(k1, d.k1_stride, esize) || !kv_aligned(k2, d.k2_stride, esize) ||
+        !kv_aligned(v, d.v_stride, esize))
+        return DIFFATTN_ERR_UNSUPPORTED;
+    DecodeParams p;
+    p.B = (int)d.B;
+    p.H = (int)d.H;
+    p.Tq = (int)d.Tq;
+    p.Tk = (int)d.Tk;
+    p.D = (int)d.D;
+    p.causal = causal ? 1 : 0;
+    p.bf16 = d.dtype == DIFFATTN_BF16 ? 1 : 0;
+    p.tq_bucket = plan.tq_bucket;
+    p.splits = plan.splits;
+    p.split_len = plan.split_len;
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.D));
+    p.lambda = lambda;
+    p.lambda_dev = lambda_dev;
+    p.q1 = q1;
+    p.k1 = k1;
+    p.q2 = q2;
+    p.k2 = k2;
+    p.v = v;
+    p.out = out;
+    copy3(p.s_q1, d.q1_stride);
+    copy3(p.s_k1, d.k1_stride);
+    copy3(p.s_q2, d.q2_stride);
+    copy3(p.s_k2, d.k2_stride);
+    copy3(p.s_v, d.v_stride);
+    copy3(p.s_o, d.o_stride);
+    p.work = static_cast<float*>(workspace);
+    p.norm = e.norm;
+    p.norm_eps = e.eps;
+    p.norm_weight = e.weight;
+    p.norm_bias = e.bias;
+    p.out_scale = e.out_scale;
+    return launch_decode(p, reinterpret_cast<cudaStream_t>(stream)) == 0 ? DIFFATTN_OK
+                                                                       : DIFFATTN_ERR_CUDA;
 }
 
 int diffattn_get_device_error(diffattn_stream_t stream) {

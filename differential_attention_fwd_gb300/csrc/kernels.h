@@ -52,7 +52,35 @@ struct SimtParams {
     float out_scale;
 };
 
+// Parameters of the decode kernels (Tq queries over Tk cached keys).
+struct DecodeParams {
+    int B, H, Tq, Tk, D;
+    int causal;
+    int bf16;               // element type: 1 bf16, 0 fp32
+    int tq_bucket;          // Tq rounded up to 1, 2, 4 or 8
+    int splits;             // key-range splits per head
+    int split_len;          // keys per split (multiple of 256)
+    float scale_log2;       // log2(e) / sqrt(D)
+    float lambda;
+    const float* lambda_dev;
+    const void* q1; const void* k1; const void* q2; const void* k2; const void* v;
+    void* out;
+    int64_t s_q1[3], s_k1[3], s_q2[3], s_k2[3], s_v[3], s_o[3];
+    float* work;            // partial results, decode_work_floats(...) floats
+    int norm;
+    float norm_eps;
+    const float* norm_weight;
+    const float* norm_bias;
+    float out_scale;
+};
+
+// Decode helpers: query-count bucket (0 if Tq is too large for D), and the
+// number of workspace floats for a launch.
+int decode_tq_bucket(int Tq, int D);
+size_t decode_work_floats(int64_t B, int64_t H, int splits, int tq_bucket, int64_t D);
+
 // Each returns 0 on success, -1 if the launch failed.
+int launch_decode(const DecodeParams& p, cudaStream_t stream);
 int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v,out*/, const TcParams& p, int grid,
                   cudaStream_t stream);
 int launch_fwd_simt_f32(const SimtParams& p, cudaStream_t stream);

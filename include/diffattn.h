@@ -189,6 +189,62 @@ int diffattn_fwd_ex(const diffattn_desc *desc, const void *q1, const void *k1,
                     diffattn_stream_t stream);
 
 /*
+ * Decode over a key/value cache: Tq new queries against Tk cached keys.
+ * Q1, Q2: [B, H, Tq, D]; K1, K2: [B, H, Tk, D]; V: [B, H, Tk, 2D]; O: [B, H,
+ * Tq, 2D].  Strides as in diffattn_desc ([0] = B, [1] = H, [2] = the sequence
+ * dimension), innermost stride 1.
+ */
+typedef struct {
+    int64_t B, H, Tq, Tk, D;
+    int32_t dtype;
+    int32_t reserved;          /* must be 0 */
+    int64_t q1_stride[3];
+    int64_t k1_stride[3];
+    int64_t q2_stride[3];
+    int64_t k2_stride[3];
+    int64_t v_stride[3];
+    int64_t o_stride[3];
+} diffattn_kv_desc;
+
+/*
+ * diffattn_decode_workspace_bytes -- bytes of device workspace diffattn_decode
+ * needs for this descriptor (partial results of the key-range splits), or 0
+ * if the descriptor is invalid or unsupported.
+ */
+size_t diffattn_decode_workspace_bytes(const diffattn_kv_desc *desc);
+
+/*
+ * diffattn_decode -- O = (softmax(Q1 K1^T / sqrt(D) + M) - lambda
+ * softmax(Q2 K2^T / sqrt(D) + M)) V for Tq queries over Tk cached keys, then
+ * the optional epilogue `epi` (as in diffattn_fwd_ex; NULL = none).
+ *
+ * causal: non-zero places query i at position Tk - Tq + i and masks keys
+ * j > Tk - Tq + i in both branches (requires Tk >= Tq); zero lets every query
+ * see every key.
+ * workspace: device memory of at least diffattn_decode_workspace_bytes(desc)
+ * bytes, 16-byte aligned, owned by the caller; its contents need no
+ * initialisation and are overwritten.  Calls that may run at the same time on
+ * the GPU must use different workspaces.
+ * Other arguments as diffattn_fwd.
+ *
+ * Supported: dtype bf16 or fp32; D in {32, 64, 128}; Tq <= 8 (D <= 64) or
+ * Tq <= 4 (D = 128); K1, K2 and V with 16-byte aligned base pointers and
+ * strides that are multiples of 16 bytes.  Two kernel launches per call (the
+ * key-range splits, then their combination).  Work is bound by reading K1,
+ * K2 and V once.
+ * Errors: DIFFATTN_ERR_INVALID (NULL pointers, sizes < 1, Tk < Tq with the
+ * causal mask, unknown dtype, negative strides, non-zero reserved field,
+ * non-finite lambda, bad epilogue, missing, small or misaligned workspace);
+ * DIFFATTN_ERR_UNSUPPORTED (D, Tq or alignment outside the supported set);
+ * DIFFATTN_ERR_CUDA (launch failure).
+ */
+int diffattn_decode(const diffattn_kv_desc *desc, const void *q1, const void *k1,
+                    const void *q2, const void *k2, const void *v, float lambda,
+                    const float *lambda_dev, int causal, const diffattn_epilogue *epi,
+                    void *out, void *workspace, size_t workspace_bytes,
+                    diffattn_stream_t stream);
+
+/*
  * diffattn_select_kernel -- which kernel diffattn_fwd would launch for this
  * descriptor and these pointers (DIFFATTN_KERNEL_*), or a negative error code
  * if the arguments are invalid.  Host only; touches no GPU state.

@@ -172,3 +172,41 @@ def test_bad_epilogue_rejected(lib, field, value):
     rc = lib.diffattn_fwd_ex(ctypes.byref(desc()), *ptrs(5), ctypes.c_float(0.5), None, 1,
                              ctypes.byref(e), ctypes.c_void_p(FAKE * 9), None, 0, None)
     assert rc == _lib.DIFFATTN_ERR_INVALID
+
+
+def kv_desc(B=2, H=3, Tq=1, Tk=1000, D=64, dtype=_lib.DIFFATTN_BF16):
+    d = _lib.DiffattnKvDesc()
+    d.B, d.H, d.Tq, d.Tk, d.D, d.dtype, d.reserved = B, H, Tq, Tk, D, dtype, 0
+    for f, T, w in (("q1_stride", Tq, D), ("q2_stride", Tq, D), ("k1_stride", Tk, D),
+                    ("k2_stride", Tk, D), ("v_stride", Tk, 2 * D), ("o_stride", Tq, 2 * D)):
+        getattr(d, f)[:] = (H * T * w, T * w, w)
+    return d
+
+
+def test_decode_workspace_query(lib):
+    d = kv_desc()
+    n = lib.diffattn_decode_workspace_bytes(ctypes.byref(d))
+    assert n > 0 and n % 4 == 0
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tk=100000))) >= n
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=48))) == 0
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=9))) == 0
+    assert lib.diffattn_decode_workspace_bytes(None) == 0
+
+
+@pytest.mark.parametrize("kw,code", [(dict(Tq=0), _lib.DIFFATTN_ERR_INVALID),
+                                     (dict(D=40), _lib.DIFFATTN_ERR_UNSUPPORTED),
+                                     (dict(Tq=5, D=128), _lib.DIFFATTN_ERR_UNSUPPORTED),
+                                     (dict(Tq=4, Tk=3), _lib.DIFFATTN_ERR_INVALID)])
+def test_decode_rejects(lib, kw, code):
+    d = kv_desc(**kw)
+    ws = ctypes.c_void_p(FAKE * 20)
+    rc = lib.diffattn_decode(ctypes.byref(d), *ptrs(5), ctypes.c_float(0.5), None, 1, None,
+                             ctypes.c_void_p(FAKE * 9), ws, 1 << 30, None)
+    assert rc == code
+
+
+def test_decode_requires_workspace(lib):
+    d = kv_desc()
+    rc = lib.diffattn_decode(ctypes.byref(d), *ptrs(5), ctypes.c_float(0.5), None, 1, None,
+                             ctypes.c_void_p(FAKE * 9), None, 0, None)
+    assert rc == _lib.DIFFATTN_ERR_INVALID

@@ -1,0 +1,90 @@
+"""GPU parity of the decode path (Tq queries over a Tk-key cache, split-KV
+kernels) against the float64 oracle's differential_attention_kv."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+import differential_attention_fwd_gb300 as da
+from differential_attention_fwd_gb300 import build as build_mod
+from tests.helpers import assert_close, to_device, to_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_mod.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def run(inp, dtype, lam, causal, **kw):
+    dev = [to_device(x, dtype) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    return da.differential_attention_decode(*dev, lam, causal=causal, **kw), dev
+
+
+@pytest.mark.parametrize("Tq,Tk", [(1, 1), (1, 100), (1, 256), (1, 257), (2, 1000), (3, 4099),
+                                   (4, 8192), (5, 300), (8, 2048), (1, 70000)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_decode_bf16_d64(Tq, Tk, causal):
+    w = W.DecodeWorkload("t", 2, 3, Tq, Tk, 64, "bf16", causal, seed=Tq * 7 + Tk)
+    inp = W.draw_kv(w)
+    out, _ = run(inp, "bf16", 0.7, causal)
+    ref = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.7, causal)
+    assert_close(to_numpy(out), ref, "bf16", f"decode Tq={Tq} Tk={Tk} causal={causal}")
+
+
+@pytest.mark.parametrize("dtype,D,Tq", [("f32", 64, 1), ("f32", 32, 8), ("f32", 128, 4),
+                                        ("bf16", 32, 3), ("bf16", 128, 2)])
+def test_decode_other_shapes(dtype, D, Tq):
+    w = W.DecodeWorkload("t", 1, 2, Tq, 1500, D, dtype, True, seed=D + Tq)
+    inp = W.draw_kv(w)
+    for causal in (True, False):
+        out, _ = run(inp, dtype, -0.3, causal)
+        ref = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, -0.3, causal)
+        assert_close(to_numpy(out), ref, dtype, f"decode {dtype} D={D} Tq={Tq}")
+
+
+def test_decode_matches_forward_last_rows():
+    inp = W.draw(W.Workload("t", B=1, H=2, T=700, D=64, dtype="bf16", causal=True, seed=9))
+    dev = [to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    full = da.differential_attention(*dev, 0.5, causal=True)
+    dec = da.differential_attention_decode(dev[0][:, :, -3:], dev[1], dev[2][:, :, -3:], dev[3],
+                                           dev[4], 0.5, causal=True)
+    assert float((full[:, :, -3:].float() - dec.float()).abs().max()) <= 2e-2
+
+
+def test_decode_epilogue_and_device_lambda():
+    w = W.DecodeWorkload("t", 2, 4, 2, 3000, 64, "bf16", True, seed=33)
+    inp = W.draw_kv(w)
+    rng = np.random.default_rng(1)
+    wt = (1 + 0.1 * rng.standard_normal((4, 128))).astype(np.float32)
+    lam_t = torch.tensor(0.6, device="cuda")
+    out, _ = run(inp, "bf16", lam_t, True, norm="rms", norm_weight=torch.from_numpy(wt).cuda(),
+                 out_scale=0.4)
+    o = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.6, True)
+    assert_close(to_numpy(out), oracle.head_norm(o, "rms", 1e-5, wt, None, 0.4), "bf16", "decode rms")
+    assert da.get_device_error() == 0
+
+
+def test_decode_workloads_sampled():
+    for w in W.DECODE_WORKLOADS.values():
+        inp = W.draw_kv(w, B=2)      # two of the sequences, full cache length
+        out, _ = run(inp, w.dtype, w.lambda_value, w.causal)
+        ref = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v,
+                                               w.lambda_value, w.causal)
+        assert_close(to_numpy(out), ref, w.dtype, w.name)
+
+
+def test_decode_unsupported_and_invalid():
+    x = torch.zeros(1, 1, 9, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 1, 100, 64, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(1, 1, 100, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(da.DiffattnError):        # Tq > 8
+        da.differential_attention_decode(x, k, x, k, v, 0.5)
+    x = torch.zeros(1, 1, 2, 48, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 1, 100, 48, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(1, 1, 100, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(da.DiffattnError):        # D not in {32, 64, 128}
+        da.differential_attention_decode(x, k, x, k, v, 0.5)

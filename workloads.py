@@ -178,3 +178,57 @@ def check_rows(T: int, extra: Sequence[int] = (), n_random: int = 0,
         rng = np.random.Generator(np.random.PCG64(seed))
         rows.update(int(r) for r in rng.integers(0, T, size=n_random))
     return np.array(sorted(r for r in rows if 0 <= r < T), dtype=np.int64)
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """Tq new queries over a cache of Tk keys (decode)."""
+    name: str
+    B: int
+    H: int
+    Tq: int
+    Tk: int
+    D: int
+    dtype: str
+    causal: bool
+    seed: int
+    lambda_value: float = 0.8
+
+    @property
+    def Dv(self) -> int:
+        return 2 * self.D
+
+    @property
+    def bytes(self) -> int:
+        """Algorithmic HBM bytes: K1, K2, V read once; Q1, Q2 read, O written."""
+        el = 2 if self.dtype == "bf16" else 4
+        return self.B * self.H * (self.Tk * 4 * self.D + self.Tq * 4 * self.D) * el
+
+
+# Decode workloads: 16 sequences with 16 heads (the V1 layout halves the heads
+# of a 32-head model), D = 64, an 8192-token cache; one query, and four
+# (speculative decoding).
+DECODE_WORKLOADS = {
+    "decode_b16h16q1k8192": DecodeWorkload("decode_b16h16q1k8192", 16, 16, 1, 8192, 64, "bf16", True, 20),
+    "decode_b16h16q4k8192": DecodeWorkload("decode_b16h16q4k8192", 16, 16, 4, 8192, 64, "bf16", True, 21),
+}
+
+
+def draw_kv(w: DecodeWorkload, **override) -> Inputs:
+    """Decode inputs: q1, q2 [B, H, Tq, D]; k1, k2 [B, H, Tk, D]; v [B, H, Tk, 2D];
+    i.i.d. N(0, 1) float32 drawn in the order q1, k1, q2, k2, v from PCG64(seed),
+    rounded to the dtype.  The lambda vectors are left zero (lambda is given
+    directly for decode workloads)."""
+    f = dict(B=w.B, H=w.H, Tq=w.Tq, Tk=w.Tk, D=w.D, dtype=w.dtype, seed=w.seed)
+    f.update(override)
+    rng = np.random.Generator(np.random.PCG64(f["seed"]))
+    B, H, Tq, Tk, D = f["B"], f["H"], f["Tq"], f["Tk"], f["D"]
+    q1 = rng.standard_normal((B, H, Tq, D), dtype=np.float32)
+    k1 = rng.standard_normal((B, H, Tk, D), dtype=np.float32)
+    q2 = rng.standard_normal((B, H, Tq, D), dtype=np.float32)
+    k2 = rng.standard_normal((B, H, Tk, D), dtype=np.float32)
+    v = rng.standard_normal((B, H, Tk, 2 * D), dtype=np.float32)
+    if f["dtype"] == "bf16":
+        q1, k1, q2, k2, v = (round_to_bf16(a) for a in (q1, k1, q2, k2, v))
+    z = np.zeros(D, dtype=np.float32)
+    return Inputs(q1, k1, q2, k2, v, z, z, z, z)
