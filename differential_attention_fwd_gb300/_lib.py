@@ -30,6 +30,7 @@ EXPORTED = (
     "diffattn_fwd_ex",
     "diffattn_decode",
     "diffattn_decode_workspace_bytes",
+    "diffattn_decode_noalloc",
     "diffattn_workspace_bytes",
     "diffattn_select_kernel",
     "diffattn_get_device_error",
@@ -100,6 +101,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                     vp, ctypes.c_int, ctypes.POINTER(DiffattnEpilogue), vp, vp,
                                     ctypes.c_size_t, vp]
     lib.diffattn_decode.restype = ctypes.c_int
+    lib.diffattn_decode_noalloc.argtypes = [ctypes.POINTER(DiffattnKvDesc), vp, vp, vp, vp, vp,
+                                            ctypes.c_float, vp, ctypes.c_int,
+                                            ctypes.POINTER(DiffattnEpilogue), vp, vp]
+    lib.diffattn_decode_noalloc.restype = ctypes.c_int
     lib.diffattn_decode_workspace_bytes.argtypes = [ctypes.POINTER(DiffattnKvDesc)]
     lib.diffattn_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.diffattn_workspace_bytes.argtypes = []

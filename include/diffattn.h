@@ -245,6 +245,33 @@ int diffattn_decode(const diffattn_kv_desc *desc, const void *q1, const void *k1
                     diffattn_stream_t stream);
 
 /*
+ * diffattn_decode_noalloc -- diffattn_decode for callers that cannot allocate
+ * device memory when they run the decode step (an inference runtime or plug-in
+ * host that owns every buffer and passes only inputs and outputs, a process
+ * held to a fixed device-memory budget, or a latency-critical loop that must
+ * not call the allocator, which may synchronise the device).  There is no
+ * counterpart on the pages; this is a library convenience.
+ *
+ * Same arguments as diffattn_decode without the workspace: the partial results
+ * of the key-range splits go to a scratch buffer of 8 MiB (8388608 bytes) that
+ * is part of the library; every GPU that loads the library holds one such
+ * buffer until the process exits.  The call allocates nothing.  The first call
+ * on a device looks up the buffer's device address (once per device, with that
+ * device current); make that first call before capturing any stream.
+ * Every call shares the one buffer: calls that run on the GPU at the same time
+ * race and corrupt each other's results.  The buffer needs no clearing; each
+ * call writes everything it reads.
+ * Errors: as diffattn_decode, and DIFFATTN_ERR_UNSUPPORTED when the problem
+ * needs more than 8 MiB of partial results (diffattn_decode_workspace_bytes
+ * reports the need; use diffattn_decode with a workspace instead).
+ */
+int diffattn_decode_noalloc(const diffattn_kv_desc *desc, const void *q1,
+                            const void *k1, const void *q2, const void *k2,
+                            const void *v, float lambda, const float *lambda_dev,
+                            int causal, const diffattn_epilogue *epi, void *out,
+                            diffattn_stream_t stream);
+
+/*
  * diffattn_select_kernel -- which kernel diffattn_fwd would launch for this
  * descriptor and these pointers (DIFFATTN_KERNEL_*), or a negative error code
  * if the arguments are invalid.  Host only; touches no GPU state.
