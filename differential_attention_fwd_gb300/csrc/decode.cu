@@ -215,7 +215,26 @@ decode_partial_kernel(const DecodeParams p) {
                 for (int c = 0; c < DPL; ++c) acc[q][br][c] *= a;
             }
         const int nk = min(CHUNK, k_end - c0);
-        for (int t = warp; t < nk; t += WARPS) {
+        int t = warp;
+        // UNROLL value rows in flight per warp before they are used
+        constexpr int UNROLL = (TQ * DPL <= 16) ? 8 : 4;
+        for (; t + (UNROLL - 1) * WARPS < nk; t += UNROLL * WARPS) {
+            float x[UNROLL][DPL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u)
+                load_cols<T, DPL>(v + (int64_t)(c0 + t + u * WARPS) * p.s_v[2] + lane * DPL, x[u]);
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u)
+#pragma unroll
+                for (int q = 0; q < TQ; ++q)
+#pragma unroll
+                    for (int br = 0; br < 2; ++br) {
+                        const float w = sc[((t + u * WARPS) * TQ + q) * 2 + br];
+#pragma unroll
+                        for (int c = 0; c < DPL; ++c) acc[q][br][c] = fmaf(w, x[u][c], acc[q][br][c]);
+                    }
+        }
+        for (; t < nk; t += WARPS) {
             float x[DPL];
             load_cols<T, DPL>(v + (int64_t)(c0 + t) * p.s_v[2] + lane * DPL, x);
 #pragma unroll
