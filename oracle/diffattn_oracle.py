@@ -130,28 +130,35 @@ def _as64(x) -> np.ndarray:
 
 
 def _check_shapes(q1, k1, q2, k2, v=None):
-    if not (q1.shape == k1.shape == q2.shape == k2.shape):
-        raise ValueError("Q1, K1, Q2, K2 must share one shape [B, H, T, D]")
-    if q1.ndim != 4 or min(q1.shape) < 1:
+    """Q1, Q2: [B, H, T, D]; K1, K2: [B, H_kv, T, D]; V: [B, H_kv, T, 2D] with
+    H a multiple of H_kv (query heads share key/value heads in groups of
+    H / H_kv, the grouped layout of DIFF V2; H_kv = H is the plain layout).
+    Returns the group size H / H_kv."""
+    if q1.shape != q2.shape or k1.shape != k2.shape:
+        raise ValueError("Q1, Q2 must share one shape, and K1, K2 another")
+    if q1.ndim != 4 or k1.ndim != 4 or min(q1.shape) < 1 or min(k1.shape) < 1:
         raise ValueError("expected non-empty [B, H, T, D] tensors")
-    if v is not None:
-        B, H, T, D = q1.shape
-        if v.shape != (B, H, T, 2 * D):
-            raise ValueError("V must be [B, H, T, 2D]")
+    B, H, T, D = q1.shape
+    Hk = k1.shape[1]
+    if k1.shape[0] != B or k1.shape[2:] != (T, D) or H % Hk != 0:
+        raise ValueError("K1/K2 must be [B, H_kv, T, D] with H a multiple of H_kv")
+    if v is not None and v.shape != (B, Hk, T, 2 * D):
+        raise ValueError("V must be [B, H_kv, T, 2D]")
+    return H // Hk
 
 
 def softmax_maps(q1, k1, q2, k2, causal: bool = True):
     """The two attention maps A_1, A_2 as [B, H, T, T] float64 (small inputs)."""
     q1, k1, q2, k2 = (_as64(x) for x in (q1, k1, q2, k2))
-    _check_shapes(q1, k1, q2, k2)
+    g = _check_shapes(q1, k1, q2, k2)
     B, H, T, _ = q1.shape
     rows = np.arange(T)
     a1 = np.empty((B, H, T, T))
     a2 = np.empty((B, H, T, T))
     for b in range(B):
         for h in range(H):
-            a1[b, h] = _softmax(_mask(_scores(q1[b, h], k1[b, h]), rows, causal))
-            a2[b, h] = _softmax(_mask(_scores(q2[b, h], k2[b, h]), rows, causal))
+            a1[b, h] = _softmax(_mask(_scores(q1[b, h], k1[b, h // g]), rows, causal))
+            a2[b, h] = _softmax(_mask(_scores(q2[b, h], k2[b, h // g]), rows, causal))
     return a1, a2
 
 
@@ -167,9 +174,10 @@ def differential_attention(q1, k1, q2, k2, v, lam: float, causal: bool = True,
                            block: int = 256) -> np.ndarray:
     """O = (A_1 - lambda A_2) V in float64.
 
-    q1, k1, q2, k2: [B, H, T, D]; v: [B, H, T, 2D] (any real dtype, upcast to
-    float64).  lam: the scalar lambda.  causal: apply the causal mask to both
-    branches.
+    q1, q2: [B, H, T, D]; k1, k2: [B, H_kv, T, D]; v: [B, H_kv, T, 2D] (any
+    real dtype, upcast to float64), H a multiple of H_kv: query head h uses
+    key/value head h // (H / H_kv).  lam: the scalar lambda.  causal: apply the
+    causal mask to both branches.
 
     rows: optional query rows to evaluate (every row when None).  Every output
     row depends only on its own query row and all keys/values of its head, so
@@ -179,7 +187,7 @@ def differential_attention(q1, k1, q2, k2, v, lam: float, causal: bool = True,
     Returns [B, H, R, 2D] for all heads, or [len(heads), R, 2D] when heads is
     given.  Query rows are processed `block` at a time only to bound memory.
     """
-    _check_shapes(q1, k1, q2, k2, v)
+    g = _check_shapes(q1, k1, q2, k2, v)
     B, H, T, D = q1.shape
     lam = float(lam)
     row_idx = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
@@ -188,7 +196,8 @@ def differential_attention(q1, k1, q2, k2, v, lam: float, causal: bool = True,
     head_list = [(b, h) for b in range(B) for h in range(H)] if heads is None else list(heads)
     out = np.empty((len(head_list), row_idx.size, 2 * D))
     for n, (b, h) in enumerate(head_list):
-        hq1, hk1, hq2, hk2, hv = (_as64(x[b, h]) for x in (q1, k1, q2, k2, v))
+        hq1, hq2 = _as64(q1[b, h]), _as64(q2[b, h])
+        hk1, hk2, hv = (_as64(x[b, h // g]) for x in (k1, k2, v))
         for r0 in range(0, row_idx.size, block):
             r = row_idx[r0:r0 + block]
             out[n, r0:r0 + block] = _head_rows(hq1, hk1, hq2, hk2, r, lam, causal) @ hv
@@ -239,24 +248,28 @@ def differential_attention_kv(q1, k1, q2, k2, v, lam: float, causal: bool = True
     """O = (A_1 - lambda A_2) V for Tq queries against Tk >= Tq keys (decode
     over a KV cache), in float64.
 
-    q1, q2: [B, H, Tq, D]; k1, k2: [B, H, Tk, D]; v: [B, H, Tk, 2D].  With the
-    causal mask, query i sits at position Tk - Tq + i of the key sequence and
+    q1, q2: [B, H, Tq, D]; k1, k2: [B, H_kv, Tk, D]; v: [B, H_kv, Tk, 2D], H a
+    multiple of H_kv (query head h reads key/value head h // (H / H_kv)).  With
+    the causal mask, query i sits at position Tk - Tq + i of the key sequence and
     sees keys j <= Tk - Tq + i (the usual KV-cache alignment; for Tq = Tk it is
     the causal mask of differential_attention).  Returns [B, H, Tq, 2D].
     """
     q1, k1, q2, k2, v = (_as64(x) for x in (q1, k1, q2, k2, v))
     if q1.shape != q2.shape or k1.shape != k2.shape or q1.ndim != 4 or k1.ndim != 4:
-        raise ValueError("Q1/Q2 must be [B, H, Tq, D] and K1/K2 [B, H, Tk, D]")
+        raise ValueError("Q1/Q2 must be [B, H, Tq, D] and K1/K2 [B, H_kv, Tk, D]")
     B, H, Tq, D = q1.shape
-    Tk = k1.shape[2]
-    if k1.shape[:2] != (B, H) or k1.shape[3] != D or v.shape != (B, H, Tk, 2 * D):
+    Hk, Tk = k1.shape[1], k1.shape[2]
+    if (k1.shape[0] != B or Hk < 1 or H % Hk != 0 or k1.shape[3] != D
+            or v.shape != (B, Hk, Tk, 2 * D)):
         raise ValueError("inconsistent shapes")
+    g = H // Hk
     if min(B, H, Tq, D, Tk) < 1 or (causal and Tk < Tq):
         raise ValueError("need non-empty tensors and Tk >= Tq for the causal mask")
     rows = np.arange(Tq)
     out = np.empty((B, H, Tq, 2 * D))
     for b in range(B):
         for h in range(H):
-            w = _head_rows(q1[b, h], k1[b, h], q2[b, h], k2[b, h], rows, float(lam), causal, Tk - Tq)
-            out[b, h] = w @ v[b, h]
+            w = _head_rows(q1[b, h], k1[b, h // g], q2[b, h], k2[b, h // g], rows, float(lam),
+                           causal, Tk - Tq)
+            out[b, h] = w @ v[b, h // g]
     return out

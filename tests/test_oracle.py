@@ -417,3 +417,48 @@ def test_kv_decode_rows_match_full_sequence():
     assert np.max(np.abs(dec - full[:, :, -3:])) <= 1e-13
     with pytest.raises(ValueError):
         oracle.differential_attention_kv(q1, k1[:, :, :5], q2, k2[:, :, :5], v[:, :, :5], 0.6, True)
+
+
+# ---------------------------------------------------------------------------
+# Grouped key/value heads (DIFF V2 layout: H query heads over H_kv KV heads)
+# ---------------------------------------------------------------------------
+
+def test_grouped_heads_lambda0_matches_torch_gqa():
+    rng = np.random.default_rng(60)
+    q1, q2 = rng.standard_normal((2, 2, 6, 20, 8))
+    k1, k2 = rng.standard_normal((2, 2, 2, 20, 8))
+    v = rng.standard_normal((2, 2, 20, 16))
+    for causal in (True, False):
+        got = oracle.differential_attention(q1, k1, q2, k2, v, 0.0, causal)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q1), torch.from_numpy(k1), torch.from_numpy(v), is_causal=causal,
+            enable_gqa=True).numpy()
+        assert np.max(np.abs(got - ref)) <= 1e-12
+
+
+def test_grouped_heads_brute_force():
+    rng = np.random.default_rng(61)
+    q1, q2 = rng.standard_normal((2, 1, 4, 6, 4))
+    k1, k2 = rng.standard_normal((2, 1, 2, 6, 4))
+    v = rng.standard_normal((1, 2, 6, 8))
+    for causal in (True, False):
+        got = oracle.differential_attention(q1, k1, q2, k2, v, 0.8, causal)
+        # brute force per query head on the key/value head it shares
+        for h in range(4):
+            ref = brute_force(q1[:, h:h + 1], k1[:, h // 2:h // 2 + 1], q2[:, h:h + 1],
+                              k2[:, h // 2:h // 2 + 1], v[:, h // 2:h // 2 + 1], 0.8, causal)
+            assert np.max(np.abs(got[:, h:h + 1] - ref)) <= 1e-12
+    with pytest.raises(ValueError):
+        oracle.differential_attention(q1[:, :3], k1, q2[:, :3], k2, v, 0.8)
+
+
+def test_grouped_heads_kv_cache_matches_full_sequence_rows():
+    # Tq queries at the end of Tk keys with grouped heads equal the last Tq rows
+    # of the full-sequence forward with the same grouping
+    rng = np.random.default_rng(62)
+    q1, q2 = rng.standard_normal((2, 1, 6, 12, 4))
+    k1, k2 = rng.standard_normal((2, 1, 3, 12, 4))
+    v = rng.standard_normal((1, 3, 12, 8))
+    full = oracle.differential_attention(q1, k1, q2, k2, v, 0.6, True)
+    tail = oracle.differential_attention_kv(q1[:, :, -3:], k1, q2[:, :, -3:], k2, v, 0.6, True)
+    assert np.max(np.abs(full[:, :, -3:] - tail)) <= 1e-12
