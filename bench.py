@@ -259,7 +259,8 @@ def lambda_for(w, inp) -> float:
 
 
 def config_of(w, lam):
-    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "D": w.D, "Dv": w.Dv,
+    grouped = {"H_kv": w.Hk, "shared_keys": w.shared_keys} if (w.Hk != w.H or w.shared_keys) else {}
+    return {"workload": w.name, "B": w.B, "H": w.H, **grouped, "T": w.T, "D": w.D, "Dv": w.Dv,
             "causal": w.causal, "lambda_init": W.lambda_init_for(w) if not w.lambdas else None,
             "lambda": lam, "gflop_per_step": w.flops / 1e9,
             "l2": "flushed between steps (256 MiB write outside the timed events); "
@@ -268,8 +269,11 @@ def config_of(w, lam):
 
 
 def input_bytes(w):
+    """Bytes of Q1, Q2 (H heads) and K1, K2, V (H_kv heads; one key tensor
+    when the branches share it)."""
     el = 2 if w.dtype == "bf16" else 4
-    return w.B * w.H * w.T * (4 * w.D + 2 * w.D) * el
+    k_tensors = 1 if w.shared_keys else 2
+    return w.B * w.T * (w.H * 2 * w.D + w.Hk * (k_tensors * w.D + 2 * w.D)) * el
 
 
 # --------------------------------------------------------------------------
@@ -292,6 +296,9 @@ def run_ours(args, w, world, rank, local):
     lam_init = W.lambda_init_for(w) if not w.lambdas else 0.0
     host = [torch.from_numpy(x).to(tdt) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
     d_in = [h.to(dev) for h in host]
+    if w.shared_keys:
+        # one key tensor for both branches: the library sees the same pointer
+        host[3], d_in[3] = host[1], d_in[1]
     d_lv = [v.to(dev) for v in lam_vecs_host]
     d_lam = torch.empty((), dtype=torch.float32, device=dev)
     d_out = torch.empty((w.B, w.H, w.T, w.Dv), dtype=tdt, device=dev)
@@ -408,17 +415,21 @@ def run_e2e(args, w, lib, da, _lib, host, lam_vecs_host, lam_init, d_in, d_lv, d
             desc, launches_per_step, flush, stream, world, ws):
     """Same metric, inputs from pinned host memory, output back to the host."""
     import torch
-    pin = [h.pin_memory() for h in host]
+    # one copy per distinct device input (a shared key tensor is copied once)
+    uniq = []
+    for d, h in zip(d_in, host):
+        if all(d is not u for u, _ in uniq):
+            uniq.append((d, h.pin_memory()))
     pin_lv = [v.pin_memory() for v in lam_vecs_host]
     out_host = torch.empty(d_out.shape, dtype=d_out.dtype).pin_memory()
     steps = max(1, min(args.steps, args.e2e_steps))
-    h2d = sum(t.numel() * t.element_size() for t in pin)
+    h2d = sum(h.numel() * h.element_size() for _, h in uniq)
     if launches_per_step == 2:
         h2d += sum(t.numel() * t.element_size() for t in pin_lv)
     d2h = out_host.numel() * out_host.element_size()
 
     def one():
-        for d, h in zip(d_in, pin):
+        for d, h in uniq:
             d.copy_(h, non_blocking=True)
         if launches_per_step == 2:
             for d, h in zip(d_lv, pin_lv):
@@ -508,13 +519,14 @@ def run_decode(args, world, rank, local):
     max_s = reduce_max(sum(ms) / 1e3, world)
     peaks, src = load_peaks()
     gbs = w.bytes / statistics.mean(ms) * 1e3 / 1e9
+    hk = f",H_kv={w.Hk}" if w.Hk != w.H else ""
     return {
-        "metric": f"diffattn_decode HBM GB/s (B={w.B},H={w.H},Tq={w.Tq},Tk={w.Tk},D={w.D})",
+        "metric": f"diffattn_decode HBM GB/s (B={w.B},H={w.H}{hk},Tq={w.Tq},Tk={w.Tk},D={w.D})",
         "value": w.bytes * args.steps * world / max_s / 1e9, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Tq": w.Tq, "Tk": w.Tk, "D": w.D,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hk, "Tq": w.Tq, "Tk": w.Tk, "D": w.D,
                    "causal": w.causal, "lambda": w.lambda_value, "gbytes_per_step": w.bytes / 1e9,
                    "l2": "flushed between steps (256 MiB write outside the timed events)",
                    "parallelism": "replicas"},
@@ -531,7 +543,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.ALL_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
@@ -551,7 +563,7 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    w = W.WORKLOADS[args.workload]
+    w = W.ALL_WORKLOADS[args.workload]
     if args.mode == "decode" and args.impl == "ours":
         res = run_decode(args, world, rank, local)
         if rank == 0:

@@ -94,12 +94,13 @@ def differential_lambda(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor, k2
 
 
 def make_desc(q1, k1, q2, k2, v, out) -> DiffattnDesc:
-    """Fill a diffattn_desc from tensors (sizes, dtype, B/H/T element strides)."""
+    """Fill a diffattn_desc from tensors (sizes, dtype, B/H/T element strides;
+    kv_group = query heads per key/value head)."""
     B, H, T, D = q1.shape
     d = DiffattnDesc()
     d.B, d.H, d.T, d.D = B, H, T, D
     d.dtype = _DTYPES[q1.dtype]
-    d.reserved = 0
+    d.kv_group = H // k1.shape[1]
     for field, t in (("q1_stride", q1), ("k1_stride", k1), ("q2_stride", q2), ("k2_stride", k2),
                      ("v_stride", v), ("o_stride", out)):
         s = t.stride()
@@ -114,11 +115,15 @@ def _prepare(q1, k1, q2, k2, value):
         _require_cuda(t, n)
         if t.dim() != 4:
             raise ValueError(f"{n} must be 4-D [B, H, T, *]")
-    if not (q1.shape == k1.shape == q2.shape == k2.shape):
-        raise ValueError("q1, k1, q2, k2 must share one shape [B, H, T, D]")
+    if q1.shape != q2.shape or k1.shape != k2.shape:
+        raise ValueError("q1, q2 must share one shape [B, H, T, D], and k1, k2 another")
     B, H, T, D = q1.shape
-    if tuple(value.shape) != (B, H, T, 2 * D):
-        raise ValueError(f"value must be [B, H, T, 2D] = {(B, H, T, 2 * D)}, got {tuple(value.shape)}")
+    Hk = k1.shape[1]
+    if k1.shape[0] != B or tuple(k1.shape[2:]) != (T, D) or Hk < 1 or H % Hk != 0:
+        raise ValueError(f"k1, k2 must be [B, H_kv, T, D] with H_kv dividing H = {H}, "
+                         f"got {tuple(k1.shape)}")
+    if tuple(value.shape) != (B, Hk, T, 2 * D):
+        raise ValueError(f"value must be [B, H_kv, T, 2D] = {(B, Hk, T, 2 * D)}, got {tuple(value.shape)}")
     dt = q1.dtype
     if dt not in _DTYPES:
         raise ValueError(f"unsupported dtype {dt}; expected bfloat16 or float32")
@@ -154,9 +159,12 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
                            out_scale: float = 1.0) -> torch.Tensor:
     """O = (softmax(Q1 K1^T/sqrt(D) + M) - lambda softmax(Q2 K2^T/sqrt(D) + M)) V.
 
-    q1, k1, q2, k2: [B, H, T, D]; value: [B, H, T, 2D]; all bfloat16 or all
-    float32 on one CUDA device, innermost dimension contiguous (other strides
-    are passed through).  coefficient: lambda, a Python number or a scalar
+    q1, q2: [B, H, T, D]; k1, k2: [B, H_kv, T, D]; value: [B, H_kv, T, 2D];
+    all bfloat16 or all float32 on one CUDA device, innermost dimension
+    contiguous (other strides are passed through).  H_kv must divide H: query
+    head h reads key/value head h // (H // H_kv) (grouped key/value heads;
+    H_kv = H is the plain layout).  Passing the same tensor as k1 and k2
+    shares the keys between the branches.  coefficient: lambda, a Python number or a scalar
     tensor (a CUDA float32 scalar is read by the kernel without a host sync).
     causal: mask key j > query i in both branches.  out: optional preallocated
     [B, H, T, 2D] output of the same dtype.  dynamic_schedule: hand out work
@@ -222,7 +230,7 @@ def make_kv_desc(q1, k1, q2, k2, v, out) -> DiffattnKvDesc:
     d = DiffattnKvDesc()
     d.B, d.H, d.Tq, d.Tk, d.D = B, H, Tq, k1.shape[2], D
     d.dtype = _DTYPES[q1.dtype]
-    d.reserved = 0
+    d.kv_group = H // k1.shape[1]
     for field, t in (("q1_stride", q1), ("k1_stride", k1), ("q2_stride", q2), ("k2_stride", k2),
                      ("v_stride", v), ("o_stride", out)):
         s = t.stride()
@@ -252,8 +260,9 @@ def differential_attention_decode(q1: torch.Tensor, k1: torch.Tensor, q2: torch.
                                   norm_bias: Optional[torch.Tensor] = None,
                                   out_scale: float = 1.0) -> torch.Tensor:
     """Decode: Tq new queries q1, q2 [B, H, Tq, D] over cached keys k1, k2
-    [B, H, Tk, D] and values [B, H, Tk, 2D].  With causal=True query i sits at
-    position Tk - Tq + i.  Epilogue arguments as differential_attention.
+    [B, H_kv, Tk, D] and values [B, H_kv, Tk, 2D] (H_kv dividing H; query head
+    h reads key/value head h // (H // H_kv)).  With causal=True query i sits
+    at position Tk - Tq + i.  Epilogue arguments as differential_attention.
     Returns [B, H, Tq, 2D].  (Forward only.)"""
     ts = [q1, k1, q2, k2, value]
     for n, t in zip(("q1", "k1", "q2", "k2", "value"), ts):
@@ -261,10 +270,11 @@ def differential_attention_decode(q1: torch.Tensor, k1: torch.Tensor, q2: torch.
         if t.dim() != 4:
             raise ValueError(f"{n} must be 4-D")
     B, H, Tq, D = q1.shape
-    Tk = k1.shape[2]
-    if q2.shape != q1.shape or k1.shape != k2.shape or tuple(k1.shape) != (B, H, Tk, D) or \
-            tuple(value.shape) != (B, H, Tk, 2 * D):
-        raise ValueError("expected q1, q2 [B, H, Tq, D], k1, k2 [B, H, Tk, D], value [B, H, Tk, 2D]")
+    Hk, Tk = k1.shape[1], k1.shape[2]
+    if q2.shape != q1.shape or k1.shape != k2.shape or tuple(k1.shape) != (B, Hk, Tk, D) or \
+            H % Hk != 0 or tuple(value.shape) != (B, Hk, Tk, 2 * D):
+        raise ValueError("expected q1, q2 [B, H, Tq, D], k1, k2 [B, H_kv, Tk, D], "
+                         "value [B, H_kv, Tk, 2D] with H_kv dividing H")
     dt, dev = q1.dtype, q1.device
     if dt not in _DTYPES or any(t.dtype != dt or t.device != dev for t in ts):
         raise ValueError("inputs must share one dtype (bfloat16 or float32) and device")

@@ -43,7 +43,7 @@ class DiffattnDesc(ctypes.Structure):
     """Mirror of diffattn_desc."""
     _fields_ = [
         ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64), ("D", ctypes.c_int64),
-        ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("kv_group", ctypes.c_int32),
         ("q1_stride", ctypes.c_int64 * 3), ("k1_stride", ctypes.c_int64 * 3),
         ("q2_stride", ctypes.c_int64 * 3), ("k2_stride", ctypes.c_int64 * 3),
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
@@ -54,7 +54,7 @@ class DiffattnKvDesc(ctypes.Structure):
     """Mirror of diffattn_kv_desc."""
     _fields_ = [
         ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("Tq", ctypes.c_int64), ("Tk", ctypes.c_int64),
-        ("D", ctypes.c_int64), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("D", ctypes.c_int64), ("dtype", ctypes.c_int32), ("kv_group", ctypes.c_int32),
         ("q1_stride", ctypes.c_int64 * 3), ("k1_stride", ctypes.c_int64 * 3),
         ("q2_stride", ctypes.c_int64 * 3), ("k2_stride", ctypes.c_int64 * 3),
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),

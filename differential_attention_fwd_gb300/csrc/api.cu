@@ -67,12 +67,23 @@ int device_state(DeviceState** out) {
 
 bool strides_nonneg(const int64_t s[3]) { return s[0] >= 0 && s[1] >= 0 && s[2] >= 0; }
 
+// Query heads per key/value head: 0 and 1 both mean one each.
+int64_t group_of(int32_t kv_group) { return kv_group > 1 ? kv_group : 1; }
+
+// K1 and K2 are the same tensor (same base and the same strides on every
+// dimension that is stepped).
+bool same_tensor(const void* a, const int64_t sa[3], const void* b, const int64_t sb[3],
+                 int64_t B, int64_t Hk, int64_t T) {
+    return a == b && (B == 1 || sa[0] == sb[0]) && (Hk == 1 || sa[1] == sb[1]) &&
+           (T == 1 || sa[2] == sb[2]);
+}
+
 int validate(const diffattn_desc* d, const void* q1, const void* k1, const void* q2,
              const void* k2, const void* v, const void* out) {
     if (!d || !q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID;
     if (d->B < 1 || d->H < 1 || d->T < 1 || d->D < 1 || d->D > 128) return DIFFATTN_ERR_INVALID;
     if (d->dtype != DIFFATTN_BF16 && d->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID;
-    if (d->reserved != 0) return DIFFATTN_ERR_INVALID;
+    if (d->kv_group < 0 || d->H % group_of(d->kv_group) != 0) return DIFFATTN_ERR_INVALID;
     if (!strides_nonneg(d->q1_stride) || !strides_nonneg(d->k1_stride) ||
         !strides_nonneg(d->q2_stride) || !strides_nonneg(d->k2_stride) ||
         !strides_nonneg(d->v_stride) || !strides_nonneg(d->o_stride))
@@ -91,31 +102,32 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool tc_stride_ok(int64_t stride, int64_t size) {
     return size == 1 || (stride > 0 && stride % 8 == 0 && stride < (int64_t(1) << 38));
 }
-bool tc_strides_ok(const int64_t s[3], const diffattn_desc* d) {
-    return tc_stride_ok(s[0], d->B) && tc_stride_ok(s[1], d->H) && tc_stride_ok(s[2], d->T);
+bool tc_strides_ok(const int64_t s[3], const diffattn_desc* d, int64_t heads) {
+    return tc_stride_ok(s[0], d->B) && tc_stride_ok(s[1], heads) && tc_stride_ok(s[2], d->T);
 }
 
 int select(const diffattn_desc* d, const void* q1, const void* k1, const void* q2,
            const void* k2, const void* v, const void* out) {
+    const int64_t hk = d->H / group_of(d->kv_group);
     if (d->dtype == DIFFATTN_BF16 && d->D == 64 && aligned16(q1) && aligned16(k1) &&
         aligned16(q2) && aligned16(k2) && aligned16(v) && aligned16(out) &&
-        tc_strides_ok(d->q1_stride, d) && tc_strides_ok(d->k1_stride, d) &&
-        tc_strides_ok(d->q2_stride, d) && tc_strides_ok(d->k2_stride, d) &&
-        tc_strides_ok(d->v_stride, d) && tc_strides_ok(d->o_stride, d))
+        tc_strides_ok(d->q1_stride, d, d->H) && tc_strides_ok(d->k1_stride, d, hk) &&
+        tc_strides_ok(d->q2_stride, d, d->H) && tc_strides_ok(d->k2_stride, d, hk) &&
+        tc_strides_ok(d->v_stride, d, hk) && tc_strides_ok(d->o_stride, d, d->H))
         return DIFFATTN_KERNEL_TCGEN05;
     return DIFFATTN_KERNEL_SIMT;
 }
 
-// 4-D bf16 tensor map {inner, T, H, B} with a {box_inner, box_rows, 1, 1} box
-// and 128-byte swizzling; rows past T read as zeros.
+// 4-D bf16 tensor map {inner, T, heads, B} with a {box_inner, box_rows, 1, 1}
+// box and 128-byte swizzling; rows past T read as zeros.
 int encode_map(CUtensorMap* m, const void* base, int64_t inner, const diffattn_desc* d,
-               const int64_t s[3], uint32_t box_inner, uint32_t box_rows) {
+               int64_t heads, const int64_t s[3], uint32_t box_inner, uint32_t box_rows) {
     int64_t sT = s[2], sH = s[1], sB = s[0];
     // A size-1 dimension is never stepped; give it a stride the encoder accepts.
     if (d->T == 1) sT = inner;
-    if (d->H == 1) sH = sT * d->T;
-    if (d->B == 1) sB = sH * d->H;
-    const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)d->T, (cuuint64_t)d->H,
+    if (heads == 1) sH = sT * d->T;
+    if (d->B == 1) sB = sH * heads;
+    const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)d->T, (cuuint64_t)heads,
                                 (cuuint64_t)d->B};
     const cuuint64_t strides[3] = {(cuuint64_t)sT * 2, (cuuint64_t)sH * 2, (cuuint64_t)sB * 2};
     const cuuint32_t box[4] = {box_inner, box_rows, 1, 1};
@@ -137,6 +149,7 @@ void copy3(int64_t dst[3], const int64_t src[3]) {
 // split plan.
 struct DecodePlan {
     int tq_bucket = 0, splits = 0, split_len = 0;
+    int kv_group = 1, Hk = 0, row_chunks = 0;
     size_t work_bytes = 0;
 };
 
@@ -144,31 +157,41 @@ int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
     if (!d) return DIFFATTN_ERR_INVALID;
     if (d->B < 1 || d->H < 1 || d->Tq < 1 || d->Tk < 1 || d->D < 1) return DIFFATTN_ERR_INVALID;
     if (d->dtype != DIFFATTN_BF16 && d->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID;
-    if (d->reserved != 0) return DIFFATTN_ERR_INVALID;
+    if (d->kv_group < 0 || d->H % group_of(d->kv_group) != 0) return DIFFATTN_ERR_INVALID;
     if (!strides_nonneg(d->q1_stride) || !strides_nonneg(d->k1_stride) ||
         !strides_nonneg(d->q2_stride) || !strides_nonneg(d->k2_stride) ||
         !strides_nonneg(d->v_stride) || !strides_nonneg(d->o_stride))
         return DIFFATTN_ERR_INVALID;
     if (causal && d->Tk < d->Tq) return DIFFATTN_ERR_INVALID;
     if (d->D != 32 && d->D != 64 && d->D != 128) return DIFFATTN_ERR_UNSUPPORTED;
-    if (d->Tk > INT32_MAX / 2 || d->Tq > 8) return DIFFATTN_ERR_UNSUPPORTED;
-    const int tqb = decode_tq_bucket((int)d->Tq, (int)d->D);
+    const int cap = decode_max_rows((int)d->D);
+    if (d->Tk > INT32_MAX / 2 || d->Tq > cap || d->H > (1 << 24)) return DIFFATTN_ERR_UNSUPPORTED;
+    // The query rows of the heads that share a key/value head (g * Tq of
+    // them) go in as few CTAs as the row capacity allows, evenly filled.
+    const int64_t g = group_of(d->kv_group);
+    const int64_t rows = g * d->Tq;
+    const int64_t row_chunks = (rows + cap - 1) / cap;
+    const int tqb = decode_tq_bucket((int)((rows + row_chunks - 1) / row_chunks), (int)d->D);
     if (tqb == 0) return DIFFATTN_ERR_UNSUPPORTED;
-    const int64_t BH = d->B * d->H;
-    if (BH > (1ll << 24)) return DIFFATTN_ERR_UNSUPPORTED;
+    const int64_t Hk = d->H / g;
+    const int64_t units = d->B * Hk * row_chunks;
+    if (units > (1ll << 24) || d->B * d->H > (1ll << 24)) return DIFFATTN_ERR_UNSUPPORTED;
     // Split every head's keys so that the whole launch has ~1024 CTAs, with
     // at least 256 keys (one chunk) per split.
     const int64_t chunks = (d->Tk + 255) / 256;
-    int64_t splits = (1024 + BH - 1) / BH;
+    int64_t splits = (1024 + units - 1) / units;
     if (splits > chunks) splits = chunks;
     if (splits < 1) splits = 1;
     const int64_t split_len = ((chunks + splits - 1) / splits) * 256;
     splits = (d->Tk + split_len - 1) / split_len;
-    if (BH * splits > INT32_MAX || BH * d->Tq > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
+    if (units * splits > INT32_MAX || d->B * d->H * d->Tq > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
     plan->tq_bucket = tqb;
     plan->splits = (int)splits;
     plan->split_len = (int)split_len;
-    plan->work_bytes = decode_work_floats(d->B, d->H, (int)splits, tqb, d->D) * sizeof(float);
+    plan->kv_group = (int)g;
+    plan->Hk = (int)Hk;
+    plan->row_chunks = (int)row_chunks;
+    plan->work_bytes = decode_work_floats(units, (int)splits, tqb, d->D) * sizeof(float);
     return DIFFATTN_OK;
 }
 
@@ -237,15 +260,18 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
 
     if (select(desc, q1, k1, q2, k2, v, out) == DIFFATTN_KERNEL_TCGEN05) {
         CUtensorMap maps[6];
+        const int64_t g = group_of(d.kv_group);
+        const int64_t hk = d.H / g;
         // Q tiles are 128 query rows; K and V tiles are 64 key rows; every box
         // is 64 elements (128 bytes) wide, the 128-byte swizzle span.  O is
-        // stored by each warp in 32-row x 64-column boxes.
-        if (encode_map(&maps[0], q1, 64, &d, d.q1_stride, 64, 128) != DIFFATTN_OK ||
-            encode_map(&maps[1], k1, 64, &d, d.k1_stride, 64, 64) != DIFFATTN_OK ||
-            encode_map(&maps[2], q2, 64, &d, d.q2_stride, 64, 128) != DIFFATTN_OK ||
-            encode_map(&maps[3], k2, 64, &d, d.k2_stride, 64, 64) != DIFFATTN_OK ||
-            encode_map(&maps[4], v, 128, &d, d.v_stride, 64, 64) != DIFFATTN_OK ||
-            encode_map(&maps[5], out, 128, &d, d.o_stride, 64, 32) != DIFFATTN_OK)
+        // stored by each warp in 32-row x 64-column boxes.  K1, K2 and V have
+        // H / kv_group heads.
+        if (encode_map(&maps[0], q1, 64, &d, d.H, d.q1_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&maps[1], k1, 64, &d, hk, d.k1_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[2], q2, 64, &d, d.H, d.q2_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&maps[3], k2, 64, &d, hk, d.k2_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[4], v, 128, &d, hk, d.v_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[5], out, 128, &d, d.H, d.o_stride, 64, 32) != DIFFATTN_OK)
             return DIFFATTN_ERR_CUDA;
         TcParams p;
         p.B = (int)d.B;
@@ -286,6 +312,8 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
         p.norm_weight = e.weight;
         p.norm_bias = e.bias;
         p.out_scale = e.out_scale;
+        p.kv_group = (int)g;
+        p.k_shared = same_tensor(k1, d.k1_stride, k2, d.k2_stride, d.B, hk, d.T) ? 1 : 0;
         const int grid = p.total_items < dev->num_sms ? p.total_items : dev->num_sms;
         return launch_fwd_tc(maps, p, grid, st) == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
     }
@@ -316,6 +344,7 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
     p.norm_weight = e.weight;
     p.norm_bias = e.bias;
     p.out_scale = e.out_scale;
+    p.kv_group = (int)group_of(d.kv_group);
     rc = (d.dtype == DIFFATTN_F32) ? launch_fwd_simt_f32(p, st) : launch_fwd_simt_bf16(p, st);
     return rc == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
@@ -360,6 +389,9 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
     p.D = (int)d.D;
     p.causal = causal ? 1 : 0;
     p.bf16 = d.dtype == DIFFATTN_BF16 ? 1 : 0;
+    p.kv_group = plan.kv_group;
+    p.Hk = plan.Hk;
+    p.row_chunks = plan.row_chunks;
     p.tq_bucket = plan.tq_bucket;
     p.splits = plan.splits;
     p.split_len = plan.split_len;

@@ -9,14 +9,20 @@
 // The work is bound by reading K1, K2 and V once (256 bytes per key and head
 // for D = 64 in bf16), so it runs on the CUDA cores with coalesced loads and
 // splits the keys of every head across CTAs:
-//   pass 1 (partial): CTA (b, h, split) walks its key range in chunks of 256
-//     keys: every thread scores one key against all queries of both branches,
+//   pass 1 (partial): CTA (b, key/value head, row chunk, split) walks its key
+//     range in chunks of 256 keys: every thread scores one key against all
+//     query rows of the CTA in both branches,
 //     the block keeps an online softmax per (query, branch) in log2 units, and
 //     every warp accumulates P V for its share of the keys, lanes spread over
 //     the output columns.  The split's (max, sum, unnormalised O) go to the
 //     workspace.
 //   pass 2 (combine): one block per (b, h, query) merges the splits, forms
 //     O1 / l1 - lambda O2 / l2 and applies the optional output epilogue.
+// Query rows: the kv_group query heads that share a key/value head (grouped
+// key/value heads, the DIFF V2 layout) contribute kv_group * Tq rows, row
+// (i, q) = i * Tq + q for the group's i-th head; they are cut into row_chunks
+// chunks of tq_bucket rows, so one pass over a head's cache serves up to
+// tq_bucket rows of several heads.
 #include "kernels.h"
 
 #include <cmath>
@@ -108,29 +114,40 @@ decode_partial_kernel(const DecodeParams p) {
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int split = blockIdx.x % p.splits;
-    const int bh = blockIdx.x / p.splits;
-    const int b = bh / p.H;
-    const int h = bh - b * p.H;
+    const int unit = blockIdx.x / p.splits;        // (b, key/value head, row chunk)
+    const int rc = unit % p.row_chunks;
+    const int bhk = unit / p.row_chunks;
+    const int b = bhk / p.Hk;
+    const int hk = bhk - b * p.Hk;
     const int k_begin = split * p.split_len;
     const int k_end = min(p.Tk, k_begin + p.split_len);
+    const int n_rows = p.kv_group * p.Tq;          // query rows of this key/value head
 
-    const T* q1 = static_cast<const T*>(p.q1) + b * p.s_q1[0] + h * p.s_q1[1];
-    const T* q2 = static_cast<const T*>(p.q2) + b * p.s_q2[0] + h * p.s_q2[1];
-    const T* k1 = static_cast<const T*>(p.k1) + b * p.s_k1[0] + h * p.s_k1[1];
-    const T* k2 = static_cast<const T*>(p.k2) + b * p.s_k2[0] + h * p.s_k2[1];
-    const T* v = static_cast<const T*>(p.v) + b * p.s_v[0] + h * p.s_v[1];
+    const T* k1 = static_cast<const T*>(p.k1) + b * p.s_k1[0] + hk * p.s_k1[1];
+    const T* k2 = static_cast<const T*>(p.k2) + b * p.s_k2[0] + hk * p.s_k2[1];
+    const T* v = static_cast<const T*>(p.v) + b * p.s_v[0] + hk * p.s_v[1];
 
-    // queries (rows past Tq are zero and never written back)
+    // query rows (rows past the group's last are zero and never written back)
     for (int i = tid; i < TQ * 2 * D; i += CHUNK) {
-        const int q = i / (2 * D), br = (i / D) & 1, d = i % D;
+        const int r = i / (2 * D), br = (i / D) & 1, d = i % D;
+        const int row = rc * TQ + r;
         float x = 0.f;
-        if (q < p.Tq) x = to_f((br ? q2 : q1)[(int64_t)q * (br ? p.s_q2[2] : p.s_q1[2]) + d]);
+        if (row < n_rows) {
+            const int h = hk * p.kv_group + row / p.Tq;
+            const int q = row % p.Tq;
+            x = br ? to_f(static_cast<const T*>(p.q2)[b * p.s_q2[0] + h * p.s_q2[1] + (int64_t)q * p.s_q2[2] + d])
+                   : to_f(static_cast<const T*>(p.q1)[b * p.s_q1[0] + h * p.s_q1[1] + (int64_t)q * p.s_q1[2] + d]);
+        }
         qs[i] = x;
     }
+
     if (tid < TQ * 2) {
         stat[2 * tid] = -INFINITY;   // running max (log2 units)
         stat[2 * tid + 1] = 0.f;     // running sum
     }
+    // last visible key of each row; causal: row (i, q) sits at position Tk - Tq + q
+    __shared__ int last_key[TQ];
+    if (tid < TQ) last_key[tid] = p.causal ? p.Tk - p.Tq + (rc * TQ + tid) % p.Tq : p.Tk;
     float acc[TQ][2][DPL];
 #pragma unroll
     for (int q = 0; q < TQ; ++q)
@@ -165,8 +182,7 @@ decode_partial_kernel(const DecodeParams p) {
         }
 #pragma unroll
         for (int q = 0; q < TQ; ++q) {
-            // causal: query q is at position Tk - Tq + q
-            const bool vis = key < k_end && (!p.causal || key <= p.Tk - p.Tq + q);
+            const bool vis = key < k_end && key <= last_key[q];
 #pragma unroll
             for (int br = 0; br < 2; ++br) {
                 const float x = vis ? s[q][br] * p.scale_log2 : -INFINITY;
@@ -258,7 +274,7 @@ decode_partial_kernel(const DecodeParams p) {
             for (int c = 0; c < DPL; ++c)
                 acc_red[((warp * TQ + q) * 2 + br) * DV + lane * DPL + c] = acc[q][br][c];
     __syncthreads();
-    float* part = p.work + ((int64_t)bh * p.splits + split) * TQ * (4 + 2 * DV);
+    float* part = p.work + ((int64_t)unit * p.splits + split) * TQ * (4 + 2 * DV);
     for (int i = tid; i < TQ * 2 * DV; i += CHUNK) {
         float sum = 0.f;
 #pragma unroll
@@ -285,7 +301,11 @@ decode_combine_kernel(const DecodeParams p) {
     const int bh = blockIdx.x / p.Tq;
     const int b = bh / p.H;
     const int h = bh - b * p.H;
-    const float* part = p.work + (int64_t)bh * p.splits * TQ * (4 + 2 * DV) + q * (4 + 2 * DV);
+    // where the partial kernel kept this (head, query) row
+    const int hk = h / p.kv_group;
+    const int row = (h - hk * p.kv_group) * p.Tq + q;
+    const int unit = (b * p.Hk + hk) * p.row_chunks + row / TQ;
+    const float* part = p.work + (int64_t)unit * p.splits * TQ * (4 + 2 * DV) + (row % TQ) * (4 + 2 * DV);
     const int64_t sstride = (int64_t)TQ * (4 + 2 * DV);
     float val[2];
 #pragma unroll
@@ -341,7 +361,7 @@ int launch_tq(const DecodeParams& p, cudaStream_t stream) {
     if (cudaFuncSetAttribute(decode_partial_kernel<T, D, TQ>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return -1;
-    decode_partial_kernel<T, D, TQ><<<p.B * p.H * p.splits, CHUNK, smem, stream>>>(p);
+    decode_partial_kernel<T, D, TQ><<<p.B * p.Hk * p.row_chunks * p.splits, CHUNK, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return -1;
     decode_combine_kernel<T, D, TQ><<<p.B * p.H * p.Tq, DV, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
@@ -368,15 +388,17 @@ int launch_t(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace dec
 
-int decode_tq_bucket(int Tq, int D) {
-    const int cap = D <= 64 ? 8 : 4;
+int decode_max_rows(int D) { return D <= 64 ? 8 : 4; }
+
+int decode_tq_bucket(int rows, int D) {
+    const int cap = decode_max_rows(D);
     for (int t = 1; t <= cap; t *= 2)
-        if (Tq <= t) return t;
+        if (rows <= t) return t;
     return 0;
 }
 
-size_t decode_work_floats(int64_t B, int64_t H, int splits, int tq_bucket, int64_t D) {
-    return (size_t)B * H * splits * tq_bucket * (4 + 4 * D);
+size_t decode_work_floats(int64_t units, int splits, int tq_bucket, int64_t D) {
+    return (size_t)units * splits * tq_bucket * (4 + 4 * D);
 }
 
 int launch_decode(const DecodeParams& p, cudaStream_t stream) {

@@ -9,7 +9,8 @@
 // chunks of 32, one key per lane for the two dot products; each branch keeps
 // a streaming-softmax state (running max, running sum) and its own output
 // accumulator, each lane holding the output columns lane, lane+32, ...
-// Masked keys (causal: key > query) are skipped.
+// Masked keys (causal: key > query) are skipped.  With grouped key/value
+// heads, query head h reads key/value head h / kv_group.
 #include "kernels.h"
 
 #include <cmath>
@@ -57,10 +58,11 @@ diffattn_fwd_simt_kernel(const SimtParams p) {
     if (i >= p.T) return;   // whole warp leaves together
 
     const T* q1 = static_cast<const T*>(p.q1) + b * p.s_q1[0] + h * p.s_q1[1];
-    const T* k1 = static_cast<const T*>(p.k1) + b * p.s_k1[0] + h * p.s_k1[1];
+    const int hk = h / p.kv_group;   // key/value head of this query head
+    const T* k1 = static_cast<const T*>(p.k1) + b * p.s_k1[0] + hk * p.s_k1[1];
     const T* q2 = static_cast<const T*>(p.q2) + b * p.s_q2[0] + h * p.s_q2[1];
-    const T* k2 = static_cast<const T*>(p.k2) + b * p.s_k2[0] + h * p.s_k2[1];
-    const T* v = static_cast<const T*>(p.v) + b * p.s_v[0] + h * p.s_v[1];
+    const T* k2 = static_cast<const T*>(p.k2) + b * p.s_k2[0] + hk * p.s_k2[1];
+    const T* v = static_cast<const T*>(p.v) + b * p.s_v[0] + hk * p.s_v[1];
     T* out = static_cast<T*>(p.out) + b * p.s_o[0] + h * p.s_o[1] + (int64_t)i * p.s_o[2];
     const int D = p.D;
     const int Dv = 2 * D;

@@ -36,6 +36,11 @@
 //   PV_b(j) has just read P_b(j) from.  Shared resources (a K or V stage, the
 //   Q tile, O) are released when both branches' commits have arrived.
 //
+// Grouped key/value heads: query head h reads the K1, K2 and V tiles of
+// key/value head h / kv_group.  When K1 and K2 are one tensor (the two
+// branches share their keys), each key tile is loaded once and both score
+// products read it from the same shared-memory stage.
+//
 // Causal masking (both branches): KV tiles above the diagonal are never
 // loaded; tiles that cross the diagonal mask key > query with -inf before the
 // row max.
@@ -289,20 +294,27 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 tma_load_4d(smem + OFF_Q1, &tm_q1, &bars[BAR_Q_FULL], 0, it.qt * BM, it.h, it.b);
                 tma_load_4d(smem + OFF_Q2, &tm_q2, &bars[BAR_Q_FULL], 0, it.qt * BM, it.h, it.b);
                 ++armed_q;
+                const int hk = it.h / p.kv_group;     // key/value head of this query head
                 for (int j = 0; j < it.n_kv; ++j) {
                     if (!(ok = mbar_wait(&bars[BAR_K_EMPTY + kst], kph ^ 1, ab))) break;
                     uint8_t* kdst = smem + OFF_K + kst * 2 * K_BYTES;
-                    mbar_arrive_expect_tx(&bars[BAR_K_FULL + kst], 2 * K_BYTES);
-                    tma_load_4d(kdst, &tm_k1, &bars[BAR_K_FULL + kst], 0, j * BN, it.h, it.b);
-                    tma_load_4d(kdst + K_BYTES, &tm_k2, &bars[BAR_K_FULL + kst], 0, j * BN, it.h, it.b);
+                    if (p.k_shared) {
+                        // one key tile serves both branches
+                        mbar_arrive_expect_tx(&bars[BAR_K_FULL + kst], K_BYTES);
+                        tma_load_4d(kdst, &tm_k1, &bars[BAR_K_FULL + kst], 0, j * BN, hk, it.b);
+                    } else {
+                        mbar_arrive_expect_tx(&bars[BAR_K_FULL + kst], 2 * K_BYTES);
+                        tma_load_4d(kdst, &tm_k1, &bars[BAR_K_FULL + kst], 0, j * BN, hk, it.b);
+                        tma_load_4d(kdst + K_BYTES, &tm_k2, &bars[BAR_K_FULL + kst], 0, j * BN, hk, it.b);
+                    }
                     ++armed_k[kst];
                     if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
 
                     if (!(ok = mbar_wait(&bars[BAR_V_EMPTY + vst], vph ^ 1, ab))) break;
                     uint8_t* vdst = smem + OFF_V + vst * V_BYTES;
                     mbar_arrive_expect_tx(&bars[BAR_V_FULL + vst], V_BYTES);
-                    tma_load_4d(vdst, &tm_v, &bars[BAR_V_FULL + vst], 0, j * BN, it.h, it.b);
-                    tma_load_4d(vdst + V_HALF_BYTES, &tm_v, &bars[BAR_V_FULL + vst], 64, j * BN, it.h, it.b);
+                    tma_load_4d(vdst, &tm_v, &bars[BAR_V_FULL + vst], 0, j * BN, hk, it.b);
+                    tma_load_4d(vdst + V_HALF_BYTES, &tm_v, &bars[BAR_V_FULL + vst], 64, j * BN, hk, it.b);
                     ++armed_v[vst];
                     if (++vst == VSTAGES) { vst = 0; vph ^= 1; }
                 }
@@ -325,7 +337,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             // differ only in the start-address field (address >> 4, which
             // stays below 2^14 for every shared-memory address).
             const uint64_t qdesc = sdesc_sw128(smem_u32(smem + (br ? OFF_Q2 : OFF_Q1)), 16, 1024);
-            const uint64_t kdesc = sdesc_sw128(smem_u32(smem + OFF_K + br * K_BYTES), 16, 1024);
+            const uint64_t kdesc =
+                sdesc_sw128(smem_u32(smem + OFF_K + (p.k_shared ? 0 : br) * K_BYTES), 16, 1024);
             const uint64_t vdesc = sdesc_sw128(smem_u32(smem + OFF_V), V_HALF_BYTES, 1024);
             const uint32_t d_o = tmem_base + TM_O + br * 128;
             uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0, oeph = 0;

@@ -33,6 +33,8 @@ struct TcParams {
     const float* norm_weight;   // [H, 2D] or nullptr
     const float* norm_bias;     // [H, 2D] or nullptr
     float out_scale;            // applied last
+    int kv_group;               // query heads per key/value head (>= 1)
+    int k_shared;               // K1 and K2 are one tensor: load each key tile once
 };
 
 // Parameters of the CUDA-core kernel (any D <= 128, fp32 or bf16).
@@ -50,14 +52,18 @@ struct SimtParams {
     const float* norm_weight;
     const float* norm_bias;
     float out_scale;
+    int kv_group;           // query head h reads key/value head h / kv_group
 };
 
 // Parameters of the decode kernels (Tq queries over Tk cached keys).
 struct DecodeParams {
     int B, H, Tq, Tk, D;
+    int kv_group;           // query heads per key/value head (>= 1)
+    int Hk;                 // key/value heads, H / kv_group
+    int row_chunks;         // CTAs along the kv_group * Tq query rows of a key/value head
     int causal;
     int bf16;               // element type: 1 bf16, 0 fp32
-    int tq_bucket;          // Tq rounded up to 1, 2, 4 or 8
+    int tq_bucket;          // query rows per CTA: 1, 2, 4 or 8
     int splits;             // key-range splits per head
     int split_len;          // keys per split (multiple of 256)
     float scale_log2;       // log2(e) / sqrt(D)
@@ -74,10 +80,12 @@ struct DecodeParams {
     float out_scale;
 };
 
-// Decode helpers: query-count bucket (0 if Tq is too large for D), and the
-// number of workspace floats for a launch.
-int decode_tq_bucket(int Tq, int D);
-size_t decode_work_floats(int64_t B, int64_t H, int splits, int tq_bucket, int64_t D);
+// Decode helpers: query-row bucket (rows rounded up to 1, 2, 4 or 8; 0 if
+// there are more rows than one CTA of width D takes), and the number of
+// workspace floats for `units` CTAs along the heads and query rows.
+int decode_tq_bucket(int rows, int D);
+int decode_max_rows(int D);
+size_t decode_work_floats(int64_t units, int splits, int tq_bucket, int64_t D);
 
 // Each returns 0 on success, -1 if the launch failed.
 int launch_decode(const DecodeParams& p, cudaStream_t stream);

@@ -64,9 +64,17 @@ typedef struct CUstream_st *diffattn_stream_t;
 /*
  * Shape and layout of one call.
  *
- * B, H, T, D: batch, heads, sequence length and Q/K width; all >= 1.  V and
- * O have width 2*D.  D <= 128.
+ * B, H, T, D: batch, (query) heads, sequence length and Q/K width; all >= 1.
+ * V and O have width 2*D.  D <= 128.
  * dtype: DIFFATTN_BF16 or DIFFATTN_F32.
+ * kv_group: query heads per key/value head (grouped key/value heads, the
+ * layout of DIFF V2: aiengineeringfromscratch lesson, "V1 vs V2" and its
+ * GQA exercise).  0 or 1: Q1, Q2, K1, K2, V and O all have H heads.  g > 1:
+ * H must be a multiple of g; Q1, Q2 and O have H heads, K1, K2 and V have
+ * H / g heads, and query head h reads key/value head h / g (integer
+ * division).  The two branches may also share one key tensor (pass the same
+ * pointer and strides as K1 and K2); the tensor-core kernel then loads each
+ * key tile once for both branches.
  * *_stride: element strides of the B, H and T dimensions of each tensor
  * ([0] = B, [1] = H, [2] = T).  The innermost (D or 2D) dimension is always
  * contiguous (stride 1).  Strides must be >= 0; a stride of 0 is allowed on B
@@ -76,7 +84,7 @@ typedef struct CUstream_st *diffattn_stream_t;
 typedef struct {
     int64_t B, H, T, D;
     int32_t dtype;
-    int32_t reserved;          /* must be 0 */
+    int32_t kv_group;          /* query heads per key/value head; 0 or 1 = none */
     int64_t q1_stride[3];
     int64_t k1_stride[3];
     int64_t q2_stride[3];
@@ -136,7 +144,8 @@ size_t diffattn_workspace_bytes(void);
  * is 16-byte aligned and every stride is a multiple of 8 elements; any other
  * valid request runs on the CUDA-core kernel.  One kernel launch per call.
  * Errors: DIFFATTN_ERR_INVALID (NULL pointers, sizes < 1, D > 128, unknown
- * dtype, negative strides, non-zero reserved field, non-finite lambda, a
+ * dtype, negative strides, negative kv_group or one that does not divide H,
+ * non-finite lambda, a
  * workspace smaller than diffattn_workspace_bytes() or not 4-byte aligned);
  * DIFFATTN_ERR_CUDA (tensor-map encoding or launch failure).
  */
@@ -190,14 +199,15 @@ int diffattn_fwd_ex(const diffattn_desc *desc, const void *q1, const void *k1,
 
 /*
  * Decode over a key/value cache: Tq new queries against Tk cached keys.
- * Q1, Q2: [B, H, Tq, D]; K1, K2: [B, H, Tk, D]; V: [B, H, Tk, 2D]; O: [B, H,
- * Tq, 2D].  Strides as in diffattn_desc ([0] = B, [1] = H, [2] = the sequence
- * dimension), innermost stride 1.
+ * Q1, Q2: [B, H, Tq, D]; K1, K2: [B, H_kv, Tk, D]; V: [B, H_kv, Tk, 2D]; O:
+ * [B, H, Tq, 2D], with H_kv = H / kv_group (kv_group as in diffattn_desc; 0
+ * or 1 = H_kv = H).  Strides as in diffattn_desc ([0] = B, [1] = H or H_kv,
+ * [2] = the sequence dimension), innermost stride 1.
  */
 typedef struct {
     int64_t B, H, Tq, Tk, D;
     int32_t dtype;
-    int32_t reserved;          /* must be 0 */
+    int32_t kv_group;          /* query heads per key/value head; 0 or 1 = none */
     int64_t q1_stride[3];
     int64_t k1_stride[3];
     int64_t q2_stride[3];
@@ -231,9 +241,13 @@ size_t diffattn_decode_workspace_bytes(const diffattn_kv_desc *desc);
  * Tq <= 4 (D = 128); K1, K2 and V with 16-byte aligned base pointers and
  * strides that are multiples of 16 bytes.  Two kernel launches per call (the
  * key-range splits, then their combination).  Work is bound by reading K1,
- * K2 and V once.
+ * K2 and V once: one CTA serves up to 8 query rows (4 for D = 128) of the
+ * query heads that share a key/value head, so with kv_group = g the cache of
+ * a key/value head is read ceil(g * Tq / 8) times (ceil(g * Tq / 4) for D =
+ * 128), not g * ceil(Tq / 8) times.
  * Errors: DIFFATTN_ERR_INVALID (NULL pointers, sizes < 1, Tk < Tq with the
- * causal mask, unknown dtype, negative strides, non-zero reserved field,
+ * causal mask, unknown dtype, negative strides, negative kv_group or one that
+ * does not divide H,
  * non-finite lambda, bad epilogue, missing, small or misaligned workspace);
  * DIFFATTN_ERR_UNSUPPORTED (D, Tq or alignment outside the supported set);
  * DIFFATTN_ERR_CUDA (launch failure).

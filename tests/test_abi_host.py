@@ -48,12 +48,13 @@ def test_version_and_strerror(lib):
 FAKE = 0x10000  # 64 KiB-aligned stand-in addresses; never dereferenced on the host path
 
 
-def desc(B=1, H=2, T=128, D=64, dtype=_lib.DIFFATTN_BF16, contiguous=True):
+def desc(B=1, H=2, T=128, D=64, dtype=_lib.DIFFATTN_BF16, contiguous=True, kv_group=0):
     d = _lib.DiffattnDesc()
-    d.B, d.H, d.T, d.D, d.dtype, d.reserved = B, H, T, D, dtype, 0
-    for f, w in (("q1_stride", D), ("k1_stride", D), ("q2_stride", D), ("k2_stride", D),
-                 ("v_stride", 2 * D), ("o_stride", 2 * D)):
-        getattr(d, f)[:] = (H * T * w, T * w, w)
+    d.B, d.H, d.T, d.D, d.dtype, d.kv_group = B, H, T, D, dtype, kv_group
+    Hk = H // max(kv_group, 1)
+    for f, w, h in (("q1_stride", D, H), ("k1_stride", D, Hk), ("q2_stride", D, H),
+                    ("k2_stride", D, Hk), ("v_stride", 2 * D, Hk), ("o_stride", 2 * D, H)):
+        getattr(d, f)[:] = (h * T * w, T * w, w)
     return d
 
 
@@ -98,7 +99,8 @@ def test_size_one_dims_ignore_strides(lib):
     lambda d: setattr(d, "D", 0),
     lambda d: setattr(d, "D", 129),
     lambda d: setattr(d, "dtype", 2),
-    lambda d: setattr(d, "reserved", 1),
+    lambda d: setattr(d, "kv_group", -1),
+    lambda d: setattr(d, "kv_group", 3),      # does not divide H = 2
     lambda d: d.k2_stride.__setitem__(1, -1),
 ])
 def test_invalid_desc_rejected_without_gpu(lib, mutate):
@@ -174,12 +176,14 @@ def test_bad_epilogue_rejected(lib, field, value):
     assert rc == _lib.DIFFATTN_ERR_INVALID
 
 
-def kv_desc(B=2, H=3, Tq=1, Tk=1000, D=64, dtype=_lib.DIFFATTN_BF16):
+def kv_desc(B=2, H=3, Tq=1, Tk=1000, D=64, dtype=_lib.DIFFATTN_BF16, kv_group=0):
     d = _lib.DiffattnKvDesc()
-    d.B, d.H, d.Tq, d.Tk, d.D, d.dtype, d.reserved = B, H, Tq, Tk, D, dtype, 0
-    for f, T, w in (("q1_stride", Tq, D), ("q2_stride", Tq, D), ("k1_stride", Tk, D),
-                    ("k2_stride", Tk, D), ("v_stride", Tk, 2 * D), ("o_stride", Tq, 2 * D)):
-        getattr(d, f)[:] = (H * T * w, T * w, w)
+    d.B, d.H, d.Tq, d.Tk, d.D, d.dtype, d.kv_group = B, H, Tq, Tk, D, dtype, kv_group
+    Hk = H // max(kv_group, 1)
+    for f, T, w, h in (("q1_stride", Tq, D, H), ("q2_stride", Tq, D, H), ("k1_stride", Tk, D, Hk),
+                       ("k2_stride", Tk, D, Hk), ("v_stride", Tk, 2 * D, Hk),
+                       ("o_stride", Tq, 2 * D, H)):
+        getattr(d, f)[:] = (h * T * w, T * w, w)
     return d
 
 
@@ -210,3 +214,23 @@ def test_decode_requires_workspace(lib):
     rc = lib.diffattn_decode(ctypes.byref(d), *ptrs(5), ctypes.c_float(0.5), None, 1, None,
                              ctypes.c_void_p(FAKE * 9), None, 0, None)
     assert rc == _lib.DIFFATTN_ERR_INVALID
+
+
+def test_grouped_heads_select_and_reject(lib):
+    # H = 8 query heads over 2 key/value heads: still the tensor-core kernel
+    assert select(lib, desc(H=8, kv_group=4)) == _lib.DIFFATTN_KERNEL_TCGEN05
+    assert select(lib, desc(H=8, kv_group=1)) == _lib.DIFFATTN_KERNEL_TCGEN05
+    assert select(lib, desc(H=8, kv_group=8)) == _lib.DIFFATTN_KERNEL_TCGEN05
+    assert select(lib, desc(H=6, kv_group=4)) == _lib.DIFFATTN_ERR_INVALID
+
+
+def test_decode_grouped_heads_share_ctas(lib):
+    # 8 query heads over 2 key/value heads, one query each: the 4 heads of a
+    # group go in one CTA (4 rows), so the partial results take as many
+    # floats as 2 heads of 4 queries -- not 8 heads of 1 query.
+    size = lambda **kw: lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(**kw)))
+    assert size(H=8, kv_group=4, Tq=1) == size(H=2, Tq=4)
+    # 16 rows per key/value head (g = 8, Tq = 2): two CTAs of 8 rows
+    assert size(H=8, kv_group=8, Tq=2) == size(H=2, Tq=8)
+    assert size(H=8, kv_group=3) == 0
+    assert size(H=8, kv_group=-2) == 0

@@ -47,6 +47,12 @@ class Workload:
     lambdas: Optional[Sequence[float]] = None  # lambda given directly (swept)
     planted: int = 0                     # planted aligned keys per head
     value_offset_sigma: float = 0.0      # std of the shared per-channel value offset
+    kv_heads: Optional[int] = None       # key/value heads (None: H)
+    shared_keys: bool = False            # K2 is K1 (one key tensor for both branches)
+
+    @property
+    def Hk(self) -> int:
+        return self.H if self.kv_heads is None else self.kv_heads
 
     @property
     def Dv(self) -> int:
@@ -83,6 +89,16 @@ WORKLOADS = {
 
 HEADLINE = "b2h16t8192"
 
+# Grouped key/value heads (the DIFF V2 layout): the headline's 16 differential
+# heads over 4 key/value heads, both branches reading one key tensor.  Same
+# algorithmic FLOPs as the headline.
+GQA_WORKLOADS = {
+    "b2h16kv4t8192_shared_k": Workload("b2h16kv4t8192_shared_k", B=2, H=16, T=8192, D=64,
+                                       dtype="bf16", causal=True, seed=5, lambda_init=0.8,
+                                       kv_heads=4, shared_keys=True),
+}
+ALL_WORKLOADS = {**WORKLOADS, **GQA_WORKLOADS}
+
 
 @dataclasses.dataclass
 class Inputs:
@@ -99,7 +115,7 @@ class Inputs:
     lk2: np.ndarray
     planted_keys: Optional[np.ndarray] = None     # [B, H, planted] key rows
     planted_queries: Optional[np.ndarray] = None  # [B, H, planted] query rows
-    value_offset: Optional[np.ndarray] = None     # [B, H, 2D]
+    value_offset: Optional[np.ndarray] = None     # [B, H_kv, 2D]
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
@@ -115,20 +131,27 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
 
 def draw(w: Workload, B: Optional[int] = None, H: Optional[int] = None,
          T: Optional[int] = None, D: Optional[int] = None, seed: Optional[int] = None,
-         dtype: Optional[str] = None) -> Inputs:
-    """Draw the inputs of workload `w` (optionally overriding its sizes)."""
+         dtype: Optional[str] = None, kv_heads: Optional[int] = None) -> Inputs:
+    """Draw the inputs of workload `w` (optionally overriding its sizes).
+
+    kv_heads: number of key/value heads (default H); K1, K2 and V then have
+    that many heads (grouped key/value heads), Q1 and Q2 keep H."""
     B = w.B if B is None else B
     H = w.H if H is None else H
     T = w.T if T is None else T
     D = w.D if D is None else D
+    Hk = (w.Hk if H == w.H else H) if kv_heads is None else kv_heads
+    if Hk < 1 or H % Hk != 0:
+        raise ValueError("kv_heads must divide H")
+    if w.planted and Hk != H:
+        raise ValueError("planted keys are defined per head; use kv_heads = H")
     dtype = w.dtype if dtype is None else dtype
     rng = np.random.Generator(np.random.PCG64(w.seed if seed is None else seed))
-    shp = (B, H, T, D)
-    q1 = rng.standard_normal(shp, dtype=np.float32)
-    k1 = rng.standard_normal(shp, dtype=np.float32)
-    q2 = rng.standard_normal(shp, dtype=np.float32)
-    k2 = rng.standard_normal(shp, dtype=np.float32)
-    v = rng.standard_normal((B, H, T, 2 * D), dtype=np.float32)
+    q1 = rng.standard_normal((B, H, T, D), dtype=np.float32)
+    k1 = rng.standard_normal((B, Hk, T, D), dtype=np.float32)
+    q2 = rng.standard_normal((B, H, T, D), dtype=np.float32)
+    k2 = rng.standard_normal((B, Hk, T, D), dtype=np.float32)
+    v = rng.standard_normal((B, Hk, T, 2 * D), dtype=np.float32)
     lam_vecs = [(0.1 * rng.standard_normal(D)).astype(np.float32) for _ in range(4)]
     planted_keys = planted_queries = offset = None
     if w.planted:
@@ -145,12 +168,14 @@ def draw(w: Workload, B: Optional[int] = None, H: Optional[int] = None,
                     k1[b, h, j] = 4.0 * q1[b, h, i]
     if w.value_offset_sigma:
         offset = (w.value_offset_sigma *
-                  rng.standard_normal((B, H, 2 * D), dtype=np.float32)).astype(np.float32)
+                  rng.standard_normal((B, Hk, 2 * D), dtype=np.float32)).astype(np.float32)
         v += offset[:, :, None, :]
     if dtype == "bf16":
         q1, k1, q2, k2, v = (round_to_bf16(a) for a in (q1, k1, q2, k2, v))
     elif dtype != "f32":
         raise ValueError(f"unknown dtype {dtype}")
+    if w.shared_keys:
+        k2 = k1
     return Inputs(q1, k1, q2, k2, v, *lam_vecs, planted_keys=planted_keys,
                   planted_queries=planted_queries, value_offset=offset)
 
@@ -193,16 +218,22 @@ class DecodeWorkload:
     causal: bool
     seed: int
     lambda_value: float = 0.8
+    kv_heads: Optional[int] = None      # key/value heads (None: H)
 
     @property
     def Dv(self) -> int:
         return 2 * self.D
 
     @property
+    def Hk(self) -> int:
+        return self.H if self.kv_heads is None else self.kv_heads
+
+    @property
     def bytes(self) -> int:
-        """Algorithmic HBM bytes: K1, K2, V read once; Q1, Q2 read, O written."""
+        """Algorithmic HBM bytes: K1, K2, V of every key/value head read once;
+        Q1, Q2 read and O written for every query head."""
         el = 2 if self.dtype == "bf16" else 4
-        return self.B * self.H * (self.Tk * 4 * self.D + self.Tq * 4 * self.D) * el
+        return (self.B * self.Hk * self.Tk * 4 * self.D + self.B * self.H * self.Tq * 4 * self.D) * el
 
 
 # Decode workloads: 16 sequences with 16 heads (the V1 layout halves the heads
@@ -211,23 +242,31 @@ class DecodeWorkload:
 DECODE_WORKLOADS = {
     "decode_b16h16q1k8192": DecodeWorkload("decode_b16h16q1k8192", 16, 16, 1, 8192, 64, "bf16", True, 20),
     "decode_b16h16q4k8192": DecodeWorkload("decode_b16h16q4k8192", 16, 16, 4, 8192, 64, "bf16", True, 21),
+    # grouped key/value heads: 32 differential heads over 8 key/value heads
+    # (the 32-query / 8-key-value-head grouping of the GQA exercise)
+    "decode_b16h32kv8q1k8192": DecodeWorkload("decode_b16h32kv8q1k8192", 16, 32, 1, 8192, 64,
+                                              "bf16", True, 22, kv_heads=8),
 }
 
 
 def draw_kv(w: DecodeWorkload, **override) -> Inputs:
-    """Decode inputs: q1, q2 [B, H, Tq, D]; k1, k2 [B, H, Tk, D]; v [B, H, Tk, 2D];
-    i.i.d. N(0, 1) float32 drawn in the order q1, k1, q2, k2, v from PCG64(seed),
-    rounded to the dtype.  The lambda vectors are left zero (lambda is given
-    directly for decode workloads)."""
-    f = dict(B=w.B, H=w.H, Tq=w.Tq, Tk=w.Tk, D=w.D, dtype=w.dtype, seed=w.seed)
+    """Decode inputs: q1, q2 [B, H, Tq, D]; k1, k2 [B, H_kv, Tk, D]; v [B, H_kv,
+    Tk, 2D] (H_kv = w.kv_heads, default H); i.i.d. N(0, 1) float32 drawn in the
+    order q1, k1, q2, k2, v from PCG64(seed), rounded to the dtype.  The lambda
+    vectors are left zero (lambda is given directly for decode workloads)."""
+    f = dict(B=w.B, H=w.H, Tq=w.Tq, Tk=w.Tk, D=w.D, dtype=w.dtype, seed=w.seed,
+             kv_heads=w.kv_heads)
     f.update(override)
     rng = np.random.Generator(np.random.PCG64(f["seed"]))
     B, H, Tq, Tk, D = f["B"], f["H"], f["Tq"], f["Tk"], f["D"]
+    Hk = H if f["kv_heads"] is None else f["kv_heads"]
+    if Hk < 1 or H % Hk != 0:
+        raise ValueError("kv_heads must divide H")
     q1 = rng.standard_normal((B, H, Tq, D), dtype=np.float32)
-    k1 = rng.standard_normal((B, H, Tk, D), dtype=np.float32)
+    k1 = rng.standard_normal((B, Hk, Tk, D), dtype=np.float32)
     q2 = rng.standard_normal((B, H, Tq, D), dtype=np.float32)
-    k2 = rng.standard_normal((B, H, Tk, D), dtype=np.float32)
-    v = rng.standard_normal((B, H, Tk, 2 * D), dtype=np.float32)
+    k2 = rng.standard_normal((B, Hk, Tk, D), dtype=np.float32)
+    v = rng.standard_normal((B, Hk, Tk, 2 * D), dtype=np.float32)
     if f["dtype"] == "bf16":
         q1, k1, q2, k2, v = (round_to_bf16(a) for a in (q1, k1, q2, k2, v))
     z = np.zeros(D, dtype=np.float32)
