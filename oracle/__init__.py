@@ -5,8 +5,10 @@ baseline use it.  It shares no code with the CUDA library.
 """
 from .diffattn_oracle import (  # noqa: F401
     differential_attention,
+    differential_attention_backward,
     differential_attention_kv,
     differential_lambda,
+    differential_lambda_backward,
     head_norm,
     lambda_init_schedule,
     signed_map,

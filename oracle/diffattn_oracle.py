@@ -38,6 +38,12 @@ The step that follows the operation in the model (per-head normalisation,
 GroupNorm or RMSNorm, then x (1 - lambda_init)) is `head_norm`, pinned
 against torch's group_norm and rms_norm.
 
+The backward (`differential_attention_backward`, `differential_lambda_backward`)
+is the chain rule through the same steps (paperleet, Return requirements:
+gradients through both Q/K branches, the value, the coefficient and the four
+lambda vectors), pinned against torch autograd, finite differences and closed
+forms in tests/test_oracle_backward.py.
+
 Parity is pinned by tests/test_oracle.py (brute-force scalar softmax on tiny
 inputs, a library attention routine at lambda = 0, row sums, the identical-map
 and value-offset identities, closed forms, and the printed worked example).
@@ -273,3 +279,103 @@ def differential_attention_kv(q1, k1, q2, k2, v, lam: float, causal: bool = True
                            causal, Tk - Tq)
             out[b, h] = w @ v[b, h // g]
     return out
+
+
+# ---------------------------------------------------------------------------
+# Backward: the vector-Jacobian product of the operation.  paperleet
+# "Differential Transformer Attention", Return requirements: gradients flow
+# through both Q/K branches, the value and a tensor coefficient, and
+# differential_lambda passes gradients to all four parameter vectors; its Toy
+# experiment section checks all of them with analytic vector-Jacobian products.
+# The steps below are the chain rule through the forward's own steps, for one
+# head, given dO = dL/dO:
+#
+#   W      = A_1 - lambda A_2                     (the signed map)
+#   dV     = W^T dO                               (O = W V)
+#   dW     = dO V^T
+#   dA_1   = dW,   dA_2 = -lambda dW,   dlambda = -sum(dW * A_2)
+#   dS_b   = A_b * (dA_b - rowsum(dA_b * A_b))    (row softmax; masked entries
+#                                                  have A_b = 0, so dS_b = 0)
+#   dQ_b   = dS_b K_b / sqrt(D),   dK_b = dS_b^T Q_b / sqrt(D)
+#
+# With grouped key/value heads, dK_b and dV of a key/value head sum the
+# contributions of every query head that reads it.
+# ---------------------------------------------------------------------------
+
+def _head_backward(q1, k1, q2, k2, v, dout, lam, causal, block=256):
+    """Gradients of one query head (float64 arrays of that head) for all rows:
+    returns dq1, dk1, dq2, dk2, dv, dlam.  Query rows go `block` at a time;
+    each row's softmax is complete within its block, so blocking is exact."""
+    T, D = q1.shape
+    scale = 1.0 / math.sqrt(D)
+    dq1, dq2 = np.zeros_like(q1), np.zeros_like(q2)
+    dk1, dk2 = np.zeros_like(k1), np.zeros_like(k2)
+    dv = np.zeros_like(v)
+    dlam = 0.0
+    for r0 in range(0, T, block):
+        rows = np.arange(r0, min(T, r0 + block))
+        a1 = _softmax(_mask(_scores(q1[rows], k1), rows, causal))
+        a2 = _softmax(_mask(_scores(q2[rows], k2), rows, causal))
+        w = _combine(a1, a2, lam)
+        g = dout[rows]
+        dv += w.T @ g
+        dw = g @ v.T
+        dlam += -float(np.sum(dw * a2))
+        for a, da, q, k, dq, dk in ((a1, dw, q1, k1, dq1, dk1),
+                                    (a2, -lam * dw, q2, k2, dq2, dk2)):
+            ds = a * (da - np.sum(da * a, axis=-1, keepdims=True))
+            dq[rows] = scale * (ds @ k)
+            dk += scale * (ds.T @ q[rows])
+    return dq1, dk1, dq2, dk2, dv, dlam
+
+
+def differential_attention_backward(q1, k1, q2, k2, v, lam: float, dout, causal: bool = True,
+                                    kv_heads: Optional[Sequence[tuple]] = None):
+    """Gradients of L with dL/dO = dout through O = (A_1 - lambda A_2) V, in
+    float64.
+
+    Shapes as differential_attention (q1, q2 [B, H, T, D]; k1, k2 [B, H_kv, T,
+    D]; v [B, H_kv, T, 2D]); dout [B, H, T, 2D].  Returns dq1, dk1, dq2, dk2,
+    dv with the shapes of their inputs, and dlambda (a float).
+
+    kv_heads: optional list of (b, hk) key/value heads to evaluate; then every
+    query head that reads them is processed, the gradients of the other heads
+    are left zero, and dlambda sums only the processed query heads.
+    """
+    g = _check_shapes(q1, k1, q2, k2, v)
+    B, H, T, D = q1.shape
+    Hk = H // g
+    dout = _as64(dout)
+    if dout.shape != (B, H, T, 2 * D):
+        raise ValueError("dout must be [B, H, T, 2D]")
+    lam = float(lam)
+    dq1 = np.zeros((B, H, T, D))
+    dq2 = np.zeros((B, H, T, D))
+    dk1 = np.zeros((B, Hk, T, D))
+    dk2 = np.zeros((B, Hk, T, D))
+    dv = np.zeros((B, Hk, T, 2 * D))
+    dlam = 0.0
+    todo = [(b, hk) for b in range(B) for hk in range(Hk)] if kv_heads is None else list(kv_heads)
+    for b, hk in todo:
+        hk1, hk2, hv = (_as64(x[b, hk]) for x in (k1, k2, v))
+        for h in range(hk * g, (hk + 1) * g):
+            r = _head_backward(_as64(q1[b, h]), hk1, _as64(q2[b, h]), hk2, hv, dout[b, h], lam,
+                               causal)
+            dq1[b, h], dq2[b, h] = r[0], r[2]
+            dk1[b, hk] += r[1]
+            dk2[b, hk] += r[3]
+            dv[b, hk] += r[4]
+            dlam += r[5]
+    return dq1, dk1, dq2, dk2, dv, dlam
+
+
+def differential_lambda_backward(lq1, lk1, lq2, lk2, dlam: float):
+    """Gradients of lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init with
+    respect to the four vectors, given dL/dlambda (float64):
+    d/dlq1 = dlam e1 lk1, d/dlk1 = dlam e1 lq1, d/dlq2 = -dlam e2 lk2,
+    d/dlk2 = -dlam e2 lq2, with e_b = exp(lq_b . lk_b)."""
+    vecs = [np.asarray(x, dtype=np.float64).reshape(-1) for x in (lq1, lk1, lq2, lk2)]
+    e1 = math.exp(float(np.dot(vecs[0], vecs[1])))
+    e2 = math.exp(float(np.dot(vecs[2], vecs[3])))
+    d = float(dlam)
+    return d * e1 * vecs[1], d * e1 * vecs[0], -d * e2 * vecs[3], -d * e2 * vecs[2]
