@@ -26,7 +26,8 @@ from ._lib import (DIFFATTN_BF16, DIFFATTN_F32, DIFFATTN_KERNEL_SIMT,  # noqa: F
                    DIFFATTN_NORM_RMS, DiffattnDesc, DiffattnEpilogue, DiffattnError,
                    DiffattnKvDesc)
 
-__all__ = ["differential_lambda", "differential_attention", "differential_attention_decode",
+__all__ = ["differential_lambda", "differential_attention", "differential_attention_backward",
+           "differential_attention_decode",
            "make_desc", "make_kv_desc", "select_kernel", "get_device_error", "version",
            "DiffattnError"]
 
@@ -69,8 +70,17 @@ def differential_lambda(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor, k2
 
     q1, k1, q2, k2 are the four lambda parameter vectors [D_lambda] (equal
     length, non-empty) on one CUDA device.  The result is float32 on that
-    device, computed in float64 by the library's kernel.  (Forward only.)
+    device, computed in float64 by the library's kernel.  When grad mode is on
+    and a vector requires grad, the result carries an autograd node whose
+    backward runs diffattn_lambda_backward.
     """
+    if torch.is_grad_enabled() and any(isinstance(t, torch.Tensor) and t.requires_grad
+                                       for t in (q1, k1, q2, k2)):
+        return _DifferentialLambdaFn.apply(q1, k1, q2, k2, lambda_init)
+    return _lambda_forward(q1, k1, q2, k2, lambda_init)
+
+
+def _lambda_forward(q1, k1, q2, k2, lambda_init):
     vecs = []
     for name, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2)):
         _require_cuda(t, name)
@@ -178,8 +188,25 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
     out_scale (e.g. 1 - lambda_init).
 
     Returns the [B, H, T, 2D] output; the launch is asynchronous on the
-    current CUDA stream.  (Forward only.)
+    current CUDA stream.  When grad mode is on and an input or a tensor
+    coefficient requires grad, the result carries an autograd node whose
+    backward runs diffattn_bwd (no epilogue and no `out` then).
     """
+    if torch.is_grad_enabled() and any(
+            isinstance(t, torch.Tensor) and t.requires_grad
+            for t in (q1, k1, q2, k2, value, coefficient)):
+        if out is not None or norm not in (None, "none") or norm_weight is not None or \
+                norm_bias is not None or out_scale != 1.0:
+            raise ValueError("gradients are available for the bare operation only "
+                             "(no out=, norm or out_scale)")
+        return _DifferentialAttentionFn.apply(q1, k1, q2, k2, value, coefficient, causal,
+                                              dynamic_schedule)
+    return _forward(q1, k1, q2, k2, value, coefficient, causal, out, dynamic_schedule, norm,
+                    norm_eps, norm_weight, norm_bias, out_scale)
+
+
+def _forward(q1, k1, q2, k2, value, coefficient, causal, out, dynamic_schedule, norm, norm_eps,
+             norm_weight, norm_bias, out_scale):
     (q1, k1, q2, k2, value), dev = _prepare(q1, k1, q2, k2, value)
     B, H, T, D = q1.shape
     if out is None:
@@ -190,21 +217,7 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
             raise ValueError("out must be [B, H, T, 2D] with the inputs' dtype and device")
         if out.stride(-1) != 1:
             raise ValueError("out must have a contiguous innermost dimension")
-    lam_host = 0.0
-    lam_dev = None
-    if isinstance(coefficient, torch.Tensor):
-        if coefficient.numel() != 1:
-            raise ValueError("coefficient must be a scalar")
-        if coefficient.device.type == "cuda":
-            if coefficient.device != dev:
-                raise ValueError("coefficient tensor must be on the inputs' device")
-            lam_dev = coefficient.detach().reshape(()).to(torch.float32)
-        else:
-            lam_host = float(coefficient.item())
-    elif isinstance(coefficient, numbers.Real):
-        lam_host = float(coefficient)
-    else:
-        raise TypeError("coefficient must be a real number or a scalar tensor")
+    lam_host, lam_dev = _coefficient(coefficient, dev)
     d = make_desc(q1, k1, q2, k2, value, out)
     epi = _epilogue(norm, norm_eps, norm_weight, norm_bias, out_scale, H, 2 * D, dev)
     lib = _lib.load()
@@ -222,6 +235,109 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
                                  ctypes.c_void_p(stream.cuda_stream))
     _lib.check(rc, "diffattn_fwd")
     return out
+
+
+def differential_attention_backward(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
+                                    k2: torch.Tensor, value: torch.Tensor, coefficient,
+                                    dout: torch.Tensor, causal: bool = True):
+    """Gradients of differential_attention given dout = dL/dO.
+
+    Inputs as differential_attention (the forward's inputs and coefficient);
+    dout: [B, H, T, 2D] of the inputs' dtype.  Returns (dq1, dk1, dq2, dk2,
+    dvalue, dcoefficient): contiguous tensors of the inputs' shapes and dtype,
+    and a float32 scalar tensor on the device.  The gradients of the four
+    lambda vectors follow from dcoefficient (see differential_lambda)."""
+    (q1, k1, q2, k2, value), dev = _prepare(q1, k1, q2, k2, value)
+    B, H, T, D = q1.shape
+    _require_cuda(dout, "dout")
+    if tuple(dout.shape) != (B, H, T, 2 * D) or dout.dtype != q1.dtype or dout.device != dev:
+        raise ValueError("dout must be [B, H, T, 2D] with the inputs' dtype and device")
+    if dout.stride(-1) != 1:
+        dout = dout.contiguous()
+    lam_host, lam_dev = _coefficient(coefficient, dev)
+    d = make_desc(q1, k1, q2, k2, value, dout)
+    grads = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (q1, k1, q2, k2, value)]
+    dlam = torch.empty((), dtype=torch.float32, device=dev)
+    lib = _lib.load()
+    need = int(lib.diffattn_bwd_workspace_bytes(ctypes.byref(d)))
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev)
+        ws = torch.empty(need // 4 + 4, dtype=torch.float32, device=dev)
+        rc = lib.diffattn_bwd(ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in
+                                                  (q1, k1, q2, k2, value)),
+                              ctypes.c_float(lam_host),
+                              ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0),
+                              1 if causal else 0, ctypes.c_void_p(dout.data_ptr()),
+                              *(ctypes.c_void_p(g.data_ptr()) for g in grads),
+                              ctypes.c_void_p(dlam.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                              ctypes.c_size_t(ws.numel() * 4), ctypes.c_void_p(stream.cuda_stream))
+    _lib.check(rc, "diffattn_bwd")
+    return (*grads, dlam)
+
+
+class _DifferentialAttentionFn(torch.autograd.Function):
+    """Autograd node: forward through diffattn_fwd, backward through diffattn_bwd."""
+
+    @staticmethod
+    def forward(ctx, q1, k1, q2, k2, value, coefficient, causal, dynamic_schedule):
+        out = _forward(q1, k1, q2, k2, value, coefficient, causal, None, dynamic_schedule, None,
+                       1e-5, None, None, 1.0)
+        coef_t = coefficient if isinstance(coefficient, torch.Tensor) else None
+        ctx.save_for_backward(q1, k1, q2, k2, value, coef_t)
+        ctx.coefficient = None if coef_t is not None else coefficient
+        ctx.causal = causal
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q1, k1, q2, k2, value, coef_t = ctx.saved_tensors
+        coefficient = coef_t if coef_t is not None else ctx.coefficient
+        dq1, dk1, dq2, dk2, dv, dlam = differential_attention_backward(
+            q1, k1, q2, k2, value, coefficient, dout.to(q1.dtype), ctx.causal)
+        dcoef = None
+        if coef_t is not None and ctx.needs_input_grad[5]:
+            dcoef = dlam.to(device=coef_t.device, dtype=coef_t.dtype).reshape(coef_t.shape)
+        return dq1, dk1, dq2, dk2, dv, dcoef, None, None
+
+
+class _DifferentialLambdaFn(torch.autograd.Function):
+    """Autograd node: forward through diffattn_lambda, backward through
+    diffattn_lambda_backward."""
+
+    @staticmethod
+    def forward(ctx, q1, k1, q2, k2, lambda_init):
+        out = _lambda_forward(q1, k1, q2, k2, lambda_init)
+        ctx.save_for_backward(q1, k1, q2, k2)
+        return out
+
+    @staticmethod
+    def backward(ctx, dlam):
+        vecs = [t.detach().to(torch.float32).contiguous() for t in ctx.saved_tensors]
+        grads = [torch.empty_like(v) for v in vecs]
+        g = dlam.detach().to(device=vecs[0].device, dtype=torch.float32).reshape(()).contiguous()
+        dev = vecs[0].device
+        with torch.cuda.device(dev):
+            rc = _lib.load().diffattn_lambda_backward(
+                *(ctypes.c_void_p(v.data_ptr()) for v in vecs), vecs[0].numel(),
+                ctypes.c_void_p(g.data_ptr()), *(ctypes.c_void_p(x.data_ptr()) for x in grads),
+                _stream_handle(dev))
+        _lib.check(rc, "diffattn_lambda_backward")
+        return (*(x.to(t.dtype) for x, t in zip(grads, ctx.saved_tensors)), None)
+
+
+def _coefficient(coefficient, dev):
+    """(host lambda, device lambda tensor or None) from a number or scalar tensor."""
+    if isinstance(coefficient, torch.Tensor):
+        if coefficient.numel() != 1:
+            raise ValueError("coefficient must be a scalar")
+        if coefficient.device.type == "cuda":
+            if coefficient.device != dev:
+                raise ValueError("coefficient tensor must be on the inputs' device")
+            return 0.0, coefficient.detach().reshape(()).to(torch.float32)
+        return float(coefficient.item()), None
+    if isinstance(coefficient, numbers.Real):
+        return float(coefficient), None
+    raise TypeError("coefficient must be a real number or a scalar tensor")
 
 
 def make_kv_desc(q1, k1, q2, k2, v, out) -> DiffattnKvDesc:

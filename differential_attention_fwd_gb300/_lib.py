@@ -26,8 +26,11 @@ DIFFATTN_NORM_GROUP = 2
 # Every symbol include/diffattn.h declares.
 EXPORTED = (
     "diffattn_lambda",
+    "diffattn_lambda_backward",
     "diffattn_fwd",
     "diffattn_fwd_ex",
+    "diffattn_bwd",
+    "diffattn_bwd_workspace_bytes",
     "diffattn_decode",
     "diffattn_decode_workspace_bytes",
     "diffattn_decode_noalloc",
@@ -91,6 +94,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
     lib.diffattn_lambda.argtypes = [vp, vp, vp, vp, i64, ctypes.c_double, vp, vp]
     lib.diffattn_lambda.restype = ctypes.c_int
+    lib.diffattn_lambda_backward.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp]
+    lib.diffattn_lambda_backward.restype = ctypes.c_int
     lib.diffattn_fwd.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, ctypes.c_float,
                                  vp, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]
     lib.diffattn_fwd_ex.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, ctypes.c_float,
@@ -105,6 +110,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                             ctypes.c_float, vp, ctypes.c_int,
                                             ctypes.POINTER(DiffattnEpilogue), vp, vp]
     lib.diffattn_decode_noalloc.restype = ctypes.c_int
+    lib.diffattn_bwd.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, ctypes.c_float,
+                                 vp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.diffattn_bwd.restype = ctypes.c_int
+    lib.diffattn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(DiffattnDesc)]
+    lib.diffattn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.diffattn_decode_workspace_bytes.argtypes = [ctypes.POINTER(DiffattnKvDesc)]
     lib.diffattn_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.diffattn_workspace_bytes.argtypes = []

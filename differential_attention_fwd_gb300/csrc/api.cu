@@ -217,6 +217,17 @@ int diffattn_lambda(const float* lq1, const float* lk1, const float* lq2, const 
                : DIFFATTN_ERR_CUDA;
 }
 
+int diffattn_lambda_backward(const float* lq1, const float* lk1, const float* lq2,
+                             const float* lk2, int64_t n, const float* dlambda, float* dlq1,
+                             float* dlk1, float* dlq2, float* dlk2, diffattn_stream_t stream) {
+    if (!lq1 || !lk1 || !lq2 || !lk2 || !dlambda || !dlq1 || !dlk1 || !dlq2 || !dlk2 || n < 1)
+        return DIFFATTN_ERR_INVALID;
+    return launch_lambda_bwd(lq1, lk1, lq2, lk2, n, dlambda, dlq1, dlk1, dlq2, dlk2,
+                             reinterpret_cast<cudaStream_t>(stream)) == 0
+               ? DIFFATTN_OK
+               : DIFFATTN_ERR_CUDA;
+}
+
 int diffattn_select_kernel(const diffattn_desc* desc, const void* q1, const void* k1,
                            const void* q2, const void* k2, const void* v, const void* out) {
     const int rc = validate(desc, q1, k1, q2, k2, v, out);
@@ -346,6 +357,59 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
     p.out_scale = e.out_scale;
     p.kv_group = (int)group_of(d.kv_group);
     rc = (d.dtype == DIFFATTN_F32) ? launch_fwd_simt_f32(p, st) : launch_fwd_simt_bf16(p, st);
+    return rc == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+size_t diffattn_bwd_workspace_bytes(const diffattn_desc* desc) {
+    if (!desc || desc->B < 1 || desc->H < 1 || desc->T < 1) return 0;
+    return (size_t)desc->B * desc->H * desc->T * 4 * sizeof(float);
+}
+
+int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
+                 const void* k2, const void* v, float lambda, const float* lambda_dev, int causal,
+                 const void* dout, void* dq1, void* dk1, void* dq2, void* dk2, void* dv,
+                 float* dlambda, void* workspace, size_t workspace_bytes,
+                 diffattn_stream_t stream) {
+    int rc = validate(desc, q1, k1, q2, k2, v, dout);
+    if (rc != DIFFATTN_OK) return rc;
+    if (!dq1 || !dk1 || !dq2 || !dk2 || !dv || !dlambda) return DIFFATTN_ERR_INVALID;
+    if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
+    const size_t need = diffattn_bwd_workspace_bytes(desc);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
+        return DIFFATTN_ERR_INVALID;
+    const diffattn_desc& d = *desc;
+    BwdParams p;
+    p.B = (int)d.B;
+    p.H = (int)d.H;
+    p.kv_group = (int)group_of(d.kv_group);
+    p.Hk = (int)(d.H / p.kv_group);
+    p.T = (int)d.T;
+    p.D = (int)d.D;
+    p.causal = causal ? 1 : 0;
+    p.scale = (float)(1.0 / std::sqrt((double)d.D));
+    p.lambda = lambda;
+    p.lambda_dev = lambda_dev;
+    p.q1 = q1;
+    p.k1 = k1;
+    p.q2 = q2;
+    p.k2 = k2;
+    p.v = v;
+    p.dout = dout;
+    p.dq1 = dq1;
+    p.dk1 = dk1;
+    p.dq2 = dq2;
+    p.dk2 = dk2;
+    p.dv = dv;
+    copy3(p.s_q1, d.q1_stride);
+    copy3(p.s_k1, d.k1_stride);
+    copy3(p.s_q2, d.q2_stride);
+    copy3(p.s_k2, d.k2_stride);
+    copy3(p.s_v, d.v_stride);
+    copy3(p.s_do, d.o_stride);
+    p.stats = static_cast<float*>(workspace);
+    p.dlambda = dlambda;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    rc = (d.dtype == DIFFATTN_F32) ? launch_bwd_simt_f32(p, st) : launch_bwd_simt_bf16(p, st);
     return rc == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 

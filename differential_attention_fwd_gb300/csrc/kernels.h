@@ -80,6 +80,23 @@ struct DecodeParams {
     float out_scale;
 };
 
+// Parameters of the backward (CUDA-core kernels, any D <= 128).  Inputs use
+// the descriptor's strides; dout uses the output strides; the gradients are
+// dense: dq [B, H, T, D], dk [B, Hk, T, D], dv [B, Hk, T, 2D].
+struct BwdParams {
+    int B, H, Hk, kv_group, T, D;
+    int causal;
+    float scale;            // 1 / sqrt(D)
+    float lambda;
+    const float* lambda_dev;
+    const void* q1; const void* k1; const void* q2; const void* k2; const void* v;
+    const void* dout;
+    void* dq1; void* dk1; void* dq2; void* dk2; void* dv;
+    int64_t s_q1[3], s_k1[3], s_q2[3], s_k2[3], s_v[3], s_do[3];
+    float* stats;           // [B, H, T, 4]: log-sum-exp of each branch, Dd_1, Dd_2
+    float* dlambda;         // one float
+};
+
 // Decode helpers: query-row bucket (rows rounded up to 1, 2, 4 or 8; 0 if
 // there are more rows than one CTA of width D takes), and the number of
 // workspace floats for `units` CTAs along the heads and query rows.
@@ -91,9 +108,14 @@ size_t decode_work_floats(int64_t units, int splits, int tq_bucket, int64_t D);
 int launch_decode(const DecodeParams& p, cudaStream_t stream);
 int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v,out*/, const TcParams& p, int grid,
                   cudaStream_t stream);
+int launch_bwd_simt_f32(const BwdParams& p, cudaStream_t stream);
+int launch_bwd_simt_bf16(const BwdParams& p, cudaStream_t stream);
 int launch_fwd_simt_f32(const SimtParams& p, cudaStream_t stream);
 int launch_fwd_simt_bf16(const SimtParams& p, cudaStream_t stream);
 int launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                   int64_t n, double lambda_init, float* out, cudaStream_t stream);
+int launch_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                      int64_t n, const float* dlambda, float* dlq1, float* dlk1, float* dlq2,
+                      float* dlk2, cudaStream_t stream);
 
 }  // namespace diffattn

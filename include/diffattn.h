@@ -111,6 +111,28 @@ int diffattn_lambda(const float *lq1, const float *lk1, const float *lq2,
                     float *lambda_out, diffattn_stream_t stream);
 
 /*
+ * diffattn_lambda_backward -- gradients of lambda = exp(lq1 . lk1) -
+ * exp(lq2 . lk2) + lambda_init with respect to the four vectors, given
+ * dlambda = dL/dlambda (paperleet "Differential Transformer Attention",
+ * Return requirements: differential_lambda passes gradients to all four
+ * parameter vectors).  With e_b = exp(lq_b . lk_b):
+ *
+ *     dlq1 = dlambda e1 lk1    dlk1 = dlambda e1 lq1
+ *     dlq2 = -dlambda e2 lk2   dlk2 = -dlambda e2 lq2
+ *
+ * lq1, lk1, lq2, lk2: device pointers to n contiguous float32 values each;
+ * dlambda: device pointer to one float32 (for example diffattn_bwd's output);
+ * dlq1, dlk1, dlq2, dlk2: device pointers to n float32 values each,
+ * overwritten.  Dot products and exponentials in float64.  One launch on
+ * `stream`.  Errors: DIFFATTN_ERR_INVALID for a NULL pointer or n < 1;
+ * DIFFATTN_ERR_CUDA if the launch fails.
+ */
+int diffattn_lambda_backward(const float *lq1, const float *lk1, const float *lq2,
+                             const float *lk2, int64_t n, const float *dlambda,
+                             float *dlq1, float *dlk1, float *dlq2, float *dlk2,
+                             diffattn_stream_t stream);
+
+/*
  * diffattn_workspace_bytes -- size of the optional scheduler workspace that
  * diffattn_fwd accepts (a few bytes; the value is stable for a given library
  * version).
@@ -196,6 +218,51 @@ int diffattn_fwd_ex(const diffattn_desc *desc, const void *q1, const void *k1,
                     const float *lambda_dev, int causal, const diffattn_epilogue *epi,
                     void *out, void *workspace, size_t workspace_bytes,
                     diffattn_stream_t stream);
+
+/*
+ * diffattn_bwd_workspace_bytes -- bytes of device workspace diffattn_bwd needs
+ * for this descriptor (four float32 row statistics per query row), or 0 for a
+ * NULL descriptor or sizes < 1.
+ */
+size_t diffattn_bwd_workspace_bytes(const diffattn_desc *desc);
+
+/*
+ * diffattn_bwd -- gradients of the operation: given dout = dL/dO, writes
+ * dL/dQ1, dL/dK1, dL/dQ2, dL/dK2, dL/dV and dL/dlambda (paperleet
+ * "Differential Transformer Attention", Return requirements: gradients flow
+ * through both Q/K branches, the value and the coefficient).  With
+ * W = A_1 - lambda A_2:
+ *
+ *     dV = W^T dO        dlambda = -sum(dO * (A_2 V))
+ *     dS_b = A_b * (dA_b - rowsum(dA_b * A_b)),  dA_1 = dO V^T, dA_2 = -lambda dO V^T
+ *     dQ_b = dS_b K_b / sqrt(D)      dK_b = dS_b^T Q_b / sqrt(D)
+ *
+ * The gradients of the four lambda vectors follow from dlambda through
+ * diffattn_lambda_backward.  With kv_group > 1, dK1, dK2 and dV of a key/value head sum the
+ * contributions of every query head that reads it.
+ *
+ * desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal: as diffattn_fwd (the
+ * forward's inputs).  dout: device pointer, [B, H, T, 2D] with desc->o_stride,
+ * same dtype as the inputs.  dq1, dq2: device pointers to dense [B, H, T, D];
+ * dk1, dk2: dense [B, H / kv_group, T, D]; dv: dense [B, H / kv_group, T, 2D];
+ * all of the inputs' dtype, all overwritten; they must not overlap each other
+ * or any input.  dlambda: device pointer to one float32, overwritten.
+ * workspace: device memory of at least diffattn_bwd_workspace_bytes(desc)
+ * bytes, 16-byte aligned, owned by the caller; its contents need no
+ * initialisation.
+ *
+ * Runs on the CUDA cores (fp32 arithmetic for either dtype): four launches on
+ * `stream` (row statistics, dQ, dK/dV, dlambda), no atomics, so the result is
+ * reproducible bit for bit.
+ * Errors: DIFFATTN_ERR_INVALID (as diffattn_fwd, plus a NULL gradient pointer,
+ * a missing, small or misaligned workspace); DIFFATTN_ERR_CUDA (launch
+ * failure).
+ */
+int diffattn_bwd(const diffattn_desc *desc, const void *q1, const void *k1,
+                 const void *q2, const void *k2, const void *v, float lambda,
+                 const float *lambda_dev, int causal, const void *dout, void *dq1,
+                 void *dk1, void *dq2, void *dk2, void *dv, float *dlambda,
+                 void *workspace, size_t workspace_bytes, diffattn_stream_t stream);
 
 /*
  * Decode over a key/value cache: Tq new queries against Tk cached keys.

@@ -89,3 +89,37 @@ def to_device(x: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
 
 def to_numpy(t: torch.Tensor) -> np.ndarray:
     return t.detach().to(device="cpu", dtype=torch.float64).numpy()
+
+
+# Gradients.  Their magnitudes grow with the number of terms each one sums
+# (queries per key, keys per query), so the output tolerances above are
+# applied to the error measured in units of the gradient tensor's own scale,
+# s = max(1, rms(reference)): max |err| / s <= 2e-2 and mean |err| / s <= 2e-3
+# for bf16, max |err| / s <= 1e-4 for float32.  For bf16 the kernel's result
+# is rounded to bf16 once more on output, which alone contributes up to half an
+# ulp (2^-9 relative) of each element; that is the same allowance as the
+# forward's.
+def grad_scale(ref: np.ndarray) -> float:
+    ref = np.asarray(ref, dtype=np.float64)
+    return max(1.0, float(np.sqrt(np.mean(ref * ref)))) if ref.size else 1.0
+
+
+def assert_grad_close(got, ref, dtype: str, what: str = "") -> dict:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite gradient"
+    s = grad_scale(ref)
+    err = np.abs(got - ref) / s
+    stats = {"scale": s, "max_rel": float(err.max()) if err.size else 0.0,
+             "mean_rel": float(err.mean()) if err.size else 0.0, "n": int(err.size)}
+    log = os.environ.get("DIFFATTN_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"case": what, "dtype": dtype, "grad": True, **stats}) + "\n")
+    if dtype == "f32":
+        assert stats["max_rel"] <= F32_MAX_ABS, f"{what} fp32 gradient {stats}"
+    else:
+        assert stats["max_rel"] <= BF16_MAX_ABS, f"{what} bf16 gradient max {stats}"
+        assert stats["mean_rel"] <= BF16_MEAN_ABS, f"{what} bf16 gradient mean {stats}"
+    return stats
