@@ -95,10 +95,12 @@ def to_numpy(t: torch.Tensor) -> np.ndarray:
 # (queries per key, keys per query), so the output tolerances above are
 # applied to the error measured in units of the gradient tensor's own scale,
 # s = max(1, rms(reference)): max |err| / s <= 2e-2 and mean |err| / s <= 2e-3
-# for bf16, max |err| / s <= 1e-4 for float32.  For bf16 the kernel's result
-# is rounded to bf16 once more on output, which alone contributes up to half an
-# ulp (2^-9 relative) of each element; that is the same allowance as the
-# forward's.
+# for bf16, max |err| / s <= 1e-4 for float32.  A bf16 gradient is rounded to
+# bf16 on output, which alone costs up to half an ulp of the element (2^-9
+# relative: 0.0156 at |g| = 4, more above); as for the forward's large
+# outputs, the bf16 bounds apply to the error in excess of that rounding:
+# max(0, |err| - half_ulp(ref)) for the max, and the mean error in excess of
+# the mean error of the exact gradient rounded to bf16 for the mean.
 def grad_scale(ref: np.ndarray) -> float:
     ref = np.asarray(ref, dtype=np.float64)
     return max(1.0, float(np.sqrt(np.mean(ref * ref)))) if ref.size else 1.0
@@ -110,9 +112,14 @@ def assert_grad_close(got, ref, dtype: str, what: str = "") -> dict:
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite gradient"
     s = grad_scale(ref)
-    err = np.abs(got - ref) / s
-    stats = {"scale": s, "max_rel": float(err.max()) if err.size else 0.0,
-             "mean_rel": float(err.mean()) if err.size else 0.0, "n": int(err.size)}
+    err = np.abs(got - ref)
+    stats = {"scale": s, "max_rel": float(err.max() / s) if err.size else 0.0,
+             "mean_rel": float(err.mean() / s) if err.size else 0.0, "n": int(err.size)}
+    if dtype == "bf16" and err.size:
+        excess = np.maximum(0.0, err - bf16_half_ulp(ref))
+        floor = float(np.abs(round_bf16(ref) - ref).mean())
+        stats["max_excess_rel"] = float(excess.max() / s)
+        stats["mean_excess_rel"] = max(0.0, float(err.mean()) - floor) / s
     log = os.environ.get("DIFFATTN_PARITY_LOG")
     if log:
         with open(log, "a") as f:
@@ -120,6 +127,6 @@ def assert_grad_close(got, ref, dtype: str, what: str = "") -> dict:
     if dtype == "f32":
         assert stats["max_rel"] <= F32_MAX_ABS, f"{what} fp32 gradient {stats}"
     else:
-        assert stats["max_rel"] <= BF16_MAX_ABS, f"{what} bf16 gradient max {stats}"
-        assert stats["mean_rel"] <= BF16_MEAN_ABS, f"{what} bf16 gradient mean {stats}"
+        assert stats["max_excess_rel"] <= BF16_MAX_ABS, f"{what} bf16 gradient max {stats}"
+        assert stats["mean_excess_rel"] <= BF16_MEAN_ABS, f"{what} bf16 gradient mean {stats}"
     return stats
