@@ -378,6 +378,92 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
         return DIFFATTN_ERR_INVALID;
     const diffattn_desc& d = *desc;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (select(desc, q1, k1, q2, k2, v, dout) == DIFFATTN_KERNEL_TCGEN05 && aligned16(dq1) &&
+        aligned16(dk1) && aligned16(dq2) && aligned16(dk2) && aligned16(dv)) {
+        DeviceState* dev = nullptr;
+        rc = device_state(&dev);
+        if (rc != DIFFATTN_OK) return rc;
+        const int64_t g = group_of(d.kv_group);
+        const int64_t hk = d.H / g;
+        // Pass 1: the forward kernel in row-statistics mode.
+        CUtensorMap fmaps[6];
+        if (encode_map(&fmaps[0], q1, 64, &d, d.H, d.q1_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&fmaps[1], k1, 64, &d, hk, d.k1_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&fmaps[2], q2, 64, &d, d.H, d.q2_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&fmaps[3], k2, 64, &d, hk, d.k2_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&fmaps[4], v, 128, &d, hk, d.v_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&fmaps[5], dout, 128, &d, d.H, d.o_stride, 64, 32) != DIFFATTN_OK)
+            return DIFFATTN_ERR_CUDA;
+        TcParams f;
+        f.B = (int)d.B;
+        f.H = (int)d.H;
+        f.T = (int)d.T;
+        f.nq = (int)((d.T + 127) / 128);
+        f.nk = (int)((d.T + 63) / 64);
+        f.total_items = (int)(d.B * d.H * f.nq);
+        f.group = (int)(d.B * d.H);
+        f.causal = causal ? 1 : 0;
+        f.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.D));
+        f.lambda = 0.f;
+        f.lambda_dev = nullptr;
+        f.out = nullptr;
+        f.o_sB = f.o_sH = f.o_sT = 0;
+        f.status = dev->status;
+        f.sched = nullptr;
+        f.norm = kNormNone;
+        f.norm_eps = 0.f;
+        f.norm_weight = f.norm_bias = nullptr;
+        f.out_scale = 1.0f;
+        f.kv_group = (int)g;
+        f.k_shared = same_tensor(k1, d.k1_stride, k2, d.k2_stride, d.B, hk, d.T) ? 1 : 0;
+        f.stats = static_cast<float*>(workspace);
+        f.dout = static_cast<const __nv_bfloat16*>(dout);
+        f.do_sB = d.o_stride[0];
+        f.do_sH = d.o_stride[1];
+        f.do_sT = d.o_stride[2];
+        const int fgrid = f.total_items < dev->num_sms ? f.total_items : dev->num_sms;
+        if (launch_fwd_tc(fmaps, f, fgrid, st) != 0) return DIFFATTN_ERR_CUDA;
+        // Pass 2: dQ, then dK and dV, on the tensor cores.
+        CUtensorMap maps[12];
+        if (encode_map(&maps[0], q1, 64, &d, d.H, d.q1_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&maps[1], k1, 64, &d, hk, d.k1_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[2], q2, 64, &d, d.H, d.q2_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&maps[3], k2, 64, &d, hk, d.k2_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[4], v, 128, &d, hk, d.v_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[5], dout, 128, &d, d.H, d.o_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&maps[6], q1, 64, &d, d.H, d.q1_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[7], k1, 64, &d, hk, d.k1_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&maps[8], q2, 64, &d, d.H, d.q2_stride, 64, 64) != DIFFATTN_OK ||
+            encode_map(&maps[9], k2, 64, &d, hk, d.k2_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&maps[10], v, 128, &d, hk, d.v_stride, 64, 128) != DIFFATTN_OK ||
+            encode_map(&maps[11], dout, 128, &d, d.H, d.o_stride, 64, 64) != DIFFATTN_OK)
+            return DIFFATTN_ERR_CUDA;
+        BwdTcParams b;
+        b.B = (int)d.B;
+        b.H = (int)d.H;
+        b.Hk = (int)hk;
+        b.kv_group = (int)g;
+        b.T = (int)d.T;
+        b.nq128 = (int)((d.T + 127) / 128);
+        b.nk64 = (int)((d.T + 63) / 64);
+        b.nk128 = (int)((d.T + 127) / 128);
+        b.causal = causal ? 1 : 0;
+        b.scale = (float)(1.0 / std::sqrt((double)d.D));
+        b.scale_log2 = f.scale_log2;
+        b.lambda = lambda;
+        b.lambda_dev = lambda_dev;
+        b.status = dev->status;
+        b.stats = f.stats;
+        b.dq1 = dq1;
+        b.dq2 = dq2;
+        b.dk1 = dk1;
+        b.dk2 = dk2;
+        b.dv = dv;
+        if (launch_bwd_tc(maps, b, dev->num_sms, st) != 0) return DIFFATTN_ERR_CUDA;
+        return launch_bwd_dlambda(f.stats, d.B * d.H * d.T, dlambda, st) == 0 ? DIFFATTN_OK
+                                                                             : DIFFATTN_ERR_CUDA;
+    }
     BwdParams p;
     p.B = (int)d.B;
     p.H = (int)d.H;
@@ -408,7 +494,6 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
     copy3(p.s_do, d.o_stride);
     p.stats = static_cast<float*>(workspace);
     p.dlambda = dlambda;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     rc = (d.dtype == DIFFATTN_F32) ? launch_bwd_simt_f32(p, st) : launch_bwd_simt_bf16(p, st);
     return rc == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }

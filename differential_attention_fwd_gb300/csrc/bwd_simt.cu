@@ -342,6 +342,11 @@ int launch(const BwdParams& p, cudaStream_t stream) {
 
 }  // namespace bwd
 
+int launch_bwd_dlambda(const float* stats, int64_t rows, float* out, cudaStream_t stream) {
+    bwd::bwd_dlambda_kernel<<<1, 1024, 0, stream>>>(stats, rows, out);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
 int launch_bwd_simt_f32(const BwdParams& p, cudaStream_t stream) { return bwd::launch<float>(p, stream); }
 int launch_bwd_simt_bf16(const BwdParams& p, cudaStream_t stream) {
     return bwd::launch<__nv_bfloat16>(p, stream);

@@ -1,0 +1,759 @@
+// bwd_tc.cu -- backward of the differential-attention forward on the sm_103a
+// tensor cores (bf16, D = 64, V width 128).
+//
+// Given dO = dL/dO for O = (A_1 - lambda A_2) V (paperleet "Differential
+// Transformer Attention", Return requirements: gradients through both Q/K
+// branches, the value and the coefficient), and the row statistics of the
+// first pass (the forward kernel in statistics mode: lse_b, the log2-sum-exp
+// of branch b's scaled scores, and Dd_b = dO . (A_b V) per query row):
+//
+//   A_b  = 2^(S_b * log2(e) / sqrt(D) - lse_b)          S_b = Q_b K_b^T
+//   dP   = dO V^T
+//   dS_1 = A_1 * (dP - Dd_1)        dS_2 = -lambda A_2 * (dP - Dd_2)
+//   dQ_b = dS_b K_b / sqrt(D)       dK_b = dS_b^T Q_b / sqrt(D)
+//   dV   = (A_1 - lambda A_2)^T dO
+//
+// Two kernels, both persistent (one CTA per SM) with a TMA producer warp, one
+// MMA-issuing thread and two warpgroups that turn scores into gradients of the
+// scores in tensor memory (TMEM):
+//
+// dq kernel: work item (b, h, 128-query tile); TMEM lanes are query rows.
+//   Per 64-key tile j: S_1, S_2 and dP (three M128 N64 MMAs from shared
+//   memory) into one of two TMEM buffers; warpgroup b forms dS_b from S_b and
+//   dP and writes it back over S_b as bf16; then dQ_b += dS_b K_b (A from
+//   TMEM, K_b read MN-major from the same shared-memory tile the score product
+//   read K-major).  Buffers alternate so that tile j+1's products overlap
+//   tile j's elementwise work.
+//
+// dkdv kernel: work item (b, key/value head, 128-key tile); TMEM lanes are key
+//   rows.  For every query head of the group and every 64-query tile:
+//   S_1^T = K_1 Q_1^T, S_2^T, dP^T = V dO^T; the two warpgroups split the 64
+//   query columns, form dS_1^T, dS_2^T and W^T = A_1^T - lambda A_2^T and write
+//   them back as bf16; then dV += W^T dO, dK_b += dS_b^T Q_b.  The item's
+//   accumulators (dV, dK_1, dK_2: 256 columns) leave room for one set of
+//   score buffers (192 columns), so the elementwise work of a tile and the
+//   products of the next do not overlap.
+//
+// Causal masking: key j is visible to query i iff j <= i; key tiles above the
+// diagonal are skipped and crossing tiles are masked element by element
+// (masked entries have A_b = 0, hence dS_b = 0 and no contribution to dV).
+// Every mbarrier wait is bounded (see ptx.cuh); on expiry the kernel records
+// DIFFATTN_ERR_TIMEOUT in the status word, drains and frees TMEM.
+#include "kernels.h"
+#include "ptx.cuh"
+
+#include <cmath>
+
+namespace diffattn {
+namespace bwdtc {
+
+constexpr int HD = 64;             // Q/K width D
+constexpr int VD = 128;            // V/O width 2D
+constexpr int NUM_THREADS = 384;
+constexpr uint32_t REGS_WORK = 200;
+constexpr uint32_t REGS_OTHER = 104;
+static_assert(256 * REGS_WORK + 128 * REGS_OTHER <= NUM_THREADS * 168, "register split");
+
+// The CTA's k-th work item in a boustrophedon order over the item list.
+__device__ __forceinline__ int item_index(int k, int cta, int grid) {
+    const int base = k * grid;
+    return base + ((k & 1) ? (grid - 1 - cta) : cta);
+}
+
+// ===========================================================================
+// dq kernel
+// ===========================================================================
+namespace dq {
+
+constexpr int BM = 128;            // query rows per item (TMEM lanes)
+constexpr int BN = 64;             // keys per tile
+constexpr int KSTAGES = 4;         // (K1, K2) ring
+constexpr int VSTAGES = 3;         // V ring
+constexpr uint32_t Q_BYTES = BM * HD * 2;          // 16 KB
+constexpr uint32_t DO_HALF = BM * 64 * 2;          // 16 KB per 64-column half
+constexpr uint32_t K_BYTES = BN * HD * 2;          // 8 KB
+constexpr uint32_t V_HALF = BN * 64 * 2;           // 8 KB
+constexpr uint32_t V_BYTES = 2 * V_HALF;
+
+constexpr uint32_t OFF_Q1 = 0;
+constexpr uint32_t OFF_Q2 = OFF_Q1 + Q_BYTES;
+constexpr uint32_t OFF_DO = OFF_Q2 + Q_BYTES;                  // two halves
+constexpr uint32_t OFF_K = OFF_DO + 2 * DO_HALF;                // stage s: K1 +0, K2 +K_BYTES
+constexpr uint32_t OFF_V = OFF_K + KSTAGES * 2 * K_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + VSTAGES * V_BYTES;
+constexpr int BAR_Q_FULL = 0;
+constexpr int BAR_Q_EMPTY = 1;
+constexpr int BAR_K_FULL = 2;
+constexpr int BAR_K_EMPTY = BAR_K_FULL + KSTAGES;
+constexpr int BAR_V_FULL = BAR_K_EMPTY + KSTAGES;
+constexpr int BAR_V_EMPTY = BAR_V_FULL + VSTAGES;
+constexpr int BAR_S_FULL = BAR_V_EMPTY + VSTAGES;     // [buffer]
+constexpr int BAR_DS_FULL = BAR_S_FULL + 2;           // [buffer], 8 warps
+constexpr int BAR_DQ_FULL = BAR_DS_FULL + 2;
+constexpr int BAR_DQ_EMPTY = BAR_DQ_FULL + 1;         // 8 warps
+constexpr int BAR_FINAL = BAR_DQ_EMPTY + 1;
+constexpr int NUM_BARS = BAR_FINAL + 1;
+constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
+constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// TMEM: buffer b at b*192: S1 +0, S2 +64, dP +128; dQ1 at 384, dQ2 at 448.
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_DQ = 384;
+constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);     // Q x K^T, dO x V^T
+constexpr uint32_t IDESC_DQ = idesc_bf16_f32(BM, HD, 0, 1);    // dS (TMEM) x K (MN-major)
+
+struct Item {
+    int b, h, qt, n_kv;
+};
+__device__ __forceinline__ Item decode_item(int idx, const BwdTcParams& p) {
+    // longest first: the last query tiles of every head, then the ones before
+    const int BH = p.B * p.H;
+    const int r = idx / BH;
+    const int bh = idx - r * BH;
+    Item it;
+    it.qt = p.causal ? (p.nq128 - 1 - r) : r;
+    it.b = bh / p.H;
+    it.h = bh - it.b * p.H;
+    it.n_kv = p.causal ? min(2 * it.qt + 2, p.nk64) : p.nk64;
+    return it;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
+                       const __grid_constant__ CUtensorMap tm_k1,
+                       const __grid_constant__ CUtensorMap tm_q2,
+                       const __grid_constant__ CUtensorMap tm_k2,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_do,
+                       const BwdTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + OFF_TMEM_PTR);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_ABORT);
+    const uint32_t warp = warp_id();
+    const uint32_t lane = threadIdx.x & 31;
+    const AbortState ab{abort_flag, p.status};
+    const int total = p.B * p.H * p.nq128;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[BAR_Q_FULL], 1);
+        mbar_init(&bars[BAR_Q_EMPTY], 1);
+        for (int s = 0; s < KSTAGES; ++s) {
+            mbar_init(&bars[BAR_K_FULL + s], 1);
+            mbar_init(&bars[BAR_K_EMPTY + s], 1);
+        }
+        for (int s = 0; s < VSTAGES; ++s) {
+            mbar_init(&bars[BAR_V_FULL + s], 1);
+            mbar_init(&bars[BAR_V_EMPTY + s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[BAR_S_FULL + i], 1);
+            mbar_init(&bars[BAR_DS_FULL + i], 8);
+        }
+        mbar_init(&bars[BAR_DQ_FULL], 1);
+        mbar_init(&bars[BAR_DQ_EMPTY], 8);
+        mbar_init(&bars[BAR_FINAL], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(tmem_ptr, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_ptr;
+    const int grid = gridDim.x, cta = blockIdx.x;
+
+    if (warp >= 8) {
+        regs_dec<REGS_OTHER>();
+        if (warp == 8) {
+            // ------------------------------------------------------ producer
+            if (elect_one()) {
+                uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0;
+                uint32_t armed_q = 0, armed_k[KSTAGES] = {}, armed_v[VSTAGES] = {};
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int idx = item_index(k, cta, grid);
+                    if (idx >= total) break;
+                    const Item it = decode_item(idx, p);
+                    const int hk = it.h / p.kv_group;
+                    if (k > 0) {
+                        if (!(ok = mbar_wait(&bars[BAR_Q_EMPTY], qph, ab))) break;
+                        qph ^= 1;
+                    }
+                    mbar_arrive_expect_tx(&bars[BAR_Q_FULL], 2 * Q_BYTES + 2 * DO_HALF);
+                    tma_load_4d(smem + OFF_Q1, &tm_q1, &bars[BAR_Q_FULL], 0, it.qt * BM, it.h, it.b);
+                    tma_load_4d(smem + OFF_Q2, &tm_q2, &bars[BAR_Q_FULL], 0, it.qt * BM, it.h, it.b);
+                    tma_load_4d(smem + OFF_DO, &tm_do, &bars[BAR_Q_FULL], 0, it.qt * BM, it.h, it.b);
+                    tma_load_4d(smem + OFF_DO + DO_HALF, &tm_do, &bars[BAR_Q_FULL], 64, it.qt * BM,
+                                it.h, it.b);
+                    ++armed_q;
+                    for (int j = 0; j < it.n_kv; ++j) {
+                        if (!(ok = mbar_wait(&bars[BAR_K_EMPTY + kst], kph ^ 1, ab))) break;
+                        uint8_t* kd = smem + OFF_K + kst * 2 * K_BYTES;
+                        mbar_arrive_expect_tx(&bars[BAR_K_FULL + kst], 2 * K_BYTES);
+                        tma_load_4d(kd, &tm_k1, &bars[BAR_K_FULL + kst], 0, j * BN, hk, it.b);
+                        tma_load_4d(kd + K_BYTES, &tm_k2, &bars[BAR_K_FULL + kst], 0, j * BN, hk, it.b);
+                        ++armed_k[kst];
+                        if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
+                        if (!(ok = mbar_wait(&bars[BAR_V_EMPTY + vst], vph ^ 1, ab))) break;
+                        uint8_t* vd = smem + OFF_V + vst * V_BYTES;
+                        mbar_arrive_expect_tx(&bars[BAR_V_FULL + vst], V_BYTES);
+                        tma_load_4d(vd, &tm_v, &bars[BAR_V_FULL + vst], 0, j * BN, hk, it.b);
+                        tma_load_4d(vd + V_HALF, &tm_v, &bars[BAR_V_FULL + vst], 64, j * BN, hk, it.b);
+                        ++armed_v[vst];
+                        if (++vst == VSTAGES) { vst = 0; vph ^= 1; }
+                    }
+                }
+                const uint64_t lim = 200ull * 1000ull * 1000ull;
+                if (armed_q) mbar_wait_teardown(&bars[BAR_Q_FULL], (armed_q - 1) & 1, lim);
+                for (int s = 0; s < KSTAGES; ++s)
+                    if (armed_k[s]) mbar_wait_teardown(&bars[BAR_K_FULL + s], (armed_k[s] - 1) & 1, lim);
+                for (int s = 0; s < VSTAGES; ++s)
+                    if (armed_v[s]) mbar_wait_teardown(&bars[BAR_V_FULL + s], (armed_v[s] - 1) & 1, lim);
+            }
+            __syncwarp();
+        } else if (warp == 9) {
+            // ------------------------------------------------------ MMA issue
+            if (elect_one()) {
+                const uint64_t q1d = sdesc_sw128(smem_u32(smem + OFF_Q1), 16, 1024);
+                const uint64_t q2d = sdesc_sw128(smem_u32(smem + OFF_Q2), 16, 1024);
+                const uint64_t dod = sdesc_sw128(smem_u32(smem + OFF_DO), 16, 1024);
+                const uint64_t kkd = sdesc_sw128(smem_u32(smem + OFF_K), 16, 1024);        // K-major
+                const uint64_t kmd = sdesc_sw128(smem_u32(smem + OFF_K), K_BYTES, 1024);   // MN-major
+                const uint64_t vd = sdesc_sw128(smem_u32(smem + OFF_V), 16, 1024);
+                uint32_t kc = 0;            // key tiles consumed so far (K ring position)
+                uint32_t vst = 0, vph = 0, qph = 0, dqph = 0, dsph = 0;
+                bool ok = true;
+                // S_1, S_2, dP of key tile t into buffer buf
+                auto issue_s = [&](uint32_t kt, int buf) -> bool {
+                    const uint32_t ks = kt % KSTAGES;
+                    if (!mbar_wait(&bars[BAR_K_FULL + ks], (kt / KSTAGES) & 1u, ab)) return false;
+                    if (!mbar_wait(&bars[BAR_V_FULL + vst], vph, ab)) return false;
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + buf * 192;
+                    const uint64_t k1 = kkd + ((ks * 2 * K_BYTES) >> 4);
+                    const uint64_t k2 = k1 + (K_BYTES >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        mma_ss(d, q1d + 2 * kk, k1 + 2 * kk, IDESC_S, kk > 0);
+                        mma_ss(d + 64, q2d + 2 * kk, k2 + 2 * kk, IDESC_S, kk > 0);
+                    }
+                    const uint64_t v0 = vd + ((vst * V_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < VD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * (DO_HALF >> 4) + 2 * (kk & 3);
+                        const uint32_t voff = (kk >> 2) * (V_HALF >> 4) + 2 * (kk & 3);
+                        mma_ss(d + 128, dod + off, v0 + voff, IDESC_S, kk > 0);
+                    }
+                    mma_commit(&bars[BAR_S_FULL + buf]);
+                    mma_commit(&bars[BAR_V_EMPTY + vst]);
+                    if (++vst == VSTAGES) { vst = 0; vph ^= 1; }
+                    return true;
+                };
+                bool first = true;
+                for (int k = 0; ok; ++k) {
+                    const int idx = item_index(k, cta, grid);
+                    if (idx >= total) break;
+                    const Item it = decode_item(idx, p);
+                    const int n = it.n_kv;
+                    if (!(ok = mbar_wait(&bars[BAR_Q_FULL], qph, ab))) break;
+                    qph ^= 1;
+                    for (int t = 0; t < 2 && t < n && ok; ++t) ok = issue_s(kc + t, t);
+                    if (!ok) break;
+                    if (n <= 2) mma_commit(&bars[BAR_Q_EMPTY]);
+                    for (int j = 0; j < n; ++j) {
+                        const int buf = j & 1;
+                        if (!(ok = mbar_wait(&bars[BAR_DS_FULL + buf], (dsph >> buf) & 1u, ab))) break;
+                        dsph ^= 1u << buf;
+                        if (j == 0 && !first) {
+                            if (!(ok = mbar_wait(&bars[BAR_DQ_EMPTY], dqph, ab))) break;
+                            dqph ^= 1;
+                        }
+                        tc_fence_after();
+                        const uint32_t ks = (kc + j) % KSTAGES;
+                        const uint64_t k1 = kmd + ((ks * 2 * K_BYTES) >> 4);
+                        const uint64_t k2 = k1 + (K_BYTES >> 4);
+                        const uint32_t a = tmem_base + buf * 192;
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            mma_ts(tmem_base + TM_DQ, a + kk * 8, k1 + 128 * kk, IDESC_DQ,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                            mma_ts(tmem_base + TM_DQ + 64, a + 64 + kk * 8, k2 + 128 * kk, IDESC_DQ,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&bars[BAR_K_EMPTY + ks]);
+                        if (j + 2 < n) {
+                            if (!(ok = issue_s(kc + j + 2, buf))) break;
+                            if (j + 3 == n) mma_commit(&bars[BAR_Q_EMPTY]);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&bars[BAR_DQ_FULL]);
+                    kc += n;
+                    first = false;
+                }
+                mma_commit(&bars[BAR_FINAL]);
+                mbar_wait_teardown(&bars[BAR_FINAL], 0, 200ull * 1000ull * 1000ull);
+            }
+            __syncwarp();
+        }
+    } else {
+        regs_inc<REGS_WORK>();
+        // ------------------------------------------- dS and the dQ epilogue
+        const int br = warp >> 2;
+        const uint32_t quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = tmem_base + ((quad * 32u) << 16);
+        const float sl2 = p.scale_log2;
+        const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
+        const float coef = br ? -lam : 1.0f;
+        uint32_t sph = 0, dqph = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int idx = item_index(k, cta, grid);
+            if (idx >= total) break;
+            const Item it = decode_item(idx, p);
+            const int q = it.qt * BM + row;
+            const bool live = q < p.T;
+            float lse = 0.f, dd = 0.f;
+            if (live) {
+                const float4 st = *reinterpret_cast<const float4*>(
+                    p.stats + (((int64_t)it.b * p.H + it.h) * p.T + q) * 4);
+                lse = br ? st.y : st.x;
+                dd = br ? st.w : st.z;
+            }
+            for (int j = 0; j < it.n_kv; ++j) {
+                const int buf = j & 1;
+                const uint32_t tS = lane_base + buf * 192 + br * 64;
+                const uint32_t tP = lane_base + buf * 192 + 128;
+                if (!(ok = mbar_wait_warp(&bars[BAR_S_FULL + buf], (sph >> buf) & 1u, ab))) break;
+                sph ^= 1u << buf;
+                tc_fence_after();
+                uint32_t s[64], dp[64];
+                tmem_ld32(tS, &s[0]);
+                tmem_ld32(tS + 32, &s[32]);
+                tmem_ld32(tP, &dp[0]);
+                tmem_ld32(tP + 32, &dp[32]);
+                tmem_wait_ld();
+                const int kv0 = j * BN;
+                // keys kv0 + c with c > lim are masked (future, or past T)
+                int lim = p.causal ? q - kv0 : 63;
+                if (p.T - 1 - kv0 < lim) lim = p.T - 1 - kv0;
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    float a0 = ex2_approx(fmaf(__uint_as_float(s[2 * c]), sl2, -lse));
+                    float a1 = ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -lse));
+                    a0 = (2 * c > lim) ? 0.f : a0;
+                    a1 = (2 * c + 1 > lim) ? 0.f : a1;
+                    const float d0 = coef * a0 * (__uint_as_float(dp[2 * c]) - dd);
+                    const float d1 = coef * a1 * (__uint_as_float(dp[2 * c + 1]) - dd);
+                    pk[c] = pack_bf16x2(d0, d1);
+                }
+                tmem_st32(tS, pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[BAR_DS_FULL + buf]);
+            }
+            if (!ok) break;
+            // dQ_b = scale * (dS_b K_b): this warpgroup's 64 columns
+            if (!(ok = mbar_wait_warp(&bars[BAR_DQ_FULL], dqph, ab))) break;
+            dqph ^= 1;
+            tc_fence_after();
+            uint32_t g[64];
+            tmem_ld32(lane_base + TM_DQ + br * 64, &g[0]);
+            tmem_ld32(lane_base + TM_DQ + br * 64 + 32, &g[32]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[BAR_DQ_EMPTY]);
+            if (live) {
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(br ? p.dq2 : p.dq1) +
+                                     (((int64_t)it.b * p.H + it.h) * p.T + q) * HD;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = 8 * i;
+                    *reinterpret_cast<uint4*>(dst + c) = make_uint4(
+                        pack_bf16x2(__uint_as_float(g[c]) * p.scale, __uint_as_float(g[c + 1]) * p.scale),
+                        pack_bf16x2(__uint_as_float(g[c + 2]) * p.scale, __uint_as_float(g[c + 3]) * p.scale),
+                        pack_bf16x2(__uint_as_float(g[c + 4]) * p.scale, __uint_as_float(g[c + 5]) * p.scale),
+                        pack_bf16x2(__uint_as_float(g[c + 6]) * p.scale, __uint_as_float(g[c + 7]) * p.scale));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace dq
+
+// ===========================================================================
+// dkdv kernel
+// ===========================================================================
+namespace dkdv {
+
+constexpr int BM = 128;            // key rows per item (TMEM lanes)
+constexpr int BN = 64;             // query rows per tile
+constexpr int QSTAGES = 3;         // (Q1, Q2, dO, row statistics) ring
+constexpr uint32_t K_BYTES = BM * HD * 2;          // 16 KB
+constexpr uint32_t V_HALF = BM * 64 * 2;           // 16 KB
+constexpr uint32_t Q_BYTES = BN * HD * 2;          // 8 KB
+constexpr uint32_t DO_HALF = BN * 64 * 2;          // 8 KB
+constexpr uint32_t ST_BYTES = BN * 16;             // 1 KB: 4 floats per query row
+constexpr uint32_t QSTAGE_BYTES = 2 * Q_BYTES + 2 * DO_HALF + ST_BYTES;   // 33 KB
+constexpr uint32_t QS_Q1 = 0, QS_Q2 = Q_BYTES, QS_DO = 2 * Q_BYTES, QS_ST = 2 * Q_BYTES + 2 * DO_HALF;
+
+constexpr uint32_t OFF_K1 = 0;
+constexpr uint32_t OFF_K2 = OFF_K1 + K_BYTES;
+constexpr uint32_t OFF_V = OFF_K2 + K_BYTES;                       // two halves
+constexpr uint32_t OFF_QS = OFF_V + 2 * V_HALF;                    // stages (1024-aligned)
+constexpr uint32_t QSTAGE_STRIDE = (QSTAGE_BYTES + 1023) & ~1023u;
+constexpr uint32_t OFF_BAR = OFF_QS + QSTAGES * QSTAGE_STRIDE;
+constexpr int BAR_KV_FULL = 0;
+constexpr int BAR_KV_EMPTY = 1;
+constexpr int BAR_Q_FULL = 2;
+constexpr int BAR_Q_EMPTY = BAR_Q_FULL + QSTAGES;
+constexpr int BAR_S_FULL = BAR_Q_EMPTY + QSTAGES;
+constexpr int BAR_DS_FULL = BAR_S_FULL + 1;           // 8 warps
+constexpr int BAR_ACC_FULL = BAR_DS_FULL + 1;
+constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + 1;       // 8 warps
+constexpr int BAR_FINAL = BAR_ACC_EMPTY + 1;
+constexpr int NUM_BARS = BAR_FINAL + 1;
+constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
+constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// TMEM: S1^T [0,64), S2^T [64,128), dP^T [128,192); dV [192,320), dK1
+// [320,384), dK2 [384,448).
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S1 = 0, TM_S2 = 64, TM_DP = 128, TM_DV = 192, TM_DK1 = 320, TM_DK2 = 384;
+constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);     // K x Q^T, V x dO^T
+constexpr uint32_t IDESC_DV = idesc_bf16_f32(BM, VD, 0, 1);    // W^T (TMEM) x dO (MN-major)
+constexpr uint32_t IDESC_DK = idesc_bf16_f32(BM, HD, 0, 1);    // dS^T (TMEM) x Q (MN-major)
+
+struct Item {
+    int b, hk, kt;
+    int qt0;        // first 64-row query tile that sees a key of the tile
+    int per_head;   // query tiles per head
+};
+__device__ __forceinline__ Item decode_item(int idx, const BwdTcParams& p) {
+    // longest first: causal key tiles near the start see the most queries
+    const int BHk = p.B * p.Hk;
+    const int r = idx / BHk;
+    const int bhk = idx - r * BHk;
+    Item it;
+    it.kt = r;
+    it.b = bhk / p.Hk;
+    it.hk = bhk - it.b * p.Hk;
+    it.qt0 = p.causal ? 2 * r : 0;
+    it.per_head = p.nk64 - it.qt0;     // 64-row query tiles [qt0, nk64)
+    return it;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
+                         const __grid_constant__ CUtensorMap tm_k1,
+                         const __grid_constant__ CUtensorMap tm_q2,
+                         const __grid_constant__ CUtensorMap tm_k2,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_do,
+                         const BwdTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + OFF_TMEM_PTR);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_ABORT);
+    const uint32_t warp = warp_id();
+    const uint32_t lane = threadIdx.x & 31;
+    const AbortState ab{abort_flag, p.status};
+    const int total = p.B * p.Hk * p.nk128;
+    const int g = p.kv_group;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[BAR_KV_FULL], 1);
+        mbar_init(&bars[BAR_KV_EMPTY], 1);
+        for (int s = 0; s < QSTAGES; ++s) {
+            mbar_init(&bars[BAR_Q_FULL + s], 1);
+            mbar_init(&bars[BAR_Q_EMPTY + s], 1);
+        }
+        mbar_init(&bars[BAR_S_FULL], 1);
+        mbar_init(&bars[BAR_DS_FULL], 8);
+        mbar_init(&bars[BAR_ACC_FULL], 1);
+        mbar_init(&bars[BAR_ACC_EMPTY], 8);
+        mbar_init(&bars[BAR_FINAL], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(tmem_ptr, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_ptr;
+    const int grid = gridDim.x, cta = blockIdx.x;
+
+    if (warp >= 8) {
+        regs_dec<REGS_OTHER>();
+        if (warp == 8) {
+            // ------------------------------------------------------ producer
+            if (elect_one()) {
+                uint32_t qs = 0, qph = 0, kvph = 0;
+                uint32_t armed_kv = 0, armed_q[QSTAGES] = {};
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int idx = item_index(k, cta, grid);
+                    if (idx >= total) break;
+                    const Item it = decode_item(idx, p);
+                    if (k > 0) {
+                        if (!(ok = mbar_wait(&bars[BAR_KV_EMPTY], kvph, ab))) break;
+                        kvph ^= 1;
+                    }
+                    const int k0 = it.kt * BM;
+                    mbar_arrive_expect_tx(&bars[BAR_KV_FULL], 2 * K_BYTES + 2 * V_HALF);
+                    tma_load_4d(smem + OFF_K1, &tm_k1, &bars[BAR_KV_FULL], 0, k0, it.hk, it.b);
+                    tma_load_4d(smem + OFF_K2, &tm_k2, &bars[BAR_KV_FULL], 0, k0, it.hk, it.b);
+                    tma_load_4d(smem + OFF_V, &tm_v, &bars[BAR_KV_FULL], 0, k0, it.hk, it.b);
+                    tma_load_4d(smem + OFF_V + V_HALF, &tm_v, &bars[BAR_KV_FULL], 64, k0, it.hk, it.b);
+                    ++armed_kv;
+                    for (int t = 0; t < g * it.per_head && ok; ++t) {
+                        const int h = it.hk * g + t / it.per_head;
+                        const int qt = it.qt0 + t % it.per_head;
+                        if (!(ok = mbar_wait(&bars[BAR_Q_EMPTY + qs], qph ^ 1, ab))) break;
+                        uint8_t* st = smem + OFF_QS + qs * QSTAGE_STRIDE;
+                        const int q0 = qt * BN;
+                        const int rows = min(BN, p.T - q0);
+                        mbar_arrive_expect_tx(&bars[BAR_Q_FULL + qs],
+                                              2 * Q_BYTES + 2 * DO_HALF + (uint32_t)rows * 16u);
+                        tma_load_4d(st + QS_Q1, &tm_q1, &bars[BAR_Q_FULL + qs], 0, q0, h, it.b);
+                        tma_load_4d(st + QS_Q2, &tm_q2, &bars[BAR_Q_FULL + qs], 0, q0, h, it.b);
+                        tma_load_4d(st + QS_DO, &tm_do, &bars[BAR_Q_FULL + qs], 0, q0, h, it.b);
+                        tma_load_4d(st + QS_DO + DO_HALF, &tm_do, &bars[BAR_Q_FULL + qs], 64, q0, h, it.b);
+                        bulk_load(st + QS_ST, p.stats + (((int64_t)it.b * p.H + h) * p.T + q0) * 4,
+                                  (uint32_t)rows * 16u, &bars[BAR_Q_FULL + qs]);
+                        ++armed_q[qs];
+                        if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                    }
+                }
+                const uint64_t lim = 200ull * 1000ull * 1000ull;
+                if (armed_kv) mbar_wait_teardown(&bars[BAR_KV_FULL], (armed_kv - 1) & 1, lim);
+                for (int s = 0; s < QSTAGES; ++s)
+                    if (armed_q[s]) mbar_wait_teardown(&bars[BAR_Q_FULL + s], (armed_q[s] - 1) & 1, lim);
+            }
+            __syncwarp();
+        } else if (warp == 9) {
+            // ------------------------------------------------------ MMA issue
+            if (elect_one()) {
+                const uint64_t k1d = sdesc_sw128(smem_u32(smem + OFF_K1), 16, 1024);
+                const uint64_t k2d = sdesc_sw128(smem_u32(smem + OFF_K2), 16, 1024);
+                const uint64_t vd = sdesc_sw128(smem_u32(smem + OFF_V), 16, 1024);
+                const uint64_t qk = sdesc_sw128(smem_u32(smem + OFF_QS), 16, 1024);       // K-major
+                const uint64_t qm = sdesc_sw128(smem_u32(smem + OFF_QS), DO_HALF, 1024);  // MN-major
+                uint32_t qs = 0, qph = 0, kvph = 0, accph = 0, dsph = 0;
+                bool ok = true, first = true;
+                for (int k = 0; ok; ++k) {
+                    const int idx = item_index(k, cta, grid);
+                    if (idx >= total) break;
+                    const Item it = decode_item(idx, p);
+                    const int n = g * it.per_head;
+                    if (!(ok = mbar_wait(&bars[BAR_KV_FULL], kvph, ab))) break;
+                    kvph ^= 1;
+                    for (int t = 0; t < n; ++t) {
+                        if (!(ok = mbar_wait(&bars[BAR_Q_FULL + qs], qph, ab))) break;
+                        tc_fence_after();
+                        const uint64_t sb = (qs * QSTAGE_STRIDE) >> 4;
+                        // S_1^T, S_2^T, dP^T
+#pragma unroll
+                        for (int kk = 0; kk < HD / 16; ++kk) {
+                            mma_ss(tmem_base + TM_S1, k1d + 2 * kk, qk + sb + (QS_Q1 >> 4) + 2 * kk,
+                                   IDESC_S, kk > 0);
+                            mma_ss(tmem_base + TM_S2, k2d + 2 * kk, qk + sb + (QS_Q2 >> 4) + 2 * kk,
+                                   IDESC_S, kk > 0);
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < VD / 16; ++kk) {
+                            const uint32_t aoff = (kk >> 2) * (V_HALF >> 4) + 2 * (kk & 3);
+                            const uint32_t boff = (QS_DO >> 4) + (kk >> 2) * (DO_HALF >> 4) + 2 * (kk & 3);
+                            mma_ss(tmem_base + TM_DP, vd + aoff, qk + sb + boff, IDESC_S, kk > 0);
+                        }
+                        mma_commit(&bars[BAR_S_FULL]);
+                        if (t == n - 1) mma_commit(&bars[BAR_KV_EMPTY]);
+                        if (!(ok = mbar_wait(&bars[BAR_DS_FULL], dsph, ab))) break;
+                        dsph ^= 1;
+                        if (t == 0 && !first) {
+                            if (!(ok = mbar_wait(&bars[BAR_ACC_EMPTY], accph, ab))) break;
+                            accph ^= 1;
+                        }
+                        tc_fence_after();
+                        // dV += W^T dO, dK_b += dS_b^T Q_b.  The bf16 A operands
+                        // sit at columns [0,16) (queries 0-31) and [32,48)
+                        // (queries 32-63) of their score regions.
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            const uint32_t acol = (kk < 2 ? 0u : 32u) + (kk & 1) * 8;
+                            const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                            const uint64_t dob = qm + sb + (QS_DO >> 4) + 128 * kk;
+                            mma_ts(tmem_base + TM_DV, tmem_base + TM_DP + acol, dob, IDESC_DV, acc);
+                            mma_ts(tmem_base + TM_DK1, tmem_base + TM_S1 + acol,
+                                   qm + sb + (QS_Q1 >> 4) + 128 * kk, IDESC_DK, acc);
+                            mma_ts(tmem_base + TM_DK2, tmem_base + TM_S2 + acol,
+                                   qm + sb + (QS_Q2 >> 4) + 128 * kk, IDESC_DK, acc);
+                        }
+                        mma_commit(&bars[BAR_Q_EMPTY + qs]);
+                        if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                    }
+                    if (!ok) break;
+                    mma_commit(&bars[BAR_ACC_FULL]);
+                    first = false;
+                }
+                mma_commit(&bars[BAR_FINAL]);
+                mbar_wait_teardown(&bars[BAR_FINAL], 0, 200ull * 1000ull * 1000ull);
+            }
+            __syncwarp();
+        }
+    } else {
+        regs_inc<REGS_WORK>();
+        // ---------------------------------- dS^T, W^T and the dK/dV epilogue
+        const int half = warp >> 2;          // query columns [32*half, 32*half + 32)
+        const uint32_t quad = warp & 3;
+        const int row = quad * 32 + lane;    // key row within the tile
+        const uint32_t lane_base = tmem_base + ((quad * 32u) << 16);
+        const float sl2 = p.scale_log2;
+        const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
+        uint32_t sph = 0, accph = 0, qc = 0;   // qc: query tiles consumed (stage ring position)
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int idx = item_index(k, cta, grid);
+            if (idx >= total) break;
+            const Item it = decode_item(idx, p);
+            const int key = it.kt * BM + row;
+            const int n = g * it.per_head;
+            for (int t = 0; t < n; ++t, ++qc) {
+                const int qt = it.qt0 + t % it.per_head;
+                const uint32_t qs = qc % QSTAGES;
+                if (!(ok = mbar_wait_warp(&bars[BAR_S_FULL], sph, ab))) break;
+                sph ^= 1;
+                // the stage's row statistics came by TMA: observe its completion
+                if (!(ok = mbar_wait_warp(&bars[BAR_Q_FULL + qs], (qc / QSTAGES) & 1u, ab))) break;
+                tc_fence_after();
+                const uint32_t c0 = 32 * half;
+                uint32_t s1[32], s2[32], dp[32];
+                tmem_ld32(lane_base + TM_S1 + c0, s1);
+                tmem_ld32(lane_base + TM_S2 + c0, s2);
+                tmem_ld32(lane_base + TM_DP + c0, dp);
+                const float4* stv = reinterpret_cast<const float4*>(
+                    smem + OFF_QS + qs * QSTAGE_STRIDE + QS_ST) + c0;
+                tmem_wait_ld();
+                // query qt*64 + c0 + c sees this key iff key <= query (and query < T)
+                const int qbase = qt * BN + (int)c0;
+                int first_vis = p.causal ? key - qbase : 0;     // columns c >= first_vis are visible
+                const int qlim = p.T - qbase;                   // columns c < qlim exist
+                uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const float4 sa = stv[c], sb = stv[c + 1];
+                    const bool v0 = c >= first_vis && c < qlim;
+                    const bool v1 = c + 1 >= first_vis && c + 1 < qlim;
+                    const float a10 = v0 ? ex2_approx(fmaf(__uint_as_float(s1[c]), sl2, -sa.x)) : 0.f;
+                    const float a11 = v1 ? ex2_approx(fmaf(__uint_as_float(s1[c + 1]), sl2, -sb.x)) : 0.f;
+                    const float a20 = v0 ? ex2_approx(fmaf(__uint_as_float(s2[c]), sl2, -sa.y)) : 0.f;
+                    const float a21 = v1 ? ex2_approx(fmaf(__uint_as_float(s2[c + 1]), sl2, -sb.y)) : 0.f;
+                    const float p0 = __uint_as_float(dp[c]), p1 = __uint_as_float(dp[c + 1]);
+                    // statistics of queries at or past T are not loaded: select, never
+                    // multiply, so that whatever the buffer holds cannot reach the sums
+                    const float d10 = v0 ? a10 * (p0 - sa.z) : 0.f;
+                    const float d11 = v1 ? a11 * (p1 - sb.z) : 0.f;
+                    const float d20 = v0 ? -lam * a20 * (p0 - sa.w) : 0.f;
+                    const float d21 = v1 ? -lam * a21 * (p1 - sb.w) : 0.f;
+                    w1[c / 2] = pack_bf16x2(d10, d11);
+                    w2[c / 2] = pack_bf16x2(d20, d21);
+                    w3[c / 2] = pack_bf16x2(a10 - lam * a20, a11 - lam * a21);
+                }
+                tmem_st16(lane_base + TM_S1 + c0, w1);
+                tmem_st16(lane_base + TM_S2 + c0, w2);
+                tmem_st16(lane_base + TM_DP + c0, w3);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[BAR_DS_FULL]);
+            }
+            if (!ok) break;
+            // epilogue: warpgroup 0 writes dV columns 0-63 and dK_1, warpgroup
+            // 1 dV columns 64-127 and dK_2
+            if (!(ok = mbar_wait_warp(&bars[BAR_ACC_FULL], accph, ab))) break;
+            accph ^= 1;
+            tc_fence_after();
+            uint32_t gv[64], gk[64];
+            tmem_ld32(lane_base + TM_DV + 64 * half, &gv[0]);
+            tmem_ld32(lane_base + TM_DV + 64 * half + 32, &gv[32]);
+            tmem_ld32(lane_base + (half ? TM_DK2 : TM_DK1), &gk[0]);
+            tmem_ld32(lane_base + (half ? TM_DK2 : TM_DK1) + 32, &gk[32]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[BAR_ACC_EMPTY]);
+            if (key < p.T) {
+                const int64_t krow = ((int64_t)it.b * p.Hk + it.hk) * p.T + key;
+                __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(p.dv) + krow * VD + 64 * half;
+                __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(half ? p.dk2 : p.dk1) + krow * HD;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = 8 * i;
+                    *reinterpret_cast<uint4*>(dv + c) = make_uint4(
+                        pack_bf16x2(__uint_as_float(gv[c]), __uint_as_float(gv[c + 1])),
+                        pack_bf16x2(__uint_as_float(gv[c + 2]), __uint_as_float(gv[c + 3])),
+                        pack_bf16x2(__uint_as_float(gv[c + 4]), __uint_as_float(gv[c + 5])),
+                        pack_bf16x2(__uint_as_float(gv[c + 6]), __uint_as_float(gv[c + 7])));
+                    *reinterpret_cast<uint4*>(dk + c) = make_uint4(
+                        pack_bf16x2(__uint_as_float(gk[c]) * p.scale, __uint_as_float(gk[c + 1]) * p.scale),
+                        pack_bf16x2(__uint_as_float(gk[c + 2]) * p.scale, __uint_as_float(gk[c + 3]) * p.scale),
+                        pack_bf16x2(__uint_as_float(gk[c + 4]) * p.scale, __uint_as_float(gk[c + 5]) * p.scale),
+                        pack_bf16x2(__uint_as_float(gk[c + 6]) * p.scale, __uint_as_float(gk[c + 7]) * p.scale));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace dkdv
+
+}  // namespace bwdtc
+
+int launch_bwd_tc(const CUtensorMap* maps, const BwdTcParams& p, int num_sms, cudaStream_t stream) {
+    using namespace bwdtc;
+    if (cudaFuncSetAttribute(dq::diffattn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dq::SMEM_BYTES) != cudaSuccess)
+        return -1;
+    if (cudaFuncSetAttribute(dkdv::diffattn_bwd_dkdv_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dkdv::SMEM_BYTES) != cudaSuccess)
+        return -1;
+    const int dq_items = p.B * p.H * p.nq128;
+    const int kv_items = p.B * p.Hk * p.nk128;
+    dq::diffattn_bwd_dq_kernel<<<dq_items < num_sms ? dq_items : num_sms, NUM_THREADS,
+                                 dq::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3],
+                                                           maps[4], maps[5], p);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    dkdv::diffattn_bwd_dkdv_kernel<<<kv_items < num_sms ? kv_items : num_sms, NUM_THREADS,
+                                     dkdv::SMEM_BYTES, stream>>>(maps[6], maps[7], maps[8],
+                                                                 maps[9], maps[10], maps[11], p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace diffattn

@@ -535,6 +535,44 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             if (!(ok = mbar_wait_warp(&bars[BAR_O_FULL], ofph, ab))) break;
             ofph ^= 1;
             tc_fence_after();
+            if (p.stats) {
+                // Row statistics for the backward: this branch's log2-sum-exp
+                // and Dd_b = dO . (O_b / l_b), 32 columns at a time.
+                const bool live = q < p.T;
+                const __nv_bfloat16* g = p.dout + it.b * p.do_sB + it.h * p.do_sH +
+                                         (int64_t)(live ? q : 0) * p.do_sT;
+                float dd = 0.f;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c4 * 32, o);
+                    uint4 gv[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        gv[i] = live ? *reinterpret_cast<const uint4*>(g + c4 * 32 + 8 * i)
+                                     : make_uint4(0, 0, 0, 0);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t w[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            dd = fmaf(__uint_as_float(o[8 * i + 2 * e]), __uint_as_float(w[e] << 16), dd);
+                            dd = fmaf(__uint_as_float(o[8 * i + 2 * e + 1]),
+                                      __uint_as_float(w[e] & 0xffff0000u), dd);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[BAR_O_EMPTY]);
+                if (live) {
+                    float* st = p.stats + (((int64_t)it.b * p.H + it.h) * p.T + q) * 4;
+                    st[br] = m_run + log2f(l);
+                    st[2 + br] = dd / l;
+                }
+                continue;
+            }
             inv_l[br * BM + row] = 1.0f / l;
             const int c0 = br * 64;          // this warpgroup writes output columns [c0, c0+64)
             uint32_t o1[64], o2[64];

@@ -35,6 +35,13 @@ struct TcParams {
     float out_scale;            // applied last
     int kv_group;               // query heads per key/value head (>= 1)
     int k_shared;               // K1 and K2 are one tensor: load each key tile once
+    // Row-statistics mode (the first pass of the backward): when stats is set,
+    // the epilogue writes, per query row, the log2-sum-exp of each branch's
+    // scaled scores and Dd_b = dO . (A_b V) to stats[(b*H + h)*T + t][0..3]
+    // (lse_1, lse_2, Dd_1, Dd_2) instead of writing O.
+    float* stats;
+    const __nv_bfloat16* dout;
+    int64_t do_sB, do_sH, do_sT;
 };
 
 // Parameters of the CUDA-core kernel (any D <= 128, fp32 or bf16).
@@ -97,6 +104,21 @@ struct BwdParams {
     float* dlambda;         // one float
 };
 
+// Parameters of the tensor-core backward (bf16, D = 64).  Gradients are dense
+// like BwdParams'; stats holds the forward kernel's row statistics (log2 units).
+struct BwdTcParams {
+    int B, H, Hk, kv_group, T;
+    int nq128, nk64, nk128;     // 128-row and 64-row tiles along T
+    int causal;
+    float scale;                // 1 / sqrt(D)
+    float scale_log2;           // log2(e) / sqrt(D)
+    float lambda;
+    const float* lambda_dev;
+    uint32_t* status;
+    const float* stats;
+    void* dq1; void* dq2; void* dk1; void* dk2; void* dv;
+};
+
 // Decode helpers: query-row bucket (rows rounded up to 1, 2, 4 or 8; 0 if
 // there are more rows than one CTA of width D takes), and the number of
 // workspace floats for `units` CTAs along the heads and query rows.
@@ -108,6 +130,9 @@ size_t decode_work_floats(int64_t units, int splits, int tq_bucket, int64_t D);
 int launch_decode(const DecodeParams& p, cudaStream_t stream);
 int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v,out*/, const TcParams& p, int grid,
                   cudaStream_t stream);
+int launch_bwd_tc(const CUtensorMap* maps /*dq: q1,k1,q2,k2,v,do; dkdv: the same*/,
+                  const BwdTcParams& p, int num_sms, cudaStream_t stream);
+int launch_bwd_dlambda(const float* stats, int64_t rows, float* out, cudaStream_t stream);
 int launch_bwd_simt_f32(const BwdParams& p, cudaStream_t stream);
 int launch_bwd_simt_bf16(const BwdParams& p, cudaStream_t stream);
 int launch_fwd_simt_f32(const SimtParams& p, cudaStream_t stream);

@@ -123,3 +123,45 @@ def test_backward_rejects_bad_arguments():
     dev = [to_device(x, "f32") for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
     with pytest.raises(ValueError):
         da.differential_attention_backward(*dev, 0.5, to_device(dout[:, :, :8], "f32"))
+
+
+# ---------------------------------------------------------------------------
+# The tensor-core backward (bf16, D = 64, aligned): ragged lengths, both masks,
+# grouped heads, shared keys, several tiles per item
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 128, 129, 200, 257, 1000])
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_tensor_core_ragged(T, causal):
+    inp, dout = draw(1, 2, 2, T, 64, "bf16", seed=100 + T)
+    check(inp, dout, "bf16", 0.8, causal, f"tc bwd T={T} causal={causal}")
+
+
+@pytest.mark.parametrize("H,Hk", [(8, 2), (4, 1), (6, 3)])
+def test_backward_tensor_core_grouped(H, Hk):
+    inp, dout = draw(2, H, Hk, 700, 64, "bf16", seed=H * 10 + Hk)
+    for causal in (True, False):
+        check(inp, dout, "bf16", -0.4, causal, f"tc bwd grouped {H}/{Hk} causal={causal}")
+
+
+def test_backward_tensor_core_long_and_reproducible():
+    inp, dout = draw(1, 4, 4, 2048, 64, "bf16", seed=200)
+    got = check(inp, dout, "bf16", 0.6, True, "tc bwd T=2048")
+    dev = [to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    again = da.differential_attention_backward(*dev, 0.6, to_device(dout, "bf16"), True)
+    for x, y in zip(got, again):
+        assert torch.equal(x, y)
+
+
+def test_backward_unaligned_view_runs_on_cuda_cores():
+    # a view that starts 2 bytes past a 16-byte boundary cannot use TMA; the
+    # CUDA-core backward takes it and must agree with the oracle as well
+    inp, dout = draw(1, 2, 2, 150, 64, "bf16", seed=201)
+    base = [to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    shifted = []
+    for t in base:
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+        view = buf[1:].view(t.shape)
+        view.copy_(t)
+        shifted.append(view)
+    assert shifted[0].data_ptr() % 16 != 0
+    check(inp, dout, "bf16", 0.7, True, "simt bwd unaligned bf16", dev_inputs=shifted)
