@@ -482,6 +482,169 @@ def run_e2e(args, w, lib, da, _lib, host, lam_vecs_host, lam_init, d_in, d_lv, d
             "ms_per_step": 1e3 * max_s / steps}
 
 
+BWD_FLOPS_PER_PAIR_PER_D = 20   # recompute S_1, S_2 (4D), dP (4D), dV (4D), dQ_1, dQ_2 (4D), dK_1, dK_2 (4D)
+
+
+def bwd_flops(w) -> int:
+    """Algorithmic backward FLOPs: 20 D per unmasked (query, key) pair."""
+    return w.B * w.H * w.pairs_per_head * BWD_FLOPS_PER_PAIR_PER_D * w.D
+
+
+def cpu_baseline_backward(inp, dout, w, lam, budget_s=15.0):
+    """The oracle's backward, as it stands, on whole heads until ~budget_s."""
+    import oracle
+    from oracle import diffattn_oracle as O
+    g = w.H // w.Hk
+    secs, heads = 0.0, 0
+    for b in range(w.B):
+        for h in range(w.H):
+            hk = h // g
+            t0 = time.perf_counter()
+            O._head_backward(*(np.asarray(x, dtype=np.float64) for x in
+                               (inp.q1[b, h], inp.k1[b, hk], inp.q2[b, h], inp.k2[b, hk],
+                                inp.v[b, hk], dout[b, h])), lam, w.causal)
+            secs += time.perf_counter() - t0
+            heads += 1
+            if secs >= budget_s:
+                break
+        if secs >= budget_s:
+            break
+    flops = heads * w.pairs_per_head * BWD_FLOPS_PER_PAIR_PER_D * w.D
+    return {"value": flops / secs / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"float64 NumPy oracle backward, {heads} whole heads of {w.B * w.H} "
+                      f"(T={w.T}, {flops / 1e9:.1f} GFLOP algorithmic) in {secs:.1f} s"}
+
+
+def run_backward(args, w, world, rank, local):
+    """The backward (diffattn_bwd): row statistics, dQ, dK/dV and dlambda."""
+    import torch
+    import differential_attention_fwd_gb300 as da
+    from differential_attention_fwd_gb300 import _lib
+    from differential_attention_fwd_gb300 import build as build_mod
+
+    build_mod.build()
+    lib = _lib.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    inp = W.draw(w)
+    rng = np.random.Generator(np.random.PCG64(w.seed + 1000))
+    dout = rng.standard_normal((w.B, w.H, w.T, w.Dv), dtype=np.float32)
+    if w.dtype == "bf16":
+        dout = W.round_to_bf16(dout)
+    lam = lambda_for(w, inp)
+    host = [torch.from_numpy(x).to(tdt) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v, dout)]
+    d_in = [h.to(dev) for h in host]
+    if w.shared_keys:
+        host[3], d_in[3] = host[1], d_in[1]
+    grads = [torch.empty(t.shape, dtype=tdt, device=dev) for t in d_in[:5]]
+    d_lam = torch.empty((), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    desc = da.make_desc(*d_in[:5], d_in[5])
+    need = int(lib.diffattn_bwd_workspace_bytes(ctypes.byref(desc)))
+    ws = torch.empty(need // 4 + 4, dtype=torch.float32, device=dev)
+    ptrs = [ctypes.c_void_p(t.data_ptr()) for t in d_in]
+    gptrs = [ctypes.c_void_p(t.data_ptr()) for t in grads]
+
+    def step():
+        rc = lib.diffattn_bwd(ctypes.byref(desc), *ptrs[:5], ctypes.c_float(lam), None,
+                              1 if w.causal else 0, ptrs[5], *gptrs, ctypes.c_void_p(d_lam.data_ptr()),
+                              ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(need),
+                              ctypes.c_void_p(stream.cuda_stream))
+        if rc:
+            raise _lib.DiffattnError(rc, "diffattn_bwd")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if da.get_device_error() != 0:
+        raise RuntimeError("a kernel wait ran out during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local) if (args.clocks and rank == 0) else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    barrier(world)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    max_s = reduce_max(sum(ms) / 1e3, world)
+    if da.get_device_error() != 0:
+        raise RuntimeError("a kernel wait ran out during the timed steps")
+    flops = bwd_flops(w)
+    peaks, src = load_peaks()
+    avg_s = statistics.mean(ms) / 1e3
+    achieved = flops / avg_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+
+    e2e = None
+    if args.e2e:
+        pin = []
+        for d, h in zip(d_in, host):
+            if all(d is not u for u, _ in pin):
+                pin.append((d, h.pin_memory()))
+        out_host = [torch.empty(g.shape, dtype=g.dtype).pin_memory() for g in grads]
+        lam_host = torch.empty((), dtype=torch.float32).pin_memory()
+        h2d = sum(h.numel() * h.element_size() for _, h in pin)
+        d2h = sum(t.numel() * t.element_size() for t in out_host) + 4
+        steps = max(1, min(args.steps, args.e2e_steps))
+
+        def one():
+            for d, h in pin:
+                d.copy_(h, non_blocking=True)
+            step()
+            for o, g in zip(out_host, grads):
+                o.copy_(g, non_blocking=True)
+            lam_host.copy_(d_lam, non_blocking=True)
+
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        barrier(world)
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            one()
+            b.record(stream)
+        torch.cuda.synchronize()
+        secs = reduce_max(sum(a.elapsed_time(b) for a, b in evs) / 1e3, world)
+        e2e = {"value": job_value(flops, steps, world, secs), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+               "ms_per_step": 1e3 * secs / steps}
+    result = {
+        "metric": f"diffattn_bwd TFLOP/s, algorithmic 20*D per unmasked pair "
+                  f"(B={w.B},H={w.H},T={w.T},D={w.D} {'causal' if w.causal else 'full'})",
+        "value": job_value(flops, args.steps, world, max_s), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {**config_of(w, lam), "gflop_per_step": flops / 1e9,
+                   "executed_gflop_per_step": flops * 2 / 1e9,
+                   "pass": "backward: forward kernel in row-statistics mode, dQ kernel, "
+                           "dK/dV kernel, dlambda reduction (4 launches per step)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{src} bf16_tflops (burst)",
+                     "scope": "the whole diffattn_bwd call (4 launches); per-kernel shares in profiles/"},
+        "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_backward(inp, dout, w, lam, args.cpu_budget)
+    return result
+
+
 def run_decode(args, world, rank, local):
     """Decode (Tq queries over a Tk-key cache): HBM-bound, so the metric is
     algorithmic GB/s (K1, K2, V read once; Q read and O written once)."""
@@ -566,7 +729,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
-    ap.add_argument("--mode", choices=["forward", "decode"], default="forward")
+    ap.add_argument("--mode", choices=["forward", "backward", "decode"], default="forward")
     ap.add_argument("--decode-workload", default="decode_b16h16q1k8192", choices=sorted(W.DECODE_WORKLOADS))
     ap.add_argument("--norm", choices=["none", "rms", "group"], default="none",
                     help="fuse a per-head norm and the (1 - lambda_init) multiplier")
@@ -591,6 +754,8 @@ def main(argv=None):
         return
     if args.impl == "reference":
         res = run_reference(args, w, world, rank)
+    elif args.mode == "backward":
+        res = run_backward(args, w, world, rank, local)
     else:
         res = run_ours(args, w, world, rank, local)
     if rank == 0 and res is not None:

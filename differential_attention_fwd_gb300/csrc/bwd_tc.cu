@@ -29,10 +29,12 @@
 //   rows.  For every query head of the group and every 64-query tile:
 //   S_1^T = K_1 Q_1^T, S_2^T, dP^T = V dO^T; the two warpgroups split the 64
 //   query columns, form dS_1^T, dS_2^T and W^T = A_1^T - lambda A_2^T and write
-//   them back as bf16; then dV += W^T dO, dK_b += dS_b^T Q_b.  The item's
-//   accumulators (dV, dK_1, dK_2: 256 columns) leave room for one set of
-//   score buffers (192 columns), so the elementwise work of a tile and the
-//   products of the next do not overlap.
+//   them as bf16 operands to shared memory; then dV += W^T dO,
+//   dK_b += dS_b^T Q_b.  The item's accumulators (dV, dK_1, dK_2: 256
+//   columns) leave room for one set of score buffers (192 columns); the
+//   warpgroups copy a tile's scores to registers and release the buffers at
+//   once, so the next tile's score products run during this tile's
+//   elementwise work.
 //
 // Causal masking: key j is visible to query i iff j <= i; key tiles above the
 // diagonal are skipped and crossing tiles are masked element by element
@@ -418,14 +420,20 @@ constexpr uint32_t OFF_K2 = OFF_K1 + K_BYTES;
 constexpr uint32_t OFF_V = OFF_K2 + K_BYTES;                       // two halves
 constexpr uint32_t OFF_QS = OFF_V + 2 * V_HALF;                    // stages (1024-aligned)
 constexpr uint32_t QSTAGE_STRIDE = (QSTAGE_BYTES + 1023) & ~1023u;
-constexpr uint32_t OFF_BAR = OFF_QS + QSTAGES * QSTAGE_STRIDE;
+// bf16 operands written by the elementwise warps: dS_1^T, dS_2^T, W^T, each
+// [128 keys x 64 queries], K-major with 128-byte swizzling
+constexpr uint32_t PK_BYTES = BM * BN * 2;                         // 16 KB
+constexpr uint32_t OFF_PK = OFF_QS + QSTAGES * QSTAGE_STRIDE;
+constexpr uint32_t OFF_BAR = OFF_PK + 3 * PK_BYTES;
 constexpr int BAR_KV_FULL = 0;
 constexpr int BAR_KV_EMPTY = 1;
 constexpr int BAR_Q_FULL = 2;
 constexpr int BAR_Q_EMPTY = BAR_Q_FULL + QSTAGES;
 constexpr int BAR_S_FULL = BAR_Q_EMPTY + QSTAGES;
-constexpr int BAR_DS_FULL = BAR_S_FULL + 1;           // 8 warps
-constexpr int BAR_ACC_FULL = BAR_DS_FULL + 1;
+constexpr int BAR_S_FREE = BAR_S_FULL + 1;            // 8 warps: scores read from TMEM
+constexpr int BAR_DS_FULL = BAR_S_FREE + 1;           // 8 warps: bf16 operands in smem
+constexpr int BAR_PK_FREE = BAR_DS_FULL + 1;          // MMA: the operands have been read
+constexpr int BAR_ACC_FULL = BAR_PK_FREE + 1;
 constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + 1;       // 8 warps
 constexpr int BAR_FINAL = BAR_ACC_EMPTY + 1;
 constexpr int NUM_BARS = BAR_FINAL + 1;
@@ -439,8 +447,8 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S1 = 0, TM_S2 = 64, TM_DP = 128, TM_DV = 192, TM_DK1 = 320, TM_DK2 = 384;
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);     // K x Q^T, V x dO^T
-constexpr uint32_t IDESC_DV = idesc_bf16_f32(BM, VD, 0, 1);    // W^T (TMEM) x dO (MN-major)
-constexpr uint32_t IDESC_DK = idesc_bf16_f32(BM, HD, 0, 1);    // dS^T (TMEM) x Q (MN-major)
+constexpr uint32_t IDESC_DV = idesc_bf16_f32(BM, VD, 0, 1);    // W^T (smem) x dO (MN-major)
+constexpr uint32_t IDESC_DK = idesc_bf16_f32(BM, HD, 0, 1);    // dS^T (smem) x Q (MN-major)
 
 struct Item {
     int b, hk, kt;
@@ -488,7 +496,9 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
             mbar_init(&bars[BAR_Q_EMPTY + s], 1);
         }
         mbar_init(&bars[BAR_S_FULL], 1);
+        mbar_init(&bars[BAR_S_FREE], 8);
         mbar_init(&bars[BAR_DS_FULL], 8);
+        mbar_init(&bars[BAR_PK_FREE], 1);
         mbar_init(&bars[BAR_ACC_FULL], 1);
         mbar_init(&bars[BAR_ACC_EMPTY], 8);
         mbar_init(&bars[BAR_FINAL], 1);
@@ -561,8 +571,36 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 const uint64_t vd = sdesc_sw128(smem_u32(smem + OFF_V), 16, 1024);
                 const uint64_t qk = sdesc_sw128(smem_u32(smem + OFF_QS), 16, 1024);       // K-major
                 const uint64_t qm = sdesc_sw128(smem_u32(smem + OFF_QS), DO_HALF, 1024);  // MN-major
-                uint32_t qs = 0, qph = 0, kvph = 0, accph = 0, dsph = 0;
+                const uint64_t pkd = sdesc_sw128(smem_u32(smem + OFF_PK), 16, 1024);      // K-major
+                uint32_t kvph = 0, accph = 0, dsph = 0;
+                uint32_t tiles = 0;       // query tiles whose scores were issued (whole launch)
+                uint32_t done = 0;        // query tiles whose dV/dK products were issued
                 bool ok = true, first = true;
+                // S_1^T, S_2^T, dP^T of the next query tile (stage tiles % QSTAGES);
+                // the previous tile's scores must have been read out of TMEM.
+                auto issue_s = [&]() -> bool {
+                    const uint32_t qs = tiles % QSTAGES;
+                    if (tiles > 0 && !mbar_wait(&bars[BAR_S_FREE], (tiles - 1) & 1u, ab)) return false;
+                    if (!mbar_wait(&bars[BAR_Q_FULL + qs], (tiles / QSTAGES) & 1u, ab)) return false;
+                    tc_fence_after();
+                    const uint64_t sb = (qs * QSTAGE_STRIDE) >> 4;
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        mma_ss(tmem_base + TM_S1, k1d + 2 * kk, qk + sb + (QS_Q1 >> 4) + 2 * kk,
+                               IDESC_S, kk > 0);
+                        mma_ss(tmem_base + TM_S2, k2d + 2 * kk, qk + sb + (QS_Q2 >> 4) + 2 * kk,
+                               IDESC_S, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < VD / 16; ++kk) {
+                        const uint32_t aoff = (kk >> 2) * (V_HALF >> 4) + 2 * (kk & 3);
+                        const uint32_t boff = (QS_DO >> 4) + (kk >> 2) * (DO_HALF >> 4) + 2 * (kk & 3);
+                        mma_ss(tmem_base + TM_DP, vd + aoff, qk + sb + boff, IDESC_S, kk > 0);
+                    }
+                    mma_commit(&bars[BAR_S_FULL]);
+                    ++tiles;
+                    return true;
+                };
                 for (int k = 0; ok; ++k) {
                     const int idx = item_index(k, cta, grid);
                     if (idx >= total) break;
@@ -570,26 +608,14 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     const int n = g * it.per_head;
                     if (!(ok = mbar_wait(&bars[BAR_KV_FULL], kvph, ab))) break;
                     kvph ^= 1;
+                    if (!(ok = issue_s())) break;
+                    if (n == 1) mma_commit(&bars[BAR_KV_EMPTY]);
                     for (int t = 0; t < n; ++t) {
-                        if (!(ok = mbar_wait(&bars[BAR_Q_FULL + qs], qph, ab))) break;
-                        tc_fence_after();
-                        const uint64_t sb = (qs * QSTAGE_STRIDE) >> 4;
-                        // S_1^T, S_2^T, dP^T
-#pragma unroll
-                        for (int kk = 0; kk < HD / 16; ++kk) {
-                            mma_ss(tmem_base + TM_S1, k1d + 2 * kk, qk + sb + (QS_Q1 >> 4) + 2 * kk,
-                                   IDESC_S, kk > 0);
-                            mma_ss(tmem_base + TM_S2, k2d + 2 * kk, qk + sb + (QS_Q2 >> 4) + 2 * kk,
-                                   IDESC_S, kk > 0);
+                        // the next tile's scores overlap this tile's elementwise work
+                        if (t + 1 < n) {
+                            if (!(ok = issue_s())) break;
+                            if (t + 2 == n) mma_commit(&bars[BAR_KV_EMPTY]);
                         }
-#pragma unroll
-                        for (int kk = 0; kk < VD / 16; ++kk) {
-                            const uint32_t aoff = (kk >> 2) * (V_HALF >> 4) + 2 * (kk & 3);
-                            const uint32_t boff = (QS_DO >> 4) + (kk >> 2) * (DO_HALF >> 4) + 2 * (kk & 3);
-                            mma_ss(tmem_base + TM_DP, vd + aoff, qk + sb + boff, IDESC_S, kk > 0);
-                        }
-                        mma_commit(&bars[BAR_S_FULL]);
-                        if (t == n - 1) mma_commit(&bars[BAR_KV_EMPTY]);
                         if (!(ok = mbar_wait(&bars[BAR_DS_FULL], dsph, ab))) break;
                         dsph ^= 1;
                         if (t == 0 && !first) {
@@ -597,22 +623,22 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                             accph ^= 1;
                         }
                         tc_fence_after();
-                        // dV += W^T dO, dK_b += dS_b^T Q_b.  The bf16 A operands
-                        // sit at columns [0,16) (queries 0-31) and [32,48)
-                        // (queries 32-63) of their score regions.
+                        const uint32_t qs = done % QSTAGES;
+                        const uint64_t sb = (qs * QSTAGE_STRIDE) >> 4;
+                        // dV += W^T dO, dK_b += dS_b^T Q_b (A operands from shared memory)
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk) {
-                            const uint32_t acol = (kk < 2 ? 0u : 32u) + (kk & 1) * 8;
                             const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                            const uint64_t dob = qm + sb + (QS_DO >> 4) + 128 * kk;
-                            mma_ts(tmem_base + TM_DV, tmem_base + TM_DP + acol, dob, IDESC_DV, acc);
-                            mma_ts(tmem_base + TM_DK1, tmem_base + TM_S1 + acol,
+                            mma_ss(tmem_base + TM_DV, pkd + 2 * (PK_BYTES >> 4) + 2 * kk,
+                                   qm + sb + (QS_DO >> 4) + 128 * kk, IDESC_DV, acc);
+                            mma_ss(tmem_base + TM_DK1, pkd + 2 * kk,
                                    qm + sb + (QS_Q1 >> 4) + 128 * kk, IDESC_DK, acc);
-                            mma_ts(tmem_base + TM_DK2, tmem_base + TM_S2 + acol,
+                            mma_ss(tmem_base + TM_DK2, pkd + (PK_BYTES >> 4) + 2 * kk,
                                    qm + sb + (QS_Q2 >> 4) + 128 * kk, IDESC_DK, acc);
                         }
+                        mma_commit(&bars[BAR_PK_FREE]);
                         mma_commit(&bars[BAR_Q_EMPTY + qs]);
-                        if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                        ++done;
                     }
                     if (!ok) break;
                     mma_commit(&bars[BAR_ACC_FULL]);
@@ -632,7 +658,7 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
         const uint32_t lane_base = tmem_base + ((quad * 32u) << 16);
         const float sl2 = p.scale_log2;
         const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
-        uint32_t sph = 0, accph = 0, qc = 0;   // qc: query tiles consumed (stage ring position)
+        uint32_t accph = 0, qc = 0;   // qc: query tiles consumed (whole launch)
         bool ok = true;
         for (int k = 0; ok; ++k) {
             const int idx = item_index(k, cta, grid);
@@ -643,8 +669,7 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
             for (int t = 0; t < n; ++t, ++qc) {
                 const int qt = it.qt0 + t % it.per_head;
                 const uint32_t qs = qc % QSTAGES;
-                if (!(ok = mbar_wait_warp(&bars[BAR_S_FULL], sph, ab))) break;
-                sph ^= 1;
+                if (!(ok = mbar_wait_warp(&bars[BAR_S_FULL], qc & 1u, ab))) break;
                 // the stage's row statistics came by TMA: observe its completion
                 if (!(ok = mbar_wait_warp(&bars[BAR_Q_FULL + qs], (qc / QSTAGES) & 1u, ab))) break;
                 tc_fence_after();
@@ -656,10 +681,14 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 const float4* stv = reinterpret_cast<const float4*>(
                     smem + OFF_QS + qs * QSTAGE_STRIDE + QS_ST) + c0;
                 tmem_wait_ld();
+                // the scores are in registers: the next tile's products may overwrite them
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[BAR_S_FREE]);
                 // query qt*64 + c0 + c sees this key iff key <= query (and query < T)
                 const int qbase = qt * BN + (int)c0;
-                int first_vis = p.causal ? key - qbase : 0;     // columns c >= first_vis are visible
-                const int qlim = p.T - qbase;                   // columns c < qlim exist
+                const int first_vis = p.causal ? key - qbase : 0;   // columns c >= first_vis are visible
+                const int qlim = p.T - qbase;                         // columns c < qlim exist
                 uint32_t w1[16], w2[16], w3[16];
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
@@ -681,11 +710,22 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     w2[c / 2] = pack_bf16x2(d20, d21);
                     w3[c / 2] = pack_bf16x2(a10 - lam * a20, a11 - lam * a21);
                 }
-                tmem_st16(lane_base + TM_S1 + c0, w1);
-                tmem_st16(lane_base + TM_S2 + c0, w2);
-                tmem_st16(lane_base + TM_DP + c0, w3);
-                tmem_wait_st();
-                tc_fence_before();
+                // the previous tile's dV/dK products must have read the operands
+                if (qc > 0 && !(ok = mbar_wait_warp(&bars[BAR_PK_FREE], (qc - 1) & 1u, ab))) break;
+                // row `row`, queries [c0, c0 + 32) = 16-byte chunks 4*half .. 4*half + 3,
+                // swizzled by the row's position within its 8-row group
+                uint8_t* prow = smem + OFF_PK + row * 128;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t off = (uint32_t)(((4 * half + i) ^ (row & 7)) * 16);
+                    *reinterpret_cast<uint4*>(prow + off) =
+                        make_uint4(w1[4 * i], w1[4 * i + 1], w1[4 * i + 2], w1[4 * i + 3]);
+                    *reinterpret_cast<uint4*>(prow + PK_BYTES + off) =
+                        make_uint4(w2[4 * i], w2[4 * i + 1], w2[4 * i + 2], w2[4 * i + 3]);
+                    *reinterpret_cast<uint4*>(prow + 2 * PK_BYTES + off) =
+                        make_uint4(w3[4 * i], w3[4 * i + 1], w3[4 * i + 2], w3[4 * i + 3]);
+                }
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[BAR_DS_FULL]);
             }
