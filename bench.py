@@ -633,12 +633,12 @@ def run_backward(args, w, world, rank, local):
         "config": {**config_of(w, lam), "gflop_per_step": flops / 1e9,
                    "executed_gflop_per_step": flops * 2 / 1e9,
                    "pass": "backward: forward kernel in row-statistics mode, dQ kernel, "
-                           "dK/dV kernel, dlambda reduction (4 launches per step)"},
+                           "dK/dV kernel, dlambda reduction in two launches (5 launches per step)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
                      "peak_source": f"{src} bf16_tflops (burst)",
-                     "scope": "the whole diffattn_bwd call (4 launches); per-kernel shares in profiles/"},
-        "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clocks,
+                     "scope": "the whole diffattn_bwd call (5 launches); per-kernel shares in profiles/"},
+        "e2e": e2e, "gpu_launches": 5 * args.steps, "clocks": clocks,
     }
     if rank == 0 and world == 1 and args.cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_backward(inp, dout, w, lam, args.cpu_budget)

@@ -362,7 +362,8 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
 
 size_t diffattn_bwd_workspace_bytes(const diffattn_desc* desc) {
     if (!desc || desc->B < 1 || desc->H < 1 || desc->T < 1) return 0;
-    return (size_t)desc->B * desc->H * desc->T * 4 * sizeof(float);
+    // row statistics (4 floats per query row), then 128 floats of partial sums
+    return (size_t)desc->B * desc->H * desc->T * 4 * sizeof(float) + 128 * sizeof(float);
 }
 
 int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,

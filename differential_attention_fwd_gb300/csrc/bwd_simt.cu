@@ -19,7 +19,7 @@
 //   dkdv    one warp per key row of a key/value head: walks the visible query
 //           rows of every query head that reads it, accumulates dK_1, dK_2
 //           and dV;
-//   dlambda one block: -sum of Dd_2 over all rows, in a fixed order.
+//   dlambda -sum of Dd_2 over all rows, in a fixed order (two small launches).
 #include "kernels.h"
 
 #include <cmath>
@@ -307,21 +307,44 @@ __global__ void __launch_bounds__(WARPS * 32) bwd_dkdv_kernel(const BwdParams p)
 }
 
 // ------------------------------------------------------------------ dlambda
-// dlambda = -sum over all rows of Dd_2, summed in a fixed order (each thread a
-// fixed strided subset, then a fixed tree), so the result is reproducible.
-__global__ void __launch_bounds__(1024) bwd_dlambda_kernel(const float* stats, int64_t rows,
-                                                           float* out) {
-    __shared__ float part[32];
+// dlambda = -sum over all rows of Dd_2, summed in a fixed order so that the
+// result is reproducible: block i sums its contiguous share of the rows
+// (threads take fixed strided subsets, then a fixed tree), then one block sums
+// the per-block partials in block order.
+constexpr int DLAMBDA_BLOCKS = 128;
+
+__global__ void __launch_bounds__(256) bwd_dlambda_partial_kernel(const float* stats, int64_t rows,
+                                                                  float* partials) {
+    __shared__ float part[8];
+    const int64_t per = (rows + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = (int64_t)blockIdx.x * per;
+    const int64_t r1 = min(rows, r0 + per);
     float s = 0.f;
-    for (int64_t r = threadIdx.x; r < rows; r += blockDim.x) s += stats[r * 4 + 3];
+    for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) s += stats[r * 4 + 3];
     s = warp_sum(s);
     if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
     __syncthreads();
-    if (threadIdx.x < 32) {
-        float t = part[threadIdx.x];
-        t = warp_sum(t);
-        if (threadIdx.x == 0) *out = -t;
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 8; ++w) t += part[w];
+        partials[blockIdx.x] = t;
     }
+}
+
+__global__ void __launch_bounds__(32) bwd_dlambda_final_kernel(const float* partials, int n,
+                                                               float* out) {
+    float s = 0.f;
+    for (int i = threadIdx.x; i < n; i += 32) s += partials[i];
+    s = warp_sum(s);
+    if (threadIdx.x == 0) *out = -s;
+}
+
+int launch_dlambda(const float* stats, int64_t rows, float* partials, float* out,
+                   cudaStream_t stream) {
+    bwd_dlambda_partial_kernel<<<DLAMBDA_BLOCKS, 256, 0, stream>>>(stats, rows, partials);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    bwd_dlambda_final_kernel<<<1, 32, 0, stream>>>(partials, DLAMBDA_BLOCKS, out);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 template <typename T>
@@ -336,15 +359,14 @@ int launch(const BwdParams& p, cudaStream_t stream) {
     if (cudaGetLastError() != cudaSuccess) return -1;
     bwd_dkdv_kernel<T><<<(unsigned)kblocks, WARPS * 32, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return -1;
-    bwd_dlambda_kernel<<<1, 1024, 0, stream>>>(p.stats, (int64_t)p.B * p.H * p.T, p.dlambda);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    const int64_t rows = (int64_t)p.B * p.H * p.T;
+    return launch_dlambda(p.stats, rows, p.stats + rows * 4, p.dlambda, stream);
 }
 
 }  // namespace bwd
 
 int launch_bwd_dlambda(const float* stats, int64_t rows, float* out, cudaStream_t stream) {
-    bwd::bwd_dlambda_kernel<<<1, 1024, 0, stream>>>(stats, rows, out);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    return bwd::launch_dlambda(stats, rows, const_cast<float*>(stats) + rows * 4, out, stream);
 }
 
 int launch_bwd_simt_f32(const BwdParams& p, cudaStream_t stream) { return bwd::launch<float>(p, stream); }

@@ -100,7 +100,8 @@ struct BwdParams {
     const void* dout;
     void* dq1; void* dk1; void* dq2; void* dk2; void* dv;
     int64_t s_q1[3], s_k1[3], s_q2[3], s_k2[3], s_v[3], s_do[3];
-    float* stats;           // [B, H, T, 4]: log-sum-exp of each branch, Dd_1, Dd_2
+    float* stats;           // [B, H, T, 4]: log-sum-exp of each branch, Dd_1, Dd_2,
+                            // then 128 floats of dlambda partial sums
     float* dlambda;         // one float
 };
 
@@ -132,6 +133,8 @@ int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v,out*/, const TcParams&
                   cudaStream_t stream);
 int launch_bwd_tc(const CUtensorMap* maps /*dq: q1,k1,q2,k2,v,do; dkdv: the same*/,
                   const BwdTcParams& p, int num_sms, cudaStream_t stream);
+// dlambda = -sum of the rows' Dd_2; the 128 floats after the rows' statistics
+// hold the per-block partial sums.
 int launch_bwd_dlambda(const float* stats, int64_t rows, float* out, cudaStream_t stream);
 int launch_bwd_simt_f32(const BwdParams& p, cudaStream_t stream);
 int launch_bwd_simt_bf16(const BwdParams& p, cudaStream_t stream);

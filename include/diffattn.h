@@ -221,8 +221,8 @@ int diffattn_fwd_ex(const diffattn_desc *desc, const void *q1, const void *k1,
 
 /*
  * diffattn_bwd_workspace_bytes -- bytes of device workspace diffattn_bwd needs
- * for this descriptor (four float32 row statistics per query row), or 0 for a
- * NULL descriptor or sizes < 1.
+ * for this descriptor (four float32 row statistics per query row, plus 512
+ * bytes of partial sums), or 0 for a NULL descriptor or sizes < 1.
  */
 size_t diffattn_bwd_workspace_bytes(const diffattn_desc *desc);
 
@@ -251,9 +251,13 @@ size_t diffattn_bwd_workspace_bytes(const diffattn_desc *desc);
  * bytes, 16-byte aligned, owned by the caller; its contents need no
  * initialisation.
  *
- * Runs on the CUDA cores (fp32 arithmetic for either dtype): four launches on
- * `stream` (row statistics, dQ, dK/dV, dlambda), no atomics, so the result is
- * reproducible bit for bit.
+ * Kernels: with bf16, D = 64, 16-byte aligned bases (inputs, dout and the
+ * gradients) and strides that are multiples of 8 elements, on the tensor
+ * cores (bf16 operands, fp32 accumulation): the forward kernel in
+ * row-statistics mode, then a dQ kernel and a dK/dV kernel.  Anything else
+ * valid runs on the CUDA cores in fp32 arithmetic.  Either way five launches on
+ * `stream` (row statistics, dQ, dK/dV, and two for dlambda), no atomics, so
+ * the result is reproducible bit for bit.
  * Errors: DIFFATTN_ERR_INVALID (as diffattn_fwd, plus a NULL gradient pointer,
  * a missing, small or misaligned workspace); DIFFATTN_ERR_CUDA (launch
  * failure).

@@ -234,3 +234,37 @@ def test_decode_grouped_heads_share_ctas(lib):
     assert size(H=8, kv_group=8, Tq=2) == size(H=2, Tq=8)
     assert size(H=8, kv_group=3) == 0
     assert size(H=8, kv_group=-2) == 0
+
+
+def test_bwd_workspace_size(lib):
+    d = desc(B=2, H=4, T=100)
+    assert lib.diffattn_bwd_workspace_bytes(ctypes.byref(d)) == 2 * 4 * 100 * 16 + 512
+    assert lib.diffattn_bwd_workspace_bytes(None) == 0
+    assert lib.diffattn_bwd_workspace_bytes(ctypes.byref(desc(T=0))) == 0
+
+
+def bwd(lib, d, grads=None, ws=FAKE * 30, ws_bytes=1 << 30, lam=0.5):
+    grads = grads if grads is not None else ptrs(5, base=FAKE * 40)
+    return lib.diffattn_bwd(ctypes.byref(d), *ptrs(5), ctypes.c_float(lam), None, 1,
+                            ctypes.c_void_p(FAKE * 9), *grads, ctypes.c_void_p(FAKE * 50),
+                            ctypes.c_void_p(ws), ctypes.c_size_t(ws_bytes), None)
+
+
+def test_bwd_rejects_without_gpu(lib):
+    assert bwd(lib, desc(D=0)) == _lib.DIFFATTN_ERR_INVALID
+    assert bwd(lib, desc(H=6, kv_group=4)) == _lib.DIFFATTN_ERR_INVALID
+    assert bwd(lib, desc(), lam=float("nan")) == _lib.DIFFATTN_ERR_INVALID
+    g = ptrs(5, base=FAKE * 40)
+    g[3] = None
+    assert bwd(lib, desc(), grads=g) == _lib.DIFFATTN_ERR_INVALID
+    assert bwd(lib, desc(), ws_bytes=16) == _lib.DIFFATTN_ERR_INVALID
+    assert bwd(lib, desc(), ws=FAKE * 30 + 4) == _lib.DIFFATTN_ERR_INVALID
+    assert bwd(lib, desc(), ws=0) == _lib.DIFFATTN_ERR_INVALID
+
+
+def test_lambda_backward_rejects_without_gpu(lib):
+    p = ptrs(9)
+    assert lib.diffattn_lambda_backward(*p[:4], 0, *p[4:], None) == _lib.DIFFATTN_ERR_INVALID
+    q = list(p)
+    q[5] = None
+    assert lib.diffattn_lambda_backward(*q[:4], 8, *q[4:], None) == _lib.DIFFATTN_ERR_INVALID
