@@ -462,8 +462,10 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
         b.dk2 = dk2;
         b.dv = dv;
         if (launch_bwd_tc(maps, b, dev->num_sms, st) != 0) return DIFFATTN_ERR_CUDA;
-        return launch_bwd_dlambda(f.stats, d.B * d.H * d.T, dlambda, st) == 0 ? DIFFATTN_OK
-                                                                             : DIFFATTN_ERR_CUDA;
+        // the statistics hold -Dd_2, so dlambda = -sum(Dd_2) is their plain sum
+        return launch_bwd_dlambda(f.stats, d.B * d.H * d.T, 1.0f, dlambda, st) == 0
+                   ? DIFFATTN_OK
+                   : DIFFATTN_ERR_CUDA;
     }
     BwdParams p;
     p.B = (int)d.B;

@@ -332,18 +332,18 @@ __global__ void __launch_bounds__(256) bwd_dlambda_partial_kernel(const float* s
 }
 
 __global__ void __launch_bounds__(32) bwd_dlambda_final_kernel(const float* partials, int n,
-                                                               float* out) {
+                                                               float sign, float* out) {
     float s = 0.f;
     for (int i = threadIdx.x; i < n; i += 32) s += partials[i];
     s = warp_sum(s);
-    if (threadIdx.x == 0) *out = -s;
+    if (threadIdx.x == 0) *out = sign * s;
 }
 
-int launch_dlambda(const float* stats, int64_t rows, float* partials, float* out,
+int launch_dlambda(const float* stats, int64_t rows, float* partials, float sign, float* out,
                    cudaStream_t stream) {
     bwd_dlambda_partial_kernel<<<DLAMBDA_BLOCKS, 256, 0, stream>>>(stats, rows, partials);
     if (cudaGetLastError() != cudaSuccess) return -1;
-    bwd_dlambda_final_kernel<<<1, 32, 0, stream>>>(partials, DLAMBDA_BLOCKS, out);
+    bwd_dlambda_final_kernel<<<1, 32, 0, stream>>>(partials, DLAMBDA_BLOCKS, sign, out);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
@@ -360,13 +360,15 @@ int launch(const BwdParams& p, cudaStream_t stream) {
     bwd_dkdv_kernel<T><<<(unsigned)kblocks, WARPS * 32, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return -1;
     const int64_t rows = (int64_t)p.B * p.H * p.T;
-    return launch_dlambda(p.stats, rows, p.stats + rows * 4, p.dlambda, stream);
+    return launch_dlambda(p.stats, rows, p.stats + rows * 4, -1.0f, p.dlambda, stream);
 }
 
 }  // namespace bwd
 
-int launch_bwd_dlambda(const float* stats, int64_t rows, float* out, cudaStream_t stream) {
-    return bwd::launch_dlambda(stats, rows, const_cast<float*>(stats) + rows * 4, out, stream);
+int launch_bwd_dlambda(const float* stats, int64_t rows, float sign, float* out,
+                       cudaStream_t stream) {
+    return bwd::launch_dlambda(stats, rows, const_cast<float*>(stats) + rows * 4, sign, out,
+                               stream);
 }
 
 int launch_bwd_simt_f32(const BwdParams& p, cudaStream_t stream) { return bwd::launch<float>(p, stream); }

@@ -5,7 +5,8 @@
 // Transformer Attention", Return requirements: gradients through both Q/K
 // branches, the value and the coefficient), and the row statistics of the
 // first pass (the forward kernel in statistics mode: lse_b, the log2-sum-exp
-// of branch b's scaled scores, and Dd_b = dO . (A_b V) per query row):
+// of branch b's scaled scores, and Dd_b = dO . (A_b V) per query row, both
+// stored negated so that the kernels below add them):
 //
 //   A_b  = 2^(S_b * log2(e) / sqrt(D) - lse_b)          S_b = Q_b K_b^T
 //   dP   = dO V^T
@@ -323,13 +324,17 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
             const Item it = decode_item(idx, p);
             const int q = it.qt * BM + row;
             const bool live = q < p.T;
-            float lse = 0.f, dd = 0.f;
+            float nlse = 0.f, ndd = 0.f;    // -lse_b and -Dd_b of this row
             if (live) {
                 const float4 st = *reinterpret_cast<const float4*>(
                     p.stats + (((int64_t)it.b * p.H + it.h) * p.T + q) * 4);
-                lse = br ? st.y : st.x;
-                dd = br ? st.w : st.z;
+                nlse = br ? st.y : st.x;
+                ndd = br ? st.w : st.z;
             }
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t nlse2 = f2_pack(nlse, nlse);
+            const uint64_t coef2 = f2_pack(coef, coef);
+            const uint64_t cndd2 = f2_pack(coef * ndd, coef * ndd);
             for (int j = 0; j < it.n_kv; ++j) {
                 const int buf = j & 1;
                 const uint32_t tS = lane_base + buf * 192 + br * 64;
@@ -344,19 +349,32 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 tmem_ld32(tP + 32, &dp[32]);
                 tmem_wait_ld();
                 const int kv0 = j * BN;
-                // keys kv0 + c with c > lim are masked (future, or past T)
-                int lim = p.causal ? q - kv0 : 63;
-                if (p.T - 1 - kv0 < lim) lim = p.T - 1 - kv0;
+                // only tiles that cross the diagonal or the end of the sequence
+                // need a mask (the decision is the same for the whole CTA)
+                const bool edge = (p.causal && kv0 + BN - 1 > it.qt * BM) || kv0 + BN > p.T;
                 uint32_t pk[32];
+                if (edge) {
+                    // keys kv0 + c with c > lim are masked (future, or past T)
+                    int lim = p.causal ? q - kv0 : 63;
+                    if (p.T - 1 - kv0 < lim) lim = p.T - 1 - kv0;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    float a0 = ex2_approx(fmaf(__uint_as_float(s[2 * c]), sl2, -lse));
-                    float a1 = ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -lse));
-                    a0 = (2 * c > lim) ? 0.f : a0;
-                    a1 = (2 * c + 1 > lim) ? 0.f : a1;
-                    const float d0 = coef * a0 * (__uint_as_float(dp[2 * c]) - dd);
-                    const float d1 = coef * a1 * (__uint_as_float(dp[2 * c + 1]) - dd);
-                    pk[c] = pack_bf16x2(d0, d1);
+                    for (int c = 0; c < 32; ++c) {
+                        const uint64_t x = f2_fma(f2_from_bits(s[2 * c], s[2 * c + 1]), sl2x2, nlse2);
+                        const float a0 = (2 * c > lim) ? 0.f : ex2_approx(f2_lo(x));
+                        const float a1 = (2 * c + 1 > lim) ? 0.f : ex2_approx(f2_hi(x));
+                        const uint64_t y = f2_fma(f2_from_bits(dp[2 * c], dp[2 * c + 1]), coef2, cndd2);
+                        const uint64_t z = f2_mul(f2_pack(a0, a1), y);
+                        pk[c] = pack_bf16x2(f2_lo(z), f2_hi(z));
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const uint64_t x = f2_fma(f2_from_bits(s[2 * c], s[2 * c + 1]), sl2x2, nlse2);
+                        const uint64_t a = f2_pack(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
+                        const uint64_t y = f2_fma(f2_from_bits(dp[2 * c], dp[2 * c + 1]), coef2, cndd2);
+                        const uint64_t z = f2_mul(a, y);
+                        pk[c] = pack_bf16x2(f2_lo(z), f2_hi(z));
+                    }
                 }
                 tmem_st32(tS, pk);
                 tmem_wait_st();
@@ -685,30 +703,54 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[BAR_S_FREE]);
-                // query qt*64 + c0 + c sees this key iff key <= query (and query < T)
+                // query qt*64 + c0 + c sees this key iff key <= query (and query < T);
+                // statistics are stored negated: (-lse_1, -lse_2, -Dd_1, -Dd_2)
                 const int qbase = qt * BN + (int)c0;
-                const int first_vis = p.causal ? key - qbase : 0;   // columns c >= first_vis are visible
-                const int qlim = p.T - qbase;                         // columns c < qlim exist
                 uint32_t w1[16], w2[16], w3[16];
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                const uint64_t nlam2 = f2_pack(-lam, -lam);
+                // only warps whose 32 queries meet the diagonal or the end of the
+                // sequence need a mask (the decision is the same for the whole warp)
+                const bool edge = (p.causal && qbase < it.kt * BM + BM - 1) || qbase + 32 > p.T;
+                if (edge) {
+                    const int first_vis = p.causal ? key - qbase : 0;   // columns c >= first_vis are visible
+                    const int qlim = p.T - qbase;                         // columns c < qlim exist
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const float4 sa = stv[c], sb = stv[c + 1];
-                    const bool v0 = c >= first_vis && c < qlim;
-                    const bool v1 = c + 1 >= first_vis && c + 1 < qlim;
-                    const float a10 = v0 ? ex2_approx(fmaf(__uint_as_float(s1[c]), sl2, -sa.x)) : 0.f;
-                    const float a11 = v1 ? ex2_approx(fmaf(__uint_as_float(s1[c + 1]), sl2, -sb.x)) : 0.f;
-                    const float a20 = v0 ? ex2_approx(fmaf(__uint_as_float(s2[c]), sl2, -sa.y)) : 0.f;
-                    const float a21 = v1 ? ex2_approx(fmaf(__uint_as_float(s2[c + 1]), sl2, -sb.y)) : 0.f;
-                    const float p0 = __uint_as_float(dp[c]), p1 = __uint_as_float(dp[c + 1]);
-                    // statistics of queries at or past T are not loaded: select, never
-                    // multiply, so that whatever the buffer holds cannot reach the sums
-                    const float d10 = v0 ? a10 * (p0 - sa.z) : 0.f;
-                    const float d11 = v1 ? a11 * (p1 - sb.z) : 0.f;
-                    const float d20 = v0 ? -lam * a20 * (p0 - sa.w) : 0.f;
-                    const float d21 = v1 ? -lam * a21 * (p1 - sb.w) : 0.f;
-                    w1[c / 2] = pack_bf16x2(d10, d11);
-                    w2[c / 2] = pack_bf16x2(d20, d21);
-                    w3[c / 2] = pack_bf16x2(a10 - lam * a20, a11 - lam * a21);
+                    for (int c = 0; c < 32; c += 2) {
+                        const float4 sa = stv[c], sb = stv[c + 1];
+                        const bool v0 = c >= first_vis && c < qlim;
+                        const bool v1 = c + 1 >= first_vis && c + 1 < qlim;
+                        const float a10 = v0 ? ex2_approx(fmaf(__uint_as_float(s1[c]), sl2, sa.x)) : 0.f;
+                        const float a11 = v1 ? ex2_approx(fmaf(__uint_as_float(s1[c + 1]), sl2, sb.x)) : 0.f;
+                        const float a20 = v0 ? ex2_approx(fmaf(__uint_as_float(s2[c]), sl2, sa.y)) : 0.f;
+                        const float a21 = v1 ? ex2_approx(fmaf(__uint_as_float(s2[c + 1]), sl2, sb.y)) : 0.f;
+                        const float p0 = __uint_as_float(dp[c]), p1 = __uint_as_float(dp[c + 1]);
+                        // statistics of queries at or past T are not loaded: select, never
+                        // multiply, so that whatever the buffer holds cannot reach the sums
+                        const float d10 = v0 ? a10 * (p0 + sa.z) : 0.f;
+                        const float d11 = v1 ? a11 * (p1 + sb.z) : 0.f;
+                        const float d20 = v0 ? -lam * a20 * (p0 + sa.w) : 0.f;
+                        const float d21 = v1 ? -lam * a21 * (p1 + sb.w) : 0.f;
+                        w1[c / 2] = pack_bf16x2(d10, d11);
+                        w2[c / 2] = pack_bf16x2(d20, d21);
+                        w3[c / 2] = pack_bf16x2(a10 - lam * a20, a11 - lam * a21);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const float4 sa = stv[c], sb = stv[c + 1];
+                        const uint64_t x1 = f2_fma(f2_from_bits(s1[c], s1[c + 1]), sl2x2, f2_pack(sa.x, sb.x));
+                        const uint64_t x2 = f2_fma(f2_from_bits(s2[c], s2[c + 1]), sl2x2, f2_pack(sa.y, sb.y));
+                        const uint64_t a1 = f2_pack(ex2_approx(f2_lo(x1)), ex2_approx(f2_hi(x1)));
+                        const uint64_t a2n = f2_mul(f2_pack(ex2_approx(f2_lo(x2)), ex2_approx(f2_hi(x2))), nlam2);
+                        const uint64_t dp2 = f2_from_bits(dp[c], dp[c + 1]);
+                        const uint64_t d1 = f2_mul(a1, f2_add(dp2, f2_pack(sa.z, sb.z)));
+                        const uint64_t d2 = f2_mul(a2n, f2_add(dp2, f2_pack(sa.w, sb.w)));
+                        const uint64_t w = f2_add(a1, a2n);
+                        w1[c / 2] = pack_bf16x2(f2_lo(d1), f2_hi(d1));
+                        w2[c / 2] = pack_bf16x2(f2_lo(d2), f2_hi(d2));
+                        w3[c / 2] = pack_bf16x2(f2_lo(w), f2_hi(w));
+                    }
                 }
                 // the previous tile's dV/dK products must have read the operands
                 if (qc > 0 && !(ok = mbar_wait_warp(&bars[BAR_PK_FREE], (qc - 1) & 1u, ab))) break;

@@ -567,9 +567,10 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[BAR_O_EMPTY]);
                 if (live) {
+                    // stored negated: the consumers add them
                     float* st = p.stats + (((int64_t)it.b * p.H + it.h) * p.T + q) * 4;
-                    st[br] = m_run + log2f(l);
-                    st[2 + br] = dd / l;
+                    st[br] = -(m_run + log2f(l));
+                    st[2 + br] = -(dd / l);
                 }
                 continue;
             }

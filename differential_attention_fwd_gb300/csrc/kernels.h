@@ -36,9 +36,10 @@ struct TcParams {
     int kv_group;               // query heads per key/value head (>= 1)
     int k_shared;               // K1 and K2 are one tensor: load each key tile once
     // Row-statistics mode (the first pass of the backward): when stats is set,
-    // the epilogue writes, per query row, the log2-sum-exp of each branch's
-    // scaled scores and Dd_b = dO . (A_b V) to stats[(b*H + h)*T + t][0..3]
-    // (lse_1, lse_2, Dd_1, Dd_2) instead of writing O.
+    // the epilogue writes, per query row, the negated log2-sum-exp of each
+    // branch's scaled scores and the negated Dd_b = dO . (A_b V) to
+    // stats[(b*H + h)*T + t][0..3] (-lse_1, -lse_2, -Dd_1, -Dd_2) instead of
+    // writing O.
     float* stats;
     const __nv_bfloat16* dout;
     int64_t do_sB, do_sH, do_sT;
@@ -133,9 +134,11 @@ int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v,out*/, const TcParams&
                   cudaStream_t stream);
 int launch_bwd_tc(const CUtensorMap* maps /*dq: q1,k1,q2,k2,v,do; dkdv: the same*/,
                   const BwdTcParams& p, int num_sms, cudaStream_t stream);
-// dlambda = -sum of the rows' Dd_2; the 128 floats after the rows' statistics
+// dlambda = sign * (sum over rows of stats[row][3]) (sign -1 when the rows hold
+// Dd_2, +1 when they hold -Dd_2); the 128 floats after the rows' statistics
 // hold the per-block partial sums.
-int launch_bwd_dlambda(const float* stats, int64_t rows, float* out, cudaStream_t stream);
+int launch_bwd_dlambda(const float* stats, int64_t rows, float sign, float* out,
+                       cudaStream_t stream);
 int launch_bwd_simt_f32(const BwdParams& p, cudaStream_t stream);
 int launch_bwd_simt_bf16(const BwdParams& p, cudaStream_t stream);
 int launch_fwd_simt_f32(const SimtParams& p, cudaStream_t stream);

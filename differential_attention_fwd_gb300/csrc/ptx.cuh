@@ -353,6 +353,15 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// Two 32-bit registers as one packed pair (lo = a).
+__device__ __forceinline__ uint64_t f2_from_bits(uint32_t a, uint32_t b) {
+    return static_cast<uint64_t>(a) | (static_cast<uint64_t>(b) << 32);
+}
 
 // Two floats -> packed bf16x2 (lo in the low half), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
