@@ -284,7 +284,7 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
             encode_map(&maps[4], v, 128, &d, hk, d.v_stride, 64, 64) != DIFFATTN_OK ||
             encode_map(&maps[5], out, 128, &d, d.H, d.o_stride, 64, 32) != DIFFATTN_OK)
             return DIFFATTN_ERR_CUDA;
-        TcParams p;
+        TcParams p{};
         p.B = (int)d.B;
         p.H = (int)d.H;
         p.T = (int)d.T;
@@ -329,7 +329,7 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
         return launch_fwd_tc(maps, p, grid, st) == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
     }
 
-    SimtParams p;
+    SimtParams p{};
     p.B = (int)d.B;
     p.H = (int)d.H;
     p.T = (int)d.T;
@@ -396,7 +396,7 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
             encode_map(&fmaps[4], v, 128, &d, hk, d.v_stride, 64, 64) != DIFFATTN_OK ||
             encode_map(&fmaps[5], dout, 128, &d, d.H, d.o_stride, 64, 32) != DIFFATTN_OK)
             return DIFFATTN_ERR_CUDA;
-        TcParams f;
+        TcParams f{};
         f.B = (int)d.B;
         f.H = (int)d.H;
         f.T = (int)d.T;
@@ -440,7 +440,7 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
             encode_map(&maps[10], v, 128, &d, hk, d.v_stride, 64, 128) != DIFFATTN_OK ||
             encode_map(&maps[11], dout, 128, &d, d.H, d.o_stride, 64, 64) != DIFFATTN_OK)
             return DIFFATTN_ERR_CUDA;
-        BwdTcParams b;
+        BwdTcParams b{};
         b.B = (int)d.B;
         b.H = (int)d.H;
         b.Hk = (int)hk;
@@ -467,7 +467,7 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
                    ? DIFFATTN_OK
                    : DIFFATTN_ERR_CUDA;
     }
-    BwdParams p;
+    BwdParams p{};
     p.B = (int)d.B;
     p.H = (int)d.H;
     p.kv_group = (int)group_of(d.kv_group);
@@ -533,7 +533,7 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
     if (!kv_aligned(k1, d.k1_stride, esize) || !kv_aligned(k2, d.k2_stride, esize) ||
         !kv_aligned(v, d.v_stride, esize))
         return DIFFATTN_ERR_UNSUPPORTED;
-    DecodeParams p;
+    DecodeParams p{};
     p.B = (int)d.B;
     p.H = (int)d.H;
     p.Tq = (int)d.Tq;
