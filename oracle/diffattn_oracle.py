@@ -379,3 +379,22 @@ def differential_lambda_backward(lq1, lk1, lq2, lk2, dlam: float):
     e2 = math.exp(float(np.dot(vecs[2], vecs[3])))
     d = float(dlam)
     return d * e1 * vecs[1], d * e1 * vecs[0], -d * e2 * vecs[3], -d * e2 * vecs[2]
+
+
+def branch_logsumexp(q, k, causal: bool = True) -> np.ndarray:
+    """log sum_j exp(S_ij) per query row of one branch, S = Q K^T / sqrt(D) + M
+    (natural log, float64): the normaliser of the row softmax of the
+    Formula-and-conventions maps, which the backward reuses.
+
+    q: [B, H, T, D]; k: [B, H_kv, T, D].  Returns [B, H, T]."""
+    q, k = _as64(q), _as64(k)
+    B, H, T, D = q.shape
+    g = H // k.shape[1]
+    out = np.empty((B, H, T))
+    rows = np.arange(T)
+    for b in range(B):
+        for h in range(H):
+            s = _mask(_scores(q[b, h], k[b, h // g]), rows, causal)
+            m = np.max(s, axis=-1)
+            out[b, h] = m + np.log(np.sum(np.exp(s - m[:, None]), axis=-1))
+    return out

@@ -207,3 +207,23 @@ def test_planted_backward_mistake_is_caught(monkeypatch, name):
             caught = True
             break
     assert caught, name
+
+
+def test_branch_logsumexp_matches_scipy_and_closed_forms():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(15)
+    q = rng.standard_normal((1, 4, 9, 5))
+    k = rng.standard_normal((1, 2, 9, 5))
+    for causal in (True, False):
+        got = oracle.branch_logsumexp(q, k, causal)
+        for h in range(4):
+            s = q[0, h] @ k[0, h // 2].T / math.sqrt(5)
+            if causal:
+                s = np.where(np.tril(np.ones((9, 9), dtype=bool)), s, -np.inf)
+            assert np.max(np.abs(got[0, h] - logsumexp(s, axis=-1))) <= 1e-12
+    # first causal row sees one key: lse = q0 . k0 / sqrt(D)
+    got = oracle.branch_logsumexp(q, k, True)
+    assert abs(got[0, 0, 0] - float(q[0, 0, 0] @ k[0, 0, 0]) / math.sqrt(5)) <= 1e-12
+    # equal scores over n visible keys: lse = s + log n
+    qz = np.zeros((1, 1, 6, 3))
+    assert np.allclose(oracle.branch_logsumexp(qz, qz, True)[0, 0], np.log(np.arange(1, 7)), atol=1e-14)
