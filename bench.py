@@ -546,12 +546,21 @@ def run_backward(args, w, world, rank, local):
     ws = torch.empty(need // 4 + 4, dtype=torch.float32, device=dev)
     ptrs = [ctypes.c_void_p(t.data_ptr()) for t in d_in]
     gptrs = [ctypes.c_void_p(t.data_ptr()) for t in grads]
+    # the forward of the training step (outside the timed region) keeps O, A_2 V
+    # and the log-sum-exp; the backward starts from them unless asked to recompute
+    saved = None
+    if not args.bwd_recompute:
+        saved = da.differential_attention_train(*d_in[:5], lam, causal=w.causal)
+        sptrs = [ctypes.c_void_p(t.data_ptr()) for t in saved]
 
     def step():
-        rc = lib.diffattn_bwd(ctypes.byref(desc), *ptrs[:5], ctypes.c_float(lam), None,
-                              1 if w.causal else 0, ptrs[5], *gptrs, ctypes.c_void_p(d_lam.data_ptr()),
-                              ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(need),
-                              ctypes.c_void_p(stream.cuda_stream))
+        head = (ctypes.byref(desc), *ptrs[:5], ctypes.c_float(lam), None, 1 if w.causal else 0)
+        tail = (ptrs[5], *gptrs, ctypes.c_void_p(d_lam.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                ctypes.c_size_t(need), ctypes.c_void_p(stream.cuda_stream))
+        if saved is not None:
+            rc = lib.diffattn_bwd_saved(*head, *sptrs, *tail)
+        else:
+            rc = lib.diffattn_bwd(*head, *tail)
         if rc:
             raise _lib.DiffattnError(rc, "diffattn_bwd")
 
@@ -632,8 +641,12 @@ def run_backward(args, w, world, rank, local):
         "data": "synthetic",
         "config": {**config_of(w, lam), "gflop_per_step": flops / 1e9,
                    "executed_gflop_per_step": flops * 2 / 1e9,
-                   "pass": "backward: forward kernel in row-statistics mode, dQ kernel, "
-                           "dK/dV kernel, dlambda reduction in two launches (5 launches per step)"},
+                   "pass": ("backward from the saved forward results: statistics pass over dO, O "
+                            "and A_2 V, dQ kernel, dK/dV kernel, dlambda reduction in two launches "
+                            "(5 launches per step)") if saved is not None else
+                           ("backward with the forward recomputed: forward kernel in "
+                            "row-statistics mode, dQ kernel, dK/dV kernel, dlambda reduction in "
+                            "two launches (5 launches per step)")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
                      "peak_source": f"{src} bf16_tflops (burst)",
@@ -731,6 +744,9 @@ def main(argv=None):
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
     ap.add_argument("--mode", choices=["forward", "backward", "decode"], default="forward")
     ap.add_argument("--decode-workload", default="decode_b16h16q1k8192", choices=sorted(W.DECODE_WORKLOADS))
+    ap.add_argument("--bwd-recompute", action="store_true",
+                    help="backward mode: recompute the forward instead of starting from the "
+                         "training forward's saved results")
     ap.add_argument("--norm", choices=["none", "rms", "group"], default="none",
                     help="fuse a per-head norm and the (1 - lambda_init) multiplier")
     args = ap.parse_args(argv)

@@ -26,7 +26,8 @@ from ._lib import (DIFFATTN_BF16, DIFFATTN_F32, DIFFATTN_KERNEL_SIMT,  # noqa: F
                    DIFFATTN_NORM_RMS, DiffattnDesc, DiffattnEpilogue, DiffattnError,
                    DiffattnKvDesc)
 
-__all__ = ["differential_lambda", "differential_attention", "differential_attention_backward",
+__all__ = ["differential_lambda", "differential_attention", "differential_attention_train",
+           "differential_attention_backward",
            "differential_attention_decode",
            "make_desc", "make_kv_desc", "select_kernel", "get_device_error", "version",
            "DiffattnError"]
@@ -206,7 +207,7 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
 
 
 def _forward(q1, k1, q2, k2, value, coefficient, causal, out, dynamic_schedule, norm, norm_eps,
-             norm_weight, norm_bias, out_scale):
+             norm_weight, norm_bias, out_scale, train=False):
     (q1, k1, q2, k2, value), dev = _prepare(q1, k1, q2, k2, value)
     B, H, T, D = q1.shape
     if out is None:
@@ -221,32 +222,53 @@ def _forward(q1, k1, q2, k2, value, coefficient, causal, out, dynamic_schedule, 
     d = make_desc(q1, k1, q2, k2, value, out)
     epi = _epilogue(norm, norm_eps, norm_weight, norm_bias, out_scale, H, 2 * D, dev)
     lib = _lib.load()
+    lam_ptr = ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0)
+    ins = [ctypes.c_void_p(t.data_ptr()) for t in (q1, k1, q2, k2, value)]
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev)
         ws = workspace_for(dev, stream) if dynamic_schedule else None
-        rc = lib.diffattn_fwd_ex(ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in
-                                                     (q1, k1, q2, k2, value)),
-                                 ctypes.c_float(lam_host),
-                                 ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0),
+        ws_args = (ctypes.c_void_p(ws.data_ptr() if ws is not None else 0),
+                   ctypes.c_size_t(ws.numel() * 4 if ws is not None else 0),
+                   ctypes.c_void_p(stream.cuda_stream))
+        if train:
+            out2 = torch.empty_like(out)
+            lse = torch.empty((B, H, T, 2), dtype=torch.float32, device=dev)
+            rc = lib.diffattn_fwd_train(ctypes.byref(d), *ins, ctypes.c_float(lam_host), lam_ptr,
+                                        1 if causal else 0, ctypes.c_void_p(out.data_ptr()),
+                                        ctypes.c_void_p(out2.data_ptr()),
+                                        ctypes.c_void_p(lse.data_ptr()), *ws_args)
+            _lib.check(rc, "diffattn_fwd_train")
+            return out, out2, lse
+        rc = lib.diffattn_fwd_ex(ctypes.byref(d), *ins, ctypes.c_float(lam_host), lam_ptr,
                                  1 if causal else 0, ctypes.byref(epi[0]) if epi else None,
-                                 ctypes.c_void_p(out.data_ptr()),
-                                 ctypes.c_void_p(ws.data_ptr() if ws is not None else 0),
-                                 ctypes.c_size_t(ws.numel() * 4 if ws is not None else 0),
-                                 ctypes.c_void_p(stream.cuda_stream))
+                                 ctypes.c_void_p(out.data_ptr()), *ws_args)
     _lib.check(rc, "diffattn_fwd")
     return out
 
 
+def differential_attention_train(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
+                                 k2: torch.Tensor, value: torch.Tensor, coefficient,
+                                 causal: bool = True, dynamic_schedule: bool = True):
+    """The forward of a training step: returns (out, out2, lse) where out is
+    differential_attention's output, out2 = A_2 V (same shape and dtype) and
+    lse the natural-log log-sum-exp of each branch's scaled scores, float32
+    [B, H, T, 2].  Pass them to differential_attention_backward(saved=...)."""
+    return _forward(q1, k1, q2, k2, value, coefficient, causal, None, dynamic_schedule, None,
+                    1e-5, None, None, 1.0, train=True)
+
+
 def differential_attention_backward(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
                                     k2: torch.Tensor, value: torch.Tensor, coefficient,
-                                    dout: torch.Tensor, causal: bool = True):
+                                    dout: torch.Tensor, causal: bool = True, saved=None):
     """Gradients of differential_attention given dout = dL/dO.
 
     Inputs as differential_attention (the forward's inputs and coefficient);
-    dout: [B, H, T, 2D] of the inputs' dtype.  Returns (dq1, dk1, dq2, dk2,
-    dvalue, dcoefficient): contiguous tensors of the inputs' shapes and dtype,
-    and a float32 scalar tensor on the device.  The gradients of the four
-    lambda vectors follow from dcoefficient (see differential_lambda)."""
+    dout: [B, H, T, 2D] of the inputs' dtype.  saved: optional (out, out2,
+    lse) from differential_attention_train with the same inputs; with it the
+    forward is not recomputed.  Returns (dq1, dk1, dq2, dk2, dvalue,
+    dcoefficient): contiguous tensors of the inputs' shapes and dtype, and a
+    float32 scalar tensor on the device.  The gradients of the four lambda
+    vectors follow from dcoefficient (see differential_lambda)."""
     (q1, k1, q2, k2, value), dev = _prepare(q1, k1, q2, k2, value)
     B, H, T, D = q1.shape
     _require_cuda(dout, "dout")
@@ -254,6 +276,19 @@ def differential_attention_backward(q1: torch.Tensor, k1: torch.Tensor, q2: torc
         raise ValueError("dout must be [B, H, T, 2D] with the inputs' dtype and device")
     if dout.stride(-1) != 1:
         dout = dout.contiguous()
+    if saved is not None:
+        out, out2, lse = saved
+        # out, out2 and dout share one layout in the ABI
+        if dout.stride() != out.stride():
+            dout = dout.contiguous()
+            out, out2 = out.contiguous(), out2.contiguous()
+        if out2.stride() != out.stride():
+            out2 = out2.contiguous()
+        if tuple(lse.shape) != (B, H, T, 2) or lse.dtype != torch.float32 or not lse.is_contiguous():
+            raise ValueError("lse must be a contiguous float32 [B, H, T, 2] tensor")
+        if out.dtype != q1.dtype or out2.dtype != q1.dtype or out.shape != dout.shape or \
+                out2.shape != dout.shape:
+            raise ValueError("out and out2 must match dout's shape and dtype")
     lam_host, lam_dev = _coefficient(coefficient, dev)
     d = make_desc(q1, k1, q2, k2, value, dout)
     grads = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (q1, k1, q2, k2, value)]
@@ -263,14 +298,19 @@ def differential_attention_backward(q1: torch.Tensor, k1: torch.Tensor, q2: torc
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev)
         ws = torch.empty(need // 4 + 4, dtype=torch.float32, device=dev)
-        rc = lib.diffattn_bwd(ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in
-                                                  (q1, k1, q2, k2, value)),
-                              ctypes.c_float(lam_host),
-                              ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0),
-                              1 if causal else 0, ctypes.c_void_p(dout.data_ptr()),
-                              *(ctypes.c_void_p(g.data_ptr()) for g in grads),
-                              ctypes.c_void_p(dlam.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
-                              ctypes.c_size_t(ws.numel() * 4), ctypes.c_void_p(stream.cuda_stream))
+        head = [ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in (q1, k1, q2, k2, value)),
+                ctypes.c_float(lam_host),
+                ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0),
+                1 if causal else 0]
+        tail = [ctypes.c_void_p(dout.data_ptr()), *(ctypes.c_void_p(g.data_ptr()) for g in grads),
+                ctypes.c_void_p(dlam.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                ctypes.c_size_t(ws.numel() * 4), ctypes.c_void_p(stream.cuda_stream)]
+        if saved is not None:
+            rc = lib.diffattn_bwd_saved(*head, ctypes.c_void_p(out.data_ptr()),
+                                        ctypes.c_void_p(out2.data_ptr()),
+                                        ctypes.c_void_p(lse.data_ptr()), *tail)
+        else:
+            rc = lib.diffattn_bwd(*head, *tail)
     _lib.check(rc, "diffattn_bwd")
     return (*grads, dlam)
 
@@ -280,20 +320,21 @@ class _DifferentialAttentionFn(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q1, k1, q2, k2, value, coefficient, causal, dynamic_schedule):
-        out = _forward(q1, k1, q2, k2, value, coefficient, causal, None, dynamic_schedule, None,
-                       1e-5, None, None, 1.0)
+        out, out2, lse = _forward(q1, k1, q2, k2, value, coefficient, causal, None,
+                                  dynamic_schedule, None, 1e-5, None, None, 1.0, train=True)
         coef_t = coefficient if isinstance(coefficient, torch.Tensor) else None
-        ctx.save_for_backward(q1, k1, q2, k2, value, coef_t)
+        ctx.save_for_backward(q1, k1, q2, k2, value, coef_t, out, out2, lse)
         ctx.coefficient = None if coef_t is not None else coefficient
         ctx.causal = causal
         return out
 
     @staticmethod
     def backward(ctx, dout):
-        q1, k1, q2, k2, value, coef_t = ctx.saved_tensors
+        q1, k1, q2, k2, value, coef_t, out, out2, lse = ctx.saved_tensors
         coefficient = coef_t if coef_t is not None else ctx.coefficient
         dq1, dk1, dq2, dk2, dv, dlam = differential_attention_backward(
-            q1, k1, q2, k2, value, coefficient, dout.to(q1.dtype), ctx.causal)
+            q1, k1, q2, k2, value, coefficient, dout.to(q1.dtype), ctx.causal,
+            saved=(out, out2, lse))
         dcoef = None
         if coef_t is not None and ctx.needs_input_grad[5]:
             dcoef = dlam.to(device=coef_t.device, dtype=coef_t.dtype).reshape(coef_t.shape)

@@ -29,7 +29,9 @@ EXPORTED = (
     "diffattn_lambda_backward",
     "diffattn_fwd",
     "diffattn_fwd_ex",
+    "diffattn_fwd_train",
     "diffattn_bwd",
+    "diffattn_bwd_saved",
     "diffattn_bwd_workspace_bytes",
     "diffattn_decode",
     "diffattn_decode_workspace_bytes",
@@ -113,6 +115,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_bwd.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, ctypes.c_float,
                                  vp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.diffattn_bwd.restype = ctypes.c_int
+    lib.diffattn_fwd_train.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp,
+                                       ctypes.c_float, vp, ctypes.c_int, vp, vp, vp, vp,
+                                       ctypes.c_size_t, vp]
+    lib.diffattn_fwd_train.restype = ctypes.c_int
+    lib.diffattn_bwd_saved.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp,
+                                       ctypes.c_float, vp, ctypes.c_int, vp, vp, vp, vp, vp, vp,
+                                       vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.diffattn_bwd_saved.restype = ctypes.c_int
     lib.diffattn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(DiffattnDesc)]
     lib.diffattn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.diffattn_decode_workspace_bytes.argtypes = [ctypes.POINTER(DiffattnKvDesc)]

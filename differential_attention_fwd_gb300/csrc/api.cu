@@ -200,6 +200,17 @@ bool kv_aligned(const void* p, const int64_t s[3], size_t esize) {
            (s[2] * (int64_t)esize) % 16 == 0;
 }
 
+int forward_impl(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
+                 const void* k2, const void* v, float lambda, const float* lambda_dev, int causal,
+                 const diffattn_epilogue* epi, void* out, void* out2, float* lse,
+                 void* workspace, size_t workspace_bytes, diffattn_stream_t stream);
+int backward_impl(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
+                  const void* k2, const void* v, float lambda, const float* lambda_dev,
+                  int causal, const void* out, const void* out2, const float* lse,
+                  const void* dout, void* dq1, void* dk1, void* dq2, void* dk2, void* dv,
+                  float* dlambda, void* workspace, size_t workspace_bytes,
+                  diffattn_stream_t stream);
+
 }  // namespace
 }  // namespace diffattn
 
@@ -249,6 +260,30 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
                     const void* k2, const void* v, float lambda, const float* lambda_dev,
                     int causal, const diffattn_epilogue* epi, void* out, void* workspace,
                     size_t workspace_bytes, diffattn_stream_t stream) {
+    return forward_impl(desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal, epi, out, nullptr,
+                        nullptr, workspace, workspace_bytes, stream);
+}
+
+int diffattn_fwd_train(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
+                       const void* k2, const void* v, float lambda, const float* lambda_dev,
+                       int causal, void* out, void* out2, float* lse, void* workspace,
+                       size_t workspace_bytes, diffattn_stream_t stream) {
+    if (!out2 || !lse) return DIFFATTN_ERR_INVALID;
+    return forward_impl(desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal, nullptr, out, out2,
+                        lse, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace diffattn {
+namespace {
+
+// The forward, optionally with the training outputs (out2 = A_2 V with the
+// output's strides, lse = [B, H, T, 2] natural-log log-sum-exp per branch).
+int forward_impl(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
+                 const void* k2, const void* v, float lambda, const float* lambda_dev, int causal,
+                 const diffattn_epilogue* epi, void* out, void* out2, float* lse,
+                 void* workspace, size_t workspace_bytes, diffattn_stream_t stream) {
     int rc = validate(desc, q1, k1, q2, k2, v, out);
     if (rc != DIFFATTN_OK) return rc;
     diffattn_epilogue e{DIFFATTN_NORM_NONE, 0.f, nullptr, nullptr, 1.0f, 0};
@@ -269,7 +304,8 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
     rc = device_state(&dev);
     if (rc != DIFFATTN_OK) return rc;
 
-    if (select(desc, q1, k1, q2, k2, v, out) == DIFFATTN_KERNEL_TCGEN05) {
+    if (select(desc, q1, k1, q2, k2, v, out) == DIFFATTN_KERNEL_TCGEN05 &&
+        (!out2 || aligned16(out2))) {
         CUtensorMap maps[6];
         const int64_t g = group_of(d.kv_group);
         const int64_t hk = d.H / g;
@@ -325,6 +361,8 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
         p.out_scale = e.out_scale;
         p.kv_group = (int)g;
         p.k_shared = same_tensor(k1, d.k1_stride, k2, d.k2_stride, d.B, hk, d.T) ? 1 : 0;
+        p.out2 = static_cast<__nv_bfloat16*>(out2);
+        p.lse = lse;
         const int grid = p.total_items < dev->num_sms ? p.total_items : dev->num_sms;
         return launch_fwd_tc(maps, p, grid, st) == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
     }
@@ -356,9 +394,16 @@ int diffattn_fwd_ex(const diffattn_desc* desc, const void* q1, const void* k1, c
     p.norm_bias = e.bias;
     p.out_scale = e.out_scale;
     p.kv_group = (int)group_of(d.kv_group);
+    p.out2 = out2;
+    p.lse = lse;
     rc = (d.dtype == DIFFATTN_F32) ? launch_fwd_simt_f32(p, st) : launch_fwd_simt_bf16(p, st);
     return rc == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
+
+}  // namespace
+}  // namespace diffattn
+
+extern "C" {
 
 size_t diffattn_bwd_workspace_bytes(const diffattn_desc* desc) {
     if (!desc || desc->B < 1 || desc->H < 1 || desc->T < 1) return 0;
@@ -371,6 +416,38 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
                  const void* dout, void* dq1, void* dk1, void* dq2, void* dk2, void* dv,
                  float* dlambda, void* workspace, size_t workspace_bytes,
                  diffattn_stream_t stream) {
+    return backward_impl(desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal, nullptr, nullptr,
+                         nullptr, dout, dq1, dk1, dq2, dk2, dv, dlambda, workspace,
+                         workspace_bytes, stream);
+}
+
+int diffattn_bwd_saved(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
+                       const void* k2, const void* v, float lambda, const float* lambda_dev,
+                       int causal, const void* out, const void* out2, const float* lse,
+                       const void* dout, void* dq1, void* dk1, void* dq2, void* dk2, void* dv,
+                       float* dlambda, void* workspace, size_t workspace_bytes,
+                       diffattn_stream_t stream) {
+    if (!out || !out2 || !lse) return DIFFATTN_ERR_INVALID;
+    return backward_impl(desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal, out, out2, lse,
+                         dout, dq1, dk1, dq2, dk2, dv, dlambda, workspace, workspace_bytes,
+                         stream);
+}
+
+}  // extern "C"
+
+namespace diffattn {
+namespace {
+
+// The backward.  With the forward's saved results (out, out2 = A_2 V and the
+// log-sum-exp, all non-NULL) the row statistics come from one elementwise
+// pass over them; without, from a recomputation of the forward.
+int backward_impl(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
+                  const void* k2, const void* v, float lambda, const float* lambda_dev,
+                  int causal, const void* out, const void* out2, const float* lse,
+                  const void* dout, void* dq1, void* dk1, void* dq2, void* dk2, void* dv,
+                  float* dlambda, void* workspace, size_t workspace_bytes,
+                  diffattn_stream_t stream) {
+    const bool saved = out != nullptr;
     int rc = validate(desc, q1, k1, q2, k2, v, dout);
     if (rc != DIFFATTN_OK) return rc;
     if (!dq1 || !dk1 || !dq2 || !dk2 || !dv || !dlambda) return DIFFATTN_ERR_INVALID;
@@ -387,6 +464,26 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
         if (rc != DIFFATTN_OK) return rc;
         const int64_t g = group_of(d.kv_group);
         const int64_t hk = d.H / g;
+        float* stats = static_cast<float*>(workspace);
+        if (saved) {
+            // Pass 1: the row statistics from the forward's saved results.
+            PrepParams pp{};
+            pp.B = (int)d.B;
+            pp.H = (int)d.H;
+            pp.T = (int)d.T;
+            pp.Dv = (int)(2 * d.D);
+            pp.bf16 = 1;
+            pp.log2_negated = 1;
+            pp.lambda = lambda;
+            pp.lambda_dev = lambda_dev;
+            pp.out = out;
+            pp.out2 = out2;
+            pp.dout = dout;
+            copy3(pp.s_o, d.o_stride);
+            pp.lse = lse;
+            pp.stats = stats;
+            if (launch_bwd_prep(pp, st) != 0) return DIFFATTN_ERR_CUDA;
+        } else {
         // Pass 1: the forward kernel in row-statistics mode.
         CUtensorMap fmaps[6];
         if (encode_map(&fmaps[0], q1, 64, &d, d.H, d.q1_stride, 64, 128) != DIFFATTN_OK ||
@@ -425,6 +522,7 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
         f.do_sT = d.o_stride[2];
         const int fgrid = f.total_items < dev->num_sms ? f.total_items : dev->num_sms;
         if (launch_fwd_tc(fmaps, f, fgrid, st) != 0) return DIFFATTN_ERR_CUDA;
+        }
         // Pass 2: dQ, then dK and dV, on the tensor cores.
         CUtensorMap maps[12];
         if (encode_map(&maps[0], q1, 64, &d, d.H, d.q1_stride, 64, 128) != DIFFATTN_OK ||
@@ -451,11 +549,11 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
         b.nk128 = (int)((d.T + 127) / 128);
         b.causal = causal ? 1 : 0;
         b.scale = (float)(1.0 / std::sqrt((double)d.D));
-        b.scale_log2 = f.scale_log2;
+        b.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.D));
         b.lambda = lambda;
         b.lambda_dev = lambda_dev;
         b.status = dev->status;
-        b.stats = f.stats;
+        b.stats = stats;
         b.dq1 = dq1;
         b.dq2 = dq2;
         b.dk1 = dk1;
@@ -463,7 +561,7 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
         b.dv = dv;
         if (launch_bwd_tc(maps, b, dev->num_sms, st) != 0) return DIFFATTN_ERR_CUDA;
         // the statistics hold -Dd_2, so dlambda = -sum(Dd_2) is their plain sum
-        return launch_bwd_dlambda(f.stats, d.B * d.H * d.T, 1.0f, dlambda, st) == 0
+        return launch_bwd_dlambda(stats, d.B * d.H * d.T, 1.0f, dlambda, st) == 0
                    ? DIFFATTN_OK
                    : DIFFATTN_ERR_CUDA;
     }
@@ -497,9 +595,37 @@ int diffattn_bwd(const diffattn_desc* desc, const void* q1, const void* k1, cons
     copy3(p.s_do, d.o_stride);
     p.stats = static_cast<float*>(workspace);
     p.dlambda = dlambda;
-    rc = (d.dtype == DIFFATTN_F32) ? launch_bwd_simt_f32(p, st) : launch_bwd_simt_bf16(p, st);
+    if (saved) {
+        PrepParams pp{};
+        pp.B = (int)d.B;
+        pp.H = (int)d.H;
+        pp.T = (int)d.T;
+        pp.Dv = (int)(2 * d.D);
+        pp.bf16 = d.dtype == DIFFATTN_BF16 ? 1 : 0;
+        pp.log2_negated = 0;
+        pp.lambda = lambda;
+        pp.lambda_dev = lambda_dev;
+        pp.out = out;
+        pp.out2 = out2;
+        pp.dout = dout;
+        copy3(pp.s_o, d.o_stride);
+        pp.lse = lse;
+        pp.stats = p.stats;
+        if (launch_bwd_prep(pp, st) != 0) return DIFFATTN_ERR_CUDA;
+        rc = (d.dtype == DIFFATTN_F32) ? launch_bwd_simt_grads_f32(p, st)
+                                       : launch_bwd_simt_grads_bf16(p, st);
+    } else {
+        rc = (d.dtype == DIFFATTN_F32) ? launch_bwd_simt_f32(p, st) : launch_bwd_simt_bf16(p, st);
+    }
     return rc == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
+
+}  // namespace
+}  // namespace diffattn
+
+extern "C" {
+
+
 
 size_t diffattn_decode_workspace_bytes(const diffattn_kv_desc* desc) {
     DecodePlan plan;

@@ -11,9 +11,11 @@
 // (rowsum(dA_b * A_b) for the softmax backward is Dd_1 for branch 1 and
 // -lambda Dd_2 for branch 2, since dA_1 = dW and dA_2 = -lambda dW.)
 //
-// Four kernels:
+// Kernels:
 //   stats   one warp per query row: a forward pass per branch that keeps the
 //           row's log-sum-exp and Dd_b (the branch output dotted with dO);
+//   prep    instead of stats, when the forward saved O, A_2 V and the
+//           log-sum-exp: Dd_b from those, one warp per row;
 //   dq      one warp per query row: recomputes A_b from the log-sum-exp, forms
 //           dS_b one key per lane and accumulates dQ_b;
 //   dkdv    one warp per key row of a key/value head: walks the visible query
@@ -347,6 +349,64 @@ int launch_dlambda(const float* stats, int64_t rows, float* partials, float sign
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
+// ------------------------------------------------------------------ prep
+// Row statistics from the forward's saved results (one warp per row):
+// Dd_2 = dO . O2, Dd_1 = dO . (O + lambda O2), since O = O1 - lambda O2.
+template <typename T>
+__global__ void __launch_bounds__(WARPS * 32) bwd_prep_kernel(const PrepParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    const int64_t rows = (int64_t)p.B * p.H * p.T;
+    if (row >= rows) return;
+    const int64_t bh = row / p.T;
+    const int t = (int)(row - bh * p.T);
+    const int b = (int)(bh / p.H);
+    const int h = (int)(bh - (int64_t)b * p.H);
+    const int64_t off = b * p.s_o[0] + h * p.s_o[1] + (int64_t)t * p.s_o[2];
+    const T* o = static_cast<const T*>(p.out) + off;
+    const T* o2 = static_cast<const T*>(p.out2) + off;
+    const T* g = static_cast<const T*>(p.dout) + off;
+    float d0 = 0.f, d2 = 0.f;
+    for (int c = lane; c < p.Dv; c += 32) {
+        const float gc = ld(g, c);
+        d0 = fmaf(gc, ld(o, c), d0);
+        d2 = fmaf(gc, ld(o2, c), d2);
+    }
+    d0 = warp_sum(d0);
+    d2 = warp_sum(d2);
+    if (lane == 0) {
+        const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
+        const float dd1 = fmaf(lam, d2, d0);
+        const float lse1 = p.lse[row * 2], lse2 = p.lse[row * 2 + 1];
+        float* st = p.stats + row * 4;
+        if (p.log2_negated) {
+            st[0] = -lse1 * 1.4426950408889634f;
+            st[1] = -lse2 * 1.4426950408889634f;
+            st[2] = -dd1;
+            st[3] = -d2;
+        } else {
+            st[0] = lse1;
+            st[1] = lse2;
+            st[2] = dd1;
+            st[3] = d2;
+        }
+    }
+}
+
+template <typename T>
+int launch_grads(const BwdParams& p, cudaStream_t stream) {
+    const int64_t rows_per_head = (p.T + WARPS - 1) / WARPS;
+    const int64_t qblocks = rows_per_head * p.B * p.H;
+    const int64_t kblocks = rows_per_head * p.B * p.Hk;
+    if (qblocks > 0x7fffffffLL) return -1;
+    bwd_dq_kernel<T><<<(unsigned)qblocks, WARPS * 32, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    bwd_dkdv_kernel<T><<<(unsigned)kblocks, WARPS * 32, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    const int64_t rows = (int64_t)p.B * p.H * p.T;
+    return launch_dlambda(p.stats, rows, p.stats + rows * 4, -1.0f, p.dlambda, stream);
+}
+
 template <typename T>
 int launch(const BwdParams& p, cudaStream_t stream) {
     const int64_t rows_per_head = (p.T + WARPS - 1) / WARPS;
@@ -371,6 +431,22 @@ int launch_bwd_dlambda(const float* stats, int64_t rows, float sign, float* out,
                                stream);
 }
 
+int launch_bwd_prep(const PrepParams& p, cudaStream_t stream) {
+    const int64_t rows = (int64_t)p.B * p.H * p.T;
+    const int64_t blocks = (rows + bwd::WARPS - 1) / bwd::WARPS;
+    if (blocks > 0x7fffffffLL) return -1;
+    if (p.bf16)
+        bwd::bwd_prep_kernel<__nv_bfloat16><<<(unsigned)blocks, bwd::WARPS * 32, 0, stream>>>(p);
+    else
+        bwd::bwd_prep_kernel<float><<<(unsigned)blocks, bwd::WARPS * 32, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+int launch_bwd_simt_grads_f32(const BwdParams& p, cudaStream_t stream) {
+    return bwd::launch_grads<float>(p, stream);
+}
+int launch_bwd_simt_grads_bf16(const BwdParams& p, cudaStream_t stream) {
+    return bwd::launch_grads<__nv_bfloat16>(p, stream);
+}
 int launch_bwd_simt_f32(const BwdParams& p, cudaStream_t stream) { return bwd::launch<float>(p, stream); }
 int launch_bwd_simt_bf16(const BwdParams& p, cudaStream_t stream) {
     return bwd::launch<__nv_bfloat16>(p, stream);

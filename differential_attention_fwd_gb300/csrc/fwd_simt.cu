@@ -129,6 +129,20 @@ diffattn_fwd_simt_kernel(const SimtParams p) {
     const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
     const float inv1 = 1.0f / l1;
     const float inv2 = 1.0f / l2;
+    if (p.out2) {
+        // training outputs: A_2 V and the natural-log log-sum-exp of each branch
+        T* o2row = static_cast<T*>(p.out2) + b * p.s_o[0] + h * p.s_o[1] + (int64_t)i * p.s_o[2];
+#pragma unroll
+        for (int k = 0; k < OPL; ++k) {
+            const int c = lane + 32 * k;
+            if (c < Dv) store(o2row, c, __fmul_rn(o2[k], inv2));
+        }
+        if (lane == 0) {
+            float* lse = p.lse + (((int64_t)b * p.H + h) * p.T + i) * 2;
+            lse[0] = m1 + logf(l1);
+            lse[1] = m2 + logf(l2);
+        }
+    }
     float r[OPL];
 #pragma unroll
     for (int k = 0; k < OPL; ++k) {

@@ -593,6 +593,22 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             lph ^= 1;
             const float inv1 = inv_l[row];
             const float inv2 = inv_l[BM + row];
+            if (p.out2 && q < p.T) {
+                // training outputs: A_2 V for this thread's 64 columns, and this
+                // branch's log-sum-exp (natural log) of the scaled scores
+                __nv_bfloat16* o2row = p.out2 + it.b * p.o_sB + it.h * p.o_sH + (int64_t)q * p.o_sT + c0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = 8 * i;
+                    *reinterpret_cast<uint4*>(o2row + c) = make_uint4(
+                        pack_bf16x2(__uint_as_float(o2[c]) * inv2, __uint_as_float(o2[c + 1]) * inv2),
+                        pack_bf16x2(__uint_as_float(o2[c + 2]) * inv2, __uint_as_float(o2[c + 3]) * inv2),
+                        pack_bf16x2(__uint_as_float(o2[c + 4]) * inv2, __uint_as_float(o2[c + 5]) * inv2),
+                        pack_bf16x2(__uint_as_float(o2[c + 6]) * inv2, __uint_as_float(o2[c + 7]) * inv2));
+                }
+                p.lse[(((int64_t)it.b * p.H + it.h) * p.T + q) * 2 + br] =
+                    (m_run + log2f(l)) * 0.6931471805599453f;
+            }
             // O = O1 / l1 - lambda O2 / l2 for this thread's 64 columns
             float r[64];
 #pragma unroll

@@ -43,6 +43,11 @@ struct TcParams {
     float* stats;
     const __nv_bfloat16* dout;
     int64_t do_sB, do_sH, do_sT;
+    // Training outputs (when out2 is set): A_2 V with the output's strides, and
+    // the natural-log log-sum-exp of each branch's scaled scores, lse[(b*H + h)*T
+    // + t][branch].
+    __nv_bfloat16* out2;
+    float* lse;
 };
 
 // Parameters of the CUDA-core kernel (any D <= 128, fp32 or bf16).
@@ -61,6 +66,8 @@ struct SimtParams {
     const float* norm_bias;
     float out_scale;
     int kv_group;           // query head h reads key/value head h / kv_group
+    void* out2;             // training outputs (optional): A_2 V with the output's strides,
+    float* lse;             // and the natural-log log-sum-exp of each branch, [B, H, T, 2]
 };
 
 // Parameters of the decode kernels (Tq queries over Tk cached keys).
@@ -121,6 +128,23 @@ struct BwdTcParams {
     void* dq1; void* dq2; void* dk1; void* dk2; void* dv;
 };
 
+// Row statistics for the backward from the forward's saved results: O (the
+// output), O2 = A_2 V and the natural-log log-sum-exp of each branch.  Dd_2 =
+// dO . O2 and Dd_1 = dO . (O + lambda O2).  log2_negated selects the layout
+// the tensor-core kernels read (-lse_1 log2(e), -lse_2 log2(e), -Dd_1, -Dd_2)
+// instead of the CUDA-core one (lse_1, lse_2, Dd_1, Dd_2).
+struct PrepParams {
+    int B, H, T, Dv;
+    int bf16;
+    int log2_negated;
+    float lambda;
+    const float* lambda_dev;
+    const void* out; const void* out2; const void* dout;
+    int64_t s_o[3];         // shared by out, out2 and dout
+    const float* lse;       // [B, H, T, 2]
+    float* stats;           // [B, H, T, 4]
+};
+
 // Decode helpers: query-row bucket (rows rounded up to 1, 2, 4 or 8; 0 if
 // there are more rows than one CTA of width D takes), and the number of
 // workspace floats for `units` CTAs along the heads and query rows.
@@ -139,6 +163,11 @@ int launch_bwd_tc(const CUtensorMap* maps /*dq: q1,k1,q2,k2,v,do; dkdv: the same
 // hold the per-block partial sums.
 int launch_bwd_dlambda(const float* stats, int64_t rows, float sign, float* out,
                        cudaStream_t stream);
+int launch_bwd_prep(const PrepParams& p, cudaStream_t stream);
+// The CUDA-core backward without its statistics pass (the statistics are in
+// p.stats already).
+int launch_bwd_simt_grads_f32(const BwdParams& p, cudaStream_t stream);
+int launch_bwd_simt_grads_bf16(const BwdParams& p, cudaStream_t stream);
 int launch_bwd_simt_f32(const BwdParams& p, cudaStream_t stream);
 int launch_bwd_simt_bf16(const BwdParams& p, cudaStream_t stream);
 int launch_fwd_simt_f32(const SimtParams& p, cudaStream_t stream);

@@ -220,6 +220,24 @@ int diffattn_fwd_ex(const diffattn_desc *desc, const void *q1, const void *k1,
                     diffattn_stream_t stream);
 
 /*
+ * diffattn_fwd_train -- diffattn_fwd that also keeps what the backward needs
+ * (the forward of a training step): besides O it writes
+ *
+ *     out2 = A_2 V                  [B, H, T, 2D], desc->o_stride, inputs' dtype
+ *     lse  = log sum_j exp(S_b)     [B, H, T, 2] float32, dense, natural log,
+ *                                   S_b = Q_b K_b^T / sqrt(D) + M, b = 1, 2
+ *
+ * (with O = A_1 V - lambda A_2 V, the pair (O, out2) gives each branch's
+ * output).  No output epilogue.  Other arguments, kernel choice and errors as
+ * diffattn_fwd, plus DIFFATTN_ERR_INVALID for a NULL out2 or lse.  out2 must
+ * not overlap any input or O.
+ */
+int diffattn_fwd_train(const diffattn_desc *desc, const void *q1, const void *k1,
+                       const void *q2, const void *k2, const void *v, float lambda,
+                       const float *lambda_dev, int causal, void *out, void *out2, float *lse,
+                       void *workspace, size_t workspace_bytes, diffattn_stream_t stream);
+
+/*
  * diffattn_bwd_workspace_bytes -- bytes of device workspace diffattn_bwd needs
  * for this descriptor (four float32 row statistics per query row, plus 512
  * bytes of partial sums), or 0 for a NULL descriptor or sizes < 1.
@@ -267,6 +285,22 @@ int diffattn_bwd(const diffattn_desc *desc, const void *q1, const void *k1,
                  const float *lambda_dev, int causal, const void *dout, void *dq1,
                  void *dk1, void *dq2, void *dk2, void *dv, float *dlambda,
                  void *workspace, size_t workspace_bytes, diffattn_stream_t stream);
+
+/*
+ * diffattn_bwd_saved -- diffattn_bwd from the results diffattn_fwd_train kept:
+ * out (O), out2 (A_2 V) and lse, with the same desc, inputs, lambda and mask.
+ * The row statistics then come from one elementwise pass over dO, O and out2
+ * instead of a recomputation of the forward: Dd_2 = dO . out2 and
+ * Dd_1 = dO . (O + lambda out2).  out, out2 and dout share desc->o_stride.
+ * Other arguments, kernels and errors as diffattn_bwd, plus
+ * DIFFATTN_ERR_INVALID for a NULL out, out2 or lse.
+ */
+int diffattn_bwd_saved(const diffattn_desc *desc, const void *q1, const void *k1,
+                       const void *q2, const void *k2, const void *v, float lambda,
+                       const float *lambda_dev, int causal, const void *out,
+                       const void *out2, const float *lse, const void *dout, void *dq1,
+                       void *dk1, void *dq2, void *dk2, void *dv, float *dlambda,
+                       void *workspace, size_t workspace_bytes, diffattn_stream_t stream);
 
 /*
  * Decode over a key/value cache: Tq new queries against Tk cached keys.

@@ -106,7 +106,16 @@ def grad_scale(ref: np.ndarray) -> float:
     return max(1.0, float(np.sqrt(np.mean(ref * ref)))) if ref.size else 1.0
 
 
-def assert_grad_close(got, ref, dtype: str, what: str = "") -> dict:
+# Backward from saved forward results: the row statistics Dd_b are formed from
+# the bf16-rounded saved outputs (Dd_2 = dO . O2, Dd_1 = dO . (O + lambda O2),
+# two roundings of half an ulp each per element of O and O2).  That error is
+# the same for every key of a row, so it adds coherently along each row of dS:
+# dQ_b and dK_b take it once more on top of the recomputing path's error.  The
+# bf16 bounds for that path are therefore twice the above (slack = 2).
+SAVED_PATH_SLACK = 2.0
+
+
+def assert_grad_close(got, ref, dtype: str, what: str = "", slack: float = 1.0) -> dict:
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
@@ -127,6 +136,6 @@ def assert_grad_close(got, ref, dtype: str, what: str = "") -> dict:
     if dtype == "f32":
         assert stats["max_rel"] <= F32_MAX_ABS, f"{what} fp32 gradient {stats}"
     else:
-        assert stats["max_excess_rel"] <= BF16_MAX_ABS, f"{what} bf16 gradient max {stats}"
-        assert stats["mean_excess_rel"] <= BF16_MEAN_ABS, f"{what} bf16 gradient mean {stats}"
+        assert stats["max_excess_rel"] <= slack * BF16_MAX_ABS, f"{what} bf16 gradient max {stats}"
+        assert stats["mean_excess_rel"] <= slack * BF16_MEAN_ABS, f"{what} bf16 gradient mean {stats}"
     return stats
