@@ -30,8 +30,8 @@
 //   rows.  For every query head of the group and every 64-query tile:
 //   S_1^T = K_1 Q_1^T, S_2^T, dP^T = V dO^T; the two warpgroups split the 64
 //   query columns, form dS_1^T, dS_2^T and W^T = A_1^T - lambda A_2^T and write
-//   them as bf16 operands to shared memory; then dV += W^T dO,
-//   dK_b += dS_b^T Q_b.  The item's accumulators (dV, dK_1, dK_2: 256
+//   them as bf16 operands (W^T and dS_1^T to the spare TMEM columns, dS_2^T
+//   to shared memory); then dV += W^T dO, dK_b += dS_b^T Q_b.  The item's accumulators (dV, dK_1, dK_2: 256
 //   columns) leave room for one set of score buffers (192 columns); the
 //   warpgroups copy a tile's scores to registers and release the buffers at
 //   once, so the next tile's score products run during this tile's
@@ -424,7 +424,7 @@ namespace dkdv {
 
 constexpr int BM = 128;            // key rows per item (TMEM lanes)
 constexpr int BN = 64;             // query rows per tile
-constexpr int QSTAGES = 3;         // (Q1, Q2, dO, row statistics) ring
+constexpr int QSTAGES = 4;         // (Q1, Q2, dO, row statistics) ring
 constexpr uint32_t K_BYTES = BM * HD * 2;          // 16 KB
 constexpr uint32_t V_HALF = BM * 64 * 2;           // 16 KB
 constexpr uint32_t Q_BYTES = BN * HD * 2;          // 8 KB
@@ -438,11 +438,12 @@ constexpr uint32_t OFF_K2 = OFF_K1 + K_BYTES;
 constexpr uint32_t OFF_V = OFF_K2 + K_BYTES;                       // two halves
 constexpr uint32_t OFF_QS = OFF_V + 2 * V_HALF;                    // stages (1024-aligned)
 constexpr uint32_t QSTAGE_STRIDE = (QSTAGE_BYTES + 1023) & ~1023u;
-// bf16 operands written by the elementwise warps: dS_1^T, dS_2^T, W^T, each
-// [128 keys x 64 queries], K-major with 128-byte swizzling
+// bf16 operand written to shared memory by the elementwise warps: dS_2^T
+// [128 keys x 64 queries], K-major with 128-byte swizzling (W^T and dS_1^T go
+// to tensor memory)
 constexpr uint32_t PK_BYTES = BM * BN * 2;                         // 16 KB
 constexpr uint32_t OFF_PK = OFF_QS + QSTAGES * QSTAGE_STRIDE;
-constexpr uint32_t OFF_BAR = OFF_PK + 3 * PK_BYTES;
+constexpr uint32_t OFF_BAR = OFF_PK + PK_BYTES;
 constexpr int BAR_KV_FULL = 0;
 constexpr int BAR_KV_EMPTY = 1;
 constexpr int BAR_Q_FULL = 2;
@@ -461,12 +462,14 @@ constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM: S1^T [0,64), S2^T [64,128), dP^T [128,192); dV [192,320), dK1
-// [320,384), dK2 [384,448).
+// [320,384), dK2 [384,448); the bf16 operands W^T [448,480) and dS1^T
+// [480,512) (32 columns each: two queries per column).
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S1 = 0, TM_S2 = 64, TM_DP = 128, TM_DV = 192, TM_DK1 = 320, TM_DK2 = 384;
+constexpr uint32_t TM_W = 448, TM_DS1 = 480;
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);     // K x Q^T, V x dO^T
-constexpr uint32_t IDESC_DV = idesc_bf16_f32(BM, VD, 0, 1);    // W^T (smem) x dO (MN-major)
-constexpr uint32_t IDESC_DK = idesc_bf16_f32(BM, HD, 0, 1);    // dS^T (smem) x Q (MN-major)
+constexpr uint32_t IDESC_DV = idesc_bf16_f32(BM, VD, 0, 1);    // W^T (TMEM) x dO (MN-major)
+constexpr uint32_t IDESC_DK = idesc_bf16_f32(BM, HD, 0, 1);    // dS^T x Q (MN-major)
 
 struct Item {
     int b, hk, kt;
@@ -643,15 +646,16 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         tc_fence_after();
                         const uint32_t qs = done % QSTAGES;
                         const uint64_t sb = (qs * QSTAGE_STRIDE) >> 4;
-                        // dV += W^T dO, dK_b += dS_b^T Q_b (A operands from shared memory)
+                        // dV += W^T dO, dK_1 += dS_1^T Q_1 (A operands from TMEM),
+                        // dK_2 += dS_2^T Q_2 (A operand from shared memory)
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk) {
                             const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                            mma_ss(tmem_base + TM_DV, pkd + 2 * (PK_BYTES >> 4) + 2 * kk,
+                            mma_ts(tmem_base + TM_DV, tmem_base + TM_W + kk * 8,
                                    qm + sb + (QS_DO >> 4) + 128 * kk, IDESC_DV, acc);
-                            mma_ss(tmem_base + TM_DK1, pkd + 2 * kk,
+                            mma_ts(tmem_base + TM_DK1, tmem_base + TM_DS1 + kk * 8,
                                    qm + sb + (QS_Q1 >> 4) + 128 * kk, IDESC_DK, acc);
-                            mma_ss(tmem_base + TM_DK2, pkd + (PK_BYTES >> 4) + 2 * kk,
+                            mma_ss(tmem_base + TM_DK2, pkd + 2 * kk,
                                    qm + sb + (QS_Q2 >> 4) + 128 * kk, IDESC_DK, acc);
                         }
                         mma_commit(&bars[BAR_PK_FREE]);
@@ -754,20 +758,23 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 }
                 // the previous tile's dV/dK products must have read the operands
                 if (qc > 0 && !(ok = mbar_wait_warp(&bars[BAR_PK_FREE], (qc - 1) & 1u, ab))) break;
-                // row `row`, queries [c0, c0 + 32) = 16-byte chunks 4*half .. 4*half + 3,
-                // swizzled by the row's position within its 8-row group
+                // W^T and dS_1^T to TMEM: queries [c0, c0 + 32) are packed columns
+                // [16*half, 16*half + 16) of their regions
+                tmem_st16(lane_base + TM_W + 16 * half, w3);
+                tmem_st16(lane_base + TM_DS1 + 16 * half, w1);
+                // dS_2^T to shared memory: row `row`, queries [c0, c0 + 32) = 16-byte
+                // chunks 4*half .. 4*half + 3, swizzled by the row's position within
+                // its 8-row group
                 uint8_t* prow = smem + OFF_PK + row * 128;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t off = (uint32_t)(((4 * half + i) ^ (row & 7)) * 16);
                     *reinterpret_cast<uint4*>(prow + off) =
-                        make_uint4(w1[4 * i], w1[4 * i + 1], w1[4 * i + 2], w1[4 * i + 3]);
-                    *reinterpret_cast<uint4*>(prow + PK_BYTES + off) =
                         make_uint4(w2[4 * i], w2[4 * i + 1], w2[4 * i + 2], w2[4 * i + 3]);
-                    *reinterpret_cast<uint4*>(prow + 2 * PK_BYTES + off) =
-                        make_uint4(w3[4 * i], w3[4 * i + 1], w3[4 * i + 2], w3[4 * i + 3]);
                 }
                 fence_proxy_async_smem();
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[BAR_DS_FULL]);
             }
