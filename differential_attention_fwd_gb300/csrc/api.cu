@@ -176,10 +176,11 @@ int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
     const int64_t Hk = d->H / g;
     const int64_t units = d->B * Hk * row_chunks;
     if (units > (1ll << 24) || d->B * d->H > (1ll << 24)) return DIFFATTN_ERR_UNSUPPORTED;
-    // Split every head's keys so that the whole launch has ~1024 CTAs, with
-    // at least 256 keys (one chunk) per split.
+    // Split every unit's keys into ~4096 work items for the whole call, with
+    // at least 256 keys (one chunk) per split: the persistent grid of the
+    // first pass then ends at most one short item apart across its CTAs.
     const int64_t chunks = (d->Tk + 255) / 256;
-    int64_t splits = (1024 + units - 1) / units;
+    int64_t splits = (4096 + units - 1) / units;
     if (splits > chunks) splits = chunks;
     if (splits < 1) splits = 1;
     const int64_t split_len = ((chunks + splits - 1) / splits) * 256;
@@ -672,6 +673,7 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
     p.row_chunks = plan.row_chunks;
     p.tq_bucket = plan.tq_bucket;
     p.splits = plan.splits;
+    p.total_items = (int)((int64_t)plan.Hk * d.B * plan.row_chunks * plan.splits);
     p.split_len = plan.split_len;
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.D));
     p.lambda = lambda;

@@ -9,8 +9,9 @@
 // The work is bound by reading K1, K2 and V once (256 bytes per key and head
 // for D = 64 in bf16), so it runs on the CUDA cores with coalesced loads and
 // splits the keys of every head across CTAs:
-//   pass 1 (partial): CTA (b, key/value head, row chunk, split) walks its key
-//     range in chunks of 256 keys: every thread scores one key against all
+//   pass 1 (partial): for each work item (b, key/value head, row chunk, split)
+//     a CTA walks the item's key range in chunks of 256 keys (the grid is one
+//     wave of persistent CTAs that take the items in turn): every thread scores one key against all
 //     query rows of the CTA in both branches,
 //     the block keeps an online softmax per (query, branch) in log2 units, and
 //     every warp accumulates P V for its share of the keys, lanes spread over
@@ -113,8 +114,14 @@ decode_partial_kernel(const DecodeParams p) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int split = blockIdx.x % p.splits;
-    const int unit = blockIdx.x / p.splits;        // (b, key/value head, row chunk)
+    __shared__ int last_key[TQ];
+    // Persistent: the grid holds as many CTAs as fit on the GPU at once, and
+    // CTA c takes work items c, c + grid, ...; items are (unit, key split)
+    // pairs of equal length, so no CTA has more than one item more than another.
+    for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
+    __syncthreads();    // the previous item's shared-memory reads are done
+    const int split = item % p.splits;
+    const int unit = item / p.splits;              // (b, key/value head, row chunk)
     const int rc = unit % p.row_chunks;
     const int bhk = unit / p.row_chunks;
     const int b = bhk / p.Hk;
@@ -146,7 +153,6 @@ decode_partial_kernel(const DecodeParams p) {
         stat[2 * tid + 1] = 0.f;     // running sum
     }
     // last visible key of each row; causal: row (i, q) sits at position Tk - Tq + q
-    __shared__ int last_key[TQ];
     if (tid < TQ) last_key[tid] = p.causal ? p.Tk - p.Tq + (rc * TQ + tid) % p.Tq : p.Tk;
     float acc[TQ][2][DPL];
 #pragma unroll
@@ -288,6 +294,7 @@ decode_partial_kernel(const DecodeParams p) {
         part[q * (4 + 2 * DV) + 2 * br] = stat[2 * tid];
         part[q * (4 + 2 * DV) + 2 * br + 1] = stat[2 * tid + 1];
     }
+    }   // work items
 }
 
 // One block per (b, h, query), one thread per output column.
@@ -361,7 +368,16 @@ int launch_tq(const DecodeParams& p, cudaStream_t stream) {
     if (cudaFuncSetAttribute(decode_partial_kernel<T, D, TQ>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return -1;
-    decode_partial_kernel<T, D, TQ><<<p.B * p.Hk * p.row_chunks * p.splits, CHUNK, smem, stream>>>(p);
+    // one wave of CTAs, as many as are resident at once
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_partial_kernel<T, D, TQ>, CHUNK,
+                                                      smem) != cudaSuccess)
+        return -1;
+    const int64_t slots = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+    const int grid = (int)(p.total_items < slots ? p.total_items : slots);
+    decode_partial_kernel<T, D, TQ><<<grid, CHUNK, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return -1;
     decode_combine_kernel<T, D, TQ><<<p.B * p.H * p.Tq, DV, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;

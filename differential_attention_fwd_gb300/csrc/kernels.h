@@ -79,7 +79,8 @@ struct DecodeParams {
     int causal;
     int bf16;               // element type: 1 bf16, 0 fp32
     int tq_bucket;          // query rows per CTA: 1, 2, 4 or 8
-    int splits;             // key-range splits per head
+    int splits;             // key-range splits per unit (b, key/value head, row chunk)
+    int total_items;        // units * splits
     int split_len;          // keys per split (multiple of 256)
     float scale_log2;       // log2(e) / sqrt(D)
     float lambda;
