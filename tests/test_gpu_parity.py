@@ -158,3 +158,43 @@ def test_lambda_kernel_matches_oracle():
     e = torch.zeros(8, device="cuda"); e[0] = 1.0
     t = torch.zeros(8, device="cuda"); t[0] = 2.0
     assert abs(float(da.differential_lambda(e, t, z[:8], z[:8], 0.2)) - (np.exp(2) - 1 + 0.2)) <= 1e-6
+
+
+def test_grouped_shared_keys_b2h16kv4t8192_sampled():
+    # the DIFF V2 layout at the headline size: 16 heads over 4 key/value heads,
+    # one key tensor for both branches
+    w = W.GQA_WORKLOADS["b2h16kv4t8192_shared_k"]
+    inp = W.draw(w)
+    lam = lambda32(w, inp)
+    dev = [to_device(x, w.dtype) for x in (inp.q1, inp.k1, inp.q2, inp.v)]
+    q1, k, q2, v = dev
+    assert da.select_kernel(q1, k, q2, k, v) == da.DIFFATTN_KERNEL_TCGEN05
+    out = da.differential_attention(q1, k, q2, k, v, lam, causal=w.causal)
+    torch.cuda.synchronize()
+    assert da.get_device_error() == 0
+    rows = W.check_rows(w.T, n_random=32, seed=5)[::4]
+    sampled_check(w, inp, out, lam, w.causal, [(0, 3), (1, 12)], rows)
+
+
+def test_headline_backward_sampled_heads():
+    # the backward at the headline size, from the training forward's saved
+    # results (the launch configuration of bench.py --mode backward); the
+    # oracle's backward for two key/value heads (query heads (0,0) and (1,15))
+    from tests.helpers import SAVED_PATH_SLACK, assert_grad_close
+    w = W.WORKLOADS["b2h16t8192"]
+    inp = W.draw(w)
+    lam = lambda32(w, inp)
+    rng = np.random.Generator(np.random.PCG64(w.seed + 1000))
+    dout = W.round_to_bf16(rng.standard_normal((w.B, w.H, w.T, w.Dv), dtype=np.float32))
+    dev = [to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    saved = da.differential_attention_train(*dev, lam, causal=True)
+    got = da.differential_attention_backward(*dev, lam, to_device(dout, "bf16"), True, saved=saved)
+    torch.cuda.synchronize()
+    assert da.get_device_error() == 0
+    heads = [(0, 0), (1, 15)]
+    ref = oracle.differential_attention_backward(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, lam, dout,
+                                                 True, kv_heads=heads)
+    for b, h in heads:
+        for name, g, r in zip(("dq1", "dk1", "dq2", "dk2", "dv"), got[:5], ref[:5]):
+            assert_grad_close(to_numpy(g[b, h]), r[b, h], "bf16", f"headline backward ({b},{h}) {name}",
+                              slack=SAVED_PATH_SLACK)
