@@ -26,7 +26,8 @@ from ._lib import (DIFFATTN_BF16, DIFFATTN_F32, DIFFATTN_KERNEL_SIMT,  # noqa: F
                    DIFFATTN_NORM_RMS, DiffattnDesc, DiffattnEpilogue, DiffattnError,
                    DiffattnKvDesc)
 
-__all__ = ["differential_lambda", "differential_attention", "differential_attention_train",
+__all__ = ["differential_lambda", "differential_attention", "differential_attention_host",
+           "differential_attention_train",
            "differential_attention_backward",
            "differential_attention_decode",
            "make_desc", "make_kv_desc", "select_kernel", "get_device_error", "version",
@@ -243,6 +244,50 @@ def _forward(q1, k1, q2, k2, value, coefficient, causal, out, dynamic_schedule, 
                                  1 if causal else 0, ctypes.byref(epi[0]) if epi else None,
                                  ctypes.c_void_p(out.data_ptr()), *ws_args)
     _lib.check(rc, "diffattn_fwd")
+    return out
+
+
+def differential_attention_host(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
+                                k2: torch.Tensor, value: torch.Tensor, coefficient,
+                                causal: bool = True, out: Optional[torch.Tensor] = None,
+                                device=None, buffers=None) -> torch.Tensor:
+    """differential_attention for inputs in host memory (CPU tensors,
+    preferably pinned): the library copies them to the device, runs the
+    forward and copies the output back, overlapping the copies of one chunk of
+    heads with the forward of another.  Returns the [B, H, T, 2D] output on
+    the host (`out`, a pinned CPU tensor, if given).  `buffers`: optional
+    device tensors (q1, k1, q2, k2, value, out) to reuse between calls.  The
+    result is ready when the current stream of `device` has completed."""
+    ts = [q1, k1, q2, k2, value]
+    if any(t.device.type != "cpu" for t in ts):
+        raise ValueError("differential_attention_host takes CPU tensors")
+    ts = [t.contiguous() for t in ts]
+    q1, k1, q2, k2, value = ts
+    B, H, T, D = q1.shape
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if out is None:
+        out = torch.empty((B, H, T, 2 * D), dtype=q1.dtype).pin_memory()
+    if buffers is None:
+        dk1 = torch.empty(k1.shape, dtype=k1.dtype, device=dev)
+        buffers = [torch.empty(q1.shape, dtype=q1.dtype, device=dev), dk1,
+                   torch.empty(q2.shape, dtype=q2.dtype, device=dev),
+                   dk1 if k2 is k1 else torch.empty(k2.shape, dtype=k2.dtype, device=dev),
+                   torch.empty(value.shape, dtype=value.dtype, device=dev),
+                   torch.empty((B, H, T, 2 * D), dtype=q1.dtype, device=dev)]
+    lam_host, lam_dev = _coefficient(coefficient, dev)
+    d = make_desc(*buffers[:5], buffers[5])
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev)
+        ws = workspace_for(dev, stream)
+        rc = lib.diffattn_fwd_host(ctypes.byref(d), *(ctypes.c_void_p(t.data_ptr()) for t in ts),
+                                   ctypes.c_float(lam_host),
+                                   ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0),
+                                   1 if causal else 0, ctypes.c_void_p(out.data_ptr()),
+                                   *(ctypes.c_void_p(t.data_ptr()) for t in buffers),
+                                   ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel() * 4),
+                                   ctypes.c_void_p(stream.cuda_stream))
+    _lib.check(rc, "diffattn_fwd_host")
     return out
 
 

@@ -29,6 +29,7 @@ EXPORTED = (
     "diffattn_lambda_backward",
     "diffattn_fwd",
     "diffattn_fwd_ex",
+    "diffattn_fwd_host",
     "diffattn_fwd_train",
     "diffattn_bwd",
     "diffattn_bwd_saved",
@@ -115,6 +116,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_bwd.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp, ctypes.c_float,
                                  vp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.diffattn_bwd.restype = ctypes.c_int
+    lib.diffattn_fwd_host.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp,
+                                      ctypes.c_float, vp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp,
+                                      vp, ctypes.c_size_t, vp]
+    lib.diffattn_fwd_host.restype = ctypes.c_int
     lib.diffattn_fwd_train.argtypes = [ctypes.POINTER(DiffattnDesc), vp, vp, vp, vp, vp,
                                        ctypes.c_float, vp, ctypes.c_int, vp, vp, vp, vp,
                                        ctypes.c_size_t, vp]

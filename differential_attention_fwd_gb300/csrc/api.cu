@@ -703,6 +703,139 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
                                                                        : DIFFATTN_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace diffattn {
+namespace {
+
+// Streams and events of the host-buffer forward, created once per device.
+constexpr int kHostChunksMax = 8;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    cudaEvent_t start = nullptr, in[kHostChunksMax] = {}, done[kHostChunksMax] = {},
+                out[kHostChunksMax] = {};
+};
+HostPipe g_pipes[kMaxDevices];
+std::mutex g_pipe_mutex;      // held while a call enqueues (the events are reused)
+
+int host_pipe(HostPipe** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DIFFATTN_ERR_CUDA;
+    HostPipe& hp = g_pipes[dev];
+    if (!hp.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&hp.copy_in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.copy_out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.start, ef) != cudaSuccess)
+            return DIFFATTN_ERR_CUDA;
+        for (int i = 0; i < kHostChunksMax; ++i)
+            if (cudaEventCreateWithFlags(&hp.in[i], ef) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.done[i], ef) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.out[i], ef) != cudaSuccess)
+                return DIFFATTN_ERR_CUDA;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return DIFFATTN_OK;
+}
+
+// Dense element strides of a [B, heads, T, inner] tensor.
+bool dense(const int64_t s[3], const diffattn_desc& d, int64_t heads, int64_t inner) {
+    return (d.T == 1 || s[2] == inner) && (heads == 1 || s[1] == d.T * inner) &&
+           (d.B == 1 || s[0] == heads * d.T * inner);
+}
+
+}  // namespace
+}  // namespace diffattn
+
+extern "C" {
+
+int diffattn_fwd_host(const diffattn_desc* desc, const void* q1_host, const void* k1_host,
+                      const void* q2_host, const void* k2_host, const void* v_host, float lambda,
+                      const float* lambda_dev, int causal, void* out_host, void* q1, void* k1,
+                      void* q2, void* k2, void* v, void* out, void* workspace,
+                      size_t workspace_bytes, diffattn_stream_t stream) {
+    int rc = validate(desc, q1, k1, q2, k2, v, out);
+    if (rc != DIFFATTN_OK) return rc;
+    if (!q1_host || !k1_host || !q2_host || !k2_host || !v_host || !out_host)
+        return DIFFATTN_ERR_INVALID;
+    if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
+    const diffattn_desc& d = *desc;
+    const int64_t g = group_of(d.kv_group);
+    const int64_t hk = d.H / g;
+    if (!dense(d.q1_stride, d, d.H, d.D) || !dense(d.q2_stride, d, d.H, d.D) ||
+        !dense(d.k1_stride, d, hk, d.D) || !dense(d.k2_stride, d, hk, d.D) ||
+        !dense(d.v_stride, d, hk, 2 * d.D) || !dense(d.o_stride, d, d.H, 2 * d.D))
+        return DIFFATTN_ERR_INVALID;
+    DeviceState* dev = nullptr;
+    rc = device_state(&dev);
+    if (rc != DIFFATTN_OK) return rc;
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipe* hp = nullptr;
+    rc = host_pipe(&hp);
+    if (rc != DIFFATTN_OK) return rc;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t es = d.dtype == DIFFATTN_BF16 ? 2 : 4;
+    // Chunks of whole key/value heads (with their g query heads: in the dense
+    // layout both are contiguous byte ranges), each with at least two work
+    // items per SM for the forward, at most kHostChunksMax.  The call then takes
+    // about the input copies' time plus one chunk's forward and output copy.
+    const int64_t units = d.B * hk;
+    const int64_t items_per_unit = g * ((d.T + 127) / 128);
+    int64_t chunks = units * items_per_unit / (2ll * dev->num_sms);
+    if (chunks > kHostChunksMax) chunks = kHostChunksMax;
+    if (chunks > units) chunks = units;
+    if (chunks < 1) chunks = 1;
+    const bool k_same = k1_host == k2_host && k1 == k2;
+    const int64_t qrow = d.T * d.D * (int64_t)es;        // bytes of one query head of Q1 / Q2
+    const int64_t orow = d.T * 2 * d.D * (int64_t)es;    // of O and of V per head
+    auto copy = [&](void* dst, const void* src, int64_t off, int64_t bytes, cudaMemcpyKind kind,
+                    cudaStream_t s) {
+        return cudaMemcpyAsync(static_cast<char*>(dst) + off, static_cast<const char*>(src) + off,
+                               (size_t)bytes, kind, s) == cudaSuccess;
+    };
+    // the copies start after the work already on the caller's stream
+    if (cudaEventRecord(hp->start, st) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->copy_in, hp->start, 0) != cudaSuccess)
+        return DIFFATTN_ERR_CUDA;
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int64_t u0 = units * c / chunks, u1 = units * (c + 1) / chunks;
+        const int64_t nq = (u1 - u0) * g;                  // query heads in the chunk
+        const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+        if (!copy(q1, q1_host, u0 * g * qrow, nq * qrow, h2d, hp->copy_in) ||
+            !copy(q2, q2_host, u0 * g * qrow, nq * qrow, h2d, hp->copy_in) ||
+            !copy(k1, k1_host, u0 * qrow, (u1 - u0) * qrow, h2d, hp->copy_in) ||
+            (!k_same && !copy(k2, k2_host, u0 * qrow, (u1 - u0) * qrow, h2d, hp->copy_in)) ||
+            !copy(v, v_host, u0 * orow, (u1 - u0) * orow, h2d, hp->copy_in) ||
+            cudaEventRecord(hp->in[c], hp->copy_in) != cudaSuccess ||
+            cudaStreamWaitEvent(st, hp->in[c], 0) != cudaSuccess)
+            return DIFFATTN_ERR_CUDA;
+        // the chunk as a problem of its own: B = 1, its query heads as H
+        diffattn_desc cd = d;
+        cd.B = 1;
+        cd.H = nq;
+        for (int64_t* sd : {cd.q1_stride, cd.q2_stride, cd.k1_stride, cd.k2_stride, cd.v_stride,
+                            cd.o_stride})
+            sd[0] = 0;
+        rc = forward_impl(&cd, static_cast<char*>(q1) + u0 * g * qrow,
+                          static_cast<char*>(k1) + u0 * qrow, static_cast<char*>(q2) + u0 * g * qrow,
+                          static_cast<char*>(k2) + u0 * qrow, static_cast<char*>(v) + u0 * orow,
+                          lambda, lambda_dev, causal, nullptr,
+                          static_cast<char*>(out) + u0 * g * orow, nullptr, nullptr, workspace,
+                          workspace_bytes, stream);
+        if (rc != DIFFATTN_OK) return rc;
+        if (cudaEventRecord(hp->done[c], st) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->copy_out, hp->done[c], 0) != cudaSuccess ||
+            !copy(out_host, out, u0 * g * orow, nq * orow, cudaMemcpyDeviceToHost, hp->copy_out) ||
+            cudaEventRecord(hp->out[c], hp->copy_out) != cudaSuccess)
+            return DIFFATTN_ERR_CUDA;
+    }
+    // the call is complete on the caller's stream once the last output copy is
+    return cudaStreamWaitEvent(st, hp->out[chunks - 1], 0) == cudaSuccess ? DIFFATTN_OK
+                                                                           : DIFFATTN_ERR_CUDA;
+}
+
 int diffattn_get_device_error(diffattn_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return DIFFATTN_ERR_CUDA;

@@ -220,6 +220,36 @@ int diffattn_fwd_ex(const diffattn_desc *desc, const void *q1, const void *k1,
                     diffattn_stream_t stream);
 
 /*
+ * diffattn_fwd_host -- diffattn_fwd with the inputs and the output in host
+ * memory: copies the inputs in, runs the forward and copies O out, as a
+ * pipeline over chunks of whole key/value heads (the copy of chunk c + 1 and
+ * the copy back of chunk c - 1 overlap the forward of chunk c).  The result
+ * is the same as diffattn_fwd's.
+ *
+ * q1_host, k1_host, q2_host, k2_host, v_host: host pointers to the inputs;
+ * out_host: host pointer that receives O.  Page-locked (pinned) host memory
+ * lets the copies run asynchronously; pageable memory also works, with copies
+ * that block the calling thread.  q1 .. v, out: device buffers of the full
+ * sizes, owned by the caller, that the call fills and uses (the same as
+ * diffattn_fwd's inputs and output).  Every tensor, on the host and on the
+ * device, must be dense in the [B, H, T, *] order desc describes (K1, K2 and V
+ * with H / kv_group heads).  The copies start after the work already queued on
+ * `stream`, and the call's last copy is ordered before later work on
+ * `stream`; synchronise the stream before reading out_host.  The library keeps
+ * two copy streams and a few events per device for this call, created on
+ * first use; calls from several host threads are enqueued one at a time.
+ * Other arguments and errors as diffattn_fwd, plus DIFFATTN_ERR_INVALID for a
+ * NULL host pointer or a tensor that is not dense.  No counterpart on the
+ * pages: a library convenience for callers whose data starts and ends on the
+ * host.
+ */
+int diffattn_fwd_host(const diffattn_desc *desc, const void *q1_host, const void *k1_host,
+                      const void *q2_host, const void *k2_host, const void *v_host,
+                      float lambda, const float *lambda_dev, int causal, void *out_host,
+                      void *q1, void *k1, void *q2, void *k2, void *v, void *out,
+                      void *workspace, size_t workspace_bytes, diffattn_stream_t stream);
+
+/*
  * diffattn_fwd_train -- diffattn_fwd that also keeps what the backward needs
  * (the forward of a training step): besides O it writes
  *

@@ -268,3 +268,19 @@ def test_lambda_backward_rejects_without_gpu(lib):
     q = list(p)
     q[5] = None
     assert lib.diffattn_lambda_backward(*q[:4], 8, *q[4:], None) == _lib.DIFFATTN_ERR_INVALID
+
+
+def test_fwd_host_rejects_without_gpu(lib):
+    def call(d, hp=None):
+        hp = hp if hp is not None else ptrs(6, base=FAKE * 60)
+        return lib.diffattn_fwd_host(ctypes.byref(d), *hp[:5], ctypes.c_float(0.5), None, 1, hp[5],
+                                     *ptrs(6), None, 0, None)
+    hp = ptrs(6, base=FAKE * 60)
+    hp[2] = None
+    assert call(desc(), hp) == _lib.DIFFATTN_ERR_INVALID
+    d = desc(B=2)
+    d.v_stride[2] = 2 * 64 + 8           # not dense
+    assert call(d) == _lib.DIFFATTN_ERR_INVALID
+    d = desc(B=2)
+    d.q1_stride[1] = 0                   # broadcast heads are not dense
+    assert call(d) == _lib.DIFFATTN_ERR_INVALID
