@@ -674,6 +674,7 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
     p.kv_group = plan.kv_group;
     p.Hk = plan.Hk;
     p.row_chunks = plan.row_chunks;
+    p.dense_kv = (d.k1_stride[2] == d.D && d.k2_stride[2] == d.D && d.v_stride[2] == 2 * d.D) ? 1 : 0;
     p.tq_bucket = plan.tq_bucket;
     p.splits = plan.splits;
     p.total_items = (int)((int64_t)plan.Hk * d.B * plan.row_chunks * plan.splits);

@@ -25,6 +25,7 @@
 // chunks of tq_bucket rows, so one pass over a head's cache serves up to
 // tq_bucket rows of several heads.
 #include "kernels.h"
+#include "ptx.cuh"
 
 #include <cmath>
 
@@ -360,6 +361,298 @@ decode_combine_kernel(const DecodeParams p) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// First pass with asynchronous staging (bf16, D = 64, key and value rows dense
+// along the sequence): every thread of the CTA copies its share of a chunk of
+// 64 keys (K1, K2 and V rows) into a ring of shared-memory stages with
+// cp.async, two chunks ahead of the chunk being computed and across the CTA's
+// work items, so the compute never waits on HBM latency; two CTAs share an SM,
+// so one computes while the other waits at a barrier.  K rows are
+// stored with their 16-byte pieces XOR-swizzled by (row mod 8), so that the
+// thread-per-key reads of a warp (32 rows, one piece each) hit distinct banks.
+// Per chunk: thread (key, branch) scores its key against the TQ query rows of
+// its branch; the block forms the online-softmax statistics; warp w
+// accumulates P V for keys w, w + 8, ... with the lanes over the columns.  The
+// partial results have the layout the combine pass reads.
+namespace as {
+
+constexpr int CH = 64;                  // keys per chunk
+constexpr int THREADS = 2 * CH;         // 2 branches x CH keys
+constexpr int WARPS = THREADS / 32;
+constexpr int WPB = WARPS / 2;          // warps per branch
+constexpr int HDIM = 64;
+constexpr int DV = 2 * HDIM;
+constexpr int KROW = HDIM * 2;          // bytes of one bf16 key row (128)
+constexpr int VROW = DV * 2;            // bytes of one bf16 value row (256)
+constexpr int STAGE = CH * (2 * KROW + VROW);   // 32 KB
+constexpr int NST = 3;                  // stages: two chunks in flight ahead
+
+template <int TQ>
+constexpr size_t smem_bytes() {
+    return (size_t)NST * STAGE +
+           sizeof(float) * (TQ * 2 * HDIM + CH * TQ * 2 + WARPS * TQ * 2 + TQ * 4 + TQ * 2 +
+                            WARPS * TQ * 2 * DV) + 16 * TQ + 128;
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The CTA's sequence of chunks: item it (the CTA's k-th), chunk c of it.
+struct Cursor {
+    int item = 0, c = 0, n = 0;        // n: chunks of the item; item >= total when done
+    int k_begin = 0, k_end = 0;
+    __device__ void set(const DecodeParams& p, int it) {
+        item = it;
+        c = 0;
+        if (it < p.total_items) {
+            const int split = it % p.splits;
+            k_begin = split * p.split_len;
+            k_end = min(p.Tk, k_begin + p.split_len);
+            n = (k_end - k_begin + CH - 1) / CH;
+        } else {
+            n = 0;
+        }
+    }
+    __device__ bool done(const DecodeParams& p) const { return item >= p.total_items; }
+    __device__ void next(const DecodeParams& p) {
+        if (++c >= n) set(p, item + gridDim.x);
+    }
+};
+
+template <int TQ>
+__global__ void __launch_bounds__(THREADS, 2) decode_async_kernel(const DecodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* stages = smem_raw;                                    // [NST][K1 | K2 | V]
+    float* qs = reinterpret_cast<float*>(smem_raw + NST * STAGE);  // [TQ][2][HDIM]
+    float* sc = qs + TQ * 2 * HDIM;                                // [CH][TQ][2]
+    float* red = sc + CH * TQ * 2;                                 // [WARPS][TQ]: per-branch partials
+    float* stat = red + WARPS * TQ * 2;                            // [TQ][2]: max, sum
+    float* alpha = stat + TQ * 4;                                  // [TQ][2]
+    float* acc_red = alpha + TQ * 2;                               // [WARPS][TQ][2][DV]
+    int* last_key = reinterpret_cast<int*>(acc_red + WARPS * TQ * 2 * DV);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kk = tid & (CH - 1);          // this thread's key within the chunk
+    const int br = tid / CH;                // and its branch
+    const __nv_bfloat16* K1 = static_cast<const __nv_bfloat16*>(p.k1);
+    const __nv_bfloat16* K2 = static_cast<const __nv_bfloat16*>(p.k2);
+    const __nv_bfloat16* Vv = static_cast<const __nv_bfloat16*>(p.v);
+
+    // copy chunk `cur` into stage st: K rows as 8 swizzled 16-byte pieces,
+    // V rows as 16 plain pieces; rows past the item's keys are zero-filled
+    auto issue = [&](const Cursor& cur, int st) {
+        const int unit = cur.item / p.splits;
+        const int bhk = unit / p.row_chunks;
+        const int b = bhk / p.Hk, hk = bhk - b * p.Hk;
+        const int key0 = cur.k_begin + cur.c * CH;
+        const char* k1 = reinterpret_cast<const char*>(K1 + b * p.s_k1[0] + hk * p.s_k1[1]);
+        const char* k2 = reinterpret_cast<const char*>(K2 + b * p.s_k2[0] + hk * p.s_k2[1]);
+        const char* vv = reinterpret_cast<const char*>(Vv + b * p.s_v[0] + hk * p.s_v[1]);
+        uint8_t* base = stages + st * STAGE;
+#pragma unroll
+        for (int i = 0; i < CH * 8 / THREADS; ++i) {        // K pieces: 8 per row
+            const int id = tid + i * THREADS;
+            const int r = id >> 3, j = id & 7;
+            const int key = key0 + r;
+            const bool ok = key < cur.k_end;
+            const int64_t off = (int64_t)(ok ? key : 0) * KROW + j * 16;
+            const int dst = r * KROW + ((j ^ (r & 7)) << 4);
+            cp_async16(base + dst, k1 + off, ok);
+            cp_async16(base + CH * KROW + dst, k2 + off, ok);
+        }
+#pragma unroll
+        for (int i = 0; i < CH * 16 / THREADS; ++i) {       // V pieces: 16 per row
+            const int id = tid + i * THREADS;
+            const int r = id >> 4, j = id & 15;
+            const int key = key0 + r;
+            const bool ok = key < cur.k_end;
+            cp_async16(base + 2 * CH * KROW + r * VROW + j * 16,
+                       vv + (int64_t)(ok ? key : 0) * VROW + j * 16, ok);
+        }
+    };
+
+    Cursor icur, ccur;                 // issue and compute positions
+    icur.set(p, blockIdx.x);
+    ccur = icur;
+#pragma unroll
+    for (int s0 = 0; s0 < NST - 1; ++s0) {
+        if (!icur.done(p)) {
+            issue(icur, s0);
+            icur.next(p);
+        }
+        cp_async_commit();
+    }
+    float acc[TQ][2][4];
+    int st = 0;                        // stage of the chunk being computed
+    int ist = NST - 1;                 // stage the next issue goes to
+    while (!ccur.done(p)) {
+        if (!icur.done(p)) {
+            issue(icur, ist);
+            icur.next(p);
+        }
+        cp_async_commit();
+        if (++ist == NST) ist = 0;
+        cp_async_wait<NST - 1>();
+        __syncthreads();
+        const int unit = ccur.item / p.splits;
+        const int rc = unit % p.row_chunks;
+        const int n_rows = p.kv_group * p.Tq;
+        if (ccur.c == 0) {
+            // a new item: its query rows, statistics and accumulators
+            const int bhk = unit / p.row_chunks;
+            const int b = bhk / p.Hk, hk = bhk - b * p.Hk;
+            for (int i = tid; i < TQ * 2 * HDIM; i += THREADS) {
+                const int r = i / (2 * HDIM), qb = (i / HDIM) & 1, d = i % HDIM;
+                const int row = rc * TQ + r;
+                float x = 0.f;
+                if (row < n_rows) {
+                    const int h = hk * p.kv_group + row / p.Tq;
+                    const int q = row % p.Tq;
+                    x = qb ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.q2)[
+                                 b * p.s_q2[0] + h * p.s_q2[1] + (int64_t)q * p.s_q2[2] + d])
+                           : __bfloat162float(static_cast<const __nv_bfloat16*>(p.q1)[
+                                 b * p.s_q1[0] + h * p.s_q1[1] + (int64_t)q * p.s_q1[2] + d]);
+                }
+                qs[i] = x;
+            }
+            if (tid < TQ * 2) {
+                stat[2 * tid] = -INFINITY;
+                stat[2 * tid + 1] = 0.f;
+            }
+            if (tid < TQ) last_key[tid] = p.causal ? p.Tk - p.Tq + (rc * TQ + tid) % p.Tq : p.Tk;
+#pragma unroll
+            for (int q = 0; q < TQ; ++q)
+#pragma unroll
+                for (int b2 = 0; b2 < 2; ++b2)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[q][b2][c] = 0.f;
+            __syncthreads();
+        }
+        const uint8_t* stg = stages + st * STAGE;
+        const int key = ccur.k_begin + ccur.c * CH + kk;
+        // ---- scores: this thread's key against the TQ rows of its branch
+        float s[TQ];
+#pragma unroll
+        for (int q = 0; q < TQ; ++q) s[q] = 0.f;
+        {
+            const uint8_t* krow = stg + br * CH * KROW + kk * KROW;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float x[8];
+                Vec<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16*>(krow + ((j ^ (kk & 7)) << 4)), x);
+#pragma unroll
+                for (int q = 0; q < TQ; ++q)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s[q] = fmaf(qs[(q * 2 + br) * HDIM + j * 8 + e], x[e], s[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < TQ; ++q) {
+            const bool vis = key < ccur.k_end && key <= last_key[q];
+            s[q] = vis ? s[q] * p.scale_log2 : -INFINITY;
+            const float wm = block_max_partial(s[q]);
+            if (lane == 0) red[warp * TQ + q] = wm;
+        }
+        __syncthreads();
+        // ---- new running max and rescale factor per (row, branch): the first
+        // WPB warps hold branch 1, the others branch 2
+        if (tid < TQ * 2) {
+            const int q = tid >> 1, b2 = tid & 1;
+            float cm = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < WPB; ++w) cm = fmaxf(cm, red[(b2 * WPB + w) * TQ + q]);
+            const float m_old = stat[2 * tid];
+            const float m_new = fmaxf(m_old, cm);
+            alpha[tid] = (m_old == m_new) ? 1.f : exp2f(m_old - m_new);
+            stat[2 * tid] = m_new;
+        }
+        __syncthreads();
+        // ---- weights and their sums
+#pragma unroll
+        for (int q = 0; q < TQ; ++q) {
+            const float w = ex2_masked(s[q], stat[2 * (q * 2 + br)]);
+            sc[(kk * TQ + q) * 2 + br] = w;
+            const float ws = warp_sum(w);
+            if (lane == 0) red[warp * TQ + q] = ws;
+        }
+        __syncthreads();
+        if (tid < TQ * 2) {
+            const int q = tid >> 1, b2 = tid & 1;
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < WPB; ++w) sum += red[(b2 * WPB + w) * TQ + q];
+            stat[2 * tid + 1] = stat[2 * tid + 1] * alpha[tid] + sum;
+        }
+        // ---- O += P V: warp w takes keys w, w + WARPS, ...; lane takes 4 columns
+#pragma unroll
+        for (int q = 0; q < TQ; ++q)
+#pragma unroll
+            for (int b2 = 0; b2 < 2; ++b2) {
+                const float a = alpha[q * 2 + b2];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[q][b2][c] *= a;
+            }
+        {
+            const uint8_t* vrows = stg + 2 * CH * KROW + lane * 8;
+#pragma unroll 4
+            for (int t = warp; t < CH; t += WARPS) {
+                float x[4];
+                load_cols<__nv_bfloat16, 4>(reinterpret_cast<const __nv_bfloat16*>(vrows + t * VROW), x);
+#pragma unroll
+                for (int q = 0; q < TQ; ++q)
+#pragma unroll
+                    for (int b2 = 0; b2 < 2; ++b2) {
+                        const float w = sc[(t * TQ + q) * 2 + b2];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) acc[q][b2][c] = fmaf(w, x[c], acc[q][b2][c]);
+                    }
+            }
+        }
+        if (ccur.c == ccur.n - 1) {
+            // ---- the item's last chunk: reduce the warps' accumulators and
+            // write the split's partial result
+#pragma unroll
+            for (int q = 0; q < TQ; ++q)
+#pragma unroll
+                for (int b2 = 0; b2 < 2; ++b2)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        acc_red[((warp * TQ + q) * 2 + b2) * DV + lane * 4 + c] = acc[q][b2][c];
+            __syncthreads();
+            const int split = ccur.item % p.splits;
+            float* part = p.work + ((int64_t)unit * p.splits + split) * TQ * (4 + 2 * DV);
+            for (int i = tid; i < TQ * 2 * DV; i += THREADS) {
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < WARPS; ++w) sum += acc_red[w * TQ * 2 * DV + i];
+                const int q = i / (2 * DV);
+                part[q * (4 + 2 * DV) + 4 + (i - q * 2 * DV)] = sum;
+            }
+            if (tid < TQ * 2) {
+                const int q = tid >> 1, b2 = tid & 1;
+                part[q * (4 + 2 * DV) + 2 * b2] = stat[2 * tid];
+                part[q * (4 + 2 * DV) + 2 * b2 + 1] = stat[2 * tid + 1];
+            }
+        }
+        __syncthreads();   // the stage and the shared statistics are free again
+        if (++st == NST) st = 0;
+        ccur.next(p);
+    }
+    cp_async_wait<0>();
+}
+
+}  // namespace as
+
 template <typename T, int D, int TQ>
 int launch_tq(const DecodeParams& p, cudaStream_t stream) {
     constexpr int DV = 2 * D;
@@ -377,6 +670,28 @@ int launch_tq(const DecodeParams& p, cudaStream_t stream) {
         return -1;
     const int64_t slots = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
     const int grid = (int)(p.total_items < slots ? p.total_items : slots);
+    // the staged first pass for up to two query rows per CTA (at Tq = 1 over
+    // an 8192-key cache: 0.73 of the copy bandwidth against 0.63); with more
+    // rows its per-chunk arithmetic outweighs the hidden latency, and the
+    // per-thread-load pass above runs faster
+    if constexpr (sizeof(T) == 2 && D == as::HDIM && TQ <= 2) {
+        if (p.dense_kv) {
+            constexpr size_t sm2 = as::smem_bytes<TQ>();
+            if (cudaFuncSetAttribute(as::decode_async_kernel<TQ>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2) != cudaSuccess)
+                return -1;
+            int per_sm2 = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm2, as::decode_async_kernel<TQ>,
+                                                              as::THREADS, sm2) != cudaSuccess)
+                return -1;
+            const int64_t slots2 = (int64_t)sms * (per_sm2 > 0 ? per_sm2 : 1);
+            const int g2 = (int)(p.total_items < slots2 ? p.total_items : slots2);
+            as::decode_async_kernel<TQ><<<g2, as::THREADS, sm2, stream>>>(p);
+            if (cudaGetLastError() != cudaSuccess) return -1;
+            decode_combine_kernel<T, D, TQ><<<p.B * p.H * p.Tq, DV, 0, stream>>>(p);
+            return cudaGetLastError() == cudaSuccess ? 0 : -1;
+        }
+    }
     decode_partial_kernel<T, D, TQ><<<grid, CHUNK, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return -1;
     decode_combine_kernel<T, D, TQ><<<p.B * p.H * p.Tq, DV, 0, stream>>>(p);

@@ -76,6 +76,7 @@ struct DecodeParams {
     int kv_group;           // query heads per key/value head (>= 1)
     int Hk;                 // key/value heads, H / kv_group
     int row_chunks;         // CTAs along the kv_group * Tq query rows of a key/value head
+    int dense_kv;           // K1, K2 and V rows contiguous along the sequence (async staging)
     int causal;
     int bf16;               // element type: 1 bf16, 0 fp32
     int tq_bucket;          // query rows per CTA: 1, 2, 4 or 8
