@@ -182,6 +182,39 @@ struct ItemRing {
     }
 };
 
+// Row max of one thread's 64 scores (four independent chains of
+// three-input maxima).
+__device__ __forceinline__ float tile_row_max(const float (&s)[64]) {
+    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+    for (int c = 4; c < 64; c += 8) {
+        mx0 = fmax3(mx0, s[c], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+    }
+    return fmax3(mx0, mx1, fmaxf(mx2, mx3));
+}
+
+// P = 2^(s * scale_log2 - m) for one thread's 64 scores, two columns per
+// packed operation: P rounded to bf16 pairs into pk, and the sum of the
+// unrounded P returned.
+__device__ __forceinline__ float tile_exp2(const float (&s)[64], float sl2, float m, uint32_t (&pk)[32]) {
+    const uint64_t scale2 = f2_pack(sl2, sl2);
+    const uint64_t negm2 = f2_pack(-m, -m);
+    uint64_t rsum[4] = {0, 0, 0, 0};     // four short addition chains
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        const uint64_t x = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), scale2, negm2);
+        const float p0 = ex2_approx(f2_lo(x));
+        const float p1 = ex2_approx(f2_hi(x));
+        rsum[c & 3] = f2_add(rsum[c & 3], f2_pack(p0, p1));
+        pk[c] = pack_bf16x2(p0, p1);
+    }
+    const uint64_t r = f2_add(f2_add(rsum[0], rsum[1]), f2_add(rsum[2], rsum[3]));
+    return f2_lo(r) + f2_hi(r);
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                        const __grid_constant__ CUtensorMap tm_k1,
@@ -466,47 +499,37 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = (c >= lim) ? -INFINITY : s[c];
                 }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-                for (int c = 4; c < 64; c += 8) {
-                    mx0 = fmax3(mx0, s[c], s[c + 1]);
-                    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-                    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
-                    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
-                }
-                mx0 = fmax3(mx0, mx1, fmaxf(mx2, mx3));
-                const float mxs = mx0 * sl2;
-
-                // Lazy rescale: move the running max only when this tile's
-                // row max exceeds it by more than 2^8 (warp-uniform decision,
-                // the O rescale below is a warp-collective TMEM access).
+                // Lazy rescale: the running max moves only when a row's tile
+                // max exceeds it by more than 8 (log2 units), i.e. when some
+                // P of the row would exceed 2^8.  Such a row's tile sum then
+                // exceeds 2^8 as well, so the exponentials are first taken
+                // against the running max and the row max (a reduction on the
+                // critical path) is formed only when some row's sum exceeds
+                // 2^8; the decision equals the one the row max alone would
+                // give.  The first tile of an item sets the running max.  The
+                // decision is warp-uniform: the O rescale below is a
+                // warp-collective TMEM access.
                 float alpha = 1.0f;
                 bool rescale = false;
-                if (j == 0) {
-                    m_run = mxs;
-                } else if (__any_sync(0xffffffffu, mxs > m_run + 8.0f)) {
-                    const float m_new = fmaxf(m_run, mxs);
-                    alpha = ex2_approx(m_run - m_new);
-                    l *= alpha;
-                    m_run = m_new;
-                    rescale = true;
-                }
-                // P = 2^(s * scale * log2(e) - m), two columns per packed op.
-                const uint64_t scale2 = f2_pack(sl2, sl2);
-                const uint64_t negm2 = f2_pack(-m_run, -m_run);
-                uint64_t rsum0 = 0, rsum1 = 0;
+                if (j == 0) m_run = tile_row_max(s) * sl2;
                 uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const uint64_t x = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), scale2, negm2);
-                    const float p0 = ex2_approx(f2_lo(x));
-                    const float p1 = ex2_approx(f2_hi(x));
-                    const uint64_t pp = f2_pack(p0, p1);
-                    if (c & 1) rsum1 = f2_add(rsum1, pp); else rsum0 = f2_add(rsum0, pp);
-                    pk[c] = pack_bf16x2(p0, p1);
-                }
-                const uint64_t rsum = f2_add(rsum0, rsum1);
+                float tsum = tile_exp2(s, sl2, m_run, pk);
+                // P goes to TMEM at once; the sum check overlaps the store,
+                // and a rescale (rare) stores the recomputed P over it.
                 tmem_st32(tS, &pk[0]);
+                if (j > 0 && __any_sync(0xffffffffu, !(tsum <= 256.0f))) {
+                    const float mxs = tile_row_max(s) * sl2;
+                    if (__any_sync(0xffffffffu, mxs > m_run + 8.0f)) {
+                        const float m_new = fmaxf(m_run, mxs);
+                        alpha = ex2_approx(m_run - m_new);
+                        l *= alpha;
+                        m_run = m_new;
+                        rescale = true;
+                        tsum = tile_exp2(s, sl2, m_run, pk);
+                        tmem_wait_st();
+                        tmem_st32(tS, &pk[0]);
+                    }
+                }
                 if (rescale) {
                     // O_b row *= alpha, once PV_b(j-1) has completed (S_b(j)
                     // completing already implies PV_b(j-2) has).
@@ -523,7 +546,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     }
                 }
                 tmem_wait_st();
-                l += f2_lo(rsum) + f2_hi(rsum);
+                l += tsum;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[BAR_P_FULL + 2 * br + buf]);
