@@ -187,12 +187,14 @@ struct ItemRing {
 __device__ __forceinline__ float tile_row_max(const float (&s)[64]) {
     float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-    for (int c = 4; c < 64; c += 8) {
+    for (int c = 4; c < 60; c += 8) {
         mx0 = fmax3(mx0, s[c], s[c + 1]);
         mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
         mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
         mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
     }
+    mx0 = fmax3(mx0, s[60], s[61]);
+    mx1 = fmax3(mx1, s[62], s[63]);
     return fmax3(mx0, mx1, fmaxf(mx2, mx3));
 }
 
