@@ -40,6 +40,7 @@ EXPORTED = (
     "diffattn_workspace_bytes",
     "diffattn_select_kernel",
     "diffattn_get_device_error",
+    "diffattn_selftest_timeout",
     "diffattn_strerror",
     "diffattn_version",
 )
@@ -139,6 +140,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_select_kernel.restype = ctypes.c_int
     lib.diffattn_get_device_error.argtypes = [vp]
     lib.diffattn_get_device_error.restype = ctypes.c_int
+    lib.diffattn_selftest_timeout.argtypes = [vp]
+    lib.diffattn_selftest_timeout.restype = ctypes.c_int
     lib.diffattn_strerror.argtypes = [ctypes.c_int]
     lib.diffattn_strerror.restype = ctypes.c_char_p
     lib.diffattn_version.argtypes = []

@@ -837,6 +837,15 @@ int diffattn_fwd_host(const diffattn_desc* desc, const void* q1_host, const void
                                                                            : DIFFATTN_ERR_CUDA;
 }
 
+int diffattn_selftest_timeout(diffattn_stream_t stream) {
+    DeviceState* dev = nullptr;
+    const int rc = device_state(&dev);
+    if (rc != DIFFATTN_OK) return rc;
+    return launch_selftest_timeout(dev->status, reinterpret_cast<cudaStream_t>(stream)) == 0
+               ? DIFFATTN_OK
+               : DIFFATTN_ERR_CUDA;
+}
+
 int diffattn_get_device_error(diffattn_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return DIFFATTN_ERR_CUDA;

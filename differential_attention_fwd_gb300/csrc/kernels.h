@@ -180,4 +180,9 @@ int launch_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, cons
                       int64_t n, const float* dlambda, float* dlq1, float* dlk1, float* dlq2,
                       float* dlk2, cudaStream_t stream);
 
+// One-thread kernel whose bounded wait on a barrier nothing completes runs
+// out and records the timeout in `status` (the failure path, tested without a
+// fault).
+int launch_selftest_timeout(uint32_t* status, cudaStream_t stream);
+
 }  // namespace diffattn

@@ -440,6 +440,19 @@ int diffattn_select_kernel(const diffattn_desc *desc, const void *q1,
  */
 int diffattn_get_device_error(diffattn_stream_t stream);
 
+/*
+ * diffattn_selftest_timeout -- test hook for the failure path above; the
+ * pages have no counterpart.  Enqueues on `stream` a one-thread kernel that
+ * waits, with the same bounded wait the library's kernels use, on a barrier
+ * that nothing ever completes.  The wait gives up after its time limit (about
+ * two seconds), records DIFFATTN_ERR_TIMEOUT in the device status word and the
+ * kernel returns normally; a following diffattn_get_device_error reports the
+ * timeout and clears it, and the CUDA context stays usable.  Returns
+ * DIFFATTN_OK once enqueued, DIFFATTN_ERR_CUDA if the launch fails.  Touches
+ * no caller memory.
+ */
+int diffattn_selftest_timeout(diffattn_stream_t stream);
+
 /* Human-readable text for a return code (static storage, never NULL). */
 const char *diffattn_strerror(int code);
 
