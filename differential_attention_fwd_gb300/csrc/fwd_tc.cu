@@ -467,10 +467,12 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
         uint32_t pv_count = 0;     // PV_b products issued for earlier items
         bool ok = true;
 
-        for (int k = 0; ok; ++k) {
-            int idx = -1;
-            if (!(ok = ring.get(k, idx)) || idx < 0) break;
-            const Item it = decode_item(idx, p);
+        int idx = -1;
+        Item next{};
+        ok = ring.get(0, idx);
+        if (ok && idx >= 0) next = decode_item(idx, p);
+        for (int k = 0; ok && idx >= 0; ++k) {
+            const Item it = next;
             const int q = it.qt * BM + row;
             float m_run = -INFINITY;
             float l = 0.f;
@@ -555,6 +557,10 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             }
             if (!ok) break;
             pv_count += it.n_kv;
+            // The next item is fetched and decoded here, while the item's last
+            // PV products complete, rather than after the epilogue.
+            if (!(ok = ring.get(k + 1, idx))) break;
+            if (idx >= 0) next = decode_item(idx, p);
 
             // ---------------------------------------------------- epilogue
             if (!(ok = mbar_wait_warp(&bars[BAR_O_FULL], ofph, ab))) break;
