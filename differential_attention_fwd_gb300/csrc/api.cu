@@ -198,8 +198,14 @@ int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
     // Split every unit's keys into ~4096 work items for the whole call, with
     // at least 256 keys (one chunk) per split: the persistent grid of the
     // first pass then ends at most one short item apart across its CTAs.
+    // Shapes the tensor-core first pass takes (four or eight rows, bf16,
+    // D = 64) get ~1024 longer items: its per-item work (query rows, the first
+    // tile's row maxima, reading O out of TMEM) then weighs less (grouped
+    // 32/8 heads over 8192 keys: 0.38 -> 0.53 of the copy bandwidth; 512 or
+    // 768 items balance worse over the SMs).
     const int64_t chunks = (d->Tk + 255) / 256;
-    int64_t splits = (4096 + units - 1) / units;
+    const int64_t target = (tqb >= 4 && d->dtype == DIFFATTN_BF16 && d->D == 64) ? 1024 : 4096;
+    int64_t splits = (target + units - 1) / units;
     if (splits > chunks) splits = chunks;
     if (splits < 1) splits = 1;
     const int64_t split_len = ((chunks + splits - 1) / splits) * 256;
@@ -675,6 +681,8 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
     p.Hk = plan.Hk;
     p.row_chunks = plan.row_chunks;
     p.dense_kv = (d.k1_stride[2] == d.D && d.k2_stride[2] == d.D && d.v_stride[2] == 2 * d.D) ? 1 : 0;
+    p.tc_ok = (p.dense_kv && d.dtype == DIFFATTN_BF16 && d.D == 64 && kv_aligned(q1, d.q1_stride, esize) &&
+               kv_aligned(q2, d.q2_stride, esize)) ? 1 : 0;
     p.tq_bucket = plan.tq_bucket;
     p.splits = plan.splits;
     p.total_items = (int)((int64_t)plan.Hk * d.B * plan.row_chunks * plan.splits);
@@ -695,6 +703,12 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
     copy3(p.s_v, d.v_stride);
     copy3(p.s_o, d.o_stride);
     p.work = static_cast<float*>(workspace);
+    if (p.tc_ok) {
+        DeviceState* dev = nullptr;
+        rc = device_state(&dev);
+        if (rc != DIFFATTN_OK) return rc;
+        p.status = dev->status;
+    }
     p.norm = e.norm;
     p.norm_eps = e.eps;
     p.norm_weight = e.weight;

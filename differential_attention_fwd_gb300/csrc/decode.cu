@@ -694,6 +694,14 @@ int launch_tq(const DecodeParams& p, cudaStream_t stream) {
             return cudaGetLastError() == cudaSuccess ? 0 : -1;
         }
     }
+    // four or eight query rows per CTA: the tensor-core first pass
+    if constexpr (sizeof(T) == 2 && D == 64 && TQ >= 4) {
+        if (p.tc_ok) {
+            if (launch_decode_tc_first_pass(p, stream) != 0) return -1;
+            decode_combine_kernel<T, D, TQ><<<p.B * p.H * p.Tq, DV, 0, stream>>>(p);
+            return cudaGetLastError() == cudaSuccess ? 0 : -1;
+        }
+    }
     decode_partial_kernel<T, D, TQ><<<grid, CHUNK, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return -1;
     decode_combine_kernel<T, D, TQ><<<p.B * p.H * p.Tq, DV, 0, stream>>>(p);

@@ -1,0 +1,431 @@
+// decode_tc.cu -- the first pass of the decode (a few queries over a long
+// key/value cache) on the tensor cores, for query rows that share a key/value
+// head: bf16, D = 64, dense cache rows, 4 to 8 rows per work item (the query
+// heads of a grouped key/value head, DIFF V2's layout, or several new
+// queries).  It computes the same split partials as the CUDA-core first pass
+// in decode.cu, which the combine pass there merges.
+//
+// Per work item (b, key/value head, row chunk, key split), per tile of 128
+// keys: the whole CTA stages K1, K2 and V with cp.async into shared memory in
+// the 128-byte swizzled layout of the MMA operands, two tiles ahead.  Then
+//   S_b^T = K_b Q_b^T        (tcgen05, M = 128 keys in TMEM lanes, N = 16 rows,
+//                             the rows past the item's TQ are zero)
+// each thread (one key) takes its scores for every row, P = 2^(S * scale - m)
+// against the running row max m, and writes P^T as bf16 to shared memory;
+//   O_b^T += V^T P_b^T       (tcgen05, A = V^T read MN-major from the staged V
+//                             tile, M = 128 output columns, N = 16 rows).
+// Row maxima are formed only when some probability would exceed 2^8 (always
+// on an item's first tile), and then O and the row sums are rescaled: the
+// lazy rescale of the tensor-core forward.  Each thread keeps per-row partial
+// sums; they are reduced at the item's end, when O^T is read out of TMEM (one
+// output column per thread) into the split's partial result.
+#include "kernels.h"
+#include "ptx.cuh"
+
+#include <cmath>
+
+namespace diffattn {
+namespace dtc {
+
+constexpr int KT = 128;                 // keys per tile = threads = TMEM lanes
+constexpr int THREADS = KT;
+constexpr int HDIM = 64;
+constexpr int DV = 2 * HDIM;
+constexpr int NR = 16;                  // MMA N: query rows per item, padded
+constexpr int KROW = HDIM * 2;          // bytes of one bf16 key row (128)
+constexpr int K_BYTES = KT * KROW;      // 16 KB per branch
+constexpr int V_HALF = KT * 128;        // 16 KB: 64 value columns of 128 keys
+constexpr int STAGE = 2 * K_BYTES + 2 * V_HALF;   // 64 KB
+constexpr int NST = 3;                  // stages: two tiles in flight ahead
+constexpr int P_SUB = NR * 128;         // 2 KB: 16 rows x 64 keys of P^T
+constexpr int P_BUF = 2 * 2 * P_SUB;    // both branches, two 64-key halves
+constexpr int Q_BYTES = NR * KROW;      // 2 KB per branch
+
+// Shared memory (offsets from a 1024-byte aligned base).
+constexpr int OFF_P = NST * STAGE;                 // stages at 0                 // [2 buffers][branch][half]
+constexpr int OFF_Q = OFF_P + 2 * P_BUF;           // [branch]
+constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;       // float [4 warps][2][NR]
+constexpr int OFF_BAR = OFF_RED + 4 * 2 * NR * 4;  // S_FULL, PV_DONE[2], FINAL
+constexpr int OFF_MISC = OFF_BAR + 4 * 8;          // tmem ptr, abort flag, rescale flag
+constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+constexpr uint32_t TMEM_COLS = 128;
+constexpr uint32_t TM_S = 0;            // S1^T at 0, S2^T at 16
+constexpr uint32_t TM_O = 32;           // O1^T at 32, O2^T at 48
+constexpr uint32_t IDESC_S = idesc_bf16_f32(KT, NR, 0, 0);   // K (K-major) x Q^T (K-major)
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(DV, NR, 1, 0);  // V^T (MN-major) x P^T (K-major)
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// 16 consecutive 32-bit TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void ld16(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// Offset of the 16-byte chunk c of row r in a 128-byte swizzled row layout
+// (8-row atoms of 1024 bytes): chunk c sits at c ^ (r % 8).
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// The CTA's sequence of tiles: item `item` (units * splits of them), tile c.
+struct Cursor {
+    int item = 0, c = 0, n = 0, k_begin = 0, k_end = 0;
+    __device__ void set(const DecodeParams& p, int it) {
+        item = it;
+        c = 0;
+        if (it < p.total_items) {
+            const int split = it % p.splits;
+            k_begin = split * p.split_len;
+            k_end = min(p.Tk, k_begin + p.split_len);
+            n = (k_end - k_begin + KT - 1) / KT;
+        } else {
+            n = 0;
+        }
+    }
+    __device__ bool done(const DecodeParams& p) const { return item >= p.total_items; }
+    __device__ void next(const DecodeParams& p) {
+        if (++c >= n) set(p, item + gridDim.x);
+    }
+};
+
+// Stage tile `cur` with every thread's share of 16-byte copies: K1 and K2
+// rows (128 bytes) swizzled as K-major operands, V rows split into two
+// 64-column halves swizzled as MN-major operands; keys past the split are
+// zero-filled.
+__device__ __forceinline__ void stage_tile(const DecodeParams& p, const Cursor& cur, uint32_t base) {
+    const int unit = cur.item / p.splits;
+    const int bhk = unit / p.row_chunks;
+    const int b = bhk / p.Hk, hk = bhk - b * p.Hk;
+    const int key0 = cur.k_begin + cur.c * KT;
+    const char* k1 = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(p.k1) +
+                                                   b * p.s_k1[0] + hk * p.s_k1[1]);
+    const char* k2 = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(p.k2) +
+                                                   b * p.s_k2[0] + hk * p.s_k2[1]);
+    const char* vv = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(p.v) +
+                                                   b * p.s_v[0] + hk * p.s_v[1]);
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < KT * 8 / THREADS; ++i) {          // K: 8 chunks per row
+        const int id = tid + i * THREADS;
+        const int r = id >> 3, c = id & 7;
+        const int key = key0 + r;
+        const bool ok = key < cur.k_end;
+        const int64_t off = (int64_t)(ok ? key : 0) * KROW + c * 16;
+        cp_async16(base + sw128(r, c), k1 + off, ok);
+        cp_async16(base + K_BYTES + sw128(r, c), k2 + off, ok);
+    }
+#pragma unroll
+    for (int i = 0; i < KT * 16 / THREADS; ++i) {         // V: 16 chunks per row
+        const int id = tid + i * THREADS;
+        const int r = id >> 4, c = id & 15;
+        const int key = key0 + r;
+        const bool ok = key < cur.k_end;
+        cp_async16(base + 2 * K_BYTES + (c >> 3) * V_HALF + sw128(r, c & 7),
+                   vv + (int64_t)(ok ? key : 0) * (2 * KROW) + c * 16, ok);
+    }
+}
+
+template <int TQ>
+__global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const DecodeParams p) {
+    static_assert(TQ >= 1 && TQ <= NR, "rows per item");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // S_FULL, PV_DONE[2], FINAL
+    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 4);
+    float* red = reinterpret_cast<float*>(smem + OFF_RED);          // [4 warps][2][NR]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const AbortState ab{abort_flag, p.status};
+
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // P^T and Q rows past the item's TQ stay zero for the whole kernel
+    for (int i = tid; i < (2 * P_BUF + 2 * Q_BYTES) / 16; i += THREADS)
+        reinterpret_cast<uint4*>(smem + OFF_P)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 0) {
+        tmem_alloc(tmem_ptr, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_ptr;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+
+    Cursor icur, ccur;                      // issue and compute positions
+    icur.set(p, blockIdx.x);
+    ccur = icur;
+#pragma unroll
+    for (int s0 = 0; s0 < NST - 1; ++s0) {
+        if (!icur.done(p)) {
+            stage_tile(p, icur, sbase + s0 * STAGE);
+            icur.next(p);
+        }
+        cp_async_commit();
+    }
+
+    float m[2][TQ], l[2][TQ];               // running row max (log2 units), this thread's row sums
+    int last_key[TQ];
+    uint32_t sph = 0;                       // S_FULL phase
+    uint32_t g = 0;                         // tiles computed so far (all items): P buffer g & 1
+    int st = 0;                             // stage of the tile being computed
+    bool ok = true;
+    while (!ccur.done(p)) {
+        cp_async_wait<NST - 2>();           // this thread's copies of the tile have landed
+        fence_proxy_async_smem();
+        const int unit = ccur.item / p.splits;
+        const int split = ccur.item - unit * p.splits;
+        if (ccur.c == 0) {
+            // a new item: its query rows (swizzled K-major rows), row state
+            const int rc = unit % p.row_chunks;
+            const int bhk = unit / p.row_chunks;
+            const int b = bhk / p.Hk, hk = bhk - b * p.Hk;
+            const int n_rows = p.kv_group * p.Tq;
+            if (tid < 16 * TQ) {
+                const int r = tid >> 4, br = (tid >> 3) & 1, c = tid & 7;
+                const int row = rc * TQ + r;
+                uint4 x = make_uint4(0, 0, 0, 0);
+                if (row < n_rows) {
+                    const int h = hk * p.kv_group + row / p.Tq;
+                    const int q = row % p.Tq;
+                    const __nv_bfloat16* src = br
+                        ? static_cast<const __nv_bfloat16*>(p.q2) + b * p.s_q2[0] + h * p.s_q2[1] + (int64_t)q * p.s_q2[2]
+                        : static_cast<const __nv_bfloat16*>(p.q1) + b * p.s_q1[0] + h * p.s_q1[1] + (int64_t)q * p.s_q1[2];
+                    x = *reinterpret_cast<const uint4*>(src + c * 8);
+                }
+                *reinterpret_cast<uint4*>(smem + OFF_Q + br * Q_BYTES + sw128(r, c)) = x;
+            }
+            fence_proxy_async_smem();
+#pragma unroll
+            for (int r = 0; r < TQ; ++r) {
+                m[0][r] = m[1][r] = -INFINITY;
+                l[0][r] = l[1][r] = 0.f;
+                last_key[r] = p.causal ? p.Tk - p.Tq + (rc * TQ + r) % p.Tq : p.Tk;
+            }
+        }
+        if (!__syncthreads_and(ok)) { ok = false; break; }   // the tile and the query rows are in shared memory
+        if (tid == 0) {
+            // S_b^T = K_b Q_b^T for both branches
+            tc_fence_after();
+#pragma unroll
+            for (int br = 0; br < 2; ++br) {
+                const uint64_t ka = sdesc_sw128(sbase + st * STAGE + br * K_BYTES, 16, 1024);
+                const uint64_t qb = sdesc_sw128(sbase + OFF_Q + br * Q_BYTES, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < HDIM / 16; ++kk)
+                    mma_ss(tmem + TM_S + br * NR, ka + 2 * kk, qb + 2 * kk, IDESC_S, kk > 0);
+            }
+            mma_commit(&bars[0]);
+        }
+        ok = mbar_wait_warp(&bars[0], sph, ab);
+        sph ^= 1;
+        tc_fence_after();
+        uint32_t u[2][NR];
+        ld16(lane_base + TM_S, u[0]);
+        ld16(lane_base + TM_S + NR, u[1]);
+        tmem_wait_ld();
+        const int key = ccur.k_begin + ccur.c * KT + tid;
+        float s[2][TQ], pr[2][TQ];
+        bool big = false;
+#pragma unroll
+        for (int r = 0; r < TQ; ++r) {
+            const bool vis = key < ccur.k_end && key <= last_key[r];
+#pragma unroll
+            for (int br = 0; br < 2; ++br) {
+                s[br][r] = vis ? __uint_as_float(u[br][r]) * sl2 : -INFINITY;
+                pr[br][r] = vis ? ex2_approx(s[br][r] - m[br][r]) : 0.f;
+                big |= !(pr[br][r] <= 256.0f);
+            }
+        }
+        // S^T is in registers (the next score product may overwrite it);
+        // block-wide: abort (bit 1) or a row whose probabilities exceed 2^8 (bit 0)
+        tc_fence_before();
+        const int vote = __syncthreads_or((ok ? 0 : 2) | (big ? 1 : 0));
+        if (vote & 2) { ok = false; break; }
+        if (vote & 1) {
+            // exact tile row maxima (warp, then the four warps), new running
+            // maxima, and the rescale of this thread's sums and of O^T
+#pragma unroll
+            for (int br = 0; br < 2; ++br)
+#pragma unroll
+                for (int r = 0; r < TQ; ++r) {
+                    float v = s[br][r];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                    if (lane == 0) red[(warp * 2 + br) * NR + r] = v;
+                }
+            __syncthreads();
+            float alpha[2][TQ];
+#pragma unroll
+            for (int br = 0; br < 2; ++br)
+#pragma unroll
+                for (int r = 0; r < TQ; ++r) {
+                    const float tmax = fmaxf(fmaxf(red[(0 + br) * NR + r], red[(2 + br) * NR + r]),
+                                             fmaxf(red[(4 + br) * NR + r], red[(6 + br) * NR + r]));
+                    const float mn = fmaxf(m[br][r], tmax);
+                    alpha[br][r] = (mn == -INFINITY) ? 1.f : ex2_approx(m[br][r] - mn);
+                    m[br][r] = mn;
+                    l[br][r] *= alpha[br][r];
+                    pr[br][r] = (s[br][r] == -INFINITY) ? 0.f : ex2_approx(s[br][r] - mn);
+                }
+            if (ccur.c > 0) {
+                // O^T holds this item's earlier tiles: rescale its columns
+                // (one per row) once the previous PV product has completed
+                ok = mbar_wait_warp(&bars[1 + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, ab);
+                tc_fence_after();
+#pragma unroll
+                for (int br = 0; br < 2; ++br) {
+                    uint32_t o[NR];
+                    ld16(lane_base + TM_O + br * NR, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int r = 0; r < TQ; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[br][r]);
+                    tmem_st16(lane_base + TM_O + br * NR, o);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+            }
+            if (!__syncthreads_and(ok)) { ok = false; break; }
+        }
+        // P^T to P buffer g & 1, free once the PV product of tile g - 2 has
+        // read it (the ((g >> 1) - 1)-th completion of that buffer's barrier);
+        // thread tid writes column tid of every row, bf16
+        const uint32_t pb = g & 1u;
+        if (g >= 2) ok = mbar_wait_warp(&bars[1 + pb], ((g >> 1) & 1u) ^ 1u, ab);
+        {
+            const int kc = tid & 63;
+            uint8_t* pbase = smem + OFF_P + pb * P_BUF + (tid >> 6) * P_SUB;
+#pragma unroll
+            for (int br = 0; br < 2; ++br)
+#pragma unroll
+                for (int r = 0; r < TQ; ++r) {
+                    *reinterpret_cast<__nv_bfloat16*>(pbase + br * 2 * P_SUB + sw128(r, kc >> 3) + (kc & 7) * 2) =
+                        __float2bfloat16_rn(pr[br][r]);
+                    l[br][r] += pr[br][r];
+                }
+        }
+        fence_proxy_async_smem();
+        if (!__syncthreads_and(ok)) { ok = false; break; }
+        if (tid == 0) {
+            // O_b^T += V^T P_b^T: A = the staged V tile (MN-major, the two
+            // 64-column halves V_HALF apart), B = P^T in two 64-key halves
+            tc_fence_after();
+            const uint64_t va = sdesc_sw128(sbase + st * STAGE + 2 * K_BYTES, V_HALF, 1024);
+#pragma unroll
+            for (int br = 0; br < 2; ++br) {
+                const uint64_t pd = sdesc_sw128(sbase + OFF_P + pb * P_BUF + br * 2 * P_SUB, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < KT / 16; ++kk)
+                    mma_ss(tmem + TM_O + br * NR, va + 128 * kk, pd + (kk >> 2) * (P_SUB >> 4) + 2 * (kk & 3),
+                           IDESC_PV, (ccur.c > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars[1 + pb]);
+        }
+        if (ccur.c == ccur.n - 1) {
+            // ---- the item's last tile: O^T (column tid) and the row sums
+            // into the split's partial result
+            ok = mbar_wait_warp(&bars[1 + pb], (g >> 1) & 1u, ab);
+            tc_fence_after();
+            uint32_t o[2][NR];
+            ld16(lane_base + TM_O, o[0]);
+            ld16(lane_base + TM_O + NR, o[1]);
+            tmem_wait_ld();
+            tc_fence_before();
+#pragma unroll
+            for (int br = 0; br < 2; ++br)
+#pragma unroll
+                for (int r = 0; r < TQ; ++r) {
+                    float v = l[br][r];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                    if (lane == 0) red[(warp * 2 + br) * NR + r] = v;
+                }
+            if (!__syncthreads_and(ok)) { ok = false; break; }
+            float* part = p.work + ((int64_t)unit * p.splits + split) * TQ * (4 + 2 * DV);
+#pragma unroll
+            for (int r = 0; r < TQ; ++r) {
+                part[r * (4 + 2 * DV) + 4 + tid] = __uint_as_float(o[0][r]);
+                part[r * (4 + 2 * DV) + 4 + DV + tid] = __uint_as_float(o[1][r]);
+            }
+#pragma unroll
+            for (int br = 0; br < 2; ++br)
+#pragma unroll
+                for (int r = 0; r < TQ; ++r)
+                    if (tid == r * 2 + br) {
+                        part[r * (4 + 2 * DV) + 2 * br] = m[br][r];
+                        part[r * (4 + 2 * DV) + 2 * br + 1] =
+                            red[(0 + br) * NR + r] + red[(2 + br) * NR + r] + red[(4 + br) * NR + r] +
+                            red[(6 + br) * NR + r];
+                    }
+        }
+        // ---- prefetch: tile g + NST - 1 into the stage of tile g - 1, once
+        // the PV product of tile g - 1 has read its values
+        if (g >= 1) ok = mbar_wait_warp(&bars[1 + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, ab);
+        const int ist = (st + NST - 1) % NST;
+        if (ok && !icur.done(p)) {
+            stage_tile(p, icur, sbase + ist * STAGE);
+            icur.next(p);
+        }
+        cp_async_commit();
+        ++g;
+        if (++st == NST) st = 0;
+        ccur.next(p);
+        if (!__syncthreads_and(ok)) { ok = false; break; }
+    }
+
+    // Teardown: no copy or MMA of this CTA may still be in flight.
+    cp_async_wait<0>();
+    if (tid == 0) {
+        mma_commit(&bars[3]);
+        mbar_wait_teardown(&bars[3], 0, 200ull * 1000ull * 1000ull);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+template <int TQ>
+int launch_first_pass_tq(const DecodeParams& p, cudaStream_t stream) {
+    if (cudaFuncSetAttribute(decode_tc_kernel<TQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+        return -1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -1;
+    const int grid = p.total_items < sms ? p.total_items : sms;
+    decode_tc_kernel<TQ><<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace dtc
+
+int launch_decode_tc_first_pass(const DecodeParams& p, cudaStream_t stream) {
+    if (p.tq_bucket == 4) return dtc::launch_first_pass_tq<4>(p, stream);
+    if (p.tq_bucket == 8) return dtc::launch_first_pass_tq<8>(p, stream);
+    return -1;
+}
+
+}  // namespace diffattn

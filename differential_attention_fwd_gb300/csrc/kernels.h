@@ -77,6 +77,9 @@ struct DecodeParams {
     int Hk;                 // key/value heads, H / kv_group
     int row_chunks;         // CTAs along the kv_group * Tq query rows of a key/value head
     int dense_kv;           // K1, K2 and V rows contiguous along the sequence (async staging)
+    int tc_ok;              // the tensor-core first pass may run: bf16, D = 64, dense K/V
+                            // rows, Q rows 16-byte aligned
+    uint32_t* status;       // device status word (bounded waits of the tensor-core pass)
     int causal;
     int bf16;               // element type: 1 bf16, 0 fp32
     int tq_bucket;          // query rows per CTA: 1, 2, 4 or 8
@@ -156,6 +159,9 @@ size_t decode_work_floats(int64_t units, int splits, int tq_bucket, int64_t D);
 
 // Each returns 0 on success, -1 if the launch failed.
 int launch_decode(const DecodeParams& p, cudaStream_t stream);
+// The tensor-core first pass of the decode (decode_tc.cu) for 4 or 8 query
+// rows per work item; the caller launches the combine pass after it.
+int launch_decode_tc_first_pass(const DecodeParams& p, cudaStream_t stream);
 int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v,out*/, const TcParams& p, int grid,
                   cudaStream_t stream);
 int launch_bwd_tc(const CUtensorMap* maps /*dq: q1,k1,q2,k2,v,do; dkdv: the same*/,
