@@ -703,11 +703,24 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
     copy3(p.s_v, d.v_stride);
     copy3(p.s_o, d.o_stride);
     p.work = static_cast<float*>(workspace);
+    CUtensorMap kv_maps[3];
     if (p.tc_ok) {
         DeviceState* dev = nullptr;
         rc = device_state(&dev);
         if (rc != DIFFATTN_OK) return rc;
         p.status = dev->status;
+        // the cache as 4-D {inner, Tk, heads, B} maps with 128-key boxes; if
+        // the encoder refuses them, the CUDA-core pass runs instead
+        diffattn_desc md{};
+        md.B = d.B;
+        md.T = d.Tk;
+        const int64_t hk = d.H / group_of(d.kv_group);
+        if (encode_map(&kv_maps[0], k1, 64, &md, hk, d.k1_stride, 64, 128) == DIFFATTN_OK &&
+            encode_map(&kv_maps[1], k2, 64, &md, hk, d.k2_stride, 64, 128) == DIFFATTN_OK &&
+            encode_map(&kv_maps[2], v, 128, &md, hk, d.v_stride, 64, 128) == DIFFATTN_OK)
+            p.tc_maps = kv_maps;
+        else
+            p.tc_ok = 0;
     }
     p.norm = e.norm;
     p.norm_eps = e.eps;

@@ -6,8 +6,9 @@
 // in decode.cu, which the combine pass there merges.
 //
 // Per work item (b, key/value head, row chunk, key split), per tile of 128
-// keys: the whole CTA stages K1, K2 and V with cp.async into shared memory in
-// the 128-byte swizzled layout of the MMA operands, two tiles ahead.  Then
+// keys: TMA brings K1, K2 and V into shared memory in the 128-byte swizzled
+// layout of the MMA operands, two tiles ahead (keys past the split's end are
+// loaded but get zero weight; past the cache's end they read as zero).  Then
 //   S_b^T = K_b Q_b^T        (tcgen05, M = 128 keys in TMEM lanes, N = 16 rows,
 //                             the rows past the item's TQ are zero)
 // each thread (one key) takes its scores for every row, P = 2^(S * scale - m)
@@ -45,8 +46,9 @@ constexpr int Q_BYTES = NR * KROW;      // 2 KB per branch
 constexpr int OFF_P = NST * STAGE;                 // stages at 0                 // [2 buffers][branch][half]
 constexpr int OFF_Q = OFF_P + 2 * P_BUF;           // [branch]
 constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;       // float [4 warps][2][NR]
-constexpr int OFF_BAR = OFF_RED + 4 * 2 * NR * 4;  // S_FULL, PV_DONE[2], FINAL
-constexpr int OFF_MISC = OFF_BAR + 4 * 8;          // tmem ptr, abort flag, rescale flag
+constexpr int OFF_BAR = OFF_RED + 4 * 2 * NR * 4;  // S_FULL, PV_DONE[2], FINAL, FULL[NST]
+constexpr int NUM_BARS = 4 + NST;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem ptr, abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
@@ -55,15 +57,6 @@ constexpr uint32_t TM_S = 0;            // S1^T at 0, S2^T at 16
 constexpr uint32_t TM_O = 32;           // O1^T at 32, O2^T at 48
 constexpr uint32_t IDESC_S = idesc_bf16_f32(KT, NR, 0, 0);   // K (K-major) x Q^T (K-major)
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(DV, NR, 1, 0);  // V^T (MN-major) x P^T (K-major)
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
-                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // 16 consecutive 32-bit TMEM columns of this warp's 32 lanes.
 __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t* r) {
@@ -103,50 +96,32 @@ struct Cursor {
     }
 };
 
-// Stage tile `cur` with every thread's share of 16-byte copies: K1 and K2
-// rows (128 bytes) swizzled as K-major operands, V rows split into two
-// 64-column halves swizzled as MN-major operands; keys past the split are
-// zero-filled.
-__device__ __forceinline__ void stage_tile(const DecodeParams& p, const Cursor& cur, uint32_t base) {
+// Stage tile `cur` into shared memory at `dst` with four TMA box loads
+// (K1, K2 and the two 64-column halves of V, 128 rows each), completion
+// counted on `full`.
+__device__ __forceinline__ void stage_tile(const DecodeParams& p, const Cursor& cur, uint8_t* dst,
+                                           uint64_t* full, const CUtensorMap* k1, const CUtensorMap* k2,
+                                           const CUtensorMap* v) {
     const int unit = cur.item / p.splits;
     const int bhk = unit / p.row_chunks;
     const int b = bhk / p.Hk, hk = bhk - b * p.Hk;
     const int key0 = cur.k_begin + cur.c * KT;
-    const char* k1 = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(p.k1) +
-                                                   b * p.s_k1[0] + hk * p.s_k1[1]);
-    const char* k2 = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(p.k2) +
-                                                   b * p.s_k2[0] + hk * p.s_k2[1]);
-    const char* vv = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(p.v) +
-                                                   b * p.s_v[0] + hk * p.s_v[1]);
-    const int tid = threadIdx.x;
-#pragma unroll
-    for (int i = 0; i < KT * 8 / THREADS; ++i) {          // K: 8 chunks per row
-        const int id = tid + i * THREADS;
-        const int r = id >> 3, c = id & 7;
-        const int key = key0 + r;
-        const bool ok = key < cur.k_end;
-        const int64_t off = (int64_t)(ok ? key : 0) * KROW + c * 16;
-        cp_async16(base + sw128(r, c), k1 + off, ok);
-        cp_async16(base + K_BYTES + sw128(r, c), k2 + off, ok);
-    }
-#pragma unroll
-    for (int i = 0; i < KT * 16 / THREADS; ++i) {         // V: 16 chunks per row
-        const int id = tid + i * THREADS;
-        const int r = id >> 4, c = id & 15;
-        const int key = key0 + r;
-        const bool ok = key < cur.k_end;
-        cp_async16(base + 2 * K_BYTES + (c >> 3) * V_HALF + sw128(r, c & 7),
-                   vv + (int64_t)(ok ? key : 0) * (2 * KROW) + c * 16, ok);
-    }
+    mbar_arrive_expect_tx(full, STAGE);
+    tma_load_4d(dst, k1, full, 0, key0, hk, b);
+    tma_load_4d(dst + K_BYTES, k2, full, 0, key0, hk, b);
+    tma_load_4d(dst + 2 * K_BYTES, v, full, 0, key0, hk, b);
+    tma_load_4d(dst + 2 * K_BYTES + V_HALF, v, full, 64, key0, hk, b);
 }
 
 template <int TQ>
-__global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(THREADS, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
+                 const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
     static_assert(TQ >= 1 && TQ <= NR, "rows per item");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // S_FULL, PV_DONE[2], FINAL
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // S_FULL, PV_DONE[2], FINAL, FULL[NST]
     uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 4);
     float* red = reinterpret_cast<float*>(smem + OFF_RED);          // [4 warps][2][NR]
@@ -154,7 +129,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const DecodeParam
     const AbortState ab{abort_flag, p.status};
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NUM_BARS; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -173,16 +148,19 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const DecodeParam
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.scale_log2;
 
-    Cursor icur, ccur;                      // issue and compute positions
+    Cursor icur, ccur;                      // issue (thread 0) and compute positions
     icur.set(p, blockIdx.x);
     ccur = icur;
-#pragma unroll
-    for (int s0 = 0; s0 < NST - 1; ++s0) {
-        if (!icur.done(p)) {
-            stage_tile(p, icur, sbase + s0 * STAGE);
+    uint32_t issued = 0;                    // tiles staged so far (thread 0)
+    if (tid == 0) {
+        tma_prefetch_desc(&tm_k1);
+        tma_prefetch_desc(&tm_k2);
+        tma_prefetch_desc(&tm_v);
+        for (int s0 = 0; s0 < NST - 1 && !icur.done(p); ++s0) {
+            stage_tile(p, icur, smem + s0 * STAGE, &bars[4 + s0], &tm_k1, &tm_k2, &tm_v);
             icur.next(p);
+            ++issued;
         }
-        cp_async_commit();
     }
 
     float m[2][TQ], l[2][TQ];               // running row max (log2 units), this thread's row sums
@@ -192,8 +170,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const DecodeParam
     int st = 0;                             // stage of the tile being computed
     bool ok = true;
     while (!ccur.done(p)) {
-        cp_async_wait<NST - 2>();           // this thread's copies of the tile have landed
-        fence_proxy_async_smem();
         const int unit = ccur.item / p.splits;
         const int split = ccur.item - unit * p.splits;
         if (ccur.c == 0) {
@@ -224,9 +200,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const DecodeParam
                 last_key[r] = p.causal ? p.Tk - p.Tq + (rc * TQ + r) % p.Tq : p.Tk;
             }
         }
-        if (!__syncthreads_and(ok)) { ok = false; break; }   // the tile and the query rows are in shared memory
+        if (!__syncthreads_and(ok)) { ok = false; break; }   // the query rows are in shared memory
         if (tid == 0) {
-            // S_b^T = K_b Q_b^T for both branches
+            // S_b^T = K_b Q_b^T for both branches, once the tile has landed
+            ok = mbar_wait(&bars[4 + st], (g / NST) & 1u, ab);
             tc_fence_after();
 #pragma unroll
             for (int br = 0; br < 2; ++br) {
@@ -236,9 +213,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const DecodeParam
                 for (int kk = 0; kk < HDIM / 16; ++kk)
                     mma_ss(tmem + TM_S + br * NR, ka + 2 * kk, qb + 2 * kk, IDESC_S, kk > 0);
             }
-            mma_commit(&bars[0]);
+            if (ok) mma_commit(&bars[0]);
         }
-        ok = mbar_wait_warp(&bars[0], sph, ab);
+        ok = __syncthreads_and(ok) && mbar_wait_warp(&bars[0], sph, ab);
         sph ^= 1;
         tc_fence_after();
         uint32_t u[2][NR];
@@ -379,15 +356,17 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const DecodeParam
                             red[(6 + br) * NR + r];
                     }
         }
-        // ---- prefetch: tile g + NST - 1 into the stage of tile g - 1, once
-        // the PV product of tile g - 1 has read its values
-        if (g >= 1) ok = mbar_wait_warp(&bars[1 + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, ab);
-        const int ist = (st + NST - 1) % NST;
-        if (ok && !icur.done(p)) {
-            stage_tile(p, icur, sbase + ist * STAGE);
-            icur.next(p);
+        // ---- prefetch (thread 0): tile g + NST - 1 into the stage of tile
+        // g - 1, once the PV product of tile g - 1 has read its values
+        if (tid == 0 && !icur.done(p)) {
+            if (g >= 1) ok = mbar_wait(&bars[1 + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, ab);
+            const int ist = (st + NST - 1) % NST;
+            if (ok) {
+                stage_tile(p, icur, smem + ist * STAGE, &bars[4 + ist], &tm_k1, &tm_k2, &tm_v);
+                icur.next(p);
+                ++issued;
+            }
         }
-        cp_async_commit();
         ++g;
         if (++st == NST) st = 0;
         ccur.next(p);
@@ -395,8 +374,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const DecodeParam
     }
 
     // Teardown: no copy or MMA of this CTA may still be in flight.
-    cp_async_wait<0>();
     if (tid == 0) {
+        for (uint32_t t = g; t < issued; ++t)       // loads staged but not consumed (abort)
+            mbar_wait_teardown(&bars[4 + t % NST], (t / NST) & 1u, 200ull * 1000ull * 1000ull);
         mma_commit(&bars[3]);
         mbar_wait_teardown(&bars[3], 0, 200ull * 1000ull * 1000ull);
     }
@@ -407,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const DecodeParam
 }
 
 template <int TQ>
-int launch_first_pass_tq(const DecodeParams& p, cudaStream_t stream) {
+int launch_first_pass_tq(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream) {
     if (cudaFuncSetAttribute(decode_tc_kernel<TQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES) != cudaSuccess)
         return -1;
@@ -416,15 +396,16 @@ int launch_first_pass_tq(const DecodeParams& p, cudaStream_t stream) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return -1;
     const int grid = p.total_items < sms ? p.total_items : sms;
-    decode_tc_kernel<TQ><<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+    decode_tc_kernel<TQ><<<grid, THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace dtc
 
 int launch_decode_tc_first_pass(const DecodeParams& p, cudaStream_t stream) {
-    if (p.tq_bucket == 4) return dtc::launch_first_pass_tq<4>(p, stream);
-    if (p.tq_bucket == 8) return dtc::launch_first_pass_tq<8>(p, stream);
+    if (!p.tc_maps) return -1;
+    if (p.tq_bucket == 4) return dtc::launch_first_pass_tq<4>(p, p.tc_maps, stream);
+    if (p.tq_bucket == 8) return dtc::launch_first_pass_tq<8>(p, p.tc_maps, stream);
     return -1;
 }
 

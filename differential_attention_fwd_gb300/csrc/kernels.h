@@ -80,6 +80,8 @@ struct DecodeParams {
     int tc_ok;              // the tensor-core first pass may run: bf16, D = 64, dense K/V
                             // rows, Q rows 16-byte aligned
     uint32_t* status;       // device status word (bounded waits of the tensor-core pass)
+    const CUtensorMap* tc_maps;   // host memory: K1, K2 and V tensor maps (128-row boxes) for
+                                  // the tensor-core pass's launch; never read on the device
     int causal;
     int bf16;               // element type: 1 bf16, 0 fp32
     int tq_bucket;          // query rows per CTA: 1, 2, 4 or 8
