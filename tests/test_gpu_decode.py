@@ -88,3 +88,22 @@ def test_decode_unsupported_and_invalid():
     v = torch.zeros(1, 1, 100, 96, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(da.DiffattnError):        # D not in {32, 64, 128}
         da.differential_attention_decode(x, k, x, k, v, 0.5)
+
+
+@pytest.mark.parametrize("H,Hk,Tq,Tk", [(2, 2, 4, 3000), (8, 2, 1, 2500), (3, 3, 8, 700)])
+def test_decode_four_plus_rows_both_first_passes(H, Hk, Tq, Tk):
+    """Four or more rows per key/value head (bf16, D = 64): a dense cache takes
+    the tensor-core first pass, a token-major view of the same cache (rows not
+    contiguous along the sequence) the CUDA-core pass; both match the oracle."""
+    w = W.DecodeWorkload("t", 2, H, Tq, Tk, 64, "bf16", True, seed=H * 31 + Tq + Tk, kv_heads=Hk)
+    inp = W.draw_kv(w)
+    q1, q2 = to_device(inp.q1, "bf16"), to_device(inp.q2, "bf16")
+    dense = [to_device(x, "bf16") for x in (inp.k1, inp.k2, inp.v)]
+    # [B, Tk, Hk, *] storage seen as [B, Hk, Tk, *]
+    token_major = [t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3) for t in dense]
+    if Hk > 1:
+        assert token_major[0].stride(2) != token_major[0].shape[-1]
+    ref = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.6, True)
+    for kv, tag in ((dense, "dense"), (token_major, "token-major")):
+        out = da.differential_attention_decode(q1, kv[0], q2, kv[1], kv[2], 0.6, causal=True)
+        assert_close(to_numpy(out), ref, "bf16", f"decode {tag} H={H} Hk={Hk} Tq={Tq}")
