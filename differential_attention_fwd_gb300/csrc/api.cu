@@ -98,16 +98,17 @@ int validate(const diffattn_desc* d, const void* q1, const void* k1, const void*
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Heads per scheduling group of the tensor-core forward, for L2 locality: the
-// CTAs working at the same time share the K1, K2 and V of one group (256 bytes
-// per key and key/value head).  Causal items have unequal lengths and run
-// longest first within a group; groups of about 32 MiB of keys and values with
-// at least four items per CTA keep both the L2 hit rate and the balance (at
-// B2 H16 T8192 that is 16 heads and 1024 items, ~2% faster than one group of
-// all heads; at B1 H16 T32768, 4 heads, ~3% faster).  Non-causal items are all
-// equally long; their groups take at most ~24 MiB with an item for every SM.
+// CTAs working at the same time share the K1, K2 and V of one group (512 bytes
+// per key and key/value head in bf16 at D = 64: K1 128, K2 128, V 256).
+// Causal items have unequal lengths and run longest first within a group;
+// groups of about 64 MiB of keys and values with at least four items per CTA
+// keep both the L2 hit rate and the balance (at B2 H16 T8192 that is 16 heads
+// and 1024 items, ~2% faster than one group of all heads; at B1 H16 T32768,
+// 4 heads, ~3% faster).  Non-causal items are all equally long; their groups
+// take at most ~48 MiB with an item for every SM.
 int head_group(const diffattn_desc& d, int nq, int causal, int num_sms) {
-    const int64_t head_bytes = d.T * 256;
-    const int64_t budget = causal ? (32ll << 20) : (24ll << 20);
+    const int64_t head_bytes = d.T * 512;
+    const int64_t budget = causal ? (64ll << 20) : (48ll << 20);
     int64_t g = budget / (head_bytes > 0 ? head_bytes : 1);
     const int64_t min_g = causal ? (4ll * num_sms + nq - 1) / nq : ((int64_t)num_sms + nq - 1) / nq;
     if (g < min_g) g = min_g;

@@ -6,7 +6,7 @@
 // cost to watch).  With the causal mask, query i sits at position
 // Tk - Tq + i and sees keys j <= Tk - Tq + i.
 //
-// The work is bound by reading K1, K2 and V once (256 bytes per key and head
+// The work is bound by reading K1, K2 and V once (512 bytes per key and head
 // for D = 64 in bf16), so it runs on the CUDA cores with coalesced loads and
 // splits the keys of every head across CTAs:
 //   pass 1 (partial): for each work item (b, key/value head, row chunk, split)
