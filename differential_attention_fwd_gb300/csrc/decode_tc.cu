@@ -43,12 +43,13 @@ constexpr int P_BUF = 2 * 2 * P_SUB;    // both branches, two 64-key halves
 constexpr int Q_BYTES = NR * KROW;      // 2 KB per branch
 
 // Shared memory (offsets from a 1024-byte aligned base).
-constexpr int OFF_P = NST * STAGE;                 // stages at 0                 // [2 buffers][branch][half]
+// The NST stages start at offset 0.
+constexpr int OFF_P = NST * STAGE;                 // P^T: [2 buffers][branch][64-key half]
 constexpr int OFF_Q = OFF_P + 2 * P_BUF;           // [branch]
 constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;       // float [4 warps][2][NR]
 constexpr int OFF_BAR = OFF_RED + 4 * 2 * NR * 4;  // S_FULL, PV_DONE[2], FINAL, FULL[NST]
 constexpr int NUM_BARS = 4 + NST;
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem ptr, abort flag
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // TMEM base address, abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
