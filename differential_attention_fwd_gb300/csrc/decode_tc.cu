@@ -13,8 +13,10 @@
 //                             the rows past the item's TQ are zero)
 // each thread (one key) takes its scores for every row, P = 2^(S * scale - m)
 // against the running row max m, and writes P^T as bf16 to shared memory;
-//   O_b^T += V^T P_b^T       (tcgen05, A = V^T read MN-major from the staged V
-//                             tile, M = 128 output columns, N = 16 rows).
+//   [O_1^T O_2^T] += V^T [P_1^T P_2^T]
+//                            (tcgen05, A = V^T read MN-major from the staged V
+//                             tile, M = 128 output columns, N = 32: both
+//                             branches' rows share the value operand).
 // Row maxima are formed only when some probability would exceed 2^8 (always
 // on an item's first tile), and then O and the row sums are rescaled: the
 // lazy rescale of the tensor-core forward.  Each thread keeps per-row partial
@@ -38,8 +40,8 @@ constexpr int K_BYTES = KT * KROW;      // 16 KB per branch
 constexpr int V_HALF = KT * 128;        // 16 KB: 64 value columns of 128 keys
 constexpr int STAGE = 2 * K_BYTES + 2 * V_HALF;   // 64 KB
 constexpr int NST = 3;                  // stages: two tiles in flight ahead
-constexpr int P_SUB = NR * 128;         // 2 KB: 16 rows x 64 keys of P^T
-constexpr int P_BUF = 2 * 2 * P_SUB;    // both branches, two 64-key halves
+constexpr int P_SUB = 2 * NR * 128;     // 4 KB: 32 rows (P_1^T, then P_2^T) x 64 keys
+constexpr int P_BUF = 2 * P_SUB;        // two 64-key halves
 constexpr int Q_BYTES = NR * KROW;      // 2 KB per branch
 
 // Shared memory (offsets from a 1024-byte aligned base).
@@ -57,7 +59,8 @@ constexpr uint32_t TMEM_COLS = 128;
 constexpr uint32_t TM_S = 0;            // S1^T at 0, S2^T at 16
 constexpr uint32_t TM_O = 32;           // O1^T at 32, O2^T at 48
 constexpr uint32_t IDESC_S = idesc_bf16_f32(KT, NR, 0, 0);   // K (K-major) x Q^T (K-major)
-constexpr uint32_t IDESC_PV = idesc_bf16_f32(DV, NR, 1, 0);  // V^T (MN-major) x P^T (K-major)
+// both branches in one product: N = 32 rows of [P_1^T; P_2^T] into O_1^T, O_2^T
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(DV, 2 * NR, 1, 0);  // V^T (MN-major) x P^T (K-major)
 
 // 16 consecutive 32-bit TMEM columns of this warp's 32 lanes.
 __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t* r) {
@@ -293,12 +296,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
         if (g >= 2) ok = mbar_wait_warp(&bars[1 + pb], ((g >> 1) & 1u) ^ 1u, ab);
         {
             const int kc = tid & 63;
-            uint8_t* pbase = smem + OFF_P + pb * P_BUF + (tid >> 6) * P_SUB;
+            uint8_t* pbase = smem + OFF_P + pb * P_BUF + (tid >> 6) * P_SUB;   // this key's half
 #pragma unroll
             for (int br = 0; br < 2; ++br)
 #pragma unroll
                 for (int r = 0; r < TQ; ++r) {
-                    *reinterpret_cast<__nv_bfloat16*>(pbase + br * 2 * P_SUB + sw128(r, kc >> 3) + (kc & 7) * 2) =
+                    *reinterpret_cast<__nv_bfloat16*>(pbase + sw128(br * NR + r, kc >> 3) + (kc & 7) * 2) =
                         __float2bfloat16_rn(pr[br][r]);
                     l[br][r] += pr[br][r];
                 }
@@ -306,18 +309,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
         fence_proxy_async_smem();
         if (!__syncthreads_and(ok)) { ok = false; break; }
         if (tid == 0) {
-            // O_b^T += V^T P_b^T: A = the staged V tile (MN-major, the two
-            // 64-column halves V_HALF apart), B = P^T in two 64-key halves
+            // [O_1^T O_2^T] += V^T [P_1^T P_2^T]: A = the staged V tile
+            // (MN-major, the two 64-column halves V_HALF apart), B = the 32
+            // rows of P^T in two 64-key halves
             tc_fence_after();
             const uint64_t va = sdesc_sw128(sbase + st * STAGE + 2 * K_BYTES, V_HALF, 1024);
+            const uint64_t pd = sdesc_sw128(sbase + OFF_P + pb * P_BUF, 16, 1024);
 #pragma unroll
-            for (int br = 0; br < 2; ++br) {
-                const uint64_t pd = sdesc_sw128(sbase + OFF_P + pb * P_BUF + br * 2 * P_SUB, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < KT / 16; ++kk)
-                    mma_ss(tmem + TM_O + br * NR, va + 128 * kk, pd + (kk >> 2) * (P_SUB >> 4) + 2 * (kk & 3),
-                           IDESC_PV, (ccur.c > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < KT / 16; ++kk)
+                mma_ss(tmem + TM_O, va + 128 * kk, pd + (kk >> 2) * (P_SUB >> 4) + 2 * (kk & 3),
+                       IDESC_PV, (ccur.c > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&bars[1 + pb]);
         }
         if (ccur.c == ccur.n - 1) {
