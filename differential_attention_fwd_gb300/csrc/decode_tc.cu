@@ -22,6 +22,13 @@
 // lazy rescale of the tensor-core forward.  Each thread keeps per-row partial
 // sums; they are reduced at the item's end, when O^T is read out of TMEM (one
 // output column per thread) into the split's partial result.
+//
+// Three single threads issue the asynchronous work, so that no one of them
+// serialises the tile: thread 0 issues the score products (and issues the
+// next tile's right after the current P^T is in shared memory, so they run
+// under the PV products), lane 0 of warp 2 issues the PV products, and lane 0
+// of warp 1 issues the TMA loads.  Each commits to its own barriers; the
+// final barrier counts both MMA issuers' commits.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -133,7 +140,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
     const AbortState ab{abort_flag, p.status};
 
     if (tid == 0) {
-        for (int i = 0; i < NUM_BARS; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NUM_BARS; ++i) mbar_init(&bars[i], i == 3 ? 2 : 1);   // FINAL: both MMA issuers
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -155,8 +162,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
     Cursor icur, ccur;                      // issue (thread 0) and compute positions
     icur.set(p, blockIdx.x);
     ccur = icur;
-    uint32_t issued = 0;                    // tiles staged so far (thread 0)
-    if (tid == 0) {
+    uint32_t issued = 0;                    // tiles staged so far (the producer thread)
+    constexpr int PRODUCER = 32;            // lane 0 of warp 1 issues the TMA loads
+    constexpr int PV_ISSUER = 64;           // lane 0 of warp 2 issues the PV products
+    if (tid == PRODUCER) {
         tma_prefetch_desc(&tm_k1);
         tma_prefetch_desc(&tm_k2);
         tma_prefetch_desc(&tm_v);
@@ -170,6 +179,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
     float m[2][TQ], l[2][TQ];               // running row max (log2 units), this thread's row sums
     int last_key[TQ];
     uint32_t sph = 0;                       // S_FULL phase
+    bool s_issued = false;                  // thread 0: the tile's score product is already issued
+    auto issue_scores = [&](uint32_t t, int stage) -> bool {
+        if (!mbar_wait(&bars[4 + stage], (t / NST) & 1u, ab)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int br = 0; br < 2; ++br) {
+            const uint64_t ka = sdesc_sw128(sbase + stage * STAGE + br * K_BYTES, 16, 1024);
+            const uint64_t qb = sdesc_sw128(sbase + OFF_Q + br * Q_BYTES, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < HDIM / 16; ++kk)
+                mma_ss(tmem + TM_S + br * NR, ka + 2 * kk, qb + 2 * kk, IDESC_S, kk > 0);
+        }
+        mma_commit(&bars[0]);
+        return true;
+    };
     uint32_t g = 0;                         // tiles computed so far (all items): P buffer g & 1
     int st = 0;                             // stage of the tile being computed
     bool ok = true;
@@ -205,20 +229,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
             }
         }
         if (!__syncthreads_and(ok)) { ok = false; break; }   // the query rows are in shared memory
-        if (tid == 0) {
-            // S_b^T = K_b Q_b^T for both branches, once the tile has landed
-            ok = mbar_wait(&bars[4 + st], (g / NST) & 1u, ab);
-            tc_fence_after();
-#pragma unroll
-            for (int br = 0; br < 2; ++br) {
-                const uint64_t ka = sdesc_sw128(sbase + st * STAGE + br * K_BYTES, 16, 1024);
-                const uint64_t qb = sdesc_sw128(sbase + OFF_Q + br * Q_BYTES, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < HDIM / 16; ++kk)
-                    mma_ss(tmem + TM_S + br * NR, ka + 2 * kk, qb + 2 * kk, IDESC_S, kk > 0);
-            }
-            if (ok) mma_commit(&bars[0]);
-        }
+        if (tid == 0 && !s_issued) ok = issue_scores(g, st);
+        s_issued = false;
         ok = __syncthreads_and(ok) && mbar_wait_warp(&bars[0], sph, ab);
         sph ^= 1;
         tc_fence_after();
@@ -308,7 +320,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
         }
         fence_proxy_async_smem();
         if (!__syncthreads_and(ok)) { ok = false; break; }
-        if (tid == 0) {
+        if (tid == PV_ISSUER) {
             // [O_1^T O_2^T] += V^T [P_1^T P_2^T]: A = the staged V tile
             // (MN-major, the two 64-column halves V_HALF apart), B = the 32
             // rows of P^T in two 64-key halves
@@ -320,6 +332,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
                 mma_ss(tmem + TM_O, va + 128 * kk, pd + (kk >> 2) * (P_SUB >> 4) + 2 * (kk & 3),
                        IDESC_PV, (ccur.c > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&bars[1 + pb]);
+        }
+        if (tid == 0) {
+            if (ccur.c + 1 < ccur.n) {      // the next tile's scores, same item
+                ok = issue_scores(g + 1, (st + 1) % NST);
+                s_issued = ok;
+            }
         }
         if (ccur.c == ccur.n - 1) {
             // ---- the item's last tile: O^T (column tid) and the row sums
@@ -360,7 +378,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
         }
         // ---- prefetch (thread 0): tile g + NST - 1 into the stage of tile
         // g - 1, once the PV product of tile g - 1 has read its values
-        if (tid == 0 && !icur.done(p)) {
+        if (tid == PRODUCER && !icur.done(p)) {
             if (g >= 1) ok = mbar_wait(&bars[1 + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, ab);
             const int ist = (st + NST - 1) % NST;
             if (ok) {
@@ -376,10 +394,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
     }
 
     // Teardown: no copy or MMA of this CTA may still be in flight.
-    if (tid == 0) {
+    if (tid == PRODUCER) {
         for (uint32_t t = g; t < issued; ++t)       // loads staged but not consumed (abort)
             mbar_wait_teardown(&bars[4 + t % NST], (t / NST) & 1u, 200ull * 1000ull * 1000ull);
-        mma_commit(&bars[3]);
+    }
+    if (tid == 0 || tid == PV_ISSUER) mma_commit(&bars[3]);
+    if (tid == 0) {
         mbar_wait_teardown(&bars[3], 0, 200ull * 1000ull * 1000ull);
     }
     tc_fence_before();
