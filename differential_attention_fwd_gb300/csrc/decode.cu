@@ -29,6 +29,7 @@
 // tq_bucket rows of several heads.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "pdl.cuh"
 
 #include <cmath>
 
@@ -119,6 +120,7 @@ decode_partial_kernel(const DecodeParams p) {
     const int warp = tid >> 5;
     const int lane = tid & 31;
     __shared__ int last_key[TQ];
+    pdl_launch_dependents();
     // Persistent: the grid holds as many CTAs as fit on the GPU at once, and
     // CTA c takes work items c, c + grid, ...; items are (unit, key split)
     // pairs of equal length, so no CTA has more than one item more than another.
@@ -301,12 +303,15 @@ decode_partial_kernel(const DecodeParams p) {
     }   // work items
 }
 
-// One block per (b, h, query), one thread per output column.
+// One block per (b, h, query), one thread per output column.  Launched as a
+// programmatic dependent of the first pass: its blocks may become resident
+// while the first pass runs and start reading as soon as it completes.
 template <typename T, int D, int TQ>
 __global__ void __launch_bounds__(2 * D)
 decode_combine_kernel(const DecodeParams p) {
     constexpr int DV = 2 * D;
     __shared__ float red[DV / 32];
+    pdl_wait();
     const int c = threadIdx.x;
     const int q = blockIdx.x % p.Tq;
     const int bh = blockIdx.x / p.Tq;
@@ -318,19 +323,25 @@ decode_combine_kernel(const DecodeParams p) {
     const int unit = (b * p.Hk + hk) * p.row_chunks + row / TQ;
     const float* part = p.work + (int64_t)unit * p.splits * TQ * (4 + 2 * DV) + (row % TQ) * (4 + 2 * DV);
     const int64_t sstride = (int64_t)TQ * (4 + 2 * DV);
-    float val[2];
-#pragma unroll
-    for (int br = 0; br < 2; ++br) {
-        float M = -INFINITY;
-        for (int s = 0; s < p.splits; ++s) M = fmaxf(M, part[s * sstride + 2 * br]);
-        float L = 0.f, O = 0.f;
-        for (int s = 0; s < p.splits; ++s) {
-            const float w = ex2_masked(part[s * sstride + 2 * br], M);
-            L = fmaf(part[s * sstride + 2 * br + 1], w, L);
-            O = fmaf(part[s * sstride + 4 + br * DV + c], w, O);
-        }
-        val[br] = O / L;
+    // both branches per split, so that each loop's loads are in flight together
+    float M[2] = {-INFINITY, -INFINITY};
+#pragma unroll 8
+    for (int s = 0; s < p.splits; ++s) {
+        M[0] = fmaxf(M[0], part[s * sstride]);
+        M[1] = fmaxf(M[1], part[s * sstride + 2]);
     }
+    float L[2] = {0.f, 0.f}, O[2] = {0.f, 0.f};
+#pragma unroll 8
+    for (int s = 0; s < p.splits; ++s) {
+        const float* ps = part + s * sstride;
+#pragma unroll
+        for (int br = 0; br < 2; ++br) {
+            const float w = ex2_masked(ps[2 * br], M[br]);
+            L[br] = fmaf(ps[2 * br + 1], w, L[br]);
+            O[br] = fmaf(ps[4 + br * DV + c], w, O[br]);
+        }
+    }
+    const float val[2] = {O[0] / L[0], O[1] / L[1]};
     const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
     float r = __fsub_rn(val[0], __fmul_rn(lam, val[1]));
     if (p.norm != kNormNone) {
@@ -448,6 +459,7 @@ __global__ void __launch_bounds__(THREADS, 3) decode_async_kernel(const DecodePa
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kk = tid & (CH - 1);          // this thread's key within the chunk
+    pdl_launch_dependents();
     const int br = tid / CH;                // and its branch
     const __nv_bfloat16* K1 = static_cast<const __nv_bfloat16*>(p.k1);
     const __nv_bfloat16* K2 = static_cast<const __nv_bfloat16*>(p.k2);
@@ -658,6 +670,23 @@ __global__ void __launch_bounds__(THREADS, 3) decode_async_kernel(const DecodePa
 
 }  // namespace as
 
+// The combine pass as a programmatic dependent of the first pass just
+// launched on `stream` (which signals at its start that it may launch).
+template <typename T, int D, int TQ>
+int launch_combine(const DecodeParams& p, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.B * p.H * p.Tq));
+    cfg.blockDim = dim3(2 * D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<T, D, TQ>, p) == cudaSuccess ? 0 : -1;
+}
+
 template <typename T, int D, int TQ>
 int launch_tq(const DecodeParams& p, cudaStream_t stream) {
     constexpr int DV = 2 * D;
@@ -693,22 +722,19 @@ int launch_tq(const DecodeParams& p, cudaStream_t stream) {
             const int g2 = (int)(p.total_items < slots2 ? p.total_items : slots2);
             as::decode_async_kernel<TQ><<<g2, as::THREADS, sm2, stream>>>(p);
             if (cudaGetLastError() != cudaSuccess) return -1;
-            decode_combine_kernel<T, D, TQ><<<p.B * p.H * p.Tq, DV, 0, stream>>>(p);
-            return cudaGetLastError() == cudaSuccess ? 0 : -1;
+            return launch_combine<T, D, TQ>(p, stream);
         }
     }
     // four or eight query rows per CTA: the tensor-core first pass
     if constexpr (sizeof(T) == 2 && D == 64 && TQ >= 4) {
         if (p.tc_ok) {
             if (launch_decode_tc_first_pass(p, stream) != 0) return -1;
-            decode_combine_kernel<T, D, TQ><<<p.B * p.H * p.Tq, DV, 0, stream>>>(p);
-            return cudaGetLastError() == cudaSuccess ? 0 : -1;
+            return launch_combine<T, D, TQ>(p, stream);
         }
     }
     decode_partial_kernel<T, D, TQ><<<grid, CHUNK, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return -1;
-    decode_combine_kernel<T, D, TQ><<<p.B * p.H * p.Tq, DV, 0, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    return launch_combine<T, D, TQ>(p, stream);
 }
 
 template <typename T, int D>

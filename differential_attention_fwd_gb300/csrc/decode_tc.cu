@@ -31,6 +31,7 @@
 // final barrier counts both MMA issuers' commits.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "pdl.cuh"
 
 #include <cmath>
 
@@ -138,6 +139,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
     float* red = reinterpret_cast<float*>(smem + OFF_RED);          // [4 warps][2][NR]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const AbortState ab{abort_flag, p.status};
+    pdl_launch_dependents();                // the combine pass may take its places now
 
     if (tid == 0) {
         for (int i = 0; i < NUM_BARS; ++i) mbar_init(&bars[i], i == 3 ? 2 : 1);   // FINAL: both MMA issuers

@@ -107,3 +107,28 @@ def test_decode_four_plus_rows_both_first_passes(H, Hk, Tq, Tk):
     for kv, tag in ((dense, "dense"), (token_major, "token-major")):
         out = da.differential_attention_decode(q1, kv[0], q2, kv[1], kv[2], 0.6, causal=True)
         assert_close(to_numpy(out), ref, "bf16", f"decode {tag} H={H} Hk={Hk} Tq={Tq}")
+
+
+@pytest.mark.parametrize("H,Hk,Tq,Tk,norm", [(4, 4, 4, 200, "rms"), (8, 2, 2, 5000, "group"),
+                                             (6, 2, 2, 9000, "group"), (3, 3, 5, 1300, None)])
+def test_decode_tensor_core_epilogue(H, Hk, Tq, Tk, norm):
+    """Four or more rows per key/value head (the tensor-core first pass) with
+    the combine's epilogue: a single split (Tk <= 256) and many, chunks with
+    padded rows (3 heads x 2 rows or 5 rows in a chunk of 8), the norm with
+    weight, bias and a device lambda, and two calls in a row on the cached
+    workspace."""
+    w = W.DecodeWorkload("t", 2, H, Tq, Tk, 64, "bf16", True, seed=H * 13 + Tq + Tk, kv_heads=Hk)
+    inp = W.draw_kv(w)
+    rng = np.random.default_rng(H + Tq)
+    wt = (1 + 0.1 * rng.standard_normal((H, 128))).astype(np.float32)
+    bs = (0.05 * rng.standard_normal((H, 128))).astype(np.float32)
+    lam_t = torch.tensor(0.55, device="cuda")
+    kw = dict(out_scale=0.7)
+    if norm:
+        kw.update(norm=norm, norm_weight=torch.from_numpy(wt).cuda(), norm_bias=torch.from_numpy(bs).cuda())
+    o = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.55, True)
+    ref = oracle.head_norm(o, norm or "none", 1e-5, wt if norm else None, bs if norm else None, 0.7)
+    for call in range(2):
+        out, _ = run(inp, "bf16", lam_t, True, **kw)
+        assert_close(to_numpy(out), ref, "bf16", f"decode epilogue H={H} Hk={Hk} Tq={Tq} Tk={Tk} call {call}")
+    assert da.get_device_error() == 0
