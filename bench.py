@@ -8,7 +8,9 @@ Default workload: B=2, H=16, T=8192, D=64, V width 128, bf16, causal.
 
 Prints one JSON line (rank 0).  Timing: W untimed warm-up steps, then K
 timed steps; each step is bracketed by CUDA events on the launch stream, and
-the L2 cache is flushed (a 256 MiB write) between steps outside the events.
+the L2 cache is flushed between steps outside the events (a 256 MiB write,
+then a 256 MiB read so that the write's dirty lines reach DRAM before the
+step rather than during it; --l2-flush write keeps the write alone).
 `value` is the algorithmic TFLOP/s of the whole job (unmasked pairs x 12 D,
 all ranks).  `e2e` repeats the measurement with inputs copied from pinned
 host memory and the output copied back inside the timed region.
@@ -45,6 +47,36 @@ METRIC = "diffattn_fwd TFLOP/s and % of GB300 bf16 tensor peak (B=2,H=16,T=8192,
 UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1000 * 1000
 FLUSH_BYTES = 256 * 1024 * 1024
+
+
+class L2Flush:
+    """The L2 flush between timed steps (outside the events): a write of a
+    buffer larger than L2 evicts the previous step's lines.  With kind
+    "write-read" a read of a second such buffer follows, so that the dirty
+    lines the write left are written back to DRAM before the step, not during
+    it, and the step starts with L2 holding clean lines of neither its inputs
+    nor its outputs."""
+
+    def __init__(self, dev, kind: str):
+        import torch
+        self.kind = kind
+        self.w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if kind == "write-read" else None
+
+    def zero_(self):
+        self.w.zero_()
+        if self.r is not None:
+            self.r.sum()
+
+    def describe(self) -> str:
+        return L2Flush.describe_kind(self.kind)
+
+    @staticmethod
+    def describe_kind(kind: str) -> str:
+        if kind == "write":
+            return "flushed between steps (256 MiB write outside the timed events)"
+        return ("flushed between steps (256 MiB write, then a 256 MiB read that cleans the "
+                "written lines, outside the timed events)")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "diffattn_fwd_tc_b2h16t8192.md")
 KERNEL_SOURCES = ["fwd_tc.cu", "ptx.cuh", "kernels.h", "api.cu"]   # the kernel and its launch plan
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -259,7 +291,7 @@ def run_reference(args, w, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_of(w, lam),
+        "data": "synthetic", "config": config_of(w, lam, args.l2_flush),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"each step: {rows_per_step} query rows of head (0,0) spread over "
                                    f"T={w.T}, float64 NumPy oracle on the host cores"},
@@ -275,13 +307,12 @@ def lambda_for(w, inp) -> float:
                                                        W.lambda_init_for(w))))
 
 
-def config_of(w, lam):
+def config_of(w, lam, l2_flush: str = "write-read"):
     grouped = {"H_kv": w.Hk, "shared_keys": w.shared_keys} if (w.Hk != w.H or w.shared_keys) else {}
     return {"workload": w.name, "B": w.B, "H": w.H, **grouped, "T": w.T, "D": w.D, "Dv": w.Dv,
             "causal": w.causal, "lambda_init": W.lambda_init_for(w) if not w.lambdas else None,
             "lambda": lam, "gflop_per_step": w.flops / 1e9,
-            "l2": "flushed between steps (256 MiB write outside the timed events); "
-                  f"inputs {input_bytes(w) / 2**20:.0f} MiB",
+            "l2": f"{L2Flush.describe_kind(l2_flush)}; inputs {input_bytes(w) / 2**20:.0f} MiB",
             "parallelism": "replicas"}
 
 
@@ -319,7 +350,7 @@ def run_ours(args, w, world, rank, local):
     d_lv = [v.to(dev) for v in lam_vecs_host]
     d_lam = torch.empty((), dtype=torch.float32, device=dev)
     d_out = torch.empty((w.B, w.H, w.T, w.Dv), dtype=tdt, device=dev)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev, args.l2_flush)
     stream = torch.cuda.current_stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
     desc = da.make_desc(*d_in, d_out)
@@ -415,7 +446,7 @@ def run_ours(args, w, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {**config_of(w, float(d_lam.item())),
+        "config": {**config_of(w, float(d_lam.item()), args.l2_flush),
                    **({"epilogue": f"{args.norm} norm + affine + x(1-lambda_init)"} if args.norm != "none" else {})},
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": roofline, "e2e": e2e,
@@ -544,7 +575,7 @@ def run_backward(args, w, world, rank, local):
         host[3], d_in[3] = host[1], d_in[1]
     grads = [torch.empty(t.shape, dtype=tdt, device=dev) for t in d_in[:5]]
     d_lam = torch.empty((), dtype=torch.float32, device=dev)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev, args.l2_flush)
     stream = torch.cuda.current_stream(dev)
     desc = da.make_desc(*d_in[:5], d_in[5])
     need = int(lib.diffattn_bwd_workspace_bytes(ctypes.byref(desc)))
@@ -644,7 +675,7 @@ def run_backward(args, w, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
-        "config": {**config_of(w, lam), "gflop_per_step": flops / 1e9,
+        "config": {**config_of(w, lam, args.l2_flush), "gflop_per_step": flops / 1e9,
                    # dQ kernel 12 D + dK/dV kernel 16 D per pair, plus 12 D when the
                    # forward is recomputed for the row statistics
                    "executed_gflop_per_step": flops * (28 if saved is not None else 40) / 20 / 1e9,
@@ -682,7 +713,7 @@ def run_decode(args, world, rank, local):
     inp = W.draw_kv(w)
     d_in = [torch.from_numpy(x).to(dev, tdt) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
     d_out = torch.empty((w.B, w.H, w.Tq, w.Dv), dtype=tdt, device=dev)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev, args.l2_flush)
     stream = torch.cuda.current_stream(dev)
     desc = da.make_kv_desc(*d_in, d_out)
     need = int(lib.diffattn_decode_workspace_bytes(ctypes.byref(desc)))
@@ -728,7 +759,7 @@ def run_decode(args, world, rank, local):
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hk, "Tq": w.Tq, "Tk": w.Tk, "D": w.D,
                    "causal": w.causal, "lambda": w.lambda_value, "gbytes_per_step": w.bytes / 1e9,
-                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "l2": flush.describe(),
                    "parallelism": "replicas"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                      "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
@@ -749,6 +780,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    ap.add_argument("--l2-flush", choices=["write", "write-read"], default="write-read",
+                    help="the L2 flush between timed steps")
     ap.add_argument("--mode", choices=["forward", "backward", "decode"], default="forward")
     ap.add_argument("--decode-workload", default="decode_b16h16q1k8192", choices=sorted(W.DECODE_WORKLOADS))
     ap.add_argument("--bwd-recompute", action="store_true",
