@@ -196,16 +196,12 @@ int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
     const int64_t Hk = d->H / g;
     const int64_t units = d->B * Hk * row_chunks;
     if (units > (1ll << 24) || d->B * d->H > (1ll << 24)) return DIFFATTN_ERR_UNSUPPORTED;
-    // Split every unit's keys into ~4096 work items for the whole call, with
-    // at least 256 keys (one chunk) per split: the persistent grid of the
-    // first pass then ends at most one short item apart across its CTAs.
-    // Shapes the tensor-core first pass takes (four or eight rows, bf16,
-    // D = 64) get ~1024 longer items: its per-item work (query rows, the first
-    // tile's row maxima, reading O out of TMEM) then weighs less (grouped
-    // 32/8 heads over 8192 keys: 0.38 -> 0.53 of the copy bandwidth; 512 or
-    // 768 items balance worse over the SMs).
+    // The CUDA-core first passes split every unit's keys into ~4096 work
+    // items for the whole call, with at least 256 keys (one chunk) per split:
+    // their persistent grids then end at most one short item apart across
+    // CTAs.  (The tensor-core pass cuts the keys itself, at launch.)
     const int64_t chunks = (d->Tk + 255) / 256;
-    const int64_t target = (tqb >= 4 && d->dtype == DIFFATTN_BF16 && d->D == 64) ? 1024 : 4096;
+    const int64_t target = 4096;
     int64_t splits = (target + units - 1) / units;
     if (splits > chunks) splits = chunks;
     if (splits < 1) splits = 1;
@@ -218,7 +214,14 @@ int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
     plan->kv_group = (int)g;
     plan->Hk = (int)Hk;
     plan->row_chunks = (int)row_chunks;
-    plan->work_bytes = decode_work_floats(units, (int)splits, tqb, d->D) * sizeof(float);
+    size_t floats = decode_work_floats(units, (int)splits, tqb, d->D);
+    if (tqb >= 4 && d->dtype == DIFFATTN_BF16 && d->D == 64) {
+        // the tensor-core pass cuts the keys its own way (contiguous tile
+        // ranges per CTA); room for whichever first pass the call takes
+        const size_t tc = decode_tc_work_floats(units, d->Tk, tqb);
+        if (tc > floats) floats = tc;
+    }
+    plan->work_bytes = floats * sizeof(float);
     return DIFFATTN_OK;
 }
 

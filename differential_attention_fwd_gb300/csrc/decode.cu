@@ -728,8 +728,9 @@ int launch_tq(const DecodeParams& p, cudaStream_t stream) {
     // four or eight query rows per CTA: the tensor-core first pass
     if constexpr (sizeof(T) == 2 && D == 64 && TQ >= 4) {
         if (p.tc_ok) {
-            if (launch_decode_tc_first_pass(p, stream) != 0) return -1;
-            return launch_combine<T, D, TQ>(p, stream);
+            DecodeParams q = p;             // the pass's own split of the keys
+            if (launch_decode_tc_first_pass(&q, stream) != 0) return -1;
+            return launch_combine<T, D, TQ>(q, stream);
         }
     }
     decode_partial_kernel<T, D, TQ><<<grid, CHUNK, smem, stream>>>(p);

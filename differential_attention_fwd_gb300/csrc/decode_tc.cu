@@ -2,13 +2,20 @@
 // key/value cache) on the tensor cores, for query rows that share a key/value
 // head: bf16, D = 64, dense cache rows, 4 to 8 rows per work item (the query
 // heads of a grouped key/value head, DIFF V2's layout, or several new
-// queries).  It computes the same split partials as the CUDA-core first pass
-// in decode.cu, which the combine pass there merges.
+// queries).  It writes split partials in the layout of the CUDA-core first
+// pass in decode.cu, which the combine pass there merges.
 //
-// Per work item (b, key/value head, row chunk, key split), per tile of 128
-// keys: TMA brings K1, K2 and V into shared memory in the 128-byte swizzled
-// layout of the MMA operands, two tiles ahead (keys past the split's end are
-// loaded but get zero weight; past the cache's end they read as zero).  Then
+// Work: a unit is (b, key/value head, row chunk); its keys form tpu tiles of
+// 128.  The units' tiles are laid end to end and every CTA streams one
+// contiguous range of them (equal lengths to within a tile), in segments cut
+// at unit boundaries; each segment leaves one partial result, in the slot
+// given by its CTA's place among the unit's CTAs, and the CTA with a unit's
+// last segment marks the unit's unused slots empty.
+//
+// Per segment, per tile of 128 keys: TMA brings K1, K2 and V into shared
+// memory in the 128-byte swizzled layout of the MMA operands, two tiles ahead
+// (keys past the segment's end are loaded but get zero weight; past the
+// cache's end they read as zero).  Then
 //   S_b^T = K_b Q_b^T        (tcgen05, M = 128 keys in TMEM lanes, N = 16 rows,
 //                             the rows past the item's TQ are zero)
 // each thread (one key) takes its scores for every row, P = 2^(S * scale - m)
@@ -87,24 +94,49 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// The CTA's sequence of tiles: item `item` (units * splits of them), tile c.
+// The CTA's tiles.  The units' key tiles are laid end to end (unit-major,
+// tpu = ceil(Tk / KT) tiles per unit, `total` in all); CTA c takes the
+// contiguous range [bound(c), bound(c + 1)), bound(c) = c * total / grid, so
+// every CTA streams the same number of tiles to within one.  The range is cut
+// into segments at unit boundaries: a segment is one unit's tiles in this
+// range, with its own row state and its own partial result.
+__device__ __forceinline__ int64_t tile_bound(const DecodeParams& p, int c) {
+    return (int64_t)c * p.tc_total / p.tc_grid;
+}
+
+// The first CTA whose range holds tiles of `unit`: the slot of a segment of
+// `unit` is its CTA's index minus this.
+__device__ __forceinline__ int first_cta(const DecodeParams& p, int unit) {
+    const int64_t t0 = (int64_t)unit * p.tc_tpu;
+    int c = (int)(t0 * p.tc_grid / p.tc_total);     // bound(c) <= t0
+    while (c + 1 < p.tc_grid && tile_bound(p, c + 1) <= t0) ++c;
+    return c;
+}
+
 struct Cursor {
-    int item = 0, c = 0, n = 0, k_begin = 0, k_end = 0;
-    __device__ void set(const DecodeParams& p, int it) {
-        item = it;
+    int64_t t = 0, t_end = 0;               // first tile of the segment; end of the CTA's range
+    int unit = 0, c = 0, n = 0, k_begin = 0, k_end = 0;
+    __device__ void start(const DecodeParams& p, int64_t tt) {
+        t = tt;
         c = 0;
-        if (it < p.total_items) {
-            const int split = it % p.splits;
-            k_begin = split * p.split_len;
-            k_end = min(p.Tk, k_begin + p.split_len);
-            n = (k_end - k_begin + KT - 1) / KT;
+        if (t < t_end) {
+            unit = (int)(t / p.tc_tpu);
+            const int tile0 = (int)(t - (int64_t)unit * p.tc_tpu);
+            const int64_t seg_end = min(t_end, (int64_t)(unit + 1) * p.tc_tpu);
+            n = (int)(seg_end - t);
+            k_begin = tile0 * KT;
+            k_end = min(p.Tk, (tile0 + n) * KT);
         } else {
             n = 0;
         }
     }
-    __device__ bool done(const DecodeParams& p) const { return item >= p.total_items; }
+    __device__ bool done() const { return t >= t_end; }
+    // the segment ends where its unit does (it holds the unit's last tiles)
+    __device__ bool unit_last(const DecodeParams& p) const {
+        return t + n == (int64_t)(unit + 1) * p.tc_tpu;
+    }
     __device__ void next(const DecodeParams& p) {
-        if (++c >= n) set(p, item + gridDim.x);
+        if (++c >= n) start(p, t + n);
     }
 };
 
@@ -114,8 +146,7 @@ struct Cursor {
 __device__ __forceinline__ void stage_tile(const DecodeParams& p, const Cursor& cur, uint8_t* dst,
                                            uint64_t* full, const CUtensorMap* k1, const CUtensorMap* k2,
                                            const CUtensorMap* v) {
-    const int unit = cur.item / p.splits;
-    const int bhk = unit / p.row_chunks;
+    const int bhk = cur.unit / p.row_chunks;
     const int b = bhk / p.Hk, hk = bhk - b * p.Hk;
     const int key0 = cur.k_begin + cur.c * KT;
     mbar_arrive_expect_tx(full, STAGE);
@@ -161,8 +192,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.scale_log2;
 
-    Cursor icur, ccur;                      // issue (thread 0) and compute positions
-    icur.set(p, blockIdx.x);
+    Cursor icur, ccur;                      // issue (producer) and compute positions
+    icur.t_end = tile_bound(p, blockIdx.x + 1);
+    icur.start(p, tile_bound(p, blockIdx.x));
     ccur = icur;
     uint32_t issued = 0;                    // tiles staged so far (the producer thread)
     constexpr int PRODUCER = 32;            // lane 0 of warp 1 issues the TMA loads
@@ -171,7 +203,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
         tma_prefetch_desc(&tm_k1);
         tma_prefetch_desc(&tm_k2);
         tma_prefetch_desc(&tm_v);
-        for (int s0 = 0; s0 < NST - 1 && !icur.done(p); ++s0) {
+        for (int s0 = 0; s0 < NST - 1 && !icur.done(); ++s0) {
             stage_tile(p, icur, smem + s0 * STAGE, &bars[4 + s0], &tm_k1, &tm_k2, &tm_v);
             icur.next(p);
             ++issued;
@@ -199,9 +231,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
     uint32_t g = 0;                         // tiles computed so far (all items): P buffer g & 1
     int st = 0;                             // stage of the tile being computed
     bool ok = true;
-    while (!ccur.done(p)) {
-        const int unit = ccur.item / p.splits;
-        const int split = ccur.item - unit * p.splits;
+    while (!ccur.done()) {
+        const int unit = ccur.unit;
         if (ccur.c == 0) {
             // a new item: its query rows (swizzled K-major rows), row state
             const int rc = unit % p.row_chunks;
@@ -361,7 +392,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
                     if (lane == 0) red[(warp * 2 + br) * NR + r] = v;
                 }
             if (!__syncthreads_and(ok)) { ok = false; break; }
-            float* part = p.work + ((int64_t)unit * p.splits + split) * TQ * (4 + 2 * DV);
+            const int slot = (int)blockIdx.x - first_cta(p, unit);
+            float* part = p.work + ((int64_t)unit * p.splits + slot) * TQ * (4 + 2 * DV);
 #pragma unroll
             for (int r = 0; r < TQ; ++r) {
                 part[r * (4 + 2 * DV) + 4 + tid] = __uint_as_float(o[0][r]);
@@ -377,10 +409,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
                             red[(0 + br) * NR + r] + red[(2 + br) * NR + r] + red[(4 + br) * NR + r] +
                             red[(6 + br) * NR + r];
                     }
+            if (ccur.unit_last(p)) {
+                // the unit's slots past its last segment saw no keys:
+                // row max -inf, sum 0, O 0 (they weigh nothing in the merge)
+                float* empty = part + TQ * (4 + 2 * DV);
+                const int nf = (p.splits - 1 - slot) * TQ * (4 + 2 * DV);
+                for (int i = tid; i < nf; i += THREADS) {
+                    const int col = i % (4 + 2 * DV);
+                    empty[i] = (col == 0 || col == 2) ? -INFINITY : 0.f;
+                }
+            }
         }
         // ---- prefetch (thread 0): tile g + NST - 1 into the stage of tile
         // g - 1, once the PV product of tile g - 1 has read its values
-        if (tid == PRODUCER && !icur.done(p)) {
+        if (tid == PRODUCER && !icur.done()) {
             if (g >= 1) ok = mbar_wait(&bars[1 + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, ab);
             const int ist = (st + NST - 1) % NST;
             if (ok) {
@@ -415,21 +457,47 @@ int launch_first_pass_tq(const DecodeParams& p, const CUtensorMap* maps, cudaStr
     if (cudaFuncSetAttribute(decode_tc_kernel<TQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES) != cudaSuccess)
         return -1;
+    decode_tc_kernel<TQ><<<p.tc_grid, THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+// Segments of one unit at most: every CTA range holds at least
+// floor(total / grid) tiles, so tpu consecutive tiles meet at most
+// ceil((tpu - 1) / that) + 1 ranges (and never more than tpu).
+int64_t tc_slots(int64_t total, int64_t tpu, int64_t grid) {
+    const int64_t per = total / grid;
+    const int64_t s = (tpu - 1 + per - 1) / per + 1;
+    return s < tpu ? s : tpu;
+}
+
+constexpr int64_t kMaxGrid = 1024;
+
+}  // namespace dtc
+
+size_t decode_tc_work_floats(int64_t units, int64_t Tk, int tq_bucket) {
+    const int64_t tpu = (Tk + dtc::KT - 1) / dtc::KT;
+    const int64_t total = units * tpu;
+    const int64_t grid = total < dtc::kMaxGrid ? total : dtc::kMaxGrid;
+    return (size_t)(units * dtc::tc_slots(total, tpu, grid) * tq_bucket * (4 + 2 * dtc::DV));
+}
+
+int launch_decode_tc_first_pass(DecodeParams* p, cudaStream_t stream) {
+    if (!p->tc_maps) return -1;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return -1;
-    const int grid = p.total_items < sms ? p.total_items : sms;
-    decode_tc_kernel<TQ><<<grid, THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
-}
-
-}  // namespace dtc
-
-int launch_decode_tc_first_pass(const DecodeParams& p, cudaStream_t stream) {
-    if (!p.tc_maps) return -1;
-    if (p.tq_bucket == 4) return dtc::launch_first_pass_tq<4>(p, p.tc_maps, stream);
-    if (p.tq_bucket == 8) return dtc::launch_first_pass_tq<8>(p, p.tc_maps, stream);
+    const int64_t units = (int64_t)p->B * p->Hk * p->row_chunks;
+    const int64_t tpu = (p->Tk + dtc::KT - 1) / dtc::KT;
+    const int64_t total = units * tpu;
+    int64_t grid = total < sms ? total : sms;
+    if (grid > dtc::kMaxGrid) grid = dtc::kMaxGrid;
+    p->tc_tpu = (int)tpu;
+    p->tc_total = total;
+    p->tc_grid = (int)grid;
+    p->splits = (int)dtc::tc_slots(total, tpu, grid);   // partial slots per unit
+    if (p->tq_bucket == 4) return dtc::launch_first_pass_tq<4>(*p, p->tc_maps, stream);
+    if (p->tq_bucket == 8) return dtc::launch_first_pass_tq<8>(*p, p->tc_maps, stream);
     return -1;
 }
 

@@ -95,6 +95,9 @@ struct DecodeParams {
     void* out;
     int64_t s_q1[3], s_k1[3], s_q2[3], s_k2[3], s_v[3], s_o[3];
     float* work;            // partial results, decode_work_floats(...) floats
+    int tc_tpu;             // tensor-core pass: key tiles per unit,
+    int tc_grid;            //   CTAs (each streams a contiguous range of the
+    int64_t tc_total;       //   units' tiles), tiles of all units
     int norm;
     float norm_eps;
     const float* norm_weight;
@@ -162,8 +165,12 @@ size_t decode_work_floats(int64_t units, int splits, int tq_bucket, int64_t D);
 // Each returns 0 on success, -1 if the launch failed.
 int launch_decode(const DecodeParams& p, cudaStream_t stream);
 // The tensor-core first pass of the decode (decode_tc.cu) for 4 or 8 query
-// rows per work item; the caller launches the combine pass after it.
-int launch_decode_tc_first_pass(const DecodeParams& p, cudaStream_t stream);
+// rows per unit.  It sets p's tc_* fields and p->splits (partial slots per
+// unit) for its launch; the caller launches the combine pass with that p.
+int launch_decode_tc_first_pass(DecodeParams* p, cudaStream_t stream);
+// Workspace floats the tensor-core pass may need (its slots per unit on any
+// GPU of up to 1024 SMs).
+size_t decode_tc_work_floats(int64_t units, int64_t Tk, int tq_bucket);
 int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v,out*/, const TcParams& p, int grid,
                   cudaStream_t stream);
 int launch_bwd_tc(const CUtensorMap* maps /*dq: q1,k1,q2,k2,v,do; dkdv: the same*/,
