@@ -1,6 +1,6 @@
 // decode_tc.cu -- the first pass of the decode (a few queries over a long
 // key/value cache) on the tensor cores, for query rows that share a key/value
-// head: bf16, D = 64, dense cache rows, 4 to 8 rows per work item (the query
+// head: bf16, D = 64, dense cache rows, 4 to 8 rows per unit (the query
 // heads of a grouped key/value head, DIFF V2's layout, or several new
 // queries).  It writes split partials in the layout of the CUDA-core first
 // pass in decode.cu, which the combine pass there merges.
@@ -17,7 +17,7 @@
 // (keys past the segment's end are loaded but get zero weight; past the
 // cache's end they read as zero).  Then
 //   S_b^T = K_b Q_b^T        (tcgen05, M = 128 keys in TMEM lanes, N = 16 rows,
-//                             the rows past the item's TQ are zero)
+//                             the rows past the unit's TQ are zero)
 // each thread (one key) takes its scores for every row, P = 2^(S * scale - m)
 // against the running row max m, and writes P^T as bf16 to shared memory;
 //   [O_1^T O_2^T] += V^T [P_1^T P_2^T]
@@ -25,10 +25,10 @@
 //                             tile, M = 128 output columns, N = 32: both
 //                             branches' rows share the value operand).
 // Row maxima are formed only when some probability would exceed 2^8 (always
-// on an item's first tile), and then O and the row sums are rescaled: the
+// on a segment's first tile), and then O and the row sums are rescaled: the
 // lazy rescale of the tensor-core forward.  Each thread keeps per-row partial
-// sums; they are reduced at the item's end, when O^T is read out of TMEM (one
-// output column per thread) into the split's partial result.
+// sums; they are reduced at the segment's end, when O^T is read out of TMEM (one
+// output column per thread) into the segment's partial result.
 //
 // Three single threads issue the asynchronous work, so that no one of them
 // serialises the tile: thread 0 issues the score products (and issues the
@@ -49,7 +49,7 @@ constexpr int KT = 128;                 // keys per tile = threads = TMEM lanes
 constexpr int THREADS = KT;
 constexpr int HDIM = 64;
 constexpr int DV = 2 * HDIM;
-constexpr int NR = 16;                  // MMA N: query rows per item, padded
+constexpr int NR = 16;                  // MMA N: query rows per unit, padded
 constexpr int KROW = HDIM * 2;          // bytes of one bf16 key row (128)
 constexpr int K_BYTES = KT * KROW;      // 16 KB per branch
 constexpr int V_HALF = KT * 128;        // 16 KB: 64 value columns of 128 keys
@@ -160,7 +160,7 @@ template <int TQ>
 __global__ void __launch_bounds__(THREADS, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
                  const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
-    static_assert(TQ >= 1 && TQ <= NR, "rows per item");
+    static_assert(TQ >= 1 && TQ <= NR, "rows per unit");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
@@ -177,7 +177,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // P^T and Q rows past the item's TQ stay zero for the whole kernel
+    // P^T and Q rows past the unit's TQ stay zero for the whole kernel
     for (int i = tid; i < (2 * P_BUF + 2 * Q_BYTES) / 16; i += THREADS)
         reinterpret_cast<uint4*>(smem + OFF_P)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
@@ -228,13 +228,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
         mma_commit(&bars[0]);
         return true;
     };
-    uint32_t g = 0;                         // tiles computed so far (all items): P buffer g & 1
+    uint32_t g = 0;                         // tiles computed so far (all segments): P buffer g & 1
     int st = 0;                             // stage of the tile being computed
     bool ok = true;
     while (!ccur.done()) {
         const int unit = ccur.unit;
         if (ccur.c == 0) {
-            // a new item: its query rows (swizzled K-major rows), row state
+            // a new segment: its unit's query rows (swizzled K-major rows), row state
             const int rc = unit % p.row_chunks;
             const int bhk = unit / p.row_chunks;
             const int b = bhk / p.Hk, hk = bhk - b * p.Hk;
@@ -316,7 +316,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
                     pr[br][r] = (s[br][r] == -INFINITY) ? 0.f : ex2_approx(s[br][r] - mn);
                 }
             if (ccur.c > 0) {
-                // O^T holds this item's earlier tiles: rescale its columns
+                // O^T holds this segment's earlier tiles: rescale its columns
                 // (one per row) once the previous PV product has completed
                 ok = mbar_wait_warp(&bars[1 + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, ab);
                 tc_fence_after();
@@ -367,14 +367,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
             mma_commit(&bars[1 + pb]);
         }
         if (tid == 0) {
-            if (ccur.c + 1 < ccur.n) {      // the next tile's scores, same item
+            if (ccur.c + 1 < ccur.n) {      // the next tile's scores, same segment
                 ok = issue_scores(g + 1, (st + 1) % NST);
                 s_issued = ok;
             }
         }
         if (ccur.c == ccur.n - 1) {
-            // ---- the item's last tile: O^T (column tid) and the row sums
-            // into the split's partial result
+            // ---- the segment's last tile: O^T (column tid) and the row sums
+            // into the segment's partial result slot
             ok = mbar_wait_warp(&bars[1 + pb], (g >> 1) & 1u, ab);
             tc_fence_after();
             uint32_t o[2][NR];
