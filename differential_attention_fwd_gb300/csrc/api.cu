@@ -199,9 +199,12 @@ int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
     // The CUDA-core first passes split every unit's keys into ~4096 work
     // items for the whole call, with at least 256 keys (one chunk) per split:
     // their persistent grids then end at most one short item apart across
-    // CTAs.  (The tensor-core pass cuts the keys itself, at launch.)
+    // CTAs.  The tensor-core pass cuts the keys itself, at launch; for the
+    // shapes it may take (four or eight rows, bf16, D = 64) the CUDA-core
+    // layout, used only when it cannot run, keeps ~1024 items, so that the
+    // workspace is about the size the tensor-core pass needs.
     const int64_t chunks = (d->Tk + 255) / 256;
-    const int64_t target = 4096;
+    const int64_t target = (tqb >= 4 && d->dtype == DIFFATTN_BF16 && d->D == 64) ? 1024 : 4096;
     int64_t splits = (target + units - 1) / units;
     if (splits > chunks) splits = chunks;
     if (splits < 1) splits = 1;

@@ -197,6 +197,17 @@ def test_decode_workspace_query(lib):
     assert lib.diffattn_decode_workspace_bytes(None) == 0
 
 
+def test_decode_workspace_four_row_shapes_fit_noalloc_buffer(lib):
+    # 32 query heads over 8 key/value heads (four rows per key/value head,
+    # the tensor-core pass's shape), 16 sequences of 8192 cached keys: the
+    # partial results fit the 8 MiB buffer of diffattn_decode_noalloc, both
+    # the tensor-core pass's slots and the CUDA-core layout it falls back to
+    n = lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(B=16, H=32, kv_group=4, Tk=8192)))
+    assert 0 < n <= 8 * 1024 * 1024
+    n4 = lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(B=16, H=16, Tq=4, Tk=8192)))
+    assert 0 < n4 <= 8 * 1024 * 1024
+
+
 @pytest.mark.parametrize("kw,code", [(dict(Tq=0), _lib.DIFFATTN_ERR_INVALID),
                                      (dict(D=40), _lib.DIFFATTN_ERR_UNSUPPORTED),
                                      (dict(Tq=5, D=128), _lib.DIFFATTN_ERR_UNSUPPORTED),
