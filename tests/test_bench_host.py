@@ -84,3 +84,11 @@ def test_headline_flops_count():
     w = bench.W.WORKLOADS["b2h16t8192"]
     assert w.flops == 2 * 16 * (8192 * 8193 // 2) * 12 * 64
     assert abs(w.flops / 1e9 - 824.734) < 1e-3
+
+
+def test_l2_flush_is_named_in_config():
+    w = bench.W.WORKLOADS["b2h16t8192"]
+    assert "then a 256 MiB read" in bench.config_of(w, 0.5)["l2"]
+    assert "then a 256 MiB read" in bench.config_of(w, 0.5, "write-read")["l2"]
+    only_write = bench.config_of(w, 0.5, "write")["l2"]
+    assert "256 MiB write" in only_write and "read" not in only_write
