@@ -420,7 +420,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
                 }
             }
         }
-        // ---- prefetch (thread 0): tile g + NST - 1 into the stage of tile
+        // ---- prefetch (the producer thread): tile g + NST - 1 into the stage of tile
         // g - 1, once the PV product of tile g - 1 has read its values
         if (tid == PRODUCER && !icur.done()) {
             if (g >= 1) ok = mbar_wait(&bars[1 + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, ab);
