@@ -295,3 +295,41 @@ def test_fwd_host_rejects_without_gpu(lib):
     d = desc(B=2)
     d.q1_stride[1] = 0                   # broadcast heads are not dense
     assert call(d) == _lib.DIFFATTN_ERR_INVALID
+
+
+def _max_segments(units, tpu, grid):
+    """Brute force: the most CTA ranges [c*total//grid, (c+1)*total//grid)
+    that meet one unit's tiles [u*tpu, (u+1)*tpu)."""
+    total = units * tpu
+    bounds = [c * total // grid for c in range(grid + 1)]
+    best = 0
+    for u in range(units):
+        t0, t1 = u * tpu, (u + 1) * tpu
+        meets = sum(1 for c in range(grid) if bounds[c] < t1 and bounds[c + 1] > t0)
+        best = max(best, meets)
+    return best
+
+
+@pytest.mark.parametrize("B,H,kv_group,Tq,Tk", [(2, 3, 0, 4, 1000), (2, 3, 0, 8, 200), (1, 4, 4, 1, 129),
+                                                 (3, 8, 4, 2, 4099), (16, 32, 4, 1, 8192), (5, 6, 3, 2, 700),
+                                                 (40, 4, 4, 1, 256), (1, 1, 0, 5, 70000)])
+def test_decode_workspace_holds_every_tensor_core_segment(lib, B, H, kv_group, Tq, Tk):
+    # Four or eight rows per key/value head (bf16, D = 64): the tensor-core
+    # first pass gives every CTA one contiguous range of the units' 128-key
+    # tiles and writes one partial slot per (unit, CTA meeting it).  The
+    # workspace must hold that many slots per unit for any GPU of up to 1024
+    # SMs (4 + 4 D floats per row and slot).
+    g = max(kv_group, 1)
+    rows = g * Tq
+    chunks = -(-rows // 8)
+    per = -(-rows // chunks)
+    tqb = 1
+    while tqb < per:
+        tqb *= 2
+    assert tqb >= 4
+    units = B * (H // g) * chunks
+    tpu = -(-Tk // 128)
+    need = lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(B=B, H=H, Tq=Tq, Tk=Tk, kv_group=kv_group)))
+    for sms in (1, 7, 148, 152, 160, 1024):
+        grid = min(units * tpu, sms)
+        assert need >= units * _max_segments(units, tpu, grid) * tqb * (4 + 4 * 64) * 4, sms
