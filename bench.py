@@ -92,6 +92,40 @@ def dist_env():
     return world, rank, local
 
 
+def check_world(gpus: int, world: int) -> None:
+    """--gpus N must match the number of ranks the launcher started: one
+    process per GPU.  Without a launcher (WORLD_SIZE unset) only N = 1 runs;
+    running one replica for N > 1 would report work N GPUs never did."""
+    if gpus < 1:
+        raise ValueError(f"--gpus must be >= 1, got {gpus}")
+    if world == 1 and gpus > 1:
+        raise ValueError(f"--gpus {gpus} needs {gpus} processes, one per GPU: launch with "
+                         f"python -m torch.distributed.run --nproc-per-node {gpus} "
+                         f"--master-addr 127.0.0.1 bench.py --gpus {gpus} ...")
+    if world > 1 and gpus != world:
+        raise ValueError(f"--gpus {gpus} does not match the {world} ranks the launcher started")
+
+
+# Dense bf16 tensor-core rate of one SM per clock (tcgen05 kind::f16 with fp32
+# accumulation; a microbenchmark of back-to-back 128 x 256 x 16 products on
+# this GPU measured 8184).  Times the SM count and the sampled SM clock it
+# gives the tensor peak at the clock the kernel actually ran at.
+BF16_FLOP_PER_CLK_PER_SM = 8192
+
+
+def clock_peak(achieved_tflops: float, clocks, num_sms: int):
+    """The kernel's fraction of the tensor peak at its own sampled SM clock."""
+    if not clocks:
+        return None
+    mhz = clocks.get("sm_mhz_loaded") or clocks.get("sm_mhz")
+    if not mhz:
+        return None
+    peak = num_sms * mhz * 1e6 * BF16_FLOP_PER_CLK_PER_SM / 1e12
+    return {"sm_mhz": mhz, "sms": num_sms, "flop_per_clk_per_sm": BF16_FLOP_PER_CLK_PER_SM,
+            "peak": peak, "frac": achieved_tflops / peak,
+            "clock": "median SM clock of the samples under load (nvidia-smi, sampled, never set)"}
+
+
 def reduce_max(value: float, world: int) -> float:
     """Max of a float over all ranks (identity for one rank)."""
     if world == 1:
@@ -189,15 +223,24 @@ class ClockSampler:
             if len(parts) != len(cls.FIELDS):
                 continue
             try:
-                rows.append((float(parts[0]), float(parts[1]), parts[4:]))
+                power = float(parts[2])
+            except ValueError:
+                power = float("nan")
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:], power))
             except ValueError:
                 continue
         if not rows:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, x in enumerate(r) if x.lower() == "active"})
-        return {"sm_mhz": statistics.median(s for s, _, _ in rows),
-                "sm_max_mhz": max(m for _, m, _ in rows), "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({names[i] for _, _, r, _ in rows for i, x in enumerate(r) if x.lower() == "active"})
+        # samples under load: power above half of the highest power seen
+        pmax = max((p for *_, p in rows if p == p), default=float("nan"))
+        loaded = [s for s, _, _, p in rows if p == p and p >= 0.5 * pmax]
+        return {"sm_mhz": statistics.median(s for s, _, _, _ in rows),
+                "sm_mhz_loaded": statistics.median(loaded) if loaded else None,
+                "samples_loaded": len(loaded), "power_w_max": pmax if pmax == pmax else None,
+                "sm_max_mhz": max(m for _, m, _, _ in rows), "reasons": reasons, "samples": len(rows)}
 
 
 # --------------------------------------------------------------------------
@@ -436,6 +479,9 @@ def run_ours(args, w, world, rank, local):
                 "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"]),
                 "fwd_ms_median": statistics.median(fwd_ms), "fwd_ms_min": min(fwd_ms),
                 "fwd_ms_max": max(fwd_ms)}
+
+    roofline["at_sampled_clock"] = clock_peak(
+        achieved, clocks, torch.cuda.get_device_properties(dev).multi_processor_count)
 
     e2e = None
     if args.e2e:
@@ -794,6 +840,10 @@ def main(argv=None):
         ap.error("at least 3 warm-up steps")
 
     world, rank, local = dist_env()
+    try:
+        check_world(args.gpus, world)
+    except ValueError as e:
+        ap.error(str(e))
     if world > 1 and args.impl == "ours":
         import torch
         import torch.distributed as dist

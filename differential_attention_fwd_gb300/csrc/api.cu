@@ -24,6 +24,7 @@ constexpr size_t kWorkspaceBytes = 64;
 
 struct DeviceState {
     bool ready = false;
+    void* ctx = nullptr;          // the context the addresses below belong to
     int num_sms = 0;
     uint32_t* status = nullptr;   // device address of g_status_word
 };
@@ -37,12 +38,37 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
+}  // namespace
+
+// The calling thread's current CUDA context (driver handle), nullptr if none
+// or if the driver entry point cannot be found.
+void* current_context() {
+    using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+    static CtxGetCurrentFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            return static_cast<CtxGetCurrentFn>(nullptr);
+        return reinterpret_cast<CtxGetCurrentFn>(f);
+    }();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+namespace {
+
 int device_state(DeviceState** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DIFFATTN_ERR_CUDA;
+    void* ctx = current_context();
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState& st = g_devices[dev];
-    if (!st.ready) {
+    // A device reset or another current context loads the library's module
+    // again, possibly at other addresses: look them up again then.  (No
+    // current context yet: the lookup below makes the primary one current.)
+    if (!st.ready || ctx == nullptr || st.ctx != ctx) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return DIFFATTN_ERR_CUDA;
@@ -50,6 +76,7 @@ int device_state(DeviceState** out) {
         if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return DIFFATTN_ERR_CUDA;
         st.num_sms = sms;
         st.status = static_cast<uint32_t*>(addr);
+        st.ctx = current_context();
         st.ready = true;
     }
     if (!g_encode) {
@@ -651,31 +678,66 @@ size_t diffattn_decode_workspace_bytes(const diffattn_kv_desc* desc) {
     return plan.work_bytes;
 }
 
+}  // extern "C"
+
+namespace diffattn {
+namespace {
+
+// Every check of a decode call except those of its workspace: pointers, the
+// descriptor (and the split plan it gives), lambda, the epilogue and the
+// alignment of the cache.
+int decode_args(const diffattn_kv_desc* desc, const void* q1, const void* k1, const void* q2,
+                const void* k2, const void* v, float lambda, const float* lambda_dev, int causal,
+                const diffattn_epilogue* epi, const void* out, DecodePlan* plan,
+                diffattn_epilogue* e) {
+    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID;
+    int rc = plan_decode(desc, causal, plan);
+    if (rc != DIFFATTN_OK) return rc;
+    if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
+    *e = diffattn_epilogue{DIFFATTN_NORM_NONE, 0.f, nullptr, nullptr, 1.0f, 0};
+    if (epi) {
+        *e = *epi;
+        if (e->reserved != 0 || e->norm < DIFFATTN_NORM_NONE || e->norm > DIFFATTN_NORM_GROUP ||
+            !std::isfinite(e->out_scale) ||
+            (e->norm != DIFFATTN_NORM_NONE && !(std::isfinite(e->eps) && e->eps > 0.f)))
+            return DIFFATTN_ERR_INVALID;
+    }
+    const size_t esize = desc->dtype == DIFFATTN_BF16 ? 2 : 4;
+    if (!kv_aligned(k1, desc->k1_stride, esize) || !kv_aligned(k2, desc->k2_stride, esize) ||
+        !kv_aligned(v, desc->v_stride, esize))
+        return DIFFATTN_ERR_UNSUPPORTED;
+    return DIFFATTN_OK;
+}
+
+}  // namespace
+
+int decode_check(const diffattn_kv_desc* desc, const void* q1, const void* k1, const void* q2,
+                 const void* k2, const void* v, float lambda, const float* lambda_dev, int causal,
+                 const diffattn_epilogue* epi, const void* out, size_t* work_bytes) {
+    DecodePlan plan;
+    diffattn_epilogue e;
+    const int rc = decode_args(desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal, epi, out, &plan, &e);
+    if (rc == DIFFATTN_OK) *work_bytes = plan.work_bytes;
+    return rc;
+}
+
+}  // namespace diffattn
+
+extern "C" {
+
 int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1, const void* q2,
                     const void* k2, const void* v, float lambda, const float* lambda_dev,
                     int causal, const diffattn_epilogue* epi, void* out, void* workspace,
                     size_t workspace_bytes, diffattn_stream_t stream) {
-    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID;
     DecodePlan plan;
-    int rc = plan_decode(desc, causal, &plan);
+    diffattn_epilogue e;
+    int rc = decode_args(desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal, epi, out, &plan, &e);
     if (rc != DIFFATTN_OK) return rc;
-    if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
     if (!workspace || workspace_bytes < plan.work_bytes ||
         (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
         return DIFFATTN_ERR_INVALID;
-    diffattn_epilogue e{DIFFATTN_NORM_NONE, 0.f, nullptr, nullptr, 1.0f, 0};
-    if (epi) {
-        e = *epi;
-        if (e.reserved != 0 || e.norm < DIFFATTN_NORM_NONE || e.norm > DIFFATTN_NORM_GROUP ||
-            !std::isfinite(e.out_scale) ||
-            (e.norm != DIFFATTN_NORM_NONE && !(std::isfinite(e.eps) && e.eps > 0.f)))
-            return DIFFATTN_ERR_INVALID;
-    }
     const diffattn_kv_desc& d = *desc;
     const size_t esize = d.dtype == DIFFATTN_BF16 ? 2 : 4;
-    if (!kv_aligned(k1, d.k1_stride, esize) || !kv_aligned(k2, d.k2_stride, esize) ||
-        !kv_aligned(v, d.v_stride, esize))
-        return DIFFATTN_ERR_UNSUPPORTED;
     DecodeParams p{};
     p.B = (int)d.B;
     p.H = (int)d.H;

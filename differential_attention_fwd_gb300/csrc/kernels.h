@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include "diffattn.h"
+
 namespace diffattn {
 
 // Output epilogue applied after O = O1/l1 - lambda O2/l2 (the same values as
@@ -194,6 +196,15 @@ int launch_lambda(const float* lq1, const float* lk1, const float* lq2, const fl
 int launch_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                       int64_t n, const float* dlambda, float* dlq1, float* dlk1, float* dlq2,
                       float* dlk2, cudaStream_t stream);
+
+// Host helpers of the C-ABI layer (api.cu).
+// The calling thread's current CUDA context, nullptr if none.
+void* current_context();
+// Every argument check diffattn_decode makes except those of its workspace;
+// on success *work_bytes receives the workspace the call needs.
+int decode_check(const diffattn_kv_desc* desc, const void* q1, const void* k1, const void* q2,
+                 const void* k2, const void* v, float lambda, const float* lambda_dev, int causal,
+                 const diffattn_epilogue* epi, const void* out, size_t* work_bytes);
 
 // One-thread kernel whose bounded wait on a barrier nothing completes runs
 // out and records the timeout in `status` (the failure path, tested without a

@@ -29,22 +29,31 @@ static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / 
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-float* g_scratch_ptr[kMaxDevices] = {};
+struct Scratch {
+    void* ctx = nullptr;      // the context the address belongs to
+    float* ptr = nullptr;
+};
+Scratch g_scratch[kMaxDevices];
 
-// Device address of the scratch array for the current device.  The array's
+// Device address of the scratch array in the current context.  The array's
 // name is a host-side stand-in in host code; the address comes from the
-// runtime, once per device, with that device current.
+// runtime, once per device and context, with that device current.  A device
+// reset or another current context (which load the module again, possibly
+// elsewhere) make the next call look it up again.
 int scratch_for_current_device(float** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DIFFATTN_ERR_CUDA;
+    void* ctx = current_context();
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
+    Scratch& s = g_scratch[dev];
+    if (!s.ptr || ctx == nullptr || s.ctx != ctx) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
             return DIFFATTN_ERR_CUDA;
-        g_scratch_ptr[dev] = static_cast<float*>(ptr);
+        s.ptr = static_cast<float*>(ptr);
+        s.ctx = current_context();
     }
-    *out = g_scratch_ptr[dev];
+    *out = s.ptr;
     return DIFFATTN_OK;
 }
 
@@ -57,16 +66,15 @@ int diffattn_decode_noalloc(const diffattn_kv_desc* desc, const void* q1, const 
                             const void* q2, const void* k2, const void* v, float lambda,
                             const float* lambda_dev, int causal, const diffattn_epilogue* epi,
                             void* out, diffattn_stream_t stream) {
-    const size_t need = diffattn_decode_workspace_bytes(desc);
-    if (need == 0) {
-        // invalid or unsupported descriptor: let the regular entry point say which
-        return diffattn_decode(desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal, epi, out,
-                               nullptr, 0, stream);
-    }
-    // more partial results than the static buffer holds
+    // the checks of diffattn_decode first, so errors come in the same order
+    size_t need = 0;
+    int rc = diffattn::decode_check(desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal, epi, out,
+                                    &need);
+    if (rc != DIFFATTN_OK) return rc;
+    // then the one limit of this entry point: the partial results must fit
     if (need > diffattn::kNoAllocScratchBytes) return DIFFATTN_ERR_UNSUPPORTED;
     float* scratch = nullptr;
-    const int rc = diffattn::scratch_for_current_device(&scratch);
+    rc = diffattn::scratch_for_current_device(&scratch);
     if (rc != DIFFATTN_OK) return rc;
     return diffattn_decode(desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal, epi, out, scratch,
                            diffattn::kNoAllocScratchBytes, stream);

@@ -405,12 +405,18 @@ int diffattn_decode(const diffattn_kv_desc *desc, const void *q1, const void *k1
  * of the key-range splits go to a scratch buffer of 8 MiB (8388608 bytes) that
  * is part of the library; every GPU that loads the library holds one such
  * buffer until the process exits.  The call allocates nothing.  The first call
- * on a device looks up the buffer's device address (once per device, with that
- * device current); make that first call before capturing any stream.
+ * on a device (and the first after a device reset, or from another context)
+ * looks up the buffer's device address, with that device current; under CUDA's
+ * lazy module loading that first call is also where the driver loads the
+ * buffer's module and commits its 8 MiB, which may synchronise the device.
+ * Make that first call at set-up, before capturing any stream and outside any
+ * latency-critical region.
  * Every call shares the one buffer: calls that run on the GPU at the same time
- * race and corrupt each other's results.  The buffer needs no clearing; each
- * call writes everything it reads.
- * Errors: as diffattn_decode, and DIFFATTN_ERR_UNSUPPORTED when the problem
+ * race and corrupt each other's results.  Calls enqueued one after another on
+ * one stream do not: each call's kernels finish before the next call's start.
+ * The buffer needs no clearing; each call writes everything it reads.
+ * Errors: every check of diffattn_decode other than the workspace's comes
+ * first and gives the same code; then DIFFATTN_ERR_UNSUPPORTED when the problem
  * needs more than 8 MiB of partial results (diffattn_decode_workspace_bytes
  * reports the need; use diffattn_decode with a workspace instead).
  */

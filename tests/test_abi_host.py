@@ -227,6 +227,23 @@ def test_decode_requires_workspace(lib):
     assert rc == _lib.DIFFATTN_ERR_INVALID
 
 
+def test_decode_noalloc_reports_argument_errors_before_its_size_limit(lib):
+    # a problem too big for the 8 MiB buffer, with a NULL output: the argument
+    # error of diffattn_decode comes first, the buffer limit only after it
+    big = kv_desc(B=128, H=64, Tq=2, Tk=2)
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(big)) > 8 * 1024 * 1024
+    rc = lib.diffattn_decode_noalloc(ctypes.byref(big), *ptrs(5), ctypes.c_float(0.5), None, 1,
+                                     None, None, None)
+    assert rc == _lib.DIFFATTN_ERR_INVALID
+    rc = lib.diffattn_decode_noalloc(ctypes.byref(big), *ptrs(5), ctypes.c_float(float("nan")), None, 1,
+                                     None, ctypes.c_void_p(FAKE * 9), None)
+    assert rc == _lib.DIFFATTN_ERR_INVALID
+    # unsupported shapes report as diffattn_decode does
+    rc = lib.diffattn_decode_noalloc(ctypes.byref(kv_desc(D=40)), *ptrs(5), ctypes.c_float(0.5),
+                                     None, 1, None, ctypes.c_void_p(FAKE * 9), None)
+    assert rc == _lib.DIFFATTN_ERR_UNSUPPORTED
+
+
 def test_grouped_heads_select_and_reject(lib):
     # H = 8 query heads over 2 key/value heads: still the tensor-core kernel
     assert select(lib, desc(H=8, kv_group=4)) == _lib.DIFFATTN_KERNEL_TCGEN05

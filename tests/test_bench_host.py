@@ -92,3 +92,28 @@ def test_l2_flush_is_named_in_config():
     assert "then a 256 MiB read" in bench.config_of(w, 0.5, "write-read")["l2"]
     only_write = bench.config_of(w, 0.5, "write")["l2"]
     assert "256 MiB write" in only_write and "read" not in only_write
+
+
+def test_gpus_flag_must_match_the_ranks(monkeypatch):
+    # one process cannot stand in for N GPUs: without a launcher --gpus 2
+    # fails loudly instead of running one replica
+    for var in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    with pytest.raises(SystemExit) as e:
+        bench.main(["--gpus", "2", "--steps", "1", "--warmup", "3"])
+    assert e.value.code != 0
+    with pytest.raises(SystemExit):
+        bench.main(["--gpus", "0"])
+    # a launcher that started a different number of ranks than --gpus says
+    monkeypatch.setenv("WORLD_SIZE", "4")
+    with pytest.raises(SystemExit):
+        bench.main(["--gpus", "2", "--impl", "reference"])
+    bench.check_world(1, 1)
+    bench.check_world(2, 2)
+
+
+def test_clock_scaled_peak():
+    r = bench.clock_peak(1500.0, {"sm_mhz": 2000.0}, 152)
+    assert r["peak"] == pytest.approx(152 * 2000e6 * 8192 / 1e12)
+    assert r["frac"] == pytest.approx(1500.0 / r["peak"])
+    assert bench.clock_peak(1500.0, None, 152) is None

@@ -9,7 +9,8 @@ import oracle
 import workloads as W
 import differential_attention_fwd_gb300 as da
 from differential_attention_fwd_gb300 import build as build_mod
-from tests.helpers import SAVED_PATH_SLACK, assert_close, assert_grad_close, to_device, to_numpy
+from tests.helpers import (SAVED_PATH_SLACK, assert_close, assert_dlambda_close, assert_grad_close,
+                           to_device, to_numpy)
 
 pytestmark = pytest.mark.gpu
 NAMES = ("dq1", "dk1", "dq2", "dk2", "dv")
@@ -66,9 +67,8 @@ def test_backward_from_saved_results(dtype, D, H, Hk, T, causal):
         assert_grad_close(to_numpy(a), r, dtype, f"saved bwd {dtype} T={T} causal={causal} {name}",
                           slack=SAVED_PATH_SLACK)
     a2v = oracle.differential_attention(inp.q2, inp.k2, inp.q2, inp.k2, inp.v, 0.0, causal)
-    rows_abs = float(np.sum(np.abs(np.sum(dout * a2v, axis=-1))))
-    tol = (1e-4 if dtype == "f32" else 2e-3) * max(1.0, rows_abs)
-    assert abs(float(got[5]) - ref[5]) <= tol
+    assert_dlambda_close(float(got[5]), ref[5], np.sum(dout * a2v, axis=-1), dtype,
+                         f"saved bwd {dtype} T={T} causal={causal} dlambda")
 
 
 def test_autograd_bf16_tensor_core_end_to_end():
@@ -83,8 +83,8 @@ def test_autograd_bf16_tensor_core_end_to_end():
         assert_grad_close(to_numpy(t.grad), r, "bf16", f"autograd bf16 {name}",
                           slack=SAVED_PATH_SLACK)
     a2v = oracle.differential_attention(inp.q2, inp.k2, inp.q2, inp.k2, inp.v, 0.0, True)
-    rows_abs = float(np.sum(np.abs(np.sum(dout * a2v, axis=-1))))
-    assert abs(float(lam.grad) - ref[5]) <= 2e-3 * max(1.0, rows_abs)
+    assert_dlambda_close(float(lam.grad), ref[5], np.sum(dout * a2v, axis=-1), "bf16",
+                         "autograd bf16 dlambda")
 
 
 def test_saved_and_recomputed_backward_agree():

@@ -57,6 +57,32 @@ def test_noalloc_decode_matches_workspace_decode_twice(lib):
     assert da.get_device_error() == 0
 
 
+def test_noalloc_calls_back_to_back_on_one_stream(lib):
+    # Two calls enqueued one after the other on one stream with no host
+    # synchronisation between them: the CUDA-core path (one query row) and
+    # the tensor-core path (four rows).  Both use the one library buffer; the
+    # second call's first pass must not overwrite it while the first call's
+    # combine pass still reads it.  Each result is checked against the
+    # workspace decode and against the float64 oracle.
+    import oracle
+    cases = ((71, 1, 6000, 0.6, True), (72, 4, 4000, 0.9, True))
+    devs = [_inputs(seed, Tq, Tk) for seed, Tq, Tk, _, _ in cases]
+    torch.cuda.synchronize()
+    outs = []
+    for dev, (_, _, _, lam, causal) in zip(devs, cases):
+        rc, out = _call_noalloc(lib, dev, lam, causal)
+        assert rc == _lib.DIFFATTN_OK, _lib.strerror(rc)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for dev, out, (_, _, _, lam, causal) in zip(devs, outs, cases):
+        ref = da.differential_attention_decode(*dev, lam, causal=causal)
+        torch.cuda.synchronize()
+        assert_close(to_numpy(out), to_numpy(ref), "bf16", "noalloc back to back vs workspace")
+        want = oracle.differential_attention_kv(*(to_numpy(t) for t in dev), lam, causal)
+        assert_close(to_numpy(out), want, "bf16", "noalloc back to back vs oracle")
+    assert da.get_device_error() == 0
+
+
 def test_noalloc_refuses_problems_beyond_its_buffer(lib):
     # 8192 heads x 1 split x 2 queries x 260 floats = 17 MB of partial results
     q = torch.zeros(128, 64, 2, 64, dtype=torch.bfloat16, device="cuda")
