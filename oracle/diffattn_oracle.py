@@ -33,6 +33,12 @@ Readings where the pages leave a step open:
     the causal mask, key j is visible to query i iff j <= i, so no row is
     ever fully masked.
   * lambda is any finite real (not clamped to [0, 1]).
+  * The value width Dv is 2D in the operation's own shape (paperleet, Formula
+    and conventions).  The DIFF V2 head of the aiengineeringfromscratch lesson
+    ("V1 contre V2": the head dimension stays that of the baseline) has V as
+    wide as Q and K, Dv = D.  O = (A_1 - lambda A_2) V holds for any V width,
+    so every function here takes V of any width Dv >= 1 and returns O of that
+    width.
 
 The step that follows the operation in the model (per-head normalisation,
 GroupNorm or RMSNorm, then x (1 - lambda_init)) is `head_norm`, pinned
@@ -136,10 +142,11 @@ def _as64(x) -> np.ndarray:
 
 
 def _check_shapes(q1, k1, q2, k2, v=None):
-    """Q1, Q2: [B, H, T, D]; K1, K2: [B, H_kv, T, D]; V: [B, H_kv, T, 2D] with
-    H a multiple of H_kv (query heads share key/value heads in groups of
-    H / H_kv, the grouped layout of DIFF V2; H_kv = H is the plain layout).
-    Returns the group size H / H_kv."""
+    """Q1, Q2: [B, H, T, D]; K1, K2: [B, H_kv, T, D]; V: [B, H_kv, T, Dv] (Dv =
+    2D for the operation's own shape, Dv = D for the DIFF V2 head) with H a
+    multiple of H_kv (query heads share key/value heads in groups of H / H_kv,
+    the grouped layout of DIFF V2; H_kv = H is the plain layout).  Returns the
+    group size H / H_kv."""
     if q1.shape != q2.shape or k1.shape != k2.shape:
         raise ValueError("Q1, Q2 must share one shape, and K1, K2 another")
     if q1.ndim != 4 or k1.ndim != 4 or min(q1.shape) < 1 or min(k1.shape) < 1:
@@ -148,8 +155,8 @@ def _check_shapes(q1, k1, q2, k2, v=None):
     Hk = k1.shape[1]
     if k1.shape[0] != B or k1.shape[2:] != (T, D) or H % Hk != 0:
         raise ValueError("K1/K2 must be [B, H_kv, T, D] with H a multiple of H_kv")
-    if v is not None and v.shape != (B, Hk, T, 2 * D):
-        raise ValueError("V must be [B, H_kv, T, 2D]")
+    if v is not None and (v.ndim != 4 or v.shape[:3] != (B, Hk, T) or v.shape[3] < 1):
+        raise ValueError("V must be [B, H_kv, T, Dv] with Dv >= 1")
     return H // Hk
 
 
@@ -180,27 +187,28 @@ def differential_attention(q1, k1, q2, k2, v, lam: float, causal: bool = True,
                            block: int = 256) -> np.ndarray:
     """O = (A_1 - lambda A_2) V in float64.
 
-    q1, q2: [B, H, T, D]; k1, k2: [B, H_kv, T, D]; v: [B, H_kv, T, 2D] (any
-    real dtype, upcast to float64), H a multiple of H_kv: query head h uses
-    key/value head h // (H / H_kv).  lam: the scalar lambda.  causal: apply the
-    causal mask to both branches.
+    q1, q2: [B, H, T, D]; k1, k2: [B, H_kv, T, D]; v: [B, H_kv, T, Dv] (any
+    real dtype, upcast to float64; Dv = 2D in the operation's own shape), H a
+    multiple of H_kv: query head h uses key/value head h // (H / H_kv).  lam:
+    the scalar lambda.  causal: apply the causal mask to both branches.
 
     rows: optional query rows to evaluate (every row when None).  Every output
     row depends only on its own query row and all keys/values of its head, so
     a row subset is exact, not an approximation.
     heads: optional list of (b, h) to evaluate (every head when None).
 
-    Returns [B, H, R, 2D] for all heads, or [len(heads), R, 2D] when heads is
+    Returns [B, H, R, Dv] for all heads, or [len(heads), R, Dv] when heads is
     given.  Query rows are processed `block` at a time only to bound memory.
     """
     g = _check_shapes(q1, k1, q2, k2, v)
     B, H, T, D = q1.shape
+    Dv = v.shape[3]
     lam = float(lam)
     row_idx = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
     if row_idx.size and (row_idx.min() < 0 or row_idx.max() >= T):
         raise ValueError("row index out of range")
     head_list = [(b, h) for b in range(B) for h in range(H)] if heads is None else list(heads)
-    out = np.empty((len(head_list), row_idx.size, 2 * D))
+    out = np.empty((len(head_list), row_idx.size, Dv))
     for n, (b, h) in enumerate(head_list):
         hq1, hq2 = _as64(q1[b, h]), _as64(q2[b, h])
         hk1, hk2, hv = (_as64(x[b, h // g]) for x in (k1, k2, v))
@@ -208,7 +216,7 @@ def differential_attention(q1, k1, q2, k2, v, lam: float, causal: bool = True,
             r = row_idx[r0:r0 + block]
             out[n, r0:r0 + block] = _head_rows(hq1, hk1, hq2, hk2, r, lam, causal) @ hv
     if heads is None:
-        out = out.reshape(B, H, row_idx.size, 2 * D)
+        out = out.reshape(B, H, row_idx.size, Dv)
     return out
 
 
@@ -254,11 +262,11 @@ def differential_attention_kv(q1, k1, q2, k2, v, lam: float, causal: bool = True
     """O = (A_1 - lambda A_2) V for Tq queries against Tk >= Tq keys (decode
     over a KV cache), in float64.
 
-    q1, q2: [B, H, Tq, D]; k1, k2: [B, H_kv, Tk, D]; v: [B, H_kv, Tk, 2D], H a
+    q1, q2: [B, H, Tq, D]; k1, k2: [B, H_kv, Tk, D]; v: [B, H_kv, Tk, Dv], H a
     multiple of H_kv (query head h reads key/value head h // (H / H_kv)).  With
     the causal mask, query i sits at position Tk - Tq + i of the key sequence and
     sees keys j <= Tk - Tq + i (the usual KV-cache alignment; for Tq = Tk it is
-    the causal mask of differential_attention).  Returns [B, H, Tq, 2D].
+    the causal mask of differential_attention).  Returns [B, H, Tq, Dv].
     """
     q1, k1, q2, k2, v = (_as64(x) for x in (q1, k1, q2, k2, v))
     if q1.shape != q2.shape or k1.shape != k2.shape or q1.ndim != 4 or k1.ndim != 4:
@@ -266,13 +274,13 @@ def differential_attention_kv(q1, k1, q2, k2, v, lam: float, causal: bool = True
     B, H, Tq, D = q1.shape
     Hk, Tk = k1.shape[1], k1.shape[2]
     if (k1.shape[0] != B or Hk < 1 or H % Hk != 0 or k1.shape[3] != D
-            or v.shape != (B, Hk, Tk, 2 * D)):
+            or v.ndim != 4 or v.shape[:3] != (B, Hk, Tk) or v.shape[3] < 1):
         raise ValueError("inconsistent shapes")
     g = H // Hk
     if min(B, H, Tq, D, Tk) < 1 or (causal and Tk < Tq):
         raise ValueError("need non-empty tensors and Tk >= Tq for the causal mask")
     rows = np.arange(Tq)
-    out = np.empty((B, H, Tq, 2 * D))
+    out = np.empty((B, H, Tq, v.shape[3]))
     for b in range(B):
         for h in range(H):
             w = _head_rows(q1[b, h], k1[b, h // g], q2[b, h], k2[b, h // g], rows, float(lam),

@@ -224,9 +224,56 @@ def test_noncausal_key_permutation_invariance():
 def test_shape_validation():
     q1, k1, q2, k2, v = rand_inputs(1, 1, 4, 4, 0)
     with pytest.raises(ValueError):
-        oracle.differential_attention(q1, k1, q2, k2, v[..., :4], 0.5)
+        oracle.differential_attention(q1, k1, q2, k2, v[..., :0], 0.5)
+    with pytest.raises(ValueError):
+        oracle.differential_attention(q1, k1, q2, k2, v[:, :, :3], 0.5)
     with pytest.raises(ValueError):
         oracle.differential_attention(q1, k1[:, :, :3], q2, k2, v, 0.5)
+    with pytest.raises(ValueError):
+        oracle.differential_attention_kv(q1, k1, q2, k2, v[:, :, :3], 0.5)
+
+
+# ---------------------------------------------------------------------------
+# The DIFF V2 head (aiengineeringfromscratch lesson, "V1 contre V2": the head
+# dimension stays that of the baseline): V as wide as Q and K, Dv = D, with
+# the two branches sharing a key/value head.
+# ---------------------------------------------------------------------------
+
+def test_value_width_d_lambda0_matches_torch_gqa():
+    # lambda = 0 is ordinary attention (paperleet, Formula and conventions);
+    # torch's attention routine takes a value width of its own and grouped heads
+    rng = np.random.default_rng(70)
+    q1, q2 = rng.standard_normal((2, 2, 6, 33, 16))
+    k1, k2 = rng.standard_normal((2, 2, 3, 33, 16))
+    for dv in (16, 5, 40):
+        v = rng.standard_normal((2, 3, 33, dv))
+        for causal in (True, False):
+            got = oracle.differential_attention(q1, k1, q2, k2, v, 0.0, causal)
+            assert got.shape == (2, 6, 33, dv)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(q1), torch.from_numpy(k1), torch.from_numpy(v), is_causal=causal,
+                enable_gqa=True).numpy()
+            assert np.max(np.abs(got - ref)) <= 1e-12
+
+
+def test_value_width_d_brute_force_and_identities():
+    rng = np.random.default_rng(71)
+    q1, k1, q2, k2 = rng.standard_normal((4, 1, 2, 7, 4))
+    v = rng.standard_normal((1, 2, 7, 4))          # Dv = D
+    for lam in (0.0, 0.8, -0.35, 1.7):
+        for causal in (True, False):
+            got = oracle.differential_attention(q1, k1, q2, k2, v, lam, causal)
+            ref = brute_force(q1, k1, q2, k2, v, lam, causal)
+            assert np.max(np.abs(got - ref)) <= 1e-12
+    # shared keys (K1 = K2) and identical queries cancel exactly at lambda = 1
+    assert np.all(oracle.differential_attention(q1, k1, q1, k1, v, 1.0, True) == 0.0)
+    # rows of O through ones of width D are 1 - lambda
+    o = oracle.differential_attention(q1, k1, q2, k1, np.ones((1, 2, 7, 4)), 0.3, True)
+    assert np.max(np.abs(o - 0.7)) <= 1e-12
+    # queries over a cache with Dv = D equal the last rows of the full pass
+    full = oracle.differential_attention(q1, k1, q2, k2, v, 0.6, True)
+    tail = oracle.differential_attention_kv(q1[:, :, -3:], k1, q2[:, :, -3:], k2, v, 0.6, True)
+    assert np.max(np.abs(full[:, :, -3:] - tail)) <= 1e-12
 
 
 # ---------------------------------------------------------------------------
