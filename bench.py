@@ -260,9 +260,11 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
-def oracle_rows_flops(rows, T, D, causal):
+def oracle_rows_flops(rows, T, D, causal, Dv=None):
+    """Algorithmic FLOPs of the given query rows: 4 D + 4 Dv per unmasked pair
+    (12 D for the operation's own value width, Dv = 2D)."""
     pairs = sum((int(r) + 1) if causal else T for r in rows)
-    return pairs * 12 * D
+    return pairs * (4 * D + 4 * (2 * D if Dv is None else Dv))
 
 
 def time_oracle(inp, w, lam, rows, head=(0, 0)):
@@ -271,7 +273,7 @@ def time_oracle(inp, w, lam, rows, head=(0, 0)):
     t0 = time.perf_counter()
     oracle.differential_attention(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, lam, w.causal,
                                   rows=rows, heads=[head])
-    return time.perf_counter() - t0, oracle_rows_flops(rows, w.T, w.D, w.causal)
+    return time.perf_counter() - t0, oracle_rows_flops(rows, w.T, w.D, w.causal, w.Dv)
 
 
 def sample_rows(T, n, seed):
@@ -364,7 +366,7 @@ def input_bytes(w):
     when the branches share it)."""
     el = 2 if w.dtype == "bf16" else 4
     k_tensors = 1 if w.shared_keys else 2
-    return w.B * w.T * (w.H * 2 * w.D + w.Hk * (k_tensors * w.D + 2 * w.D)) * el
+    return w.B * w.T * (w.H * 2 * w.D + w.Hk * (k_tensors * w.D + w.Dv)) * el
 
 
 # --------------------------------------------------------------------------
@@ -489,7 +491,10 @@ def run_ours(args, w, world, rank, local):
                       d_out, desc, launches_per_step, flush, stream, world, ws)
 
     result = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if w.name == W.HEADLINE else
+                  f"diffattn_fwd TFLOP/s and % of GB300 bf16 tensor peak ({w.name}: B={w.B},H={w.H},"
+                  f"H_kv={w.Hk},T={w.T},D={w.D},Dv={w.Dv} {'causal' if w.causal else 'full'})",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {**config_of(w, float(d_lam.item()), args.l2_flush),
@@ -752,12 +757,15 @@ def run_decode(args, world, rank, local):
 
     build_mod.build()
     lib = _lib.load()
-    w = W.DECODE_WORKLOADS[args.decode_workload]
+    prefill = args.mode == "prefill"
+    w = W.PREFILL_WORKLOADS[args.prefill_workload] if prefill else W.DECODE_WORKLOADS[args.decode_workload]
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     inp = W.draw_kv(w)
     d_in = [torch.from_numpy(x).to(dev, tdt) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    if getattr(w, "shared_keys", False):
+        d_in[3] = d_in[1]
     d_out = torch.empty((w.B, w.H, w.Tq, w.Dv), dtype=tdt, device=dev)
     flush = L2Flush(dev, args.l2_flush)
     stream = torch.cuda.current_stream(dev)
@@ -797,6 +805,27 @@ def run_decode(args, world, rank, local):
     peaks, src = load_peaks()
     gbs = w.bytes / statistics.mean(ms) * 1e3 / 1e9
     hk = f",H_kv={w.Hk}" if w.Hk != w.H else ""
+    config = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hk, "Tq": w.Tq, "Tk": w.Tk, "D": w.D,
+              "Dv": w.Dv, "causal": w.causal, "lambda": w.lambda_value,
+              "gbytes_per_step": w.bytes / 1e9, "l2": flush.describe(), "parallelism": "replicas"}
+    if prefill:
+        # a chunk of queries over the cache: one forward launch, compute-bound
+        tflops = w.flops / statistics.mean(ms) * 1e3 / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                    "frac": tflops / peak, "traffic": None,
+                    "peak_source": f"{src} bf16_tflops (burst; kernel timed alone)",
+                    "at_sampled_clock": clock_peak(
+                        tflops, clocks, torch.cuda.get_device_properties(dev).multi_processor_count)}
+        return {
+            "metric": f"diffattn_decode (queries over a cache) TFLOP/s (B={w.B},H={w.H}{hk},"
+                      f"Tq={w.Tq},Tk={w.Tk},D={w.D},Dv={w.Dv})",
+            "value": w.flops * args.steps * world / max_s / 1e12, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "config": {**config, "gflop_per_step": w.flops / 1e9},
+            "roofline": roofline, "gpu_launches": args.steps, "clocks": clocks,
+        }
     return {
         "metric": f"diffattn_decode HBM GB/s (B={w.B},H={w.H}{hk},Tq={w.Tq},Tk={w.Tk},D={w.D})",
         "value": w.bytes * args.steps * world / max_s / 1e9, "unit": "GB/s", "n_gpus": world,
@@ -828,8 +857,10 @@ def main(argv=None):
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
     ap.add_argument("--l2-flush", choices=["write", "write-read"], default="write-read",
                     help="the L2 flush between timed steps")
-    ap.add_argument("--mode", choices=["forward", "backward", "decode"], default="forward")
+    ap.add_argument("--mode", choices=["forward", "backward", "decode", "prefill"], default="forward")
     ap.add_argument("--decode-workload", default="decode_b16h16q1k8192", choices=sorted(W.DECODE_WORKLOADS))
+    ap.add_argument("--prefill-workload", default="prefill_b4h16q1024k8192",
+                    choices=sorted(W.PREFILL_WORKLOADS))
     ap.add_argument("--bwd-recompute", action="store_true",
                     help="backward mode: recompute the forward instead of starting from the "
                          "training forward's saved results")
@@ -850,7 +881,7 @@ def main(argv=None):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     w = W.ALL_WORKLOADS[args.workload]
-    if args.mode == "decode" and args.impl == "ours":
+    if args.mode in ("decode", "prefill") and args.impl == "ours":
         res = run_decode(args, world, rank, local)
         if rank == 0:
             print(json.dumps(res), flush=True)

@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import ctypes
 import numbers
+import warnings
 from typing import Optional
 
 import torch
@@ -111,6 +112,7 @@ def make_desc(q1, k1, q2, k2, v, out) -> DiffattnDesc:
     B, H, T, D = q1.shape
     d = DiffattnDesc()
     d.B, d.H, d.T, d.D = B, H, T, D
+    d.Dv = v.shape[-1]
     d.dtype = _DTYPES[q1.dtype]
     d.kv_group = H // k1.shape[1]
     for field, t in (("q1_stride", q1), ("k1_stride", k1), ("q2_stride", q2), ("k2_stride", k2),
@@ -118,6 +120,25 @@ def make_desc(q1, k1, q2, k2, v, out) -> DiffattnDesc:
         s = t.stride()
         getattr(d, field)[:] = (s[0], s[1], s[2])
     return d
+
+
+_WARNED_SLOW = set()
+
+
+def _warn_if_cuda_cores(lib, d, ptrs, what: str) -> None:
+    """Warn once per call site when a bf16 call of a shape the tensor-core
+    kernel takes (value width 128 with D = 64 or 128) runs on the CUDA-core
+    kernel instead, because a base pointer or a stride is not 16-byte aligned
+    (or a stride is 0)."""
+    tc_shape = (d.D == 64 and d.Dv in (0, 128)) or (d.D == 128 and d.Dv == 128)
+    if d.dtype != DIFFATTN_BF16 or not tc_shape or what in _WARNED_SLOW:
+        return
+    if lib.diffattn_select_kernel(ctypes.byref(d), *ptrs) == DIFFATTN_KERNEL_SIMT:
+        _WARNED_SLOW.add(what)
+        warnings.warn(f"{what}: a bf16 call of a tensor-core shape runs on the CUDA-core kernel because a base "
+                      "pointer or stride is not 16-byte aligned (or a stride is 0); pass "
+                      "16-byte-aligned tensors for the tensor-core kernel", RuntimeWarning,
+                      stacklevel=3)
 
 
 def _prepare(q1, k1, q2, k2, value):
@@ -134,8 +155,9 @@ def _prepare(q1, k1, q2, k2, value):
     if k1.shape[0] != B or tuple(k1.shape[2:]) != (T, D) or Hk < 1 or H % Hk != 0:
         raise ValueError(f"k1, k2 must be [B, H_kv, T, D] with H_kv dividing H = {H}, "
                          f"got {tuple(k1.shape)}")
-    if tuple(value.shape) != (B, Hk, T, 2 * D):
-        raise ValueError(f"value must be [B, H_kv, T, 2D] = {(B, Hk, T, 2 * D)}, got {tuple(value.shape)}")
+    if tuple(value.shape[:3]) != (B, Hk, T) or not 1 <= value.shape[3] <= 256:
+        raise ValueError(f"value must be [B, H_kv, T, Dv] = {(B, Hk, T)} + (Dv <= 256,) (Dv = 2D "
+                         f"is the operation's own shape), got {tuple(value.shape)}")
     dt = q1.dtype
     if dt not in _DTYPES:
         raise ValueError(f"unsupported dtype {dt}; expected bfloat16 or float32")
@@ -171,7 +193,9 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
                            out_scale: float = 1.0) -> torch.Tensor:
     """O = (softmax(Q1 K1^T/sqrt(D) + M) - lambda softmax(Q2 K2^T/sqrt(D) + M)) V.
 
-    q1, q2: [B, H, T, D]; k1, k2: [B, H_kv, T, D]; value: [B, H_kv, T, 2D];
+    q1, q2: [B, H, T, D]; k1, k2: [B, H_kv, T, D]; value: [B, H_kv, T, Dv]
+    with Dv = 2D (the operation's own shape) or any width up to 256 (Dv = D
+    is the DIFF V2 head; D = 128, Dv = 128 runs on the tensor cores too);
     all bfloat16 or all float32 on one CUDA device, innermost dimension
     contiguous (other strides are passed through).  H_kv must divide H: query
     head h reads key/value head h // (H // H_kv) (grouped key/value heads;
@@ -179,17 +203,17 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
     shares the keys between the branches.  coefficient: lambda, a Python number or a scalar
     tensor (a CUDA float32 scalar is read by the kernel without a host sync).
     causal: mask key j > query i in both branches.  out: optional preallocated
-    [B, H, T, 2D] output of the same dtype.  dynamic_schedule: hand out work
+    [B, H, T, Dv] output of the same dtype.  dynamic_schedule: hand out work
     items at run time through a small per-stream workspace (the result is
     the same either way).
 
     Optional fused epilogue (the step after the operation in the model):
-    norm "rms" or "group" normalises each (b, h, t) row over the head's 2D
+    norm "rms" or "group" normalises each (b, h, t) row over the head's Dv
     channels (eps norm_eps), then multiplies by norm_weight and adds
-    norm_bias ([H, 2D] float32 tensors, optional), and finally scales by
+    norm_bias ([H, Dv] float32 tensors, optional), and finally scales by
     out_scale (e.g. 1 - lambda_init).
 
-    Returns the [B, H, T, 2D] output; the launch is asynchronous on the
+    Returns the [B, H, T, Dv] output; the launch is asynchronous on the
     current CUDA stream.  When grad mode is on and an input or a tensor
     coefficient requires grad, the result carries an autograd node whose
     backward runs diffattn_bwd (no epilogue and no `out` then).
@@ -211,20 +235,22 @@ def _forward(q1, k1, q2, k2, value, coefficient, causal, out, dynamic_schedule, 
              norm_weight, norm_bias, out_scale, train=False):
     (q1, k1, q2, k2, value), dev = _prepare(q1, k1, q2, k2, value)
     B, H, T, D = q1.shape
+    Dv = value.shape[3]
     if out is None:
-        out = torch.empty((B, H, T, 2 * D), dtype=q1.dtype, device=dev)
+        out = torch.empty((B, H, T, Dv), dtype=q1.dtype, device=dev)
     else:
         _require_cuda(out, "out")
-        if tuple(out.shape) != (B, H, T, 2 * D) or out.dtype != q1.dtype or out.device != dev:
-            raise ValueError("out must be [B, H, T, 2D] with the inputs' dtype and device")
+        if tuple(out.shape) != (B, H, T, Dv) or out.dtype != q1.dtype or out.device != dev:
+            raise ValueError("out must be [B, H, T, Dv] with the inputs' dtype and device")
         if out.stride(-1) != 1:
             raise ValueError("out must have a contiguous innermost dimension")
     lam_host, lam_dev = _coefficient(coefficient, dev)
     d = make_desc(q1, k1, q2, k2, value, out)
-    epi = _epilogue(norm, norm_eps, norm_weight, norm_bias, out_scale, H, 2 * D, dev)
+    epi = _epilogue(norm, norm_eps, norm_weight, norm_bias, out_scale, H, Dv, dev)
     lib = _lib.load()
     lam_ptr = ctypes.c_void_p(lam_dev.data_ptr() if lam_dev is not None else 0)
     ins = [ctypes.c_void_p(t.data_ptr()) for t in (q1, k1, q2, k2, value)]
+    _warn_if_cuda_cores(lib, d, ins + [ctypes.c_void_p(out.data_ptr())], "differential_attention")
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev)
         ws = workspace_for(dev, stream) if dynamic_schedule else None
@@ -254,7 +280,7 @@ def differential_attention_host(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Te
     """differential_attention for inputs in host memory (CPU tensors,
     preferably pinned): the library copies them to the device, runs the
     forward and copies the output back, overlapping the copies of one chunk of
-    heads with the forward of another.  Returns the [B, H, T, 2D] output on
+    heads with the forward of another.  Returns the [B, H, T, Dv] output on
     the host (`out`, a pinned CPU tensor, if given).  `buffers`: optional
     device tensors (q1, k1, q2, k2, value, out) to reuse between calls.  The
     result is ready when the current stream of `device` has completed."""
@@ -264,16 +290,17 @@ def differential_attention_host(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Te
     ts = [t.contiguous() for t in ts]
     q1, k1, q2, k2, value = ts
     B, H, T, D = q1.shape
+    Dv = value.shape[3]
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     if out is None:
-        out = torch.empty((B, H, T, 2 * D), dtype=q1.dtype).pin_memory()
+        out = torch.empty((B, H, T, Dv), dtype=q1.dtype).pin_memory()
     if buffers is None:
         dk1 = torch.empty(k1.shape, dtype=k1.dtype, device=dev)
         buffers = [torch.empty(q1.shape, dtype=q1.dtype, device=dev), dk1,
                    torch.empty(q2.shape, dtype=q2.dtype, device=dev),
                    dk1 if k2 is k1 else torch.empty(k2.shape, dtype=k2.dtype, device=dev),
                    torch.empty(value.shape, dtype=value.dtype, device=dev),
-                   torch.empty((B, H, T, 2 * D), dtype=q1.dtype, device=dev)]
+                   torch.empty((B, H, T, Dv), dtype=q1.dtype, device=dev)]
     lam_host, lam_dev = _coefficient(coefficient, dev)
     d = make_desc(*buffers[:5], buffers[5])
     lib = _lib.load()
@@ -308,7 +335,8 @@ def differential_attention_backward(q1: torch.Tensor, k1: torch.Tensor, q2: torc
     """Gradients of differential_attention given dout = dL/dO.
 
     Inputs as differential_attention (the forward's inputs and coefficient);
-    dout: [B, H, T, 2D] of the inputs' dtype.  saved: optional (out, out2,
+    dout: [B, H, T, 2D] of the inputs' dtype (the backward takes the
+    operation's own shape, value width 2D).  saved: optional (out, out2,
     lse) from differential_attention_train with the same inputs; with it the
     forward is not recomputed.  Returns (dq1, dk1, dq2, dk2, dvalue,
     dcoefficient): contiguous tensors of the inputs' shapes and dtype, and a
@@ -431,6 +459,7 @@ def make_kv_desc(q1, k1, q2, k2, v, out) -> DiffattnKvDesc:
     B, H, Tq, D = q1.shape
     d = DiffattnKvDesc()
     d.B, d.H, d.Tq, d.Tk, d.D = B, H, Tq, k1.shape[2], D
+    d.Dv = v.shape[-1]
     d.dtype = _DTYPES[q1.dtype]
     d.kv_group = H // k1.shape[1]
     for field, t in (("q1_stride", q1), ("k1_stride", k1), ("q2_stride", q2), ("k2_stride", k2),
@@ -461,11 +490,14 @@ def differential_attention_decode(q1: torch.Tensor, k1: torch.Tensor, q2: torch.
                                   norm_weight: Optional[torch.Tensor] = None,
                                   norm_bias: Optional[torch.Tensor] = None,
                                   out_scale: float = 1.0) -> torch.Tensor:
-    """Decode: Tq new queries q1, q2 [B, H, Tq, D] over cached keys k1, k2
-    [B, H_kv, Tk, D] and values [B, H_kv, Tk, 2D] (H_kv dividing H; query head
-    h reads key/value head h // (H // H_kv)).  With causal=True query i sits
-    at position Tk - Tq + i.  Epilogue arguments as differential_attention.
-    Returns [B, H, Tq, 2D].  (Forward only.)"""
+    """Queries over a key/value cache: Tq new queries q1, q2 [B, H, Tq, D]
+    over cached keys k1, k2 [B, H_kv, Tk, D] and values [B, H_kv, Tk, Dv]
+    (H_kv dividing H; query head h reads key/value head h // (H // H_kv);
+    Dv = 2D is the operation's own shape).  With causal=True query i sits at
+    position Tk - Tq + i.  A few queries (a decode step) run on the split-key
+    decode kernels; more (a chunk of a prefill) on the forward kernels.
+    Epilogue arguments as differential_attention.  Returns [B, H, Tq, Dv].
+    (Forward only.)"""
     ts = [q1, k1, q2, k2, value]
     for n, t in zip(("q1", "k1", "q2", "k2", "value"), ts):
         _require_cuda(t, n)
@@ -474,16 +506,17 @@ def differential_attention_decode(q1: torch.Tensor, k1: torch.Tensor, q2: torch.
     B, H, Tq, D = q1.shape
     Hk, Tk = k1.shape[1], k1.shape[2]
     if q2.shape != q1.shape or k1.shape != k2.shape or tuple(k1.shape) != (B, Hk, Tk, D) or \
-            H % Hk != 0 or tuple(value.shape) != (B, Hk, Tk, 2 * D):
+            H % Hk != 0 or tuple(value.shape[:3]) != (B, Hk, Tk) or not 1 <= value.shape[3] <= 256:
         raise ValueError("expected q1, q2 [B, H, Tq, D], k1, k2 [B, H_kv, Tk, D], "
-                         "value [B, H_kv, Tk, 2D] with H_kv dividing H")
+                         "value [B, H_kv, Tk, Dv] with H_kv dividing H and Dv <= 256")
+    Dv = value.shape[3]
     dt, dev = q1.dtype, q1.device
     if dt not in _DTYPES or any(t.dtype != dt or t.device != dev for t in ts):
         raise ValueError("inputs must share one dtype (bfloat16 or float32) and device")
     ts = [t if t.stride(-1) == 1 else t.contiguous() for t in ts]
     q1, k1, q2, k2, value = ts
     if out is None:
-        out = torch.empty((B, H, Tq, 2 * D), dtype=dt, device=dev)
+        out = torch.empty((B, H, Tq, Dv), dtype=dt, device=dev)
     lam_host, lam_dev = 0.0, None
     if isinstance(coefficient, torch.Tensor):
         if coefficient.device.type == "cuda":
@@ -493,7 +526,7 @@ def differential_attention_decode(q1: torch.Tensor, k1: torch.Tensor, q2: torch.
     else:
         lam_host = float(coefficient)
     d = make_kv_desc(q1, k1, q2, k2, value, out)
-    epi = _epilogue(norm, norm_eps, norm_weight, norm_bias, out_scale, H, 2 * D, dev)
+    epi = _epilogue(norm, norm_eps, norm_weight, norm_bias, out_scale, H, Dv, dev)
     lib = _lib.load()
     need = int(lib.diffattn_decode_workspace_bytes(ctypes.byref(d)))
     if need == 0:
@@ -531,7 +564,7 @@ def _epilogue(norm, eps, weight, bias, out_scale, H, Dv, dev):
             continue
         _require_cuda(t, name)
         if t.device != dev or tuple(t.shape) not in ((H, Dv), (H * Dv,)):
-            raise ValueError(f"{name} must be [H, 2D] = {(H, Dv)} on the inputs' device")
+            raise ValueError(f"{name} must be [H, Dv] = {(H, Dv)} on the inputs' device")
         t = t.detach().to(torch.float32).contiguous()
         keep.append(t)
         ptrs.append(t.data_ptr())

@@ -54,6 +54,7 @@ class DiffattnDesc(ctypes.Structure):
         ("q1_stride", ctypes.c_int64 * 3), ("k1_stride", ctypes.c_int64 * 3),
         ("q2_stride", ctypes.c_int64 * 3), ("k2_stride", ctypes.c_int64 * 3),
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+        ("Dv", ctypes.c_int64),
     ]
 
 
@@ -65,6 +66,7 @@ class DiffattnKvDesc(ctypes.Structure):
         ("q1_stride", ctypes.c_int64 * 3), ("k1_stride", ctypes.c_int64 * 3),
         ("q2_stride", ctypes.c_int64 * 3), ("k2_stride", ctypes.c_int64 * 3),
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+        ("Dv", ctypes.c_int64),
     ]
 
 

@@ -105,10 +105,14 @@ bool same_tensor(const void* a, const int64_t sa[3], const void* b, const int64_
            (T == 1 || sa[2] == sb[2]);
 }
 
+// Value width of a descriptor: 0 means 2D (the operation's own shape).
+int64_t value_width(int64_t Dv, int64_t D) { return Dv == 0 ? 2 * D : Dv; }
+
 int validate(const diffattn_desc* d, const void* q1, const void* k1, const void* q2,
              const void* k2, const void* v, const void* out) {
     if (!d || !q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID;
     if (d->B < 1 || d->H < 1 || d->T < 1 || d->D < 1 || d->D > 128) return DIFFATTN_ERR_INVALID;
+    if (d->Dv < 0 || value_width(d->Dv, d->D) > 256) return DIFFATTN_ERR_INVALID;
     if (d->dtype != DIFFATTN_BF16 && d->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID;
     if (d->kv_group < 0 || d->H % group_of(d->kv_group) != 0) return DIFFATTN_ERR_INVALID;
     if (!strides_nonneg(d->q1_stride) || !strides_nonneg(d->k1_stride) ||
@@ -125,22 +129,23 @@ int validate(const diffattn_desc* d, const void* q1, const void* k1, const void*
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Heads per scheduling group of the tensor-core forward, for L2 locality: the
-// CTAs working at the same time share the K1, K2 and V of one group (512 bytes
-// per key and key/value head in bf16 at D = 64: K1 128, K2 128, V 256).
+// CTAs working at the same time share the K1, K2 and V of one group
+// (kv_bytes per key and key/value head: 512 in bf16 at D = 64 -- K1 128, K2
+// 128, V 256).
 // Causal items have unequal lengths and run longest first within a group;
 // groups of about 64 MiB of keys and values with at least four items per CTA
 // keep both the L2 hit rate and the balance (at B2 H16 T8192 that is 16 heads
 // and 1024 items, ~2% faster than one group of all heads; at B1 H16 T32768,
 // 4 heads, ~3% faster).  Non-causal items are all equally long; their groups
 // take at most ~48 MiB with an item for every SM.
-int head_group(const diffattn_desc& d, int nq, int causal, int num_sms) {
-    const int64_t head_bytes = d.T * 512;
+int head_group(int64_t BH, int64_t Tk, int64_t kv_bytes, int nq, int causal, int num_sms) {
+    const int64_t head_bytes = Tk * kv_bytes;
     const int64_t budget = causal ? (64ll << 20) : (48ll << 20);
     int64_t g = budget / (head_bytes > 0 ? head_bytes : 1);
     const int64_t min_g = causal ? (4ll * num_sms + nq - 1) / nq : ((int64_t)num_sms + nq - 1) / nq;
     if (g < min_g) g = min_g;
     if (g < 1) g = 1;
-    if (g > d.B * d.H) g = d.B * d.H;
+    if (g > BH) g = BH;
     return (int)g;
 }
 
@@ -149,33 +154,50 @@ int head_group(const diffattn_desc& d, int nq, int causal, int num_sms) {
 bool tc_stride_ok(int64_t stride, int64_t size) {
     return size == 1 || (stride > 0 && stride % 8 == 0 && stride < (int64_t(1) << 38));
 }
-bool tc_strides_ok(const int64_t s[3], const diffattn_desc* d, int64_t heads) {
-    return tc_stride_ok(s[0], d->B) && tc_stride_ok(s[1], heads) && tc_stride_ok(s[2], d->T);
+bool tc_strides_ok(const int64_t s[3], int64_t B, int64_t heads, int64_t T) {
+    return tc_stride_ok(s[0], B) && tc_stride_ok(s[1], heads) && tc_stride_ok(s[2], T);
+}
+
+// Shapes the tensor-core kernel takes: bf16, value width 128, Q/K width 64 (the
+// operation's V = 2D) or 128 (the DIFF V2 head, V as wide as Q and K).
+bool tc_shape(int32_t dtype, int64_t D, int64_t Dv) {
+    return dtype == DIFFATTN_BF16 && Dv == 128 && (D == 64 || D == 128);
+}
+
+// The tensor-core kernel for Tq query rows over Tk keys (queries and the
+// output with Tq rows, K1, K2 and V with Tk rows).
+bool tc_ok(int32_t dtype, int64_t B, int64_t H, int64_t Hk, int64_t Tq, int64_t Tk, int64_t D,
+           int64_t Dv, const int64_t* sq1, const int64_t* sk1, const int64_t* sq2,
+           const int64_t* sk2, const int64_t* sv, const int64_t* so, const void* q1,
+           const void* k1, const void* q2, const void* k2, const void* v, const void* out) {
+    return tc_shape(dtype, D, Dv) && aligned16(q1) && aligned16(k1) && aligned16(q2) &&
+           aligned16(k2) && aligned16(v) && aligned16(out) && tc_strides_ok(sq1, B, H, Tq) &&
+           tc_strides_ok(sk1, B, Hk, Tk) && tc_strides_ok(sq2, B, H, Tq) &&
+           tc_strides_ok(sk2, B, Hk, Tk) && tc_strides_ok(sv, B, Hk, Tk) &&
+           tc_strides_ok(so, B, H, Tq);
 }
 
 int select(const diffattn_desc* d, const void* q1, const void* k1, const void* q2,
            const void* k2, const void* v, const void* out) {
     const int64_t hk = d->H / group_of(d->kv_group);
-    if (d->dtype == DIFFATTN_BF16 && d->D == 64 && aligned16(q1) && aligned16(k1) &&
-        aligned16(q2) && aligned16(k2) && aligned16(v) && aligned16(out) &&
-        tc_strides_ok(d->q1_stride, d, d->H) && tc_strides_ok(d->k1_stride, d, hk) &&
-        tc_strides_ok(d->q2_stride, d, d->H) && tc_strides_ok(d->k2_stride, d, hk) &&
-        tc_strides_ok(d->v_stride, d, hk) && tc_strides_ok(d->o_stride, d, d->H))
-        return DIFFATTN_KERNEL_TCGEN05;
-    return DIFFATTN_KERNEL_SIMT;
+    return tc_ok(d->dtype, d->B, d->H, hk, d->T, d->T, d->D, value_width(d->Dv, d->D), d->q1_stride,
+                 d->k1_stride, d->q2_stride, d->k2_stride, d->v_stride, d->o_stride, q1, k1, q2,
+                 k2, v, out)
+               ? DIFFATTN_KERNEL_TCGEN05
+               : DIFFATTN_KERNEL_SIMT;
 }
 
 // 4-D bf16 tensor map {inner, T, heads, B} with a {box_inner, box_rows, 1, 1}
 // box and 128-byte swizzling; rows past T read as zeros.
-int encode_map(CUtensorMap* m, const void* base, int64_t inner, const diffattn_desc* d,
-               int64_t heads, const int64_t s[3], uint32_t box_inner, uint32_t box_rows) {
+int encode_map_t(CUtensorMap* m, const void* base, int64_t inner, int64_t B, int64_t T,
+                 int64_t heads, const int64_t s[3], uint32_t box_inner, uint32_t box_rows) {
     int64_t sT = s[2], sH = s[1], sB = s[0];
     // A size-1 dimension is never stepped; give it a stride the encoder accepts.
-    if (d->T == 1) sT = inner;
-    if (heads == 1) sH = sT * d->T;
-    if (d->B == 1) sB = sH * heads;
-    const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)d->T, (cuuint64_t)heads,
-                                (cuuint64_t)d->B};
+    if (T == 1) sT = inner;
+    if (heads == 1) sH = sT * T;
+    if (B == 1) sB = sH * heads;
+    const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)T, (cuuint64_t)heads,
+                                (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)sT * 2, (cuuint64_t)sH * 2, (cuuint64_t)sB * 2};
     const cuuint32_t box[4] = {box_inner, box_rows, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -184,6 +206,11 @@ int encode_map(CUtensorMap* m, const void* base, int64_t inner, const diffattn_d
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+int encode_map(CUtensorMap* m, const void* base, int64_t inner, const diffattn_desc* d,
+               int64_t heads, const int64_t s[3], uint32_t box_inner, uint32_t box_rows) {
+    return encode_map_t(m, base, inner, d->B, d->T, heads, s, box_inner, box_rows);
 }
 
 void copy3(int64_t dst[3], const int64_t src[3]) {
@@ -198,21 +225,39 @@ struct DecodePlan {
     int tq_bucket = 0, splits = 0, split_len = 0;
     int kv_group = 1, Hk = 0, row_chunks = 0;
     size_t work_bytes = 0;
+    // The queries go through the forward kernels instead (more query rows than
+    // the split-key decode takes, or a value width other than 2D).
+    bool forward = false;
 };
+
+// Bytes a call asks for when it runs on the forward kernels: none are used,
+// but the workspace contract (a non-zero size for a valid request) holds.
+constexpr size_t kForwardPathWorkBytes = 16;
 
 int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
     if (!d) return DIFFATTN_ERR_INVALID;
     if (d->B < 1 || d->H < 1 || d->Tq < 1 || d->Tk < 1 || d->D < 1) return DIFFATTN_ERR_INVALID;
     if (d->dtype != DIFFATTN_BF16 && d->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID;
     if (d->kv_group < 0 || d->H % group_of(d->kv_group) != 0) return DIFFATTN_ERR_INVALID;
+    if (d->Dv < 0 || d->D > 128 || value_width(d->Dv, d->D) > 256) return DIFFATTN_ERR_INVALID;
     if (!strides_nonneg(d->q1_stride) || !strides_nonneg(d->k1_stride) ||
         !strides_nonneg(d->q2_stride) || !strides_nonneg(d->k2_stride) ||
         !strides_nonneg(d->v_stride) || !strides_nonneg(d->o_stride))
         return DIFFATTN_ERR_INVALID;
     if (causal && d->Tk < d->Tq) return DIFFATTN_ERR_INVALID;
-    if (d->D != 32 && d->D != 64 && d->D != 128) return DIFFATTN_ERR_UNSUPPORTED;
-    const int cap = decode_max_rows((int)d->D);
-    if (d->Tk > INT32_MAX / 2 || d->Tq > cap || d->H > (1 << 24)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (d->Tk > INT32_MAX / 2 || d->Tq > INT32_MAX / 2 || d->H > (1 << 24))
+        return DIFFATTN_ERR_UNSUPPORTED;
+    const int cap = (d->D == 32 || d->D == 64 || d->D == 128) ? decode_max_rows((int)d->D) : 0;
+    if (d->Tq > cap || value_width(d->Dv, d->D) != 2 * d->D) {
+        // queries over the cache on the forward kernels (chunked prefill)
+        const int64_t nq = (d->Tq + 127) / 128;
+        if (d->B * d->H > INT32_MAX / nq) return DIFFATTN_ERR_UNSUPPORTED;
+        plan->forward = true;
+        plan->kv_group = (int)group_of(d->kv_group);
+        plan->Hk = (int)(d->H / plan->kv_group);
+        plan->work_bytes = kForwardPathWorkBytes;
+        return DIFFATTN_OK;
+    }
     // The query rows of the heads that share a key/value head (g * Tq of
     // them) go in as few CTAs as the row capacity allows, evenly filled.
     const int64_t g = group_of(d->kv_group);
@@ -338,64 +383,71 @@ int diffattn_fwd_train(const diffattn_desc* desc, const void* q1, const void* k1
 namespace diffattn {
 namespace {
 
-// The forward, optionally with the training outputs (out2 = A_2 V with the
-// output's strides, lse = [B, H, T, 2] natural-log log-sum-exp per branch).
-int forward_impl(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
-                 const void* k2, const void* v, float lambda, const float* lambda_dev, int causal,
-                 const diffattn_epilogue* epi, void* out, void* out2, float* lse,
-                 void* workspace, size_t workspace_bytes, diffattn_stream_t stream) {
-    int rc = validate(desc, q1, k1, q2, k2, v, out);
-    if (rc != DIFFATTN_OK) return rc;
-    diffattn_epilogue e{DIFFATTN_NORM_NONE, 0.f, nullptr, nullptr, 1.0f, 0};
-    if (epi) {
-        e = *epi;
-        if (e.reserved != 0 || e.norm < DIFFATTN_NORM_NONE || e.norm > DIFFATTN_NORM_GROUP ||
-            !std::isfinite(e.out_scale) ||
-            (e.norm != DIFFATTN_NORM_NONE && !(std::isfinite(e.eps) && e.eps > 0.f)))
-            return DIFFATTN_ERR_INVALID;
-    }
-    if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
-    if (workspace && (workspace_bytes < kWorkspaceBytes ||
-                      (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0))
-        return DIFFATTN_ERR_INVALID;
-    const diffattn_desc& d = *desc;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    DeviceState* dev = nullptr;
-    rc = device_state(&dev);
-    if (rc != DIFFATTN_OK) return rc;
+// Shape and layout of one forward launch: Tq query rows over Tk keys, query
+// row i at key position i + kv_off (causal mask: keys j > i + kv_off hidden).
+struct FwdShape {
+    int64_t B, H, Hk, Tq, Tk, D, Dv, kv_off;
+    int32_t dtype;
+    const int64_t *sq1, *sk1, *sq2, *sk2, *sv, *so;
+};
 
-    if (select(desc, q1, k1, q2, k2, v, out) == DIFFATTN_KERNEL_TCGEN05 &&
+int check_epilogue(const diffattn_epilogue* epi, diffattn_epilogue* e) {
+    *e = diffattn_epilogue{DIFFATTN_NORM_NONE, 0.f, nullptr, nullptr, 1.0f, 0};
+    if (!epi) return DIFFATTN_OK;
+    *e = *epi;
+    if (e->reserved != 0 || e->norm < DIFFATTN_NORM_NONE || e->norm > DIFFATTN_NORM_GROUP ||
+        !std::isfinite(e->out_scale) ||
+        (e->norm != DIFFATTN_NORM_NONE && !(std::isfinite(e->eps) && e->eps > 0.f)))
+        return DIFFATTN_ERR_INVALID;
+    return DIFFATTN_OK;
+}
+
+// One forward launch (arguments already checked): the tensor-core kernel when
+// the shape, pointers and strides allow it, else the CUDA-core kernel.
+int launch_forward(const FwdShape& f, const void* q1, const void* k1, const void* q2,
+                   const void* k2, const void* v, float lambda, const float* lambda_dev,
+                   int causal, const diffattn_epilogue& e, void* out, void* out2, float* lse,
+                   void* workspace, cudaStream_t st) {
+    DeviceState* dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != DIFFATTN_OK) return rc;
+    const int64_t g = f.H / f.Hk;
+    if (tc_ok(f.dtype, f.B, f.H, f.Hk, f.Tq, f.Tk, f.D, f.Dv, f.sq1, f.sk1, f.sq2, f.sk2, f.sv, f.so,
+              q1, k1, q2, k2, v, out) &&
         (!out2 || aligned16(out2))) {
         CUtensorMap maps[6];
-        const int64_t g = group_of(d.kv_group);
-        const int64_t hk = d.H / g;
         // Q tiles are 128 query rows; K and V tiles are 64 key rows; every box
-        // is 64 elements (128 bytes) wide, the 128-byte swizzle span.  O is
-        // stored by each warp in 32-row x 64-column boxes.  K1, K2 and V have
-        // H / kv_group heads.
-        if (encode_map(&maps[0], q1, 64, &d, d.H, d.q1_stride, 64, 128) != DIFFATTN_OK ||
-            encode_map(&maps[1], k1, 64, &d, hk, d.k1_stride, 64, 64) != DIFFATTN_OK ||
-            encode_map(&maps[2], q2, 64, &d, d.H, d.q2_stride, 64, 128) != DIFFATTN_OK ||
-            encode_map(&maps[3], k2, 64, &d, hk, d.k2_stride, 64, 64) != DIFFATTN_OK ||
-            encode_map(&maps[4], v, 128, &d, hk, d.v_stride, 64, 64) != DIFFATTN_OK ||
-            encode_map(&maps[5], out, 128, &d, d.H, d.o_stride, 64, 32) != DIFFATTN_OK)
+        // is 64 elements (128 bytes) wide, the 128-byte swizzle span (Q and K
+        // rows of width 128 take two boxes).  O is stored by each warp in
+        // 32-row x 64-column boxes.  K1, K2 and V have H / kv_group heads.
+        if (encode_map_t(&maps[0], q1, f.D, f.B, f.Tq, f.H, f.sq1, 64, 128) != DIFFATTN_OK ||
+            encode_map_t(&maps[1], k1, f.D, f.B, f.Tk, f.Hk, f.sk1, 64, 64) != DIFFATTN_OK ||
+            encode_map_t(&maps[2], q2, f.D, f.B, f.Tq, f.H, f.sq2, 64, 128) != DIFFATTN_OK ||
+            encode_map_t(&maps[3], k2, f.D, f.B, f.Tk, f.Hk, f.sk2, 64, 64) != DIFFATTN_OK ||
+            encode_map_t(&maps[4], v, 128, f.B, f.Tk, f.Hk, f.sv, 64, 64) != DIFFATTN_OK ||
+            encode_map_t(&maps[5], out, 128, f.B, f.Tq, f.H, f.so, 64, 32) != DIFFATTN_OK)
             return DIFFATTN_ERR_CUDA;
+        const bool k_shared = same_tensor(k1, f.sk1, k2, f.sk2, f.B, f.Hk, f.Tk);
         TcParams p{};
-        p.B = (int)d.B;
-        p.H = (int)d.H;
-        p.T = (int)d.T;
-        p.nq = (int)((d.T + 127) / 128);
-        p.nk = (int)((d.T + 63) / 64);
-        p.total_items = (int)(d.B * d.H * p.nq);
-        p.group = head_group(d, p.nq, causal, dev->num_sms);
+        p.B = (int)f.B;
+        p.H = (int)f.H;
+        p.T = (int)f.Tq;
+        p.Tk = (int)f.Tk;
+        p.kv_off = causal ? (int)f.kv_off : 0;
+        p.nq = (int)((f.Tq + 127) / 128);
+        p.nk = (int)((f.Tk + 63) / 64);
+        p.total_items = (int)(f.B * f.H * p.nq);
+        // key/value bytes per key and key/value head, for the L2 grouping
+        const int64_t kv_bytes = ((k_shared ? 1 : 2) * f.D + f.Dv) * 2;
+        p.group = head_group(f.B * f.H, f.Tk, kv_bytes, p.nq, causal, dev->num_sms);
         p.causal = causal ? 1 : 0;
-        p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.D));
+        p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)f.D));
         p.lambda = lambda;
         p.lambda_dev = lambda_dev;
         p.out = static_cast<__nv_bfloat16*>(out);
-        p.o_sB = d.o_stride[0];
-        p.o_sH = d.o_stride[1];
-        p.o_sT = d.o_stride[2];
+        p.o_sB = f.so[0];
+        p.o_sH = f.so[1];
+        p.o_sT = f.so[2];
         p.status = dev->status;
         p.sched = static_cast<uint32_t*>(workspace);
         p.norm = e.norm;
@@ -404,20 +456,23 @@ int forward_impl(const diffattn_desc* desc, const void* q1, const void* k1, cons
         p.norm_bias = e.bias;
         p.out_scale = e.out_scale;
         p.kv_group = (int)g;
-        p.k_shared = same_tensor(k1, d.k1_stride, k2, d.k2_stride, d.B, hk, d.T) ? 1 : 0;
+        p.k_shared = k_shared ? 1 : 0;
         p.out2 = static_cast<__nv_bfloat16*>(out2);
         p.lse = lse;
         const int grid = p.total_items < dev->num_sms ? p.total_items : dev->num_sms;
-        return launch_fwd_tc(maps, p, grid, st) == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+        return launch_fwd_tc(maps, p, (int)f.D, grid, st) == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
     }
 
     SimtParams p{};
-    p.B = (int)d.B;
-    p.H = (int)d.H;
-    p.T = (int)d.T;
-    p.D = (int)d.D;
+    p.B = (int)f.B;
+    p.H = (int)f.H;
+    p.T = (int)f.Tq;
+    p.D = (int)f.D;
+    p.Tk = (int)f.Tk;
+    p.kv_off = causal ? (int)f.kv_off : 0;
+    p.Dv = (int)f.Dv;
     p.causal = causal ? 1 : 0;
-    p.scale = (float)(1.0 / std::sqrt((double)d.D));
+    p.scale = (float)(1.0 / std::sqrt((double)f.D));
     p.lambda = lambda;
     p.lambda_dev = lambda_dev;
     p.q1 = q1;
@@ -426,22 +481,45 @@ int forward_impl(const diffattn_desc* desc, const void* q1, const void* k1, cons
     p.k2 = k2;
     p.v = v;
     p.out = out;
-    copy3(p.s_q1, d.q1_stride);
-    copy3(p.s_k1, d.k1_stride);
-    copy3(p.s_q2, d.q2_stride);
-    copy3(p.s_k2, d.k2_stride);
-    copy3(p.s_v, d.v_stride);
-    copy3(p.s_o, d.o_stride);
+    copy3(p.s_q1, f.sq1);
+    copy3(p.s_k1, f.sk1);
+    copy3(p.s_q2, f.sq2);
+    copy3(p.s_k2, f.sk2);
+    copy3(p.s_v, f.sv);
+    copy3(p.s_o, f.so);
     p.norm = e.norm;
     p.norm_eps = e.eps;
     p.norm_weight = e.weight;
     p.norm_bias = e.bias;
     p.out_scale = e.out_scale;
-    p.kv_group = (int)group_of(d.kv_group);
+    p.kv_group = (int)g;
     p.out2 = out2;
     p.lse = lse;
-    rc = (d.dtype == DIFFATTN_F32) ? launch_fwd_simt_f32(p, st) : launch_fwd_simt_bf16(p, st);
+    rc = (f.dtype == DIFFATTN_F32) ? launch_fwd_simt_f32(p, st) : launch_fwd_simt_bf16(p, st);
     return rc == 0 ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+// The forward, optionally with the training outputs (out2 = A_2 V with the
+// output's strides, lse = [B, H, T, 2] natural-log log-sum-exp per branch).
+int forward_impl(const diffattn_desc* desc, const void* q1, const void* k1, const void* q2,
+                 const void* k2, const void* v, float lambda, const float* lambda_dev, int causal,
+                 const diffattn_epilogue* epi, void* out, void* out2, float* lse,
+                 void* workspace, size_t workspace_bytes, diffattn_stream_t stream) {
+    int rc = validate(desc, q1, k1, q2, k2, v, out);
+    if (rc != DIFFATTN_OK) return rc;
+    diffattn_epilogue e;
+    rc = check_epilogue(epi, &e);
+    if (rc != DIFFATTN_OK) return rc;
+    if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
+    if (workspace && (workspace_bytes < kWorkspaceBytes ||
+                      (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0))
+        return DIFFATTN_ERR_INVALID;
+    const diffattn_desc& d = *desc;
+    const FwdShape f{d.B, d.H, d.H / group_of(d.kv_group), d.T, d.T, d.D, value_width(d.Dv, d.D), 0,
+                     d.dtype, d.q1_stride, d.k1_stride, d.q2_stride, d.k2_stride, d.v_stride,
+                     d.o_stride};
+    return launch_forward(f, q1, k1, q2, k2, v, lambda, lambda_dev, causal, e, out, out2, lse,
+                          workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -494,6 +572,8 @@ int backward_impl(const diffattn_desc* desc, const void* q1, const void* k1, con
     const bool saved = out != nullptr;
     int rc = validate(desc, q1, k1, q2, k2, v, dout);
     if (rc != DIFFATTN_OK) return rc;
+    // the backward kernels take the operation's own shape, V = 2D
+    if (value_width(desc->Dv, desc->D) != 2 * desc->D) return DIFFATTN_ERR_UNSUPPORTED;
     if (!dq1 || !dk1 || !dq2 || !dk2 || !dv || !dlambda) return DIFFATTN_ERR_INVALID;
     if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
     const size_t need = diffattn_bwd_workspace_bytes(desc);
@@ -501,7 +581,7 @@ int backward_impl(const diffattn_desc* desc, const void* q1, const void* k1, con
         return DIFFATTN_ERR_INVALID;
     const diffattn_desc& d = *desc;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (select(desc, q1, k1, q2, k2, v, dout) == DIFFATTN_KERNEL_TCGEN05 && aligned16(dq1) &&
+    if (d.D == 64 && select(desc, q1, k1, q2, k2, v, dout) == DIFFATTN_KERNEL_TCGEN05 && aligned16(dq1) &&
         aligned16(dk1) && aligned16(dq2) && aligned16(dk2) && aligned16(dv)) {
         DeviceState* dev = nullptr;
         rc = device_state(&dev);
@@ -541,10 +621,12 @@ int backward_impl(const diffattn_desc* desc, const void* q1, const void* k1, con
         f.B = (int)d.B;
         f.H = (int)d.H;
         f.T = (int)d.T;
+        f.Tk = (int)d.T;
+        f.kv_off = 0;
         f.nq = (int)((d.T + 127) / 128);
         f.nk = (int)((d.T + 63) / 64);
         f.total_items = (int)(d.B * d.H * f.nq);
-        f.group = head_group(d, f.nq, causal, dev->num_sms);
+        f.group = head_group(d.B * d.H, d.T, 512, f.nq, causal, dev->num_sms);
         f.causal = causal ? 1 : 0;
         f.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.D));
         f.lambda = 0.f;
@@ -565,7 +647,7 @@ int backward_impl(const diffattn_desc* desc, const void* q1, const void* k1, con
         f.do_sH = d.o_stride[1];
         f.do_sT = d.o_stride[2];
         const int fgrid = f.total_items < dev->num_sms ? f.total_items : dev->num_sms;
-        if (launch_fwd_tc(fmaps, f, fgrid, st) != 0) return DIFFATTN_ERR_CUDA;
+        if (launch_fwd_tc(fmaps, f, 64, fgrid, st) != 0) return DIFFATTN_ERR_CUDA;
         }
         // Pass 2: dQ, then dK and dV, on the tensor cores.
         CUtensorMap maps[12];
@@ -694,14 +776,9 @@ int decode_args(const diffattn_kv_desc* desc, const void* q1, const void* k1, co
     int rc = plan_decode(desc, causal, plan);
     if (rc != DIFFATTN_OK) return rc;
     if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
-    *e = diffattn_epilogue{DIFFATTN_NORM_NONE, 0.f, nullptr, nullptr, 1.0f, 0};
-    if (epi) {
-        *e = *epi;
-        if (e->reserved != 0 || e->norm < DIFFATTN_NORM_NONE || e->norm > DIFFATTN_NORM_GROUP ||
-            !std::isfinite(e->out_scale) ||
-            (e->norm != DIFFATTN_NORM_NONE && !(std::isfinite(e->eps) && e->eps > 0.f)))
-            return DIFFATTN_ERR_INVALID;
-    }
+    rc = check_epilogue(epi, e);
+    if (rc != DIFFATTN_OK) return rc;
+    if (plan->forward) return DIFFATTN_OK;   // the forward kernels take any alignment
     const size_t esize = desc->dtype == DIFFATTN_BF16 ? 2 : 4;
     if (!kv_aligned(k1, desc->k1_stride, esize) || !kv_aligned(k2, desc->k2_stride, esize) ||
         !kv_aligned(v, desc->v_stride, esize))
@@ -737,6 +814,15 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
         (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
         return DIFFATTN_ERR_INVALID;
     const diffattn_kv_desc& d = *desc;
+    if (plan.forward) {
+        // Tq query rows at the end of the Tk-key sequence: query i at key
+        // position Tk - Tq + i; one forward launch with the static schedule
+        const FwdShape f{d.B, d.H, plan.Hk, d.Tq, d.Tk, d.D, value_width(d.Dv, d.D), d.Tk - d.Tq,
+                         d.dtype, d.q1_stride, d.k1_stride, d.q2_stride, d.k2_stride, d.v_stride,
+                         d.o_stride};
+        return launch_forward(f, q1, k1, q2, k2, v, lambda, lambda_dev, causal, e, out, nullptr,
+                              nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+    }
     const size_t esize = d.dtype == DIFFATTN_BF16 ? 2 : 4;
     DecodeParams p{};
     p.B = (int)d.B;
@@ -861,9 +947,10 @@ int diffattn_fwd_host(const diffattn_desc* desc, const void* q1_host, const void
     const diffattn_desc& d = *desc;
     const int64_t g = group_of(d.kv_group);
     const int64_t hk = d.H / g;
+    const int64_t dv = value_width(d.Dv, d.D);
     if (!dense(d.q1_stride, d, d.H, d.D) || !dense(d.q2_stride, d, d.H, d.D) ||
         !dense(d.k1_stride, d, hk, d.D) || !dense(d.k2_stride, d, hk, d.D) ||
-        !dense(d.v_stride, d, hk, 2 * d.D) || !dense(d.o_stride, d, d.H, 2 * d.D))
+        !dense(d.v_stride, d, hk, dv) || !dense(d.o_stride, d, d.H, dv))
         return DIFFATTN_ERR_INVALID;
     DeviceState* dev = nullptr;
     rc = device_state(&dev);
@@ -886,7 +973,7 @@ int diffattn_fwd_host(const diffattn_desc* desc, const void* q1_host, const void
     if (chunks < 1) chunks = 1;
     const bool k_same = k1_host == k2_host && k1 == k2;
     const int64_t qrow = d.T * d.D * (int64_t)es;        // bytes of one query head of Q1 / Q2
-    const int64_t orow = d.T * 2 * d.D * (int64_t)es;    // of O and of V per head
+    const int64_t orow = d.T * dv * (int64_t)es;         // of O and of V per head
     auto copy = [&](void* dst, const void* src, int64_t off, int64_t bytes, cudaMemcpyKind kind,
                     cudaStream_t s) {
         return cudaMemcpyAsync(static_cast<char*>(dst) + off, static_cast<const char*>(src) + off,
@@ -968,6 +1055,6 @@ const char* diffattn_strerror(int code) {
     }
 }
 
-int diffattn_version(void) { return 100; }
+int diffattn_version(void) { return 200; }
 
 }  // extern "C"

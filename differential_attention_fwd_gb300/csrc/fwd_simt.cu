@@ -5,12 +5,13 @@
 //
 // The general path: fp32 inputs (exact fp32 arithmetic, expf), and bf16
 // inputs of any shape the tensor-core kernel does not take (D != 64,
-// unaligned strides).  One warp owns one query row.  Keys are visited in
-// chunks of 32, one key per lane for the two dot products; each branch keeps
-// a streaming-softmax state (running max, running sum) and its own output
-// accumulator, each lane holding the output columns lane, lane+32, ...
-// Masked keys (causal: key > query) are skipped.  With grouped key/value
-// heads, query head h reads key/value head h / kv_group.
+// unaligned strides, a value width other than the tensor-core kernel's).  One
+// warp owns one query row.  Keys are visited in chunks of 32, one key per lane
+// for the two dot products; each branch keeps a streaming-softmax state
+// (running max, running sum) and its own output accumulator, each lane holding
+// the output columns lane, lane+32, ...  Masked keys (causal: key > query +
+// kv_off) are skipped.  With grouped key/value heads, query head h reads
+// key/value head h / kv_group.
 #include "kernels.h"
 
 #include <cmath>
@@ -20,7 +21,7 @@ namespace simt {
 
 constexpr int WARPS = 4;          // query rows per block
 constexpr int MAX_D = 128;
-constexpr int MAX_DV = 2 * MAX_D;
+constexpr int MAX_DV = 256;
 constexpr int OPL = MAX_DV / 32;  // output columns per lane
 
 __device__ __forceinline__ float load(const float* p, int64_t i) { return p[i]; }
@@ -65,7 +66,7 @@ diffattn_fwd_simt_kernel(const SimtParams p) {
     const T* v = static_cast<const T*>(p.v) + b * p.s_v[0] + hk * p.s_v[1];
     T* out = static_cast<T*>(p.out) + b * p.s_o[0] + h * p.s_o[1] + (int64_t)i * p.s_o[2];
     const int D = p.D;
-    const int Dv = 2 * D;
+    const int Dv = p.Dv;
 
     for (int d = lane; d < D; d += 32) {
         qs[warp][0][d] = load(q1, (int64_t)i * p.s_q1[2] + d);
@@ -78,7 +79,8 @@ diffattn_fwd_simt_kernel(const SimtParams p) {
 #pragma unroll
     for (int r = 0; r < OPL; ++r) o1[r] = o2[r] = 0.f;
 
-    const int kend = p.causal ? i + 1 : p.T;   // keys [0, kend) are visible
+    // keys [0, kend) are visible; the causal offset keeps kend >= 1
+    const int kend = p.causal ? min(i + p.kv_off + 1, p.Tk) : p.Tk;
     for (int k0 = 0; k0 < kend; k0 += 32) {
         const int key = k0 + lane;
         const bool valid = key < kend;

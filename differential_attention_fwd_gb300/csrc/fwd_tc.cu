@@ -3,7 +3,14 @@
 // Computes O = (softmax(Q1 K1^T / sqrt(D) + M) - lambda softmax(Q2 K2^T / sqrt(D) + M)) V
 // (paperleet "Differential Transformer Attention", Formula and conventions;
 // aifetchly "Differential Transformer...", section 1) for bf16 inputs with
-// D = 64 and V width 128, fp32 accumulation, bf16 output.
+// V width 128 and Q/K width D = 64 (the operation's own shape, V = 2D) or
+// D = 128 (the DIFF V2 head of the aiengineeringfromscratch lesson, "V1 contre
+// V2": the head dimension stays that of the baseline, so V is as wide as Q and
+// K), fp32 accumulation, bf16 output.
+//
+// Queries and keys may be sequences of different lengths (queries over a
+// key/value cache): query row i sits at key position i + kv_off, and the
+// causal mask hides keys j > i + kv_off.
 //
 // One CTA per SM (persistent).  A work item is (batch b, head h, 128-query
 // tile).  Per item the CTA loads Q1/Q2 once and streams (K1, K2) and V tiles
@@ -29,7 +36,13 @@
 // warpgroup gives registers back (104 per thread) and the two softmax
 // warpgroups take them (200 per thread): 256 x 200 + 128 x 104 = 64512.
 // TMEM columns: S1 buffers [0,64) [64,128), S2 buffers [128,192) [192,256),
-// O1 [256,384), O2 [384,512).
+// O1 [256,384), O2 [384,512) (the same at D = 64 and D = 128: only the depth of
+// the score products changes).
+//
+// Shared memory holds Q and K rows as 64-column panels of 128 bytes per row
+// (the 128-byte swizzle span): one panel at D = 64, two at D = 128.  The key
+// ring has 5 stages of (K1, K2) at D = 64; at D = 128 it has 2 such stages, or
+// 4 stages of one shared key tile when the branches share their keys.
 //
 // Tensor-core order per branch b (its own issuing thread, executed in order):
 //   S_b(0), S_b(1), then for each tile j: PV_b(j), S_b(j+2) into the buffer
@@ -59,36 +72,55 @@ namespace tc {
 
 constexpr int BM = 128;            // query rows per tile (= TMEM lanes)
 constexpr int BN = 64;             // keys per KV tile
-constexpr int HD = 64;             // Q/K width D
-constexpr int VD = 128;            // V/O width 2D
-constexpr int KSTAGES = 5;         // (K1, K2) ring depth
-constexpr int VSTAGES = 4;         // V ring depth
+constexpr int VD = 128;            // V/O width
+constexpr int KSTAGES = 5;         // key ring stages allocated (barriers)
 constexpr int NUM_THREADS = 384;
 constexpr uint32_t REGS_SOFTMAX = 200;
 constexpr uint32_t REGS_OTHER = 104;
 static_assert(256 * REGS_SOFTMAX + 128 * REGS_OTHER <= NUM_THREADS * 168, "register split");
 
-constexpr uint32_t Q_BYTES = BM * HD * 2;        // 16 KB per branch
-constexpr uint32_t K_BYTES = BN * HD * 2;        // 8 KB per branch
+constexpr uint32_t Q_PANEL = BM * 64 * 2;        // 16 KB: 128 query rows x 64 columns
+constexpr uint32_t K_PANEL = BN * 64 * 2;        // 8 KB: 64 key rows x 64 columns
 constexpr uint32_t V_HALF_BYTES = BN * 64 * 2;   // 8 KB per 64-column half
 constexpr uint32_t V_BYTES = 2 * V_HALF_BYTES;   // 16 KB
+constexpr uint32_t OUT_BYTES = BM * VD * 2;      // 32 KB
 
-// Shared-memory layout (offsets from a 1024-byte aligned base).
-constexpr uint32_t OFF_Q1 = 0;
-constexpr uint32_t OFF_Q2 = OFF_Q1 + Q_BYTES;
-constexpr uint32_t OFF_K = OFF_Q2 + Q_BYTES;                    // stage s: K1 at +0, K2 at +K_BYTES
-constexpr uint32_t OFF_V = OFF_K + KSTAGES * 2 * K_BYTES;       // stage s: cols 0-63 at +0, 64-127 at +V_HALF
-constexpr uint32_t OFF_OUT = OFF_V + VSTAGES * V_BYTES;          // output staging: [branch][warp] 32 rows x 128 B
-constexpr uint32_t OUT_BYTES = BM * VD * 2;                      // 32 KB
-constexpr uint32_t OFF_BAR = OFF_OUT + OUT_BYTES;
+// Shared-memory layout for Q/K width HD (offsets from a 1024-byte aligned
+// base).  Q1, Q2: PANELS panels each; the key ring: K_RING bytes; the value
+// ring: VSTAGES stages (cols 0-63 at +0, 64-127 at +V_HALF_BYTES); the output
+// staging: [branch][warp] 32 rows x 128 bytes.
+template <int HD>
+struct Cfg {
+    static_assert(HD == 64 || HD == 128, "Q/K width");
+    static constexpr int PANELS = HD / 64;
+    static constexpr uint32_t Q_BYTES = BM * HD * 2;       // per branch
+    static constexpr uint32_t K_BYTES = BN * HD * 2;       // one branch's key tile
+    static constexpr uint32_t K_RING = HD == 64 ? KSTAGES * 2 * K_BYTES : 4 * K_BYTES;
+    static constexpr int VSTAGES = HD == 64 ? 4 : 3;
+    static constexpr uint32_t OFF_Q1 = 0;
+    static constexpr uint32_t OFF_Q2 = OFF_Q1 + Q_BYTES;
+    static constexpr uint32_t OFF_K = OFF_Q2 + Q_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + K_RING;
+    static constexpr uint32_t OFF_OUT = OFF_V + VSTAGES * V_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_OUT + OUT_BYTES;
+    // key ring: stages and the byte stride between them (one key tile per
+    // branch, or one shared by both)
+    __device__ __forceinline__ static int kstages(bool shared) {
+        return HD == 64 ? KSTAGES : (shared ? 4 : 2);
+    }
+    __device__ __forceinline__ static uint32_t kstride(bool shared) {
+        return (HD == 128 && shared) ? K_BYTES : 2 * K_BYTES;
+    }
+};
+constexpr int VSTAGES_MAX = 4;
 // barriers
 constexpr int BAR_Q_FULL = 0;
 constexpr int BAR_Q_EMPTY = 1;
 constexpr int BAR_K_FULL = 2;
 constexpr int BAR_K_EMPTY = BAR_K_FULL + KSTAGES;
 constexpr int BAR_V_FULL = BAR_K_EMPTY + KSTAGES;
-constexpr int BAR_V_EMPTY = BAR_V_FULL + VSTAGES;
-constexpr int BAR_S_FULL = BAR_V_EMPTY + VSTAGES;      // [branch][buffer]
+constexpr int BAR_V_EMPTY = BAR_V_FULL + VSTAGES_MAX;
+constexpr int BAR_S_FULL = BAR_V_EMPTY + VSTAGES_MAX;  // [branch][buffer]
 constexpr int BAR_P_FULL = BAR_S_FULL + 4;             // [branch][buffer]
 constexpr int BAR_PV_DONE = BAR_P_FULL + 4;            // [branch]
 constexpr int BAR_O_FULL = BAR_PV_DONE + 2;
@@ -102,19 +134,21 @@ constexpr int NUM_ITEM_CONSUMERS = 10;                  // 2 MMA warps + 8 softm
 constexpr int BAR_NORM_A = BAR_ITEM_EMPTY + ITEM_RING;  // per-row partial sums of both halves
 constexpr int BAR_NORM_B = BAR_NORM_A + 1;              // per-row partial squared deviations
 constexpr int NUM_BARS = BAR_NORM_B + 1;
-constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
-constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
-constexpr uint32_t OFF_INVL = (OFF_ABORT + 4 + 15) & ~15u;    // float [2][128]
-constexpr uint32_t OFF_RING = OFF_INVL + 2 * BM * 4;            // int [ITEM_RING]
-constexpr uint32_t OFF_STAT = OFF_RING + ITEM_RING * 4;         // float [2 stats][2 halves][128]
-constexpr uint32_t SMEM_USED = OFF_STAT + 2 * 2 * BM * 4;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;               // + alignment slack
+// small state after the barriers (offsets from OFF_BAR)
+constexpr uint32_t REL_TMEM_PTR = NUM_BARS * 8;
+constexpr uint32_t REL_ABORT = REL_TMEM_PTR + 4;
+constexpr uint32_t REL_INVL = (REL_ABORT + 4 + 15) & ~15u;     // float [2][128]
+constexpr uint32_t REL_RING = REL_INVL + 2 * BM * 4;             // int [ITEM_RING]
+constexpr uint32_t REL_STAT = REL_RING + ITEM_RING * 4;          // float [2 stats][2 halves][128]
+constexpr uint32_t REL_END = REL_STAT + 2 * 2 * BM * 4;
+template <int HD>
+constexpr uint32_t smem_bytes() { return Cfg<HD>::OFF_BAR + REL_END + 1024; }   // + alignment slack
 
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(smem_bytes<64>() <= 232448 && smem_bytes<128>() <= 232448, "shared memory budget");
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 256;                                   // O1 at 256, O2 at 384
-constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);   // Q (K-major) x K^T (K-major)
+constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);   // Q (K-major) x K^T (K-major), K = 16 per product
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, VD, 0, 1);  // P (TMEM) x V (MN-major)
 
 __device__ __forceinline__ uint32_t tm_s(int br, int buf) { return br * 128 + buf * 64; }
@@ -148,8 +182,8 @@ __device__ __forceinline__ Item decode_item(int idx, const TcParams& p) {
     it.b = bh / p.H;
     it.h = bh - it.b * p.H;
     // 64-key tiles: all of them, or (causal) those holding a key <= the
-    // tile's last query.
-    it.n_kv = p.causal ? min(2 * it.qt + 2, p.nk) : p.nk;
+    // position of the tile's last query.
+    it.n_kv = p.causal ? min((it.qt * BM + BM - 1 + p.kv_off) / BN + 1, p.nk) : p.nk;
     return it;
 }
 
@@ -217,6 +251,7 @@ __device__ __forceinline__ float tile_exp2(const float (&s)[64], float sl2, floa
     return f2_lo(r) + f2_hi(r);
 }
 
+template <int HD>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                        const __grid_constant__ CUtensorMap tm_k1,
@@ -225,12 +260,16 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_o,
                        const TcParams p) {
+    using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + OFF_TMEM_PTR);
-    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_ABORT);
-    float* inv_l = reinterpret_cast<float*>(smem + OFF_INVL);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + REL_TMEM_PTR);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + REL_ABORT);
+    float* inv_l = reinterpret_cast<float*>(smem + C::OFF_BAR + REL_INVL);
+    const bool k_shared = p.k_shared != 0;
+    const int kstages = C::kstages(k_shared);
+    const uint32_t kstride = C::kstride(k_shared);
 
     const uint32_t warp = warp_id();
     const uint32_t lane = threadIdx.x & 31;
@@ -243,7 +282,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             mbar_init(&bars[BAR_K_FULL + s], 1);
             mbar_init(&bars[BAR_K_EMPTY + s], 2);
         }
-        for (int s = 0; s < VSTAGES; ++s) {
+        for (int s = 0; s < C::VSTAGES; ++s) {
             mbar_init(&bars[BAR_V_FULL + s], 1);
             mbar_init(&bars[BAR_V_EMPTY + s], 2);
         }
@@ -278,7 +317,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
 
     const int grid = gridDim.x;
     const int cta = blockIdx.x;
-    const ItemRing ring{bars, reinterpret_cast<volatile int*>(smem + OFF_RING), &ab};
+    const ItemRing ring{bars, reinterpret_cast<volatile int*>(smem + C::OFF_BAR + REL_RING), &ab};
 
     if (warp >= 8) {
       regs_dec<REGS_OTHER>();
@@ -291,7 +330,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             tma_prefetch_desc(&tm_k2);
             tma_prefetch_desc(&tm_v);
             uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0;
-            uint32_t armed_q = 0, armed_k[KSTAGES] = {}, armed_v[VSTAGES] = {};
+            uint32_t armed_q = 0, armed_k[KSTAGES] = {}, armed_v[VSTAGES_MAX] = {};
             bool ok = true;
             bool first = true;
             // Item claimed for the current position of the sequence; the next
@@ -325,33 +364,39 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     qph ^= 1;
                 }
                 first = false;
-                mbar_arrive_expect_tx(&bars[BAR_Q_FULL], 2 * Q_BYTES);
-                tma_load_4d(smem + OFF_Q1, &tm_q1, &bars[BAR_Q_FULL], 0, it.qt * BM, it.h, it.b);
-                tma_load_4d(smem + OFF_Q2, &tm_q2, &bars[BAR_Q_FULL], 0, it.qt * BM, it.h, it.b);
+                mbar_arrive_expect_tx(&bars[BAR_Q_FULL], 2 * C::Q_BYTES);
+#pragma unroll
+                for (int pn = 0; pn < C::PANELS; ++pn) {
+                    tma_load_4d(smem + C::OFF_Q1 + pn * Q_PANEL, &tm_q1, &bars[BAR_Q_FULL], pn * 64,
+                                it.qt * BM, it.h, it.b);
+                    tma_load_4d(smem + C::OFF_Q2 + pn * Q_PANEL, &tm_q2, &bars[BAR_Q_FULL], pn * 64,
+                                it.qt * BM, it.h, it.b);
+                }
                 ++armed_q;
                 const int hk = it.h / p.kv_group;     // key/value head of this query head
                 for (int j = 0; j < it.n_kv; ++j) {
                     if (!(ok = mbar_wait(&bars[BAR_K_EMPTY + kst], kph ^ 1, ab))) break;
-                    uint8_t* kdst = smem + OFF_K + kst * 2 * K_BYTES;
-                    if (p.k_shared) {
-                        // one key tile serves both branches
-                        mbar_arrive_expect_tx(&bars[BAR_K_FULL + kst], K_BYTES);
-                        tma_load_4d(kdst, &tm_k1, &bars[BAR_K_FULL + kst], 0, j * BN, hk, it.b);
-                    } else {
-                        mbar_arrive_expect_tx(&bars[BAR_K_FULL + kst], 2 * K_BYTES);
-                        tma_load_4d(kdst, &tm_k1, &bars[BAR_K_FULL + kst], 0, j * BN, hk, it.b);
-                        tma_load_4d(kdst + K_BYTES, &tm_k2, &bars[BAR_K_FULL + kst], 0, j * BN, hk, it.b);
+                    uint8_t* kdst = smem + C::OFF_K + kst * kstride;
+                    // one key tile for both branches when they share their keys
+                    mbar_arrive_expect_tx(&bars[BAR_K_FULL + kst], (k_shared ? 1 : 2) * C::K_BYTES);
+#pragma unroll
+                    for (int pn = 0; pn < C::PANELS; ++pn) {
+                        tma_load_4d(kdst + pn * K_PANEL, &tm_k1, &bars[BAR_K_FULL + kst], pn * 64, j * BN,
+                                    hk, it.b);
+                        if (!k_shared)
+                            tma_load_4d(kdst + C::K_BYTES + pn * K_PANEL, &tm_k2, &bars[BAR_K_FULL + kst],
+                                        pn * 64, j * BN, hk, it.b);
                     }
                     ++armed_k[kst];
-                    if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
+                    if (++kst == (uint32_t)kstages) { kst = 0; kph ^= 1; }
 
                     if (!(ok = mbar_wait(&bars[BAR_V_EMPTY + vst], vph ^ 1, ab))) break;
-                    uint8_t* vdst = smem + OFF_V + vst * V_BYTES;
+                    uint8_t* vdst = smem + C::OFF_V + vst * V_BYTES;
                     mbar_arrive_expect_tx(&bars[BAR_V_FULL + vst], V_BYTES);
                     tma_load_4d(vdst, &tm_v, &bars[BAR_V_FULL + vst], 0, j * BN, hk, it.b);
                     tma_load_4d(vdst + V_HALF_BYTES, &tm_v, &bars[BAR_V_FULL + vst], 64, j * BN, hk, it.b);
                     ++armed_v[vst];
-                    if (++vst == VSTAGES) { vst = 0; vph ^= 1; }
+                    if (++vst == (uint32_t)C::VSTAGES) { vst = 0; vph ^= 1; }
                 }
             }
             // Never leave a copy in flight into shared memory we are about to
@@ -360,7 +405,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             if (armed_q) mbar_wait_teardown(&bars[BAR_Q_FULL], (armed_q - 1) & 1, lim);
             for (int s = 0; s < KSTAGES; ++s)
                 if (armed_k[s]) mbar_wait_teardown(&bars[BAR_K_FULL + s], (armed_k[s] - 1) & 1, lim);
-            for (int s = 0; s < VSTAGES; ++s)
+            for (int s = 0; s < C::VSTAGES; ++s)
                 if (armed_v[s]) mbar_wait_teardown(&bars[BAR_V_FULL + s], (armed_v[s] - 1) & 1, lim);
         }
         __syncwarp();
@@ -371,21 +416,26 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             // Descriptors for stage 0 and K-step 0; other stages and K-steps
             // differ only in the start-address field (address >> 4, which
             // stays below 2^14 for every shared-memory address).
-            const uint64_t qdesc = sdesc_sw128(smem_u32(smem + (br ? OFF_Q2 : OFF_Q1)), 16, 1024);
+            const uint64_t qdesc = sdesc_sw128(smem_u32(smem + (br ? C::OFF_Q2 : C::OFF_Q1)), 16, 1024);
             const uint64_t kdesc =
-                sdesc_sw128(smem_u32(smem + OFF_K + (p.k_shared ? 0 : br) * K_BYTES), 16, 1024);
-            const uint64_t vdesc = sdesc_sw128(smem_u32(smem + OFF_V), V_HALF_BYTES, 1024);
+                sdesc_sw128(smem_u32(smem + C::OFF_K + (k_shared ? 0 : br) * C::K_BYTES), 16, 1024);
+            const uint64_t vdesc = sdesc_sw128(smem_u32(smem + C::OFF_V), V_HALF_BYTES, 1024);
             const uint32_t d_o = tmem_base + TM_O + br * 128;
             uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0, oeph = 0;
             uint32_t pph = 0;     // bit buffer: phase of P_FULL[br][buffer]
             bool ok = true;
 
+            // S_b = Q_b K_b^T: HD / 16 products of depth 16, four per 64-column
+            // panel (a step of 32 bytes inside the swizzle span)
             auto issue_s = [&](uint32_t stage, int buf) {
                 const uint32_t d = tmem_base + tm_s(br, buf);
-                const uint64_t kd = kdesc + ((stage * 2 * K_BYTES) >> 4);
+                const uint64_t kd = kdesc + ((stage * kstride) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    mma_ss(d, qdesc + 2 * kk, kd + 2 * kk, IDESC_S, kk > 0);
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t pn = kk >> 2, ks = kk & 3;
+                    mma_ss(d, qdesc + pn * (Q_PANEL >> 4) + 2 * ks, kd + pn * (K_PANEL >> 4) + 2 * ks,
+                           IDESC_S, kk > 0);
+                }
             };
             auto issue_pv = [&](uint32_t stage, int buf, bool acc) {
                 const uint32_t pa = tmem_base + tm_s(br, buf);
@@ -410,7 +460,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     issue_s(kst, t);
                     mma_commit(&bars[BAR_S_FULL + 2 * br + t]);
                     mma_commit(&bars[BAR_K_EMPTY + kst]);
-                    if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
+                    if (++kst == (uint32_t)kstages) { kst = 0; kph ^= 1; }
                 }
                 if (!ok) break;
                 if (n <= 2) mma_commit(&bars[BAR_Q_EMPTY]);
@@ -429,7 +479,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     issue_pv(vst, buf, j > 0);
                     mma_commit(&bars[BAR_PV_DONE + br]);
                     mma_commit(&bars[BAR_V_EMPTY + vst]);
-                    if (++vst == VSTAGES) { vst = 0; vph ^= 1; }
+                    if (++vst == (uint32_t)C::VSTAGES) { vst = 0; vph ^= 1; }
                     // S_b(j+2) into the buffer P_b(j) was just read from
                     if (j + 2 < n) {
                         if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
@@ -437,7 +487,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         issue_s(kst, buf);
                         mma_commit(&bars[BAR_S_FULL + 2 * br + buf]);
                         mma_commit(&bars[BAR_K_EMPTY + kst]);
-                        if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
+                        if (++kst == (uint32_t)kstages) { kst = 0; kph ^= 1; }
                         if (j + 3 == n) mma_commit(&bars[BAR_Q_EMPTY]);
                     }
                 }
@@ -463,7 +513,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
         const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
         uint32_t sph = 0;          // bit buf: phase of S_FULL[br][buf]
         uint32_t ofph = 0, lph = 0, naph = 0, nbph = 0;
-        float* stat = reinterpret_cast<float*>(smem + OFF_STAT);
+        float* stat = reinterpret_cast<float*>(smem + C::OFF_BAR + REL_STAT);
         uint32_t pv_count = 0;     // PV_b products issued for earlier items
         bool ok = true;
 
@@ -493,13 +543,13 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
 
                 const int kv0 = j * BN;
                 if (p.causal) {
-                    if (kv0 + BN - 1 > it.qt * BM) {     // the tile crosses the diagonal
-                        const int lim = q - kv0;          // keys kv0 + c with c > lim are in the future
+                    if (kv0 + BN - 1 > it.qt * BM + p.kv_off) {   // the tile crosses the diagonal
+                        const int lim = q + p.kv_off - kv0;        // keys kv0 + c with c > lim are in the future
 #pragma unroll
                         for (int c = 0; c < 64; ++c) s[c] = (c > lim) ? -INFINITY : s[c];
                     }
-                } else if (kv0 + BN > p.T) {
-                    const int lim = p.T - kv0;            // keys at or beyond T do not exist
+                } else if (kv0 + BN > p.Tk) {
+                    const int lim = p.Tk - kv0;           // keys at or beyond Tk do not exist
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = (c >= lim) ? -INFINITY : s[c];
                 }
@@ -698,7 +748,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             // Stage this warp's 32 rows x 64 columns in shared memory (128-byte
             // swizzled rows, as the output tensor map expects) and write them
             // with one TMA store; rows at or past T are clipped by the TMA unit.
-            uint8_t* stage = smem + OFF_OUT + br * (OUT_BYTES / 2) + quad * 4096;
+            uint8_t* stage = smem + C::OFF_OUT + br * (OUT_BYTES / 2) + quad * 4096;
             if (lane == 0) bulk_wait_read_all();     // the previous store has read the buffer
             __syncwarp();
 #pragma unroll
@@ -737,15 +787,25 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
 
 }  // namespace tc
 
-int launch_fwd_tc(const CUtensorMap* maps, const TcParams& p, int grid, cudaStream_t stream) {
-    static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
-    cudaError_t e = cudaFuncSetAttribute(tc::diffattn_fwd_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tc::SMEM_BYTES);
+namespace {
+template <int HD>
+int launch_hd(const CUtensorMap* maps, const TcParams& p, int grid, cudaStream_t stream) {
+    constexpr uint32_t smem = tc::smem_bytes<HD>();
+    cudaError_t e = cudaFuncSetAttribute(tc::diffattn_fwd_tc_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return -1;
-    tc::diffattn_fwd_tc_kernel<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, stream>>>(
+    tc::diffattn_fwd_tc_kernel<HD><<<grid, tc::NUM_THREADS, smem, stream>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+}  // namespace
+
+int launch_fwd_tc(const CUtensorMap* maps, const TcParams& p, int head_dim, int grid,
+                  cudaStream_t stream) {
+    static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
+    if (head_dim == 64) return launch_hd<64>(maps, p, grid, stream);
+    if (head_dim == 128) return launch_hd<128>(maps, p, grid, stream);
+    return -1;
 }
 
 }  // namespace diffattn

@@ -15,11 +15,17 @@ namespace diffattn {
 // DIFFATTN_NORM_* in the public header).
 enum : int { kNormNone = 0, kNormRms = 1, kNormGroup = 2 };
 
-// Parameters of the tensor-core kernel (bf16, D = 64).
+// Parameters of the tensor-core kernel (bf16; D = 64 or 128, value width 128).
+// Queries and keys may be sequences of different lengths: query row i sits at
+// position i + kv_off of the key sequence (kv_off = Tk - Tq for queries at the
+// end of a key/value cache, 0 when queries and keys are one sequence), and the
+// causal mask hides keys j > i + kv_off.
 struct TcParams {
-    int B, H, T;
+    int B, H, T;            // T: query rows (Tq)
+    int Tk;                 // keys
+    int kv_off;             // causal offset of query row 0 in the key sequence (>= 0)
     int nq;                 // number of 128-row query tiles along T
-    int nk;                 // number of 64-row key tiles along T
+    int nk;                 // number of 64-row key tiles along Tk
     int total_items;        // B * H * nq
     int group;              // heads per scheduling group (L2 locality)
     int causal;
@@ -52,9 +58,12 @@ struct TcParams {
     float* lse;
 };
 
-// Parameters of the CUDA-core kernel (any D <= 128, fp32 or bf16).
+// Parameters of the CUDA-core kernel (any D <= 128, value width Dv <= 256,
+// fp32 or bf16).  T query rows over Tk keys; query row i sees keys
+// j <= i + kv_off under the causal mask.
 struct SimtParams {
     int B, H, T, D;
+    int Tk, kv_off, Dv;
     int causal;
     float scale;            // 1 / sqrt(D)
     float lambda;
@@ -173,8 +182,9 @@ int launch_decode_tc_first_pass(DecodeParams* p, cudaStream_t stream);
 // Workspace floats the tensor-core pass may need (its slots per unit on any
 // GPU of up to 1024 SMs).
 size_t decode_tc_work_floats(int64_t units, int64_t Tk, int tq_bucket);
-int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v,out*/, const TcParams& p, int grid,
-                  cudaStream_t stream);
+// head_dim: the Q/K width, 64 or 128 (the value width is 128 either way).
+int launch_fwd_tc(const CUtensorMap* maps /*q1,k1,q2,k2,v,out*/, const TcParams& p, int head_dim,
+                  int grid, cudaStream_t stream);
 int launch_bwd_tc(const CUtensorMap* maps /*dq: q1,k1,q2,k2,v,do; dkdv: the same*/,
                   const BwdTcParams& p, int num_sms, cudaStream_t stream);
 // dlambda = sign * (sum over rows of stats[row][3]) (sign -1 when the rows hold

@@ -58,14 +58,20 @@ typedef struct CUstream_st *diffattn_stream_t;
 #define DIFFATTN_F32  1   /* float32 storage and arithmetic */
 
 /* Kernel identifiers returned by diffattn_select_kernel. */
-#define DIFFATTN_KERNEL_TCGEN05 1  /* tensor-core kernel: bf16, D == 64 */
+#define DIFFATTN_KERNEL_TCGEN05 1  /* tensor-core kernel: bf16, value width 128, D == 64 or 128 */
 #define DIFFATTN_KERNEL_SIMT    2  /* CUDA-core kernel: any supported shape */
 
 /*
  * Shape and layout of one call.
  *
  * B, H, T, D: batch, (query) heads, sequence length and Q/K width; all >= 1.
- * V and O have width 2*D.  D <= 128.
+ * D <= 128.
+ * Dv: width of V and O.  0 means 2*D, the operation's own shape (paperleet,
+ * Formula and conventions: V and O are [B, H, T, 2D]).  Any other value
+ * 1 .. 256 is the head shape of DIFF V2 and similar layouts (the
+ * aiengineeringfromscratch lesson, "V1 vs V2": the head dimension stays that
+ * of the baseline, so V is as wide as Q and K, Dv = D).  The field is last in
+ * the struct, so a zero-initialised descriptor keeps the 2*D shape.
  * dtype: DIFFATTN_BF16 or DIFFATTN_F32.
  * kv_group: query heads per key/value head (grouped key/value heads, the
  * layout of DIFF V2: aiengineeringfromscratch lesson, "V1 vs V2" and its
@@ -91,6 +97,7 @@ typedef struct {
     int64_t k2_stride[3];
     int64_t v_stride[3];
     int64_t o_stride[3];
+    int64_t Dv;                /* V and O width; 0 = 2 * D */
 } diffattn_desc;
 
 /*
@@ -149,7 +156,7 @@ size_t diffattn_workspace_bytes(void);
  * example the output of diffattn_lambda); when non-NULL it overrides `lambda`
  * and is read by the kernel, so no host synchronisation is needed.
  * causal: non-zero applies the causal mask to both branches.
- * out: device pointer to O, [B, H, T, 2D] with desc->o_stride, same dtype as
+ * out: device pointer to O, [B, H, T, Dv] with desc->o_stride, same dtype as
  * the inputs (bf16 results are rounded to nearest even from fp32).
  * workspace, workspace_bytes: optional device scratch of at least
  * diffattn_workspace_bytes() bytes, 4-byte aligned, owned by the caller.  With
@@ -162,11 +169,13 @@ size_t diffattn_workspace_bytes(void);
  * depend on the schedule.
  * stream: the CUDA stream to launch on.
  *
- * The tensor-core kernel runs when dtype is bf16, D == 64, every base pointer
- * is 16-byte aligned and every stride is a multiple of 8 elements; any other
- * valid request runs on the CUDA-core kernel.  One kernel launch per call.
- * Errors: DIFFATTN_ERR_INVALID (NULL pointers, sizes < 1, D > 128, unknown
- * dtype, negative strides, negative kv_group or one that does not divide H,
+ * The tensor-core kernel runs when dtype is bf16, the value width is 128 with
+ * D == 64 (Dv = 2D) or D == 128 (Dv = D), every base pointer is 16-byte
+ * aligned and every stride is a multiple of 8 elements; any other valid
+ * request runs on the CUDA-core kernel.  One kernel launch per call.
+ * Errors: DIFFATTN_ERR_INVALID (NULL pointers, sizes < 1, D > 128, Dv < 0 or
+ * > 256, unknown dtype, negative strides, negative kv_group or one that does
+ * not divide H,
  * non-finite lambda, a
  * workspace smaller than diffattn_workspace_bytes() or not 4-byte aligned);
  * DIFFATTN_ERR_CUDA (tensor-map encoding or launch failure).
@@ -183,7 +192,7 @@ int diffattn_fwd(const diffattn_desc *desc, const void *q1, const void *k1,
 
 /*
  * Output epilogue of diffattn_fwd_ex: for every (b, h, t) row x of O (the
- * head's 2D output channels),
+ * head's Dv output channels; Dv = 2D unless the descriptor says otherwise),
  *
  *     y = out_scale * (norm(x) * weight[h] + bias[h])
  *
@@ -193,7 +202,7 @@ int diffattn_fwd(const diffattn_desc *desc, const void *q1, const void *k1,
  * aiengineeringfromscratch lesson), then the fixed multiplier (1 - lambda_init).
  *
  * norm: DIFFATTN_NORM_*.  eps: > 0 when norm != NONE (e.g. 1e-5).
- * weight, bias: optional device pointers to [H, 2D] float32 per-channel
+ * weight, bias: optional device pointers to [H, Dv] float32 per-channel
  * affine parameters (NULL = 1 and 0).  out_scale: finite multiplier applied
  * last (e.g. 1 - lambda_init; 1 for none).
  */
@@ -253,7 +262,7 @@ int diffattn_fwd_host(const diffattn_desc *desc, const void *q1_host, const void
  * diffattn_fwd_train -- diffattn_fwd that also keeps what the backward needs
  * (the forward of a training step): besides O it writes
  *
- *     out2 = A_2 V                  [B, H, T, 2D], desc->o_stride, inputs' dtype
+ *     out2 = A_2 V                  [B, H, T, Dv], desc->o_stride, inputs' dtype
  *     lse  = log sum_j exp(S_b)     [B, H, T, 2] float32, dense, natural log,
  *                                   S_b = Q_b K_b^T / sqrt(D) + M, b = 1, 2
  *
@@ -307,8 +316,9 @@ size_t diffattn_bwd_workspace_bytes(const diffattn_desc *desc);
  * `stream` (row statistics, dQ, dK/dV, and two for dlambda), no atomics, so
  * the result is reproducible bit for bit.
  * Errors: DIFFATTN_ERR_INVALID (as diffattn_fwd, plus a NULL gradient pointer,
- * a missing, small or misaligned workspace); DIFFATTN_ERR_CUDA (launch
- * failure).
+ * a missing, small or misaligned workspace); DIFFATTN_ERR_UNSUPPORTED for a
+ * value width other than 2D (desc->Dv not 0 or 2 * D); DIFFATTN_ERR_CUDA
+ * (launch failure).
  */
 int diffattn_bwd(const diffattn_desc *desc, const void *q1, const void *k1,
                  const void *q2, const void *k2, const void *v, float lambda,
@@ -333,11 +343,13 @@ int diffattn_bwd_saved(const diffattn_desc *desc, const void *q1, const void *k1
                        void *workspace, size_t workspace_bytes, diffattn_stream_t stream);
 
 /*
- * Decode over a key/value cache: Tq new queries against Tk cached keys.
- * Q1, Q2: [B, H, Tq, D]; K1, K2: [B, H_kv, Tk, D]; V: [B, H_kv, Tk, 2D]; O:
- * [B, H, Tq, 2D], with H_kv = H / kv_group (kv_group as in diffattn_desc; 0
- * or 1 = H_kv = H).  Strides as in diffattn_desc ([0] = B, [1] = H or H_kv,
- * [2] = the sequence dimension), innermost stride 1.
+ * Queries over a key/value cache: Tq new queries against Tk cached keys (one
+ * decode step for small Tq, a chunk of a prefill for larger Tq).
+ * Q1, Q2: [B, H, Tq, D]; K1, K2: [B, H_kv, Tk, D]; V: [B, H_kv, Tk, Dv]; O:
+ * [B, H, Tq, Dv], with H_kv = H / kv_group (kv_group as in diffattn_desc; 0
+ * or 1 = H_kv = H) and Dv as in diffattn_desc (last field; 0 = 2D).  Strides
+ * as in diffattn_desc ([0] = B, [1] = H or H_kv, [2] = the sequence
+ * dimension), innermost stride 1.
  */
 typedef struct {
     int64_t B, H, Tq, Tk, D;
@@ -349,12 +361,14 @@ typedef struct {
     int64_t k2_stride[3];
     int64_t v_stride[3];
     int64_t o_stride[3];
+    int64_t Dv;                /* V and O width; 0 = 2 * D */
 } diffattn_kv_desc;
 
 /*
  * diffattn_decode_workspace_bytes -- bytes of device workspace diffattn_decode
- * needs for this descriptor (partial results of the key-range splits), or 0
- * if the descriptor is invalid or unsupported.
+ * needs for this descriptor (partial results of the key-range splits; 16 bytes,
+ * unused, when the call runs on the forward kernels), or 0 if the descriptor
+ * is invalid or unsupported.
  */
 size_t diffattn_decode_workspace_bytes(const diffattn_kv_desc *desc);
 
@@ -372,20 +386,25 @@ size_t diffattn_decode_workspace_bytes(const diffattn_kv_desc *desc);
  * the GPU must use different workspaces.
  * Other arguments as diffattn_fwd.
  *
- * Supported: dtype bf16 or fp32; D in {32, 64, 128}; Tq <= 8 (D <= 64) or
- * Tq <= 4 (D = 128); K1, K2 and V with 16-byte aligned base pointers and
- * strides that are multiples of 16 bytes.  Two kernel launches per call (the
- * key-range splits, then their combination).  Work is bound by reading K1,
- * K2 and V once: one CTA serves up to 8 query rows (4 for D = 128) of the
- * query heads that share a key/value head, so with kv_group = g the cache of
- * a key/value head is read ceil(g * Tq / 8) times (ceil(g * Tq / 4) for D =
- * 128), not g * ceil(Tq / 8) times.
- * Errors: DIFFATTN_ERR_INVALID (NULL pointers, sizes < 1, Tk < Tq with the
- * causal mask, unknown dtype, negative strides, negative kv_group or one that
- * does not divide H,
- * non-finite lambda, bad epilogue, missing, small or misaligned workspace);
- * DIFFATTN_ERR_UNSUPPORTED (D, Tq or alignment outside the supported set);
- * DIFFATTN_ERR_CUDA (launch failure).
+ * Kernels.  Split-key decode: dtype bf16 or fp32, D in {32, 64, 128}, Dv =
+ * 2D, Tq <= 8 (D <= 64) or Tq <= 4 (D = 128), K1, K2 and V with 16-byte
+ * aligned base pointers and strides that are multiples of 16 bytes.  Two
+ * kernel launches per call (the key-range splits, then their combination).
+ * Work is bound by reading K1, K2 and V once: one CTA serves up to 8 query
+ * rows (4 for D = 128) of the query heads that share a key/value head, so with
+ * kv_group = g the cache of a key/value head is read ceil(g * Tq / 8) times
+ * (ceil(g * Tq / 4) for D = 128), not g * ceil(Tq / 8) times.
+ * Any other request (more query rows, another D or Dv) runs as one launch of
+ * the forward kernels with the queries placed at the end of the key sequence:
+ * on the tensor cores when diffattn_fwd would choose them for this shape and
+ * layout (bf16, value width 128, D = 64 or 128, aligned), else on the CUDA
+ * cores; the workspace is then not used.
+ * Errors: DIFFATTN_ERR_INVALID (NULL pointers, sizes < 1, D > 128, Dv < 0 or
+ * > 256, Tk < Tq with the causal mask, unknown dtype, negative strides,
+ * negative kv_group or one that does not divide H, non-finite lambda, bad
+ * epilogue, missing, small or misaligned workspace); DIFFATTN_ERR_UNSUPPORTED
+ * (a split-key decode with unaligned K1, K2 or V, or sizes beyond the int32
+ * index range); DIFFATTN_ERR_CUDA (launch failure).
  */
 int diffattn_decode(const diffattn_kv_desc *desc, const void *q1, const void *k1,
                     const void *q2, const void *k2, const void *v, float lambda,

@@ -34,12 +34,14 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_desc_layout_matches_header():
-    # 4 x int64, 2 x int32, 6 x int64[3]
-    assert ctypes.sizeof(_lib.DiffattnDesc) == 4 * 8 + 2 * 4 + 6 * 3 * 8
+    # 4 x int64, 2 x int32, 6 x int64[3], then Dv (int64) last
+    assert ctypes.sizeof(_lib.DiffattnDesc) == 4 * 8 + 2 * 4 + 6 * 3 * 8 + 8
+    assert _lib.DiffattnDesc.Dv.offset == 4 * 8 + 2 * 4 + 6 * 3 * 8
+    assert ctypes.sizeof(_lib.DiffattnKvDesc) == 5 * 8 + 2 * 4 + 6 * 3 * 8 + 8
 
 
 def test_version_and_strerror(lib):
-    assert lib.diffattn_version() == 100
+    assert lib.diffattn_version() == 200
     for code in (0, -1, -2, -3, -4, 7):
         assert isinstance(lib.diffattn_strerror(code), bytes)
     assert lib.diffattn_strerror(-4) != lib.diffattn_strerror(0)
@@ -48,12 +50,14 @@ def test_version_and_strerror(lib):
 FAKE = 0x10000  # 64 KiB-aligned stand-in addresses; never dereferenced on the host path
 
 
-def desc(B=1, H=2, T=128, D=64, dtype=_lib.DIFFATTN_BF16, contiguous=True, kv_group=0):
+def desc(B=1, H=2, T=128, D=64, dtype=_lib.DIFFATTN_BF16, contiguous=True, kv_group=0, Dv=0):
     d = _lib.DiffattnDesc()
     d.B, d.H, d.T, d.D, d.dtype, d.kv_group = B, H, T, D, dtype, kv_group
+    d.Dv = Dv
     Hk = H // max(kv_group, 1)
+    wv = Dv or 2 * D
     for f, w, h in (("q1_stride", D, H), ("k1_stride", D, Hk), ("q2_stride", D, H),
-                    ("k2_stride", D, Hk), ("v_stride", 2 * D, Hk), ("o_stride", 2 * D, H)):
+                    ("k2_stride", D, Hk), ("v_stride", wv, Hk), ("o_stride", wv, H)):
         getattr(d, f)[:] = (h * T * w, T * w, w)
     return d
 
@@ -71,9 +75,23 @@ def test_select_tcgen05_for_aligned_bf16_d64(lib):
     assert select(lib, desc()) == _lib.DIFFATTN_KERNEL_TCGEN05
 
 
-@pytest.mark.parametrize("kw", [dict(D=32), dict(D=128), dict(D=48), dict(dtype=_lib.DIFFATTN_F32)])
+@pytest.mark.parametrize("kw", [dict(D=32), dict(D=128), dict(D=48), dict(dtype=_lib.DIFFATTN_F32),
+                                dict(D=64, Dv=64), dict(D=128, Dv=64), dict(D=96, Dv=128),
+                                dict(D=128, Dv=128, dtype=_lib.DIFFATTN_F32)])
 def test_select_simt_otherwise(lib, kw):
     assert select(lib, desc(**kw)) == _lib.DIFFATTN_KERNEL_SIMT
+
+
+@pytest.mark.parametrize("kw", [dict(D=64, Dv=128), dict(D=128, Dv=128), dict(D=64)])
+def test_select_tcgen05_for_value_width_128(lib, kw):
+    # the tensor-core kernel's value width is 128: V = 2D at D = 64 (Dv 0 or
+    # 128), and the DIFF V2 head D = Dv = 128
+    assert select(lib, desc(**kw)) == _lib.DIFFATTN_KERNEL_TCGEN05
+
+
+def test_value_width_rejected_out_of_range(lib):
+    for dv in (-1, 257):
+        assert select(lib, desc(Dv=dv)) == _lib.DIFFATTN_ERR_INVALID
 
 
 def test_select_simt_for_unaligned(lib):
@@ -176,13 +194,15 @@ def test_bad_epilogue_rejected(lib, field, value):
     assert rc == _lib.DIFFATTN_ERR_INVALID
 
 
-def kv_desc(B=2, H=3, Tq=1, Tk=1000, D=64, dtype=_lib.DIFFATTN_BF16, kv_group=0):
+def kv_desc(B=2, H=3, Tq=1, Tk=1000, D=64, dtype=_lib.DIFFATTN_BF16, kv_group=0, Dv=0):
     d = _lib.DiffattnKvDesc()
     d.B, d.H, d.Tq, d.Tk, d.D, d.dtype, d.kv_group = B, H, Tq, Tk, D, dtype, kv_group
+    d.Dv = Dv
     Hk = H // max(kv_group, 1)
+    wv = Dv or 2 * D
     for f, T, w, h in (("q1_stride", Tq, D, H), ("q2_stride", Tq, D, H), ("k1_stride", Tk, D, Hk),
-                       ("k2_stride", Tk, D, Hk), ("v_stride", Tk, 2 * D, Hk),
-                       ("o_stride", Tq, 2 * D, H)):
+                       ("k2_stride", Tk, D, Hk), ("v_stride", Tk, wv, Hk),
+                       ("o_stride", Tq, wv, H)):
         getattr(d, f)[:] = (h * T * w, T * w, w)
     return d
 
@@ -192,8 +212,16 @@ def test_decode_workspace_query(lib):
     n = lib.diffattn_decode_workspace_bytes(ctypes.byref(d))
     assert n > 0 and n % 4 == 0
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tk=100000))) >= n
-    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=48))) == 0
-    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=9))) == 0
+    # shapes the split-key decode does not take run on the forward kernels,
+    # which use no workspace (a nominal 16 bytes)
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=48))) == 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=9))) == 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=1024, Tk=8192))) == 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=128))) == 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=64, Dv=128))) == n
+    # invalid descriptors
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=200))) == 0
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Dv=300))) == 0
     assert lib.diffattn_decode_workspace_bytes(None) == 0
 
 
@@ -209,8 +237,10 @@ def test_decode_workspace_four_row_shapes_fit_noalloc_buffer(lib):
 
 
 @pytest.mark.parametrize("kw,code", [(dict(Tq=0), _lib.DIFFATTN_ERR_INVALID),
-                                     (dict(D=40), _lib.DIFFATTN_ERR_UNSUPPORTED),
-                                     (dict(Tq=5, D=128), _lib.DIFFATTN_ERR_UNSUPPORTED),
+                                     (dict(D=200), _lib.DIFFATTN_ERR_INVALID),
+                                     (dict(Dv=-2), _lib.DIFFATTN_ERR_INVALID),
+                                     (dict(Dv=257), _lib.DIFFATTN_ERR_INVALID),
+                                     (dict(Tk=2 ** 31), _lib.DIFFATTN_ERR_UNSUPPORTED),
                                      (dict(Tq=4, Tk=3), _lib.DIFFATTN_ERR_INVALID)])
 def test_decode_rejects(lib, kw, code):
     d = kv_desc(**kw)
@@ -238,9 +268,10 @@ def test_decode_noalloc_reports_argument_errors_before_its_size_limit(lib):
     rc = lib.diffattn_decode_noalloc(ctypes.byref(big), *ptrs(5), ctypes.c_float(float("nan")), None, 1,
                                      None, ctypes.c_void_p(FAKE * 9), None)
     assert rc == _lib.DIFFATTN_ERR_INVALID
-    # unsupported shapes report as diffattn_decode does
-    rc = lib.diffattn_decode_noalloc(ctypes.byref(kv_desc(D=40)), *ptrs(5), ctypes.c_float(0.5),
-                                     None, 1, None, ctypes.c_void_p(FAKE * 9), None)
+    # unsupported sizes report as diffattn_decode does
+    rc = lib.diffattn_decode_noalloc(ctypes.byref(kv_desc(Tk=2 ** 31)), *ptrs(5),
+                                     ctypes.c_float(0.5), None, 1, None, ctypes.c_void_p(FAKE * 9),
+                                     None)
     assert rc == _lib.DIFFATTN_ERR_UNSUPPORTED
 
 

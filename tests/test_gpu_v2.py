@@ -1,0 +1,148 @@
+"""GPU parity of the DIFF V2 head shape against the float64 oracle.
+
+The aiengineeringfromscratch lesson ("V1 contre V2") keeps the baseline's head
+dimension for DIFF V2: Q, K and V are all D = 128 wide (value width Dv = D),
+the two branches of a differential head share their key/value head, and 32
+query heads run over 8 key/value heads.  bf16 with D = Dv = 128 runs on the
+tensor-core kernel; other value widths on the CUDA-core kernel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+import differential_attention_fwd_gb300 as da
+from differential_attention_fwd_gb300 import build as build_mod
+from tests.helpers import assert_close, to_device, to_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_mod.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def inputs(B, H, T, D, Dv, seed, kv_heads=None, shared=False, dtype="bf16"):
+    w = W.Workload("v2", B=B, H=H, T=T, D=D, dtype=dtype, causal=True, seed=seed,
+                   kv_heads=kv_heads, shared_keys=shared, value_dim=Dv, lambda_init=0.8)
+    return W.draw(w)
+
+
+def run(inp, lam, causal, dtype="bf16", shared=False, **kw):
+    q1, k1, q2, k2, v = (to_device(x, dtype) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v))
+    if shared:
+        k2 = k1
+    kern = da.select_kernel(q1, k1, q2, k2, v)
+    out = da.differential_attention(q1, k1, q2, k2, v, lam, causal=causal, **kw)
+    torch.cuda.synchronize()
+    assert da.get_device_error() == 0
+    return out, kern
+
+
+def ref(inp, lam, causal, **kw):
+    return oracle.differential_attention(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, lam, causal, **kw)
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 128, 129, 200, 257, 1000])
+@pytest.mark.parametrize("causal", [True, False])
+def test_d128_dv128_tensor_core_ragged(T, causal):
+    inp = inputs(2, 2, T, 128, 128, seed=300 + T)
+    out, kern = run(inp, 0.7, causal)
+    assert kern == da.DIFFATTN_KERNEL_TCGEN05
+    assert_close(to_numpy(out), ref(inp, 0.7, causal), "bf16", f"V2 head T={T} causal={causal}")
+
+
+@pytest.mark.parametrize("lam", [0.0, 0.5, 1.0, -0.4, 1.6])
+def test_d128_grouped_shared_keys(lam):
+    # 8 differential heads over 2 key/value heads, one key tensor for both branches
+    inp = inputs(2, 8, 700, 128, 128, seed=310, kv_heads=2, shared=True)
+    for causal in (True, False):
+        out, kern = run(inp, lam, causal, shared=True)
+        assert kern == da.DIFFATTN_KERNEL_TCGEN05
+        assert_close(to_numpy(out), ref(inp, lam, causal), "bf16",
+                     f"V2 grouped shared lam={lam} causal={causal}")
+
+
+def test_d128_separate_keys_and_identical_branches():
+    inp = inputs(1, 4, 513, 128, 128, seed=311, kv_heads=2)
+    out, _ = run(inp, 0.3, True)
+    assert_close(to_numpy(out), ref(inp, 0.3, True), "bf16", "V2 separate keys")
+    # identical branches cancel exactly at lambda = 1
+    q1, k1, v = (to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.v))
+    o = da.differential_attention(q1, k1, q1, k1, v, 1.0, causal=True)
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(o)) == 0
+
+
+def test_d128_value_rows_through_ones():
+    # V = 1 everywhere: every output is 1 - lambda (each map's rows sum to 1)
+    inp = inputs(1, 2, 300, 128, 128, seed=312)
+    inp.v = np.ones_like(inp.v)
+    out, _ = run(inp, 0.35, True)
+    assert float((out.float() - 0.65).abs().max()) <= 2e-2
+
+
+def test_d128_group_norm_epilogue():
+    inp = inputs(1, 4, 384, 128, 128, seed=313)
+    g = torch.Generator().manual_seed(3)
+    nw = 1 + 0.1 * torch.randn(4, 128, generator=g)
+    nb = 0.1 * torch.randn(4, 128, generator=g)
+    out, _ = run(inp, 0.6, True, norm="group", norm_eps=1e-5, norm_weight=nw.cuda(),
+                 norm_bias=nb.cuda(), out_scale=0.2)
+    want = oracle.head_norm(ref(inp, 0.6, True), "group", 1e-5, nw.numpy(), nb.numpy(), 0.2)
+    assert_close(to_numpy(out), want, "bf16", "V2 group norm epilogue")
+
+
+def test_d128_training_outputs():
+    inp = inputs(1, 2, 400, 128, 128, seed=314)
+    dev = [to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    out, out2, lse = da.differential_attention_train(*dev, 0.4, causal=True)
+    torch.cuda.synchronize()
+    assert_close(to_numpy(out), ref(inp, 0.4, True), "bf16", "V2 train out")
+    a2v = oracle.differential_attention(inp.q2, inp.k2, inp.q2, inp.k2, inp.v, 0.0, True)
+    assert_close(to_numpy(out2), a2v, "bf16", "V2 train A2 V")
+    for b, (q, k) in enumerate(((inp.q1, inp.k1), (inp.q2, inp.k2))):
+        want = oracle.branch_logsumexp(q, k, True)
+        assert np.max(np.abs(to_numpy(lse[..., b]) - want)) <= 1e-3
+
+
+def test_headline_size_v2_b2h16kv8t8192_sampled():
+    w = W.GQA_WORKLOADS["b2h16kv8t8192_d128_shared_k"]
+    inp = W.draw(w)
+    lam = float(np.float32(oracle.differential_lambda(inp.lq1, inp.lk1, inp.lq2, inp.lk2,
+                                                      W.lambda_init_for(w))))
+    q1, k, q2, v = (to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.q2, inp.v))
+    assert da.select_kernel(q1, k, q2, k, v) == da.DIFFATTN_KERNEL_TCGEN05
+    out = da.differential_attention(q1, k, q2, k, v, lam, causal=True)
+    torch.cuda.synchronize()
+    assert da.get_device_error() == 0
+    for b, h in ((0, 5), (1, 14)):
+        want = oracle.differential_attention(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, lam, True,
+                                             heads=[(b, h)])[0]
+        assert_close(to_numpy(out[b, h]), want, "bf16", f"{w.name} head ({b},{h})")
+    rows = W.check_rows(w.T, n_random=32, seed=7)[::4]
+    want = oracle.differential_attention(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, lam, True, rows=rows)
+    got = to_numpy(out[:, :, torch.as_tensor(rows, device=out.device)])
+    assert_close(got, want, "bf16", f"{w.name} sampled rows")
+
+
+@pytest.mark.parametrize("dtype,D,Dv", [("f32", 32, 32), ("bf16", 64, 64), ("bf16", 48, 5),
+                                        ("f32", 16, 256), ("bf16", 128, 200)])
+def test_other_value_widths_on_cuda_cores(dtype, D, Dv):
+    inp = inputs(2, 2, 150, D, Dv, seed=320 + Dv, dtype=dtype)
+    for causal in (True, False):
+        out, kern = run(inp, 0.8, causal, dtype=dtype)
+        assert kern == da.DIFFATTN_KERNEL_SIMT
+        assert tuple(out.shape) == (2, 2, 150, Dv)
+        assert_close(to_numpy(out), ref(inp, 0.8, causal), dtype, f"{dtype} D={D} Dv={Dv}")
+
+
+def test_backward_refuses_other_value_widths():
+    inp = inputs(1, 2, 64, 128, 128, seed=330)
+    dev = [to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    dout = torch.zeros(1, 2, 64, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        da.differential_attention_backward(*dev, 0.5, dout, True)

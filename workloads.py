@@ -7,17 +7,19 @@ the two sides see bit-identical inputs.
 
 Shapes follow the exercise specification of the Differential Transformer
 attention (paperleet "Differential Transformer Attention", Formula and
-conventions): Q1, K1, Q2, K2 are [B, H, T, D]; V is [B, H, T, 2D].
+conventions): Q1, K1, Q2, K2 are [B, H, T, D]; V is [B, H, T, 2D].  The DIFF
+V2 head (aiengineeringfromscratch lesson, "V1 contre V2") keeps the baseline's
+head dimension, so its V is [B, H, T, D]: workloads may set the value width.
 
 Recipe (all draws from numpy's PCG64 generator, float32, in this order):
   q1, k1, q2, k2 ~ N(0, 1)      each [B, H, T, D]
-  v               ~ N(0, 1)      [B, H, T, 2D]
+  v               ~ N(0, 1)      [B, H, T, Dv]   (Dv = 2D unless stated)
   lq1, lk1, lq2, lk2 ~ N(0, 0.1^2)  each [D]   (the lambda parameter vectors)
   then, per workload:
     planted keys: for each (b, h), 8 distinct key rows j_s ~ U[0, T) and a
       partner query row i_s ~ U[j_s, T); K1[b, h, j_s] = 4 * Q1[b, h, i_s]
       (a causally visible, strongly aligned key in branch 1 only)
-    value offset: one vector c ~ N(0, 2^2) of width 2D per (b, h), added to
+    value offset: one vector c ~ N(0, 2^2) of width Dv per (b, h), added to
       every token's value row
 The float32 draws are then rounded to the compute dtype (bf16 round to nearest
 even, or kept as float32).
@@ -49,6 +51,7 @@ class Workload:
     value_offset_sigma: float = 0.0      # std of the shared per-channel value offset
     kv_heads: Optional[int] = None       # key/value heads (None: H)
     shared_keys: bool = False            # K2 is K1 (one key tensor for both branches)
+    value_dim: Optional[int] = None      # V and O width (None: 2D)
 
     @property
     def Hk(self) -> int:
@@ -56,7 +59,7 @@ class Workload:
 
     @property
     def Dv(self) -> int:
-        return 2 * self.D
+        return 2 * self.D if self.value_dim is None else self.value_dim
 
     @property
     def pairs_per_head(self) -> int:
@@ -66,8 +69,9 @@ class Workload:
 
     @property
     def flops(self) -> int:
-        """Algorithmic FLOPs: 2 QK^T (2D each) + 2 PV (2*2D each) per unmasked pair."""
-        return self.B * self.H * self.pairs_per_head * 12 * self.D
+        """Algorithmic FLOPs: 2 QK^T (2D each) + 2 PV (2 Dv each) per unmasked
+        pair (12 D when Dv = 2D)."""
+        return self.B * self.H * self.pairs_per_head * (4 * self.D + 4 * self.Dv)
 
 
 # The five input recipes.  Sizes, distributions and lambda recipes are the
@@ -96,6 +100,13 @@ GQA_WORKLOADS = {
     "b2h16kv4t8192_shared_k": Workload("b2h16kv4t8192_shared_k", B=2, H=16, T=8192, D=64,
                                        dtype="bf16", causal=True, seed=5, lambda_init=0.8,
                                        kv_heads=4, shared_keys=True),
+    # The DIFF V2 head: the baseline's head dimension (128) for Q, K and V, the
+    # two branches of a differential head reading one key tensor, 16
+    # differential heads (32 query heads) over 8 key/value heads.
+    "b2h16kv8t8192_d128_shared_k": Workload("b2h16kv8t8192_d128_shared_k", B=2, H=16, T=8192,
+                                            D=128, dtype="bf16", causal=True, seed=6,
+                                            lambda_init=0.8, kv_heads=8, shared_keys=True,
+                                            value_dim=128),
 }
 ALL_WORKLOADS = {**WORKLOADS, **GQA_WORKLOADS}
 
@@ -115,7 +126,7 @@ class Inputs:
     lk2: np.ndarray
     planted_keys: Optional[np.ndarray] = None     # [B, H, planted] key rows
     planted_queries: Optional[np.ndarray] = None  # [B, H, planted] query rows
-    value_offset: Optional[np.ndarray] = None     # [B, H_kv, 2D]
+    value_offset: Optional[np.ndarray] = None     # [B, H_kv, Dv]
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
@@ -151,7 +162,8 @@ def draw(w: Workload, B: Optional[int] = None, H: Optional[int] = None,
     k1 = rng.standard_normal((B, Hk, T, D), dtype=np.float32)
     q2 = rng.standard_normal((B, H, T, D), dtype=np.float32)
     k2 = rng.standard_normal((B, Hk, T, D), dtype=np.float32)
-    v = rng.standard_normal((B, Hk, T, 2 * D), dtype=np.float32)
+    Dv = 2 * D if w.value_dim is None else w.value_dim
+    v = rng.standard_normal((B, Hk, T, Dv), dtype=np.float32)
     lam_vecs = [(0.1 * rng.standard_normal(D)).astype(np.float32) for _ in range(4)]
     planted_keys = planted_queries = offset = None
     if w.planted:
@@ -168,7 +180,7 @@ def draw(w: Workload, B: Optional[int] = None, H: Optional[int] = None,
                     k1[b, h, j] = 4.0 * q1[b, h, i]
     if w.value_offset_sigma:
         offset = (w.value_offset_sigma *
-                  rng.standard_normal((B, Hk, 2 * D), dtype=np.float32)).astype(np.float32)
+                  rng.standard_normal((B, Hk, Dv), dtype=np.float32)).astype(np.float32)
         v += offset[:, :, None, :]
     if dtype == "bf16":
         q1, k1, q2, k2, v = (round_to_bf16(a) for a in (q1, k1, q2, k2, v))
@@ -207,7 +219,8 @@ def check_rows(T: int, extra: Sequence[int] = (), n_random: int = 0,
 
 @dataclasses.dataclass(frozen=True)
 class DecodeWorkload:
-    """Tq new queries over a cache of Tk keys (decode)."""
+    """Tq new queries over a cache of Tk keys (a decode step for small Tq, a
+    chunk of a prefill for larger Tq)."""
     name: str
     B: int
     H: int
@@ -219,10 +232,12 @@ class DecodeWorkload:
     seed: int
     lambda_value: float = 0.8
     kv_heads: Optional[int] = None      # key/value heads (None: H)
+    value_dim: Optional[int] = None     # V and O width (None: 2D)
+    shared_keys: bool = False           # K2 is K1 (one key tensor for both branches)
 
     @property
     def Dv(self) -> int:
-        return 2 * self.D
+        return 2 * self.D if self.value_dim is None else self.value_dim
 
     @property
     def Hk(self) -> int:
@@ -230,10 +245,26 @@ class DecodeWorkload:
 
     @property
     def bytes(self) -> int:
-        """Algorithmic HBM bytes: K1, K2, V of every key/value head read once;
-        Q1, Q2 read and O written for every query head."""
+        """Algorithmic HBM bytes: K1, K2 (one tensor when shared), V of every
+        key/value head read once; Q1, Q2 read and O written for every query
+        head."""
         el = 2 if self.dtype == "bf16" else 4
-        return (self.B * self.Hk * self.Tk * 4 * self.D + self.B * self.H * self.Tq * 4 * self.D) * el
+        k_tensors = 1 if self.shared_keys else 2
+        return (self.B * self.Hk * self.Tk * (k_tensors * self.D + self.Dv) +
+                self.B * self.H * self.Tq * (2 * self.D + self.Dv)) * el
+
+    @property
+    def pairs_per_head(self) -> int:
+        """Unmasked (query, key) pairs of one head: query i sees keys
+        j <= Tk - Tq + i under the causal mask."""
+        if not self.causal:
+            return self.Tq * self.Tk
+        return self.Tq * (self.Tk - self.Tq) + self.Tq * (self.Tq + 1) // 2
+
+    @property
+    def flops(self) -> int:
+        """Algorithmic FLOPs: 4 D + 4 Dv per unmasked pair."""
+        return self.B * self.H * self.pairs_per_head * (4 * self.D + 4 * self.Dv)
 
 
 # Decode workloads: 16 sequences with 16 heads (the V1 layout halves the heads
@@ -248,14 +279,27 @@ DECODE_WORKLOADS = {
                                               "bf16", True, 22, kv_heads=8),
 }
 
+# Chunked prefill: the next 1024 tokens of 4 sequences (16 heads, D = 64)
+# against their cache of 8192 keys (the chunk's own keys at its end), and the
+# same with the DIFF V2 head (D = Dv = 128, 16 differential heads over 8
+# key/value heads, shared keys).  Compute-bound: timed in TFLOP/s.
+PREFILL_WORKLOADS = {
+    "prefill_b4h16q1024k8192": DecodeWorkload("prefill_b4h16q1024k8192", 4, 16, 1024, 8192, 64,
+                                              "bf16", True, 23),
+    "prefill_b4h16kv8q1024k8192_d128_shared_k": DecodeWorkload(
+        "prefill_b4h16kv8q1024k8192_d128_shared_k", 4, 16, 1024, 8192, 128, "bf16", True, 24,
+        kv_heads=8, value_dim=128, shared_keys=True),
+}
+
 
 def draw_kv(w: DecodeWorkload, **override) -> Inputs:
     """Decode inputs: q1, q2 [B, H, Tq, D]; k1, k2 [B, H_kv, Tk, D]; v [B, H_kv,
-    Tk, 2D] (H_kv = w.kv_heads, default H); i.i.d. N(0, 1) float32 drawn in the
-    order q1, k1, q2, k2, v from PCG64(seed), rounded to the dtype.  The lambda
-    vectors are left zero (lambda is given directly for decode workloads)."""
+    Tk, Dv] (H_kv = w.kv_heads, default H; Dv = w.Dv); i.i.d. N(0, 1) float32
+    drawn in the order q1, k1, q2, k2, v from PCG64(seed), rounded to the
+    dtype.  The lambda vectors are left zero (lambda is given directly for
+    decode workloads)."""
     f = dict(B=w.B, H=w.H, Tq=w.Tq, Tk=w.Tk, D=w.D, dtype=w.dtype, seed=w.seed,
-             kv_heads=w.kv_heads)
+             kv_heads=w.kv_heads, value_dim=w.value_dim)
     f.update(override)
     rng = np.random.Generator(np.random.PCG64(f["seed"]))
     B, H, Tq, Tk, D = f["B"], f["H"], f["Tq"], f["Tk"], f["D"]
@@ -266,7 +310,8 @@ def draw_kv(w: DecodeWorkload, **override) -> Inputs:
     k1 = rng.standard_normal((B, Hk, Tk, D), dtype=np.float32)
     q2 = rng.standard_normal((B, H, Tq, D), dtype=np.float32)
     k2 = rng.standard_normal((B, Hk, Tk, D), dtype=np.float32)
-    v = rng.standard_normal((B, Hk, Tk, 2 * D), dtype=np.float32)
+    Dv = 2 * D if f["value_dim"] is None else f["value_dim"]
+    v = rng.standard_normal((B, Hk, Tk, Dv), dtype=np.float32)
     if f["dtype"] == "bf16":
         q1, k1, q2, k2, v = (round_to_bf16(a) for a in (q1, k1, q2, k2, v))
     z = np.zeros(D, dtype=np.float32)
