@@ -843,6 +843,30 @@ def run_decode(args, world, rank, local):
     }
 
 
+WAIT_ROLES = ("producer", "mma_issuers", "softmax_warps")
+WAIT_KINDS = ("total_cycles", "tma", "tensor", "peer")
+
+
+def wait_profile_summary(raw):
+    """Shares of each role's cycles spent waiting, by what completes the
+    barrier (the counters of the wait-profile build: [role][kind])."""
+    out = {}
+    for r, role in enumerate(WAIT_ROLES):
+        tot = raw[4 * r]
+        out[role] = {"cycles": tot, **{k: (raw[4 * r + i] / tot if tot else None)
+                                        for i, k in enumerate(WAIT_KINDS) if i}}
+    return {
+        "build": "libdiffattn_waitprof.so: the same sources with -DDIFFATTN_WAIT_PROFILE (clock64 "
+                 "around every mbarrier wait of the forward kernel; timings of this run are not "
+                 "bench values)",
+        "roles": out,
+        # the MMA-issuing threads are the consumers of the TMA loads: the share
+        # of their time spent waiting for Q/K/V tiles to land
+        "tma_stall_share": out["mma_issuers"]["tma"],
+        "tensor_wait_share_softmax": out["softmax_warps"]["tensor"],
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -866,6 +890,9 @@ def main(argv=None):
                          "training forward's saved results")
     ap.add_argument("--norm", choices=["none", "rms", "group"], default="none",
                     help="fuse a per-head norm and the (1 - lambda_init) multiplier")
+    ap.add_argument("--wait-profile", action="store_true",
+                    help="forward mode: run the wait-profile build of the library and report "
+                         "each warp role's barrier-wait shares (a measurement run, not a bench value)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("at least 3 warm-up steps")
@@ -893,6 +920,20 @@ def main(argv=None):
         res = run_reference(args, w, world, rank)
     elif args.mode == "backward":
         res = run_backward(args, w, world, rank, local)
+    elif args.wait_profile:
+        import ctypes as C
+        from differential_attention_fwd_gb300 import _lib
+        from differential_attention_fwd_gb300 import build as build_mod
+        lib = _lib.load(build_mod.build(variant="waitprof"))
+        lib.diffattn_wait_profile.argtypes = [C.POINTER(C.c_ulonglong), C.c_int]
+        lib.diffattn_wait_profile.restype = C.c_int
+        res = run_ours(args, w, world, rank, local)
+        raw = (C.c_ulonglong * 12)()
+        if lib.diffattn_wait_profile(raw, 12) != 0:
+            raise RuntimeError("diffattn_wait_profile failed")
+        res = {"wait_profile": wait_profile_summary(list(raw)), "workload": w.name,
+               "steps": args.steps, "warmup": args.warmup,
+               "instrumented_kernel_ms_median": res["roofline"]["fwd_ms_median"]}
     else:
         res = run_ours(args, w, world, rank, local)
     if rank == 0 and res is not None:

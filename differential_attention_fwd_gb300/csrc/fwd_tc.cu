@@ -216,6 +216,45 @@ struct ItemRing {
     }
 };
 
+// Wait profile (only in a separate build of the library compiled with
+// -DDIFFATTN_WAIT_PROFILE; the regular build has none of it): each role's
+// issuing thread (lane 0 of each softmax warp) counts the SM cycles it spends
+// in mbarrier waits, by what completes the barrier, and adds them to
+// g_wait_prof[role][kind] when the CTA ends.  Roles: 0 the TMA producer, 1 the
+// two MMA-issuing threads, 2 the eight softmax warps.  Kinds: 0 the role's
+// cycles from start to end, 1 waits on TMA loads (Q, K, V full), 2 waits on
+// tensor-core products (S full, PV done, O full; stages released by MMA
+// commits), 3 waits on other warps (P full, O read out, the item ring, the
+// epilogue's exchanges).
+enum : int { kWaitTotal = 0, kWaitTma = 1, kWaitTensor = 2, kWaitPeer = 3 };
+#ifdef DIFFATTN_WAIT_PROFILE
+__device__ unsigned long long g_wait_prof[3][4];
+struct WaitProf {
+    unsigned long long c[4] = {0, 0, 0, 0};
+    long long t0 = 0;
+    __device__ __forceinline__ void start() { t0 = clock64(); }
+    template <class F>
+    __device__ __forceinline__ bool timed(int kind, F&& f) {
+        const long long a = clock64();
+        const bool r = f();
+        c[kind] += (unsigned long long)(clock64() - a);
+        return r;
+    }
+    __device__ __forceinline__ void flush(int role, bool reporter) {
+        c[kWaitTotal] = (unsigned long long)(clock64() - t0);
+        if (reporter)
+            for (int i = 0; i < 4; ++i) atomicAdd(&g_wait_prof[role][i], c[i]);
+    }
+};
+#define TIMED_WAIT(wp, kind, expr) (wp).timed((kind), [&]() -> bool { return (expr); })
+#else
+struct WaitProf {
+    __device__ __forceinline__ void start() {}
+    __device__ __forceinline__ void flush(int, bool) {}
+};
+#define TIMED_WAIT(wp, kind, expr) (expr)
+#endif
+
 // Row max of one thread's 64 scores (four independent chains of
 // three-input maxima).
 __device__ __forceinline__ float tile_row_max(const float (&s)[64]) {
@@ -329,6 +368,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             tma_prefetch_desc(&tm_q2);
             tma_prefetch_desc(&tm_k2);
             tma_prefetch_desc(&tm_v);
+            WaitProf wp;
+            wp.start();
             uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0;
             uint32_t armed_q = 0, armed_k[KSTAGES] = {}, armed_v[VSTAGES_MAX] = {};
             bool ok = true;
@@ -352,7 +393,9 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 // publish item k (or the end of the sequence) to the consumers
                 const int slot = k % ITEM_RING;
                 if (k >= ITEM_RING) {
-                    if (!(ok = mbar_wait(&bars[BAR_ITEM_EMPTY + slot], (uint32_t)(k / ITEM_RING - 1) & 1u, ab))) break;
+                    if (!(ok = TIMED_WAIT(wp, kWaitPeer, mbar_wait(&bars[BAR_ITEM_EMPTY + slot],
+                                                                   (uint32_t)(k / ITEM_RING - 1) & 1u, ab))))
+                        break;
                 }
                 ring.slots[slot] = idx;
                 mbar_arrive(&bars[BAR_ITEM_FULL + slot]);
@@ -360,7 +403,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 const Item it = decode_item(idx, p);
                 idx = claim();
                 if (!first) {
-                    if (!(ok = mbar_wait(&bars[BAR_Q_EMPTY], qph, ab))) break;
+                    if (!(ok = TIMED_WAIT(wp, kWaitTensor, mbar_wait(&bars[BAR_Q_EMPTY], qph, ab)))) break;
                     qph ^= 1;
                 }
                 first = false;
@@ -375,7 +418,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 ++armed_q;
                 const int hk = it.h / p.kv_group;     // key/value head of this query head
                 for (int j = 0; j < it.n_kv; ++j) {
-                    if (!(ok = mbar_wait(&bars[BAR_K_EMPTY + kst], kph ^ 1, ab))) break;
+                    if (!(ok = TIMED_WAIT(wp, kWaitTensor, mbar_wait(&bars[BAR_K_EMPTY + kst], kph ^ 1, ab))))
+                        break;
                     uint8_t* kdst = smem + C::OFF_K + kst * kstride;
                     // one key tile for both branches when they share their keys
                     mbar_arrive_expect_tx(&bars[BAR_K_FULL + kst], (k_shared ? 1 : 2) * C::K_BYTES);
@@ -390,7 +434,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     ++armed_k[kst];
                     if (++kst == (uint32_t)kstages) { kst = 0; kph ^= 1; }
 
-                    if (!(ok = mbar_wait(&bars[BAR_V_EMPTY + vst], vph ^ 1, ab))) break;
+                    if (!(ok = TIMED_WAIT(wp, kWaitTensor, mbar_wait(&bars[BAR_V_EMPTY + vst], vph ^ 1, ab))))
+                        break;
                     uint8_t* vdst = smem + C::OFF_V + vst * V_BYTES;
                     mbar_arrive_expect_tx(&bars[BAR_V_FULL + vst], V_BYTES);
                     tma_load_4d(vdst, &tm_v, &bars[BAR_V_FULL + vst], 0, j * BN, hk, it.b);
@@ -407,6 +452,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 if (armed_k[s]) mbar_wait_teardown(&bars[BAR_K_FULL + s], (armed_k[s] - 1) & 1, lim);
             for (int s = 0; s < C::VSTAGES; ++s)
                 if (armed_v[s]) mbar_wait_teardown(&bars[BAR_V_FULL + s], (armed_v[s] - 1) & 1, lim);
+            wp.flush(0, true);
         }
         __syncwarp();
       } else if (warp == 9 || warp == 10) {
@@ -421,6 +467,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 sdesc_sw128(smem_u32(smem + C::OFF_K + (k_shared ? 0 : br) * C::K_BYTES), 16, 1024);
             const uint64_t vdesc = sdesc_sw128(smem_u32(smem + C::OFF_V), V_HALF_BYTES, 1024);
             const uint32_t d_o = tmem_base + TM_O + br * 128;
+            WaitProf wp;
+            wp.start();
             uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0, oeph = 0;
             uint32_t pph = 0;     // bit buffer: phase of P_FULL[br][buffer]
             bool ok = true;
@@ -448,14 +496,14 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             bool first = true;
             for (int k = 0; ok; ++k) {
                 int idx = -1;
-                if (!(ok = ring.get_one(k, idx)) || idx < 0) break;
+                if (!(ok = TIMED_WAIT(wp, kWaitPeer, ring.get_one(k, idx))) || idx < 0) break;
                 const Item it = decode_item(idx, p);
                 const int n = it.n_kv;
-                if (!(ok = mbar_wait(&bars[BAR_Q_FULL], qph, ab))) break;
+                if (!(ok = TIMED_WAIT(wp, kWaitTma, mbar_wait(&bars[BAR_Q_FULL], qph, ab)))) break;
                 qph ^= 1;
                 // S_b(0), S_b(1) into buffers 0 and 1
                 for (int t = 0; t < 2 && t < n; ++t) {
-                    if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
+                    if (!(ok = TIMED_WAIT(wp, kWaitTma, mbar_wait(&bars[BAR_K_FULL + kst], kph, ab)))) break;
                     tc_fence_after();
                     issue_s(kst, t);
                     mma_commit(&bars[BAR_S_FULL + 2 * br + t]);
@@ -468,13 +516,15 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 for (int j = 0; j < n; ++j) {
                     const int buf = j & 1;
                     // O_b += P_b(j) V(j)
-                    if (!(ok = mbar_wait(&bars[BAR_P_FULL + 2 * br + buf], (pph >> buf) & 1u, ab))) break;
+                    if (!(ok = TIMED_WAIT(wp, kWaitPeer,
+                                          mbar_wait(&bars[BAR_P_FULL + 2 * br + buf], (pph >> buf) & 1u, ab))))
+                        break;
                     pph ^= 1u << buf;
                     if (j == 0 && !first) {
-                        if (!(ok = mbar_wait(&bars[BAR_O_EMPTY], oeph, ab))) break;
+                        if (!(ok = TIMED_WAIT(wp, kWaitPeer, mbar_wait(&bars[BAR_O_EMPTY], oeph, ab)))) break;
                         oeph ^= 1;
                     }
-                    if (!(ok = mbar_wait(&bars[BAR_V_FULL + vst], vph, ab))) break;
+                    if (!(ok = TIMED_WAIT(wp, kWaitTma, mbar_wait(&bars[BAR_V_FULL + vst], vph, ab)))) break;
                     tc_fence_after();
                     issue_pv(vst, buf, j > 0);
                     mma_commit(&bars[BAR_PV_DONE + br]);
@@ -482,7 +532,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     if (++vst == (uint32_t)C::VSTAGES) { vst = 0; vph ^= 1; }
                     // S_b(j+2) into the buffer P_b(j) was just read from
                     if (j + 2 < n) {
-                        if (!(ok = mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))) break;
+                        if (!(ok = TIMED_WAIT(wp, kWaitTma, mbar_wait(&bars[BAR_K_FULL + kst], kph, ab)))) break;
                         tc_fence_after();
                         issue_s(kst, buf);
                         mma_commit(&bars[BAR_S_FULL + 2 * br + buf]);
@@ -498,6 +548,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             // Every MMA this thread issued must have finished before TMEM is freed.
             mma_commit(&bars[BAR_FINAL + br]);
             mbar_wait_teardown(&bars[BAR_FINAL + br], 0, 200ull * 1000ull * 1000ull);
+            wp.flush(1, true);
         }
         __syncwarp();
       }
@@ -517,9 +568,11 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
         uint32_t pv_count = 0;     // PV_b products issued for earlier items
         bool ok = true;
 
+        WaitProf wp;
+        wp.start();
         int idx = -1;
         Item next{};
-        ok = ring.get(0, idx);
+        ok = TIMED_WAIT(wp, kWaitPeer, ring.get(0, idx));
         if (ok && idx >= 0) next = decode_item(idx, p);
         for (int k = 0; ok && idx >= 0; ++k) {
             const Item it = next;
@@ -530,7 +583,9 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             for (int j = 0; j < it.n_kv; ++j) {
                 const int buf = j & 1;
                 const uint32_t tS = lane_base + tm_s(br, buf);
-                if (!(ok = mbar_wait_warp(&bars[BAR_S_FULL + 2 * br + buf], (sph >> buf) & 1u, ab))) break;
+                if (!(ok = TIMED_WAIT(wp, kWaitTensor,
+                                      mbar_wait_warp(&bars[BAR_S_FULL + 2 * br + buf], (sph >> buf) & 1u, ab))))
+                    break;
                 sph ^= 1u << buf;
                 tc_fence_after();
                 uint32_t u[64];
@@ -587,7 +642,9 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 if (rescale) {
                     // O_b row *= alpha, once PV_b(j-1) has completed (S_b(j)
                     // completing already implies PV_b(j-2) has).
-                    if (!(ok = mbar_wait_warp(&bars[BAR_PV_DONE + br], (pv_count + j - 1) & 1u, ab))) break;
+                    if (!(ok = TIMED_WAIT(wp, kWaitTensor,
+                                          mbar_wait_warp(&bars[BAR_PV_DONE + br], (pv_count + j - 1) & 1u, ab))))
+                        break;
                     tc_fence_after();
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) {
@@ -609,11 +666,11 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             pv_count += it.n_kv;
             // The next item is fetched and decoded here, while the item's last
             // PV products complete, rather than after the epilogue.
-            if (!(ok = ring.get(k + 1, idx))) break;
+            if (!(ok = TIMED_WAIT(wp, kWaitPeer, ring.get(k + 1, idx)))) break;
             if (idx >= 0) next = decode_item(idx, p);
 
             // ---------------------------------------------------- epilogue
-            if (!(ok = mbar_wait_warp(&bars[BAR_O_FULL], ofph, ab))) break;
+            if (!(ok = TIMED_WAIT(wp, kWaitTensor, mbar_wait_warp(&bars[BAR_O_FULL], ofph, ab)))) break;
             ofph ^= 1;
             tc_fence_after();
             if (p.stats) {
@@ -670,7 +727,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 mbar_arrive(&bars[BAR_O_EMPTY]);
                 mbar_arrive(&bars[BAR_L_READY]);
             }
-            if (!(ok = mbar_wait_warp(&bars[BAR_L_READY], lph, ab))) break;
+            if (!(ok = TIMED_WAIT(wp, kWaitPeer, mbar_wait_warp(&bars[BAR_L_READY], lph, ab)))) break;
             lph ^= 1;
             const float inv1 = inv_l[row];
             const float inv2 = inv_l[BM + row];
@@ -713,7 +770,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 stat[br * BM + row] = part;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[BAR_NORM_A]);
-                if (!(ok = mbar_wait_warp(&bars[BAR_NORM_A], naph, ab))) break;
+                if (!(ok = TIMED_WAIT(wp, kWaitPeer, mbar_wait_warp(&bars[BAR_NORM_A], naph, ab)))) break;
                 naph ^= 1;
                 const float tot = stat[row] + stat[BM + row];
                 float mu = 0.f, rinv;
@@ -727,7 +784,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     stat[2 * BM + br * BM + row] = dev;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[BAR_NORM_B]);
-                    if (!(ok = mbar_wait_warp(&bars[BAR_NORM_B], nbph, ab))) break;
+                    if (!(ok = TIMED_WAIT(wp, kWaitPeer, mbar_wait_warp(&bars[BAR_NORM_B], nbph, ab)))) break;
                     nbph ^= 1;
                     const float var = (stat[2 * BM + row] + stat[3 * BM + row]) * (1.0f / VD);
                     rinv = rsqrtf(var + p.norm_eps);
@@ -768,6 +825,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
         // Every output store must be complete before the CTA exits.
         if (lane == 0) bulk_wait_all();
         __syncwarp();
+        wp.flush(2, lane == 0);
     }
 
     tc_fence_before();
@@ -799,6 +857,20 @@ int launch_hd(const CUtensorMap* maps, const TcParams& p, int grid, cudaStream_t
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 }  // namespace
+
+#ifdef DIFFATTN_WAIT_PROFILE
+// The wait profile of the launches since the previous call ([3 roles][4
+// kinds], see WaitProf), copied to `out` and cleared.  Only in the build with
+// -DDIFFATTN_WAIT_PROFILE.
+extern "C" int diffattn_wait_profile(unsigned long long* out, int n) {
+    if (!out || n < 12) return -1;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(out, tc::g_wait_prof, 12 * sizeof(unsigned long long)) != cudaSuccess)
+        return -3;
+    unsigned long long zero[12] = {};
+    return cudaMemcpyToSymbol(tc::g_wait_prof, zero, sizeof(zero)) == cudaSuccess ? 0 : -3;
+}
+#endif
 
 int launch_fwd_tc(const CUtensorMap* maps, const TcParams& p, int head_dim, int grid,
                   cudaStream_t stream) {

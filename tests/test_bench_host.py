@@ -117,3 +117,14 @@ def test_clock_scaled_peak():
     assert r["peak"] == pytest.approx(152 * 2000e6 * 8192 / 1e12)
     assert r["frac"] == pytest.approx(1500.0 / r["peak"])
     assert bench.clock_peak(1500.0, None, 152) is None
+
+
+def test_wait_profile_summary_shares():
+    raw = [1000, 0, 600, 100,   # producer: total, tma, tensor, peer
+           2000, 500, 0, 700,   # MMA issuers
+           8000, 0, 2000, 400]  # softmax warps
+    s = bench.wait_profile_summary(raw)
+    assert s["tma_stall_share"] == pytest.approx(0.25)
+    assert s["roles"]["producer"]["tensor"] == pytest.approx(0.6)
+    assert s["roles"]["softmax_warps"]["peer"] == pytest.approx(0.05)
+    assert s["tensor_wait_share_softmax"] == pytest.approx(0.25)

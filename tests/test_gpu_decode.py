@@ -77,17 +77,22 @@ def test_decode_workloads_sampled():
         assert_close(to_numpy(out), ref, w.dtype, w.name)
 
 
-def test_decode_unsupported_and_invalid():
+def test_decode_invalid_and_forward_routed_shapes():
+    # more queries than keys under the causal mask: no alignment exists
     x = torch.zeros(1, 1, 9, 64, dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros(1, 1, 100, 64, dtype=torch.bfloat16, device="cuda")
-    v = torch.zeros(1, 1, 100, 128, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(da.DiffattnError):        # Tq > 8
-        da.differential_attention_decode(x, k, x, k, v, 0.5)
-    x = torch.zeros(1, 1, 2, 48, dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros(1, 1, 100, 48, dtype=torch.bfloat16, device="cuda")
-    v = torch.zeros(1, 1, 100, 96, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(da.DiffattnError):        # D not in {32, 64, 128}
-        da.differential_attention_decode(x, k, x, k, v, 0.5)
+    k = torch.zeros(1, 1, 5, 64, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(1, 1, 5, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(da.DiffattnError):
+        da.differential_attention_decode(x, k, x, k, v, 0.5, causal=True)
+    # Tq > 8 and D outside {32, 64, 128} run on the forward kernels: with V = 1
+    # every output is 1 - lambda
+    for Tq, D in ((9, 64), (2, 48)):
+        x = torch.zeros(1, 1, Tq, D, dtype=torch.bfloat16, device="cuda")
+        k = torch.zeros(1, 1, 100, D, dtype=torch.bfloat16, device="cuda")
+        v = torch.ones(1, 1, 100, 2 * D, dtype=torch.bfloat16, device="cuda")
+        o = da.differential_attention_decode(x, k, x, k, v, 0.25)
+        torch.cuda.synchronize()
+        assert float((o.float() - 0.75).abs().max()) == 0.0
 
 
 @pytest.mark.parametrize("H,Hk,Tq,Tk", [(2, 2, 4, 3000), (8, 2, 1, 2500), (3, 3, 8, 700)])

@@ -170,8 +170,11 @@ def test_many_items_multiple_waves():
 def test_empty_and_mismatched_inputs_rejected():
     x = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device="cuda")
     v = torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(ValueError):
-        da.differential_attention(x, x, x, x, v[..., :64], 0.5)
+    with pytest.raises(ValueError):          # V with another sequence length
+        da.differential_attention(x, x, x, x, v[:, :, :3], 0.5)
+    with pytest.raises(ValueError):          # V wider than 256
+        da.differential_attention(x, x, x, x, torch.zeros(1, 1, 4, 300, dtype=torch.bfloat16,
+                                                          device="cuda"), 0.5)
     with pytest.raises(ValueError):
         da.differential_attention(x, x, x, x.float(), v, 0.5)
     e = torch.zeros(1, 1, 0, 64, dtype=torch.bfloat16, device="cuda")
