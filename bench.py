@@ -844,17 +844,48 @@ def run_decode(args, world, rank, local):
 
 
 WAIT_ROLES = ("producer", "mma_issuers", "softmax_warps")
-WAIT_KINDS = ("total_cycles", "tma", "tensor", "peer")
+WAIT_KINDS = ("total_cycles", "q_load", "k_load", "v_load", "item_start", "tensor", "epilogue", "peer",
+              "k_lead_sum", "k_lead_count", "k_late_sum", "k_late_count", "k_floor_sum")
+WAIT_SPAN_CTAS = 1024
+WAIT_SHARES = 8     # kinds 1..7 are shares of the role's cycles; the rest are key-tile counters
 
 
-def wait_profile_summary(raw):
+def wait_profile_summary(raw, spans=None):
     """Shares of each role's cycles spent waiting, by what completes the
-    barrier (the counters of the wait-profile build: [role][kind])."""
+    barrier (the counters of the wait-profile build: [role][kind]), and the
+    spread of the CTAs' start and end times (spans: [cta][start, end] in ns,
+    zero for CTAs that did not run)."""
     out = {}
+    n = len(WAIT_KINDS)
     for r, role in enumerate(WAIT_ROLES):
-        tot = raw[4 * r]
-        out[role] = {"cycles": tot, **{k: (raw[4 * r + i] / tot if tot else None)
-                                        for i, k in enumerate(WAIT_KINDS) if i}}
+        tot = raw[n * r]
+        out[role] = {"cycles": tot, **{k: (raw[n * r + i] / tot if tot else None)
+                                        for i, k in enumerate(WAIT_KINDS[:WAIT_SHARES]) if i}}
+    mma = out["mma_issuers"]
+    base = n * WAIT_ROLES.index("mma_issuers")
+    lead_n, late_n = raw[base + 9], raw[base + 11]
+    floor = raw[base + 12] / lead_n if lead_n else None
+    mean_wait = raw[base + 2] / lead_n if lead_n else None
+    mma["key_tiles"] = {
+        "waits": lead_n,
+        "mean_lead_cycles": raw[base + 8] / lead_n if lead_n else None,
+        "mean_wait_cycles": mean_wait,
+        "mean_wait_floor_cycles": floor,
+        "late_waits": late_n,
+        "mean_issue_to_landing_cycles_of_late": raw[base + 10] / late_n if late_n else None}
+    # the part of the key-tile waits beyond the floor of a wait whose data is
+    # already there, as a share of the MMA threads' cycles
+    k_beyond = (max(0.0, (mean_wait - floor)) * lead_n / mma["cycles"]) if (lead_n and mma["cycles"]) else None
+    span = None
+    if spans:
+        pairs = [(spans[2 * i], spans[2 * i + 1]) for i in range(len(spans) // 2)
+                 if spans[2 * i] and spans[2 * i + 1]]
+        if pairs:
+            t0 = min(a for a, _ in pairs)
+            ends = sorted(b - t0 for _, b in pairs)
+            span = {"ctas": len(pairs), "first_end_us": ends[0] / 1e3,
+                    "median_end_us": ends[len(ends) // 2] / 1e3, "last_end_us": ends[-1] / 1e3,
+                    "last_start_us": (max(a for a, _ in pairs) - t0) / 1e3}
     return {
         "build": "libdiffattn_waitprof.so: the same sources with -DDIFFATTN_WAIT_PROFILE (clock64 "
                  "around every mbarrier wait of the forward kernel; timings of this run are not "
@@ -862,8 +893,11 @@ def wait_profile_summary(raw):
         "roles": out,
         # the MMA-issuing threads are the consumers of the TMA loads: the share
         # of their time spent waiting for Q/K/V tiles to land
-        "tma_stall_share": out["mma_issuers"]["tma"],
-        "tensor_wait_share_softmax": out["softmax_warps"]["tensor"],
+        "tma_stall_share": (mma["q_load"] or 0) + (mma["k_load"] or 0) + (mma["v_load"] or 0),
+        "k_wait_share_beyond_floor": k_beyond,
+        "cta_span_last_launch": span,
+        "tensor_wait_share_softmax": sum(out["softmax_warps"][k] or 0
+                                         for k in ("item_start", "tensor", "epilogue")),
     }
 
 
@@ -928,10 +962,11 @@ def main(argv=None):
         lib.diffattn_wait_profile.argtypes = [C.POINTER(C.c_ulonglong), C.c_int]
         lib.diffattn_wait_profile.restype = C.c_int
         res = run_ours(args, w, world, rank, local)
-        raw = (C.c_ulonglong * 12)()
-        if lib.diffattn_wait_profile(raw, 12) != 0:
+        n = 3 * len(WAIT_KINDS)
+        raw = (C.c_ulonglong * (n + 2 * WAIT_SPAN_CTAS))()
+        if lib.diffattn_wait_profile(raw, n + 2 * WAIT_SPAN_CTAS) != 0:
             raise RuntimeError("diffattn_wait_profile failed")
-        res = {"wait_profile": wait_profile_summary(list(raw)), "workload": w.name,
+        res = {"wait_profile": wait_profile_summary(list(raw)[:n], list(raw)[n:]), "workload": w.name,
                "steps": args.steps, "warmup": args.warmup,
                "instrumented_kernel_ms_median": res["roofline"]["fwd_ms_median"]}
     else:

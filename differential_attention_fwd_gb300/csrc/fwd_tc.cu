@@ -222,15 +222,30 @@ struct ItemRing {
 // in mbarrier waits, by what completes the barrier, and adds them to
 // g_wait_prof[role][kind] when the CTA ends.  Roles: 0 the TMA producer, 1 the
 // two MMA-issuing threads, 2 the eight softmax warps.  Kinds: 0 the role's
-// cycles from start to end, 1 waits on TMA loads (Q, K, V full), 2 waits on
-// tensor-core products (S full, PV done, O full; stages released by MMA
-// commits), 3 waits on other warps (P full, O read out, the item ring, the
-// epilogue's exchanges).
-enum : int { kWaitTotal = 0, kWaitTma = 1, kWaitTensor = 2, kWaitPeer = 3 };
+// cycles from start to end; waits on TMA loads: 1 Q full, 2 K full, 3 V full;
+// waits on tensor-core work: 4 at an item's start (the first S full; the
+// producer's Q slot released by the item's last score product), 5 within an
+// item (later S full, PV done; K and V stages released by MMA commits), 6 the
+// item's last products before the epilogue (O full); 7 waits on other warps
+// (P full, O read out, the item ring, the epilogue's exchanges).  For the key
+// tiles the MMA threads also record the lead of each wait, the cycles from the
+// tile's TMA issue to the start of the wait (8: sum, 9: count), and for the
+// waits longer than 64 cycles the cycles from issue to landing (10: sum, 11:
+// count); and, right after each key-tile wait, the time of a second wait on the
+// same (now complete) phase: the floor of a wait that finds its data there
+// (12: sum).  Each CTA also stamps the global timer at its start and end
+// (g_cta_span), which shows the spread of the CTAs' finishing times.
+enum : int {
+    kWaitTotal = 0, kWaitQ = 1, kWaitK = 2, kWaitV = 3, kWaitItemStart = 4, kWaitTensor = 5,
+    kWaitEpilogue = 6, kWaitPeer = 7, kLeadSum = 8, kLeadCount = 9, kLateSum = 10,
+    kLateCount = 11, kFloorSum = 12, kWaitKinds = 13
+};
+constexpr int kSpanCtas = 1024;
 #ifdef DIFFATTN_WAIT_PROFILE
-__device__ unsigned long long g_wait_prof[3][4];
+__device__ unsigned long long g_wait_prof[3][kWaitKinds];
+__device__ unsigned long long g_cta_span[kSpanCtas][2];
 struct WaitProf {
-    unsigned long long c[4] = {0, 0, 0, 0};
+    unsigned long long c[kWaitKinds] = {};
     long long t0 = 0;
     __device__ __forceinline__ void start() { t0 = clock64(); }
     template <class F>
@@ -240,19 +255,41 @@ struct WaitProf {
         c[kind] += (unsigned long long)(clock64() - a);
         return r;
     }
+    // a key-tile wait: its lead after the TMA issue stamped in `issued`
+    template <class F>
+    __device__ __forceinline__ bool key_wait(long long issued, F&& f) {
+        const long long a = clock64();
+        const bool r = f();
+        const long long b = clock64();
+        c[kWaitK] += (unsigned long long)(b - a);
+        c[kLeadSum] += (unsigned long long)(a > issued ? a - issued : 0);
+        c[kLeadCount] += 1;
+        if (b - a > 64) {
+            c[kLateSum] += (unsigned long long)(b - issued);
+            c[kLateCount] += 1;
+        }
+        const long long f0 = clock64();
+        f();                                   // the same phase again: complete
+        c[kFloorSum] += (unsigned long long)(clock64() - f0);
+        return r;
+    }
     __device__ __forceinline__ void flush(int role, bool reporter) {
         c[kWaitTotal] = (unsigned long long)(clock64() - t0);
         if (reporter)
-            for (int i = 0; i < 4; ++i) atomicAdd(&g_wait_prof[role][i], c[i]);
+            for (int i = 0; i < kWaitKinds; ++i) atomicAdd(&g_wait_prof[role][i], c[i]);
     }
 };
 #define TIMED_WAIT(wp, kind, expr) (wp).timed((kind), [&]() -> bool { return (expr); })
+#define KEY_WAIT(wp, stage, expr) (wp).key_wait(kissue[stage], [&]() -> bool { return (expr); })
+#define STAMP_KEY_ISSUE(stage) (kissue[stage] = clock64())
 #else
 struct WaitProf {
     __device__ __forceinline__ void start() {}
     __device__ __forceinline__ void flush(int, bool) {}
 };
 #define TIMED_WAIT(wp, kind, expr) (expr)
+#define KEY_WAIT(wp, stage, expr) (expr)
+#define STAMP_KEY_ISSUE(stage) ((void)0)
 #endif
 
 // Row max of one thread's 64 scores (four independent chains of
@@ -306,6 +343,9 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
     uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + REL_TMEM_PTR);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + REL_ABORT);
     float* inv_l = reinterpret_cast<float*>(smem + C::OFF_BAR + REL_INVL);
+#ifdef DIFFATTN_WAIT_PROFILE
+    __shared__ volatile long long kissue[KSTAGES];    // TMA issue time of each key stage
+#endif
     const bool k_shared = p.k_shared != 0;
     const int kstages = C::kstages(k_shared);
     const uint32_t kstride = C::kstride(k_shared);
@@ -313,6 +353,9 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
     const uint32_t warp = warp_id();
     const uint32_t lane = threadIdx.x & 31;
     const AbortState ab{abort_flag, p.status};
+#ifdef DIFFATTN_WAIT_PROFILE
+    if (threadIdx.x == 0 && blockIdx.x < kSpanCtas) g_cta_span[blockIdx.x][0] = globaltimer_ns();
+#endif
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[BAR_Q_FULL], 1);
@@ -403,7 +446,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 const Item it = decode_item(idx, p);
                 idx = claim();
                 if (!first) {
-                    if (!(ok = TIMED_WAIT(wp, kWaitTensor, mbar_wait(&bars[BAR_Q_EMPTY], qph, ab)))) break;
+                    if (!(ok = TIMED_WAIT(wp, kWaitItemStart, mbar_wait(&bars[BAR_Q_EMPTY], qph, ab)))) break;
                     qph ^= 1;
                 }
                 first = false;
@@ -431,6 +474,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                             tma_load_4d(kdst + C::K_BYTES + pn * K_PANEL, &tm_k2, &bars[BAR_K_FULL + kst],
                                         pn * 64, j * BN, hk, it.b);
                     }
+                    STAMP_KEY_ISSUE(kst);
                     ++armed_k[kst];
                     if (++kst == (uint32_t)kstages) { kst = 0; kph ^= 1; }
 
@@ -499,11 +543,11 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 if (!(ok = TIMED_WAIT(wp, kWaitPeer, ring.get_one(k, idx))) || idx < 0) break;
                 const Item it = decode_item(idx, p);
                 const int n = it.n_kv;
-                if (!(ok = TIMED_WAIT(wp, kWaitTma, mbar_wait(&bars[BAR_Q_FULL], qph, ab)))) break;
+                if (!(ok = TIMED_WAIT(wp, kWaitQ, mbar_wait(&bars[BAR_Q_FULL], qph, ab)))) break;
                 qph ^= 1;
                 // S_b(0), S_b(1) into buffers 0 and 1
                 for (int t = 0; t < 2 && t < n; ++t) {
-                    if (!(ok = TIMED_WAIT(wp, kWaitTma, mbar_wait(&bars[BAR_K_FULL + kst], kph, ab)))) break;
+                    if (!(ok = KEY_WAIT(wp, kst, mbar_wait(&bars[BAR_K_FULL + kst], kph, ab)))) break;
                     tc_fence_after();
                     issue_s(kst, t);
                     mma_commit(&bars[BAR_S_FULL + 2 * br + t]);
@@ -515,16 +559,23 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
 
                 for (int j = 0; j < n; ++j) {
                     const int buf = j & 1;
+                    // The tiles PV_b(j) and S_b(j+2) read were loaded long
+                    // before P_b(j) is ready (the rings run far ahead), so
+                    // their barriers are checked first: once P_b(j) arrives,
+                    // both products issue with no other wait in between.
+                    if (!(ok = TIMED_WAIT(wp, kWaitV, mbar_wait(&bars[BAR_V_FULL + vst], vph, ab)))) break;
+                    if (j + 2 < n &&
+                        !(ok = KEY_WAIT(wp, kst, mbar_wait(&bars[BAR_K_FULL + kst], kph, ab))))
+                        break;
+                    if (j == 0 && !first) {
+                        if (!(ok = TIMED_WAIT(wp, kWaitPeer, mbar_wait(&bars[BAR_O_EMPTY], oeph, ab)))) break;
+                        oeph ^= 1;
+                    }
                     // O_b += P_b(j) V(j)
                     if (!(ok = TIMED_WAIT(wp, kWaitPeer,
                                           mbar_wait(&bars[BAR_P_FULL + 2 * br + buf], (pph >> buf) & 1u, ab))))
                         break;
                     pph ^= 1u << buf;
-                    if (j == 0 && !first) {
-                        if (!(ok = TIMED_WAIT(wp, kWaitPeer, mbar_wait(&bars[BAR_O_EMPTY], oeph, ab)))) break;
-                        oeph ^= 1;
-                    }
-                    if (!(ok = TIMED_WAIT(wp, kWaitTma, mbar_wait(&bars[BAR_V_FULL + vst], vph, ab)))) break;
                     tc_fence_after();
                     issue_pv(vst, buf, j > 0);
                     mma_commit(&bars[BAR_PV_DONE + br]);
@@ -532,8 +583,6 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     if (++vst == (uint32_t)C::VSTAGES) { vst = 0; vph ^= 1; }
                     // S_b(j+2) into the buffer P_b(j) was just read from
                     if (j + 2 < n) {
-                        if (!(ok = TIMED_WAIT(wp, kWaitTma, mbar_wait(&bars[BAR_K_FULL + kst], kph, ab)))) break;
-                        tc_fence_after();
                         issue_s(kst, buf);
                         mma_commit(&bars[BAR_S_FULL + 2 * br + buf]);
                         mma_commit(&bars[BAR_K_EMPTY + kst]);
@@ -583,7 +632,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             for (int j = 0; j < it.n_kv; ++j) {
                 const int buf = j & 1;
                 const uint32_t tS = lane_base + tm_s(br, buf);
-                if (!(ok = TIMED_WAIT(wp, kWaitTensor,
+                if (!(ok = TIMED_WAIT(wp, j == 0 ? kWaitItemStart : kWaitTensor,
                                       mbar_wait_warp(&bars[BAR_S_FULL + 2 * br + buf], (sph >> buf) & 1u, ab))))
                     break;
                 sph ^= 1u << buf;
@@ -670,7 +719,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             if (idx >= 0) next = decode_item(idx, p);
 
             // ---------------------------------------------------- epilogue
-            if (!(ok = TIMED_WAIT(wp, kWaitTensor, mbar_wait_warp(&bars[BAR_O_FULL], ofph, ab)))) break;
+            if (!(ok = TIMED_WAIT(wp, kWaitEpilogue, mbar_wait_warp(&bars[BAR_O_FULL], ofph, ab)))) break;
             ofph ^= 1;
             tc_fence_after();
             if (p.stats) {
@@ -831,6 +880,9 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+#ifdef DIFFATTN_WAIT_PROFILE
+    if (threadIdx.x == 0 && blockIdx.x < kSpanCtas) g_cta_span[blockIdx.x][1] = globaltimer_ns();
+#endif
     if (warp == 9) tmem_dealloc(tmem_base, TMEM_COLS);
     // The last CTA to finish returns the scheduler counter to zero for the
     // next launch that uses it.
@@ -859,16 +911,24 @@ int launch_hd(const CUtensorMap* maps, const TcParams& p, int grid, cudaStream_t
 }  // namespace
 
 #ifdef DIFFATTN_WAIT_PROFILE
-// The wait profile of the launches since the previous call ([3 roles][4
-// kinds], see WaitProf), copied to `out` and cleared.  Only in the build with
-// -DDIFFATTN_WAIT_PROFILE.
+// The wait profile of the launches since the previous call ([3 roles][13
+// kinds], see WaitProf), copied to `out` and cleared; then the start and end
+// global-timer stamps of the last launch's CTAs ([1024][2], zero past the
+// grid).  Only in the build with -DDIFFATTN_WAIT_PROFILE.
 extern "C" int diffattn_wait_profile(unsigned long long* out, int n) {
-    if (!out || n < 12) return -1;
+    constexpr int kN = 3 * tc::kWaitKinds;
+    constexpr int kS = 2 * tc::kSpanCtas;
+    if (!out || n < kN + kS) return -1;
     if (cudaDeviceSynchronize() != cudaSuccess ||
-        cudaMemcpyFromSymbol(out, tc::g_wait_prof, 12 * sizeof(unsigned long long)) != cudaSuccess)
+        cudaMemcpyFromSymbol(out, tc::g_wait_prof, kN * sizeof(unsigned long long)) != cudaSuccess ||
+        cudaMemcpyFromSymbol(out + kN, tc::g_cta_span, kS * sizeof(unsigned long long)) != cudaSuccess)
         return -3;
-    unsigned long long zero[12] = {};
-    return cudaMemcpyToSymbol(tc::g_wait_prof, zero, sizeof(zero)) == cudaSuccess ? 0 : -3;
+    static unsigned long long zero[kN + kS] = {};
+    return cudaMemcpyToSymbol(tc::g_wait_prof, zero, kN * sizeof(unsigned long long)) == cudaSuccess &&
+                   cudaMemcpyToSymbol(tc::g_cta_span, zero, kS * sizeof(unsigned long long)) ==
+                       cudaSuccess
+               ? 0
+               : -3;
 }
 #endif
 

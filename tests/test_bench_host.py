@@ -120,11 +120,19 @@ def test_clock_scaled_peak():
 
 
 def test_wait_profile_summary_shares():
-    raw = [1000, 0, 600, 100,   # producer: total, tma, tensor, peer
-           2000, 500, 0, 700,   # MMA issuers
-           8000, 0, 2000, 400]  # softmax warps
-    s = bench.wait_profile_summary(raw)
+    # [role][total, q, k, v, item_start, tensor, epilogue, peer]
+    raw = [1000, 0, 0, 0, 100, 500, 0, 100, 0, 0, 0, 0, 0,           # producer
+           2000, 100, 200, 200, 0, 0, 0, 700, 900, 3, 400, 2, 150,   # MMA issuers
+           8000, 0, 0, 0, 400, 1200, 400, 400, 0, 0, 0, 0, 0]        # softmax warps
+    spans = [1000, 5000, 1200, 9000, 0, 0]
+    s = bench.wait_profile_summary(raw, spans)
     assert s["tma_stall_share"] == pytest.approx(0.25)
-    assert s["roles"]["producer"]["tensor"] == pytest.approx(0.6)
+    assert s["roles"]["producer"]["tensor"] == pytest.approx(0.5)
     assert s["roles"]["softmax_warps"]["peer"] == pytest.approx(0.05)
     assert s["tensor_wait_share_softmax"] == pytest.approx(0.25)
+    kt = s["roles"]["mma_issuers"]["key_tiles"]
+    assert kt["mean_lead_cycles"] == pytest.approx(300) and kt["late_waits"] == 2
+    # key waits: 200 cycles over 3 waits with a floor of 50 each -> 50 cycles beyond it
+    assert s["k_wait_share_beyond_floor"] == pytest.approx(50 / 2000)
+    assert s["cta_span_last_launch"]["ctas"] == 2
+    assert s["cta_span_last_launch"]["last_end_us"] == pytest.approx(8.0)
