@@ -43,6 +43,7 @@
 // Every mbarrier wait is bounded (see ptx.cuh); on expiry the kernel records
 // DIFFATTN_ERR_TIMEOUT in the status word, drains and frees TMEM.
 #include "kernels.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 
 #include <cmath>
@@ -131,6 +132,9 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do,
                        const BwdTcParams p) {
+    // The dK/dV kernel that follows reads nothing this kernel writes: it may
+    // take each SM as soon as this kernel's CTA there has finished.
+    pdl_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -839,10 +843,25 @@ int launch_bwd_tc(const CUtensorMap* maps, const BwdTcParams& p, int num_sms, cu
                                  dq::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3],
                                                            maps[4], maps[5], p);
     if (cudaGetLastError() != cudaSuccess) return -1;
-    dkdv::diffattn_bwd_dkdv_kernel<<<kv_items < num_sms ? kv_items : num_sms, NUM_THREADS,
-                                     dkdv::SMEM_BYTES, stream>>>(maps[6], maps[7], maps[8],
-                                                                 maps[9], maps[10], maps[11], p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    // The dK/dV kernel depends on the row statistics (complete before the dQ
+    // kernel started), not on dQ: it is launched as a programmatic dependent of
+    // the dQ kernel, so its CTAs fill the SMs the dQ kernel's tail leaves idle.
+    // One CTA of either kernel takes a whole SM's registers, so they never
+    // share an SM (nor its tensor memory).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kv_items < num_sms ? kv_items : num_sms);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = dkdv::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dkdv::diffattn_bwd_dkdv_kernel, maps[6], maps[7], maps[8], maps[9],
+                              maps[10], maps[11], p) == cudaSuccess
+               ? 0
+               : -1;
 }
 
 }  // namespace diffattn

@@ -240,8 +240,8 @@ enum : int {
     kWaitEpilogue = 6, kWaitPeer = 7, kLeadSum = 8, kLeadCount = 9, kLateSum = 10,
     kLateCount = 11, kFloorSum = 12, kWaitKinds = 13
 };
-constexpr int kSpanCtas = 1024;
 #ifdef DIFFATTN_WAIT_PROFILE
+constexpr int kSpanCtas = 1024;
 __device__ unsigned long long g_wait_prof[3][kWaitKinds];
 __device__ unsigned long long g_cta_span[kSpanCtas][2];
 struct WaitProf {

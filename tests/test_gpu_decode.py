@@ -53,6 +53,11 @@ def test_decode_matches_forward_last_rows():
     dec = da.differential_attention_decode(dev[0][:, :, -3:], dev[1], dev[2][:, :, -3:], dev[3],
                                            dev[4], 0.5, causal=True)
     assert float((full[:, :, -3:].float() - dec.float()).abs().max()) <= 2e-2
+    # both against the oracle's rows 697..699 of the full sequence
+    want = oracle.differential_attention(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.5, True,
+                                         rows=[697, 698, 699])
+    assert_close(to_numpy(dec), want, "bf16", "decode last rows vs oracle")
+    assert_close(to_numpy(full[:, :, -3:]), want, "bf16", "forward last rows vs oracle")
 
 
 def test_decode_epilogue_and_device_lambda():

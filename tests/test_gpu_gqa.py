@@ -117,6 +117,10 @@ def test_decode_grouped_matches_forward_last_rows():
     dec = da.differential_attention_decode(dev[0][:, :, -2:], dev[1], dev[2][:, :, -2:], dev[3],
                                            dev[4], 0.5, causal=True)
     assert float((full[:, :, -2:].float() - dec.float()).abs().max()) <= 2e-2
+    want = oracle.differential_attention(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.5, True,
+                                         rows=[638, 639])
+    assert_close(to_numpy(dec), want, "bf16", "grouped decode last rows vs oracle")
+    assert_close(to_numpy(full[:, :, -2:]), want, "bf16", "grouped forward last rows vs oracle")
 
 
 def test_grouped_heads_rejected_shapes():
