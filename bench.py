@@ -845,7 +845,10 @@ def run_decode(args, world, rank, local):
 
 WAIT_ROLES = ("producer", "mma_issuers", "softmax_warps")
 WAIT_KINDS = ("total_cycles", "q_load", "k_load", "v_load", "item_start", "tensor", "epilogue", "peer",
-              "k_lead_sum", "k_lead_count", "k_late_sum", "k_late_count", "k_floor_sum")
+              "k_lead_sum", "k_lead_count", "k_late_sum", "k_late_count", "k_floor_sum",
+              "first_tile_busy", "tile_busy", "epilogue_busy", "tile_count", "item_count",
+              "epilogue_o_load", "epilogue_l_exchange", "epilogue_math", "epilogue_stage_wait",
+              "epilogue_store")
 WAIT_SPAN_CTAS = 1024
 WAIT_SHARES = 8     # kinds 1..7 are shares of the role's cycles; the rest are key-tile counters
 
@@ -876,6 +879,19 @@ def wait_profile_summary(raw, spans=None):
     # the part of the key-tile waits beyond the floor of a wait whose data is
     # already there, as a share of the MMA threads' cycles
     k_beyond = (max(0.0, (mean_wait - floor)) * lead_n / mma["cycles"]) if (lead_n and mma["cycles"]) else None
+    sm = n * WAIT_ROLES.index("softmax_warps")
+    tiles, items = raw[sm + 16], raw[sm + 17]
+    if tiles and items:
+        # per warp: first tiles are one per item, the rest are tiles - items
+        out["softmax_warps"]["per_warp_cycles"] = {
+            "first_tile": raw[sm + 13] / items,
+            "other_tile": raw[sm + 14] / max(1, tiles - items),
+            "epilogue": raw[sm + 15] / items,
+            "epilogue_o_load": raw[sm + 18] / items,
+            "epilogue_l_exchange": raw[sm + 19] / items,
+            "epilogue_math": raw[sm + 20] / items,
+            "epilogue_stage_wait": raw[sm + 21] / items,
+            "epilogue_store": raw[sm + 22] / items}
     span = None
     if spans:
         pairs = [(spans[2 * i], spans[2 * i + 1]) for i in range(len(spans) // 2)

@@ -234,11 +234,19 @@ struct ItemRing {
 // count); and, right after each key-tile wait, the time of a second wait on the
 // same (now complete) phase: the floor of a wait that finds its data there
 // (12: sum).  Each CTA also stamps the global timer at its start and end
-// (g_cta_span), which shows the spread of the CTAs' finishing times.
+// (g_cta_span), which shows the spread of the CTAs' finishing times.  The
+// softmax warps also time their work outside waits: an item's first tile (13),
+// its other tiles (14), each from the score wait to the P hand-off, and the
+// epilogue from the O wait to the output store (15); with the tile and item
+// counts (16, 17); and the epilogue's steps: O read out of TMEM (18), the
+// exchange of 1/l with the other warpgroup (19), the arithmetic (20), the
+// wait for the staging buffer (21) and the staging writes with the store (22).
 enum : int {
     kWaitTotal = 0, kWaitQ = 1, kWaitK = 2, kWaitV = 3, kWaitItemStart = 4, kWaitTensor = 5,
     kWaitEpilogue = 6, kWaitPeer = 7, kLeadSum = 8, kLeadCount = 9, kLateSum = 10,
-    kLateCount = 11, kFloorSum = 12, kWaitKinds = 13
+    kLateCount = 11, kFloorSum = 12, kFirstTileBusy = 13, kTileBusy = 14, kEpilogueBusy = 15,
+    kTileCount = 16, kItemCount = 17, kEpiLoad = 18, kEpiSync = 19, kEpiMath = 20,
+    kEpiStageWait = 21, kEpiStore = 22, kWaitKinds = 23
 };
 #ifdef DIFFATTN_WAIT_PROFILE
 constexpr int kSpanCtas = 1024;
@@ -282,6 +290,9 @@ struct WaitProf {
 #define TIMED_WAIT(wp, kind, expr) (wp).timed((kind), [&]() -> bool { return (expr); })
 #define KEY_WAIT(wp, stage, expr) (wp).key_wait(kissue[stage], [&]() -> bool { return (expr); })
 #define STAMP_KEY_ISSUE(stage) (kissue[stage] = clock64())
+#define PROF_MARK(var) const long long var = clock64()
+#define PROF_ADD(wp, kind, since) ((wp).c[kind] += (unsigned long long)(clock64() - (since)))
+#define PROF_COUNT(wp, kind) ((wp).c[kind] += 1)
 #else
 struct WaitProf {
     __device__ __forceinline__ void start() {}
@@ -290,6 +301,9 @@ struct WaitProf {
 #define TIMED_WAIT(wp, kind, expr) (expr)
 #define KEY_WAIT(wp, stage, expr) (expr)
 #define STAMP_KEY_ISSUE(stage) ((void)0)
+#define PROF_MARK(var) ((void)0)
+#define PROF_ADD(wp, kind, since) ((void)0)
+#define PROF_COUNT(wp, kind) ((void)0)
 #endif
 
 // Row max of one thread's 64 scores (four independent chains of
@@ -635,6 +649,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 if (!(ok = TIMED_WAIT(wp, j == 0 ? kWaitItemStart : kWaitTensor,
                                       mbar_wait_warp(&bars[BAR_S_FULL + 2 * br + buf], (sph >> buf) & 1u, ab))))
                     break;
+                PROF_MARK(tile_t0);
                 sph ^= 1u << buf;
                 tc_fence_after();
                 uint32_t u[64];
@@ -710,8 +725,11 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[BAR_P_FULL + 2 * br + buf]);
+                PROF_ADD(wp, j == 0 ? kFirstTileBusy : kTileBusy, tile_t0);
+                PROF_COUNT(wp, kTileCount);
             }
             if (!ok) break;
+            PROF_COUNT(wp, kItemCount);
             pv_count += it.n_kv;
             // The next item is fetched and decoded here, while the item's last
             // PV products complete, rather than after the epilogue.
@@ -720,6 +738,7 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
 
             // ---------------------------------------------------- epilogue
             if (!(ok = TIMED_WAIT(wp, kWaitEpilogue, mbar_wait_warp(&bars[BAR_O_FULL], ofph, ab)))) break;
+            PROF_MARK(epi_t0);
             ofph ^= 1;
             tc_fence_after();
             if (p.stats) {
@@ -769,6 +788,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             tmem_ld32(lane_base + TM_O + 128 + c0, &o2[0]);
             tmem_ld32(lane_base + TM_O + 128 + c0 + 32, &o2[32]);
             tmem_wait_ld();
+            PROF_ADD(wp, kEpiLoad, epi_t0);
+            PROF_MARK(sync_t0);
             // O is in registers: the next item's PV may overwrite TMEM.
             tc_fence_before();
             __syncwarp();
@@ -778,6 +799,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             }
             if (!(ok = TIMED_WAIT(wp, kWaitPeer, mbar_wait_warp(&bars[BAR_L_READY], lph, ab)))) break;
             lph ^= 1;
+            PROF_ADD(wp, kEpiSync, sync_t0);
+            PROF_MARK(math_t0);
             const float inv1 = inv_l[row];
             const float inv2 = inv_l[BM + row];
             if (p.out2 && q < p.T) {
@@ -796,13 +819,15 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 p.lse[(((int64_t)it.b * p.H + it.h) * p.T + q) * 2 + br] =
                     (m_run + log2f(l)) * 0.6931471805599453f;
             }
-            // O = O1 / l1 - lambda O2 / l2 for this thread's 64 columns
+            // O = O1 / l1 - lambda O2 / l2 for this thread's 64 columns: a = O1 / l1
+            // and b = O2 / l2 rounded, then a - lambda b in one fused step
+            // (identical branches at lambda = 1 give a = b, hence exactly 0)
             float r[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
                 const float a = __fmul_rn(__uint_as_float(o1[c]), inv1);
                 const float bb = __fmul_rn(__uint_as_float(o2[c]), inv2);
-                r[c] = __fsub_rn(a, __fmul_rn(lam, bb));
+                r[c] = __fmaf_rn(bb, -lam, a);
             }
             if (p.norm != kNormNone) {
                 // Per-head normalisation over the row's 2D = 128 channels; the
@@ -855,8 +880,12 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
             // swizzled rows, as the output tensor map expects) and write them
             // with one TMA store; rows at or past T are clipped by the TMA unit.
             uint8_t* stage = smem + C::OFF_OUT + br * (OUT_BYTES / 2) + quad * 4096;
+            PROF_ADD(wp, kEpiMath, math_t0);
+            PROF_MARK(stage_t0);
             if (lane == 0) bulk_wait_read_all();     // the previous store has read the buffer
             __syncwarp();
+            PROF_ADD(wp, kEpiStageWait, stage_t0);
+            PROF_MARK(store_t0);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int c = 8 * i;
@@ -870,6 +899,8 @@ diffattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 tma_store_4d(&tm_o, stage, c0, it.qt * BM + (int)quad * 32, it.h, it.b);
                 bulk_commit();
             }
+            PROF_ADD(wp, kEpiStore, store_t0);
+            PROF_ADD(wp, kEpilogueBusy, epi_t0);
         }
         // Every output store must be complete before the CTA exits.
         if (lane == 0) bulk_wait_all();
@@ -911,7 +942,7 @@ int launch_hd(const CUtensorMap* maps, const TcParams& p, int grid, cudaStream_t
 }  // namespace
 
 #ifdef DIFFATTN_WAIT_PROFILE
-// The wait profile of the launches since the previous call ([3 roles][13
+// The wait profile of the launches since the previous call ([3 roles][23
 // kinds], see WaitProf), copied to `out` and cleared; then the start and end
 // global-timer stamps of the last launch's CTAs ([1024][2], zero past the
 // grid).  Only in the build with -DDIFFATTN_WAIT_PROFILE.

@@ -121,9 +121,11 @@ def test_clock_scaled_peak():
 
 def test_wait_profile_summary_shares():
     # [role][total, q, k, v, item_start, tensor, epilogue, peer]
-    raw = [1000, 0, 0, 0, 100, 500, 0, 100, 0, 0, 0, 0, 0,           # producer
-           2000, 100, 200, 200, 0, 0, 0, 700, 900, 3, 400, 2, 150,   # MMA issuers
-           8000, 0, 0, 0, 400, 1200, 400, 400, 0, 0, 0, 0, 0]        # softmax warps
+    z5 = [0] * 10
+    raw = ([1000, 0, 0, 0, 100, 500, 0, 100, 0, 0, 0, 0, 0] + z5 +            # producer
+           [2000, 100, 200, 200, 0, 0, 0, 700, 900, 3, 400, 2, 150] + z5 +    # MMA issuers
+           [8000, 0, 0, 0, 400, 1200, 400, 400, 0, 0, 0, 0, 0,                # softmax warps
+            300, 900, 200, 10, 2, 60, 40, 30, 20, 10])
     spans = [1000, 5000, 1200, 9000, 0, 0]
     s = bench.wait_profile_summary(raw, spans)
     assert s["tma_stall_share"] == pytest.approx(0.25)
@@ -136,3 +138,6 @@ def test_wait_profile_summary_shares():
     assert s["k_wait_share_beyond_floor"] == pytest.approx(50 / 2000)
     assert s["cta_span_last_launch"]["ctas"] == 2
     assert s["cta_span_last_launch"]["last_end_us"] == pytest.approx(8.0)
+    pw = s["roles"]["softmax_warps"]["per_warp_cycles"]
+    assert pw["first_tile"] == pytest.approx(150) and pw["other_tile"] == pytest.approx(112.5)
+    assert pw["epilogue"] == pytest.approx(100) and pw["epilogue_o_load"] == pytest.approx(30)
