@@ -24,7 +24,7 @@ constexpr size_t kWorkspaceBytes = 64;
 
 struct DeviceState {
     bool ready = false;
-    void* ctx = nullptr;          // the context the addresses below belong to
+    unsigned long long ctx = 0;   // ID of the context the addresses below belong to
     int num_sms = 0;
     uint32_t* status = nullptr;   // device address of g_status_word
 };
@@ -40,11 +40,14 @@ EncodeTiledFn g_encode = nullptr;
 
 }  // namespace
 
-// The calling thread's current CUDA context (driver handle), nullptr if none
-// or if the driver entry point cannot be found.
-void* current_context() {
+// A unique identifier of the calling thread's current CUDA context (the
+// driver's context ID, never reused within the process, so a context created
+// again after a device reset gets a new one), 0 if there is no current context
+// or the driver entry points cannot be found.
+unsigned long long current_context() {
     using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-    static CtxGetCurrentFn fn = [] {
+    using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static CtxGetCurrentFn get_current = [] {
         void* f = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
@@ -52,9 +55,20 @@ void* current_context() {
             return static_cast<CtxGetCurrentFn>(nullptr);
         return reinterpret_cast<CtxGetCurrentFn>(f);
     }();
+    static CtxGetIdFn get_id = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            return static_cast<CtxGetIdFn>(nullptr);
+        return reinterpret_cast<CtxGetIdFn>(f);
+    }();
     CUcontext c = nullptr;
-    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
-    return c;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c ||
+        get_id(c, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
 }
 
 namespace {
@@ -62,13 +76,13 @@ namespace {
 int device_state(DeviceState** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DIFFATTN_ERR_CUDA;
-    void* ctx = current_context();
+    const unsigned long long ctx = current_context();
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState& st = g_devices[dev];
     // A device reset or another current context loads the library's module
     // again, possibly at other addresses: look them up again then.  (No
     // current context yet: the lookup below makes the primary one current.)
-    if (!st.ready || ctx == nullptr || st.ctx != ctx) {
+    if (!st.ready || ctx == 0 || st.ctx != ctx) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return DIFFATTN_ERR_CUDA;

@@ -208,8 +208,8 @@ int launch_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, cons
                       float* dlk2, cudaStream_t stream);
 
 // Host helpers of the C-ABI layer (api.cu).
-// The calling thread's current CUDA context, nullptr if none.
-void* current_context();
+// Unique ID of the calling thread's current CUDA context, 0 if none.
+unsigned long long current_context();
 // Every argument check diffattn_decode makes except those of its workspace;
 // on success *work_bytes receives the workspace the call needs.
 int decode_check(const diffattn_kv_desc* desc, const void* q1, const void* k1, const void* q2,

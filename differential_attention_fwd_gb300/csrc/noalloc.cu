@@ -30,7 +30,7 @@ static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 struct Scratch {
-    void* ctx = nullptr;      // the context the address belongs to
+    unsigned long long ctx = 0;   // ID of the context the address belongs to
     float* ptr = nullptr;
 };
 Scratch g_scratch[kMaxDevices];
@@ -43,10 +43,10 @@ Scratch g_scratch[kMaxDevices];
 int scratch_for_current_device(float** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DIFFATTN_ERR_CUDA;
-    void* ctx = current_context();
+    const unsigned long long ctx = current_context();
     std::lock_guard<std::mutex> lock(g_mutex);
     Scratch& s = g_scratch[dev];
-    if (!s.ptr || ctx == nullptr || s.ctx != ctx) {
+    if (!s.ptr || ctx == 0 || s.ctx != ctx) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
             return DIFFATTN_ERR_CUDA;
