@@ -225,6 +225,10 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
                 norm_bias is not None or out_scale != 1.0:
             raise ValueError("gradients are available for the bare operation only "
                              "(no out=, norm or out_scale)")
+        if isinstance(value, torch.Tensor) and isinstance(q1, torch.Tensor) and \
+                value.dim() == 4 and q1.dim() == 4 and value.shape[-1] != 2 * q1.shape[-1]:
+            raise ValueError("gradients are available for the operation's own shape, value "
+                             f"width 2D = {2 * q1.shape[-1]} (got {value.shape[-1]})")
         return _DifferentialAttentionFn.apply(q1, k1, q2, k2, value, coefficient, causal,
                                               dynamic_schedule)
     return _forward(q1, k1, q2, k2, value, coefficient, causal, out, dynamic_schedule, norm,

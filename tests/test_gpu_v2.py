@@ -146,3 +146,7 @@ def test_backward_refuses_other_value_widths():
     dout = torch.zeros(1, 2, 64, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ValueError):
         da.differential_attention_backward(*dev, 0.5, dout, True)
+    # autograd refuses at the forward call, not later in the backward
+    q1 = dev[0].clone().requires_grad_()
+    with pytest.raises(ValueError, match="value width"):
+        da.differential_attention(q1, *dev[1:], 0.5)
