@@ -343,8 +343,9 @@ def differential_attention_backward(q1, k1, q2, k2, v, lam: float, dout, causal:
     float64.
 
     Shapes as differential_attention (q1, q2 [B, H, T, D]; k1, k2 [B, H_kv, T,
-    D]; v [B, H_kv, T, 2D]); dout [B, H, T, 2D].  Returns dq1, dk1, dq2, dk2,
-    dv with the shapes of their inputs, and dlambda (a float).
+    D]; v [B, H_kv, T, Dv], Dv = 2D in the operation's own shape); dout [B, H,
+    T, Dv].  Returns dq1, dk1, dq2, dk2, dv with the shapes of their inputs, and
+    dlambda (a float).
 
     kv_heads: optional list of (b, hk) key/value heads to evaluate; then every
     query head that reads them is processed, the gradients of the other heads
@@ -354,14 +355,15 @@ def differential_attention_backward(q1, k1, q2, k2, v, lam: float, dout, causal:
     B, H, T, D = q1.shape
     Hk = H // g
     dout = _as64(dout)
-    if dout.shape != (B, H, T, 2 * D):
-        raise ValueError("dout must be [B, H, T, 2D]")
+    Dv = v.shape[3]
+    if dout.shape != (B, H, T, Dv):
+        raise ValueError("dout must be [B, H, T, Dv], Dv the width of V")
     lam = float(lam)
     dq1 = np.zeros((B, H, T, D))
     dq2 = np.zeros((B, H, T, D))
     dk1 = np.zeros((B, Hk, T, D))
     dk2 = np.zeros((B, Hk, T, D))
-    dv = np.zeros((B, Hk, T, 2 * D))
+    dv = np.zeros((B, Hk, T, Dv))
     dlam = 0.0
     todo = [(b, hk) for b in range(B) for hk in range(Hk)] if kv_heads is None else list(kv_heads)
     for b, hk in todo:

@@ -26,12 +26,13 @@ import oracle
 from oracle import diffattn_oracle as O
 
 
-def inputs(B, H, Hk, T, D, seed):
+def inputs(B, H, Hk, T, D, seed, Dv=None):
     rng = np.random.default_rng(seed)
+    Dv = 2 * D if Dv is None else Dv
     q1, q2 = rng.standard_normal((2, B, H, T, D))
     k1, k2 = rng.standard_normal((2, B, Hk, T, D))
-    v = rng.standard_normal((B, Hk, T, 2 * D))
-    dout = rng.standard_normal((B, H, T, 2 * D))
+    v = rng.standard_normal((B, Hk, T, Dv))
+    dout = rng.standard_normal((B, H, T, Dv))
     return q1, k1, q2, k2, v, dout
 
 
@@ -77,6 +78,23 @@ def test_backward_matches_torch_autograd(case):
         assert a.shape == b.shape, name
         assert np.max(np.abs(a - b)) <= 1e-10, name
     assert abs(got[5] - ref[5]) <= 1e-10 * max(1.0, abs(ref[5]))
+
+
+@pytest.mark.parametrize("case", [(1, 4, 2, 9, 4, 4, 0.7, True), (2, 2, 1, 7, 3, 3, -0.4, False),
+                                  (1, 2, 2, 6, 4, 5, 1.2, True)])
+def test_backward_value_width_matches_torch_autograd(case):
+    # the DIFF V2 head's value width (Dv = D) and another width: the chain
+    # rule is the same for any width of V
+    B, H, Hk, T, D, Dv, lam, causal = case
+    q1, k1, q2, k2, v, dout = inputs(B, H, Hk, T, D, seed=T * 7 + Dv, Dv=Dv)
+    got = oracle.differential_attention_backward(q1, k1, q2, k2, v, lam, dout, causal)
+    ref = autograd_grads(q1, k1, q2, k2, v, dout, lam, causal)
+    for name, a, b in zip(("dq1", "dk1", "dq2", "dk2", "dv"), got[:5], ref[:5]):
+        assert a.shape == b.shape, name
+        assert np.max(np.abs(a - b)) <= 1e-10, name
+    assert abs(got[5] - ref[5]) <= 1e-10 * max(1.0, abs(ref[5]))
+    with pytest.raises(ValueError):
+        oracle.differential_attention_backward(q1, k1, q2, k2, v, lam, dout[..., :-1], causal)
 
 
 def test_backward_finite_differences():
