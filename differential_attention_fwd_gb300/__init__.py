@@ -225,10 +225,6 @@ def differential_attention(q1: torch.Tensor, k1: torch.Tensor, q2: torch.Tensor,
                 norm_bias is not None or out_scale != 1.0:
             raise ValueError("gradients are available for the bare operation only "
                              "(no out=, norm or out_scale)")
-        if isinstance(value, torch.Tensor) and isinstance(q1, torch.Tensor) and \
-                value.dim() == 4 and q1.dim() == 4 and value.shape[-1] != 2 * q1.shape[-1]:
-            raise ValueError("gradients are available for the operation's own shape, value "
-                             f"width 2D = {2 * q1.shape[-1]} (got {value.shape[-1]})")
         return _DifferentialAttentionFn.apply(q1, k1, q2, k2, value, coefficient, causal,
                                               dynamic_schedule)
     return _forward(q1, k1, q2, k2, value, coefficient, causal, out, dynamic_schedule, norm,
@@ -339,8 +335,9 @@ def differential_attention_backward(q1: torch.Tensor, k1: torch.Tensor, q2: torc
     """Gradients of differential_attention given dout = dL/dO.
 
     Inputs as differential_attention (the forward's inputs and coefficient);
-    dout: [B, H, T, 2D] of the inputs' dtype (the backward takes the
-    operation's own shape, value width 2D).  saved: optional (out, out2,
+    dout: [B, H, T, Dv] of the inputs' dtype (Dv the width of value; the
+    tensor cores take bf16 with D = 64 and Dv = 2D, other shapes run on the
+    CUDA cores).  saved: optional (out, out2,
     lse) from differential_attention_train with the same inputs; with it the
     forward is not recomputed.  Returns (dq1, dk1, dq2, dk2, dvalue,
     dcoefficient): contiguous tensors of the inputs' shapes and dtype, and a
@@ -348,9 +345,10 @@ def differential_attention_backward(q1: torch.Tensor, k1: torch.Tensor, q2: torc
     vectors follow from dcoefficient (see differential_lambda)."""
     (q1, k1, q2, k2, value), dev = _prepare(q1, k1, q2, k2, value)
     B, H, T, D = q1.shape
+    Dv = value.shape[3]
     _require_cuda(dout, "dout")
-    if tuple(dout.shape) != (B, H, T, 2 * D) or dout.dtype != q1.dtype or dout.device != dev:
-        raise ValueError("dout must be [B, H, T, 2D] with the inputs' dtype and device")
+    if tuple(dout.shape) != (B, H, T, Dv) or dout.dtype != q1.dtype or dout.device != dev:
+        raise ValueError("dout must be [B, H, T, Dv] with the inputs' dtype and device")
     if dout.stride(-1) != 1:
         dout = dout.contiguous()
     if saved is not None:

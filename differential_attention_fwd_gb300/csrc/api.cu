@@ -586,8 +586,7 @@ int backward_impl(const diffattn_desc* desc, const void* q1, const void* k1, con
     const bool saved = out != nullptr;
     int rc = validate(desc, q1, k1, q2, k2, v, dout);
     if (rc != DIFFATTN_OK) return rc;
-    // the backward kernels take the operation's own shape, V = 2D
-    if (value_width(desc->Dv, desc->D) != 2 * desc->D) return DIFFATTN_ERR_UNSUPPORTED;
+    const int64_t dv_width = value_width(desc->Dv, desc->D);
     if (!dq1 || !dk1 || !dq2 || !dk2 || !dv || !dlambda) return DIFFATTN_ERR_INVALID;
     if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
     const size_t need = diffattn_bwd_workspace_bytes(desc);
@@ -595,7 +594,8 @@ int backward_impl(const diffattn_desc* desc, const void* q1, const void* k1, con
         return DIFFATTN_ERR_INVALID;
     const diffattn_desc& d = *desc;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (d.D == 64 && select(desc, q1, k1, q2, k2, v, dout) == DIFFATTN_KERNEL_TCGEN05 && aligned16(dq1) &&
+    // the tensor-core backward takes the operation's own shape at D = 64
+    if (d.D == 64 && dv_width == 128 && select(desc, q1, k1, q2, k2, v, dout) == DIFFATTN_KERNEL_TCGEN05 && aligned16(dq1) &&
         aligned16(dk1) && aligned16(dq2) && aligned16(dk2) && aligned16(dv)) {
         DeviceState* dev = nullptr;
         rc = device_state(&dev);
@@ -712,6 +712,7 @@ int backward_impl(const diffattn_desc* desc, const void* q1, const void* k1, con
     p.Hk = (int)(d.H / p.kv_group);
     p.T = (int)d.T;
     p.D = (int)d.D;
+    p.Dv = (int)dv_width;
     p.causal = causal ? 1 : 0;
     p.scale = (float)(1.0 / std::sqrt((double)d.D));
     p.lambda = lambda;
@@ -740,7 +741,7 @@ int backward_impl(const diffattn_desc* desc, const void* q1, const void* k1, con
         pp.B = (int)d.B;
         pp.H = (int)d.H;
         pp.T = (int)d.T;
-        pp.Dv = (int)(2 * d.D);
+        pp.Dv = (int)dv_width;
         pp.bf16 = d.dtype == DIFFATTN_BF16 ? 1 : 0;
         pp.log2_negated = 0;
         pp.lambda = lambda;

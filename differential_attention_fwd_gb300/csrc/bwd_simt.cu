@@ -1,5 +1,6 @@
 // bwd_simt.cu -- backward of the differential-attention forward on the CUDA
-// cores (any D <= 128, fp32 or bf16 storage, fp32 arithmetic).
+// cores (any D <= 128, any value width Dv <= 256, fp32 or bf16 storage, fp32
+// arithmetic).
 //
 // Given dO = dL/dO for O = (A_1 - lambda A_2) V (paperleet "Differential
 // Transformer Attention", Return requirements: gradients through both Q/K
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(WARPS * 32) bwd_stats_kernel(const BwdParams p
     const T* k2 = static_cast<const T*>(p.k2) + r.b * p.s_k2[0] + r.hk * p.s_k2[1];
     const T* v = static_cast<const T*>(p.v) + r.b * p.s_v[0] + r.hk * p.s_v[1];
     const T* dout = static_cast<const T*>(p.dout) + r.b * p.s_do[0] + r.h * p.s_do[1] + (int64_t)r.i * p.s_do[2];
-    const int D = p.D, Dv = 2 * p.D;
+    const int D = p.D, Dv = p.Dv;
     for (int d = lane; d < D; d += 32) {
         qs[warp][0][d] = ld(q1, d);
         qs[warp][1][d] = ld(q2, d);
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(WARPS * 32) bwd_dq_kernel(const BwdParams p) {
     const T* k2 = static_cast<const T*>(p.k2) + r.b * p.s_k2[0] + r.hk * p.s_k2[1];
     const T* v = static_cast<const T*>(p.v) + r.b * p.s_v[0] + r.hk * p.s_v[1];
     const T* dout = static_cast<const T*>(p.dout) + r.b * p.s_do[0] + r.h * p.s_do[1] + (int64_t)r.i * p.s_do[2];
-    const int D = p.D, Dv = 2 * p.D;
+    const int D = p.D, Dv = p.Dv;
     for (int d = lane; d < D; d += 32) {
         qs[warp][0][d] = ld(q1, d);
         qs[warp][1][d] = ld(q2, d);
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(WARPS * 32) bwd_dkdv_kernel(const BwdParams p)
     const T* k1 = static_cast<const T*>(p.k1) + b * p.s_k1[0] + hk * p.s_k1[1] + (int64_t)j * p.s_k1[2];
     const T* k2 = static_cast<const T*>(p.k2) + b * p.s_k2[0] + hk * p.s_k2[1] + (int64_t)j * p.s_k2[2];
     const T* v = static_cast<const T*>(p.v) + b * p.s_v[0] + hk * p.s_v[1] + (int64_t)j * p.s_v[2];
-    const int D = p.D, Dv = 2 * p.D;
+    const int D = p.D, Dv = p.Dv;
     for (int d = lane; d < D; d += 32) {
         ks[warp][0][d] = ld(k1, d);
         ks[warp][1][d] = ld(k2, d);

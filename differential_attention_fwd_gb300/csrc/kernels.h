@@ -116,11 +116,12 @@ struct DecodeParams {
     float out_scale;
 };
 
-// Parameters of the backward (CUDA-core kernels, any D <= 128).  Inputs use
-// the descriptor's strides; dout uses the output strides; the gradients are
-// dense: dq [B, H, T, D], dk [B, Hk, T, D], dv [B, Hk, T, 2D].
+// Parameters of the backward (CUDA-core kernels, any D <= 128, value width Dv
+// <= 256).  Inputs use the descriptor's strides; dout uses the output strides;
+// the gradients are dense: dq [B, H, T, D], dk [B, Hk, T, D], dv [B, Hk, T, Dv].
 struct BwdParams {
     int B, H, Hk, kv_group, T, D;
+    int Dv;
     int causal;
     float scale;            // 1 / sqrt(D)
     float lambda;

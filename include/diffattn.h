@@ -299,26 +299,26 @@ size_t diffattn_bwd_workspace_bytes(const diffattn_desc *desc);
  * contributions of every query head that reads it.
  *
  * desc, q1, k1, q2, k2, v, lambda, lambda_dev, causal: as diffattn_fwd (the
- * forward's inputs).  dout: device pointer, [B, H, T, 2D] with desc->o_stride,
+ * forward's inputs).  dout: device pointer, [B, H, T, Dv] with desc->o_stride,
  * same dtype as the inputs.  dq1, dq2: device pointers to dense [B, H, T, D];
- * dk1, dk2: dense [B, H / kv_group, T, D]; dv: dense [B, H / kv_group, T, 2D];
+ * dk1, dk2: dense [B, H / kv_group, T, D]; dv: dense [B, H / kv_group, T, Dv];
  * all of the inputs' dtype, all overwritten; they must not overlap each other
  * or any input.  dlambda: device pointer to one float32, overwritten.
  * workspace: device memory of at least diffattn_bwd_workspace_bytes(desc)
  * bytes, 16-byte aligned, owned by the caller; its contents need no
  * initialisation.
  *
- * Kernels: with bf16, D = 64, 16-byte aligned bases (inputs, dout and the
- * gradients) and strides that are multiples of 8 elements, on the tensor
- * cores (bf16 operands, fp32 accumulation): the forward kernel in
+ * Kernels: with bf16, D = 64 and V = 2D, 16-byte aligned bases (inputs, dout
+ * and the gradients) and strides that are multiples of 8 elements, on the
+ * tensor cores (bf16 operands, fp32 accumulation): the forward kernel in
  * row-statistics mode, then a dQ kernel and a dK/dV kernel.  Anything else
- * valid runs on the CUDA cores in fp32 arithmetic.  Either way five launches on
+ * valid (other D, other value widths such as the DIFF V2 head's Dv = D, fp32)
+ * runs on the CUDA cores in fp32 arithmetic.  Either way five launches on
  * `stream` (row statistics, dQ, dK/dV, and two for dlambda), no atomics, so
  * the result is reproducible bit for bit.
  * Errors: DIFFATTN_ERR_INVALID (as diffattn_fwd, plus a NULL gradient pointer,
- * a missing, small or misaligned workspace); DIFFATTN_ERR_UNSUPPORTED for a
- * value width other than 2D (desc->Dv not 0 or 2 * D); DIFFATTN_ERR_CUDA
- * (launch failure).
+ * a missing, small or misaligned workspace); DIFFATTN_ERR_CUDA (launch
+ * failure).
  */
 int diffattn_bwd(const diffattn_desc *desc, const void *q1, const void *k1,
                  const void *q2, const void *k2, const void *v, float lambda,

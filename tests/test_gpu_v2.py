@@ -140,13 +140,54 @@ def test_other_value_widths_on_cuda_cores(dtype, D, Dv):
         assert_close(to_numpy(out), ref(inp, 0.8, causal), dtype, f"{dtype} D={D} Dv={Dv}")
 
 
-def test_backward_refuses_other_value_widths():
+def test_backward_rejects_mismatched_dout():
     inp = inputs(1, 2, 64, 128, 128, seed=330)
     dev = [to_device(x, "bf16") for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
-    dout = torch.zeros(1, 2, 64, 128, dtype=torch.bfloat16, device="cuda")
+    dout = torch.zeros(1, 2, 64, 256, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ValueError):
         da.differential_attention_backward(*dev, 0.5, dout, True)
-    # autograd refuses at the forward call, not later in the backward
-    q1 = dev[0].clone().requires_grad_()
-    with pytest.raises(ValueError, match="value width"):
-        da.differential_attention(q1, *dev[1:], 0.5)
+
+
+def _dout(inp, dtype, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    d = rng.standard_normal(inp.q1.shape[:3] + (inp.v.shape[-1],), dtype=np.float32)
+    return W.round_to_bf16(d) if dtype == "bf16" else d
+
+
+@pytest.mark.parametrize("dtype,D,Dv,T", [("bf16", 128, 128, 1), ("bf16", 128, 128, 150),
+                                          ("f32", 32, 32, 77), ("bf16", 64, 64, 130),
+                                          ("f32", 16, 40, 33)])
+def test_backward_other_value_widths(dtype, D, Dv, T):
+    # the DIFF V2 head (Dv = D) and other widths: the CUDA-core backward
+    from tests.helpers import assert_dlambda_close, assert_grad_close
+    inp = inputs(1, 4, T, D, Dv, seed=340 + T + Dv, kv_heads=2, dtype=dtype)
+    dout = _dout(inp, dtype, 341 + T)
+    dev = [to_device(x, dtype) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    for causal in (True, False):
+        got = da.differential_attention_backward(*dev, 0.6, to_device(dout, dtype), causal)
+        ref = oracle.differential_attention_backward(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.6,
+                                                     dout, causal)
+        for name, g, r in zip(("dq1", "dk1", "dq2", "dk2", "dv"), got[:5], ref[:5]):
+            assert tuple(g.shape) == r.shape
+            assert_grad_close(to_numpy(g), r, dtype, f"V2 bwd {dtype} D={D} Dv={Dv} T={T} {name}")
+        a2v = oracle.differential_attention(inp.q2, inp.k2, inp.q2, inp.k2, inp.v, 0.0, causal)
+        assert_dlambda_close(float(got[5]), ref[5], np.sum(dout * a2v, axis=-1), dtype,
+                             f"V2 bwd {dtype} D={D} Dv={Dv} T={T} dlambda")
+
+
+def test_autograd_v2_head_shared_keys():
+    # training through the V2 head: the forward on the tensor cores with its
+    # saved results, the backward on the CUDA cores, one key tensor for both
+    # branches (its gradient sums both branches' contributions)
+    from tests.helpers import SAVED_PATH_SLACK, assert_grad_close
+    inp = inputs(1, 4, 200, 128, 128, seed=350, kv_heads=2, shared=True)
+    dout = _dout(inp, "bf16", 351)
+    q1, k, q2, v = (to_device(x, "bf16").requires_grad_() for x in (inp.q1, inp.k1, inp.q2, inp.v))
+    assert da.select_kernel(q1.detach(), k.detach(), q2.detach(), k.detach(), v.detach()) == \
+        da.DIFFATTN_KERNEL_TCGEN05
+    out = da.differential_attention(q1, k, q2, k, v, 0.5, causal=True)
+    out.backward(to_device(dout, "bf16"))
+    ref = oracle.differential_attention_backward(inp.q1, inp.k1, inp.q2, inp.k1, inp.v, 0.5, dout, True)
+    want_k = ref[1] + ref[3]
+    for name, t, r in (("dq1", q1, ref[0]), ("dq2", q2, ref[2]), ("dk", k, want_k), ("dv", v, ref[4])):
+        assert_grad_close(to_numpy(t.grad), r, "bf16", f"autograd V2 {name}", slack=SAVED_PATH_SLACK)
