@@ -277,6 +277,11 @@ DECODE_WORKLOADS = {
     # (the 32-query / 8-key-value-head grouping of the GQA exercise)
     "decode_b16h32kv8q1k8192": DecodeWorkload("decode_b16h32kv8q1k8192", 16, 32, 1, 8192, 64,
                                               "bf16", True, 22, kv_heads=8),
+    # the DIFF V2 head: 16 differential heads over 8 key/value heads, D = Dv =
+    # 128, one key tensor for both branches
+    "decode_b16h16kv8q1k8192_d128_shared_k": DecodeWorkload(
+        "decode_b16h16kv8q1k8192_d128_shared_k", 16, 16, 1, 8192, 128, "bf16", True, 25,
+        kv_heads=8, value_dim=128, shared_keys=True),
 }
 
 # Chunked prefill: the next 1024 tokens of 4 sequences (16 heads, D = 64)
