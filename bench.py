@@ -839,7 +839,11 @@ def run_decode(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                      "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
                      "peak_source": f"{src} hbm_gbs (copy bandwidth)"},
-        "gpu_launches": 2 * args.steps, "clocks": clocks,
+        # two launches (the key-range splits, then their combination), or one
+        # when the call runs on the forward kernels (16 bytes of workspace)
+        "gpu_launches": (1 if need == 16 else 2) * args.steps, "clocks": clocks,
+        "path": "forward kernels (queries at the end of the key sequence)" if need == 16
+                else "split-key decode",
     }
 
 
