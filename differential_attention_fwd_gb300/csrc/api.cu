@@ -242,7 +242,18 @@ struct DecodePlan {
     // The queries go through the forward kernels instead (more query rows than
     // the split-key decode takes, or a value width other than 2D).
     bool forward = false;
+    // The DIFF V2 head (bf16, D = 128, value width 128, up to 8 queries): the
+    // tensor-core split-key decode when the call's cache allows it (one key
+    // tensor, dense 16-byte aligned rows), else the forward kernels.
+    bool v2 = false;
 };
+
+// Query rows per unit of the V2 decode (1, 2, 4 or 8) for `rows` rows.
+int v2_bucket(int64_t rows) {
+    for (int t = 1; t <= 8; t *= 2)
+        if (rows <= t) return t;
+    return 8;
+}
 
 // Bytes a call asks for when it runs on the forward kernels: none are used,
 // but the workspace contract (a non-zero size for a valid request) holds.
@@ -262,6 +273,25 @@ int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
     if (d->Tk > INT32_MAX / 2 || d->Tq > INT32_MAX / 2 || d->H > (1 << 24))
         return DIFFATTN_ERR_UNSUPPORTED;
     const int cap = (d->D == 32 || d->D == 64 || d->D == 128) ? decode_max_rows((int)d->D) : 0;
+    if (d->dtype == DIFFATTN_BF16 && d->D == 128 && value_width(d->Dv, d->D) == 128 && d->Tq <= 8) {
+        // rows of the heads that share a key/value head, 8 per unit at most
+        const int64_t g = group_of(d->kv_group);
+        const int64_t rows = g * d->Tq;
+        const int64_t row_chunks = (rows + 7) / 8;
+        const int64_t Hk = d->H / g;
+        const int64_t units = d->B * Hk * row_chunks;
+        if (units > (1ll << 24) || d->B * d->H > (1ll << 24) || d->B * d->H * d->Tq > INT32_MAX)
+            return DIFFATTN_ERR_UNSUPPORTED;
+        plan->v2 = true;
+        plan->tq_bucket = v2_bucket((rows + row_chunks - 1) / row_chunks);
+        plan->splits = 1;                   // the tensor-core pass sets its own
+        plan->split_len = (int)(((d->Tk + 255) / 256) * 256);
+        plan->kv_group = (int)g;
+        plan->Hk = (int)Hk;
+        plan->row_chunks = (int)row_chunks;
+        plan->work_bytes = decode_tc_work_floats(units, d->Tk, plan->tq_bucket) * sizeof(float);
+        return DIFFATTN_OK;
+    }
     if (d->Tq > cap || value_width(d->Dv, d->D) != 2 * d->D) {
         // queries over the cache on the forward kernels (chunked prefill)
         const int64_t nq = (d->Tq + 127) / 128;
@@ -793,7 +823,9 @@ int decode_args(const diffattn_kv_desc* desc, const void* q1, const void* k1, co
     if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
     rc = check_epilogue(epi, e);
     if (rc != DIFFATTN_OK) return rc;
-    if (plan->forward) return DIFFATTN_OK;   // the forward kernels take any alignment
+    // the forward kernels take any alignment (and so does the V2 decode,
+    // which falls back to them)
+    if (plan->forward || plan->v2) return DIFFATTN_OK;
     const size_t esize = desc->dtype == DIFFATTN_BF16 ? 2 : 4;
     if (!kv_aligned(k1, desc->k1_stride, esize) || !kv_aligned(k2, desc->k2_stride, esize) ||
         !kv_aligned(v, desc->v_stride, esize))
@@ -829,16 +861,26 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
         (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
         return DIFFATTN_ERR_INVALID;
     const diffattn_kv_desc& d = *desc;
-    if (plan.forward) {
+    const size_t esize = d.dtype == DIFFATTN_BF16 ? 2 : 4;
+    const int64_t dv = value_width(d.Dv, d.D);
+    const int64_t hk = d.H / group_of(d.kv_group);
+    const bool k_shared = same_tensor(k1, d.k1_stride, k2, d.k2_stride, d.B, hk, d.Tk);
+    const bool dense_kv = d.k1_stride[2] == d.D && d.k2_stride[2] == d.D && d.v_stride[2] == dv;
+    // the V2 decode on the tensor cores needs one key tensor and dense,
+    // aligned rows of the cache and of the queries
+    const bool v2_tc = plan.v2 && k_shared && dense_kv && kv_aligned(k1, d.k1_stride, esize) &&
+                       kv_aligned(v, d.v_stride, esize) && kv_aligned(q1, d.q1_stride, esize) &&
+                       kv_aligned(q2, d.q2_stride, esize);
+    auto run_forward = [&]() {
         // Tq query rows at the end of the Tk-key sequence: query i at key
         // position Tk - Tq + i; one forward launch with the static schedule
-        const FwdShape f{d.B, d.H, plan.Hk, d.Tq, d.Tk, d.D, value_width(d.Dv, d.D), d.Tk - d.Tq,
+        const FwdShape f{d.B, d.H, plan.Hk, d.Tq, d.Tk, d.D, dv, d.Tk - d.Tq,
                          d.dtype, d.q1_stride, d.k1_stride, d.q2_stride, d.k2_stride, d.v_stride,
                          d.o_stride};
         return launch_forward(f, q1, k1, q2, k2, v, lambda, lambda_dev, causal, e, out, nullptr,
                               nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
-    }
-    const size_t esize = d.dtype == DIFFATTN_BF16 ? 2 : 4;
+    };
+    if (plan.forward || (plan.v2 && !v2_tc)) return run_forward();
     DecodeParams p{};
     p.B = (int)d.B;
     p.H = (int)d.H;
@@ -850,9 +892,12 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
     p.kv_group = plan.kv_group;
     p.Hk = plan.Hk;
     p.row_chunks = plan.row_chunks;
-    p.dense_kv = (d.k1_stride[2] == d.D && d.k2_stride[2] == d.D && d.v_stride[2] == 2 * d.D) ? 1 : 0;
-    p.tc_ok = (p.dense_kv && d.dtype == DIFFATTN_BF16 && d.D == 64 && kv_aligned(q1, d.q1_stride, esize) &&
-               kv_aligned(q2, d.q2_stride, esize)) ? 1 : 0;
+    p.dense_kv = dense_kv ? 1 : 0;
+    p.v2 = plan.v2 ? 1 : 0;
+    p.k_shared = k_shared ? 1 : 0;
+    p.tc_ok = plan.v2 || (p.dense_kv && d.dtype == DIFFATTN_BF16 && d.D == 64 &&
+                          kv_aligned(q1, d.q1_stride, esize) && kv_aligned(q2, d.q2_stride, esize))
+                  ? 1 : 0;
     p.tq_bucket = plan.tq_bucket;
     p.splits = plan.splits;
     p.total_items = (int)((int64_t)plan.Hk * d.B * plan.row_chunks * plan.splits);
@@ -884,11 +929,12 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
         diffattn_desc md{};
         md.B = d.B;
         md.T = d.Tk;
-        const int64_t hk = d.H / group_of(d.kv_group);
-        if (encode_map(&kv_maps[0], k1, 64, &md, hk, d.k1_stride, 64, 128) == DIFFATTN_OK &&
-            encode_map(&kv_maps[1], k2, 64, &md, hk, d.k2_stride, 64, 128) == DIFFATTN_OK &&
-            encode_map(&kv_maps[2], v, 128, &md, hk, d.v_stride, 64, 128) == DIFFATTN_OK)
+        if (encode_map(&kv_maps[0], k1, d.D, &md, hk, d.k1_stride, 64, 128) == DIFFATTN_OK &&
+            encode_map(&kv_maps[1], k2, d.D, &md, hk, d.k2_stride, 64, 128) == DIFFATTN_OK &&
+            encode_map(&kv_maps[2], v, dv, &md, hk, d.v_stride, 64, 128) == DIFFATTN_OK)
             p.tc_maps = kv_maps;
+        else if (plan.v2)
+            return run_forward();
         else
             p.tc_ok = 0;
     }

@@ -749,6 +749,24 @@ int launch_d(const DecodeParams& p, cudaStream_t stream) {
     return -1;
 }
 
+// The DIFF V2 head (D = 128, value width 128): the tensor-core first pass,
+// then the combine pass of value width 128 (its instance for D = 64).
+template <int TQ>
+int launch_v2_tq(const DecodeParams& p, cudaStream_t stream) {
+    DecodeParams q = p;
+    if (launch_decode_tc_first_pass(&q, stream) != 0) return -1;
+    return launch_combine<__nv_bfloat16, 64, TQ>(q, stream);
+}
+
+int launch_v2(const DecodeParams& p, cudaStream_t stream) {
+    if (!p.tc_ok || !p.bf16 || p.D != 128) return -1;
+    if (p.tq_bucket == 1) return launch_v2_tq<1>(p, stream);
+    if (p.tq_bucket == 2) return launch_v2_tq<2>(p, stream);
+    if (p.tq_bucket == 4) return launch_v2_tq<4>(p, stream);
+    if (p.tq_bucket == 8) return launch_v2_tq<8>(p, stream);
+    return -1;
+}
+
 template <typename T>
 int launch_t(const DecodeParams& p, cudaStream_t stream) {
     if (p.D == 32) return launch_d<T, 32>(p, stream);
@@ -773,6 +791,7 @@ size_t decode_work_floats(int64_t units, int splits, int tq_bucket, int64_t D) {
 }
 
 int launch_decode(const DecodeParams& p, cudaStream_t stream) {
+    if (p.v2) return dec::launch_v2(p, stream);
     return p.bf16 ? dec::launch_t<__nv_bfloat16>(p, stream) : dec::launch_t<float>(p, stream);
 }
 

@@ -1,9 +1,13 @@
 // decode_tc.cu -- the first pass of the decode (a few queries over a long
 // key/value cache) on the tensor cores, for query rows that share a key/value
-// head: bf16, D = 64, dense cache rows, 4 to 8 rows per unit (the query
-// heads of a grouped key/value head, DIFF V2's layout, or several new
-// queries).  It writes split partials in the layout of the CUDA-core first
-// pass in decode.cu, which the combine pass there merges.
+// head: bf16, value width 128, dense cache rows, up to 8 rows per unit (the
+// query heads of a grouped key/value head, DIFF V2's layout, or several new
+// queries).  Two head shapes: D = 64 (V = 2D) with 4 or 8 rows per unit, and
+// the DIFF V2 head D = 128 (V = D; aiengineeringfromscratch lesson, "V1 contre
+// V2") with 1 to 8, whose two branches usually share one key tensor (then one
+// key tile per stage serves both score products).  It writes split partials
+// in the layout of the CUDA-core first pass in decode.cu for a value width of
+// 128, which the combine pass there merges.
 //
 // Work: a unit is (b, key/value head, row chunk); its keys form tpu tiles of
 // 128.  The units' tiles are laid end to end and every CTA streams one
@@ -47,33 +51,45 @@ namespace dtc {
 
 constexpr int KT = 128;                 // keys per tile = threads = TMEM lanes
 constexpr int THREADS = KT;
-constexpr int HDIM = 64;
-constexpr int DV = 2 * HDIM;
+constexpr int DV = 128;                 // value width
 constexpr int NR = 16;                  // MMA N: query rows per unit, padded
-constexpr int KROW = HDIM * 2;          // bytes of one bf16 key row (128)
-constexpr int K_BYTES = KT * KROW;      // 16 KB per branch
+constexpr int K_PANEL = KT * 128;       // 16 KB: 128 keys x 64 columns (the swizzle span)
+constexpr int Q_PANEL = NR * 128;       // 2 KB: 16 rows x 64 columns
 constexpr int V_HALF = KT * 128;        // 16 KB: 64 value columns of 128 keys
-constexpr int STAGE = 2 * K_BYTES + 2 * V_HALF;   // 64 KB
-constexpr int NST = 3;                  // stages: two tiles in flight ahead
 constexpr int P_SUB = 2 * NR * 128;     // 4 KB: 32 rows (P_1^T, then P_2^T) x 64 keys
 constexpr int P_BUF = 2 * P_SUB;        // two 64-key halves
-constexpr int Q_BYTES = NR * KROW;      // 2 KB per branch
 
-// Shared memory (offsets from a 1024-byte aligned base).
-// The NST stages start at offset 0.
-constexpr int OFF_P = NST * STAGE;                 // P^T: [2 buffers][branch][64-key half]
-constexpr int OFF_Q = OFF_P + 2 * P_BUF;           // [branch]
-constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;       // float [4 warps][2][NR]
-constexpr int OFF_BAR = OFF_RED + 4 * 2 * NR * 4;  // S_FULL, PV_DONE[2], FINAL, FULL[NST]
-constexpr int NUM_BARS = 4 + NST;
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // TMEM base address, abort flag
-constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+// Shared memory for Q/K width HD, KS = one key tile shared by both branches
+// (offsets from a 1024-byte aligned base).  A stage holds the key tile(s) as
+// HD / 64 panels each, then the two 64-column halves of V: 64 KB for D = 64
+// with two key tensors and for D = 128 with one.  The NST = 3 stages start at
+// offset 0 (two tiles in flight ahead of the one computed).  D = 128 with two
+// key tensors would need 96 KB stages, two of which leave no tile in flight
+// while one is computed; that shape runs on the forward kernels.
+template <int HD, bool KS>
+struct Cfg {
+    static_assert((HD == 64 && !KS) || (HD == 128 && KS), "Q/K width and key sharing");
+    static constexpr int PANELS = HD / 64;
+    static constexpr int K_BYTES = KT * HD * 2;          // one branch's key tile
+    static constexpr int NK = KS ? 1 : 2;                // key tiles per stage
+    static constexpr int STAGE = NK * K_BYTES + 2 * V_HALF;
+    static constexpr int NST = 3;
+    static_assert(STAGE == 64 * 1024, "stage size");
+    static constexpr int Q_BYTES = NR * HD * 2;          // per branch
+    static constexpr int OFF_P = NST * STAGE;            // P^T: [2 buffers][branch][64-key half]
+    static constexpr int OFF_Q = OFF_P + 2 * P_BUF;      // [branch]
+    static constexpr int OFF_RED = OFF_Q + 2 * Q_BYTES;  // float [4 warps][2][NR]
+    static constexpr int OFF_BAR = OFF_RED + 4 * 2 * NR * 4;   // S_FULL, PV_DONE[2], FINAL, FULL[NST]
+    static constexpr int NUM_BARS = 4 + NST;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;    // TMEM base address, abort flag
+    static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
 
 constexpr uint32_t TMEM_COLS = 128;
 constexpr uint32_t TM_S = 0;            // S1^T at 0, S2^T at 16
 constexpr uint32_t TM_O = 32;           // O1^T at 32, O2^T at 48
-constexpr uint32_t IDESC_S = idesc_bf16_f32(KT, NR, 0, 0);   // K (K-major) x Q^T (K-major)
+constexpr uint32_t IDESC_S = idesc_bf16_f32(KT, NR, 0, 0);   // K (K-major) x Q^T (K-major), K = 16 per product
 // both branches in one product: N = 32 rows of [P_1^T; P_2^T] into O_1^T, O_2^T
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(DV, 2 * NR, 1, 0);  // V^T (MN-major) x P^T (K-major)
 
@@ -140,27 +156,36 @@ struct Cursor {
     }
 };
 
-// Stage tile `cur` into shared memory at `dst` with four TMA box loads
-// (K1, K2 and the two 64-column halves of V, 128 rows each), completion
-// counted on `full`.
+// Stage tile `cur` into shared memory at `dst` with TMA box loads of 128
+// rows x 64 columns (the panels of K1, of K2 unless the keys are shared, and
+// the two 64-column halves of V), completion counted on `full`.
+template <int HD, bool KS>
 __device__ __forceinline__ void stage_tile(const DecodeParams& p, const Cursor& cur, uint8_t* dst,
                                            uint64_t* full, const CUtensorMap* k1, const CUtensorMap* k2,
                                            const CUtensorMap* v) {
+    using C = Cfg<HD, KS>;
     const int bhk = cur.unit / p.row_chunks;
     const int b = bhk / p.Hk, hk = bhk - b * p.Hk;
     const int key0 = cur.k_begin + cur.c * KT;
-    mbar_arrive_expect_tx(full, STAGE);
-    tma_load_4d(dst, k1, full, 0, key0, hk, b);
-    tma_load_4d(dst + K_BYTES, k2, full, 0, key0, hk, b);
-    tma_load_4d(dst + 2 * K_BYTES, v, full, 0, key0, hk, b);
-    tma_load_4d(dst + 2 * K_BYTES + V_HALF, v, full, 64, key0, hk, b);
+    mbar_arrive_expect_tx(full, C::STAGE);
+#pragma unroll
+    for (int pn = 0; pn < C::PANELS; ++pn) {
+        tma_load_4d(dst + pn * K_PANEL, k1, full, pn * 64, key0, hk, b);
+        if (!KS) tma_load_4d(dst + C::K_BYTES + pn * K_PANEL, k2, full, pn * 64, key0, hk, b);
+    }
+    tma_load_4d(dst + C::NK * C::K_BYTES, v, full, 0, key0, hk, b);
+    tma_load_4d(dst + C::NK * C::K_BYTES + V_HALF, v, full, 64, key0, hk, b);
 }
 
-template <int TQ>
+template <int TQ, int HD, bool KS>
 __global__ void __launch_bounds__(THREADS, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
                  const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
     static_assert(TQ >= 1 && TQ <= NR, "rows per unit");
+    using C = Cfg<HD, KS>;
+    constexpr int STAGE = C::STAGE, NST = C::NST, K_BYTES = C::K_BYTES, Q_BYTES = C::Q_BYTES;
+    constexpr int OFF_P = C::OFF_P, OFF_Q = C::OFF_Q, OFF_RED = C::OFF_RED, OFF_BAR = C::OFF_BAR;
+    constexpr int NUM_BARS = C::NUM_BARS, OFF_MISC = C::OFF_MISC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
@@ -204,7 +229,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
         tma_prefetch_desc(&tm_k2);
         tma_prefetch_desc(&tm_v);
         for (int s0 = 0; s0 < NST - 1 && !icur.done(); ++s0) {
-            stage_tile(p, icur, smem + s0 * STAGE, &bars[4 + s0], &tm_k1, &tm_k2, &tm_v);
+            stage_tile<HD, KS>(p, icur, smem + s0 * STAGE, &bars[4 + s0], &tm_k1, &tm_k2, &tm_v);
             icur.next(p);
             ++issued;
         }
@@ -219,11 +244,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
         tc_fence_after();
 #pragma unroll
         for (int br = 0; br < 2; ++br) {
-            const uint64_t ka = sdesc_sw128(sbase + stage * STAGE + br * K_BYTES, 16, 1024);
+            const uint64_t ka = sdesc_sw128(sbase + stage * STAGE + (KS ? 0 : br) * K_BYTES, 16, 1024);
             const uint64_t qb = sdesc_sw128(sbase + OFF_Q + br * Q_BYTES, 16, 1024);
+            // HD / 16 products of depth 16, four per 64-column panel
 #pragma unroll
-            for (int kk = 0; kk < HDIM / 16; ++kk)
-                mma_ss(tmem + TM_S + br * NR, ka + 2 * kk, qb + 2 * kk, IDESC_S, kk > 0);
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                const int pn = kk >> 2, ks = kk & 3;
+                mma_ss(tmem + TM_S + br * NR, ka + pn * (K_PANEL >> 4) + 2 * ks,
+                       qb + pn * (Q_PANEL >> 4) + 2 * ks, IDESC_S, kk > 0);
+            }
         }
         mma_commit(&bars[0]);
         return true;
@@ -239,8 +268,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
             const int bhk = unit / p.row_chunks;
             const int b = bhk / p.Hk, hk = bhk - b * p.Hk;
             const int n_rows = p.kv_group * p.Tq;
-            if (tid < 16 * TQ) {
-                const int r = tid >> 4, br = (tid >> 3) & 1, c = tid & 7;
+            constexpr int QCH = HD / 8;          // 16-byte chunks of a query row
+            for (int i = tid; i < TQ * 2 * QCH; i += THREADS) {
+                const int r = i / (2 * QCH), br = (i / QCH) & 1, c = i % QCH;
                 const int row = rc * TQ + r;
                 uint4 x = make_uint4(0, 0, 0, 0);
                 if (row < n_rows) {
@@ -251,7 +281,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
                         : static_cast<const __nv_bfloat16*>(p.q1) + b * p.s_q1[0] + h * p.s_q1[1] + (int64_t)q * p.s_q1[2];
                     x = *reinterpret_cast<const uint4*>(src + c * 8);
                 }
-                *reinterpret_cast<uint4*>(smem + OFF_Q + br * Q_BYTES + sw128(r, c)) = x;
+                *reinterpret_cast<uint4*>(smem + OFF_Q + br * Q_BYTES + (c >> 3) * Q_PANEL + sw128(r, c & 7)) = x;
             }
             fence_proxy_async_smem();
 #pragma unroll
@@ -358,7 +388,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
             // (MN-major, the two 64-column halves V_HALF apart), B = the 32
             // rows of P^T in two 64-key halves
             tc_fence_after();
-            const uint64_t va = sdesc_sw128(sbase + st * STAGE + 2 * K_BYTES, V_HALF, 1024);
+            const uint64_t va = sdesc_sw128(sbase + st * STAGE + C::NK * K_BYTES, V_HALF, 1024);
             const uint64_t pd = sdesc_sw128(sbase + OFF_P + pb * P_BUF, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < KT / 16; ++kk)
@@ -426,7 +456,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
             if (g >= 1) ok = mbar_wait(&bars[1 + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, ab);
             const int ist = (st + NST - 1) % NST;
             if (ok) {
-                stage_tile(p, icur, smem + ist * STAGE, &bars[4 + ist], &tm_k1, &tm_k2, &tm_v);
+                stage_tile<HD, KS>(p, icur, smem + ist * STAGE, &bars[4 + ist], &tm_k1, &tm_k2, &tm_v);
                 icur.next(p);
                 ++issued;
             }
@@ -452,13 +482,25 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constan
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int TQ>
+template <int TQ, int HD, bool KS>
 int launch_first_pass_tq(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t stream) {
-    if (cudaFuncSetAttribute(decode_tc_kernel<TQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
+    constexpr int smem = Cfg<HD, KS>::SMEM_BYTES;
+    if (cudaFuncSetAttribute(decode_tc_kernel<TQ, HD, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
         return -1;
-    decode_tc_kernel<TQ><<<p.tc_grid, THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], p);
+    decode_tc_kernel<TQ, HD, KS><<<p.tc_grid, THREADS, smem, stream>>>(maps[0], maps[1], maps[2], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+template <int HD, bool KS>
+int launch_first_pass_hd(const DecodeParams& p, cudaStream_t stream) {
+    if (p.tq_bucket == 4) return launch_first_pass_tq<4, HD, KS>(p, p.tc_maps, stream);
+    if (p.tq_bucket == 8) return launch_first_pass_tq<8, HD, KS>(p, p.tc_maps, stream);
+    if constexpr (HD == 128) {
+        if (p.tq_bucket == 1) return launch_first_pass_tq<1, HD, KS>(p, p.tc_maps, stream);
+        if (p.tq_bucket == 2) return launch_first_pass_tq<2, HD, KS>(p, p.tc_maps, stream);
+    }
+    return -1;
 }
 
 // Segments of one unit at most: every CTA range holds at least
@@ -496,8 +538,8 @@ int launch_decode_tc_first_pass(DecodeParams* p, cudaStream_t stream) {
     p->tc_total = total;
     p->tc_grid = (int)grid;
     p->splits = (int)dtc::tc_slots(total, tpu, grid);   // partial slots per unit
-    if (p->tq_bucket == 4) return dtc::launch_first_pass_tq<4>(*p, p->tc_maps, stream);
-    if (p->tq_bucket == 8) return dtc::launch_first_pass_tq<8>(*p, p->tc_maps, stream);
+    if (p->D == 64) return dtc::launch_first_pass_hd<64, false>(*p, stream);
+    if (p->D == 128 && p->k_shared) return dtc::launch_first_pass_hd<128, true>(*p, stream);
     return -1;
 }
 

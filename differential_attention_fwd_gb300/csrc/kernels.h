@@ -88,8 +88,12 @@ struct DecodeParams {
     int Hk;                 // key/value heads, H / kv_group
     int row_chunks;         // CTAs along the kv_group * Tq query rows of a key/value head
     int dense_kv;           // K1, K2 and V rows contiguous along the sequence (async staging)
-    int tc_ok;              // the tensor-core first pass may run: bf16, D = 64, dense K/V
-                            // rows, Q rows 16-byte aligned
+    int tc_ok;              // the tensor-core first pass may run: bf16, D = 64 (V = 2D) or
+                            // D = 128 with V = D and one key tensor, dense K/V rows,
+                            // Q rows 16-byte aligned
+    int v2;                 // value width D = 128 (the DIFF V2 head): the tensor-core
+                            // first pass and the combine pass of value width 128 only
+    int k_shared;           // K1 and K2 are one tensor
     uint32_t* status;       // device status word (bounded waits of the tensor-core pass)
     const CUtensorMap* tc_maps;   // host memory: K1, K2 and V tensor maps (128-row boxes) for
                                   // the tensor-core pass's launch; never read on the device
@@ -176,8 +180,8 @@ size_t decode_work_floats(int64_t units, int splits, int tq_bucket, int64_t D);
 
 // Each returns 0 on success, -1 if the launch failed.
 int launch_decode(const DecodeParams& p, cudaStream_t stream);
-// The tensor-core first pass of the decode (decode_tc.cu) for 4 or 8 query
-// rows per unit.  It sets p's tc_* fields and p->splits (partial slots per
+// The tensor-core first pass of the decode (decode_tc.cu): D = 64 with 4 or 8
+// query rows per unit, D = 128 (value width 128, one key tensor) with 1 to 8.  It sets p's tc_* fields and p->splits (partial slots per
 // unit) for its launch; the caller launches the combine pass with that p.
 int launch_decode_tc_first_pass(DecodeParams* p, cudaStream_t stream);
 // Workspace floats the tensor-core pass may need (its slots per unit on any

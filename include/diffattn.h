@@ -69,12 +69,12 @@ typedef struct CUstream_st *diffattn_stream_t;
  * Dv: width of V and O.  0 means 2*D, the operation's own shape (paperleet,
  * Formula and conventions: V and O are [B, H, T, 2D]).  Any other value
  * 1 .. 256 is the head shape of DIFF V2 and similar layouts (the
- * aiengineeringfromscratch lesson, "V1 vs V2": the head dimension stays that
+ * aiengineeringfromscratch lesson, "V1 contre V2": the head dimension stays that
  * of the baseline, so V is as wide as Q and K, Dv = D).  The field is last in
  * the struct, so a zero-initialised descriptor keeps the 2*D shape.
  * dtype: DIFFATTN_BF16 or DIFFATTN_F32.
  * kv_group: query heads per key/value head (grouped key/value heads, the
- * layout of DIFF V2: aiengineeringfromscratch lesson, "V1 vs V2" and its
+ * layout of DIFF V2: aiengineeringfromscratch lesson, "V1 contre V2" and its
  * GQA exercise).  0 or 1: Q1, Q2, K1, K2, V and O all have H heads.  g > 1:
  * H must be a multiple of g; Q1, Q2 and O have H heads, K1, K2 and V have
  * H / g heads, and query head h reads key/value head h / g (integer
@@ -394,6 +394,13 @@ size_t diffattn_decode_workspace_bytes(const diffattn_kv_desc *desc);
  * rows (4 for D = 128) of the query heads that share a key/value head, so with
  * kv_group = g the cache of a key/value head is read ceil(g * Tq / 8) times
  * (ceil(g * Tq / 4) for D = 128), not g * ceil(Tq / 8) times.
+ * The DIFF V2 head (bf16, D = Dv = 128, Tq <= 8; aiengineeringfromscratch
+ * lesson, "V1 contre V2"): the workspace is sized for the split-key decode on
+ * the tensor cores (8 query rows per CTA, the cache of a key/value head read
+ * ceil(g * Tq / 8) times), which runs when K1 and K2 are one tensor (same
+ * pointer and strides) and Q1, Q2, K and V have 16-byte aligned bases and
+ * strides with rows dense along the sequence; with two key tensors or
+ * another layout the call runs on the forward kernels instead.
  * Any other request (more query rows, another D or Dv) runs as one launch of
  * the forward kernels with the queries placed at the end of the key sequence:
  * on the tensor cores when diffattn_fwd would choose them for this shape and
@@ -403,7 +410,8 @@ size_t diffattn_decode_workspace_bytes(const diffattn_kv_desc *desc);
  * > 256, Tk < Tq with the causal mask, unknown dtype, negative strides,
  * negative kv_group or one that does not divide H, non-finite lambda, bad
  * epilogue, missing, small or misaligned workspace); DIFFATTN_ERR_UNSUPPORTED
- * (a split-key decode with unaligned K1, K2 or V, or sizes beyond the int32
+ * (a split-key decode other than the V2 head's with unaligned K1, K2 or V,
+ * or sizes beyond the int32
  * index range); DIFFATTN_ERR_CUDA (launch failure).
  */
 int diffattn_decode(const diffattn_kv_desc *desc, const void *q1, const void *k1,

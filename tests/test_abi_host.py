@@ -217,8 +217,21 @@ def test_decode_workspace_query(lib):
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=48))) == 16
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=9))) == 16
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=1024, Tk=8192))) == 16
-    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=128))) == 16
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=64, Dv=128))) == n
+    # the DIFF V2 head (bf16, D = Dv = 128) up to 8 queries: the tensor-core
+    # split-key decode's partial results; more queries or fp32: the forward
+    v2 = lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=128)))
+    assert v2 > 16 and v2 % 4 == 0
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=128, Tq=8))) > 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=128, Tq=9))) == 16
+    assert lib.diffattn_decode_workspace_bytes(
+        ctypes.byref(kv_desc(D=128, Dv=128, dtype=_lib.DIFFATTN_F32))) == 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=64))) == 16
+    # the V2 decode workload (16 sequences of 8192 keys, 16 heads over 8)
+    # fits the 8 MiB buffer of diffattn_decode_noalloc
+    w = lib.diffattn_decode_workspace_bytes(
+        ctypes.byref(kv_desc(B=16, H=16, kv_group=2, Tk=8192, D=128, Dv=128)))
+    assert 16 < w <= 8 * 1024 * 1024
     # invalid descriptors
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=200))) == 0
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Dv=300))) == 0

@@ -21,6 +21,8 @@ def _built():
 
 def run(inp, dtype, lam, causal, **kw):
     dev = [to_device(x, dtype) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v)]
+    if inp.k2 is inp.k1:
+        dev[3] = dev[1]             # one key tensor for both branches
     return da.differential_attention_decode(*dev, lam, causal=causal, **kw), dev
 
 
@@ -76,6 +78,8 @@ def test_decode_epilogue_and_device_lambda():
 def test_decode_workloads_sampled():
     for w in W.DECODE_WORKLOADS.values():
         inp = W.draw_kv(w, B=2)      # two of the sequences, full cache length
+        if w.shared_keys:
+            inp.k2 = inp.k1
         out, _ = run(inp, w.dtype, w.lambda_value, w.causal)
         ref = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v,
                                                w.lambda_value, w.causal)

@@ -4,7 +4,10 @@ The aiengineeringfromscratch lesson ("V1 contre V2") keeps the baseline's head
 dimension for DIFF V2: Q, K and V are all D = 128 wide (value width Dv = D),
 the two branches of a differential head share their key/value head, and 32
 query heads run over 8 key/value heads.  bf16 with D = Dv = 128 runs on the
-tensor-core kernel; other value widths on the CUDA-core kernel.
+tensor-core kernel; other value widths on the CUDA-core kernel.  A decode step
+of that head (bf16, up to 8 queries, one key tensor, dense cache rows) runs on
+the tensor-core split-key decode; the rest of its decode shapes on the forward
+kernels.
 """
 import numpy as np
 import pytest
@@ -191,3 +194,121 @@ def test_autograd_v2_head_shared_keys():
     want_k = ref[1] + ref[3]
     for name, t, r in (("dq1", q1, ref[0]), ("dq2", q2, ref[2]), ("dk", k, want_k), ("dv", v, ref[4])):
         assert_grad_close(to_numpy(t.grad), r, "bf16", f"autograd V2 {name}", slack=SAVED_PATH_SLACK)
+
+
+def decode_inputs(B, H, Hk, Tq, Tk, seed, shared=True, dtype="bf16"):
+    w = W.DecodeWorkload("v2dec", B, H, Tq, Tk, 128, dtype, True, seed=seed, kv_heads=Hk,
+                         value_dim=128, shared_keys=shared)
+    inp = W.draw_kv(w)
+    if shared:
+        inp.k2 = inp.k1
+    return inp
+
+
+def decode_run(inp, lam, causal, dtype="bf16", kv=None, **kw):
+    q1, k1, q2, k2, v = (to_device(x, dtype) for x in (inp.q1, inp.k1, inp.q2, inp.k2, inp.v))
+    if inp.k2 is inp.k1:
+        k2 = k1
+    if kv is not None:
+        k1, k2, v = kv(k1, k2, v)
+    out = da.differential_attention_decode(q1, k1, q2, k2, v, lam, causal=causal, **kw)
+    torch.cuda.synchronize()
+    assert da.get_device_error() == 0
+    return out
+
+
+def decode_ref(inp, lam, causal):
+    return oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, lam, causal)
+
+
+def split_key_workspace(B, H, Hk, Tq, Tk):
+    """Workspace bytes of a V2 decode call: more than the forward kernels'
+    nominal 16 when the call is planned for the split-key decode."""
+    from differential_attention_fwd_gb300 import _lib
+    import ctypes
+    d = _lib.DiffattnKvDesc()
+    d.B, d.H, d.Tq, d.Tk, d.D, d.Dv = B, H, Tq, Tk, 128, 128
+    d.dtype, d.kv_group = _lib.DIFFATTN_BF16, H // Hk
+    for f, T, h in (("q1_stride", Tq, H), ("q2_stride", Tq, H), ("k1_stride", Tk, Hk),
+                    ("k2_stride", Tk, Hk), ("v_stride", Tk, Hk), ("o_stride", Tq, H)):
+        getattr(d, f)[:] = (h * T * 128, T * 128, 128)
+    return _lib.load().diffattn_decode_workspace_bytes(ctypes.byref(d))
+
+
+# rows per key/value head (H / Hk * Tq): 1, 2, 4, 6 (padded to 8), 8, 16 (two
+# units of 8); caches of one key, a ragged tail, one tile, many tiles
+@pytest.mark.parametrize("B,H,Hk,Tq,Tk", [(2, 4, 4, 1, 1), (2, 16, 8, 1, 8192), (1, 8, 2, 1, 300),
+                                          (2, 8, 1, 1, 1000), (1, 4, 2, 3, 1000), (1, 4, 1, 4, 2000),
+                                          (2, 2, 2, 8, 129), (1, 32, 8, 2, 5000), (1, 2, 2, 5, 128)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_v2_decode_split_key_tensor_core(B, H, Hk, Tq, Tk, causal):
+    assert split_key_workspace(B, H, Hk, Tq, Tk) > 16
+    inp = decode_inputs(B, H, Hk, Tq, Tk, seed=400 + H * Tq + Tk)
+    out = decode_run(inp, 0.7, causal)
+    assert tuple(out.shape) == (B, H, Tq, 128)
+    assert_close(to_numpy(out), decode_ref(inp, 0.7, causal), "bf16",
+                 f"V2 decode B={B} H={H} Hk={Hk} Tq={Tq} Tk={Tk} causal={causal}")
+
+
+@pytest.mark.parametrize("norm", [None, "rms", "group"])
+def test_v2_decode_epilogue_device_lambda_repeat(norm):
+    inp = decode_inputs(2, 8, 4, 2, 3000, seed=420)
+    rng = np.random.default_rng(5)
+    wt = (1 + 0.1 * rng.standard_normal((8, 128))).astype(np.float32)
+    bs = (0.05 * rng.standard_normal((8, 128))).astype(np.float32)
+    lam_t = torch.tensor(-0.3, device="cuda")
+    kw = dict(out_scale=0.6)
+    if norm:
+        kw.update(norm=norm, norm_weight=torch.from_numpy(wt).cuda(), norm_bias=torch.from_numpy(bs).cuda())
+    want = oracle.head_norm(decode_ref(inp, -0.3, True), norm or "none", 1e-5, wt if norm else None,
+                            bs if norm else None, 0.6)
+    for call in range(2):
+        out = decode_run(inp, lam_t, True, **kw)
+        assert_close(to_numpy(out), want, "bf16", f"V2 decode epilogue {norm} call {call}")
+
+
+def test_v2_decode_value_rows_through_ones_and_cancellation():
+    # V = 1: every output is 1 - lambda; identical branches cancel at lambda = 1
+    inp = decode_inputs(1, 8, 2, 1, 777, seed=430)
+    inp.v = np.ones_like(inp.v)
+    out = decode_run(inp, 0.35, True)
+    assert float((out.float() - 0.65).abs().max()) <= 2e-2
+    inp.q2 = inp.q1
+    out = decode_run(inp, 1.0, True)
+    assert int(torch.count_nonzero(out)) == 0
+
+
+def test_v2_decode_shapes_on_the_forward_kernels():
+    """The V2 decode shapes the split-key pass does not take (two key
+    tensors, a cache with rows not contiguous along the sequence, fp32, more
+    than 8 queries) run on the forward kernels; all match the oracle."""
+    inp = decode_inputs(1, 8, 2, 1, 1500, seed=440, shared=False)
+    assert_close(to_numpy(decode_run(inp, 0.5, True)), decode_ref(inp, 0.5, True), "bf16",
+                 "V2 decode two key tensors")
+    inp = decode_inputs(2, 8, 2, 2, 1500, seed=441)
+
+    def token_major(k1, k2, v):
+        # [B, Tk, Hk, *] storage seen as [B, Hk, Tk, *], one key tensor
+        tm = lambda t: t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+        k = tm(k1)
+        return k, k, tm(v)
+
+    out = decode_run(inp, 0.5, True, kv=token_major)
+    assert_close(to_numpy(out), decode_ref(inp, 0.5, True), "bf16", "V2 decode token-major cache")
+    inp = decode_inputs(1, 4, 2, 2, 600, seed=442, dtype="f32")
+    assert_close(to_numpy(decode_run(inp, 0.5, True, dtype="f32")), decode_ref(inp, 0.5, True),
+                 "f32", "V2 decode fp32")
+    assert split_key_workspace(1, 4, 2, 9, 600) == 16
+    inp = decode_inputs(1, 4, 2, 9, 600, seed=443)
+    assert_close(to_numpy(decode_run(inp, 0.5, True)), decode_ref(inp, 0.5, True), "bf16",
+                 "V2 decode Tq=9")
+
+
+def test_v2_decode_matches_oracle_last_rows_at_full_size():
+    # the decode workload's shape (16 heads over 8 key/value heads, 8192
+    # cached keys, one new query per head), two of its sequences
+    w = W.DECODE_WORKLOADS["decode_b16h16kv8q1k8192_d128_shared_k"]
+    inp = W.draw_kv(w, B=2)
+    inp.k2 = inp.k1
+    out = decode_run(inp, w.lambda_value, w.causal)
+    assert_close(to_numpy(out), decode_ref(inp, w.lambda_value, w.causal), "bf16", w.name)
