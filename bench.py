@@ -921,6 +921,41 @@ def wait_profile_summary(raw, spans=None):
     }
 
 
+BWD_WAIT_ROLES = ("producer", "mma_issuer", "elementwise_warps")
+BWD_WAIT_KINDS = ("total_cycles", "kv_slot_free", "query_stage_free", "kv_load", "scores_read_out",
+                  "query_stage_load", "operands_ready", "accumulators_read_out", "scores_ready",
+                  "row_statistics", "scores_tmem_read", "math", "previous_products_done",
+                  "operand_stores", "accumulators_ready", "epilogue", "tile_count", "item_count")
+BWD_WAIT_SHARES = 16   # kinds 1..15 are shares of the role's cycles; the last two are counts
+
+
+def bwd_wait_profile_summary(raw):
+    """The dK/dV kernel's wait profile ([role][kind] counters of the
+    wait-profile build): each role's cycles by what it waits for or works on,
+    as shares of the role's cycles, and per query tile for the elementwise
+    warps."""
+    n = len(BWD_WAIT_KINDS)
+    out = {}
+    for r, role in enumerate(BWD_WAIT_ROLES):
+        tot = raw[n * r]
+        out[role] = {"cycles": tot}
+        for i, k in enumerate(BWD_WAIT_KINDS[1:BWD_WAIT_SHARES], start=1):
+            if raw[n * r + i]:
+                out[role][k] = raw[n * r + i] / tot if tot else None
+    ew = n * BWD_WAIT_ROLES.index("elementwise_warps")
+    tiles, items = raw[ew + 16], raw[ew + 17]
+    if tiles:
+        out["elementwise_warps"]["per_tile_cycles"] = {
+            k: raw[ew + i] / tiles for i, k in enumerate(BWD_WAIT_KINDS) if 8 <= i <= 13}
+        out["elementwise_warps"]["per_tile_cycles"]["all"] = raw[ew] / tiles
+    if items:
+        out["elementwise_warps"]["per_item_epilogue_cycles"] = raw[ew + 15] / items
+    return {"build": "libdiffattn_waitprof.so: the same sources with -DDIFFATTN_WAIT_PROFILE "
+                     "(clock64 around the dK/dV kernel's barrier waits and work; timings of this "
+                     "run are not bench values)",
+            "kernel": "dkdv::diffattn_bwd_dkdv_kernel", "roles": out}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -945,8 +980,9 @@ def main(argv=None):
     ap.add_argument("--norm", choices=["none", "rms", "group"], default="none",
                     help="fuse a per-head norm and the (1 - lambda_init) multiplier")
     ap.add_argument("--wait-profile", action="store_true",
-                    help="forward mode: run the wait-profile build of the library and report "
-                         "each warp role's barrier-wait shares (a measurement run, not a bench value)")
+                    help="forward or backward mode: run the wait-profile build of the library and "
+                         "report each warp role's barrier-wait shares (of the forward kernel, or of "
+                         "the dK/dV kernel; a measurement run, not a bench value)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("at least 3 warm-up steps")
@@ -972,6 +1008,22 @@ def main(argv=None):
         return
     if args.impl == "reference":
         res = run_reference(args, w, world, rank)
+    elif args.mode == "backward" and args.wait_profile:
+        import ctypes as C
+        from differential_attention_fwd_gb300 import _lib
+        from differential_attention_fwd_gb300 import build as build_mod
+        lib = _lib.load(build_mod.build(variant="waitprof"))
+        lib.diffattn_bwd_wait_profile.argtypes = [C.POINTER(C.c_ulonglong), C.c_int]
+        lib.diffattn_bwd_wait_profile.restype = C.c_int
+        clear = (C.c_ulonglong * (3 * len(BWD_WAIT_KINDS)))()
+        lib.diffattn_bwd_wait_profile(clear, len(clear))
+        res = run_backward(args, w, world, rank, local)
+        raw = (C.c_ulonglong * (3 * len(BWD_WAIT_KINDS)))()
+        if lib.diffattn_bwd_wait_profile(raw, len(raw)) != 0:
+            raise RuntimeError("diffattn_bwd_wait_profile failed")
+        res = {"wait_profile": bwd_wait_profile_summary(list(raw)), "workload": w.name,
+               "steps": args.steps, "warmup": args.warmup,
+               "instrumented_backward_ms": res.get("ms_per_step")}
     elif args.mode == "backward":
         res = run_backward(args, w, world, rank, local)
     elif args.wait_profile:

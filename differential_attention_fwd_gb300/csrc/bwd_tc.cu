@@ -426,16 +426,72 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
 // ===========================================================================
 namespace dkdv {
 
+// Wait profile of this kernel (only in the separate build compiled with
+// -DDIFFATTN_WAIT_PROFILE; the regular build has none of it): each role's
+// issuing thread (lane 0 of each elementwise warp) counts SM cycles by what it
+// waits for or works on and adds them to g_prof[role][kind] when the CTA ends.
+// Roles: 0 the TMA producer, 1 the MMA-issuing thread, 2 the eight
+// elementwise warps.  Kinds: 0 the role's cycles from start to end; the
+// producer's waits for the K/V slot (1) and for a query stage (2) to be
+// released; the MMA thread's waits for K/V (3), for the scores to be read out
+// (4), for a query stage (5), for the bf16 operands (6) and for the
+// accumulators to be read out (7); the elementwise warps' waits for the
+// scores (8), their handling of the row statistics (9: scratch writes and the
+// next tile's load), their TMEM read of the
+// scores (10), arithmetic (11), wait for the previous tile's gradient
+// products (12), operand stores (13), wait for the accumulators (14) and the
+// epilogue (15); the tile (16) and item (17) counts.
+enum : int {
+    kPTotal = 0, kPKvEmpty = 1, kPQEmpty = 2, kPKvFull = 3, kPSFree = 4, kPQFull = 5,
+    kPDsFull = 6, kPAccEmpty = 7, kPSFull = 8, kPStats = 9, kPRead = 10, kPMath = 11,
+    kPPkFree = 12, kPStore = 13, kPAccFull = 14, kPEpilogue = 15, kPTiles = 16, kPItems = 17,
+    kPKinds = 18
+};
+#ifdef DIFFATTN_WAIT_PROFILE
+__device__ unsigned long long g_prof[3][kPKinds];
+struct Prof {
+    unsigned long long c[kPKinds] = {};
+    long long t0 = 0;
+    __device__ __forceinline__ void start() { t0 = clock64(); }
+    template <class F>
+    __device__ __forceinline__ bool timed(int kind, F&& f) {
+        const long long a = clock64();
+        const bool r = f();
+        c[kind] += (unsigned long long)(clock64() - a);
+        return r;
+    }
+    __device__ __forceinline__ void flush(int role, bool reporter) {
+        c[kPTotal] = (unsigned long long)(clock64() - t0);
+        if (reporter)
+            for (int i = 0; i < kPKinds; ++i) atomicAdd(&g_prof[role][i], c[i]);
+    }
+};
+#define BP_WAIT(pf, kind, expr) (pf).timed((kind), [&]() -> bool { return (expr); })
+#define BP_MARK(var) long long var = clock64()
+#define BP_ADD(pf, kind, since) ((pf).c[kind] += (unsigned long long)(clock64() - (since)))
+#define BP_RESET(var) (var = clock64())
+#define BP_COUNT(pf, kind) ((pf).c[kind] += 1)
+#else
+struct Prof {
+    __device__ __forceinline__ void start() {}
+    __device__ __forceinline__ void flush(int, bool) {}
+};
+#define BP_WAIT(pf, kind, expr) (expr)
+#define BP_MARK(var) ((void)0)
+#define BP_ADD(pf, kind, since) ((void)0)
+#define BP_RESET(var) ((void)0)
+#define BP_COUNT(pf, kind) ((void)0)
+#endif
+
 constexpr int BM = 128;            // key rows per item (TMEM lanes)
 constexpr int BN = 64;             // query rows per tile
-constexpr int QSTAGES = 4;         // (Q1, Q2, dO, row statistics) ring
+constexpr int QSTAGES = 4;         // (Q1, Q2, dO) ring
 constexpr uint32_t K_BYTES = BM * HD * 2;          // 16 KB
 constexpr uint32_t V_HALF = BM * 64 * 2;           // 16 KB
 constexpr uint32_t Q_BYTES = BN * HD * 2;          // 8 KB
 constexpr uint32_t DO_HALF = BN * 64 * 2;          // 8 KB
-constexpr uint32_t ST_BYTES = BN * 16;             // 1 KB: 4 floats per query row
-constexpr uint32_t QSTAGE_BYTES = 2 * Q_BYTES + 2 * DO_HALF + ST_BYTES;   // 33 KB
-constexpr uint32_t QS_Q1 = 0, QS_Q2 = Q_BYTES, QS_DO = 2 * Q_BYTES, QS_ST = 2 * Q_BYTES + 2 * DO_HALF;
+constexpr uint32_t QSTAGE_BYTES = 2 * Q_BYTES + 2 * DO_HALF;   // 32 KB
+constexpr uint32_t QS_Q1 = 0, QS_Q2 = Q_BYTES, QS_DO = 2 * Q_BYTES;
 
 constexpr uint32_t OFF_K1 = 0;
 constexpr uint32_t OFF_K2 = OFF_K1 + K_BYTES;
@@ -447,7 +503,11 @@ constexpr uint32_t QSTAGE_STRIDE = (QSTAGE_BYTES + 1023) & ~1023u;
 // to tensor memory)
 constexpr uint32_t PK_BYTES = BM * BN * 2;                         // 16 KB
 constexpr uint32_t OFF_PK = OFF_QS + QSTAGES * QSTAGE_STRIDE;
-constexpr uint32_t OFF_BAR = OFF_PK + PK_BYTES;
+// per elementwise warp: the row statistics of its 32 query columns, by
+// quantity (-lse_1, -lse_2, -Dd_1, -Dd_2: 4 x 32 floats)
+constexpr uint32_t SCR_BYTES = 8 * 4 * 32 * 4;                     // 4 KB
+constexpr uint32_t OFF_SCR = OFF_PK + PK_BYTES;
+constexpr uint32_t OFF_BAR = OFF_SCR + SCR_BYTES;
 constexpr int BAR_KV_FULL = 0;
 constexpr int BAR_KV_EMPTY = 1;
 constexpr int BAR_Q_FULL = 2;
@@ -545,6 +605,8 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
         if (warp == 8) {
             // ------------------------------------------------------ producer
             if (elect_one()) {
+                Prof pf;
+                pf.start();
                 uint32_t qs = 0, qph = 0, kvph = 0;
                 uint32_t armed_kv = 0, armed_q[QSTAGES] = {};
                 bool ok = true;
@@ -553,7 +615,7 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     if (idx >= total) break;
                     const Item it = decode_item(idx, p);
                     if (k > 0) {
-                        if (!(ok = mbar_wait(&bars[BAR_KV_EMPTY], kvph, ab))) break;
+                        if (!(ok = BP_WAIT(pf, kPKvEmpty, mbar_wait(&bars[BAR_KV_EMPTY], kvph, ab)))) break;
                         kvph ^= 1;
                     }
                     const int k0 = it.kt * BM;
@@ -566,18 +628,14 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     for (int t = 0; t < g * it.per_head && ok; ++t) {
                         const int h = it.hk * g + t / it.per_head;
                         const int qt = it.qt0 + t % it.per_head;
-                        if (!(ok = mbar_wait(&bars[BAR_Q_EMPTY + qs], qph ^ 1, ab))) break;
+                        if (!(ok = BP_WAIT(pf, kPQEmpty, mbar_wait(&bars[BAR_Q_EMPTY + qs], qph ^ 1, ab)))) break;
                         uint8_t* st = smem + OFF_QS + qs * QSTAGE_STRIDE;
                         const int q0 = qt * BN;
-                        const int rows = min(BN, p.T - q0);
-                        mbar_arrive_expect_tx(&bars[BAR_Q_FULL + qs],
-                                              2 * Q_BYTES + 2 * DO_HALF + (uint32_t)rows * 16u);
+                        mbar_arrive_expect_tx(&bars[BAR_Q_FULL + qs], QSTAGE_BYTES);
                         tma_load_4d(st + QS_Q1, &tm_q1, &bars[BAR_Q_FULL + qs], 0, q0, h, it.b);
                         tma_load_4d(st + QS_Q2, &tm_q2, &bars[BAR_Q_FULL + qs], 0, q0, h, it.b);
                         tma_load_4d(st + QS_DO, &tm_do, &bars[BAR_Q_FULL + qs], 0, q0, h, it.b);
                         tma_load_4d(st + QS_DO + DO_HALF, &tm_do, &bars[BAR_Q_FULL + qs], 64, q0, h, it.b);
-                        bulk_load(st + QS_ST, p.stats + (((int64_t)it.b * p.H + h) * p.T + q0) * 4,
-                                  (uint32_t)rows * 16u, &bars[BAR_Q_FULL + qs]);
                         ++armed_q[qs];
                         if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
                     }
@@ -586,11 +644,14 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 if (armed_kv) mbar_wait_teardown(&bars[BAR_KV_FULL], (armed_kv - 1) & 1, lim);
                 for (int s = 0; s < QSTAGES; ++s)
                     if (armed_q[s]) mbar_wait_teardown(&bars[BAR_Q_FULL + s], (armed_q[s] - 1) & 1, lim);
+                pf.flush(0, true);
             }
             __syncwarp();
         } else if (warp == 9) {
             // ------------------------------------------------------ MMA issue
             if (elect_one()) {
+                Prof pf;
+                pf.start();
                 const uint64_t k1d = sdesc_sw128(smem_u32(smem + OFF_K1), 16, 1024);
                 const uint64_t k2d = sdesc_sw128(smem_u32(smem + OFF_K2), 16, 1024);
                 const uint64_t vd = sdesc_sw128(smem_u32(smem + OFF_V), 16, 1024);
@@ -605,8 +666,10 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 // the previous tile's scores must have been read out of TMEM.
                 auto issue_s = [&]() -> bool {
                     const uint32_t qs = tiles % QSTAGES;
-                    if (tiles > 0 && !mbar_wait(&bars[BAR_S_FREE], (tiles - 1) & 1u, ab)) return false;
-                    if (!mbar_wait(&bars[BAR_Q_FULL + qs], (tiles / QSTAGES) & 1u, ab)) return false;
+                    if (tiles > 0 && !BP_WAIT(pf, kPSFree, mbar_wait(&bars[BAR_S_FREE], (tiles - 1) & 1u, ab)))
+                        return false;
+                    if (!BP_WAIT(pf, kPQFull, mbar_wait(&bars[BAR_Q_FULL + qs], (tiles / QSTAGES) & 1u, ab)))
+                        return false;
                     tc_fence_after();
                     const uint64_t sb = (qs * QSTAGE_STRIDE) >> 4;
 #pragma unroll
@@ -631,7 +694,7 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     if (idx >= total) break;
                     const Item it = decode_item(idx, p);
                     const int n = g * it.per_head;
-                    if (!(ok = mbar_wait(&bars[BAR_KV_FULL], kvph, ab))) break;
+                    if (!(ok = BP_WAIT(pf, kPKvFull, mbar_wait(&bars[BAR_KV_FULL], kvph, ab)))) break;
                     kvph ^= 1;
                     if (!(ok = issue_s())) break;
                     if (n == 1) mma_commit(&bars[BAR_KV_EMPTY]);
@@ -641,10 +704,10 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                             if (!(ok = issue_s())) break;
                             if (t + 2 == n) mma_commit(&bars[BAR_KV_EMPTY]);
                         }
-                        if (!(ok = mbar_wait(&bars[BAR_DS_FULL], dsph, ab))) break;
+                        if (!(ok = BP_WAIT(pf, kPDsFull, mbar_wait(&bars[BAR_DS_FULL], dsph, ab)))) break;
                         dsph ^= 1;
                         if (t == 0 && !first) {
-                            if (!(ok = mbar_wait(&bars[BAR_ACC_EMPTY], accph, ab))) break;
+                            if (!(ok = BP_WAIT(pf, kPAccEmpty, mbar_wait(&bars[BAR_ACC_EMPTY], accph, ab)))) break;
                             accph ^= 1;
                         }
                         tc_fence_after();
@@ -672,12 +735,15 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 }
                 mma_commit(&bars[BAR_FINAL]);
                 mbar_wait_teardown(&bars[BAR_FINAL], 0, 200ull * 1000ull * 1000ull);
+                pf.flush(1, true);
             }
             __syncwarp();
         }
     } else {
         regs_inc<REGS_WORK>();
         // ---------------------------------- dS^T, W^T and the dK/dV epilogue
+        Prof pf;
+        pf.start();
         const int half = warp >> 2;          // query columns [32*half, 32*half + 32)
         const uint32_t quad = warp & 3;
         const int row = quad * 32 + lane;    // key row within the tile
@@ -686,6 +752,24 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
         const float lam = p.lambda_dev ? __ldg(p.lambda_dev) : p.lambda;
         uint32_t accph = 0, qc = 0;   // qc: query tiles consumed (whole launch)
         bool ok = true;
+        // Row statistics (-lse_1, -lse_2, -Dd_1, -Dd_2) of the warp's 32 query
+        // columns: lane l loads column l's from global memory one tile ahead
+        // (zeros past T) and, when the tile starts, writes them to the warp's
+        // scratch by quantity, so that the packed f32x2 arithmetic reads the
+        // values of a column pair with one load and the tile's products wait
+        // on no copy of them.
+        float* scr = reinterpret_cast<float*>(smem + OFF_SCR) + warp * 128;
+        const int col = 32 * half + (int)lane;
+        auto stats_of = [&](int b, int h, int qt) -> float4 {
+            const int q = qt * BN + col;
+            if (q >= p.T) return make_float4(0.f, 0.f, 0.f, 0.f);
+            return __ldg(reinterpret_cast<const float4*>(p.stats) + (((int64_t)b * p.H + h) * p.T + q));
+        };
+        float4 nst = make_float4(0.f, 0.f, 0.f, 0.f);     // the next tile's statistics
+        if (item_index(0, cta, grid) < total) {
+            const Item it0 = decode_item(item_index(0, cta, grid), p);
+            nst = stats_of(it0.b, it0.hk * g, it0.qt0);
+        }
         for (int k = 0; ok; ++k) {
             const int idx = item_index(k, cta, grid);
             if (idx >= total) break;
@@ -694,23 +778,38 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
             const int n = g * it.per_head;
             for (int t = 0; t < n; ++t, ++qc) {
                 const int qt = it.qt0 + t % it.per_head;
-                const uint32_t qs = qc % QSTAGES;
-                if (!(ok = mbar_wait_warp(&bars[BAR_S_FULL], qc & 1u, ab))) break;
-                // the stage's row statistics came by TMA: observe its completion
-                if (!(ok = mbar_wait_warp(&bars[BAR_Q_FULL + qs], (qc / QSTAGES) & 1u, ab))) break;
+                BP_MARK(tp);
+                __syncwarp();               // the previous tile's reads of the scratch are done
+                scr[lane] = nst.x;
+                scr[32 + lane] = nst.y;
+                scr[64 + lane] = nst.z;
+                scr[96 + lane] = nst.w;
+                __syncwarp();
+                if (t + 1 < n) {
+                    nst = stats_of(it.b, it.hk * g + (t + 1) / it.per_head, it.qt0 + (t + 1) % it.per_head);
+                } else {
+                    const int nidx = item_index(k + 1, cta, grid);
+                    if (nidx < total) {
+                        const Item nit = decode_item(nidx, p);
+                        nst = stats_of(nit.b, nit.hk * g, nit.qt0);
+                    }
+                }
+                BP_ADD(pf, kPStats, tp);
+                if (!(ok = BP_WAIT(pf, kPSFull, mbar_wait_warp(&bars[BAR_S_FULL], qc & 1u, ab)))) break;
+                BP_RESET(tp);
                 tc_fence_after();
                 const uint32_t c0 = 32 * half;
                 uint32_t s1[32], s2[32], dp[32];
                 tmem_ld32(lane_base + TM_S1 + c0, s1);
                 tmem_ld32(lane_base + TM_S2 + c0, s2);
                 tmem_ld32(lane_base + TM_DP + c0, dp);
-                const float4* stv = reinterpret_cast<const float4*>(
-                    smem + OFF_QS + qs * QSTAGE_STRIDE + QS_ST) + c0;
                 tmem_wait_ld();
                 // the scores are in registers: the next tile's products may overwrite them
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[BAR_S_FREE]);
+                BP_ADD(pf, kPRead, tp);
+                BP_RESET(tp);
                 // query qt*64 + c0 + c sees this key iff key <= query (and query < T);
                 // statistics are stored negated: (-lse_1, -lse_2, -Dd_1, -Dd_2)
                 const int qbase = qt * BN + (int)c0;
@@ -725,7 +824,8 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     const int qlim = p.T - qbase;                         // columns c < qlim exist
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
-                        const float4 sa = stv[c], sb = stv[c + 1];
+                        const float4 sa = make_float4(scr[c], scr[32 + c], scr[64 + c], scr[96 + c]);
+                        const float4 sb = make_float4(scr[c + 1], scr[33 + c], scr[65 + c], scr[97 + c]);
                         const bool v0 = c >= first_vis && c < qlim;
                         const bool v1 = c + 1 >= first_vis && c + 1 < qlim;
                         const float a10 = v0 ? ex2_approx(fmaf(__uint_as_float(s1[c]), sl2, sa.x)) : 0.f;
@@ -744,24 +844,38 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         w3[c / 2] = pack_bf16x2(a10 - lam * a20, a11 - lam * a21);
                     }
                 } else {
+                    // columns c .. c + 3: one load of each quantity, two column pairs
+                    const float4* pl = reinterpret_cast<const float4*>(scr);
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const float4 sa = stv[c], sb = stv[c + 1];
-                        const uint64_t x1 = f2_fma(f2_from_bits(s1[c], s1[c + 1]), sl2x2, f2_pack(sa.x, sb.x));
-                        const uint64_t x2 = f2_fma(f2_from_bits(s2[c], s2[c + 1]), sl2x2, f2_pack(sa.y, sb.y));
-                        const uint64_t a1 = f2_pack(ex2_approx(f2_lo(x1)), ex2_approx(f2_hi(x1)));
-                        const uint64_t a2n = f2_mul(f2_pack(ex2_approx(f2_lo(x2)), ex2_approx(f2_hi(x2))), nlam2);
-                        const uint64_t dp2 = f2_from_bits(dp[c], dp[c + 1]);
-                        const uint64_t d1 = f2_mul(a1, f2_add(dp2, f2_pack(sa.z, sb.z)));
-                        const uint64_t d2 = f2_mul(a2n, f2_add(dp2, f2_pack(sa.w, sb.w)));
-                        const uint64_t w = f2_add(a1, a2n);
-                        w1[c / 2] = pack_bf16x2(f2_lo(d1), f2_hi(d1));
-                        w2[c / 2] = pack_bf16x2(f2_lo(d2), f2_hi(d2));
-                        w3[c / 2] = pack_bf16x2(f2_lo(w), f2_hi(w));
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 l1 = pl[c / 4], l2 = pl[8 + c / 4], e1 = pl[16 + c / 4], e2 = pl[24 + c / 4];
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int cc = c + 2 * hh;
+                            const uint64_t L1 = hh ? f2_pack(l1.z, l1.w) : f2_pack(l1.x, l1.y);
+                            const uint64_t L2 = hh ? f2_pack(l2.z, l2.w) : f2_pack(l2.x, l2.y);
+                            const uint64_t E1 = hh ? f2_pack(e1.z, e1.w) : f2_pack(e1.x, e1.y);
+                            const uint64_t E2 = hh ? f2_pack(e2.z, e2.w) : f2_pack(e2.x, e2.y);
+                            const uint64_t x1 = f2_fma(f2_from_bits(s1[cc], s1[cc + 1]), sl2x2, L1);
+                            const uint64_t x2 = f2_fma(f2_from_bits(s2[cc], s2[cc + 1]), sl2x2, L2);
+                            const uint64_t a1 = f2_pack(ex2_approx(f2_lo(x1)), ex2_approx(f2_hi(x1)));
+                            const uint64_t a2n =
+                                f2_mul(f2_pack(ex2_approx(f2_lo(x2)), ex2_approx(f2_hi(x2))), nlam2);
+                            const uint64_t dp2 = f2_from_bits(dp[cc], dp[cc + 1]);
+                            const uint64_t d1 = f2_mul(a1, f2_add(dp2, E1));
+                            const uint64_t d2 = f2_mul(a2n, f2_add(dp2, E2));
+                            const uint64_t w = f2_add(a1, a2n);
+                            w1[cc / 2] = pack_bf16x2(f2_lo(d1), f2_hi(d1));
+                            w2[cc / 2] = pack_bf16x2(f2_lo(d2), f2_hi(d2));
+                            w3[cc / 2] = pack_bf16x2(f2_lo(w), f2_hi(w));
+                        }
                     }
                 }
+                BP_ADD(pf, kPMath, tp);
                 // the previous tile's dV/dK products must have read the operands
-                if (qc > 0 && !(ok = mbar_wait_warp(&bars[BAR_PK_FREE], (qc - 1) & 1u, ab))) break;
+                if (qc > 0 && !(ok = BP_WAIT(pf, kPPkFree, mbar_wait_warp(&bars[BAR_PK_FREE], (qc - 1) & 1u, ab))))
+                    break;
+                BP_RESET(tp);
                 // W^T and dS_1^T to TMEM: queries [c0, c0 + 32) are packed columns
                 // [16*half, 16*half + 16) of their regions
                 tmem_st16(lane_base + TM_W + 16 * half, w3);
@@ -781,11 +895,15 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[BAR_DS_FULL]);
+                BP_ADD(pf, kPStore, tp);
+                BP_COUNT(pf, kPTiles);
             }
             if (!ok) break;
+            BP_COUNT(pf, kPItems);
             // epilogue: warpgroup 0 writes dV columns 0-63 and dK_1, warpgroup
             // 1 dV columns 64-127 and dK_2
-            if (!(ok = mbar_wait_warp(&bars[BAR_ACC_FULL], accph, ab))) break;
+            if (!(ok = BP_WAIT(pf, kPAccFull, mbar_wait_warp(&bars[BAR_ACC_FULL], accph, ab)))) break;
+            BP_MARK(te);
             accph ^= 1;
             tc_fence_after();
             uint32_t gv[64], gk[64];
@@ -816,7 +934,9 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         pack_bf16x2(__uint_as_float(gk[c + 6]) * p.scale, __uint_as_float(gk[c + 7]) * p.scale));
                 }
             }
+            BP_ADD(pf, kPEpilogue, te);
         }
+        pf.flush(2, lane == 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -827,6 +947,23 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
 }  // namespace dkdv
 
 }  // namespace bwdtc
+
+#ifdef DIFFATTN_WAIT_PROFILE
+// The dK/dV kernel's wait-profile counters accumulated since the last call
+// ([3 roles][18 kinds], see dkdv::Prof), copied to `out` and cleared.  Only in
+// the build with -DDIFFATTN_WAIT_PROFILE.
+extern "C" int diffattn_bwd_wait_profile(unsigned long long* out, int n) {
+    constexpr int kN = 3 * bwdtc::dkdv::kPKinds;
+    if (!out || n < kN) return -1;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(out, bwdtc::dkdv::g_prof, kN * sizeof(unsigned long long)) != cudaSuccess)
+        return -3;
+    static unsigned long long zero[kN] = {};
+    return cudaMemcpyToSymbol(bwdtc::dkdv::g_prof, zero, kN * sizeof(unsigned long long)) == cudaSuccess
+               ? 0
+               : -3;
+}
+#endif
 
 int launch_bwd_tc(const CUtensorMap* maps, const BwdTcParams& p, int num_sms, cudaStream_t stream) {
     using namespace bwdtc;

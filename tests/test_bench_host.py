@@ -141,3 +141,22 @@ def test_wait_profile_summary_shares():
     pw = s["roles"]["softmax_warps"]["per_warp_cycles"]
     assert pw["first_tile"] == pytest.approx(150) and pw["other_tile"] == pytest.approx(112.5)
     assert pw["epilogue"] == pytest.approx(100) and pw["epilogue_o_load"] == pytest.approx(30)
+
+
+def test_bwd_wait_profile_summary():
+    n = len(bench.BWD_WAIT_KINDS)
+    raw = [0] * (3 * n)
+    raw[0:3] = [1000, 200, 300]                      # producer: total, K/V slot, query stage
+    raw[n + 0], raw[n + 4], raw[n + 6] = 2000, 500, 1000   # MMA: total, scores read out, operands
+    ew = 2 * n
+    raw[ew + 0] = 8000
+    raw[ew + 8:ew + 14] = [800, 0, 400, 4000, 1200, 800]   # scores, stats, read, math, prev, stores
+    raw[ew + 15], raw[ew + 16], raw[ew + 17] = 400, 4, 2
+    s = bench.bwd_wait_profile_summary(raw)
+    r = s["roles"]
+    assert r["producer"]["kv_slot_free"] == pytest.approx(0.2)
+    assert r["mma_issuer"]["operands_ready"] == pytest.approx(0.5)
+    assert "row_statistics" not in r["elementwise_warps"]
+    pt = r["elementwise_warps"]["per_tile_cycles"]
+    assert pt["math"] == pytest.approx(1000) and pt["all"] == pytest.approx(2000)
+    assert r["elementwise_warps"]["per_item_epilogue_cycles"] == pytest.approx(200)
