@@ -371,12 +371,21 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         pk[c] = pack_bf16x2(f2_lo(z), f2_hi(z));
                     }
                 } else {
+                    // in three phases, in place in the score registers, so that
+                    // each is a run of independent operations: the exponents, the
+                    // exponentials, then dS_b = coef * A_b * (dP - Dd_b)
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const uint64_t x = f2_fma(f2_from_bits(s[2 * c], s[2 * c + 1]), sl2x2, nlse2);
-                        const uint64_t a = f2_pack(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
+                        s[2 * c] = static_cast<uint32_t>(x);
+                        s[2 * c + 1] = static_cast<uint32_t>(x >> 32);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) s[c] = __float_as_uint(ex2_approx(__uint_as_float(s[c])));
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
                         const uint64_t y = f2_fma(f2_from_bits(dp[2 * c], dp[2 * c + 1]), coef2, cndd2);
-                        const uint64_t z = f2_mul(a, y);
+                        const uint64_t z = f2_mul(f2_from_bits(s[2 * c], s[2 * c + 1]), y);
                         pk[c] = pack_bf16x2(f2_lo(z), f2_hi(z));
                     }
                 }
@@ -776,8 +785,13 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
             const Item it = decode_item(idx, p);
             const int key = it.kt * BM + row;
             const int n = g * it.per_head;
+            int h = it.hk * g, qt = it.qt0;  // the tile's query head and 64-row query tile
             for (int t = 0; t < n; ++t, ++qc) {
-                const int qt = it.qt0 + t % it.per_head;
+                int h1 = h, qt1 = qt + 1;    // the next tile's
+                if (qt1 == p.nk64) {
+                    qt1 = it.qt0;
+                    ++h1;
+                }
                 BP_MARK(tp);
                 __syncwarp();               // the previous tile's reads of the scratch are done
                 scr[lane] = nst.x;
@@ -786,7 +800,7 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 scr[96 + lane] = nst.w;
                 __syncwarp();
                 if (t + 1 < n) {
-                    nst = stats_of(it.b, it.hk * g + (t + 1) / it.per_head, it.qt0 + (t + 1) % it.per_head);
+                    nst = stats_of(it.b, h1, qt1);
                 } else {
                     const int nidx = item_index(k + 1, cta, grid);
                     if (nidx < total) {
@@ -844,23 +858,43 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         w3[c / 2] = pack_bf16x2(a10 - lam * a20, a11 - lam * a21);
                     }
                 } else {
-                    // columns c .. c + 3: one load of each quantity, two column pairs
+                    // In three phases over all 32 columns, in place in the score
+                    // registers, so that every phase is a run of independent
+                    // operations: the exponents, the exponentials (A_1, A_2), then
+                    // dS_1, dS_2 and W.  Columns c .. c + 3 take one load of each
+                    // statistic (two column pairs).
                     const float4* pl = reinterpret_cast<const float4*>(scr);
 #pragma unroll
                     for (int c = 0; c < 32; c += 4) {
-                        const float4 l1 = pl[c / 4], l2 = pl[8 + c / 4], e1 = pl[16 + c / 4], e2 = pl[24 + c / 4];
+                        const float4 l1 = pl[c / 4], l2 = pl[8 + c / 4];
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
                             const int cc = c + 2 * hh;
                             const uint64_t L1 = hh ? f2_pack(l1.z, l1.w) : f2_pack(l1.x, l1.y);
                             const uint64_t L2 = hh ? f2_pack(l2.z, l2.w) : f2_pack(l2.x, l2.y);
-                            const uint64_t E1 = hh ? f2_pack(e1.z, e1.w) : f2_pack(e1.x, e1.y);
-                            const uint64_t E2 = hh ? f2_pack(e2.z, e2.w) : f2_pack(e2.x, e2.y);
                             const uint64_t x1 = f2_fma(f2_from_bits(s1[cc], s1[cc + 1]), sl2x2, L1);
                             const uint64_t x2 = f2_fma(f2_from_bits(s2[cc], s2[cc + 1]), sl2x2, L2);
-                            const uint64_t a1 = f2_pack(ex2_approx(f2_lo(x1)), ex2_approx(f2_hi(x1)));
-                            const uint64_t a2n =
-                                f2_mul(f2_pack(ex2_approx(f2_lo(x2)), ex2_approx(f2_hi(x2))), nlam2);
+                            s1[cc] = static_cast<uint32_t>(x1);
+                            s1[cc + 1] = static_cast<uint32_t>(x1 >> 32);
+                            s2[cc] = static_cast<uint32_t>(x2);
+                            s2[cc + 1] = static_cast<uint32_t>(x2 >> 32);
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        s1[c] = __float_as_uint(ex2_approx(__uint_as_float(s1[c])));
+                        s2[c] = __float_as_uint(ex2_approx(__uint_as_float(s2[c])));
+                    }
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 e1 = pl[16 + c / 4], e2 = pl[24 + c / 4];
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int cc = c + 2 * hh;
+                            const uint64_t E1 = hh ? f2_pack(e1.z, e1.w) : f2_pack(e1.x, e1.y);
+                            const uint64_t E2 = hh ? f2_pack(e2.z, e2.w) : f2_pack(e2.x, e2.y);
+                            const uint64_t a1 = f2_from_bits(s1[cc], s1[cc + 1]);
+                            const uint64_t a2n = f2_mul(f2_from_bits(s2[cc], s2[cc + 1]), nlam2);
                             const uint64_t dp2 = f2_from_bits(dp[cc], dp[cc + 1]);
                             const uint64_t d1 = f2_mul(a1, f2_add(dp2, E1));
                             const uint64_t d2 = f2_mul(a2n, f2_add(dp2, E2));
@@ -897,6 +931,8 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 if (lane == 0) mbar_arrive(&bars[BAR_DS_FULL]);
                 BP_ADD(pf, kPStore, tp);
                 BP_COUNT(pf, kPTiles);
+                h = h1;
+                qt = qt1;
             }
             if (!ok) break;
             BP_COUNT(pf, kPItems);
