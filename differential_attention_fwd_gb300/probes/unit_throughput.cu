@@ -1,8 +1,9 @@
 // unit_throughput.cu -- throughput of the instructions the attention kernels'
 // elementwise warps use (ex2.approx.f32, ex2.approx.bf16x2, fma.rn.f32x2,
-// cvt.rn.bf16x2.f32, scalar fmul) and of pairs of them interleaved, on one CTA
-// of 512 threads per SM with eight independent dependency chains per thread,
-// timed with clock64 per CTA.  Not part of the library: a measurement that
+// cvt.rn.bf16x2.f32, scalar fmul) and of mixes of them, on one CTA of 512
+// threads per SM (or 256, two warps per SM sub-partition as in the kernels)
+// with eight independent dependency chains per thread, timed with clock64 per
+// CTA.  Not part of the library: a measurement that
 // tells which unit bounds a warp's arithmetic.
 //
 //   nvcc -gencode arch=compute_103a,code=sm_103a -O3 -o unit_throughput unit_throughput.cu
@@ -46,9 +47,12 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
 
 // MODE: 0 ex2 (+fadd), 1 ex2.bf16x2 (+xor), 2 fma.f32x2, 3 cvt (+fadd, or),
 // 4 fmul (+xor), 5 ex2 (+fadd) with two fma.f32x2, 6 ex2 (+fadd) with a cvt
-// (+xor), 7 ex2 alone, 8 fma.f32x2 with a cvt (+xor).
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) probe(unsigned long long* cycles, float* sink) {
+// (+xor), 7 ex2 alone, 8 fma.f32x2 with a cvt (+xor), 9 ex2 of arguments in
+// [-16, -1] (+ffma), 10 the pattern of a softmax column pair: an fma.f32x2
+// forming two exponents, two ex2, an add.f32x2 into a running sum and a cvt
+// of the pair.
+template <int MODE, int NT>
+__global__ void __launch_bounds__(NT, 1) probe(unsigned long long* cycles, float* sink) {
     float x[kChains];
     uint32_t xb[kChains];
     uint64_t x2[kChains];
@@ -83,6 +87,18 @@ __global__ void __launch_bounds__(kThreads, 1) probe(unsigned long long* cycles,
                 x2[i] = fma_f32x2(x2[i], m, a);
                 xb[i] = cvt_bf16x2(__uint_as_float(static_cast<uint32_t>(x2[(i + 3) % kChains])), 1.f) ^ xb[i];
             }
+            if (MODE == 9) x[i] = fmaf(ex2_f32(x[i]), -15.0f, -1.0f);
+            if (MODE == 10) {
+                // exponents of a column pair, their 2^x, the running sum, the bf16 pair
+                const uint64_t e = fma_f32x2(x2[i], m, a);
+                const float p0 = ex2_f32(__uint_as_float(static_cast<uint32_t>(e)));
+                const float p1 = ex2_f32(__uint_as_float(static_cast<uint32_t>(e >> 32)));
+                const uint64_t pp = (static_cast<uint64_t>(__float_as_uint(p1)) << 32) | __float_as_uint(p0);
+                uint64_t sum;
+                asm volatile("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(pp), "l"(x2[(i + 1) % kChains]));
+                xb[i] ^= cvt_bf16x2(p0, p1);
+                x2[i] = (sum & 0x807FFFFF807FFFFFull) | 0x3F0000003F000000ull;   // back to [-1, 1)
+            }
         }
     }
     const long long t1 = clock64();
@@ -94,9 +110,10 @@ __global__ void __launch_bounds__(kThreads, 1) probe(unsigned long long* cycles,
     sink[blockIdx.x * blockDim.x + threadIdx.x] = s;     // keeps the chains live
 }
 
-template <int MODE>
+template <int MODE, int NT = kThreads>
 int run(int sms, unsigned long long* cycles, float* sink, const char* name) {
-    for (int rep = 0; rep < 2; ++rep) probe<MODE><<<sms, kThreads>>>(cycles, sink);
+    static_assert(NT <= kThreads, "sink size");
+    for (int rep = 0; rep < 2; ++rep) probe<MODE, NT><<<sms, NT>>>(cycles, sink);
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
     static unsigned long long h[4096];
     if (cudaMemcpy(h, cycles, sms * sizeof(unsigned long long), cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -104,7 +121,7 @@ int run(int sms, unsigned long long* cycles, float* sink, const char* name) {
     double mean = 0;
     for (int i = 0; i < sms; ++i) mean += static_cast<double>(h[i]);
     mean /= sms;
-    const double ops = static_cast<double>(kThreads) * kIters * kChains;
+    const double ops = static_cast<double>(NT) * kIters * kChains;
     std::printf("%-28s %9.0f cycles  %6.2f operations/clock/SM\n", name, mean, ops / mean);
     return 0;
 }
@@ -131,6 +148,10 @@ int main() {
     rc |= run<6>(sms, cycles, sink, "ex2 (+fadd) + cvt (+xor)");
     rc |= run<7>(sms, cycles, sink, "ex2 alone");
     rc |= run<8>(sms, cycles, sink, "fma.f32x2 + cvt (+xor)");
+    rc |= run<9>(sms, cycles, sink, "ex2 of [-16, -1] (+ffma)");
+    rc |= run<10>(sms, cycles, sink, "softmax pair: fma2 2ex2 add2 cvt");
+    rc |= run<7, 256>(sms, cycles, sink, "ex2 alone, 256 threads");
+    rc |= run<10, 256>(sms, cycles, sink, "softmax pair, 256 threads");
     cudaFree(cycles);
     cudaFree(sink);
     return rc == 0 ? 0 : 1;
