@@ -50,7 +50,9 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
 // (+xor), 7 ex2 alone, 8 fma.f32x2 with a cvt (+xor), 9 ex2 of arguments in
 // [-16, -1] (+ffma), 10 the pattern of a softmax column pair: an fma.f32x2
 // forming two exponents, two ex2, an add.f32x2 into a running sum and a cvt
-// of the pair.
+// of the pair (+xor, and two 64-bit logic operations that keep the chain in
+// range), 11 the same pattern without the logic operations: the pair's 2^x
+// feed the next exponents directly (+xor only).
 template <int MODE, int NT>
 __global__ void __launch_bounds__(NT, 1) probe(unsigned long long* cycles, float* sink) {
     float x[kChains];
@@ -63,6 +65,13 @@ __global__ void __launch_bounds__(NT, 1) probe(unsigned long long* cycles, float
     }
     const uint64_t m = (static_cast<uint64_t>(__float_as_uint(0.999f)) << 32) | __float_as_uint(0.999f);
     const uint64_t a = (static_cast<uint64_t>(__float_as_uint(-1e-4f)) << 32) | __float_as_uint(-1e-4f);
+    const uint64_t h = (static_cast<uint64_t>(__float_as_uint(-1.0f)) << 32) | __float_as_uint(-1.0f);
+    const uint64_t z = 0;
+    uint64_t rs[kChains];
+    for (int i = 0; i < kChains; ++i) {
+        rs[i] = 0;
+        if (MODE == 11) x2[i] = (static_cast<uint64_t>(__float_as_uint(0.7f)) << 32) | __float_as_uint(0.6f);
+    }
     __syncthreads();
     const long long t0 = clock64();
     for (int it = 0; it < kIters; ++it) {
@@ -88,6 +97,15 @@ __global__ void __launch_bounds__(NT, 1) probe(unsigned long long* cycles, float
                 xb[i] = cvt_bf16x2(__uint_as_float(static_cast<uint32_t>(x2[(i + 3) % kChains])), 1.f) ^ xb[i];
             }
             if (MODE == 9) x[i] = fmaf(ex2_f32(x[i]), -15.0f, -1.0f);
+            if (MODE == 11) {
+                const uint64_t e = fma_f32x2(x2[i], h, z);     // exponents in [-1, -0.25]
+                const float p0 = ex2_f32(__uint_as_float(static_cast<uint32_t>(e)));
+                const float p1 = ex2_f32(__uint_as_float(static_cast<uint32_t>(e >> 32)));
+                const uint64_t pp = (static_cast<uint64_t>(__float_as_uint(p1)) << 32) | __float_as_uint(p0);
+                asm volatile("add.rn.f32x2 %0, %0, %1;" : "+l"(rs[i]) : "l"(pp));
+                xb[i] ^= cvt_bf16x2(p0, p1);
+                x2[i] = pp;                                       // in [0.5, 1)
+            }
             if (MODE == 10) {
                 // exponents of a column pair, their 2^x, the running sum, the bf16 pair
                 const uint64_t e = fma_f32x2(x2[i], m, a);
@@ -106,7 +124,8 @@ __global__ void __launch_bounds__(NT, 1) probe(unsigned long long* cycles, float
     if (threadIdx.x == 0) cycles[blockIdx.x] = static_cast<unsigned long long>(t1 - t0);
     float s = 0.f;
     for (int i = 0; i < kChains; ++i)
-        s += x[i] + __uint_as_float(xb[i]) + __uint_as_float(static_cast<uint32_t>(x2[i]));
+        s += x[i] + __uint_as_float(xb[i]) + __uint_as_float(static_cast<uint32_t>(x2[i])) +
+             __uint_as_float(static_cast<uint32_t>(rs[i]));
     sink[blockIdx.x * blockDim.x + threadIdx.x] = s;     // keeps the chains live
 }
 
@@ -150,6 +169,8 @@ int main() {
     rc |= run<8>(sms, cycles, sink, "fma.f32x2 + cvt (+xor)");
     rc |= run<9>(sms, cycles, sink, "ex2 of [-16, -1] (+ffma)");
     rc |= run<10>(sms, cycles, sink, "softmax pair: fma2 2ex2 add2 cvt");
+    rc |= run<11>(sms, cycles, sink, "softmax pair, no logic ops");
+    rc |= run<11, 256>(sms, cycles, sink, "same, 256 threads");
     rc |= run<7, 256>(sms, cycles, sink, "ex2 alone, 256 threads");
     rc |= run<10, 256>(sms, cycles, sink, "softmax pair, 256 threads");
     cudaFree(cycles);
