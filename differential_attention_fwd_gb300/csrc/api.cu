@@ -242,66 +242,33 @@ struct DecodePlan {
     // The queries go through the forward kernels instead (more query rows than
     // the split-key decode takes, or a value width other than 2D).
     bool forward = false;
-    // The DIFF V2 head (bf16, D = 128, value width 128, up to 8 queries): the
-    // tensor-core split-key decode when the call's cache allows it (one key
-    // tensor, dense 16-byte aligned rows), else the forward kernels.
-    bool v2 = false;
+    // The tensor-core split-key decode in units of up to 16 query rows, or the
+    // forward kernels when the call's layout does not allow it: the DIFF V2
+    // head (bf16, D = 128, value width 128, up to 16 queries; it needs one key
+    // tensor for both branches), and bf16 D = 64 with more than 8 query rows
+    // per key/value head (up to 16 queries).  Dense 16-byte aligned rows.
+    bool tc_only = false;
+    // For a tensor-core plan at D = 64: the split-key layout of up to 8-row
+    // units that a call runs on the CUDA cores when its layout does not allow
+    // the tensor-core pass (the workspace has room for both).
+    bool fb_valid = false;
+    int fb_tq_bucket = 0, fb_splits = 0, fb_split_len = 0, fb_row_chunks = 0;
 };
 
-// Query rows per unit of the V2 decode (1, 2, 4 or 8) for `rows` rows.
-int v2_bucket(int64_t rows) {
-    for (int t = 1; t <= 8; t *= 2)
+// Query rows per unit of the tensor-core decode (1, 2, 4, 8 or 16).
+int tc_bucket(int64_t rows) {
+    for (int t = 1; t <= 16; t *= 2)
         if (rows <= t) return t;
-    return 8;
+    return 16;
 }
 
 // Bytes a call asks for when it runs on the forward kernels: none are used,
 // but the workspace contract (a non-zero size for a valid request) holds.
 constexpr size_t kForwardPathWorkBytes = 16;
 
-int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
-    if (!d) return DIFFATTN_ERR_INVALID;
-    if (d->B < 1 || d->H < 1 || d->Tq < 1 || d->Tk < 1 || d->D < 1) return DIFFATTN_ERR_INVALID;
-    if (d->dtype != DIFFATTN_BF16 && d->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID;
-    if (d->kv_group < 0 || d->H % group_of(d->kv_group) != 0) return DIFFATTN_ERR_INVALID;
-    if (d->Dv < 0 || d->D > 128 || value_width(d->Dv, d->D) > 256) return DIFFATTN_ERR_INVALID;
-    if (!strides_nonneg(d->q1_stride) || !strides_nonneg(d->k1_stride) ||
-        !strides_nonneg(d->q2_stride) || !strides_nonneg(d->k2_stride) ||
-        !strides_nonneg(d->v_stride) || !strides_nonneg(d->o_stride))
-        return DIFFATTN_ERR_INVALID;
-    if (causal && d->Tk < d->Tq) return DIFFATTN_ERR_INVALID;
-    if (d->Tk > INT32_MAX / 2 || d->Tq > INT32_MAX / 2 || d->H > (1 << 24))
-        return DIFFATTN_ERR_UNSUPPORTED;
-    const int cap = (d->D == 32 || d->D == 64 || d->D == 128) ? decode_max_rows((int)d->D) : 0;
-    if (d->dtype == DIFFATTN_BF16 && d->D == 128 && value_width(d->Dv, d->D) == 128 && d->Tq <= 8) {
-        // rows of the heads that share a key/value head, 8 per unit at most
-        const int64_t g = group_of(d->kv_group);
-        const int64_t rows = g * d->Tq;
-        const int64_t row_chunks = (rows + 7) / 8;
-        const int64_t Hk = d->H / g;
-        const int64_t units = d->B * Hk * row_chunks;
-        if (units > (1ll << 24) || d->B * d->H > (1ll << 24) || d->B * d->H * d->Tq > INT32_MAX)
-            return DIFFATTN_ERR_UNSUPPORTED;
-        plan->v2 = true;
-        plan->tq_bucket = v2_bucket((rows + row_chunks - 1) / row_chunks);
-        plan->splits = 1;                   // the tensor-core pass sets its own
-        plan->split_len = (int)(((d->Tk + 255) / 256) * 256);
-        plan->kv_group = (int)g;
-        plan->Hk = (int)Hk;
-        plan->row_chunks = (int)row_chunks;
-        plan->work_bytes = decode_tc_work_floats(units, d->Tk, plan->tq_bucket) * sizeof(float);
-        return DIFFATTN_OK;
-    }
-    if (d->Tq > cap || value_width(d->Dv, d->D) != 2 * d->D) {
-        // queries over the cache on the forward kernels (chunked prefill)
-        const int64_t nq = (d->Tq + 127) / 128;
-        if (d->B * d->H > INT32_MAX / nq) return DIFFATTN_ERR_UNSUPPORTED;
-        plan->forward = true;
-        plan->kv_group = (int)group_of(d->kv_group);
-        plan->Hk = (int)(d->H / plan->kv_group);
-        plan->work_bytes = kForwardPathWorkBytes;
-        return DIFFATTN_OK;
-    }
+// The split-key layout of a decode with up to `cap` rows per unit (the
+// descriptor already checked; Tq <= cap, value width 2D).
+int plan_split_key(const diffattn_kv_desc* d, int cap, DecodePlan* plan) {
     // The query rows of the heads that share a key/value head (g * Tq of
     // them) go in as few CTAs as the row capacity allows, evenly filled.
     const int64_t g = group_of(d->kv_group);
@@ -342,6 +309,66 @@ int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
     }
     plan->work_bytes = floats * sizeof(float);
     return DIFFATTN_OK;
+}
+
+int plan_decode(const diffattn_kv_desc* d, int causal, DecodePlan* plan) {
+    if (!d) return DIFFATTN_ERR_INVALID;
+    if (d->B < 1 || d->H < 1 || d->Tq < 1 || d->Tk < 1 || d->D < 1) return DIFFATTN_ERR_INVALID;
+    if (d->dtype != DIFFATTN_BF16 && d->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID;
+    if (d->kv_group < 0 || d->H % group_of(d->kv_group) != 0) return DIFFATTN_ERR_INVALID;
+    if (d->Dv < 0 || d->D > 128 || value_width(d->Dv, d->D) > 256) return DIFFATTN_ERR_INVALID;
+    if (!strides_nonneg(d->q1_stride) || !strides_nonneg(d->k1_stride) ||
+        !strides_nonneg(d->q2_stride) || !strides_nonneg(d->k2_stride) ||
+        !strides_nonneg(d->v_stride) || !strides_nonneg(d->o_stride))
+        return DIFFATTN_ERR_INVALID;
+    if (causal && d->Tk < d->Tq) return DIFFATTN_ERR_INVALID;
+    if (d->Tk > INT32_MAX / 2 || d->Tq > INT32_MAX / 2 || d->H > (1 << 24))
+        return DIFFATTN_ERR_UNSUPPORTED;
+    const int cap = (d->D == 32 || d->D == 64 || d->D == 128) ? decode_max_rows((int)d->D) : 0;
+    const bool bf16_vw128 = d->dtype == DIFFATTN_BF16 && value_width(d->Dv, d->D) == 128;
+    const int64_t rows_per_kv = group_of(d->kv_group) * d->Tq;
+    if (bf16_vw128 && d->Tq <= 16 && (d->D == 128 || (d->D == 64 && rows_per_kv > 8))) {
+        // rows of the heads that share a key/value head, 16 per unit at most,
+        // evenly filled
+        const int64_t g = group_of(d->kv_group);
+        const int64_t rows = rows_per_kv;
+        const int64_t row_chunks = (rows + 15) / 16;
+        const int64_t Hk = d->H / g;
+        const int64_t units = d->B * Hk * row_chunks;
+        if (units > (1ll << 24) || d->B * d->H > (1ll << 24) || d->B * d->H * d->Tq > INT32_MAX)
+            return DIFFATTN_ERR_UNSUPPORTED;
+        plan->tc_only = true;
+        plan->tq_bucket = tc_bucket((rows + row_chunks - 1) / row_chunks);
+        plan->splits = 1;                   // the tensor-core pass sets its own
+        plan->split_len = (int)(((d->Tk + 255) / 256) * 256);
+        plan->kv_group = (int)g;
+        plan->Hk = (int)Hk;
+        plan->row_chunks = (int)row_chunks;
+        plan->work_bytes = decode_tc_work_floats(units, d->Tk, plan->tq_bucket) * sizeof(float);
+        if (d->D == 64 && d->Tq <= cap) {
+            DecodePlan fb;
+            const int rc = plan_split_key(d, cap, &fb);
+            if (rc != DIFFATTN_OK) return rc;
+            plan->fb_valid = true;
+            plan->fb_tq_bucket = fb.tq_bucket;
+            plan->fb_splits = fb.splits;
+            plan->fb_split_len = fb.split_len;
+            plan->fb_row_chunks = fb.row_chunks;
+            if (fb.work_bytes > plan->work_bytes) plan->work_bytes = fb.work_bytes;
+        }
+        return DIFFATTN_OK;
+    }
+    if (d->Tq > cap || value_width(d->Dv, d->D) != 2 * d->D) {
+        // queries over the cache on the forward kernels (chunked prefill)
+        const int64_t nq = (d->Tq + 127) / 128;
+        if (d->B * d->H > INT32_MAX / nq) return DIFFATTN_ERR_UNSUPPORTED;
+        plan->forward = true;
+        plan->kv_group = (int)group_of(d->kv_group);
+        plan->Hk = (int)(d->H / plan->kv_group);
+        plan->work_bytes = kForwardPathWorkBytes;
+        return DIFFATTN_OK;
+    }
+    return plan_split_key(d, cap, plan);
 }
 
 bool kv_aligned(const void* p, const int64_t s[3], size_t esize) {
@@ -823,9 +850,9 @@ int decode_args(const diffattn_kv_desc* desc, const void* q1, const void* k1, co
     if (!lambda_dev && !std::isfinite(lambda)) return DIFFATTN_ERR_INVALID;
     rc = check_epilogue(epi, e);
     if (rc != DIFFATTN_OK) return rc;
-    // the forward kernels take any alignment (and so does the V2 decode,
-    // which falls back to them)
-    if (plan->forward || plan->v2) return DIFFATTN_OK;
+    // the forward kernels take any alignment (and so does the tensor-core
+    // decode of up to 16 rows, which falls back to them)
+    if (plan->forward || plan->tc_only) return DIFFATTN_OK;
     const size_t esize = desc->dtype == DIFFATTN_BF16 ? 2 : 4;
     if (!kv_aligned(k1, desc->k1_stride, esize) || !kv_aligned(k2, desc->k2_stride, esize) ||
         !kv_aligned(v, desc->v_stride, esize))
@@ -866,11 +893,12 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
     const int64_t hk = d.H / group_of(d.kv_group);
     const bool k_shared = same_tensor(k1, d.k1_stride, k2, d.k2_stride, d.B, hk, d.Tk);
     const bool dense_kv = d.k1_stride[2] == d.D && d.k2_stride[2] == d.D && d.v_stride[2] == dv;
-    // the V2 decode on the tensor cores needs one key tensor and dense,
-    // aligned rows of the cache and of the queries
-    const bool v2_tc = plan.v2 && k_shared && dense_kv && kv_aligned(k1, d.k1_stride, esize) &&
-                       kv_aligned(v, d.v_stride, esize) && kv_aligned(q1, d.q1_stride, esize) &&
-                       kv_aligned(q2, d.q2_stride, esize);
+    // the tensor-core decode of up to 16 rows needs dense, aligned rows of the
+    // cache and of the queries, and at D = 128 one key tensor for both branches
+    const bool tc_call = plan.tc_only && (d.D == 64 || k_shared) && dense_kv &&
+                         kv_aligned(k1, d.k1_stride, esize) && kv_aligned(k2, d.k2_stride, esize) &&
+                         kv_aligned(v, d.v_stride, esize) && kv_aligned(q1, d.q1_stride, esize) &&
+                         kv_aligned(q2, d.q2_stride, esize);
     auto run_forward = [&]() {
         // Tq query rows at the end of the Tk-key sequence: query i at key
         // position Tk - Tq + i; one forward launch with the static schedule
@@ -880,7 +908,19 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
         return launch_forward(f, q1, k1, q2, k2, v, lambda, lambda_dev, causal, e, out, nullptr,
                               nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
     };
-    if (plan.forward || (plan.v2 && !v2_tc)) return run_forward();
+    if (plan.forward) return run_forward();
+    if (plan.tc_only && !tc_call) {
+        // at D = 64 the split-key layout of up to 8-row units on the CUDA cores
+        // (which needs aligned K1, K2 and V); else the forward kernels
+        if (!plan.fb_valid || !kv_aligned(k1, d.k1_stride, esize) || !kv_aligned(k2, d.k2_stride, esize) ||
+            !kv_aligned(v, d.v_stride, esize))
+            return run_forward();
+        plan.tc_only = false;
+        plan.tq_bucket = plan.fb_tq_bucket;
+        plan.splits = plan.fb_splits;
+        plan.split_len = plan.fb_split_len;
+        plan.row_chunks = plan.fb_row_chunks;
+    }
     DecodeParams p{};
     p.B = (int)d.B;
     p.H = (int)d.H;
@@ -893,9 +933,9 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
     p.Hk = plan.Hk;
     p.row_chunks = plan.row_chunks;
     p.dense_kv = dense_kv ? 1 : 0;
-    p.v2 = plan.v2 ? 1 : 0;
+    p.tc_only = plan.tc_only ? 1 : 0;
     p.k_shared = k_shared ? 1 : 0;
-    p.tc_ok = plan.v2 || (p.dense_kv && d.dtype == DIFFATTN_BF16 && d.D == 64 &&
+    p.tc_ok = plan.tc_only || (p.dense_kv && d.dtype == DIFFATTN_BF16 && d.D == 64 &&
                           kv_aligned(q1, d.q1_stride, esize) && kv_aligned(q2, d.q2_stride, esize))
                   ? 1 : 0;
     p.tq_bucket = plan.tq_bucket;
@@ -933,7 +973,7 @@ int diffattn_decode(const diffattn_kv_desc* desc, const void* q1, const void* k1
             encode_map(&kv_maps[1], k2, d.D, &md, hk, d.k2_stride, 64, 128) == DIFFATTN_OK &&
             encode_map(&kv_maps[2], v, dv, &md, hk, d.v_stride, 64, 128) == DIFFATTN_OK)
             p.tc_maps = kv_maps;
-        else if (plan.v2)
+        else if (plan.tc_only)
             return run_forward();
         else
             p.tc_ok = 0;

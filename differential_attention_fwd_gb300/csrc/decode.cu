@@ -749,21 +749,24 @@ int launch_d(const DecodeParams& p, cudaStream_t stream) {
     return -1;
 }
 
-// The DIFF V2 head (D = 128, value width 128): the tensor-core first pass,
-// then the combine pass of value width 128 (its instance for D = 64).
+// Units of up to 16 rows on the tensor cores only (the DIFF V2 head, D = 128,
+// or D = 64 with more than 8 rows per key/value head; value width 128 either
+// way): the tensor-core first pass, then the combine pass of value width 128
+// (its instance for D = 64).
 template <int TQ>
-int launch_v2_tq(const DecodeParams& p, cudaStream_t stream) {
+int launch_tc_only_tq(const DecodeParams& p, cudaStream_t stream) {
     DecodeParams q = p;
     if (launch_decode_tc_first_pass(&q, stream) != 0) return -1;
     return launch_combine<__nv_bfloat16, 64, TQ>(q, stream);
 }
 
-int launch_v2(const DecodeParams& p, cudaStream_t stream) {
-    if (!p.tc_ok || !p.bf16 || p.D != 128) return -1;
-    if (p.tq_bucket == 1) return launch_v2_tq<1>(p, stream);
-    if (p.tq_bucket == 2) return launch_v2_tq<2>(p, stream);
-    if (p.tq_bucket == 4) return launch_v2_tq<4>(p, stream);
-    if (p.tq_bucket == 8) return launch_v2_tq<8>(p, stream);
+int launch_tc_only(const DecodeParams& p, cudaStream_t stream) {
+    if (!p.tc_ok || !p.bf16 || (p.D != 64 && p.D != 128)) return -1;
+    if (p.tq_bucket == 1) return launch_tc_only_tq<1>(p, stream);
+    if (p.tq_bucket == 2) return launch_tc_only_tq<2>(p, stream);
+    if (p.tq_bucket == 4) return launch_tc_only_tq<4>(p, stream);
+    if (p.tq_bucket == 8) return launch_tc_only_tq<8>(p, stream);
+    if (p.tq_bucket == 16) return launch_tc_only_tq<16>(p, stream);
     return -1;
 }
 
@@ -791,7 +794,7 @@ size_t decode_work_floats(int64_t units, int splits, int tq_bucket, int64_t D) {
 }
 
 int launch_decode(const DecodeParams& p, cudaStream_t stream) {
-    if (p.v2) return dec::launch_v2(p, stream);
+    if (p.tc_only) return dec::launch_tc_only(p, stream);
     return p.bf16 ? dec::launch_t<__nv_bfloat16>(p, stream) : dec::launch_t<float>(p, stream);
 }
 

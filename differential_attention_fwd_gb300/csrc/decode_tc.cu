@@ -1,11 +1,11 @@
 // decode_tc.cu -- the first pass of the decode (a few queries over a long
 // key/value cache) on the tensor cores, for query rows that share a key/value
-// head: bf16, value width 128, dense cache rows, up to 8 rows per unit (the
-// query heads of a grouped key/value head, DIFF V2's layout, or several new
-// queries).  Two head shapes: D = 64 (V = 2D) with 4 or 8 rows per unit, and
-// the DIFF V2 head D = 128 (V = D; aiengineeringfromscratch lesson, "V1 contre
-// V2") with 1 to 8, whose two branches usually share one key tensor (then one
-// key tile per stage serves both score products).  It writes split partials
+// head: bf16, value width 128, dense cache rows, up to 16 rows per unit (the
+// MMA's N: the query heads of a grouped key/value head, DIFF V2's layout, or
+// several new queries).  Two head shapes: D = 64 (V = 2D) with 4, 8 or 16 rows
+// per unit, and the DIFF V2 head D = 128 (V = D; aiengineeringfromscratch
+// lesson, "V1 contre V2") with 1 to 16, whose two branches usually share one key
+// tensor (then one key tile per stage serves both score products).  It writes split partials
 // in the layout of the CUDA-core first pass in decode.cu for a value width of
 // 128, which the combine pass there merges.
 //
@@ -496,6 +496,7 @@ template <int HD, bool KS>
 int launch_first_pass_hd(const DecodeParams& p, cudaStream_t stream) {
     if (p.tq_bucket == 4) return launch_first_pass_tq<4, HD, KS>(p, p.tc_maps, stream);
     if (p.tq_bucket == 8) return launch_first_pass_tq<8, HD, KS>(p, p.tc_maps, stream);
+    if (p.tq_bucket == 16) return launch_first_pass_tq<16, HD, KS>(p, p.tc_maps, stream);
     if constexpr (HD == 128) {
         if (p.tq_bucket == 1) return launch_first_pass_tq<1, HD, KS>(p, p.tc_maps, stream);
         if (p.tq_bucket == 2) return launch_first_pass_tq<2, HD, KS>(p, p.tc_maps, stream);

@@ -91,15 +91,16 @@ struct DecodeParams {
     int tc_ok;              // the tensor-core first pass may run: bf16, D = 64 (V = 2D) or
                             // D = 128 with V = D and one key tensor, dense K/V rows,
                             // Q rows 16-byte aligned
-    int v2;                 // value width D = 128 (the DIFF V2 head): the tensor-core
-                            // first pass and the combine pass of value width 128 only
+    int tc_only;            // units of up to 16 rows (the DIFF V2 head, or bf16 D = 64 with
+                            // more than 8 rows per key/value head): the tensor-core first
+                            // pass and the combine pass of value width 128 only
     int k_shared;           // K1 and K2 are one tensor
     uint32_t* status;       // device status word (bounded waits of the tensor-core pass)
     const CUtensorMap* tc_maps;   // host memory: K1, K2 and V tensor maps (128-row boxes) for
                                   // the tensor-core pass's launch; never read on the device
     int causal;
     int bf16;               // element type: 1 bf16, 0 fp32
-    int tq_bucket;          // query rows per CTA: 1, 2, 4 or 8
+    int tq_bucket;          // query rows per CTA: 1, 2, 4, 8 (or 16 on the tensor-core pass)
     int splits;             // key-range splits per unit (b, key/value head, row chunk)
     int total_items;        // units * splits
     int split_len;          // keys per split (multiple of 256)
@@ -180,8 +181,8 @@ size_t decode_work_floats(int64_t units, int splits, int tq_bucket, int64_t D);
 
 // Each returns 0 on success, -1 if the launch failed.
 int launch_decode(const DecodeParams& p, cudaStream_t stream);
-// The tensor-core first pass of the decode (decode_tc.cu): D = 64 with 4 or 8
-// query rows per unit, D = 128 (value width 128, one key tensor) with 1 to 8.  It sets p's tc_* fields and p->splits (partial slots per
+// The tensor-core first pass of the decode (decode_tc.cu): D = 64 with 4, 8 or
+// 16 query rows per unit, D = 128 (value width 128, one key tensor) with 1 to 16.  It sets p's tc_* fields and p->splits (partial slots per
 // unit) for its launch; the caller launches the combine pass with that p.
 int launch_decode_tc_first_pass(DecodeParams* p, cudaStream_t stream);
 // Workspace floats the tensor-core pass may need (its slots per unit on any

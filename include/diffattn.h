@@ -394,13 +394,17 @@ size_t diffattn_decode_workspace_bytes(const diffattn_kv_desc *desc);
  * rows (4 for D = 128) of the query heads that share a key/value head, so with
  * kv_group = g the cache of a key/value head is read ceil(g * Tq / 8) times
  * (ceil(g * Tq / 4) for D = 128), not g * ceil(Tq / 8) times.
- * The DIFF V2 head (bf16, D = Dv = 128, Tq <= 8; aiengineeringfromscratch
- * lesson, "V1 contre V2"): the workspace is sized for the split-key decode on
- * the tensor cores (8 query rows per CTA, the cache of a key/value head read
- * ceil(g * Tq / 8) times), which runs when K1 and K2 are one tensor (same
- * pointer and strides) and Q1, Q2, K and V have 16-byte aligned bases and
- * strides with rows dense along the sequence; with two key tensors or
- * another layout the call runs on the forward kernels instead.
+ * Units of up to 16 query rows on the tensor cores: bf16 with value width
+ * 128 and either D = 64 with more than 8 query rows per key/value head
+ * (g * Tq > 8, Tq <= 16), or the DIFF V2 head D = Dv = 128 with Tq <= 16
+ * (aiengineeringfromscratch lesson, "V1 contre V2").  The workspace is sized
+ * for the split-key decode on the tensor cores (the cache of a key/value head
+ * read ceil(g * Tq / 16) times), which runs when Q1, Q2, K1, K2 and V have
+ * 16-byte aligned bases and strides with the cache rows dense along the
+ * sequence, and at D = 128 K1 and K2 are one tensor (same pointer and
+ * strides).  Otherwise the call runs, at D = 64 with Tq <= 8, the split-key
+ * layout of up to 8-row units on the CUDA cores (the workspace has room for
+ * it; it needs aligned K1, K2 and V), else the forward kernels.
  * Any other request (more query rows, another D or Dv) runs as one launch of
  * the forward kernels with the queries placed at the end of the key sequence:
  * on the tensor cores when diffattn_fwd would choose them for this shape and

@@ -215,15 +215,17 @@ def test_decode_workspace_query(lib):
     # shapes the split-key decode does not take run on the forward kernels,
     # which use no workspace (a nominal 16 bytes)
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=48))) == 16
-    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=9))) == 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=17))) == 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=9, dtype=_lib.DIFFATTN_F32))) == 16
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=1024, Tk=8192))) == 16
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=64, Dv=128))) == n
-    # the DIFF V2 head (bf16, D = Dv = 128) up to 8 queries: the tensor-core
+    # the DIFF V2 head (bf16, D = Dv = 128) up to 16 queries: the tensor-core
     # split-key decode's partial results; more queries or fp32: the forward
     v2 = lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=128)))
     assert v2 > 16 and v2 % 4 == 0
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=128, Tq=8))) > 16
-    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=128, Tq=9))) == 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=128, Tq=16))) > 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=128, Tq=17))) == 16
     assert lib.diffattn_decode_workspace_bytes(
         ctypes.byref(kv_desc(D=128, Dv=128, dtype=_lib.DIFFATTN_F32))) == 16
     assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(D=128, Dv=64))) == 16
@@ -394,3 +396,19 @@ def test_decode_workspace_holds_every_tensor_core_segment(lib, B, H, kv_group, T
     for sms in (1, 7, 148, 152, 160, 1024):
         grid = min(units * tpu, sms)
         assert need >= units * _max_segments(units, tpu, grid) * tqb * (4 + 4 * 64) * 4, sms
+
+
+def test_decode_workspace_sixteen_row_units(lib):
+    # bf16 D = 64 with 9 to 16 query rows per key/value head (here 4 query
+    # heads per key/value head and 4 new queries): units of 16 rows on the
+    # tensor cores, with room for the split-key layout of 8-row units that a
+    # call runs on the CUDA cores when its cache rows are not dense
+    d16 = kv_desc(B=16, H=32, kv_group=4, Tq=4, Tk=8192)
+    n16 = lib.diffattn_decode_workspace_bytes(ctypes.byref(d16))
+    assert n16 > 16 and n16 % 4 == 0
+    d8 = kv_desc(B=16, H=32, kv_group=4, Tq=2, Tk=8192)      # 8 rows: one 8-row unit
+    assert n16 > lib.diffattn_decode_workspace_bytes(ctypes.byref(d8))
+    # Tq up to 16 with one query head per key/value head: the tensor cores
+    # alone (no split-key layout of 8-row units exists beyond 8 queries)
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=16))) > 16
+    assert lib.diffattn_decode_workspace_bytes(ctypes.byref(kv_desc(Tq=12, H=4, kv_group=2))) > 16

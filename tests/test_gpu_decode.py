@@ -93,9 +93,10 @@ def test_decode_invalid_and_forward_routed_shapes():
     v = torch.zeros(1, 1, 5, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(da.DiffattnError):
         da.differential_attention_decode(x, k, x, k, v, 0.5, causal=True)
-    # Tq > 8 and D outside {32, 64, 128} run on the forward kernels: with V = 1
-    # every output is 1 - lambda
-    for Tq, D in ((9, 64), (2, 48)):
+    # Tq > 16 and D outside {32, 64, 128} run on the forward kernels, Tq = 9 on
+    # the tensor-core decode in a unit of 16 rows: with V = 1 every output is
+    # 1 - lambda
+    for Tq, D in ((17, 64), (2, 48), (9, 64)):
         x = torch.zeros(1, 1, Tq, D, dtype=torch.bfloat16, device="cuda")
         k = torch.zeros(1, 1, 100, D, dtype=torch.bfloat16, device="cuda")
         v = torch.ones(1, 1, 100, 2 * D, dtype=torch.bfloat16, device="cuda")
@@ -145,4 +146,59 @@ def test_decode_tensor_core_epilogue(H, Hk, Tq, Tk, norm):
     for call in range(2):
         out, _ = run(inp, "bf16", lam_t, True, **kw)
         assert_close(to_numpy(out), ref, "bf16", f"decode epilogue H={H} Hk={Hk} Tq={Tq} Tk={Tk} call {call}")
+    assert da.get_device_error() == 0
+
+
+def padded_rows(t):
+    """The same cache with every row stored in a wider buffer (row stride
+    D + 8 elements): not dense along the sequence, still 16-byte aligned."""
+    B, H, T, W_ = t.shape
+    wide = torch.zeros(B, H, T, W_ + 8, dtype=t.dtype, device=t.device)
+    wide[..., :W_] = t
+    return wide[..., :W_]
+
+
+@pytest.mark.parametrize("H,Hk,Tq,Tk,causal", [
+    (4, 1, 4, 3000, True),     # 16 rows per key/value head: 4 heads x 4 new queries
+    (2, 1, 5, 1000, True),     # 10 rows
+    (8, 1, 3, 777, False),     # 24 rows: two units of 12
+    (2, 2, 12, 2000, True),    # Tq = 12, one query head per key/value head
+    (1, 1, 16, 129, True),     # Tq = 16
+    (16, 1, 1, 4096, True),    # 16 query heads per key/value head
+    (32, 2, 2, 500, False),    # 32 rows per key/value head: two units of 16
+])
+def test_decode_sixteen_row_units(H, Hk, Tq, Tk, causal):
+    """9 to 16 query rows per unit (bf16, D = 64): the tensor-core pass in units
+    of 16 rows over a dense cache; over a cache with padded rows the split-key
+    layout of 8-row units on the CUDA cores (Tq <= 8) or the forward kernels
+    (Tq > 8).  All against the oracle."""
+    w = W.DecodeWorkload("t16", 2, H, Tq, Tk, 64, "bf16", causal, seed=H * 7 + Tq * 3 + Tk, kv_heads=Hk)
+    inp = W.draw_kv(w)
+    q1, q2 = to_device(inp.q1, "bf16"), to_device(inp.q2, "bf16")
+    dense = [to_device(x, "bf16") for x in (inp.k1, inp.k2, inp.v)]
+    padded = [padded_rows(t) for t in dense]
+    assert padded[0].stride(2) == 72
+    ref = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.6, causal)
+    for kv, tag in ((dense, "dense"), (padded, "padded rows")):
+        out = da.differential_attention_decode(q1, kv[0], q2, kv[1], kv[2], 0.6, causal=causal)
+        torch.cuda.synchronize()
+        assert da.get_device_error() == 0
+        assert_close(to_numpy(out), ref, "bf16", f"decode 16-row units {tag} H={H} Hk={Hk} Tq={Tq} Tk={Tk}")
+
+
+@pytest.mark.parametrize("norm", ["rms", "group"])
+def test_decode_sixteen_row_units_epilogue(norm):
+    # 16 rows per unit with the norm epilogue and a device lambda, called twice
+    w = W.DecodeWorkload("t16e", 2, 8, 4, 2500, 64, "bf16", True, seed=77, kv_heads=2)
+    inp = W.draw_kv(w)
+    rng = np.random.default_rng(9)
+    wt = (1 + 0.1 * rng.standard_normal((8, 128))).astype(np.float32)
+    bs = (0.05 * rng.standard_normal((8, 128))).astype(np.float32)
+    lam_t = torch.tensor(0.45, device="cuda")
+    o = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.45, True)
+    ref = oracle.head_norm(o, norm, 1e-5, wt, bs, 0.5)
+    for call in range(2):
+        out, _ = run(inp, "bf16", lam_t, True, norm=norm, norm_weight=torch.from_numpy(wt).cuda(),
+                     norm_bias=torch.from_numpy(bs).cuda(), out_scale=0.5)
+        assert_close(to_numpy(out), ref, "bf16", f"decode 16-row units {norm} call {call}")
     assert da.get_device_error() == 0

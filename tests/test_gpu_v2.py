@@ -235,11 +235,13 @@ def split_key_workspace(B, H, Hk, Tq, Tk):
     return _lib.load().diffattn_decode_workspace_bytes(ctypes.byref(d))
 
 
-# rows per key/value head (H / Hk * Tq): 1, 2, 4, 6 (padded to 8), 8, 16 (two
-# units of 8); caches of one key, a ragged tail, one tile, many tiles
+# rows per key/value head (H / Hk * Tq): 1, 2, 4, 6 (padded to 8), 8, 16 (one
+# unit), 48 (three units of 16); caches of one key, a ragged tail, one tile,
+# many tiles
 @pytest.mark.parametrize("B,H,Hk,Tq,Tk", [(2, 4, 4, 1, 1), (2, 16, 8, 1, 8192), (1, 8, 2, 1, 300),
                                           (2, 8, 1, 1, 1000), (1, 4, 2, 3, 1000), (1, 4, 1, 4, 2000),
-                                          (2, 2, 2, 8, 129), (1, 32, 8, 2, 5000), (1, 2, 2, 5, 128)])
+                                          (2, 2, 2, 8, 129), (1, 32, 8, 2, 5000), (1, 2, 2, 5, 128),
+                                          (2, 4, 2, 8, 1500), (1, 4, 1, 12, 640), (1, 2, 2, 16, 300)])
 @pytest.mark.parametrize("causal", [True, False])
 def test_v2_decode_split_key_tensor_core(B, H, Hk, Tq, Tk, causal):
     assert split_key_workspace(B, H, Hk, Tq, Tk) > 16
@@ -281,7 +283,7 @@ def test_v2_decode_value_rows_through_ones_and_cancellation():
 def test_v2_decode_shapes_on_the_forward_kernels():
     """The V2 decode shapes the split-key pass does not take (two key
     tensors, a cache with rows not contiguous along the sequence, fp32, more
-    than 8 queries) run on the forward kernels; all match the oracle."""
+    than 16 queries) run on the forward kernels; all match the oracle."""
     inp = decode_inputs(1, 8, 2, 1, 1500, seed=440, shared=False)
     assert_close(to_numpy(decode_run(inp, 0.5, True)), decode_ref(inp, 0.5, True), "bf16",
                  "V2 decode two key tensors")
@@ -298,10 +300,10 @@ def test_v2_decode_shapes_on_the_forward_kernels():
     inp = decode_inputs(1, 4, 2, 2, 600, seed=442, dtype="f32")
     assert_close(to_numpy(decode_run(inp, 0.5, True, dtype="f32")), decode_ref(inp, 0.5, True),
                  "f32", "V2 decode fp32")
-    assert split_key_workspace(1, 4, 2, 9, 600) == 16
-    inp = decode_inputs(1, 4, 2, 9, 600, seed=443)
+    assert split_key_workspace(1, 4, 2, 17, 600) == 16
+    inp = decode_inputs(1, 4, 2, 17, 600, seed=443)
     assert_close(to_numpy(decode_run(inp, 0.5, True)), decode_ref(inp, 0.5, True), "bf16",
-                 "V2 decode Tq=9")
+                 "V2 decode Tq=17")
 
 
 def test_v2_decode_matches_oracle_last_rows_at_full_size():

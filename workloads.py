@@ -277,6 +277,10 @@ DECODE_WORKLOADS = {
     # (the 32-query / 8-key-value-head grouping of the GQA exercise)
     "decode_b16h32kv8q1k8192": DecodeWorkload("decode_b16h32kv8q1k8192", 16, 32, 1, 8192, 64,
                                               "bf16", True, 22, kv_heads=8),
+    # the same grouping with four speculative tokens: 16 query rows per
+    # key/value head
+    "decode_b16h32kv8q4k8192": DecodeWorkload("decode_b16h32kv8q4k8192", 16, 32, 4, 8192, 64,
+                                              "bf16", True, 26, kv_heads=8),
     # the DIFF V2 head: 16 differential heads over 8 key/value heads, D = Dv =
     # 128, one key tensor for both branches
     "decode_b16h16kv8q1k8192_d128_shared_k": DecodeWorkload(
