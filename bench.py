@@ -929,6 +929,35 @@ BWD_WAIT_KINDS = ("total_cycles", "kv_slot_free", "query_stage_free", "kv_load",
 BWD_WAIT_SHARES = 16   # kinds 1..15 are shares of the role's cycles; the last two are counts
 
 
+DQ_WAIT_ROLES = ("producer", "mma_issuer", "elementwise_warps")
+DQ_WAIT_KINDS = ("total_cycles", "q_slot_free", "k_slot_free", "v_slot_free", "q_load", "k_load",
+                 "v_load", "ds_ready", "dq_read_out", "scores_ready", "tmem_read", "math", "ds_store",
+                 "dq_ready", "epilogue", "tile_count", "item_count")
+DQ_WAIT_SHARES = 15   # kinds 1..14 are shares of the role's cycles; the last two are counts
+
+
+def dq_wait_profile_summary(raw):
+    """The dQ kernel's wait profile ([role][kind] counters of the wait-profile
+    build), as bwd_wait_profile_summary for the dK/dV kernel."""
+    n = len(DQ_WAIT_KINDS)
+    out = {}
+    for r, role in enumerate(DQ_WAIT_ROLES):
+        tot = raw[n * r]
+        out[role] = {"cycles": tot}
+        for i, k in enumerate(DQ_WAIT_KINDS[1:DQ_WAIT_SHARES], start=1):
+            if raw[n * r + i]:
+                out[role][k] = raw[n * r + i] / tot if tot else None
+    ew = n * DQ_WAIT_ROLES.index("elementwise_warps")
+    tiles, items = raw[ew + 15], raw[ew + 16]
+    if tiles:
+        out["elementwise_warps"]["per_tile_cycles"] = {
+            k: raw[ew + i] / tiles for i, k in enumerate(DQ_WAIT_KINDS) if 9 <= i <= 12}
+        out["elementwise_warps"]["per_tile_cycles"]["all"] = raw[ew] / tiles
+    if items:
+        out["elementwise_warps"]["per_item_epilogue_cycles"] = raw[ew + 14] / items
+    return {"kernel": "dq::diffattn_bwd_dq_kernel", "roles": out}
+
+
 def bwd_wait_profile_summary(raw):
     """The dK/dV kernel's wait profile ([role][kind] counters of the
     wait-profile build): each role's cycles by what it waits for or works on,
@@ -1015,13 +1044,16 @@ def main(argv=None):
         lib = _lib.load(build_mod.build(variant="waitprof"))
         lib.diffattn_bwd_wait_profile.argtypes = [C.POINTER(C.c_ulonglong), C.c_int]
         lib.diffattn_bwd_wait_profile.restype = C.c_int
-        clear = (C.c_ulonglong * (3 * len(BWD_WAIT_KINDS)))()
+        nk = 3 * len(BWD_WAIT_KINDS)
+        nq = 3 * len(DQ_WAIT_KINDS)
+        clear = (C.c_ulonglong * (nk + nq))()
         lib.diffattn_bwd_wait_profile(clear, len(clear))
         res = run_backward(args, w, world, rank, local)
-        raw = (C.c_ulonglong * (3 * len(BWD_WAIT_KINDS)))()
+        raw = (C.c_ulonglong * (nk + nq))()
         if lib.diffattn_bwd_wait_profile(raw, len(raw)) != 0:
             raise RuntimeError("diffattn_bwd_wait_profile failed")
-        res = {"wait_profile": bwd_wait_profile_summary(list(raw)), "workload": w.name,
+        res = {"wait_profile": bwd_wait_profile_summary(list(raw)[:nk]),
+               "wait_profile_dq": dq_wait_profile_summary(list(raw)[nk:]), "workload": w.name,
                "steps": args.steps, "warmup": args.warmup,
                "instrumented_backward_ms": res.get("ms_per_step")}
     elif args.mode == "backward":

@@ -58,6 +58,49 @@ constexpr uint32_t REGS_WORK = 200;
 constexpr uint32_t REGS_OTHER = 104;
 static_assert(256 * REGS_WORK + 128 * REGS_OTHER <= NUM_THREADS * 168, "register split");
 
+// Wait profiles (only in the separate build compiled with
+// -DDIFFATTN_WAIT_PROFILE; the regular build has none of it): a role's
+// issuing thread (lane 0 of each elementwise warp) counts SM cycles by what it
+// waits for or works on, in N kinds, and adds them to a [3 roles][N] array of
+// its kernel when the CTA ends.
+#ifdef DIFFATTN_WAIT_PROFILE
+template <int N>
+struct ProfT {
+    unsigned long long c[N] = {};
+    long long t0 = 0;
+    __device__ __forceinline__ void start() { t0 = clock64(); }
+    template <class F>
+    __device__ __forceinline__ bool timed(int kind, F&& f) {
+        const long long a = clock64();
+        const bool r = f();
+        c[kind] += (unsigned long long)(clock64() - a);
+        return r;
+    }
+    __device__ __forceinline__ void flush(unsigned long long (*g)[N], int role, bool reporter) {
+        c[0] = (unsigned long long)(clock64() - t0);
+        if (reporter)
+            for (int i = 0; i < N; ++i) atomicAdd(&g[role][i], c[i]);
+    }
+};
+#define BP_WAIT(pf, kind, expr) (pf).timed((kind), [&]() -> bool { return (expr); })
+#define BP_MARK(var) long long var = clock64()
+#define BP_ADD(pf, kind, since) ((pf).c[kind] += (unsigned long long)(clock64() - (since)))
+#define BP_RESET(var) (var = clock64())
+#define BP_COUNT(pf, kind) ((pf).c[kind] += 1)
+#define BP_FLUSH(pf, g, role, rep) (pf).flush((g), (role), (rep))
+#else
+template <int N>
+struct ProfT {
+    __device__ __forceinline__ void start() {}
+};
+#define BP_WAIT(pf, kind, expr) (expr)
+#define BP_MARK(var) ((void)0)
+#define BP_ADD(pf, kind, since) ((void)0)
+#define BP_RESET(var) ((void)0)
+#define BP_COUNT(pf, kind) ((void)0)
+#define BP_FLUSH(pf, g, role, rep) ((void)0)
+#endif
+
 // The CTA's k-th work item in a boustrophedon order over the item list.
 __device__ __forceinline__ int item_index(int k, int cta, int grid) {
     const int base = k * grid;
@@ -107,6 +150,25 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_DQ = 384;
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);     // Q x K^T, dO x V^T
 constexpr uint32_t IDESC_DQ = idesc_bf16_f32(BM, HD, 0, 1);    // dS (TMEM) x K (MN-major)
+
+// Wait profile of this kernel (g_prof[role][kind], see ProfT).  Roles: 0 the
+// TMA producer, 1 the MMA-issuing thread, 2 the eight elementwise warps.
+// Kinds: 0 the role's cycles from start to end; the producer's waits for the
+// Q/dO slot (1), a K stage (2) and a V stage (3) to be released; the MMA
+// thread's waits for Q/dO (4), K (5), V (6), the dS operands (7) and the dQ
+// accumulators to be read out (8); the elementwise warps' waits for the scores
+// (9), their TMEM read of S_b and dP (10), arithmetic (11), the dS store into
+// TMEM with its fences (12), the wait for the dQ accumulators (13) and the
+// epilogue (14); tile (15) and item (16) counts.
+enum : int {
+    kQTotal = 0, kQQEmpty = 1, kQKEmpty = 2, kQVEmpty = 3, kQQFull = 4, kQKFull = 5, kQVFull = 6,
+    kQDsFull = 7, kQDqEmpty = 8, kQSFull = 9, kQRead = 10, kQMath = 11, kQStore = 12,
+    kQDqFull = 13, kQEpilogue = 14, kQTiles = 15, kQItems = 16, kQKinds = 17
+};
+#ifdef DIFFATTN_WAIT_PROFILE
+__device__ unsigned long long g_prof[3][kQKinds];
+#endif
+using Prof = ProfT<kQKinds>;
 
 struct Item {
     int b, h, qt, n_kv;
@@ -181,6 +243,8 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
         if (warp == 8) {
             // ------------------------------------------------------ producer
             if (elect_one()) {
+                Prof pf;
+                pf.start();
                 uint32_t kst = 0, kph = 0, vst = 0, vph = 0, qph = 0;
                 uint32_t armed_q = 0, armed_k[KSTAGES] = {}, armed_v[VSTAGES] = {};
                 bool ok = true;
@@ -190,7 +254,7 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     const Item it = decode_item(idx, p);
                     const int hk = it.h / p.kv_group;
                     if (k > 0) {
-                        if (!(ok = mbar_wait(&bars[BAR_Q_EMPTY], qph, ab))) break;
+                        if (!(ok = BP_WAIT(pf, kQQEmpty, mbar_wait(&bars[BAR_Q_EMPTY], qph, ab)))) break;
                         qph ^= 1;
                     }
                     mbar_arrive_expect_tx(&bars[BAR_Q_FULL], 2 * Q_BYTES + 2 * DO_HALF);
@@ -201,14 +265,14 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                                 it.h, it.b);
                     ++armed_q;
                     for (int j = 0; j < it.n_kv; ++j) {
-                        if (!(ok = mbar_wait(&bars[BAR_K_EMPTY + kst], kph ^ 1, ab))) break;
+                        if (!(ok = BP_WAIT(pf, kQKEmpty, mbar_wait(&bars[BAR_K_EMPTY + kst], kph ^ 1, ab)))) break;
                         uint8_t* kd = smem + OFF_K + kst * 2 * K_BYTES;
                         mbar_arrive_expect_tx(&bars[BAR_K_FULL + kst], 2 * K_BYTES);
                         tma_load_4d(kd, &tm_k1, &bars[BAR_K_FULL + kst], 0, j * BN, hk, it.b);
                         tma_load_4d(kd + K_BYTES, &tm_k2, &bars[BAR_K_FULL + kst], 0, j * BN, hk, it.b);
                         ++armed_k[kst];
                         if (++kst == KSTAGES) { kst = 0; kph ^= 1; }
-                        if (!(ok = mbar_wait(&bars[BAR_V_EMPTY + vst], vph ^ 1, ab))) break;
+                        if (!(ok = BP_WAIT(pf, kQVEmpty, mbar_wait(&bars[BAR_V_EMPTY + vst], vph ^ 1, ab)))) break;
                         uint8_t* vd = smem + OFF_V + vst * V_BYTES;
                         mbar_arrive_expect_tx(&bars[BAR_V_FULL + vst], V_BYTES);
                         tma_load_4d(vd, &tm_v, &bars[BAR_V_FULL + vst], 0, j * BN, hk, it.b);
@@ -223,11 +287,14 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     if (armed_k[s]) mbar_wait_teardown(&bars[BAR_K_FULL + s], (armed_k[s] - 1) & 1, lim);
                 for (int s = 0; s < VSTAGES; ++s)
                     if (armed_v[s]) mbar_wait_teardown(&bars[BAR_V_FULL + s], (armed_v[s] - 1) & 1, lim);
+                BP_FLUSH(pf, g_prof, 0, true);
             }
             __syncwarp();
         } else if (warp == 9) {
             // ------------------------------------------------------ MMA issue
             if (elect_one()) {
+                Prof pf;
+                pf.start();
                 const uint64_t q1d = sdesc_sw128(smem_u32(smem + OFF_Q1), 16, 1024);
                 const uint64_t q2d = sdesc_sw128(smem_u32(smem + OFF_Q2), 16, 1024);
                 const uint64_t dod = sdesc_sw128(smem_u32(smem + OFF_DO), 16, 1024);
@@ -240,8 +307,9 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 // S_1, S_2, dP of key tile t into buffer buf
                 auto issue_s = [&](uint32_t kt, int buf) -> bool {
                     const uint32_t ks = kt % KSTAGES;
-                    if (!mbar_wait(&bars[BAR_K_FULL + ks], (kt / KSTAGES) & 1u, ab)) return false;
-                    if (!mbar_wait(&bars[BAR_V_FULL + vst], vph, ab)) return false;
+                    if (!BP_WAIT(pf, kQKFull, mbar_wait(&bars[BAR_K_FULL + ks], (kt / KSTAGES) & 1u, ab)))
+                        return false;
+                    if (!BP_WAIT(pf, kQVFull, mbar_wait(&bars[BAR_V_FULL + vst], vph, ab))) return false;
                     tc_fence_after();
                     const uint32_t d = tmem_base + buf * 192;
                     const uint64_t k1 = kkd + ((ks * 2 * K_BYTES) >> 4);
@@ -269,17 +337,18 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     if (idx >= total) break;
                     const Item it = decode_item(idx, p);
                     const int n = it.n_kv;
-                    if (!(ok = mbar_wait(&bars[BAR_Q_FULL], qph, ab))) break;
+                    if (!(ok = BP_WAIT(pf, kQQFull, mbar_wait(&bars[BAR_Q_FULL], qph, ab)))) break;
                     qph ^= 1;
                     for (int t = 0; t < 2 && t < n && ok; ++t) ok = issue_s(kc + t, t);
                     if (!ok) break;
                     if (n <= 2) mma_commit(&bars[BAR_Q_EMPTY]);
                     for (int j = 0; j < n; ++j) {
                         const int buf = j & 1;
-                        if (!(ok = mbar_wait(&bars[BAR_DS_FULL + buf], (dsph >> buf) & 1u, ab))) break;
+                        if (!(ok = BP_WAIT(pf, kQDsFull, mbar_wait(&bars[BAR_DS_FULL + buf], (dsph >> buf) & 1u, ab))))
+                            break;
                         dsph ^= 1u << buf;
                         if (j == 0 && !first) {
-                            if (!(ok = mbar_wait(&bars[BAR_DQ_EMPTY], dqph, ab))) break;
+                            if (!(ok = BP_WAIT(pf, kQDqEmpty, mbar_wait(&bars[BAR_DQ_EMPTY], dqph, ab)))) break;
                             dqph ^= 1;
                         }
                         tc_fence_after();
@@ -307,12 +376,15 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 }
                 mma_commit(&bars[BAR_FINAL]);
                 mbar_wait_teardown(&bars[BAR_FINAL], 0, 200ull * 1000ull * 1000ull);
+                BP_FLUSH(pf, g_prof, 1, true);
             }
             __syncwarp();
         }
     } else {
         regs_inc<REGS_WORK>();
         // ------------------------------------------- dS and the dQ epilogue
+        Prof pf;
+        pf.start();
         const int br = warp >> 2;
         const uint32_t quad = warp & 3;
         const int row = quad * 32 + lane;
@@ -343,7 +415,9 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 const int buf = j & 1;
                 const uint32_t tS = lane_base + buf * 192 + br * 64;
                 const uint32_t tP = lane_base + buf * 192 + 128;
-                if (!(ok = mbar_wait_warp(&bars[BAR_S_FULL + buf], (sph >> buf) & 1u, ab))) break;
+                if (!(ok = BP_WAIT(pf, kQSFull, mbar_wait_warp(&bars[BAR_S_FULL + buf], (sph >> buf) & 1u, ab))))
+                    break;
+                BP_MARK(tp);
                 sph ^= 1u << buf;
                 tc_fence_after();
                 uint32_t s[64], dp[64];
@@ -352,6 +426,8 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 tmem_ld32(tP, &dp[0]);
                 tmem_ld32(tP + 32, &dp[32]);
                 tmem_wait_ld();
+                BP_ADD(pf, kQRead, tp);
+                BP_RESET(tp);
                 const int kv0 = j * BN;
                 // only tiles that cross the diagonal or the end of the sequence
                 // need a mask (the decision is the same for the whole CTA)
@@ -389,15 +465,21 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         pk[c] = pack_bf16x2(f2_lo(z), f2_hi(z));
                     }
                 }
+                BP_ADD(pf, kQMath, tp);
+                BP_RESET(tp);
                 tmem_st32(tS, pk);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[BAR_DS_FULL + buf]);
+                BP_ADD(pf, kQStore, tp);
+                BP_COUNT(pf, kQTiles);
             }
             if (!ok) break;
+            BP_COUNT(pf, kQItems);
             // dQ_b = scale * (dS_b K_b): this warpgroup's 64 columns
-            if (!(ok = mbar_wait_warp(&bars[BAR_DQ_FULL], dqph, ab))) break;
+            if (!(ok = BP_WAIT(pf, kQDqFull, mbar_wait_warp(&bars[BAR_DQ_FULL], dqph, ab)))) break;
+            BP_MARK(te);
             dqph ^= 1;
             tc_fence_after();
             uint32_t g[64];
@@ -420,7 +502,9 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         pack_bf16x2(__uint_as_float(g[c + 6]) * p.scale, __uint_as_float(g[c + 7]) * p.scale));
                 }
             }
+            BP_ADD(pf, kQEpilogue, te);
         }
+        BP_FLUSH(pf, g_prof, 2, lane == 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -435,11 +519,7 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
 // ===========================================================================
 namespace dkdv {
 
-// Wait profile of this kernel (only in the separate build compiled with
-// -DDIFFATTN_WAIT_PROFILE; the regular build has none of it): each role's
-// issuing thread (lane 0 of each elementwise warp) counts SM cycles by what it
-// waits for or works on and adds them to g_prof[role][kind] when the CTA ends.
-// Roles: 0 the TMA producer, 1 the MMA-issuing thread, 2 the eight
+// Wait profile of this kernel (g_prof[role][kind], see ProfT).  Roles: 0 the TMA producer, 1 the MMA-issuing thread, 2 the eight
 // elementwise warps.  Kinds: 0 the role's cycles from start to end; the
 // producer's waits for the K/V slot (1) and for a query stage (2) to be
 // released; the MMA thread's waits for K/V (3), for the scores to be read out
@@ -458,39 +538,8 @@ enum : int {
 };
 #ifdef DIFFATTN_WAIT_PROFILE
 __device__ unsigned long long g_prof[3][kPKinds];
-struct Prof {
-    unsigned long long c[kPKinds] = {};
-    long long t0 = 0;
-    __device__ __forceinline__ void start() { t0 = clock64(); }
-    template <class F>
-    __device__ __forceinline__ bool timed(int kind, F&& f) {
-        const long long a = clock64();
-        const bool r = f();
-        c[kind] += (unsigned long long)(clock64() - a);
-        return r;
-    }
-    __device__ __forceinline__ void flush(int role, bool reporter) {
-        c[kPTotal] = (unsigned long long)(clock64() - t0);
-        if (reporter)
-            for (int i = 0; i < kPKinds; ++i) atomicAdd(&g_prof[role][i], c[i]);
-    }
-};
-#define BP_WAIT(pf, kind, expr) (pf).timed((kind), [&]() -> bool { return (expr); })
-#define BP_MARK(var) long long var = clock64()
-#define BP_ADD(pf, kind, since) ((pf).c[kind] += (unsigned long long)(clock64() - (since)))
-#define BP_RESET(var) (var = clock64())
-#define BP_COUNT(pf, kind) ((pf).c[kind] += 1)
-#else
-struct Prof {
-    __device__ __forceinline__ void start() {}
-    __device__ __forceinline__ void flush(int, bool) {}
-};
-#define BP_WAIT(pf, kind, expr) (expr)
-#define BP_MARK(var) ((void)0)
-#define BP_ADD(pf, kind, since) ((void)0)
-#define BP_RESET(var) ((void)0)
-#define BP_COUNT(pf, kind) ((void)0)
 #endif
+using Prof = ProfT<kPKinds>;
 
 constexpr int BM = 128;            // key rows per item (TMEM lanes)
 constexpr int BN = 64;             // query rows per tile
@@ -653,7 +702,7 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 if (armed_kv) mbar_wait_teardown(&bars[BAR_KV_FULL], (armed_kv - 1) & 1, lim);
                 for (int s = 0; s < QSTAGES; ++s)
                     if (armed_q[s]) mbar_wait_teardown(&bars[BAR_Q_FULL + s], (armed_q[s] - 1) & 1, lim);
-                pf.flush(0, true);
+                BP_FLUSH(pf, g_prof, 0, true);
             }
             __syncwarp();
         } else if (warp == 9) {
@@ -744,7 +793,7 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 }
                 mma_commit(&bars[BAR_FINAL]);
                 mbar_wait_teardown(&bars[BAR_FINAL], 0, 200ull * 1000ull * 1000ull);
-                pf.flush(1, true);
+                BP_FLUSH(pf, g_prof, 1, true);
             }
             __syncwarp();
         }
@@ -972,7 +1021,7 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
             }
             BP_ADD(pf, kPEpilogue, te);
         }
-        pf.flush(2, lane == 0);
+        BP_FLUSH(pf, g_prof, 2, lane == 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -985,19 +1034,24 @@ diffattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q1,
 }  // namespace bwdtc
 
 #ifdef DIFFATTN_WAIT_PROFILE
-// The dK/dV kernel's wait-profile counters accumulated since the last call
-// ([3 roles][18 kinds], see dkdv::Prof), copied to `out` and cleared.  Only in
-// the build with -DDIFFATTN_WAIT_PROFILE.
+// The backward kernels' wait-profile counters accumulated since the last call,
+// copied to `out` and cleared: the dK/dV kernel's [3 roles][18 kinds], then,
+// when `n` has room, the dQ kernel's [3][17].  Only in the build with
+// -DDIFFATTN_WAIT_PROFILE.
 extern "C" int diffattn_bwd_wait_profile(unsigned long long* out, int n) {
     constexpr int kN = 3 * bwdtc::dkdv::kPKinds;
+    constexpr int kQ = 3 * bwdtc::dq::kQKinds;
     if (!out || n < kN) return -1;
+    static unsigned long long zero[kN > kQ ? kN : kQ] = {};
     if (cudaDeviceSynchronize() != cudaSuccess ||
-        cudaMemcpyFromSymbol(out, bwdtc::dkdv::g_prof, kN * sizeof(unsigned long long)) != cudaSuccess)
+        cudaMemcpyFromSymbol(out, bwdtc::dkdv::g_prof, kN * sizeof(unsigned long long)) != cudaSuccess ||
+        cudaMemcpyToSymbol(bwdtc::dkdv::g_prof, zero, kN * sizeof(unsigned long long)) != cudaSuccess)
         return -3;
-    static unsigned long long zero[kN] = {};
-    return cudaMemcpyToSymbol(bwdtc::dkdv::g_prof, zero, kN * sizeof(unsigned long long)) == cudaSuccess
-               ? 0
-               : -3;
+    if (n >= kN + kQ &&
+        (cudaMemcpyFromSymbol(out + kN, bwdtc::dq::g_prof, kQ * sizeof(unsigned long long)) != cudaSuccess ||
+         cudaMemcpyToSymbol(bwdtc::dq::g_prof, zero, kQ * sizeof(unsigned long long)) != cudaSuccess))
+        return -3;
+    return 0;
 }
 #endif
 

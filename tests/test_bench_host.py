@@ -160,3 +160,18 @@ def test_bwd_wait_profile_summary():
     pt = r["elementwise_warps"]["per_tile_cycles"]
     assert pt["math"] == pytest.approx(1000) and pt["all"] == pytest.approx(2000)
     assert r["elementwise_warps"]["per_item_epilogue_cycles"] == pytest.approx(200)
+
+
+def test_dq_wait_profile_summary():
+    n = len(bench.DQ_WAIT_KINDS)
+    raw = [0] * (3 * n)
+    raw[n + 0], raw[n + 7] = 1000, 250                 # MMA: waiting for dS a quarter of its time
+    ew = 2 * n
+    raw[ew + 0] = 6400
+    raw[ew + 9:ew + 13] = [400, 800, 2400, 800]        # scores, TMEM read, math, dS store
+    raw[ew + 14], raw[ew + 15], raw[ew + 16] = 300, 4, 1
+    s = bench.dq_wait_profile_summary(raw)
+    assert s["roles"]["mma_issuer"]["ds_ready"] == pytest.approx(0.25)
+    pt = s["roles"]["elementwise_warps"]["per_tile_cycles"]
+    assert pt["math"] == pytest.approx(600) and pt["all"] == pytest.approx(1600)
+    assert s["roles"]["elementwise_warps"]["per_item_epilogue_cycles"] == pytest.approx(300)
