@@ -21,7 +21,8 @@
 //     O1 / l1 - lambda O2 / l2 and applies the optional output epilogue.
 // For bf16, D = 64 and dense cache rows, pass 1 has two faster forms: the
 // staged kernel below (cp.async ring) for one or two query rows per CTA, and
-// for four or eight rows the tensor-core pass in decode_tc.cu.
+// for four to sixteen rows the tensor-core pass in decode_tc.cu (units of 16
+// rows, and the DIFF V2 head D = 128, run on that pass only).
 // Query rows: the kv_group query heads that share a key/value head (grouped
 // key/value heads, the DIFF V2 layout) contribute kv_group * Tq rows, row
 // (i, q) = i * Tq + q for the group's i-th head; they are cut into row_chunks

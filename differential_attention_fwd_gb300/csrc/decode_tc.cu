@@ -4,10 +4,10 @@
 // MMA's N: the query heads of a grouped key/value head, DIFF V2's layout, or
 // several new queries).  Two head shapes: D = 64 (V = 2D) with 4, 8 or 16 rows
 // per unit, and the DIFF V2 head D = 128 (V = D; aiengineeringfromscratch
-// lesson, "V1 contre V2") with 1 to 16, whose two branches usually share one key
-// tensor (then one key tile per stage serves both score products).  It writes split partials
-// in the layout of the CUDA-core first pass in decode.cu for a value width of
-// 128, which the combine pass there merges.
+// lesson, "V1 contre V2") with 1 to 16, whose two branches share one key tensor
+// (one key tile per stage serves both score products).  It writes split
+// partials in the layout of the CUDA-core first pass in decode.cu for a value
+// width of 128, which the combine pass there merges.
 //
 // Work: a unit is (b, key/value head, row chunk); its keys form tpu tiles of
 // 128.  The units' tiles are laid end to end and every CTA streams one
@@ -16,8 +16,9 @@
 // given by its CTA's place among the unit's CTAs, and the CTA with a unit's
 // last segment marks the unit's unused slots empty.
 //
-// Per segment, per tile of 128 keys: TMA brings K1, K2 and V into shared
-// memory in the 128-byte swizzled layout of the MMA operands, two tiles ahead
+// Per segment, per tile of 128 keys: TMA brings K1, K2 (or the one shared key
+// tile, in 64-column panels at D = 128) and V into shared memory in the
+// 128-byte swizzled layout of the MMA operands, two tiles ahead
 // (keys past the segment's end are loaded but get zero weight; past the
 // cache's end they read as zero).  Then
 //   S_b^T = K_b Q_b^T        (tcgen05, M = 128 keys in TMEM lanes, N = 16 rows,
