@@ -202,3 +202,34 @@ def test_decode_sixteen_row_units_epilogue(norm):
                      norm_bias=torch.from_numpy(bs).cuda(), out_scale=0.5)
         assert_close(to_numpy(out), ref, "bf16", f"decode 16-row units {norm} call {call}")
     assert da.get_device_error() == 0
+
+
+def misaligned(x):
+    """A bf16 copy of x seen one element into a wider buffer: element-aligned,
+    not 16-byte aligned."""
+    D = x.shape[-1]
+    wide = torch.zeros(*x.shape[:-1], D + 8, dtype=torch.bfloat16, device="cuda")
+    wide[..., 1:1 + D] = to_device(x, "bf16")
+    return wide[..., 1:1 + D]
+
+
+@pytest.mark.parametrize("H,Hk,Tq,Tk,D", [(4, 1, 4, 1500, 64), (2, 2, 12, 900, 64), (4, 2, 4, 700, 128)])
+def test_decode_sixteen_row_shapes_with_misaligned_queries(H, Hk, Tq, Tk, D):
+    """Queries whose rows are not 16-byte aligned: the tensor-core pass cannot
+    take them; the split-key layout of 8-row units on the CUDA cores (D = 64,
+    Tq <= 8) or the forward kernels run the call.  Against the oracle."""
+    shared = D == 128
+    w = W.DecodeWorkload("mis", 2, H, Tq, Tk, D, "bf16", True, seed=H + Tq + Tk + D, kv_heads=Hk,
+                         value_dim=128, shared_keys=shared)
+    inp = W.draw_kv(w)
+    if shared:
+        inp.k2 = inp.k1
+    q1, q2 = misaligned(inp.q1), misaligned(inp.q2)
+    assert q1.data_ptr() % 16 != 0
+    k1, v = to_device(inp.k1, "bf16"), to_device(inp.v, "bf16")
+    k2 = k1 if shared else to_device(inp.k2, "bf16")
+    out = da.differential_attention_decode(q1, k1, q2, k2, v, 0.6, causal=True)
+    torch.cuda.synchronize()
+    assert da.get_device_error() == 0
+    ref = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.6, True)
+    assert_close(to_numpy(out), ref, "bf16", f"misaligned Q H={H} Hk={Hk} Tq={Tq} D={D}")
