@@ -139,14 +139,23 @@ constexpr int BAR_DS_FULL = BAR_S_FULL + 2;           // [buffer], 8 warps
 constexpr int BAR_DQ_FULL = BAR_DS_FULL + 2;
 constexpr int BAR_DQ_EMPTY = BAR_DQ_FULL + 1;         // 8 warps
 constexpr int BAR_FINAL = BAR_DQ_EMPTY + 1;
-constexpr int NUM_BARS = BAR_FINAL + 1;
+constexpr int BAR_DP_FREE = BAR_FINAL + 1;            // 8 warps: a tile's dP read out of TMEM
+constexpr int BAR_DO_READY = BAR_DP_FREE + 1;         // 4 warps: the item's dO copied into TMEM
+constexpr int BAR_DO_FREE = BAR_DO_READY + 1;         // MMA: the item's last dP product done
+constexpr int NUM_BARS = BAR_DO_FREE + 1;
 constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
 constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// TMEM: buffer b at b*192: S1 +0, S2 +64, dP +128; dQ1 at 384, dQ2 at 448.
+// TMEM: buffer b at b*128: S1 +0, S2 +64 (dS_1, dS_2 written over them);
+// dP at 256 (one buffer: the elementwise warps read it at the start of their
+// tile, so the next tile's dP may follow at once); the item's dO at 320 as the
+// A operand of dP = dO V^T (64 columns: bf16 pairs, dO being fixed for the
+// item, so the products read only V from shared memory); dQ1 at 384, dQ2 at 448.
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_DP = 256;
+constexpr uint32_t TM_DO = 320;
 constexpr uint32_t TM_DQ = 384;
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);     // Q x K^T, dO x V^T
 constexpr uint32_t IDESC_DQ = idesc_bf16_f32(BM, HD, 0, 1);    // dS (TMEM) x K (MN-major)
@@ -155,8 +164,9 @@ constexpr uint32_t IDESC_DQ = idesc_bf16_f32(BM, HD, 0, 1);    // dS (TMEM) x K 
 // TMA producer, 1 the MMA-issuing thread, 2 the eight elementwise warps.
 // Kinds: 0 the role's cycles from start to end; the producer's waits for the
 // Q/dO slot (1), a K stage (2) and a V stage (3) to be released; the MMA
-// thread's waits for Q/dO (4), K (5), V (6), the dS operands (7) and the dQ
-// accumulators to be read out (8); the elementwise warps' waits for the scores
+// thread's waits for Q/dO and the item's dO in TMEM (4), K (5), V (6), the dS
+// operands and the previous tile's dP read out (7), and the dQ accumulators to
+// be read out (8); the elementwise warps' waits for the scores
 // (9), their TMEM read of S_b and dP (10), arithmetic (11), the dS store into
 // TMEM with its fences (12), the wait for the dQ accumulators (13) and the
 // epilogue (14); tile (15) and item (16) counts.
@@ -225,6 +235,9 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
         mbar_init(&bars[BAR_DQ_FULL], 1);
         mbar_init(&bars[BAR_DQ_EMPTY], 8);
         mbar_init(&bars[BAR_FINAL], 1);
+        mbar_init(&bars[BAR_DP_FREE], 8);
+        mbar_init(&bars[BAR_DO_READY], 4);
+        mbar_init(&bars[BAR_DO_FREE], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -297,21 +310,23 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 pf.start();
                 const uint64_t q1d = sdesc_sw128(smem_u32(smem + OFF_Q1), 16, 1024);
                 const uint64_t q2d = sdesc_sw128(smem_u32(smem + OFF_Q2), 16, 1024);
-                const uint64_t dod = sdesc_sw128(smem_u32(smem + OFF_DO), 16, 1024);
                 const uint64_t kkd = sdesc_sw128(smem_u32(smem + OFF_K), 16, 1024);        // K-major
                 const uint64_t kmd = sdesc_sw128(smem_u32(smem + OFF_K), K_BYTES, 1024);   // MN-major
                 const uint64_t vd = sdesc_sw128(smem_u32(smem + OFF_V), 16, 1024);
                 uint32_t kc = 0;            // key tiles consumed so far (K ring position)
                 uint32_t vst = 0, vph = 0, qph = 0, dqph = 0, dsph = 0;
                 bool ok = true;
-                // S_1, S_2, dP of key tile t into buffer buf
-                auto issue_s = [&](uint32_t kt, int buf) -> bool {
+                // S_1, S_2 of key tile kt into buffer buf, then dP into its buffer
+                // once the elementwise warps have read tile kt - 1's and, for an
+                // item's first tile, the item's dO is in TMEM (item number ki);
+                // an item's last dP releases the dO columns
+                auto issue_s = [&](uint32_t kt, int buf, int ki, bool first_tile, bool last_tile) -> bool {
                     const uint32_t ks = kt % KSTAGES;
                     if (!BP_WAIT(pf, kQKFull, mbar_wait(&bars[BAR_K_FULL + ks], (kt / KSTAGES) & 1u, ab)))
                         return false;
                     if (!BP_WAIT(pf, kQVFull, mbar_wait(&bars[BAR_V_FULL + vst], vph, ab))) return false;
                     tc_fence_after();
-                    const uint32_t d = tmem_base + buf * 192;
+                    const uint32_t d = tmem_base + buf * 128;
                     const uint64_t k1 = kkd + ((ks * 2 * K_BYTES) >> 4);
                     const uint64_t k2 = k1 + (K_BYTES >> 4);
 #pragma unroll
@@ -319,15 +334,21 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         mma_ss(d, q1d + 2 * kk, k1 + 2 * kk, IDESC_S, kk > 0);
                         mma_ss(d + 64, q2d + 2 * kk, k2 + 2 * kk, IDESC_S, kk > 0);
                     }
+                    if (kt > 0 && !BP_WAIT(pf, kQDsFull, mbar_wait(&bars[BAR_DP_FREE], (kt - 1) & 1u, ab)))
+                        return false;
+                    if (first_tile &&
+                        !BP_WAIT(pf, kQQFull, mbar_wait(&bars[BAR_DO_READY], (uint32_t)ki & 1u, ab)))
+                        return false;
+                    tc_fence_after();
                     const uint64_t v0 = vd + ((vst * V_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < VD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * (DO_HALF >> 4) + 2 * (kk & 3);
                         const uint32_t voff = (kk >> 2) * (V_HALF >> 4) + 2 * (kk & 3);
-                        mma_ss(d + 128, dod + off, v0 + voff, IDESC_S, kk > 0);
+                        mma_ts(tmem_base + TM_DP, tmem_base + TM_DO + kk * 8, v0 + voff, IDESC_S, kk > 0);
                     }
                     mma_commit(&bars[BAR_S_FULL + buf]);
                     mma_commit(&bars[BAR_V_EMPTY + vst]);
+                    if (last_tile) mma_commit(&bars[BAR_DO_FREE]);
                     if (++vst == VSTAGES) { vst = 0; vph ^= 1; }
                     return true;
                 };
@@ -339,7 +360,7 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                     const int n = it.n_kv;
                     if (!(ok = BP_WAIT(pf, kQQFull, mbar_wait(&bars[BAR_Q_FULL], qph, ab)))) break;
                     qph ^= 1;
-                    for (int t = 0; t < 2 && t < n && ok; ++t) ok = issue_s(kc + t, t);
+                    for (int t = 0; t < 2 && t < n && ok; ++t) ok = issue_s(kc + t, t, k, t == 0, t == n - 1);
                     if (!ok) break;
                     if (n <= 2) mma_commit(&bars[BAR_Q_EMPTY]);
                     for (int j = 0; j < n; ++j) {
@@ -355,7 +376,7 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         const uint32_t ks = (kc + j) % KSTAGES;
                         const uint64_t k1 = kmd + ((ks * 2 * K_BYTES) >> 4);
                         const uint64_t k2 = k1 + (K_BYTES >> 4);
-                        const uint32_t a = tmem_base + buf * 192;
+                        const uint32_t a = tmem_base + buf * 128;
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk) {
                             mma_ts(tmem_base + TM_DQ, a + kk * 8, k1 + 128 * kk, IDESC_DQ,
@@ -365,7 +386,7 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         }
                         mma_commit(&bars[BAR_K_EMPTY + ks]);
                         if (j + 2 < n) {
-                            if (!(ok = issue_s(kc + j + 2, buf))) break;
+                            if (!(ok = issue_s(kc + j + 2, buf, k, false, j + 3 == n))) break;
                             if (j + 3 == n) mma_commit(&bars[BAR_Q_EMPTY]);
                         }
                     }
@@ -407,14 +428,40 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 nlse = br ? st.y : st.x;
                 ndd = br ? st.w : st.z;
             }
+            if (br == 0) {
+                // the item's dO rows into TMEM (the dP products' A operand), once
+                // its TMA load has landed and the previous item's last dP is done
+                if (!(ok = mbar_wait_warp(&bars[BAR_Q_FULL], (uint32_t)k & 1u, ab))) break;
+                if (k > 0 && !(ok = mbar_wait_warp(&bars[BAR_DO_FREE], (uint32_t)(k - 1) & 1u, ab))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // 64 columns: row `row` of the 128-byte swizzled half, chunk c at c ^ (row % 8)
+                    const uint8_t* src = smem + OFF_DO + h * DO_HALF + row * 128;
+                    uint32_t w[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(src + ((c ^ (row & 7)) * 16));
+                        w[4 * c] = x.x;
+                        w[4 * c + 1] = x.y;
+                        w[4 * c + 2] = x.z;
+                        w[4 * c + 3] = x.w;
+                    }
+                    tmem_st32(lane_base + TM_DO + 32 * h, w);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[BAR_DO_READY]);
+            }
             const uint64_t sl2x2 = f2_pack(sl2, sl2);
             const uint64_t nlse2 = f2_pack(nlse, nlse);
             const uint64_t coef2 = f2_pack(coef, coef);
             const uint64_t cndd2 = f2_pack(coef * ndd, coef * ndd);
             for (int j = 0; j < it.n_kv; ++j) {
                 const int buf = j & 1;
-                const uint32_t tS = lane_base + buf * 192 + br * 64;
-                const uint32_t tP = lane_base + buf * 192 + 128;
+                const uint32_t tS = lane_base + buf * 128 + br * 64;
+                const uint32_t tP = lane_base + TM_DP;
                 if (!(ok = BP_WAIT(pf, kQSFull, mbar_wait_warp(&bars[BAR_S_FULL + buf], (sph >> buf) & 1u, ab))))
                     break;
                 BP_MARK(tp);
@@ -426,6 +473,10 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1,
                 tmem_ld32(tP, &dp[0]);
                 tmem_ld32(tP + 32, &dp[32]);
                 tmem_wait_ld();
+                // dP is in registers: the next tile's dP may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[BAR_DP_FREE]);
                 BP_ADD(pf, kQRead, tp);
                 BP_RESET(tp);
                 const int kv0 = j * BN;
