@@ -19,12 +19,14 @@
 // scores in tensor memory (TMEM):
 //
 // dq kernel: work item (b, h, 128-query tile); TMEM lanes are query rows.
-//   Per 64-key tile j: S_1, S_2 and dP (three M128 N64 MMAs from shared
-//   memory) into one of two TMEM buffers; warpgroup b forms dS_b from S_b and
-//   dP and writes it back over S_b as bf16; then dQ_b += dS_b K_b (A from
-//   TMEM, K_b read MN-major from the same shared-memory tile the score product
-//   read K-major).  Buffers alternate so that tile j+1's products overlap
-//   tile j's elementwise work.
+//   The item's dO is copied into TMEM once (warpgroup 0), as the A operand of
+//   dP = dO V^T.  Per 64-key tile j: S_1 and S_2 (M128 N64 MMAs from shared
+//   memory) into one of two TMEM buffers, dP into its single buffer (the
+//   elementwise warps read it at the start of their tile and release it);
+//   warpgroup b forms dS_b from S_b and dP and writes it back over S_b as
+//   bf16; then dQ_b += dS_b K_b (A from TMEM, K_b read MN-major from the same
+//   shared-memory tile the score product read K-major).  The score buffers
+//   alternate so that tile j+1's products overlap tile j's elementwise work.
 //
 // dkdv kernel: work item (b, key/value head, 128-key tile); TMEM lanes are key
 //   rows.  For every query head of the group and every 64-query tile:
