@@ -233,3 +233,17 @@ def test_decode_sixteen_row_shapes_with_misaligned_queries(H, Hk, Tq, Tk, D):
     assert da.get_device_error() == 0
     ref = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.6, True)
     assert_close(to_numpy(out), ref, "bf16", f"misaligned Q H={H} Hk={Hk} Tq={Tq} D={D}")
+
+
+@pytest.mark.parametrize("B,H,Hk,Tq,Tk,causal", [(1, 1, 1, 16, 16, True), (2, 16, 1, 1, 1, True),
+                                                 (1, 8, 1, 2, 2, True), (2, 4, 2, 8, 8, False)])
+def test_decode_sixteen_row_units_edges(B, H, Hk, Tq, Tk, causal):
+    # units of 16 rows at their edges: a cache holding exactly the new queries
+    # (the first query sees one key), one cached key for 16 query heads
+    w = W.DecodeWorkload("e16", B, H, Tq, Tk, 64, "bf16", causal, seed=B + H * 5 + Tq * 7 + Tk, kv_heads=Hk)
+    inp = W.draw_kv(w)
+    out, _ = run(inp, "bf16", 0.6, causal)
+    torch.cuda.synchronize()
+    assert da.get_device_error() == 0
+    ref = oracle.differential_attention_kv(inp.q1, inp.k1, inp.q2, inp.k2, inp.v, 0.6, causal)
+    assert_close(to_numpy(out), ref, "bf16", f"16-row edges B={B} H={H} Hk={Hk} Tq={Tq} Tk={Tk}")
